@@ -1,0 +1,342 @@
+/*
+ * Plain fp64 CPU oracle for the selective state-space scan.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU-baseline
+ * leg of the benchmark may load or call this library; the product path never does.
+ * It shares no code, header or constant with the CUDA implementation.
+ *
+ * Everything is computed in double precision, one channel at a time, in the order
+ * the pages write the method.  Channels are independent, so they are spread over
+ * POSIX threads; that changes no arithmetic.
+ *
+ * Sources (page title, section):
+ *  [S1] "Mamba и State Space Models", sections "Mamba: Selective State Space Model"
+ *       and "Selective Scan (core algorithm)": the selective recurrence
+ *       h_t = exp(Δ_t A) h_{t-1} + Δ_t B_t x_t, y_t = C_t h_t, with Δ = softplus(dt_proj(.)),
+ *       and the block's output gate y * SiLU(res) (section "Реализация MambaBlock").
+ *  [S2] "Модуль 8. Альтернативы Transformer: SSM, Mamba и гибриды":
+ *       §4 (discrete SSM, exact ZOH input term A^{-1}(e^{ΔA}-I)B and its a→0 limit Δ),
+ *       §6 (Δ_t = softplus(.), softplus(u) = log(1+e^u); the depthwise causal conv and
+ *       its cache), §7 (affine pairs (a,b), composition (a2,b2)∘(a1,b1) = (a2 a1, a2 b1 + b2)),
+ *       §14 (conv_state and ssm_state caches of a Mamba-1 layer).
+ *  [S3] "State Space Models: Mamba и альтернатива Transformer", section
+ *       "Mamba: Selective State Space" (D skip y = C·h + D·x, SiLU after the conv,
+ *       y * SiLU(res)) and "SSM Scan Algorithm" (recurrent form, closed-form prefix).
+ *
+ * Readings where the pages are silent or disagree (each also listed in the design notes):
+ *  - input term is Δ·B·x (the Mamba parameterisation, [S1], [S2] §4/§14); the exact ZOH
+ *    term is a separate option (discretization = 1);
+ *  - Δ = softplus(Δ_raw + bias) with a per-channel bias added before softplus;
+ *  - the D skip is included and the gate multiplies (C·h + D·x);
+ *  - the conv has no bias, kernel width K, and conv_state holds the last K-1 raw inputs,
+ *    oldest first; a SiLU follows the conv ([S3]).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <pthread.h>
+#include <unistd.h>
+
+#define ORACLE_API __attribute__((visibility("default")))
+
+/* softplus(v) = log(1 + e^v) ([S2] §6), written in the overflow-free form. */
+static double softplus(double v) {
+  return v > 0.0 ? v + log1p(exp(-v)) : log1p(exp(v));
+}
+
+/* SiLU(z) = z * sigmoid(z) = z / (1 + e^{-z}). */
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+
+/* The affine step h -> a h + b, composed "later after earlier" ([S2] §7). */
+ORACLE_API void oracle_compose_affine(double a2, double b2, double a1, double b1,
+                                      double* a_out, double* b_out) {
+  *a_out = a2 * a1;
+  *b_out = a2 * b1 + b2;
+}
+
+/* Discrete coefficients for one state coordinate and one step:
+ *   abar = exp(Δ a)
+ *   bbar = Δ b                         (discretization 0, the Mamba input term)
+ *   bbar = (exp(Δ a) - 1) / a * b      (discretization 1, exact ZOH, [S2] §4),
+ *          with the a -> 0 limit Δ b. */
+static void discretize(double delta, double a, double b, int discretization,
+                       double* abar, double* bbar) {
+  *abar = exp(delta * a);
+  if (discretization == 1 && a != 0.0)
+    *bbar = expm1(delta * a) / a * b;
+  else
+    *bbar = delta * b;
+}
+
+/* ------------------------------------------------------------------------------------
+ * Channel-list problem description.  A "channel" is one (batch b, inner channel d) pair.
+ * Per-channel arrays are indexed by the channel's position c in the list; B and C stay
+ * in their (batch, dstate, L) layout and are read through bidx[c].
+ * ---------------------------------------------------------------------------------- */
+typedef struct {
+  const double* u;          /* (n, L) */
+  const double* delta;      /* (n, L)  Δ_raw */
+  const double* A;          /* (n, N) */
+  const double* B;          /* (batch, N, L) */
+  const double* C;          /* (batch, N, L) */
+  const double* D;          /* (n) or NULL */
+  const double* z;          /* (n, L) or NULL: no gate */
+  const double* bias;       /* (n) or NULL */
+  const double* h0;         /* (n, N) or NULL: zero initial state */
+  const int64_t* bidx;      /* (n) batch index of each channel */
+  double* y;                /* (n, L) */
+  double* hL;               /* (n, N) or NULL */
+  int64_t n, L;
+  int N;
+  int softplus_flag;
+  int discretization;
+  int64_t chunk;            /* chunked variant: chunk length (>0) */
+} scan_problem;
+
+static double delta_at(const scan_problem* p, int64_t c, int64_t t) {
+  double v = p->delta[c * p->L + t] + (p->bias ? p->bias[c] : 0.0);
+  return p->softplus_flag ? softplus(v) : v;
+}
+
+/* Readout for step t: y = C_t·h + D x_t, then the gate y * SiLU(z_t). */
+static double readout(const scan_problem* p, int64_t c, int64_t t, const double* h) {
+  const int N = p->N;
+  const double* Cb = p->C + p->bidx[c] * (int64_t)N * p->L;
+  double y = 0.0;
+  for (int n = 0; n < N; ++n) y += Cb[(int64_t)n * p->L + t] * h[n];
+  double x = p->u[c * p->L + t];
+  if (p->D) y += p->D[c] * x;
+  if (p->z) y *= silu(p->z[c * p->L + t]);
+  return y;
+}
+
+/* One recurrence step h <- abar ⊙ h + bbar x for step t ([S1] "Selective Scan"). */
+static void step(const scan_problem* p, int64_t c, int64_t t, double* h) {
+  const int N = p->N;
+  const double* Bb = p->B + p->bidx[c] * (int64_t)N * p->L;
+  double dlt = delta_at(p, c, t);
+  double x = p->u[c * p->L + t];
+  for (int n = 0; n < N; ++n) {
+    double abar, bbar;
+    discretize(dlt, p->A[c * N + n], Bb[(int64_t)n * p->L + t], p->discretization, &abar, &bbar);
+    h[n] = abar * h[n] + bbar * x;
+  }
+}
+
+/* Sequential scan of one channel: the plain recurrence, update then read ([S1], [S3]). */
+static void scan_channel(const scan_problem* p, int64_t c) {
+  double h[64];
+  const int N = p->N;
+  for (int n = 0; n < N; ++n) h[n] = p->h0 ? p->h0[c * N + n] : 0.0;
+  for (int64_t t = 0; t < p->L; ++t) {
+    step(p, c, t, h);
+    p->y[c * p->L + t] = readout(p, c, t, h);
+  }
+  if (p->hL)
+    for (int n = 0; n < N; ++n) p->hL[c * N + n] = h[n];
+}
+
+/* Chunked scan of one channel, the two-level form of [S2] §7:
+ *  1. for every chunk, its aggregate affine pair per state coordinate: (Π abar, h_end from 0);
+ *  2. the carry into chunk k is the composition of the aggregates of chunks < k applied
+ *     to the initial state;
+ *  3. every chunk is re-run from its carried-in state to produce y. */
+static void chunked_scan_channel(const scan_problem* p, int64_t c) {
+  const int N = p->N;
+  const int64_t T = p->chunk, L = p->L;
+  const int64_t nchunks = (L + T - 1) / T;
+  double carry[64], agg_a[64], agg_b[64], h[64];
+  for (int n = 0; n < N; ++n) carry[n] = p->h0 ? p->h0[c * N + n] : 0.0;
+  const double* Bb = p->B + p->bidx[c] * (int64_t)N * L;
+  for (int64_t k = 0; k < nchunks; ++k) {
+    int64_t t0 = k * T, t1 = t0 + T < L ? t0 + T : L;
+    /* 1. aggregate of chunk k, built step by step with the composition operator */
+    for (int n = 0; n < N; ++n) { agg_a[n] = 1.0; agg_b[n] = 0.0; }
+    for (int64_t t = t0; t < t1; ++t) {
+      double dlt = delta_at(p, c, t);
+      double x = p->u[c * L + t];
+      for (int n = 0; n < N; ++n) {
+        double abar, bbar;
+        discretize(dlt, p->A[c * N + n], Bb[(int64_t)n * L + t], p->discretization, &abar, &bbar);
+        oracle_compose_affine(abar, bbar * x, agg_a[n], agg_b[n], &agg_a[n], &agg_b[n]);
+      }
+    }
+    /* 3. re-run chunk k from the carried-in state */
+    for (int n = 0; n < N; ++n) h[n] = carry[n];
+    for (int64_t t = t0; t < t1; ++t) {
+      step(p, c, t, h);
+      p->y[c * L + t] = readout(p, c, t, h);
+    }
+    /* 2. carry into chunk k+1 = aggregate_k applied to carry_k */
+    for (int n = 0; n < N; ++n) {
+      double a_unused;
+      oracle_compose_affine(agg_a[n], agg_b[n], 1.0, carry[n], &a_unused, &carry[n]);
+    }
+  }
+  if (p->hL)
+    for (int n = 0; n < N; ++n) p->hL[c * N + n] = carry[n];
+}
+
+/* ------------------------------------------------------------------------------------
+ * A minimal thread pool over channels.
+ * ---------------------------------------------------------------------------------- */
+typedef struct {
+  void (*fn)(const void*, int64_t);
+  const void* problem;
+  int64_t n;
+  int64_t next;
+  pthread_mutex_t mu;
+} pool;
+
+static void* pool_worker(void* arg) {
+  pool* q = (pool*)arg;
+  for (;;) {
+    pthread_mutex_lock(&q->mu);
+    int64_t c = q->next++;
+    pthread_mutex_unlock(&q->mu);
+    if (c >= q->n) break;
+    q->fn(q->problem, c);
+  }
+  return NULL;
+}
+
+static void run_channels(void (*fn)(const void*, int64_t), const void* problem, int64_t n,
+                         int threads) {
+  if (threads <= 0) threads = (int)sysconf(_SC_NPROCESSORS_ONLN);
+  if (threads < 1) threads = 1;
+  if (threads > 256) threads = 256;
+  if ((int64_t)threads > n) threads = (int)(n > 0 ? n : 1);
+  pool q;
+  q.fn = fn; q.problem = problem; q.n = n; q.next = 0;
+  pthread_mutex_init(&q.mu, NULL);
+  if (threads == 1) {
+    pool_worker(&q);
+  } else {
+    pthread_t tid[256];
+    for (int i = 0; i < threads; ++i) pthread_create(&tid[i], NULL, pool_worker, &q);
+    for (int i = 0; i < threads; ++i) pthread_join(tid[i], NULL);
+  }
+  pthread_mutex_destroy(&q.mu);
+}
+
+static void scan_fn(const void* p, int64_t c) { scan_channel((const scan_problem*)p, c); }
+static void chunked_fn(const void* p, int64_t c) { chunked_scan_channel((const scan_problem*)p, c); }
+
+/* Returns 0 on success, -1 on a bad argument. */
+static int fill_problem(scan_problem* p, const double* u, const double* delta, const double* A,
+                        const double* B, const double* C, const double* D, const double* z,
+                        const double* bias, int softplus_flag, int discretization,
+                        const double* h0, const int64_t* bidx, double* y, double* hL,
+                        int64_t n, int N, int64_t L) {
+  if (!u || !delta || !A || !B || !C || !bidx || !y) return -1;
+  if (n < 0 || L < 0 || N < 1 || N > 64) return -1;
+  if (discretization != 0 && discretization != 1) return -1;
+  p->u = u; p->delta = delta; p->A = A; p->B = B; p->C = C; p->D = D; p->z = z;
+  p->bias = bias; p->h0 = h0; p->bidx = bidx; p->y = y; p->hL = hL;
+  p->n = n; p->L = L; p->N = N; p->softplus_flag = softplus_flag;
+  p->discretization = discretization; p->chunk = 0;
+  return 0;
+}
+
+ORACLE_API int oracle_selective_scan(const double* u, const double* delta, const double* A,
+                                     const double* B, const double* C, const double* D,
+                                     const double* z, const double* bias, int softplus_flag,
+                                     int discretization, const double* h0, const int64_t* bidx,
+                                     double* y, double* hL, int64_t n, int N, int64_t L,
+                                     int threads) {
+  scan_problem p;
+  if (fill_problem(&p, u, delta, A, B, C, D, z, bias, softplus_flag, discretization, h0, bidx,
+                   y, hL, n, N, L))
+    return -1;
+  run_channels(scan_fn, &p, n, threads);
+  return 0;
+}
+
+ORACLE_API int oracle_chunked_scan(const double* u, const double* delta, const double* A,
+                                   const double* B, const double* C, const double* D,
+                                   const double* z, const double* bias, int softplus_flag,
+                                   int discretization, const double* h0, const int64_t* bidx,
+                                   double* y, double* hL, int64_t n, int N, int64_t L,
+                                   int64_t chunk, int threads) {
+  scan_problem p;
+  if (fill_problem(&p, u, delta, A, B, C, D, z, bias, softplus_flag, discretization, h0, bidx,
+                   y, hL, n, N, L))
+    return -1;
+  if (chunk < 1) return -1;
+  p.chunk = chunk;
+  run_channels(chunked_fn, &p, n, threads);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------------------
+ * Causal depthwise conv1d of width K followed (optionally) by SiLU, per channel:
+ *   out[t] = SiLU( Σ_{k=0}^{K-1} w[k] · xpad[t + k] ),  xpad = [state (K-1 values), x_0 .. x_{L-1}]
+ * i.e. a cross-correlation with K-1 leading pad values, keeping the first L outputs
+ * ("Mamba и State Space Models", "Реализация MambaBlock"; "State Space Models: Mamba и
+ * альтернатива Transformer", "Mamba: Selective State Space").  With a NULL state the pad
+ * is zero.  state_out receives the last K-1 entries of xpad, oldest first.
+ * ---------------------------------------------------------------------------------- */
+ORACLE_API int oracle_causal_conv1d(const double* x, const double* w, const double* state_in,
+                                    double* out, double* state_out, int64_t n, int64_t L,
+                                    int K, int apply_silu) {
+  if (!x || !w || !out || n < 0 || L < 0 || K < 1 || K > 64) return -1;
+  double* xpad = (double*)malloc(sizeof(double) * (size_t)(L + K - 1));
+  if (!xpad) return -1;
+  for (int64_t c = 0; c < n; ++c) {
+    for (int k = 0; k < K - 1; ++k) xpad[k] = state_in ? state_in[c * (K - 1) + k] : 0.0;
+    for (int64_t t = 0; t < L; ++t) xpad[K - 1 + t] = x[c * L + t];
+    for (int64_t t = 0; t < L; ++t) {
+      double s = 0.0;
+      for (int k = 0; k < K; ++k) s += w[c * K + k] * xpad[t + k];
+      out[c * L + t] = apply_silu ? silu(s) : s;
+    }
+    if (state_out)
+      for (int k = 0; k < K - 1; ++k) state_out[c * (K - 1) + k] = xpad[L + k];
+  }
+  free(xpad);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------------------
+ * One decode step of a Mamba-1 layer with its two caches ([S2] §6 and §14):
+ *   window  = [conv_state[0..K-2], x_t]
+ *   u       = SiLU(Σ_k w[k] window[k]);  conv_state <- window[1..K-1]
+ *   Δ       = softplus(Δ_raw + bias)
+ *   h       <- exp(Δ A) ⊙ h + Δ B_t u
+ *   y_t     = (C_t·h + D u) · SiLU(z_t)
+ * Per-channel arrays are indexed by channel c; B_t and C_t are (batch, N) via bidx.
+ * ---------------------------------------------------------------------------------- */
+ORACLE_API int oracle_state_update(const double* x_t, const double* delta_t, const double* A,
+                                   const double* B_t, const double* C_t, const double* D,
+                                   const double* z_t, const double* bias, int softplus_flag,
+                                   double* state, double* conv_state, const double* conv_w,
+                                   double* y_t, const int64_t* bidx, int64_t n, int N, int K) {
+  if (!x_t || !delta_t || !A || !B_t || !C_t || !state || !conv_state || !conv_w || !y_t ||
+      !bidx || n < 0 || N < 1 || N > 64 || K < 1 || K > 64)
+    return -1;
+  for (int64_t c = 0; c < n; ++c) {
+    double window[64];
+    for (int k = 0; k < K - 1; ++k) window[k] = conv_state[c * (K - 1) + k];
+    window[K - 1] = x_t[c];
+    double s = 0.0;
+    for (int k = 0; k < K; ++k) s += conv_w[c * K + k] * window[k];
+    double u = silu(s);
+    for (int k = 0; k < K - 1; ++k) conv_state[c * (K - 1) + k] = window[k + 1];
+
+    double v = delta_t[c] + (bias ? bias[c] : 0.0);
+    double dlt = softplus_flag ? softplus(v) : v;
+    const double* Bb = B_t + bidx[c] * N;
+    const double* Cb = C_t + bidx[c] * N;
+    double y = 0.0;
+    for (int nn = 0; nn < N; ++nn) {
+      double* h = &state[c * N + nn];
+      *h = exp(dlt * A[c * N + nn]) * *h + dlt * Bb[nn] * u;
+      y += Cb[nn] * *h;
+    }
+    if (D) y += D[c] * u;
+    if (z_t) y *= silu(z_t[c]);
+    y_t[c] = y;
+  }
+  return 0;
+}

@@ -1,0 +1,170 @@
+"""Seeded synthetic inputs for the selective scan and the decode step.
+
+This module only draws random numbers and lays them out; it holds none of the method's
+arithmetic, so both the CUDA path and the CPU oracle can be fed from it.  Every workload is
+identified by name and sizes; the seed is fixed per workload.
+
+Shapes (all contiguous):
+    u, delta (Δ_raw), z : (batch, dim, L)      io dtype (float32 or bfloat16)
+    B, C                : (batch, dstate, L)   io dtype
+    A                   : (dim, dstate)        float32
+    D, delta_bias       : (dim,)               float32
+Decode step inputs are the same per token with L dropped; conv_w is (dim, 4) float32.
+
+Distributions follow the layer shapes named on the pages (Mamba-130M: d_inner 1536; Mamba-2.8B:
+d_inner 5120; d_state 16; d_conv 4):
+    u, Δ_raw, z, B, C, D ~ N(0, 1)
+    delta_bias = log(expm1(s)), s log-uniform in [1e-3, 1e-1]   (so that softplus(bias) = s)
+    A[d, n] = -(n + 1) * scale_d, scale_d = 1 or log-uniform in [0.5, 2]
+    long-sequence u[:, :, t] = E[sym_t], sym_t iid uniform over a 4-letter alphabet,
+        E (4, dim) ~ N(0, 1)  (a stand-in for DNA-like symbol streams)
+    conv_w ~ N(0, 1/4)
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Dict, Optional, Tuple
+
+import torch
+
+
+@dataclass(frozen=True)
+class ScanWorkload:
+    name: str
+    batch: int
+    dim: int
+    dstate: int
+    seqlen: int
+    io_dtype: str                      # "f32" or "bf16"
+    seed: int
+    a_scale: Optional[Tuple[float, float]] = None   # log-uniform per-channel scale of A, or None (=1)
+    symbol_alphabet: int = 0           # >0: u drawn from an alphabet mapped to fixed embeddings
+
+    @property
+    def tokens(self) -> int:
+        return self.batch * self.seqlen
+
+    @property
+    def torch_dtype(self):
+        return torch.float32 if self.io_dtype == "f32" else torch.bfloat16
+
+    def algorithmic_bytes(self) -> int:
+        """Reads of u, Δ, z, B, C and writes of y and the final state (fp32), plus A, D, bias."""
+        e = 4 if self.io_dtype == "f32" else 2
+        bdl = self.batch * self.dim * self.seqlen
+        bnl = self.batch * self.dstate * self.seqlen
+        return (4 * bdl + 2 * bnl) * e + self.batch * self.dim * self.dstate * 4 + \
+            self.dim * self.dstate * 4 + 2 * self.dim * 4
+
+
+@dataclass(frozen=True)
+class DecodeWorkload:
+    name: str
+    batch: int
+    dim: int
+    dstate: int
+    dconv: int
+    steps: int
+    io_dtype: str
+    seed: int
+    a_scale: Optional[Tuple[float, float]] = None
+
+    @property
+    def tokens_per_step(self) -> int:
+        return self.batch
+
+    def bytes_per_step(self) -> int:
+        """State read+write (fp32), conv_state read+write (fp32), per-token io, conv weights, params."""
+        e = 4 if self.io_dtype == "f32" else 2
+        bd = self.batch * self.dim
+        return (2 * bd * self.dstate * 4 + 2 * bd * (self.dconv - 1) * 4 + 4 * bd * e +
+                2 * self.batch * self.dstate * e + self.dim * self.dconv * 4 +
+                self.dim * self.dstate * 4 + 2 * self.dim * 4)
+
+
+WORKLOADS: Dict[str, object] = {
+    "tiny-f32": ScanWorkload("tiny-f32", 1, 64, 16, 256, "f32", 1000),
+    "mamba130m-layer": ScanWorkload("mamba130m-layer", 8, 1536, 16, 2048, "bf16", 1001),
+    "mamba2.8b-layer": ScanWorkload("mamba2.8b-layer", 4, 5120, 16, 4096, "bf16", 1002, a_scale=(0.5, 2.0)),
+    "long-dna": ScanWorkload("long-dna", 1, 1536, 16, 1 << 20, "bf16", 1003, symbol_alphabet=4),
+    "decode-2.8b": DecodeWorkload("decode-2.8b", 256, 5120, 16, 4, 1000, "bf16", 1004, a_scale=(0.5, 2.0)),
+}
+
+
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def _loguniform(n: int, lo: float, hi: float, g: torch.Generator, device) -> torch.Tensor:
+    r = torch.rand(n, generator=g, device=device, dtype=torch.float64)
+    return torch.exp(math.log(lo) + r * (math.log(hi) - math.log(lo)))
+
+
+def make_params(dim: int, dstate: int, seed: int, a_scale=None, device="cpu") -> Dict[str, torch.Tensor]:
+    """A (dim, dstate), D (dim), delta_bias (dim), all float32."""
+    g = _gen(seed * 7919 + 17, device)
+    n1 = torch.arange(1, dstate + 1, device=device, dtype=torch.float32)
+    if a_scale is None:
+        scale = torch.ones(dim, device=device, dtype=torch.float32)
+    else:
+        scale = _loguniform(dim, a_scale[0], a_scale[1], g, device).to(torch.float32)
+    A = -(scale[:, None] * n1[None, :])                      # float32 products
+    D = torch.randn(dim, generator=g, device=device, dtype=torch.float32)
+    s = _loguniform(dim, 1e-3, 1e-1, g, device)
+    delta_bias = torch.log(torch.expm1(s)).to(torch.float32)  # inverse of softplus: softplus(bias) = s
+    return {"A": A.contiguous(), "D": D, "delta_bias": delta_bias}
+
+
+def make_scan_inputs(w: ScanWorkload, device="cpu", seed: Optional[int] = None) -> Dict[str, torch.Tensor]:
+    """All inputs of one prefill call, generated on ``device``."""
+    seed = w.seed if seed is None else seed
+    g = _gen(seed, device)
+    dt = w.torch_dtype
+    shp = (w.batch, w.dim, w.seqlen)
+    out = make_params(w.dim, w.dstate, seed, w.a_scale, device)
+    if w.symbol_alphabet:
+        E = torch.randn(w.symbol_alphabet, w.dim, generator=g, device=device, dtype=torch.float32).to(dt)
+        sym = torch.randint(0, w.symbol_alphabet, (w.batch, w.seqlen), generator=g, device=device)
+        u = torch.empty(shp, device=device, dtype=dt)
+        for b in range(w.batch):
+            u[b] = E[sym[b]].transpose(0, 1)
+        out["symbols"] = sym
+        out["embedding"] = E
+    else:
+        u = torch.randn(shp, generator=g, device=device, dtype=torch.float32).to(dt)
+    out["u"] = u.contiguous()
+    out["delta"] = torch.randn(shp, generator=g, device=device, dtype=torch.float32).to(dt)
+    out["z"] = torch.randn(shp, generator=g, device=device, dtype=torch.float32).to(dt)
+    out["B"] = torch.randn((w.batch, w.dstate, w.seqlen), generator=g, device=device, dtype=torch.float32).to(dt)
+    out["C"] = torch.randn((w.batch, w.dstate, w.seqlen), generator=g, device=device, dtype=torch.float32).to(dt)
+    return out
+
+
+def make_decode_inputs(w: DecodeWorkload, steps: Optional[int] = None, device="cpu",
+                       seed: Optional[int] = None) -> Dict[str, torch.Tensor]:
+    """Per-token inputs for ``steps`` tokens, stacked along a leading time axis:
+    x, delta, z (steps, batch, dim); B, C (steps, batch, dstate); plus A, D, delta_bias, conv_w."""
+    seed = w.seed if seed is None else seed
+    steps = w.steps if steps is None else steps
+    g = _gen(seed, device)
+    dt = torch.float32 if w.io_dtype == "f32" else torch.bfloat16
+    out = make_params(w.dim, w.dstate, seed, w.a_scale, device)
+    out["conv_w"] = (0.5 * torch.randn((w.dim, w.dconv), generator=g, device=device, dtype=torch.float32)).contiguous()
+    shp = (steps, w.batch, w.dim)
+    out["x"] = torch.randn(shp, generator=g, device=device, dtype=torch.float32).to(dt)
+    out["delta"] = torch.randn(shp, generator=g, device=device, dtype=torch.float32).to(dt)
+    out["z"] = torch.randn(shp, generator=g, device=device, dtype=torch.float32).to(dt)
+    out["B"] = torch.randn((steps, w.batch, w.dstate), generator=g, device=device, dtype=torch.float32).to(dt)
+    out["C"] = torch.randn((steps, w.batch, w.dstate), generator=g, device=device, dtype=torch.float32).to(dt)
+    return out
+
+
+def random_scan_inputs(batch: int, dim: int, dstate: int, seqlen: int, io_dtype: str = "f32", seed: int = 0,
+                       a_scale=None, device="cpu") -> Dict[str, torch.Tensor]:
+    """Ad-hoc sizes with the same distributions (parity tests on ragged shapes)."""
+    w = ScanWorkload(f"adhoc-{batch}x{dim}x{dstate}x{seqlen}", batch, dim, dstate, seqlen, io_dtype, seed,
+                     a_scale=a_scale)
+    return make_scan_inputs(w, device=device)
