@@ -1,0 +1,421 @@
+#!/usr/bin/env python3
+"""Benchmark of the B300 selective scan.
+
+Default workload: the Mamba-2.8B layer scan (batch 4, d_inner 5120, d_state 16, L 4096, bf16 io,
+float32 state).  One step = one ssm_scan_fwd call over that batch (every prefill row of the hot
+path: load, softplus, discretise, recurrence, readout + D skip, gate, store, final state).
+The decode row (batch 256, d_inner 5120, 1000 tokens) is measured after it and reported in the
+same JSON line under "decode".
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Under torchrun every rank runs its own replica (its own batch of the workload, no collective on the
+data path); value = tokens of all ranks / the slowest rank's time ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "selective-scan tokens/s and achieved HBM GB/s (% of B300 peak), 2.8B layer"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6400.0
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.gpu)], stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+            os.unlink(self.path)
+        except Exception:
+            pass
+        return self.summary(rows)
+
+    @staticmethod
+    def summary(rows):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.strip().lower() == "active"})
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+def _src_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _ncu_traffic(kernel_key, workload):
+    """dram bytes per launch from the committed ncu summary, if it was taken on the current source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        e = j[kernel_key]
+        srcs = [os.path.join(ROOT, s) for s in e["sources"]]
+        if e.get("workload") != workload or e.get("source_hash") != _src_hash(srcs):
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+
+def cpu_oracle_sample(w, target_s: float = 12.0, min_channels: int = 2):
+    """Times the fp64 oracle on a bounded sample of channels of the workload; returns tokens/s of the
+    whole workload extrapolated from the sample, the cores used and a description."""
+    import torch
+    import oracle
+    from selective_state_space_139_b300 import workloads as W
+
+    cores = os.cpu_count() or 1
+    n_total = w.batch * w.dim
+    # calibrate with one channel
+    g = np.random.default_rng(0)
+
+    def make(nc):
+        inp = W.random_scan_inputs(1, nc, w.dstate, w.seqlen, w.io_dtype, seed=1, a_scale=w.a_scale)
+        f = lambda t: t.double().numpy()
+        return (f(inp["u"][0]), f(inp["delta"][0]), f(inp["A"]), f(inp["B"]), f(inp["C"]), np.zeros(nc, np.int64),
+                f(inp["D"]), f(inp["z"][0]), f(inp["delta_bias"]))
+
+    def run(args):
+        u, dl, A, B, C, bidx, D, z, bias = args
+        t0 = time.perf_counter()
+        oracle.selective_scan_channels(u, dl, A, B, C, bidx, D=D, z=z, delta_bias=bias, threads=cores)
+        return time.perf_counter() - t0
+
+    one = run(make(min(cores, n_total)))
+    per_round = max(one, 1e-4)
+    rounds = max(1, int(target_s / per_round))
+    nc = min(n_total, max(min_channels, rounds * min(cores, n_total)))
+    secs = run(make(nc))
+    tokens_per_s = (w.batch * w.seqlen) * (nc / n_total) / secs
+    sample = f"{nc} of {n_total} channels x {w.seqlen} steps (fp64 oracle, {secs:.1f} s)"
+    return tokens_per_s, cores, sample, secs
+
+
+# ----------------------------------------------------------------------------- GPU measurement
+
+def measure_scan(w, steps, warmup, dev, rank, peak, peak_kind):
+    import torch
+    from selective_state_space_139_b300 import ssm
+    from selective_state_space_139_b300 import workloads as W
+
+    inp = W.make_scan_inputs(w, device=dev, seed=w.seed + rank)
+    y = torch.empty_like(inp["u"])
+    hL = torch.empty((w.batch, w.dim, w.dstate), device=dev, dtype=torch.float32)
+    ws_bytes = ssm.scan_workspace_size(w.batch, w.dim, w.dstate, w.seqlen, inp["u"].dtype)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    launches_per_step = 3 if ws_bytes else 1
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ssm.selective_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], D=inp["D"], z=inp["z"],
+                               delta_bias=inp["delta_bias"], out=y, last_state=hL, workspace=ws)
+
+    sampler = ClockSampler(dev.index if dev.index is not None else 0).start()
+    # soak for ~1 s so that the clock record has samples under load, then the W warm-up steps
+    t_end = time.time() + 1.0
+    while time.time() < t_end:
+        step()
+        torch.cuda.synchronize(dev)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    _barrier()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    _barrier()
+    clocks = sampler.stop()
+    total_ms = t0.elapsed_time(t1)
+    per_launch_ms = [a.elapsed_time(b) for a, b in evs]
+    assert ssm.device_status() == ssm.SSM_OK
+
+    # end to end through the public API: pinned host inputs in, host outputs back, every step
+    host = {k: inp[k].cpu().pin_memory() for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias")}
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    h_host = torch.empty(hL.shape, dtype=hL.dtype, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = y.numel() * y.element_size() + hL.numel() * hL.element_size()
+
+    def e2e_step():
+        for k, v in host.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        ssm.selective_scan_fwd(dev_in["u"], dev_in["delta"], dev_in["A"], dev_in["B"], dev_in["C"], D=dev_in["D"],
+                               z=dev_in["z"], delta_bias=dev_in["delta_bias"], out=y, last_state=hL, workspace=ws)
+        y_host.copy_(y, non_blocking=True)
+        h_host.copy_(hL, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e_steps = max(3, min(steps, 20))
+    _barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = _max_over_ranks(a.elapsed_time(b) / e_steps)
+
+    ms_step = _max_over_ranks(total_ms / steps)
+    kern_ms = statistics.mean(per_launch_ms)
+    bytes_alg = w.algorithmic_bytes()
+    achieved = bytes_alg / (kern_ms * 1e-3) / 1e9
+    return {
+        "ms_per_step": ms_step, "tokens_per_step": w.tokens, "kernel_ms": kern_ms, "bytes_alg": bytes_alg,
+        "achieved_gbs": achieved, "clocks": clocks, "launches_per_step": launches_per_step,
+        "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h, "algorithm": "chunked" if ws_bytes else "single_pass",
+    }
+
+
+def measure_decode(w, steps_tokens, dev, rank):
+    import torch
+    from selective_state_space_139_b300 import ssm
+    from selective_state_space_139_b300 import workloads as W
+
+    inp = W.make_decode_inputs(w, steps=steps_tokens, device=dev, seed=w.seed + rank)
+    state = torch.zeros((w.batch, w.dim, w.dstate), device=dev)
+    conv_state = torch.zeros((w.batch, w.dim, w.dconv - 1), device=dev)
+    y = torch.empty((w.batch, w.dim), device=dev, dtype=inp["x"].dtype)
+    stream = torch.cuda.current_stream(dev)
+
+    def tok(t):
+        ssm.selective_state_update(inp["x"][t], inp["delta"][t], inp["A"], inp["B"][t], inp["C"][t], inp["D"],
+                                   inp["z"][t], state, conv_state, inp["conv_w"], delta_bias=inp["delta_bias"], out=y)
+
+    for t in range(min(20, steps_tokens)):
+        tok(t)
+    torch.cuda.synchronize(dev)
+    state.zero_()
+    conv_state.zero_()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps_tokens)]
+    for t in range(steps_tokens):
+        evs[t][0].record(stream)
+        tok(t)
+        evs[t][1].record(stream)
+    torch.cuda.synchronize(dev)
+    per = [a.elapsed_time(b) for a, b in evs]
+    k_ms = statistics.mean(per[5:]) if len(per) > 10 else statistics.mean(per)
+    return {"steps": steps_tokens, "ms_per_token_step": k_ms, "bytes_per_step": w.bytes_per_step(),
+            "achieved_gbs": w.bytes_per_step() / (k_ms * 1e-3) / 1e9,
+            "tokens_per_s": w.batch / (k_ms * 1e-3)}
+
+
+# ----------------------------------------------------------------------------- distributed helpers
+
+_PG = None
+
+
+def _init_dist():
+    global _PG
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        _PG = dist
+    return ws, rank, local
+
+
+def _barrier():
+    if _PG is not None:
+        _PG.barrier()
+
+
+def _max_over_ranks(x: float) -> float:
+    if _PG is None:
+        return x
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    _PG.all_reduce(t, op=_PG.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- main
+
+def run_reference(args, ws, rank):
+    from selective_state_space_139_b300 import workloads as W
+    if rank != 0:
+        return 0
+    w = W.WORKLOADS[args.workload]
+    values = []
+    sample = ""
+    cores = os.cpu_count() or 1
+    budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
+    for i in range(args.warmup + args.steps):
+        v, cores, sample, secs = cpu_oracle_sample(w, target_s=budget)
+        if i >= args.warmup:
+            values.append(v)
+    value = statistics.mean(values)
+    ms = w.tokens / value * 1e3
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "d_inner": w.dim, "d_state": w.dstate,
+                       "seq_len": w.seqlen, "io": w.io_dtype},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="mamba2.8b-layer")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--decode-steps", type=int, default=1000)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    ws, rank, local = _init_dist()
+    if args.impl == "reference":
+        return run_reference(args, ws, rank)
+
+    import torch
+    from selective_state_space_139_b300 import build, ssm
+    from selective_state_space_139_b300 import workloads as W
+
+    build.build()
+    ssm.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peak, peak_kind = _peaks()
+    w = W.WORKLOADS[args.workload]
+    if not isinstance(w, W.ScanWorkload):
+        raise SystemExit("--workload must name a prefill workload; decode is reported under 'decode'")
+    r = measure_scan(w, args.steps, args.warmup, dev, rank, peak, peak_kind)
+    dec = None
+    if not args.no_decode:
+        dw = W.WORKLOADS["decode-2.8b"]
+        dec = measure_decode(dw, args.decode_steps, dev, rank)
+        dec["ms_per_token_step"] = _max_over_ranks(dec["ms_per_token_step"])
+    if rank != 0:
+        return 0
+    tokens_all = w.tokens * ws
+    value = tokens_all / (r["ms_per_step"] * 1e-3)
+    traffic = _ncu_traffic("scan_fwd", w.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": r["ms_per_step"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 (bf16 io)", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "d_inner": w.dim, "d_state": w.dstate, "seq_len": w.seqlen,
+                   "io": w.io_dtype, "algorithm": r["algorithm"],
+                   "l2": "inputs larger than L2 (%.0f MB per step vs 126 MB)" % (r["bytes_alg"] / 1e6),
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": {"bound": "hbm", "achieved": r["achieved_gbs"], "peak": peak, "unit": "GB/s",
+                     "frac": r["achieved_gbs"] / peak, "traffic": traffic, "peak_source": peak_kind,
+                     "kernel_ms": r["kernel_ms"], "bytes_per_launch": r["bytes_alg"]},
+        "clocks": r["clocks"],
+        "e2e": {"value": tokens_all / (r["e2e_ms"] * 1e-3), "unit": UNIT, "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": args.steps * r["launches_per_step"],
+    }
+    if dec is not None:
+        line["decode"] = {"workload": "decode-2.8b", "tokens_per_s": 256 * ws / (dec["ms_per_token_step"] * 1e-3),
+                          "ms_per_token_step": dec["ms_per_token_step"], "achieved_gbs": dec["achieved_gbs"],
+                          "frac": dec["achieved_gbs"] / peak, "bytes_per_step": dec["bytes_per_step"],
+                          "steps": dec["steps"]}
+    if not args.no_cpu_baseline:
+        v, cores, sample, _ = cpu_oracle_sample(w)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,150 @@
+/*
+ * ssm.h -- C ABI of the B300 selective state-space scan library (libssm_b300.so).
+ *
+ * The operation is the Mamba-1 selective SSM ("Mamba и State Space Models", sections
+ * "Mamba: Selective State Space Model" and "Selective Scan (core algorithm)"; "Модуль 8.
+ * Альтернативы Transformer: SSM, Mamba и гибриды", §4 and §6; "State Space Models: Mamba и
+ * альтернатива Transformer", "Mamba: Selective State Space"), per batch b and channel d:
+ *
+ *     Δ_t  = softplus(Δ_raw[b,d,t] + delta_bias[d])        (or Δ_raw + bias if softplus is off)
+ *     h_t  = exp(Δ_t A[d,:]) ⊙ h_{t-1} + Δ_t B[b,:,t] u[b,d,t],    h_{-1} = 0
+ *     y_t  = (C[b,:,t]·h_t + D[d] u[b,d,t]) · SiLU(z[b,d,t])
+ *
+ * Conventions shared by every entry point:
+ *  - All pointers are DEVICE pointers, owned by the caller; the library never allocates or frees
+ *    device memory.  Every tensor is dense and row-major (contiguous) in the layout stated.
+ *  - Calls are asynchronous on `stream` (0 = legacy default stream).  Host-side argument checks run
+ *    before anything is enqueued; a call that returns an error has enqueued nothing.
+ *  - Inputs must not alias outputs, except the in/out state buffers of ssm_state_update.
+ *  - io tensors (u, delta, z, B, C, y and the per-token decode inputs) share one dtype, `io_dtype`;
+ *    A, D, delta_bias, conv weights and all states are float32.  Arithmetic is float32.
+ *  - Supported sizes: 1 <= dstate <= 16, d_conv == 4; batch, dim >= 1; seqlen >= 0.
+ *  - On a CUDA error the call returns SSM_ERR_CUDA; ssm_last_error_message() gives the text.
+ *  - Device-side failures that are not CUDA errors (a pipeline wait that exceeded its time limit)
+ *    set a device status word, read and cleared by ssm_device_status().
+ */
+#ifndef SSM_B300_H
+#define SSM_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define SSM_API __attribute__((visibility("default")))
+#else
+#define SSM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SSM_OK = 0,
+  SSM_ERR_INVALID_ARG = 1,   /* null pointer, bad size, bad flag, aliasing, short workspace */
+  SSM_ERR_UNSUPPORTED = 2,   /* valid but outside what this build implements (dstate > 16, d_conv != 4) */
+  SSM_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
+  SSM_ERR_TIMEOUT = 4        /* reported by ssm_device_status(): a device wait gave up */
+} ssm_status;
+
+typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
+
+typedef enum {
+  SSM_ALGO_AUTO = 0,         /* pick from the shape */
+  SSM_ALGO_SINGLE_PASS = 1,  /* one pass over time per channel tile */
+  SSM_ALGO_CHUNKED = 2       /* split time into chunks: aggregates, carry, re-run */
+} ssm_algorithm;
+
+typedef enum {
+  SSM_DISC_DELTA_B = 0,      /* input term Δ·B·x (the Mamba parameterisation) */
+  SSM_DISC_ZOH = 1           /* exact zero-order hold: (exp(ΔA) - 1)/A · B · x ("Модуль 8", §4) */
+} ssm_discretization;
+
+/* Options for ssm_scan_fwd_ex.  Zero-initialise, then set struct_size = sizeof(ssm_scan_options). */
+typedef struct {
+  int struct_size;
+  int algorithm;             /* ssm_algorithm */
+  int64_t chunk_len;         /* SSM_ALGO_CHUNKED: steps per chunk, a multiple of 64; 0 = choose */
+  int discretization;        /* ssm_discretization */
+  const float* h0;           /* initial state (batch, dim, dstate) float32, or NULL for zeros */
+} ssm_scan_options;
+
+/* ABI version of this header (increments on any signature change). */
+SSM_API int ssm_abi_version(void);
+
+/* Human-readable name of a status code (static string). */
+SSM_API const char* ssm_status_string(ssm_status s);
+
+/* Text of the last error raised on the calling host thread (empty if none). */
+SSM_API const char* ssm_last_error_message(void);
+
+/*
+ * Bytes of caller-provided device workspace that ssm_scan_fwd needs for this shape with the
+ * default algorithm choice.  0 means no workspace is needed.  Never fails; returns 0 for
+ * invalid sizes (the scan call then rejects them).
+ */
+SSM_API size_t ssm_scan_fwd_workspace_size(int batch, int dim, int dstate, int64_t seqlen, ssm_dtype io_dtype);
+
+/* Same, for a given option set (NULL = defaults). */
+SSM_API size_t ssm_scan_fwd_workspace_size_ex(int batch, int dim, int dstate, int64_t seqlen, ssm_dtype io_dtype,
+                                      const ssm_scan_options* opts);
+
+/*
+ * Prefill: the selective scan over a whole sequence.
+ *   u, delta, z, y : (batch, dim, seqlen)   io_dtype.  delta holds Δ_raw.  z may be NULL (no gate).
+ *   A              : (dim, dstate)          float32, diagonal real state matrix (any sign).
+ *   B, C           : (batch, dstate, seqlen) io_dtype, one group shared by all channels.
+ *   D, delta_bias  : (dim)                  float32, each may be NULL (treated as zero).
+ *   softplus_flag  : nonzero: Δ = softplus(Δ_raw + bias); zero: Δ = Δ_raw + bias.
+ *   last_state     : (batch, dim, dstate)   float32 output h at the last step, or NULL.
+ *   workspace      : device buffer of at least ssm_scan_fwd_workspace_size(...) bytes, 256-byte
+ *                    aligned; may be NULL when that size is 0.
+ * Precision: y matches the exact recurrence to about 1e-6 relative for float32 io and to bf16
+ * rounding (plus about 1e-4 relative) for bfloat16 io; the state is kept in float32 throughout.
+ */
+SSM_API ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                        const float* D, const void* z, const float* delta_bias, int softplus_flag,
+                        void* y, float* last_state, int batch, int dim, int dstate, int64_t seqlen,
+                        ssm_dtype io_dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ssm_scan_fwd with options (NULL = defaults): algorithm choice, chunk length, exact-ZOH input
+ * term, initial state. */
+SSM_API ssm_status ssm_scan_fwd_ex(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                           const float* D, const void* z, const float* delta_bias, int softplus_flag,
+                           void* y, float* last_state, int batch, int dim, int dstate, int64_t seqlen,
+                           ssm_dtype io_dtype, void* workspace, size_t workspace_bytes,
+                           const ssm_scan_options* opts, cudaStream_t stream);
+
+/*
+ * Decode: one token of a Mamba-1 layer with its two caches ("Модуль 8", §6 and §14):
+ *   window      = [conv_state[b,d,0..2], x_t[b,d]]
+ *   u           = SiLU(Σ_k conv_w[d,k] window[k]);   conv_state[b,d,:] <- window[1..3]
+ *   Δ           = softplus(delta_t + delta_bias[d])  (or without softplus)
+ *   state[b,d,:] <- exp(Δ A[d,:]) ⊙ state[b,d,:] + Δ B_t[b,:] u
+ *   y_t[b,d]    = (C_t[b,:]·state[b,d,:] + D[d] u) · SiLU(z_t[b,d])
+ *   x_t, delta_t, z_t, y_t : (batch, dim)     io_dtype; z_t may be NULL (no gate)
+ *   B_t, C_t               : (batch, dstate)  io_dtype
+ *   A                      : (dim, dstate)    float32;  D, delta_bias: (dim) float32 or NULL
+ *   state                  : (batch, dim, dstate) float32, updated in place
+ *   conv_state             : (batch, dim, dconv-1) float32, updated in place, oldest input first
+ *   conv_w                 : (dim, dconv)     float32; conv_w[d, dconv-1] multiplies x_t
+ * dconv must be 4.  The conv has no bias.
+ */
+SSM_API ssm_status ssm_state_update(const void* x_t, const void* delta_t, const float* A, const void* B_t,
+                            const void* C_t, const float* D, const void* z_t, float* state,
+                            float* conv_state, const float* conv_w, const float* delta_bias,
+                            int softplus_flag, void* y_t, int batch, int dim, int dstate, int dconv,
+                            ssm_dtype io_dtype, cudaStream_t stream);
+
+/*
+ * Reads and clears the device status word (synchronises `stream`).  Returns SSM_OK, SSM_ERR_TIMEOUT
+ * if a kernel gave up a bounded wait since the last call, or SSM_ERR_CUDA.
+ */
+SSM_API ssm_status ssm_device_status(cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_B300_H */

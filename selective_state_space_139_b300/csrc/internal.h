@@ -1,0 +1,73 @@
+// Internal interfaces between the C-ABI layer (ssm_api.cu) and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace ssm {
+
+// Everything a prefill pass needs; filled and validated by the API layer.
+struct ScanParams {
+  const void* u;
+  const void* delta;
+  const void* z;          // may be null
+  const void* B;
+  const void* C;
+  const float* A;
+  const float* D;         // may be null
+  const float* bias;      // may be null
+  void* y;
+  float* last_state;      // may be null
+  const float* h0;        // user initial state (batch, dim, N) or null
+  const float* h_in;      // initial state per chunk: h_in + chunk * h_in_chunk_stride, or null
+  int64_t h_in_chunk_stride;
+  float* agg_P;           // chunk aggregates (workspace), chunked algorithm only
+  float* agg_Q;
+  int batch, dim, N;
+  int64_t L;
+  int64_t chunk_len;      // steps per chunk (== L for a single pass)
+  int softplus;
+  int disc;               // 0: Δ·B, 1: exact ZOH
+  int io_bf16;            // 1: bfloat16 io, 0: float32 io
+  int tma_ok;             // the layout allows 2D TMA tensor maps
+  int vec_ok;             // y rows allow 16-byte stores
+};
+
+// Steps per time tile for an io element size (64 for bf16, 32 for float32).
+int scan_tile_steps(int io_bytes);
+
+// Launches the passes of one prefill call on `stream` (nchunks == 1: single pass).
+cudaError_t scan_fwd_launch(const ScanParams& p, int nchunks, cudaStream_t stream, char* err, size_t errlen);
+
+// Builds a 2D tiled tensor map (rows of `inner` elements, `rows` rows, 128-byte swizzle, zero fill).
+bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint64_t inner, uint64_t rows,
+                          uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows, char* err,
+                          size_t errlen);
+
+struct DecodeParams {
+  const void* x;
+  const void* delta;
+  const void* z;          // may be null
+  const void* B;
+  const void* C;
+  const float* A;
+  const float* D;         // may be null
+  const float* bias;      // may be null
+  const float* conv_w;
+  float* state;
+  float* conv_state;
+  void* y;
+  int batch, dim, N;
+  int softplus;
+  int io_bf16;
+  int vec16;              // dstate == 16 and state, A, conv_w, B, C aligned for vector access
+};
+
+cudaError_t state_update_launch(const DecodeParams& p, cudaStream_t stream);
+
+// Device status word access (scan_fwd.cu owns the symbol).
+cudaError_t read_and_clear_device_status(unsigned int* out, cudaStream_t stream);
+
+}  // namespace ssm

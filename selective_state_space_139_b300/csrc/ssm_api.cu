@@ -1,0 +1,351 @@
+// C ABI of libssm_b300.so (declared in include/ssm.h): argument checks, algorithm choice,
+// workspace layout, TMA tensor-map encoding and dispatch to the kernels.  Every check runs on the
+// host before anything is enqueued.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "ssm.h"
+
+namespace {
+
+thread_local char g_err[512] = {0};
+
+void set_err(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+
+ssm_status fail(ssm_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+ssm_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(SSM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int kChannelsPerCta = 128;
+constexpr int64_t kMinChunkTiles = 4;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Range {
+  uintptr_t lo, hi;
+};
+Range range_of(const void* p, size_t bytes) {
+  uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return {a, a + bytes};
+}
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 148;
+  }
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return 148;
+  }
+  return n;
+}
+
+struct Plan {
+  int nchunks = 1;
+  int64_t chunk_len = 0;
+  size_t workspace = 0;
+  size_t off_P = 0, off_Q = 0, off_hin = 0;
+};
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Decides single pass vs chunked and lays out the workspace.  Returns false on bad options.
+bool make_plan(int batch, int dim, int dstate, int64_t seqlen, ssm_dtype io, const ssm_scan_options* o, Plan* pl) {
+  const int T = ssm::scan_tile_steps(io == SSM_BF16 ? 2 : 4);
+  const int algo = o ? o->algorithm : SSM_ALGO_AUTO;
+  const int64_t groups = static_cast<int64_t>(batch) * ((dim + kChannelsPerCta - 1) / kChannelsPerCta);
+  int64_t chunk = 0;
+  if (algo == SSM_ALGO_SINGLE_PASS) {
+    chunk = 0;
+  } else if (algo == SSM_ALGO_CHUNKED) {
+    chunk = o->chunk_len;
+    if (chunk < 0 || chunk % 64 != 0) return false;
+    if (chunk == 0) {
+      const int64_t target = std::max<int64_t>(2, (4 * sm_count() + groups - 1) / groups);
+      chunk = round_up(static_cast<size_t>((seqlen + target - 1) / target), 64);
+    }
+  } else if (algo == SSM_ALGO_AUTO) {
+    const int sms = sm_count();
+    if (groups < sms && seqlen >= 2 * kMinChunkTiles * T) {
+      const int64_t target = (4 * sms + groups - 1) / groups;
+      int64_t c = round_up(static_cast<size_t>((seqlen + target - 1) / target), 64);
+      c = std::max<int64_t>(c, kMinChunkTiles * 64);
+      if (c < seqlen) chunk = c;
+    }
+  } else {
+    return false;
+  }
+  // grid.z holds the chunk index: keep the chunk count within 65535
+  if (chunk > 0 && (seqlen + chunk - 1) / chunk > 65535)
+    chunk = round_up(static_cast<size_t>((seqlen + 65534) / 65535), 64);
+  if (chunk <= 0 || chunk >= seqlen) {
+    pl->nchunks = 1;
+    pl->chunk_len = seqlen;
+    pl->workspace = 0;
+    return true;
+  }
+  pl->chunk_len = chunk;
+  pl->nchunks = static_cast<int>((seqlen + chunk - 1) / chunk);
+  const size_t per_chunk = static_cast<size_t>(batch) * dim * dstate * sizeof(float);
+  pl->off_P = 0;
+  pl->off_Q = round_up(per_chunk * (pl->nchunks - 1), 256);
+  pl->off_hin = pl->off_Q + round_up(per_chunk * (pl->nchunks - 1), 256);
+  pl->workspace = pl->off_hin + round_up(per_chunk * pl->nchunks, 256);
+  return true;
+}
+
+bool sizes_ok(int batch, int dim, int dstate, int64_t seqlen, ssm_dtype io) {
+  return batch >= 1 && dim >= 1 && dstate >= 1 && dstate <= 16 && seqlen >= 0 && (io == SSM_F32 || io == SSM_BF16);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+}  // namespace
+
+namespace ssm {
+
+bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint64_t inner, uint64_t rows,
+                          uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows, char* err,
+                          size_t errlen) {
+  auto enc = tensor_map_encoder();
+  if (!enc) {
+    snprintf(err, errlen, "cuTensorMapEncodeTiled is not available");
+    return false;
+  }
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {row_pitch_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, dtype, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(err, errlen, "cuTensorMapEncodeTiled failed with %d", static_cast<int>(r));
+    return false;
+  }
+  return true;
+}
+
+}  // namespace ssm
+
+extern "C" {
+
+int ssm_abi_version(void) { return 1; }
+
+const char* ssm_status_string(ssm_status s) {
+  switch (s) {
+    case SSM_OK: return "SSM_OK";
+    case SSM_ERR_INVALID_ARG: return "SSM_ERR_INVALID_ARG";
+    case SSM_ERR_UNSUPPORTED: return "SSM_ERR_UNSUPPORTED";
+    case SSM_ERR_CUDA: return "SSM_ERR_CUDA";
+    case SSM_ERR_TIMEOUT: return "SSM_ERR_TIMEOUT";
+  }
+  return "SSM_ERR_UNKNOWN";
+}
+
+const char* ssm_last_error_message(void) { return g_err; }
+
+size_t ssm_scan_fwd_workspace_size_ex(int batch, int dim, int dstate, int64_t seqlen, ssm_dtype io_dtype,
+                                      const ssm_scan_options* opts) {
+  if (!sizes_ok(batch, dim, dstate, seqlen, io_dtype)) return 0;
+  if (opts && opts->struct_size != static_cast<int>(sizeof(ssm_scan_options))) return 0;
+  Plan pl;
+  if (!make_plan(batch, dim, dstate, seqlen, io_dtype, opts, &pl)) return 0;
+  return pl.workspace;
+}
+
+size_t ssm_scan_fwd_workspace_size(int batch, int dim, int dstate, int64_t seqlen, ssm_dtype io_dtype) {
+  return ssm_scan_fwd_workspace_size_ex(batch, dim, dstate, seqlen, io_dtype, nullptr);
+}
+
+ssm_status ssm_scan_fwd_ex(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                           const float* D, const void* z, const float* delta_bias, int softplus_flag, void* y,
+                           float* last_state, int batch, int dim, int dstate, int64_t seqlen, ssm_dtype io_dtype,
+                           void* workspace, size_t workspace_bytes, const ssm_scan_options* opts,
+                           cudaStream_t stream) {
+  g_err[0] = 0;
+  if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return fail(SSM_ERR_INVALID_ARG, "unknown io_dtype %d", io_dtype);
+  if (batch < 1 || dim < 1 || seqlen < 0 || dstate < 1)
+    return fail(SSM_ERR_INVALID_ARG, "bad sizes batch=%d dim=%d dstate=%d seqlen=%lld", batch, dim, dstate,
+                static_cast<long long>(seqlen));
+  if (dstate > 16) return fail(SSM_ERR_UNSUPPORTED, "dstate=%d > 16 is not supported", dstate);
+  if (seqlen > (int64_t(1) << 32)) return fail(SSM_ERR_UNSUPPORTED, "seqlen above 2^32 is not supported");
+  if (batch > 65535) return fail(SSM_ERR_UNSUPPORTED, "batch=%d above 65535 is not supported", batch);
+  if (opts && opts->struct_size != static_cast<int>(sizeof(ssm_scan_options)))
+    return fail(SSM_ERR_INVALID_ARG, "ssm_scan_options.struct_size mismatch");
+  const int disc = opts ? opts->discretization : SSM_DISC_DELTA_B;
+  if (disc != SSM_DISC_DELTA_B && disc != SSM_DISC_ZOH)
+    return fail(SSM_ERR_INVALID_ARG, "unknown discretization %d", disc);
+  const float* h0 = opts ? opts->h0 : nullptr;
+  if (seqlen > 0 && (!u || !delta || !A || !B || !C || !y))
+    return fail(SSM_ERR_INVALID_ARG, "null required pointer (u, delta, A, B, C, y)");
+  const size_t e = io_dtype == SSM_BF16 ? 2 : 4;
+  const void* io_ptrs[] = {u, delta, z, B, C, y};
+  for (const void* p : io_ptrs)
+    if (p && !aligned(p, e)) return fail(SSM_ERR_INVALID_ARG, "io pointer not aligned to its element size");
+  const void* f_ptrs[] = {A, D, delta_bias, last_state, h0};
+  for (const void* p : f_ptrs)
+    if (p && !aligned(p, 4)) return fail(SSM_ERR_INVALID_ARG, "float32 pointer not 4-byte aligned");
+  Plan pl;
+  if (!make_plan(batch, dim, dstate, seqlen, io_dtype, opts, &pl))
+    return fail(SSM_ERR_INVALID_ARG, "bad algorithm or chunk_len (a multiple of 64 is required)");
+
+  const size_t bdl = static_cast<size_t>(batch) * dim * seqlen * e;
+  const size_t bnl = static_cast<size_t>(batch) * dstate * seqlen * e;
+  const size_t st = static_cast<size_t>(batch) * dim * dstate * 4;
+  const Range outs[] = {range_of(y, bdl), range_of(last_state, last_state ? st : 0)};
+  const Range ins[] = {range_of(u, bdl), range_of(delta, bdl), range_of(z, z ? bdl : 0), range_of(B, bnl),
+                       range_of(C, bnl), range_of(A, static_cast<size_t>(dim) * dstate * 4),
+                       range_of(D, D ? dim * 4 : 0), range_of(delta_bias, delta_bias ? dim * 4 : 0),
+                       range_of(h0, h0 ? st : 0)};
+  for (const Range& o : outs)
+    for (const Range& i : ins)
+      if (overlap(o, i)) return fail(SSM_ERR_INVALID_ARG, "an output overlaps an input");
+  if (y && last_state && overlap(outs[0], outs[1])) return fail(SSM_ERR_INVALID_ARG, "y overlaps last_state");
+  if (pl.workspace > 0) {
+    if (!workspace || workspace_bytes < pl.workspace)
+      return fail(SSM_ERR_INVALID_ARG, "workspace of %zu bytes required, %zu given", pl.workspace, workspace_bytes);
+    if (!aligned(workspace, 256)) return fail(SSM_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    const Range w = range_of(workspace, pl.workspace);
+    for (const Range& i : ins)
+      if (overlap(w, i)) return fail(SSM_ERR_INVALID_ARG, "workspace overlaps an input");
+    for (const Range& o : outs)
+      if (overlap(w, o)) return fail(SSM_ERR_INVALID_ARG, "workspace overlaps an output");
+  }
+
+  if (seqlen == 0) {
+    // no steps: the final state is the initial state
+    if (last_state) {
+      cudaError_t ce = h0 ? cudaMemcpyAsync(last_state, h0, st, cudaMemcpyDeviceToDevice, stream)
+                          : cudaMemsetAsync(last_state, 0, st, stream);
+      if (ce != cudaSuccess) return cuda_fail(ce, "seqlen 0 state copy");
+    }
+    return SSM_OK;
+  }
+
+  ssm::ScanParams p;
+  memset(&p, 0, sizeof(p));
+  p.u = u; p.delta = delta; p.z = z; p.B = B; p.C = C; p.A = A; p.D = D; p.bias = delta_bias;
+  p.y = y; p.last_state = last_state; p.h0 = h0;
+  p.batch = batch; p.dim = dim; p.N = dstate; p.L = seqlen;
+  p.softplus = softplus_flag != 0; p.disc = disc; p.io_bf16 = io_dtype == SSM_BF16;
+  const int T = ssm::scan_tile_steps(static_cast<int>(e));
+  bool tma = ((seqlen * e) % 16 == 0) && seqlen >= T && static_cast<int64_t>(batch) * dim >= kChannelsPerCta;
+  for (const void* q : {u, delta, z, B, C})
+    if (q && !aligned(q, 16)) tma = false;
+  p.tma_ok = tma;
+  p.vec_ok = aligned(y, 16) && (seqlen * e) % 16 == 0;
+  if (pl.nchunks > 1) {
+    char* ws = static_cast<char*>(workspace);
+    p.agg_P = reinterpret_cast<float*>(ws + pl.off_P);
+    p.agg_Q = reinterpret_cast<float*>(ws + pl.off_Q);
+    p.h_in = reinterpret_cast<float*>(ws + pl.off_hin);
+    p.h_in_chunk_stride = static_cast<int64_t>(batch) * dim * dstate;
+    p.chunk_len = pl.chunk_len;
+  } else {
+    p.h_in = h0;
+    p.h_in_chunk_stride = 0;
+    p.chunk_len = seqlen;
+  }
+  char err[256] = {0};
+  cudaError_t ce = ssm::scan_fwd_launch(p, pl.nchunks, stream, err, sizeof(err));
+  if (ce != cudaSuccess) return cuda_fail(ce, "scan launch");
+  return SSM_OK;
+}
+
+ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                        const float* D, const void* z, const float* delta_bias, int softplus_flag, void* y,
+                        float* last_state, int batch, int dim, int dstate, int64_t seqlen, ssm_dtype io_dtype,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return ssm_scan_fwd_ex(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state, batch, dim, dstate,
+                         seqlen, io_dtype, workspace, workspace_bytes, nullptr, stream);
+}
+
+ssm_status ssm_state_update(const void* x_t, const void* delta_t, const float* A, const void* B_t, const void* C_t,
+                            const float* D, const void* z_t, float* state, float* conv_state, const float* conv_w,
+                            const float* delta_bias, int softplus_flag, void* y_t, int batch, int dim, int dstate,
+                            int dconv, ssm_dtype io_dtype, cudaStream_t stream) {
+  g_err[0] = 0;
+  if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return fail(SSM_ERR_INVALID_ARG, "unknown io_dtype %d", io_dtype);
+  if (batch < 1 || dim < 1 || dstate < 1 || dconv < 1)
+    return fail(SSM_ERR_INVALID_ARG, "bad sizes batch=%d dim=%d dstate=%d dconv=%d", batch, dim, dstate, dconv);
+  if (dstate > 16) return fail(SSM_ERR_UNSUPPORTED, "dstate=%d > 16 is not supported", dstate);
+  if (dconv != 4) return fail(SSM_ERR_UNSUPPORTED, "d_conv=%d is not supported (only 4)", dconv);
+  if (!x_t || !delta_t || !A || !B_t || !C_t || !state || !conv_state || !conv_w || !y_t)
+    return fail(SSM_ERR_INVALID_ARG, "null required pointer");
+  const size_t e = io_dtype == SSM_BF16 ? 2 : 4;
+  for (const void* p : {x_t, delta_t, z_t, B_t, C_t, static_cast<const void*>(y_t)})
+    if (p && !aligned(p, e)) return fail(SSM_ERR_INVALID_ARG, "io pointer not aligned to its element size");
+  for (const void* p : {static_cast<const void*>(A), static_cast<const void*>(D),
+                        static_cast<const void*>(delta_bias), static_cast<const void*>(state),
+                        static_cast<const void*>(conv_state), static_cast<const void*>(conv_w)})
+    if (p && !aligned(p, 4)) return fail(SSM_ERR_INVALID_ARG, "float32 pointer not 4-byte aligned");
+  const size_t bd = static_cast<size_t>(batch) * dim;
+  const Range outs[] = {range_of(y_t, bd * e), range_of(state, bd * dstate * 4),
+                        range_of(conv_state, bd * (dconv - 1) * 4)};
+  const Range ins[] = {range_of(x_t, bd * e), range_of(delta_t, bd * e), range_of(z_t, z_t ? bd * e : 0),
+                       range_of(B_t, batch * dstate * e), range_of(C_t, batch * dstate * e),
+                       range_of(A, static_cast<size_t>(dim) * dstate * 4), range_of(D, D ? dim * 4 : 0),
+                       range_of(delta_bias, delta_bias ? dim * 4 : 0), range_of(conv_w, dim * dconv * 4)};
+  for (const Range& o : outs)
+    for (const Range& i : ins)
+      if (overlap(o, i)) return fail(SSM_ERR_INVALID_ARG, "an output or state overlaps an input");
+  if (overlap(outs[0], outs[1]) || overlap(outs[0], outs[2]) || overlap(outs[1], outs[2]))
+    return fail(SSM_ERR_INVALID_ARG, "y_t, state and conv_state overlap");
+  ssm::DecodeParams p;
+  memset(&p, 0, sizeof(p));
+  p.x = x_t; p.delta = delta_t; p.z = z_t; p.B = B_t; p.C = C_t; p.A = A; p.D = D; p.bias = delta_bias;
+  p.conv_w = conv_w; p.state = state; p.conv_state = conv_state; p.y = y_t;
+  p.batch = batch; p.dim = dim; p.N = dstate; p.softplus = softplus_flag != 0; p.io_bf16 = io_dtype == SSM_BF16;
+  p.vec16 = dstate == 16 && aligned(state, 16) && aligned(A, 16) && aligned(conv_w, 16) && aligned(B_t, 8) &&
+            aligned(C_t, 8);
+  cudaError_t ce = ssm::state_update_launch(p, stream);
+  if (ce != cudaSuccess) return cuda_fail(ce, "state update launch");
+  return SSM_OK;
+}
+
+ssm_status ssm_device_status(cudaStream_t stream) {
+  unsigned int word = 0;
+  cudaError_t ce = ssm::read_and_clear_device_status(&word, stream);
+  if (ce != cudaSuccess) return cuda_fail(ce, "device status read");
+  if (word != 0) return fail(SSM_ERR_TIMEOUT, "a device wait gave up (status word 0x%x)", word);
+  return SSM_OK;
+}
+
+}  // extern "C"

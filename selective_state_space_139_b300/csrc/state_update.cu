@@ -1,0 +1,140 @@
+// One-token decode step of a Mamba-1 layer with its two caches ("Модуль 8. Альтернативы
+// Transformer: SSM, Mamba и гибриды", §6 and §14; conv + SiLU as in "State Space Models: Mamba и
+// альтернатива Transformer", "Mamba: Selective State Space"):
+//   u = SiLU(Σ_k w[d,k] · [conv_state, x_t][k]);  conv_state <- last 3 raw inputs
+//   Δ = softplus(Δ_raw + bias);  h <- exp(Δ A) ⊙ h + Δ B_t u;  y = (C_t·h + D u) · SiLU(z_t)
+//
+// The step is bound by HBM traffic on the float32 state (read + write 64 bytes per channel for
+// dstate 16).  Four lanes share a channel, each owning four consecutive states, so a warp moves
+// 8 channels x 64 contiguous bytes with 128-bit accesses; the per-channel scalars are computed
+// redundantly by the four lanes and the readout is reduced with two shuffles.
+#include "internal.h"
+#include "ssm_device.cuh"
+
+namespace ssm {
+namespace {
+
+constexpr int kLanesPerChannel = 4;
+constexpr int kThreads = 256;
+constexpr int kChannelsPerBlock = kThreads / kLanesPerChannel;
+
+template <typename IO>
+__device__ __forceinline__ float ld_io(const void* p, int64_t i) {
+  return IoTraits<IO>::to_f32(static_cast<const IO*>(p)[i]);
+}
+
+template <typename IO, bool kFull16>
+__global__ void __launch_bounds__(kThreads) state_update_kernel(const DecodeParams p) {
+  constexpr bool kFast = sizeof(IO) == 2;
+  const int tid = threadIdx.x;
+  const int64_t c_raw = static_cast<int64_t>(blockIdx.x) * kChannelsPerBlock + tid / kLanesPerChannel;
+  const int j = tid % kLanesPerChannel;
+  const int64_t nchan = static_cast<int64_t>(p.batch) * p.dim;
+  // lanes past the last channel still take part in the shuffles; they read a valid channel and
+  // write nothing
+  const bool live = c_raw < nchan;
+  const int64_t c = live ? c_raw : nchan - 1;
+  const int b = static_cast<int>(c / p.dim);
+  const int d = static_cast<int>(c % p.dim);
+  const int N = kFull16 ? 16 : p.N;
+
+  // conv window [cs0, cs1, cs2, x_t] and its weights
+  const float x = ld_io<IO>(p.x, c);
+  float* cs = p.conv_state + c * 3;
+  const float cs0 = cs[0], cs1 = cs[1], cs2 = cs[2];
+  float4 w;
+  if (kFull16) {
+    w = *reinterpret_cast<const float4*>(p.conv_w + static_cast<int64_t>(d) * 4);
+  } else {
+    const float* wr = p.conv_w + static_cast<int64_t>(d) * 4;
+    w = make_float4(wr[0], wr[1], wr[2], wr[3]);
+  }
+  const float s = fmaf(w.w, x, fmaf(w.z, cs2, fmaf(w.y, cs1, w.x * cs0)));
+  const float u = kFast ? silu_fast(s) : silu_accurate(s);
+
+  const float v = ld_io<IO>(p.delta, c) + (p.bias ? p.bias[d] : 0.0f);
+  const float dl = p.softplus ? (kFast ? softplus_fast(v) : softplus_accurate(v)) : v;
+  const float wu = dl * u;
+
+  float hv[4], av[4], bv[4], cv[4];
+  float* srow = p.state + c * N;
+  const float* arow = p.A + static_cast<int64_t>(d) * N;
+  const int64_t bcrow = static_cast<int64_t>(b) * N;
+  if (kFull16) {
+    const float4 h4 = *reinterpret_cast<const float4*>(srow + 4 * j);
+    const float4 a4 = *reinterpret_cast<const float4*>(arow + 4 * j);
+    hv[0] = h4.x; hv[1] = h4.y; hv[2] = h4.z; hv[3] = h4.w;
+    av[0] = a4.x; av[1] = a4.y; av[2] = a4.z; av[3] = a4.w;
+    if (kFast) {
+      const uint2 braw = *reinterpret_cast<const uint2*>(static_cast<const IO*>(p.B) + bcrow + 4 * j);
+      const uint2 craw = *reinterpret_cast<const uint2*>(static_cast<const IO*>(p.C) + bcrow + 4 * j);
+      bv[0] = bf16lo_to_f32(braw.x); bv[1] = bf16hi_to_f32(braw.x);
+      bv[2] = bf16lo_to_f32(braw.y); bv[3] = bf16hi_to_f32(braw.y);
+      cv[0] = bf16lo_to_f32(craw.x); cv[1] = bf16hi_to_f32(craw.x);
+      cv[2] = bf16lo_to_f32(craw.y); cv[3] = bf16hi_to_f32(craw.y);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        bv[i] = ld_io<IO>(p.B, bcrow + 4 * j + i);
+        cv[i] = ld_io<IO>(p.C, bcrow + 4 * j + i);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int n = 4 * j + i;
+      const bool in = n < N;
+      hv[i] = in ? srow[n] : 0.0f;
+      av[i] = in ? arow[n] : 0.0f;
+      bv[i] = in ? ld_io<IO>(p.B, bcrow + n) : 0.0f;
+      cv[i] = in ? ld_io<IO>(p.C, bcrow + n) : 0.0f;
+    }
+  }
+
+  float py = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float a = kFast ? ex2_approx(dl * av[i] * kLog2e) : expf(dl * av[i]);
+    hv[i] = fmaf(a, hv[i], wu * bv[i]);
+    py = fmaf(cv[i], hv[i], py);
+  }
+  py += __shfl_xor_sync(0xffffffffu, py, 1);
+  py += __shfl_xor_sync(0xffffffffu, py, 2);
+
+  // every lane has read the old conv window before any lane overwrites it
+  __syncwarp();
+  if (!live) return;
+  if (kFull16) {
+    *reinterpret_cast<float4*>(srow + 4 * j) = make_float4(hv[0], hv[1], hv[2], hv[3]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (4 * j + i < N) srow[4 * j + i] = hv[i];
+  }
+  if (j < 3) cs[j] = j == 0 ? cs1 : (j == 1 ? cs2 : x);
+  if (j == 0) {
+    float y = fmaf(p.D ? p.D[d] : 0.0f, u, py);
+    if (p.z) {
+      const float z = ld_io<IO>(p.z, c);
+      y *= kFast ? silu_fast(z) : silu_accurate(z);
+    }
+    static_cast<IO*>(p.y)[c] = IoTraits<IO>::from_f32(y);
+  }
+}
+
+template <typename IO>
+cudaError_t launch(const DecodeParams& p, cudaStream_t stream) {
+  const int64_t nchan = static_cast<int64_t>(p.batch) * p.dim;
+  const unsigned blocks = static_cast<unsigned>((nchan + kChannelsPerBlock - 1) / kChannelsPerBlock);
+  if (p.vec16) state_update_kernel<IO, true><<<blocks, kThreads, 0, stream>>>(p);
+  else state_update_kernel<IO, false><<<blocks, kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t state_update_launch(const DecodeParams& p, cudaStream_t stream) {
+  return p.io_bf16 ? launch<__nv_bfloat16>(p, stream) : launch<float>(p, stream);
+}
+
+}  // namespace ssm

@@ -1,0 +1,217 @@
+"""Thin Python binding over libssm_b300.so (C ABI in include/ssm.h).
+
+Argument marshalling only: every step of the scan and the decode step runs in the library's CUDA
+kernels.  PyTorch supplies device memory and the current stream.  There is no CPU fallback: if the
+library is missing or a tensor is not on a CUDA device, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+from . import build as _build
+
+SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_TIMEOUT = range(5)
+SSM_F32, SSM_BF16 = 0, 1
+ALGORITHMS = {"auto": 0, "single_pass": 1, "chunked": 2}
+DISCRETIZATIONS = {"delta_b": 0, "zoh": 1}
+
+_lib = None
+
+
+class SSMError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_status_name(status)}: {message}")
+        self.status = status
+
+
+class ScanOptions(ctypes.Structure):
+    _fields_ = [("struct_size", ctypes.c_int), ("algorithm", ctypes.c_int), ("chunk_len", ctypes.c_int64),
+                ("discretization", ctypes.c_int), ("h0", ctypes.c_void_p)]
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Loads the in-tree library (built beforehand by ``build.py``); raises if it is missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    path = path or _build.LIB
+    if not os.path.exists(path):
+        raise ImportError(f"libssm_b300.so not found at {path}; build it with "
+                          f"`python -m selective_state_space_139_b300.build`")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    lib.ssm_abi_version.restype = i32
+    lib.ssm_abi_version.argtypes = []
+    lib.ssm_status_string.restype = ctypes.c_char_p
+    lib.ssm_status_string.argtypes = [i32]
+    lib.ssm_last_error_message.restype = ctypes.c_char_p
+    lib.ssm_last_error_message.argtypes = []
+    lib.ssm_scan_fwd_workspace_size.restype = sz
+    lib.ssm_scan_fwd_workspace_size.argtypes = [i32, i32, i32, i64, i32]
+    lib.ssm_scan_fwd_workspace_size_ex.restype = sz
+    lib.ssm_scan_fwd_workspace_size_ex.argtypes = [i32, i32, i32, i64, i32, ctypes.POINTER(ScanOptions)]
+    scan = [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i64, i32, vp, sz]
+    lib.ssm_scan_fwd.restype = i32
+    lib.ssm_scan_fwd.argtypes = scan + [vp]
+    lib.ssm_scan_fwd_ex.restype = i32
+    lib.ssm_scan_fwd_ex.argtypes = scan + [ctypes.POINTER(ScanOptions), vp]
+    lib.ssm_state_update.restype = i32
+    lib.ssm_state_update.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, vp]
+    lib.ssm_device_status.restype = i32
+    lib.ssm_device_status.argtypes = [vp]
+    if path == _build.LIB:
+        _lib = lib
+    return lib
+
+
+def _status_name(s: int) -> str:
+    return {0: "SSM_OK", 1: "SSM_ERR_INVALID_ARG", 2: "SSM_ERR_UNSUPPORTED", 3: "SSM_ERR_CUDA",
+            4: "SSM_ERR_TIMEOUT"}.get(s, f"status {s}")
+
+
+def _check(lib, status: int):
+    if status != SSM_OK:
+        raise SSMError(status, lib.ssm_last_error_message().decode(errors="replace"))
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _io_code(dtype) -> int:
+    if dtype == torch.bfloat16:
+        return SSM_BF16
+    if dtype == torch.float32:
+        return SSM_F32
+    raise TypeError(f"io dtype must be bfloat16 or float32, got {dtype}")
+
+
+def _need(t: Optional[torch.Tensor], name: str, shape, dtype, device, optional=False):
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU path exists)")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream_handle(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _options(algorithm: str, chunk_len: int, discretization: str, h0: Optional[torch.Tensor]) -> ScanOptions:
+    o = ScanOptions()
+    o.struct_size = ctypes.sizeof(ScanOptions)
+    o.algorithm = ALGORITHMS[algorithm]
+    o.chunk_len = int(chunk_len)
+    o.discretization = DISCRETIZATIONS[discretization]
+    o.h0 = _ptr(h0)
+    return o
+
+
+def scan_workspace_size(batch: int, dim: int, dstate: int, seqlen: int, dtype=torch.bfloat16,
+                        algorithm: str = "auto", chunk_len: int = 0, discretization: str = "delta_b") -> int:
+    lib = load_library()
+    o = _options(algorithm, chunk_len, discretization, None)
+    return int(lib.ssm_scan_fwd_workspace_size_ex(batch, dim, dstate, seqlen, _io_code(dtype), ctypes.byref(o)))
+
+
+def selective_scan_fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor, C: torch.Tensor,
+                       D: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
+                       delta_bias: Optional[torch.Tensor] = None, delta_softplus: bool = True,
+                       return_last_state: bool = True, *, algorithm: str = "auto", chunk_len: int = 0,
+                       discretization: str = "delta_b", h0: Optional[torch.Tensor] = None,
+                       out: Optional[torch.Tensor] = None, last_state: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None, stream=None
+                       ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Prefill scan.  u, delta, z: (batch, dim, L); A: (dim, N) f32; B, C: (batch, N, L);
+    D, delta_bias: (dim,) f32; h0: (batch, dim, N) f32.  Returns (y, last_state)."""
+    lib = load_library()
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    dev = u.device
+    io = u.dtype
+    _need(u, "u", (batch, dim, L), io, dev)
+    _need(delta, "delta", (batch, dim, L), io, dev)
+    _need(z, "z", (batch, dim, L), io, dev, optional=True)
+    _need(A, "A", (dim, N), torch.float32, dev)
+    _need(B, "B", (batch, N, L), io, dev)
+    _need(C, "C", (batch, N, L), io, dev)
+    _need(D, "D", (dim,), torch.float32, dev, optional=True)
+    _need(delta_bias, "delta_bias", (dim,), torch.float32, dev, optional=True)
+    _need(h0, "h0", (batch, dim, N), torch.float32, dev, optional=True)
+    y = torch.empty_like(u) if out is None else out
+    _need(y, "out", (batch, dim, L), io, dev)
+    if return_last_state and last_state is None:
+        last_state = torch.empty((batch, dim, N), dtype=torch.float32, device=dev)
+    if last_state is not None:
+        _need(last_state, "last_state", (batch, dim, N), torch.float32, dev)
+    o = _options(algorithm, chunk_len, discretization, h0)
+    ws_bytes = int(lib.ssm_scan_fwd_workspace_size_ex(batch, dim, N, L, _io_code(io), ctypes.byref(o)))
+    if ws_bytes and (workspace is None or workspace.numel() < ws_bytes):
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.ssm_scan_fwd_ex(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+                                 int(bool(delta_softplus)), _ptr(y), _ptr(last_state), batch, dim, N, L, _io_code(io),
+                                 _ptr(workspace) if ws_bytes else None, ws_bytes, ctypes.byref(o),
+                                 _stream_handle(stream))
+    _check(lib, st)
+    return y, last_state
+
+
+def selective_state_update(x_t: torch.Tensor, delta_t: torch.Tensor, A: torch.Tensor, B_t: torch.Tensor,
+                           C_t: torch.Tensor, D: Optional[torch.Tensor], z_t: Optional[torch.Tensor],
+                           state: torch.Tensor, conv_state: torch.Tensor, conv_w: torch.Tensor,
+                           delta_bias: Optional[torch.Tensor] = None, delta_softplus: bool = True,
+                           out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """One decode step; updates ``state`` (batch, dim, N) and ``conv_state`` (batch, dim, 3) in place.
+    x_t, delta_t, z_t: (batch, dim); B_t, C_t: (batch, N); conv_w: (dim, 4) f32.  Returns y_t."""
+    lib = load_library()
+    batch, dim = x_t.shape
+    N = A.shape[1]
+    K = conv_w.shape[1]
+    dev = x_t.device
+    io = x_t.dtype
+    _need(x_t, "x_t", (batch, dim), io, dev)
+    _need(delta_t, "delta_t", (batch, dim), io, dev)
+    _need(z_t, "z_t", (batch, dim), io, dev, optional=True)
+    _need(A, "A", (dim, N), torch.float32, dev)
+    _need(B_t, "B_t", (batch, N), io, dev)
+    _need(C_t, "C_t", (batch, N), io, dev)
+    _need(D, "D", (dim,), torch.float32, dev, optional=True)
+    _need(delta_bias, "delta_bias", (dim,), torch.float32, dev, optional=True)
+    _need(state, "state", (batch, dim, N), torch.float32, dev)
+    _need(conv_state, "conv_state", (batch, dim, K - 1), torch.float32, dev)
+    _need(conv_w, "conv_w", (dim, K), torch.float32, dev)
+    y = torch.empty_like(x_t) if out is None else out
+    _need(y, "out", (batch, dim), io, dev)
+    with torch.cuda.device(dev):
+        st = lib.ssm_state_update(_ptr(x_t), _ptr(delta_t), _ptr(A), _ptr(B_t), _ptr(C_t), _ptr(D), _ptr(z_t),
+                                  _ptr(state), _ptr(conv_state), _ptr(conv_w), _ptr(delta_bias),
+                                  int(bool(delta_softplus)), _ptr(y), batch, dim, N, K, _io_code(io),
+                                  _stream_handle(stream))
+    _check(lib, st)
+    return y
+
+
+def device_status(stream=None) -> int:
+    """Reads and clears the library's device status word (synchronises the stream)."""
+    lib = load_library()
+    return int(lib.ssm_device_status(_stream_handle(stream)))

@@ -1,0 +1,114 @@
+"""The C ABI without a GPU: the library loads, exports every entry point include/ssm.h declares,
+and rejects bad arguments on the host (before any CUDA call) with the documented status codes."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from selective_state_space_139_b300 import build, ssm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return ssm.load_library()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "ssm.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S).replace("SSM_API", "")
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z_0-9]*\s*\*?\s*([a-z_][a-z_0-9]*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n.startswith("ssm_")))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert "ssm_scan_fwd" in names and "ssm_state_update" in names and len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in ssm.h but not exported"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.ssm_abi_version() == 1
+    assert lib.ssm_status_string(0) == b"SSM_OK"
+    assert lib.ssm_status_string(2) == b"SSM_ERR_UNSUPPORTED"
+
+
+# Fake device addresses: validation never dereferences them.
+P = 0x7f0000000000
+
+
+def _scan(lib, **kw):
+    a = dict(u=P, delta=P + 0x10000000, A=P + 0x20000000, B=P + 0x30000000, C=P + 0x40000000, D=None, z=None,
+             bias=None, softplus=1, y=P + 0x50000000, last=None, batch=2, dim=8, dstate=16, seqlen=64, io=ssm.SSM_BF16,
+             ws=None, wsb=0, opts=None, stream=None)
+    a.update(kw)
+    return lib.ssm_scan_fwd_ex(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"], a["bias"], a["softplus"],
+                               a["y"], a["last"], a["batch"], a["dim"], a["dstate"], a["seqlen"], a["io"], a["ws"],
+                               a["wsb"], a["opts"], a["stream"])
+
+
+def test_scan_rejects_bad_arguments_on_host(lib):
+    assert _scan(lib, dstate=17) == ssm.SSM_ERR_UNSUPPORTED
+    assert _scan(lib, dstate=0) == ssm.SSM_ERR_INVALID_ARG
+    assert _scan(lib, batch=0) == ssm.SSM_ERR_INVALID_ARG
+    assert _scan(lib, seqlen=-1) == ssm.SSM_ERR_INVALID_ARG
+    assert _scan(lib, io=7) == ssm.SSM_ERR_INVALID_ARG
+    assert _scan(lib, u=None) == ssm.SSM_ERR_INVALID_ARG
+    assert _scan(lib, y=None) == ssm.SSM_ERR_INVALID_ARG
+    assert _scan(lib, u=P + 1) == ssm.SSM_ERR_INVALID_ARG                 # misaligned bf16
+    assert _scan(lib, A=P + 0x20000002) == ssm.SSM_ERR_INVALID_ARG        # misaligned float32
+    assert _scan(lib, y=P + 0x10) == ssm.SSM_ERR_INVALID_ARG              # y overlaps u
+    assert b"overlaps" in lib.ssm_last_error_message()
+    bad = ssm.ScanOptions()
+    bad.struct_size = 3
+    assert _scan(lib, opts=ctypes.pointer(bad)) == ssm.SSM_ERR_INVALID_ARG
+    o = ssm.ScanOptions()
+    o.struct_size = ctypes.sizeof(ssm.ScanOptions)
+    o.algorithm = 2
+    o.chunk_len = 100                                                     # not a multiple of 64
+    assert _scan(lib, opts=ctypes.pointer(o)) == ssm.SSM_ERR_INVALID_ARG
+    o.chunk_len = 64
+    assert _scan(lib, seqlen=256, opts=ctypes.pointer(o)) == ssm.SSM_ERR_INVALID_ARG   # chunked needs a workspace
+    assert b"workspace" in lib.ssm_last_error_message()
+    o.discretization = 5
+    o.chunk_len = 0
+    o.algorithm = 1
+    assert _scan(lib, opts=ctypes.pointer(o)) == ssm.SSM_ERR_INVALID_ARG
+
+
+def test_workspace_query(lib):
+    o = ssm.ScanOptions()
+    o.struct_size = ctypes.sizeof(ssm.ScanOptions)
+    o.algorithm = 2
+    o.chunk_len = 64
+    n = lib.ssm_scan_fwd_workspace_size_ex(2, 8, 16, 64 * 5, ssm.SSM_BF16, ctypes.pointer(o))
+    per_chunk = 2 * 8 * 16 * 4
+    # aggregates P and Q for the first 4 chunks, carried-in states for all 5 chunks
+    assert n == per_chunk * (4 + 4 + 5)
+    o.algorithm = 1
+    assert lib.ssm_scan_fwd_workspace_size_ex(2, 8, 16, 64 * 5, ssm.SSM_BF16, ctypes.pointer(o)) == 0
+    assert lib.ssm_scan_fwd_workspace_size(2, 8, 17, 64, ssm.SSM_BF16) == 0
+
+
+def _upd(lib, **kw):
+    a = dict(x=P, dl=P + 0x1000000, A=P + 0x2000000, B=P + 0x3000000, C=P + 0x4000000, D=None, z=None,
+             state=P + 0x5000000, cs=P + 0x6000000, w=P + 0x7000000, bias=None, softplus=1, y=P + 0x8000000,
+             batch=2, dim=8, dstate=16, dconv=4, io=ssm.SSM_BF16, stream=None)
+    a.update(kw)
+    return lib.ssm_state_update(a["x"], a["dl"], a["A"], a["B"], a["C"], a["D"], a["z"], a["state"], a["cs"], a["w"],
+                                a["bias"], a["softplus"], a["y"], a["batch"], a["dim"], a["dstate"], a["dconv"],
+                                a["io"], a["stream"])
+
+
+def test_state_update_rejects_bad_arguments_on_host(lib):
+    assert _upd(lib, dconv=3) == ssm.SSM_ERR_UNSUPPORTED
+    assert _upd(lib, dstate=32) == ssm.SSM_ERR_UNSUPPORTED
+    assert _upd(lib, state=None) == ssm.SSM_ERR_INVALID_ARG
+    assert _upd(lib, cs=None) == ssm.SSM_ERR_INVALID_ARG
+    assert _upd(lib, x=P + 1) == ssm.SSM_ERR_INVALID_ARG
+    assert _upd(lib, y=P + 0x5000000) == ssm.SSM_ERR_INVALID_ARG          # y aliases state
+    assert _upd(lib, state=P + 0x2000000) == ssm.SSM_ERR_INVALID_ARG      # state aliases A
