@@ -21,10 +21,11 @@ struct ScanParams {
   void* y;
   float* last_state;      // may be null
   const float* h0;        // user initial state (batch, dim, N) or null
-  const float* h_in;      // initial state per chunk: h_in + chunk * h_in_chunk_stride, or null
+  const void* h_in;       // initial state per chunk: h_in + chunk * h_in_chunk_stride, or null
   int64_t h_in_chunk_stride;
-  float* agg_P;           // chunk aggregates (workspace), chunked algorithm only
-  float* agg_Q;
+  void* agg_P;            // chunk aggregates (workspace), chunked algorithm only
+  void* agg_Q;
+  int carry_f64;          // h_in / agg_P / agg_Q hold doubles (float32-io chunked), else floats
   int batch, dim, N;
   int64_t L;
   int64_t chunk_len;      // steps per chunk (== L for a single pass)

@@ -154,6 +154,47 @@ __device__ __forceinline__ float scan_step(const Chan& ch, float u, float draw, 
   return y;
 }
 
+// Float32-io step in double precision.  A float32 evaluation of the recurrence does not meet the
+// 2e-5 parity bound beyond a few hundred steps (rounding of Δ, exp(ΔA) and of the state compounds),
+// so the float32 io path keeps its coefficients, state and readout in double.
+struct ChanD {
+  double A[kNmax];
+  double D, bias;
+};
+
+template <int kDisc, int kMode>
+__device__ __forceinline__ double scan_step_precise(const ChanD& ch, double u, double draw, double z, uint32_t bc_row,
+                                                    double (&h)[kNmax], bool softplus, bool has_z,
+                                                    double& sum_delta) {
+  const double v = draw + ch.bias;
+  const double dl = softplus ? (v > 0.0 ? v + log1p(exp(-v)) : log1p(exp(v))) : v;
+  if (kMode == kModeAggregate) sum_delta += dl;
+  double y = 0.0;
+#pragma unroll
+  for (int q = 0; q < kNmax / 4; ++q) {
+    const float4 b4 = lds128f(bc_row + q * 16);
+    float4 c4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (kMode == kModeMain) c4 = lds128f(bc_row + 64 + q * 16);
+    const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+    const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int n = 4 * q + k;
+      const double x = dl * ch.A[n];
+      const double a = exp(x);
+      double bbar;
+      if (kDisc == 1 && ch.A[n] != 0.0) bbar = expm1(x) / ch.A[n] * bb[k];
+      else bbar = dl * bb[k];
+      h[n] = a * h[n] + bbar * u;
+      y += cc[k] * h[n];
+    }
+  }
+  if (kMode == kModeAggregate) return 0.0;
+  y += ch.D * u;
+  if (has_z) y *= z / (1.0 + exp(-z));
+  return y;
+}
+
 // Widen the B and C tiles of one stage into the float32 table [t][B0..15 | C0..15].
 // Rows n >= dstate are written as zeros, so the unused states stay at zero.
 template <typename IO>
@@ -276,40 +317,48 @@ __global__ void __launch_bounds__(kCH, 1)
     for (int k = 0; k < kStages - 1 && k < ntiles; ++k) issue(k);
   }
 
-  // per-channel constants
+  // per-channel constants (the float32-io path keeps them in double)
   Chan ch;
+  ChanD chd;
   ch.structured = true;
   {
     const float a0 = valid ? p.A[static_cast<int64_t>(d) * p.N] : 0.0f;
 #pragma unroll
     for (int n = 0; n < kNmax; ++n) {
       const float an = (valid && n < p.N) ? p.A[static_cast<int64_t>(d) * p.N + n] : 0.0f;
-      ch.AL2[n] = kFast ? an * kLog2e : an;
+      ch.AL2[n] = an * kLog2e;
       ch.invA[n] = an != 0.0f ? 1.0f / an : 0.0f;
+      chd.A[n] = an;
       if (n < p.N && an != static_cast<float>(n + 1) * a0) ch.structured = false;
     }
     ch.D = (valid && p.D) ? p.D[d] : 0.0f;
     ch.bias = (valid && p.bias) ? p.bias[d] : 0.0f;
+    chd.D = ch.D;
+    chd.bias = ch.bias;
   }
   // the decay shortcut is decided per warp
   const bool warp_structured = __all_sync(0xffffffffu, ch.structured) && kFast && kDisc == 0;
 
+  // state: 8 packed f32x2 pairs (bf16 io) or 16 doubles (float32 io)
   f2 h[kNmax / 2];
+  double hd[kNmax];
   {
-    const float* h0 = nullptr;
-    if (p.h_in) h0 = p.h_in + static_cast<int64_t>(chunk) * p.h_in_chunk_stride;
+    const int64_t base = (static_cast<int64_t>(b) * p.dim + d) * p.N;
+    const int64_t coff = static_cast<int64_t>(chunk) * p.h_in_chunk_stride;
 #pragma unroll
-    for (int i = 0; i < kNmax / 2; ++i) {
-      float lo = 0.0f, hi = 0.0f;
-      if (h0 && valid) {
-        const int64_t base = (static_cast<int64_t>(b) * p.dim + d) * p.N;
-        if (2 * i < p.N) lo = h0[base + 2 * i];
-        if (2 * i + 1 < p.N) hi = h0[base + 2 * i + 1];
+    for (int n = 0; n < kNmax; ++n) {
+      double v = 0.0;
+      if (p.h_in && valid && n < p.N) {
+        v = p.carry_f64 ? static_cast<const double*>(p.h_in)[coff + base + n]
+                        : static_cast<double>(static_cast<const float*>(p.h_in)[coff + base + n]);
       }
-      h[i] = f2_make(lo, hi);
+      hd[n] = v;
     }
+#pragma unroll
+    for (int i = 0; i < kNmax / 2; ++i) h[i] = f2_make(static_cast<float>(hd[2 * i]), static_cast<float>(hd[2 * i + 1]));
   }
   float sum_delta = 0.0f;
+  double sum_delta_d = 0.0;
   bool ok = true;
   int failed_at = -1;
 
@@ -345,8 +394,20 @@ __global__ void __launch_bounds__(kCH, 1)
     const uint32_t bcb = smem_u32(bc32[k & 1]);
     const int sw = tid & 7;
 
-    auto run = [&](auto structured_tag) {
+    auto one = [&](auto structured_tag, int c, int j, const float* uu, const float* dd, const float* zz) -> float {
       constexpr bool kS = decltype(structured_tag)::value;
+      const uint32_t row = bcb + (c * TL::kVec + j) * 128;
+      if constexpr (kFast) {
+        BC x;
+        load_bc(row, x);
+        return scan_step<true, kS, kDisc, kMode>(ch, uu[j], dd[j], zz[j], x, h, p.softplus, has_z, sum_delta);
+      } else {
+        return static_cast<float>(scan_step_precise<kDisc, kMode>(chd, uu[j], dd[j], zz[j], row, hd, p.softplus,
+                                                                   has_z, sum_delta_d));
+      }
+    };
+
+    auto run = [&](auto structured_tag) {
 #pragma unroll 1
       for (int c = 0; c < TL::kChunks; ++c) {
         if (c * TL::kVec >= steps) break;
@@ -361,12 +422,7 @@ __global__ void __launch_bounds__(kCH, 1)
         const int nvalid = steps - c * TL::kVec;
         if (nvalid >= TL::kVec) {
 #pragma unroll
-          for (int j = 0; j < TL::kVec; ++j) {
-            BC x;
-            load_bc(bcb + (c * TL::kVec + j) * 128, x);
-            yy[j] = scan_step<kFast, kS, kDisc, kMode>(ch, uu[j], dd[j], zz[j], x, h, p.softplus, has_z,
-                                                        sum_delta);
-          }
+          for (int j = 0; j < TL::kVec; ++j) yy[j] = one(structured_tag, c, j, uu, dd, zz);
           if (kMode == kModeMain && valid) {
             const int64_t t = t0 + c * TL::kVec;
             if (vec_store) {
@@ -380,10 +436,7 @@ __global__ void __launch_bounds__(kCH, 1)
 #pragma unroll
           for (int j = 0; j < TL::kVec; ++j) {
             if (j < nvalid) {
-              BC x;
-              load_bc(bcb + (c * TL::kVec + j) * 128, x);
-              yy[j] = scan_step<kFast, kS, kDisc, kMode>(ch, uu[j], dd[j], zz[j], x, h, p.softplus, has_z,
-                                                          sum_delta);
+              yy[j] = one(structured_tag, c, j, uu, dd, zz);
               if (kMode == kModeMain && valid) yrow[t0 + c * TL::kVec + j] = IoTraits<IO>::from_f32(yy[j]);
             }
           }
@@ -404,12 +457,20 @@ __global__ void __launch_bounds__(kCH, 1)
     return;
   }
   if (!valid) return;
+  if constexpr (kFast) {
+#pragma unroll
+    for (int i = 0; i < kNmax / 2; ++i) {
+      hd[2 * i] = f2_lo(h[i]);
+      hd[2 * i + 1] = f2_hi(h[i]);
+    }
+    sum_delta_d = sum_delta;
+  }
   const int64_t sbase = (static_cast<int64_t>(b) * p.dim + d) * p.N;
   if (kMode == kModeMain) {
     if (p.last_state && chunk == static_cast<int>(gridDim.z) - 1) {
 #pragma unroll
       for (int n = 0; n < kNmax; ++n)
-        if (n < p.N) p.last_state[sbase + n] = n & 1 ? f2_hi(h[n >> 1]) : f2_lo(h[n >> 1]);
+        if (n < p.N) p.last_state[sbase + n] = static_cast<float>(hd[n]);
     }
   } else {
     // aggregate of this chunk: P = Π exp(Δ A) = exp(A ΣΔ) (one accurate exp per state), Q = h_end
@@ -418,22 +479,28 @@ __global__ void __launch_bounds__(kCH, 1)
     for (int n = 0; n < kNmax; ++n) {
       if (n < p.N) {
         const float an = p.A[static_cast<int64_t>(d) * p.N + n];
-        p.agg_P[cbase + n] = expf(an * sum_delta);
-        p.agg_Q[cbase + n] = n & 1 ? f2_hi(h[n >> 1]) : f2_lo(h[n >> 1]);
+        if (p.carry_f64) {
+          static_cast<double*>(p.agg_P)[cbase + n] = exp(static_cast<double>(an) * sum_delta_d);
+          static_cast<double*>(p.agg_Q)[cbase + n] = hd[n];
+        } else {
+          static_cast<float*>(p.agg_P)[cbase + n] = expf(an * sum_delta);
+          static_cast<float*>(p.agg_Q)[cbase + n] = static_cast<float>(hd[n]);
+        }
       }
     }
   }
 }
 
 // Carry pass: h_in[0] = h0 (or 0); h_in[k+1] = P[k] ⊙ h_in[k] + Q[k].  One thread per (b, d, n).
-__global__ void carry_kernel(const float* __restrict__ P, const float* __restrict__ Q, const float* __restrict__ h0,
-                             float* __restrict__ h_in, int64_t per_chunk, int nchunks) {
+template <typename T>
+__global__ void carry_kernel(const T* __restrict__ P, const T* __restrict__ Q, const float* __restrict__ h0,
+                             T* __restrict__ h_in, int64_t per_chunk, int nchunks) {
   const int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
   if (i >= per_chunk) return;
-  float h = h0 ? h0[i] : 0.0f;
+  T h = h0 ? static_cast<T>(h0[i]) : T(0);
   h_in[i] = h;
   for (int k = 0; k + 1 < nchunks; ++k) {
-    h = fmaf(P[k * per_chunk + i], h, Q[k * per_chunk + i]);
+    h = P[k * per_chunk + i] * h + Q[k * per_chunk + i];
     h_in[(k + 1) * per_chunk + i] = h;
   }
 }
@@ -512,8 +579,17 @@ cudaError_t scan_fwd_launch(const ScanParams& p_in, int nchunks, cudaStream_t st
     if (e != cudaSuccess) return e;
     // 2. carry
     const int64_t per_chunk = static_cast<int64_t>(p.batch) * p.dim * p.N;
-    carry_kernel<<<static_cast<unsigned>((per_chunk + 255) / 256), 256, 0, stream>>>(
-        p.agg_P, p.agg_Q, p.h0, const_cast<float*>(p.h_in), per_chunk, nchunks);
+    const unsigned blocks = static_cast<unsigned>((per_chunk + 255) / 256);
+    if (p.carry_f64)
+      carry_kernel<double><<<blocks, 256, 0, stream>>>(static_cast<const double*>(p.agg_P),
+                                                        static_cast<const double*>(p.agg_Q), p.h0,
+                                                        static_cast<double*>(const_cast<void*>(p.h_in)),
+                                                        per_chunk, nchunks);
+    else
+      carry_kernel<float><<<blocks, 256, 0, stream>>>(static_cast<const float*>(p.agg_P),
+                                                       static_cast<const float*>(p.agg_Q), p.h0,
+                                                       static_cast<float*>(const_cast<void*>(p.h_in)),
+                                                       per_chunk, nchunks);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

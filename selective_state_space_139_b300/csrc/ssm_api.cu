@@ -108,7 +108,8 @@ bool make_plan(int batch, int dim, int dstate, int64_t seqlen, ssm_dtype io, con
   }
   pl->chunk_len = chunk;
   pl->nchunks = static_cast<int>((seqlen + chunk - 1) / chunk);
-  const size_t per_chunk = static_cast<size_t>(batch) * dim * dstate * sizeof(float);
+  // float32 io keeps its chunk carries in double (see the float32-io note in scan_fwd.cu)
+  const size_t per_chunk = static_cast<size_t>(batch) * dim * dstate * (io == SSM_F32 ? sizeof(double) : sizeof(float));
   pl->off_P = 0;
   pl->off_Q = round_up(per_chunk * (pl->nchunks - 1), 256);
   pl->off_hin = pl->off_Q + round_up(per_chunk * (pl->nchunks - 1), 256);
@@ -273,9 +274,10 @@ ssm_status ssm_scan_fwd_ex(const void* u, const void* delta, const float* A, con
   p.vec_ok = aligned(y, 16) && (seqlen * e) % 16 == 0;
   if (pl.nchunks > 1) {
     char* ws = static_cast<char*>(workspace);
-    p.agg_P = reinterpret_cast<float*>(ws + pl.off_P);
-    p.agg_Q = reinterpret_cast<float*>(ws + pl.off_Q);
-    p.h_in = reinterpret_cast<float*>(ws + pl.off_hin);
+    p.agg_P = ws + pl.off_P;
+    p.agg_Q = ws + pl.off_Q;
+    p.h_in = ws + pl.off_hin;
+    p.carry_f64 = io_dtype == SSM_F32;
     p.h_in_chunk_stride = static_cast<int64_t>(batch) * dim * dstate;
     p.chunk_len = pl.chunk_len;
   } else {

@@ -92,14 +92,32 @@ __global__ void __launch_bounds__(kThreads) state_update_kernel(const DecodePara
   }
 
   float py = 0.0f;
+  double pyd = 0.0, ud = 0.0;
+  if constexpr (kFast) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float a = kFast ? ex2_approx(dl * av[i] * kLog2e) : expf(dl * av[i]);
-    hv[i] = fmaf(a, hv[i], wu * bv[i]);
-    py = fmaf(cv[i], hv[i], py);
+    for (int i = 0; i < 4; ++i) {
+      const float a = ex2_approx(dl * av[i] * kLog2e);
+      hv[i] = fmaf(a, hv[i], wu * bv[i]);
+      py = fmaf(cv[i], hv[i], py);
+    }
+    py += __shfl_xor_sync(0xffffffffu, py, 1);
+    py += __shfl_xor_sync(0xffffffffu, py, 2);
+  } else {
+    // float32 io: conv, Δ, decays and readout in double; the state is stored back as float32
+    const double sd = static_cast<double>(w.w) * x + static_cast<double>(w.z) * cs2 +
+                      static_cast<double>(w.y) * cs1 + static_cast<double>(w.x) * cs0;
+    ud = sd / (1.0 + exp(-sd));
+    const double vd = static_cast<double>(ld_io<IO>(p.delta, c)) + (p.bias ? p.bias[d] : 0.0f);
+    const double dld = p.softplus ? (vd > 0.0 ? vd + log1p(exp(-vd)) : log1p(exp(vd))) : vd;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const double hn = exp(dld * av[i]) * hv[i] + dld * bv[i] * ud;
+      hv[i] = static_cast<float>(hn);
+      pyd += cv[i] * hn;
+    }
+    pyd += __shfl_xor_sync(0xffffffffu, pyd, 1);
+    pyd += __shfl_xor_sync(0xffffffffu, pyd, 2);
   }
-  py += __shfl_xor_sync(0xffffffffu, py, 1);
-  py += __shfl_xor_sync(0xffffffffu, py, 2);
 
   // every lane has read the old conv window before any lane overwrites it
   __syncwarp();
@@ -113,12 +131,18 @@ __global__ void __launch_bounds__(kThreads) state_update_kernel(const DecodePara
   }
   if (j < 3) cs[j] = j == 0 ? cs1 : (j == 1 ? cs2 : x);
   if (j == 0) {
-    float y = fmaf(p.D ? p.D[d] : 0.0f, u, py);
-    if (p.z) {
-      const float z = ld_io<IO>(p.z, c);
-      y *= kFast ? silu_fast(z) : silu_accurate(z);
+    if constexpr (kFast) {
+      float y = fmaf(p.D ? p.D[d] : 0.0f, u, py);
+      if (p.z) y *= silu_fast(ld_io<IO>(p.z, c));
+      static_cast<IO*>(p.y)[c] = IoTraits<IO>::from_f32(y);
+    } else {
+      double y = pyd + (p.D ? static_cast<double>(p.D[d]) : 0.0) * ud;
+      if (p.z) {
+        const double z = ld_io<IO>(p.z, c);
+        y *= z / (1.0 + exp(-z));
+      }
+      static_cast<IO*>(p.y)[c] = IoTraits<IO>::from_f32(static_cast<float>(y));
     }
-    static_cast<IO*>(p.y)[c] = IoTraits<IO>::from_f32(y);
   }
 }
 

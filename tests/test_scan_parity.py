@@ -114,8 +114,9 @@ def test_optional_operands_and_softplus_off(dtype):
     bare = dict(inp, z=None, D=None, delta_bias=None)
     y, hL = _run(bare)
     _check_full(bare, y, hL, TOL[dtype])
-    # softplus off: Δ = Δ_raw + bias must be positive for a sane recurrence; use |Δ_raw| * 0.1
-    pos = dict(inp, delta=(inp["delta"].float().abs() * 0.1).to(inp["delta"].dtype))
+    # softplus off: Δ = Δ_raw must then be non-negative for a decaying recurrence: use 0.1|Δ_raw|
+    # and no bias (the generated biases are negative, softplus^-1 of values below 0.1)
+    pos = dict(inp, delta=(inp["delta"].float().abs() * 0.1).to(inp["delta"].dtype), delta_bias=None)
     y, hL = _run(pos, delta_softplus=False)
     _check_full(pos, y, hL, TOL[dtype], softplus=False)
 
