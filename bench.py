@@ -179,9 +179,10 @@ def measure_scan(w, steps, warmup, dev, rank, peak, peak_kind):
     inp = W.make_scan_inputs(w, device=dev, seed=w.seed + rank)
     y = torch.empty_like(inp["u"])
     hL = torch.empty((w.batch, w.dim, w.dstate), device=dev, dtype=torch.float32)
-    ws_bytes = ssm.scan_workspace_size(w.batch, w.dim, w.dstate, w.seqlen, inp["u"].dtype)
+    plan = ssm.describe_scan(w.batch, w.dim, w.dstate, w.seqlen, inp["u"].dtype)
+    ws_bytes = plan["workspace_bytes"]
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
-    launches_per_step = 3 if ws_bytes else 1
+    launches_per_step = plan["kernel_launches"]
     stream = torch.cuda.current_stream(dev)
 
     def step():
@@ -250,7 +251,8 @@ def measure_scan(w, steps, warmup, dev, rank, peak, peak_kind):
     return {
         "ms_per_step": ms_step, "tokens_per_step": w.tokens, "kernel_ms": kern_ms, "bytes_alg": bytes_alg,
         "achieved_gbs": achieved, "clocks": clocks, "launches_per_step": launches_per_step,
-        "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h, "algorithm": "chunked" if ws_bytes else "single_pass",
+        "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h, "algorithm": f"{plan['path']}/{plan['schedule']}",
+        "ctas": plan["ctas"],
     }
 
 
@@ -394,7 +396,7 @@ def main():
         "ms_per_step": r["ms_per_step"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32 (bf16 io)", "data": "synthetic",
         "config": {"workload": w.name, "batch": w.batch, "d_inner": w.dim, "d_state": w.dstate, "seq_len": w.seqlen,
-                   "io": w.io_dtype, "algorithm": r["algorithm"],
+                   "io": w.io_dtype, "kernel": r["algorithm"], "ctas": r["ctas"],
                    "l2": "inputs larger than L2 (%.0f MB per step vs 126 MB)" % (r["bytes_alg"] / 1e6),
                    "parallelism": f"replicas x{ws}"},
         "roofline": {"bound": "hbm", "achieved": r["achieved_gbs"], "peak": peak, "unit": "GB/s",

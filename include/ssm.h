@@ -137,6 +137,24 @@ SSM_API ssm_status ssm_state_update(const void* x_t, const void* delta_t, const 
                             int softplus_flag, void* y_t, int batch, int dim, int dstate, int dconv,
                             ssm_dtype io_dtype, cudaStream_t stream);
 
+/* How a prefill call with these sizes and options would run (filled by ssm_scan_fwd_describe). */
+typedef struct {
+  int struct_size;           /* set to sizeof(ssm_scan_plan) before the call */
+  int path;                  /* 0: general kernel (float32 io, exact ZOH, or layouts TMA cannot use); 1: bf16 fast path */
+  int schedule;              /* 0: one CTA per channel tile; 1: balanced persistent ranges; 2: chunked (aggregates, carry, re-run) */
+  int nchunks;               /* time chunks (1 unless schedule 2) */
+  int64_t chunk_len;         /* steps per chunk */
+  int ctas;                  /* CTAs of the main pass */
+  int kernel_launches;       /* kernels one call launches (memsets not counted) */
+  size_t workspace_bytes;    /* same as ssm_scan_fwd_workspace_size_ex */
+} ssm_scan_plan;
+
+/* Describes the plan ssm_scan_fwd_ex would use for these sizes and options, assuming 16-byte
+ * aligned buffers (a call with less aligned buffers runs the general kernel in one pass).
+ * Returns SSM_ERR_INVALID_ARG / SSM_ERR_UNSUPPORTED like the scan itself; enqueues nothing. */
+SSM_API ssm_status ssm_scan_fwd_describe(int batch, int dim, int dstate, int64_t seqlen, ssm_dtype io_dtype,
+                                         const ssm_scan_options* opts, ssm_scan_plan* plan);
+
 /*
  * Reads and clears the device status word (synchronises `stream`).  Returns SSM_OK, SSM_ERR_TIMEOUT
  * if a kernel gave up a bounded wait since the last call, or SSM_ERR_CUDA.

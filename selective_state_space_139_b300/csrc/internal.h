@@ -34,6 +34,11 @@ struct ScanParams {
   int io_bf16;            // 1: bfloat16 io, 0: float32 io
   int tma_ok;             // the layout allows 2D TMA tensor maps
   int vec_ok;             // y rows allow 16-byte stores
+  // bf16 fast path, balanced persistent schedule
+  int sched_balanced;     // 1: one range of (group, tile) work per resident CTA
+  int64_t range_tiles;    // tiles per CTA range
+  float* carry;           // (ctas, 64, 16) states handed from one CTA to the next
+  unsigned* flags;        // (ctas) publication flags
 };
 
 // Steps per time tile for an io element size (64 for bf16, 32 for float32).
@@ -70,5 +75,16 @@ cudaError_t state_update_launch(const DecodeParams& p, cudaStream_t stream);
 
 // Device status word access (scan_fwd.cu owns the symbol).
 cudaError_t read_and_clear_device_status(unsigned int* out, cudaStream_t stream);
+
+// Carry pass of the chunked algorithm over float carries (scan_fwd.cu).
+cudaError_t carry_launch_f32(const ScanParams& p, int nchunks, cudaStream_t stream);
+
+// bf16 fast path (scan_fast.cu).
+int fast_channels_per_cta();
+int fast_resident_ctas();   // co-resident CTAs on the current device (0 if unknown)
+cudaError_t fast_status_read_and_clear(unsigned int* out);
+// balanced_ctas > 0: balanced persistent schedule; else one CTA per (group, chunk)
+cudaError_t scan_fast_launch(const ScanParams& p, int nchunks, int balanced_ctas, cudaStream_t stream, char* err,
+                             size_t errlen);
 
 }  // namespace ssm

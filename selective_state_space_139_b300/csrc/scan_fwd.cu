@@ -538,7 +538,22 @@ cudaError_t read_and_clear_device_status(unsigned int* out, cudaStream_t stream)
   e = cudaMemcpyFromSymbol(out, g_device_status, sizeof(unsigned int));
   if (e != cudaSuccess) return e;
   const unsigned int zero = 0;
-  return cudaMemcpyToSymbol(g_device_status, &zero, sizeof(unsigned int));
+  e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  unsigned int fast = 0;
+  e = fast_status_read_and_clear(&fast);
+  *out |= fast;
+  return e;
+}
+
+cudaError_t carry_launch_f32(const ScanParams& p, int nchunks, cudaStream_t stream) {
+  const int64_t per_chunk = static_cast<int64_t>(p.batch) * p.dim * p.N;
+  const unsigned blocks = static_cast<unsigned>((per_chunk + 255) / 256);
+  carry_kernel<float><<<blocks, 256, 0, stream>>>(static_cast<const float*>(p.agg_P),
+                                                   static_cast<const float*>(p.agg_Q), p.h0,
+                                                   static_cast<float*>(const_cast<void*>(p.h_in)), per_chunk,
+                                                   nchunks);
+  return cudaGetLastError();
 }
 
 // Builds the tensor maps (when the layout allows TMA) and launches the passes.

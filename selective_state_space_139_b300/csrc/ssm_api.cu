@@ -63,39 +63,105 @@ int sm_count() {
 }
 
 struct Plan {
+  int path = 0;           // 0: general kernel (float32 io, ZOH, layouts TMA cannot describe); 1: bf16 fast path
   int nchunks = 1;
   int64_t chunk_len = 0;
+  int balanced_ctas = 0;  // fast path: > 0 selects the balanced persistent schedule
+  int64_t range_tiles = 0;
   size_t workspace = 0;
   size_t off_P = 0, off_Q = 0, off_hin = 0;
+  size_t off_carry = 0, off_flags = 0;
 };
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Decides single pass vs chunked and lays out the workspace.  Returns false on bad options.
+// The bf16 fast path needs: bf16 io, the Δ·B input term, rows TMA can describe (L a multiple of 8,
+// at least one 64-step tile, at least 64 rows).  Pointer alignment is checked at call time.
+bool fast_eligible(int batch, int dim, int64_t seqlen, ssm_dtype io, int disc) {
+  return io == SSM_BF16 && disc == SSM_DISC_DELTA_B && seqlen % 8 == 0 && seqlen >= 64 &&
+         static_cast<int64_t>(batch) * dim >= 64;
+}
+
+void layout_chunked(Plan* pl, int batch, int dim, int dstate, size_t carry_bytes) {
+  const size_t per_chunk = static_cast<size_t>(batch) * dim * dstate * carry_bytes;
+  pl->off_P = 0;
+  pl->off_Q = round_up(per_chunk * (pl->nchunks - 1), 256);
+  pl->off_hin = pl->off_Q + round_up(per_chunk * (pl->nchunks - 1), 256);
+  pl->workspace = pl->off_hin + round_up(per_chunk * pl->nchunks, 256);
+}
+
+// Decides the kernel path and schedule and lays out the workspace.  Returns false on bad options.
 bool make_plan(int batch, int dim, int dstate, int64_t seqlen, ssm_dtype io, const ssm_scan_options* o, Plan* pl) {
-  const int T = ssm::scan_tile_steps(io == SSM_BF16 ? 2 : 4);
   const int algo = o ? o->algorithm : SSM_ALGO_AUTO;
+  const int disc = o ? o->discretization : SSM_DISC_DELTA_B;
+  if (algo != SSM_ALGO_AUTO && algo != SSM_ALGO_SINGLE_PASS && algo != SSM_ALGO_CHUNKED) return false;
+  int64_t user_chunk = 0;
+  if (algo == SSM_ALGO_CHUNKED) {
+    user_chunk = o->chunk_len;
+    if (user_chunk < 0 || user_chunk % 64 != 0) return false;
+  }
+  const int sms = sm_count();
+  *pl = Plan();
+  if (fast_eligible(batch, dim, seqlen, io, disc)) {
+    pl->path = 1;
+    const int64_t cpc = ssm::fast_channels_per_cta();
+    const int64_t G = static_cast<int64_t>(batch) * ((dim + cpc - 1) / cpc);
+    const int64_t Lt = (seqlen + 63) / 64;
+    const int64_t S = ssm::fast_resident_ctas();     // 0 when unknown (no device)
+    int64_t chunk = 0;
+    if (algo == SSM_ALGO_CHUNKED) {
+      chunk = user_chunk;
+      if (chunk == 0) {
+        const int64_t target = std::max<int64_t>(2, (2 * std::max<int64_t>(S, sms) + G - 1) / G);
+        chunk = round_up(static_cast<size_t>((seqlen + target - 1) / target), 64);
+      }
+    } else if (S > 0 && G >= S) {
+      // enough groups for every resident CTA: balanced persistent schedule
+      pl->balanced_ctas = static_cast<int>(S);
+      pl->range_tiles = (G * Lt + S - 1) / S;
+      pl->nchunks = 1;
+      pl->chunk_len = seqlen;
+      pl->off_carry = 0;
+      pl->off_flags = round_up(static_cast<size_t>(S) * cpc * 16 * sizeof(float), 256);
+      pl->workspace = pl->off_flags + round_up(static_cast<size_t>(S) * sizeof(unsigned), 256);
+      return true;
+    } else if (algo == SSM_ALGO_AUTO && Lt >= 8) {
+      // too few groups: split time into chunks (aggregates, carry, re-run)
+      const int64_t slots = std::max<int64_t>(S, sms);
+      const int64_t target = (2 * slots + G - 1) / G;
+      chunk = std::max<int64_t>(round_up(static_cast<size_t>((seqlen + target - 1) / target), 64), 4 * 64);
+    }
+    if (chunk > 0 && (seqlen + chunk - 1) / chunk > 65535)
+      chunk = round_up(static_cast<size_t>((seqlen + 65534) / 65535), 64);
+    if (chunk <= 0 || chunk >= seqlen) {
+      pl->nchunks = 1;
+      pl->chunk_len = static_cast<int64_t>(round_up(static_cast<size_t>(seqlen), 64));
+      pl->workspace = 0;
+      return true;
+    }
+    pl->chunk_len = chunk;
+    pl->nchunks = static_cast<int>((seqlen + chunk - 1) / chunk);
+    layout_chunked(pl, batch, dim, dstate, sizeof(float));
+    return true;
+  }
+  // general kernel
+  pl->path = 0;
+  const int T = ssm::scan_tile_steps(io == SSM_BF16 ? 2 : 4);
   const int64_t groups = static_cast<int64_t>(batch) * ((dim + kChannelsPerCta - 1) / kChannelsPerCta);
   int64_t chunk = 0;
-  if (algo == SSM_ALGO_SINGLE_PASS) {
-    chunk = 0;
-  } else if (algo == SSM_ALGO_CHUNKED) {
-    chunk = o->chunk_len;
-    if (chunk < 0 || chunk % 64 != 0) return false;
+  if (algo == SSM_ALGO_CHUNKED) {
+    chunk = user_chunk;
     if (chunk == 0) {
-      const int64_t target = std::max<int64_t>(2, (4 * sm_count() + groups - 1) / groups);
+      const int64_t target = std::max<int64_t>(2, (4 * sms + groups - 1) / groups);
       chunk = round_up(static_cast<size_t>((seqlen + target - 1) / target), 64);
     }
   } else if (algo == SSM_ALGO_AUTO) {
-    const int sms = sm_count();
     if (groups < sms && seqlen >= 2 * kMinChunkTiles * T) {
       const int64_t target = (4 * sms + groups - 1) / groups;
       int64_t c = round_up(static_cast<size_t>((seqlen + target - 1) / target), 64);
       c = std::max<int64_t>(c, kMinChunkTiles * 64);
       if (c < seqlen) chunk = c;
     }
-  } else {
-    return false;
   }
   // grid.z holds the chunk index: keep the chunk count within 65535
   if (chunk > 0 && (seqlen + chunk - 1) / chunk > 65535)
@@ -109,11 +175,7 @@ bool make_plan(int batch, int dim, int dstate, int64_t seqlen, ssm_dtype io, con
   pl->chunk_len = chunk;
   pl->nchunks = static_cast<int>((seqlen + chunk - 1) / chunk);
   // float32 io keeps its chunk carries in double (see the float32-io note in scan_fwd.cu)
-  const size_t per_chunk = static_cast<size_t>(batch) * dim * dstate * (io == SSM_F32 ? sizeof(double) : sizeof(float));
-  pl->off_P = 0;
-  pl->off_Q = round_up(per_chunk * (pl->nchunks - 1), 256);
-  pl->off_hin = pl->off_Q + round_up(per_chunk * (pl->nchunks - 1), 256);
-  pl->workspace = pl->off_hin + round_up(per_chunk * pl->nchunks, 256);
+  layout_chunked(pl, batch, dim, dstate, io == SSM_F32 ? sizeof(double) : sizeof(float));
   return true;
 }
 
@@ -191,6 +253,41 @@ size_t ssm_scan_fwd_workspace_size_ex(int batch, int dim, int dstate, int64_t se
   return pl.workspace;
 }
 
+ssm_status ssm_scan_fwd_describe(int batch, int dim, int dstate, int64_t seqlen, ssm_dtype io_dtype,
+                                 const ssm_scan_options* opts, ssm_scan_plan* plan) {
+  g_err[0] = 0;
+  if (!plan || plan->struct_size != static_cast<int>(sizeof(ssm_scan_plan)))
+    return fail(SSM_ERR_INVALID_ARG, "ssm_scan_plan.struct_size mismatch");
+  if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return fail(SSM_ERR_INVALID_ARG, "unknown io_dtype %d", io_dtype);
+  if (batch < 1 || dim < 1 || seqlen < 0 || dstate < 1) return fail(SSM_ERR_INVALID_ARG, "bad sizes");
+  if (dstate > 16) return fail(SSM_ERR_UNSUPPORTED, "dstate=%d > 16 is not supported", dstate);
+  if (opts && opts->struct_size != static_cast<int>(sizeof(ssm_scan_options)))
+    return fail(SSM_ERR_INVALID_ARG, "ssm_scan_options.struct_size mismatch");
+  Plan pl;
+  if (!make_plan(batch, dim, dstate, seqlen, io_dtype, opts, &pl))
+    return fail(SSM_ERR_INVALID_ARG, "bad algorithm or chunk_len (a multiple of 64 is required)");
+  plan->path = pl.path;
+  plan->nchunks = pl.nchunks;
+  plan->chunk_len = pl.chunk_len;
+  plan->workspace_bytes = pl.workspace;
+  const int64_t cpc = pl.path == 1 ? ssm::fast_channels_per_cta() : kChannelsPerCta;
+  const int64_t groups = static_cast<int64_t>(batch) * ((dim + cpc - 1) / cpc);
+  if (pl.balanced_ctas > 0) {
+    plan->schedule = 1;
+    plan->ctas = pl.balanced_ctas;
+    plan->kernel_launches = 1;
+  } else if (pl.nchunks > 1) {
+    plan->schedule = 2;
+    plan->ctas = static_cast<int>(groups * pl.nchunks);
+    plan->kernel_launches = 3;
+  } else {
+    plan->schedule = 0;
+    plan->ctas = static_cast<int>(groups);
+    plan->kernel_launches = seqlen > 0 ? 1 : 0;
+  }
+  return SSM_OK;
+}
+
 size_t ssm_scan_fwd_workspace_size(int batch, int dim, int dstate, int64_t seqlen, ssm_dtype io_dtype) {
   return ssm_scan_fwd_workspace_size_ex(batch, dim, dstate, seqlen, io_dtype, nullptr);
 }
@@ -266,28 +363,54 @@ ssm_status ssm_scan_fwd_ex(const void* u, const void* delta, const float* A, con
   p.y = y; p.last_state = last_state; p.h0 = h0;
   p.batch = batch; p.dim = dim; p.N = dstate; p.L = seqlen;
   p.softplus = softplus_flag != 0; p.disc = disc; p.io_bf16 = io_dtype == SSM_BF16;
+  bool aligned16 = true;
+  for (const void* q : {u, delta, z, B, C, static_cast<const void*>(y)})
+    if (q && !aligned(q, 16)) aligned16 = false;
+  char err[256] = {0};
+  char* ws = static_cast<char*>(workspace);
+  if (pl.path == 1 && aligned16) {
+    if (pl.balanced_ctas > 0) {
+      p.sched_balanced = 1;
+      p.range_tiles = pl.range_tiles;
+      p.carry = reinterpret_cast<float*>(ws + pl.off_carry);
+      p.flags = reinterpret_cast<unsigned*>(ws + pl.off_flags);
+      p.chunk_len = seqlen;
+    } else if (pl.nchunks > 1) {
+      p.agg_P = ws + pl.off_P;
+      p.agg_Q = ws + pl.off_Q;
+      p.h_in = ws + pl.off_hin;
+      p.h_in_chunk_stride = static_cast<int64_t>(batch) * dim * dstate;
+      p.chunk_len = pl.chunk_len;
+    } else {
+      p.chunk_len = pl.chunk_len;
+    }
+    cudaError_t ce = ssm::scan_fast_launch(p, pl.nchunks, pl.balanced_ctas, stream, err, sizeof(err));
+    if (ce != cudaSuccess) return cuda_fail(ce, err[0] ? err : "scan launch");
+    return SSM_OK;
+  }
+  // general kernel (also the fallback for buffers whose alignment TMA cannot use)
   const int T = ssm::scan_tile_steps(static_cast<int>(e));
   bool tma = ((seqlen * e) % 16 == 0) && seqlen >= T && static_cast<int64_t>(batch) * dim >= kChannelsPerCta;
   for (const void* q : {u, delta, z, B, C})
     if (q && !aligned(q, 16)) tma = false;
   p.tma_ok = tma;
   p.vec_ok = aligned(y, 16) && (seqlen * e) % 16 == 0;
-  if (pl.nchunks > 1) {
-    char* ws = static_cast<char*>(workspace);
+  int nchunks = pl.nchunks;
+  if (pl.path == 0 && nchunks > 1) {
     p.agg_P = ws + pl.off_P;
     p.agg_Q = ws + pl.off_Q;
     p.h_in = ws + pl.off_hin;
-    p.carry_f64 = io_dtype == SSM_F32;
     p.h_in_chunk_stride = static_cast<int64_t>(batch) * dim * dstate;
     p.chunk_len = pl.chunk_len;
+    p.carry_f64 = io_dtype == SSM_F32;
   } else {
+    nchunks = 1;   // the fast plan's workspace layout does not apply here: run one pass
     p.h_in = h0;
     p.h_in_chunk_stride = 0;
     p.chunk_len = seqlen;
   }
-  char err[256] = {0};
-  cudaError_t ce = ssm::scan_fwd_launch(p, pl.nchunks, stream, err, sizeof(err));
-  if (ce != cudaSuccess) return cuda_fail(ce, "scan launch");
+  cudaError_t ce = ssm::scan_fwd_launch(p, nchunks, stream, err, sizeof(err));
+  if (ce != cudaSuccess) return cuda_fail(ce, err[0] ? err : "scan launch");
   return SSM_OK;
 }
 

@@ -33,6 +33,12 @@ class ScanOptions(ctypes.Structure):
                 ("discretization", ctypes.c_int), ("h0", ctypes.c_void_p)]
 
 
+class ScanPlan(ctypes.Structure):
+    _fields_ = [("struct_size", ctypes.c_int), ("path", ctypes.c_int), ("schedule", ctypes.c_int),
+                ("nchunks", ctypes.c_int), ("chunk_len", ctypes.c_int64), ("ctas", ctypes.c_int),
+                ("kernel_launches", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t)]
+
+
 def library_path() -> str:
     return _build.LIB
 
@@ -65,6 +71,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ssm_scan_fwd_ex.argtypes = scan + [ctypes.POINTER(ScanOptions), vp]
     lib.ssm_state_update.restype = i32
     lib.ssm_state_update.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, vp]
+    lib.ssm_scan_fwd_describe.restype = i32
+    lib.ssm_scan_fwd_describe.argtypes = [i32, i32, i32, i64, i32, ctypes.POINTER(ScanOptions), ctypes.POINTER(ScanPlan)]
     lib.ssm_device_status.restype = i32
     lib.ssm_device_status.argtypes = [vp]
     if path == _build.LIB:
@@ -131,6 +139,19 @@ def scan_workspace_size(batch: int, dim: int, dstate: int, seqlen: int, dtype=to
     lib = load_library()
     o = _options(algorithm, chunk_len, discretization, None)
     return int(lib.ssm_scan_fwd_workspace_size_ex(batch, dim, dstate, seqlen, _io_code(dtype), ctypes.byref(o)))
+
+
+def describe_scan(batch: int, dim: int, dstate: int, seqlen: int, dtype=torch.bfloat16, algorithm: str = "auto",
+                  chunk_len: int = 0, discretization: str = "delta_b") -> dict:
+    """The plan a prefill call with these sizes would run (kernel path, schedule, launches, workspace)."""
+    lib = load_library()
+    o = _options(algorithm, chunk_len, discretization, None)
+    pl = ScanPlan()
+    pl.struct_size = ctypes.sizeof(ScanPlan)
+    _check(lib, lib.ssm_scan_fwd_describe(batch, dim, dstate, seqlen, _io_code(dtype), ctypes.byref(o), ctypes.byref(pl)))
+    return {"path": ("general", "fast")[pl.path], "schedule": ("grid", "balanced", "chunked")[pl.schedule],
+            "nchunks": pl.nchunks, "chunk_len": pl.chunk_len, "ctas": pl.ctas, "kernel_launches": pl.kernel_launches,
+            "workspace_bytes": pl.workspace_bytes}
 
 
 def selective_scan_fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor, C: torch.Tensor,
