@@ -333,7 +333,7 @@ def run_reference(args, ws, rank):
     values = []
     sample = ""
     cores = os.cpu_count() or 1
-    budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
+    budget = max(0.5, args.ref_budget / max(1, args.steps + args.warmup))
     for i in range(args.warmup + args.steps):
         v, cores, sample, secs = cpu_oracle_sample(w, target_s=budget)
         if i >= args.warmup:
@@ -361,6 +361,8 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=150.0,
+                    help="seconds of oracle work for the whole --impl reference run")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
