@@ -137,6 +137,34 @@ SSM_API ssm_status ssm_state_update(const void* x_t, const void* delta_t, const 
                             int softplus_flag, void* y_t, int batch, int dim, int dstate, int dconv,
                             ssm_dtype io_dtype, cudaStream_t stream);
 
+/*
+ * Prefill scan for callers that cannot allocate device memory.  The paper has no counterpart: this
+ * is a library convenience.  Some callers cannot call cudaMalloc or hand over a workspace -- code
+ * running where allocation is forbidden or unavailable (a host callback, a plugin hook that must not
+ * allocate, a process whose device allocator belongs to another framework, a memory-capped sandbox)
+ * or code that cannot afford an allocation on its latency path.  This call allocates nothing:
+ * its scratch is a fixed array of ssm_scan_fwd_noalloc_max_scratch() bytes (8 MiB) inside this
+ * library's device image, which every GPU that loads the library holds until the process exits.
+ *  - Arguments and results are those of ssm_scan_fwd_ex without the workspace: the caller still
+ *    passes every input and output buffer.
+ *  - Shapes whose schedule needs more scratch than the fixed size return SSM_ERR_UNSUPPORTED
+ *    with a message naming the size; use ssm_scan_fwd with a caller workspace for those.
+ *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ *    that device current; make that first call before any stream capture.
+ *  - All calls on a device share the one array and it keeps the last call's contents (each call
+ *    writes the scratch words it reads, so results do not depend on them).  Two calls whose
+ *    kernels overlap on the GPU (different streams, or host threads without ordering) race on
+ *    the array: order them.
+ */
+SSM_API ssm_status ssm_scan_fwd_noalloc(const void* u, const void* delta, const float* A, const void* B,
+                                        const void* C, const float* D, const void* z, const float* delta_bias,
+                                        int softplus_flag, void* y, float* last_state, int batch, int dim,
+                                        int dstate, int64_t seqlen, ssm_dtype io_dtype,
+                                        const ssm_scan_options* opts, cudaStream_t stream);
+
+/* Size in bytes of the fixed scratch array used by ssm_scan_fwd_noalloc. */
+SSM_API size_t ssm_scan_fwd_noalloc_max_scratch(void);
+
 /* How a prefill call with these sizes and options would run (filled by ssm_scan_fwd_describe). */
 typedef struct {
   int struct_size;           /* set to sizeof(ssm_scan_plan) before the call */

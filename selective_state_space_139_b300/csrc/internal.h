@@ -73,6 +73,9 @@ struct DecodeParams {
 
 cudaError_t state_update_launch(const DecodeParams& p, cudaStream_t stream);
 
+// Sets the text returned by ssm_last_error_message() on the calling host thread (ssm_api.cu).
+void set_last_error(const char* fmt, ...);
+
 // Device status word access (scan_fwd.cu owns the symbol).
 cudaError_t read_and_clear_device_status(unsigned int* out, cudaStream_t stream);
 

@@ -203,6 +203,13 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 namespace ssm {
 
+void set_last_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+
 bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint64_t inner, uint64_t rows,
                           uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows, char* err,
                           size_t errlen) {
