@@ -5,12 +5,13 @@
 //   Δ_t = softplus(Δ_raw + bias);  h_t = exp(Δ_t A) ⊙ h_{t-1} + Δ_t B_t u_t;  y_t = (C_t·h_t + D u_t)·SiLU(z_t)
 //
 // Layout of the work:
-//  * A CTA owns 64 consecutive channels of one batch row (a "group") and 128 threads: two adjacent
-//    lanes per channel, lane parity p holding states [8p, 8p+8) as four packed f32x2 pairs.  The
-//    per-step scalars (softplus, decay exponent, Δu, gate, D skip) are computed by one lane of the
-//    pair -- the one whose parity matches the step's -- and exchanged with one shuffle each, so the
-//    pair does them once; each lane reduces its half of the readout and the owner of the step adds
-//    the partner's half.
+//  * A CTA owns 64 consecutive channels of one batch row (a "group").  kLanes adjacent lanes share a
+//    channel (2 or 4; the build default is the measured faster one), lane q holding the states
+//    [q·16/kLanes, (q+1)·16/kLanes) as packed f32x2 pairs.  The per-step scalars (softplus, decay
+//    exponent, Δu, gate, D skip) of each step are computed once, by the lane that owns the step,
+//    and broadcast to the other lanes of the channel with shuffles; each lane reduces its part of
+//    the readout and a shuffle butterfly hands every lane the totals of the steps it owns, which it
+//    gates, rounds and stores.
 //  * u, Δ_raw, z tiles [64 channels x 64 steps] and B, C tiles [dstate x 64 steps] arrive by TMA with
 //    a 128-byte swizzle through a 3-stage mbarrier pipeline (100 KB of shared memory, two CTAs per
 //    SM); B and C are widened once per tile into a float32 table read with broadcast 128-bit loads.
@@ -37,7 +38,13 @@
 #define SSM_FAST_SOFTPLUS_LOG 0     // 1: ln2 * log2(1 + e^v) everywhere below v = 15 (no series branch)
 #endif
 #ifndef SSM_FAST_UNROLL
-#define SSM_FAST_UNROLL 1           // unroll factor of the 8-step chunk loop
+#define SSM_FAST_UNROLL 1           // unroll factor of the chunk-pair loop
+#endif
+#ifndef SSM_FAST_LANES
+#define SSM_FAST_LANES 2            // lanes per channel: 2 or 4
+#endif
+#ifndef SSM_FAST_DECAYS_FIRST
+#define SSM_FAST_DECAYS_FIRST 0     // 1: compute the chunk's decay factors before its recurrence
 #endif
 
 namespace ssm {
@@ -46,12 +53,11 @@ namespace {
 __device__ unsigned int g_fast_status = 0;
 
 constexpr int kCh = 64;    // channels per CTA
-constexpr int kThr = 128;  // two lanes per channel
+constexpr int kLanesDefault = SSM_FAST_LANES;
 constexpr int kSt = 3;     // TMA stages
 constexpr int kRow = 128;  // bytes of one tile row = 64 bf16 steps
 constexpr int kT = 64;     // steps per tile
 constexpr int kN = 16;     // state width
-constexpr int kNh = 8;     // states per lane
 constexpr int kUnrollChunks = SSM_FAST_UNROLL;
 
 struct SmemF {
@@ -136,16 +142,19 @@ __device__ __forceinline__ f2 silu2(f2 z) {
   return f2_mul(z, f2_make(rcp_approx(f2_lo(den)), rcp_approx(f2_hi(den))));
 }
 
+template <int kNl>
 struct Lane {
   float A0L2;           // A[d,0]·log2(e)
-  float kb;             // 8p + 1: exponent multiplier of this lane's first decay
-  float AL2[kNh];       // A[d, 8p + i]·log2(e) (general A)
+  float kb;             // q·kNl + 1: exponent multiplier of this lane's first decay
+  float AL2[kNl];       // A[d, q·kNl + i]·log2(e) (general A)
   float D, bias;
-  bool structured;
 };
 
-template <int kMode>
-__global__ void __launch_bounds__(kThr, 2) scan_fast_kernel(const __grid_constant__ Maps tm, const ScanParams p) {
+template <int kLanes, int kMode>
+__global__ void __launch_bounds__(kCh * kLanes, 2) scan_fast_kernel(const __grid_constant__ Maps tm,
+                                                                      const ScanParams p) {
+  constexpr int kThr = kCh * kLanes;
+  constexpr int kNh = kN / kLanes;      // states per lane
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* bc32[2] = {reinterpret_cast<float*>(smem + kSt * SmemF::kStage),
@@ -153,9 +162,9 @@ __global__ void __launch_bounds__(kThr, 2) scan_fast_kernel(const __grid_constan
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SmemF::kBars);
 
   const int tid = threadIdx.x;
-  const int ch = tid >> 1;
-  const int pl = tid & 1;
-  const uint32_t sel = pl ? 0x3244u : 0x1044u;    // byte_perm selector: this lane's bf16 half -> f32
+  const int ch = tid / kLanes;
+  const int pl = tid % kLanes;                     // lane within the channel
+  const uint32_t sel = pl ? 0x3244u : 0x1044u;    // (2 lanes) byte_perm selector: this lane's bf16 half -> f32
   const int sw = ch & 7;                           // 128-byte swizzle of this channel's tile row
   const int64_t Lt = (p.L + kT - 1) / kT;
   const int gpb = (p.dim + kCh - 1) / kCh;         // groups per batch row
@@ -209,7 +218,7 @@ __global__ void __launch_bounds__(kThr, 2) scan_fast_kernel(const __grid_constan
   if (tid == 0)
     for (int64_t k = 0; k < kSt - 1 && k < ntiles; ++k) issue(k);
 
-  Lane ln;
+  Lane<kNh> ln;
   f2 h[kNh / 2];
   float sum_delta = 0.0f;
   bool warp_structured = true;
@@ -302,7 +311,7 @@ __global__ void __launch_bounds__(kThr, 2) scan_fast_kernel(const __grid_constan
       float* tab = bc32[k & 1];
       const uint32_t tB = smem_u32(st + 3 * SmemF::kTileIO);
 #pragma unroll
-      for (int rep = 0; rep < 2; ++rep) {
+      for (int rep = 0; rep < 256 / kThr; ++rep) {
         const int job = tid + rep * kThr;
         const int arr = job >> 7;
         const int n = job & 15;
@@ -329,147 +338,233 @@ __global__ void __launch_bounds__(kThr, 2) scan_fast_kernel(const __grid_constan
     const int64_t t0 = t * kT;
     const int nch = static_cast<int>(((p.L - t0 < kT) ? (p.L - t0) : kT) / 8);
     const uint32_t urow = smem_u32(st) + ch * kRow;
-    const uint32_t bct = smem_u32(bc32[k & 1]) + pl * 32;
+    const uint32_t bct = smem_u32(bc32[k & 1]) + pl * kNh * 4;
     __nv_bfloat16* yrow = (kMode == kMain && valid)
                               ? static_cast<__nv_bfloat16*>(p.y) + (static_cast<int64_t>(cur_b) * p.dim + cur_d) * p.L
                               : nullptr;
 
-    // Per chunk of 8 steps: "prep" reads the inputs, computes this lane's own-step scalars and
-    // exchanges them with the partner lane; "run" does the recurrence, the readout and the store.
-    // The loop prepares chunk c+1 while it runs chunk c, so the two latency chains overlap.
+    // Per chunk of 8 steps: "prep" reads the inputs, computes the scalars of the steps this lane owns
+    // and broadcasts them to the channel's lanes; "run" does the recurrence, the readout, the
+    // reduction over the channel's lanes and the store.  The loop prepares chunk c+1 while it runs
+    // chunk c (two Prep buffers used in turn), so the two latency chains overlap.
     struct Prep {
       float qs[8], ws[8], dls[8];
-      float g[4], du[4];       // SiLU(z) and D·u of this lane's own steps 2i + pl
+      float g[8 / kLanes], du[8 / kLanes];   // SiLU(z) and D·u of this lane's own steps
     };
 
     auto prep = [&](auto structured_tag, int c, Prep& P) {
       constexpr bool kS = decltype(structured_tag)::value;
       const uint32_t off = (c ^ sw) << 4;
-      const uint4 uw = lds128(urow + off);
-      const uint4 dw = lds128(urow + SmemF::kTileIO + off);
-      // this lane's four steps 2i + pl, as two packed pairs (i = 0,1) and (i = 2,3)
-      const f2 u01 = f2_make(prmt_half(uw.x, sel), prmt_half(uw.y, sel));
-      const f2 u23 = f2_make(prmt_half(uw.z, sel), prmt_half(uw.w, sel));
-      const f2 bias2 = f2_splat(ln.bias);
-      f2 d01 = f2_add(f2_make(prmt_half(dw.x, sel), prmt_half(dw.y, sel)), bias2);
-      f2 d23 = f2_add(f2_make(prmt_half(dw.z, sel), prmt_half(dw.w, sel)), bias2);
-      if (p.softplus) {
-        d01 = softplus2(d01);
-        d23 = softplus2(d23);
-      }
-      if (kMode == kAgg) sum_delta += (f2_lo(d01) + f2_hi(d01)) + (f2_lo(d23) + f2_hi(d23));
-      const f2 a0 = f2_splat(ln.A0L2);
-      const f2 q01 = f2_mul(d01, a0), q23 = f2_mul(d23, a0);     // log2 of the step's base decay
-      const f2 w01 = f2_mul(d01, u01), w23 = f2_mul(d23, u23);   // Δ·u
-      const float qo[4] = {f2_lo(q01), f2_hi(q01), f2_lo(q23), f2_hi(q23)};
-      const float wo[4] = {f2_lo(w01), f2_hi(w01), f2_lo(w23), f2_hi(w23)};
-      const float dlo[4] = {f2_lo(d01), f2_hi(d01), f2_lo(d23), f2_hi(d23)};
-#if SSM_FAST_SHFL_DIRECT
-      const int pair0 = (threadIdx.x & 31) & ~1;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        P.qs[j] = __shfl_sync(0xffffffffu, qo[j >> 1], pair0 | (j & 1));
-        P.ws[j] = __shfl_sync(0xffffffffu, wo[j >> 1], pair0 | (j & 1));
-        if (!kS) P.dls[j] = __shfl_sync(0xffffffffu, dlo[j >> 1], pair0 | (j & 1));
-      }
-#else
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float qx = __shfl_xor_sync(0xffffffffu, qo[i], 1);
-        const float wx = __shfl_xor_sync(0xffffffffu, wo[i], 1);
-        P.qs[2 * i] = pl ? qx : qo[i];
-        P.qs[2 * i + 1] = pl ? qo[i] : qx;
-        P.ws[2 * i] = pl ? wx : wo[i];
-        P.ws[2 * i + 1] = pl ? wo[i] : wx;
-        if (!kS) {
-          const float dx = __shfl_xor_sync(0xffffffffu, dlo[i], 1);
-          P.dls[2 * i] = pl ? dx : dlo[i];
-          P.dls[2 * i + 1] = pl ? dlo[i] : dx;
+      if constexpr (kLanes == 2) {
+        // own steps 2i + pl: the pl half of each 32-bit word of the 16-byte chunk
+        const uint4 uw = lds128(urow + off);
+        const uint4 dw = lds128(urow + SmemF::kTileIO + off);
+        const f2 u01 = f2_make(prmt_half(uw.x, sel), prmt_half(uw.y, sel));
+        const f2 u23 = f2_make(prmt_half(uw.z, sel), prmt_half(uw.w, sel));
+        const f2 bias2 = f2_splat(ln.bias);
+        f2 d01 = f2_add(f2_make(prmt_half(dw.x, sel), prmt_half(dw.y, sel)), bias2);
+        f2 d23 = f2_add(f2_make(prmt_half(dw.z, sel), prmt_half(dw.w, sel)), bias2);
+        if (p.softplus) {
+          d01 = softplus2(d01);
+          d23 = softplus2(d23);
         }
-      }
-#endif
-      if (kMode == kMain) {
-        f2 g01 = f2_splat(1.0f), g23 = f2_splat(1.0f);
-        if (has_z) {
-          const uint4 zw = lds128(urow + 2 * SmemF::kTileIO + off);
-          g01 = silu2(f2_make(prmt_half(zw.x, sel), prmt_half(zw.y, sel)));
-          g23 = silu2(f2_make(prmt_half(zw.z, sel), prmt_half(zw.w, sel)));
+        if (kMode == kAgg) sum_delta += (f2_lo(d01) + f2_hi(d01)) + (f2_lo(d23) + f2_hi(d23));
+        const f2 a0 = f2_splat(ln.A0L2);
+        const f2 q01 = f2_mul(d01, a0), q23 = f2_mul(d23, a0);     // log2 of the step's base decay
+        const f2 w01 = f2_mul(d01, u01), w23 = f2_mul(d23, u23);   // Δ·u
+        const float qo[4] = {f2_lo(q01), f2_hi(q01), f2_lo(q23), f2_hi(q23)};
+        const float wo[4] = {f2_lo(w01), f2_hi(w01), f2_lo(w23), f2_hi(w23)};
+        const float dlo[4] = {f2_lo(d01), f2_hi(d01), f2_lo(d23), f2_hi(d23)};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float qx = __shfl_xor_sync(0xffffffffu, qo[i], 1);
+          const float wx = __shfl_xor_sync(0xffffffffu, wo[i], 1);
+          P.qs[2 * i] = pl ? qx : qo[i];
+          P.qs[2 * i + 1] = pl ? qo[i] : qx;
+          P.ws[2 * i] = pl ? wx : wo[i];
+          P.ws[2 * i + 1] = pl ? wo[i] : wx;
+          if (!kS) {
+            const float dx = __shfl_xor_sync(0xffffffffu, dlo[i], 1);
+            P.dls[2 * i] = pl ? dx : dlo[i];
+            P.dls[2 * i + 1] = pl ? dlo[i] : dx;
+          }
         }
-        const f2 dd = f2_splat(ln.D);
-        const f2 du01 = f2_mul(dd, u01), du23 = f2_mul(dd, u23);
-        P.g[0] = f2_lo(g01); P.g[1] = f2_hi(g01); P.g[2] = f2_lo(g23); P.g[3] = f2_hi(g23);
-        P.du[0] = f2_lo(du01); P.du[1] = f2_hi(du01); P.du[2] = f2_lo(du23); P.du[3] = f2_hi(du23);
+        if (kMode == kMain) {
+          f2 g01 = f2_splat(1.0f), g23 = f2_splat(1.0f);
+          if (has_z) {
+            const uint4 zw = lds128(urow + 2 * SmemF::kTileIO + off);
+            g01 = silu2(f2_make(prmt_half(zw.x, sel), prmt_half(zw.y, sel)));
+            g23 = silu2(f2_make(prmt_half(zw.z, sel), prmt_half(zw.w, sel)));
+          }
+          const f2 dd = f2_splat(ln.D);
+          const f2 du01 = f2_mul(dd, u01), du23 = f2_mul(dd, u23);
+          P.g[0] = f2_lo(g01); P.g[1] = f2_hi(g01); P.g[2] = f2_lo(g23); P.g[3] = f2_hi(g23);
+          P.du[0] = f2_lo(du01); P.du[1] = f2_hi(du01); P.du[2] = f2_lo(du23); P.du[3] = f2_hi(du23);
+        }
+      } else {
+        // own steps 2·pl and 2·pl + 1: the 32-bit word pl of the 16-byte chunk
+        const uint32_t woff = off + 4 * pl;
+        const uint32_t uw = lds32(urow + woff);
+        const uint32_t dw = lds32(urow + SmemF::kTileIO + woff);
+        const f2 u2 = f2_make(bf16lo_to_f32(uw), bf16hi_to_f32(uw));
+        f2 d2 = f2_add(f2_make(bf16lo_to_f32(dw), bf16hi_to_f32(dw)), f2_splat(ln.bias));
+        if (p.softplus) d2 = softplus2(d2);
+        if (kMode == kAgg) sum_delta += f2_lo(d2) + f2_hi(d2);
+        const f2 q2 = f2_mul(d2, f2_splat(ln.A0L2));
+        const f2 w2 = f2_mul(d2, u2);
+        const int quad0 = (threadIdx.x & 31) & ~3;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int src = quad0 | (j >> 1);
+          P.qs[j] = __shfl_sync(0xffffffffu, (j & 1) ? f2_hi(q2) : f2_lo(q2), src);
+          P.ws[j] = __shfl_sync(0xffffffffu, (j & 1) ? f2_hi(w2) : f2_lo(w2), src);
+          if (!kS) P.dls[j] = __shfl_sync(0xffffffffu, (j & 1) ? f2_hi(d2) : f2_lo(d2), src);
+        }
+        if (kMode == kMain) {
+          f2 g2 = f2_splat(1.0f);
+          if (has_z) {
+            const uint32_t zw = lds32(urow + 2 * SmemF::kTileIO + woff);
+            g2 = silu2(f2_make(bf16lo_to_f32(zw), bf16hi_to_f32(zw)));
+          }
+          const f2 du2 = f2_mul(f2_splat(ln.D), u2);
+          P.g[0] = f2_lo(g2); P.g[1] = f2_hi(g2);
+          P.du[0] = f2_lo(du2); P.du[1] = f2_hi(du2);
+        }
       }
     };
 
     auto run = [&](auto structured_tag, int c, const Prep& P) {
       constexpr bool kS = decltype(structured_tag)::value;
       float py[8];
+#if SSM_FAST_DECAYS_FIRST
+      f2 aa[8][kNh / 2];
+      if (kS) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        f2 a[kNh / 2];
-        if (kS) {
+        for (int j = 0; j < 8; ++j) {
           const float r = ex2_approx(P.qs[j]);
           const float bse = ex2_approx(P.qs[j] * ln.kb);
           const float r2 = r * r;
-          const float r4 = r2 * r2;
+          aa[j][0] = f2_make(bse, bse * r);
+          aa[j][1] = f2_mul(aa[j][0], f2_splat(r2));
+          if constexpr (kNh == 8) {
+            const float r4 = r2 * r2;
+            aa[j][2] = f2_mul(aa[j][0], f2_splat(r4));
+            aa[j][3] = f2_mul(aa[j][1], f2_splat(r4));
+          }
+        }
+      }
+#endif
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        f2 a[kNh / 2];
+#if SSM_FAST_DECAYS_FIRST
+        if (kS) {
+#pragma unroll
+          for (int i = 0; i < kNh / 2; ++i) a[i] = aa[j][i];
+        } else
+#endif
+        if (kS) {
+          // powers r^(q·kNl + 1) .. r^(q·kNl + kNl) of r = exp(Δ A[d,0])
+          const float r = ex2_approx(P.qs[j]);
+          const float bse = ex2_approx(P.qs[j] * ln.kb);
+          const float r2 = r * r;
           a[0] = f2_make(bse, bse * r);
           a[1] = f2_mul(a[0], f2_splat(r2));
-          a[2] = f2_mul(a[0], f2_splat(r4));
-          a[3] = f2_mul(a[1], f2_splat(r4));
+          if constexpr (kNh == 8) {
+            const float r4 = r2 * r2;
+            a[2] = f2_mul(a[0], f2_splat(r4));
+            a[3] = f2_mul(a[1], f2_splat(r4));
+          }
         } else {
 #pragma unroll
           for (int i = 0; i < kNh / 2; ++i)
             a[i] = f2_make(ex2_approx(P.dls[j] * ln.AL2[2 * i]), ex2_approx(P.dls[j] * ln.AL2[2 * i + 1]));
         }
         const uint32_t rowb = bct + (c * 8 + j) * 128;
-        const float4 b0 = lds128f(rowb), b1 = lds128f(rowb + 16);
         const f2 wj = f2_splat(P.ws[j]);
-        h[0] = f2_fma(a[0], h[0], f2_mul(wj, f2_make(b0.x, b0.y)));
-        h[1] = f2_fma(a[1], h[1], f2_mul(wj, f2_make(b0.z, b0.w)));
-        h[2] = f2_fma(a[2], h[2], f2_mul(wj, f2_make(b1.x, b1.y)));
-        h[3] = f2_fma(a[3], h[3], f2_mul(wj, f2_make(b1.z, b1.w)));
-        if (kMode == kMain) {
-          const float4 c0 = lds128f(rowb + 64), c1 = lds128f(rowb + 80);
-          f2 acc = f2_mul(f2_make(c0.x, c0.y), h[0]);
-          acc = f2_fma(f2_make(c0.z, c0.w), h[1], acc);
-          acc = f2_fma(f2_make(c1.x, c1.y), h[2], acc);
-          acc = f2_fma(f2_make(c1.z, c1.w), h[3], acc);
-          py[j] = f2_lo(acc) + f2_hi(acc);
+        f2 acc;
+        if constexpr (kNh == 8) {
+          const float4 b0 = lds128f(rowb), b1 = lds128f(rowb + 16);
+          h[0] = f2_fma(a[0], h[0], f2_mul(wj, f2_make(b0.x, b0.y)));
+          h[1] = f2_fma(a[1], h[1], f2_mul(wj, f2_make(b0.z, b0.w)));
+          h[2] = f2_fma(a[2], h[2], f2_mul(wj, f2_make(b1.x, b1.y)));
+          h[3] = f2_fma(a[3], h[3], f2_mul(wj, f2_make(b1.z, b1.w)));
+          if (kMode == kMain) {
+            const float4 c0 = lds128f(rowb + 64), c1 = lds128f(rowb + 80);
+            acc = f2_mul(f2_make(c0.x, c0.y), h[0]);
+            acc = f2_fma(f2_make(c0.z, c0.w), h[1], acc);
+            acc = f2_fma(f2_make(c1.x, c1.y), h[2], acc);
+            acc = f2_fma(f2_make(c1.z, c1.w), h[3], acc);
+          }
+        } else {
+          const float4 b0 = lds128f(rowb);
+          h[0] = f2_fma(a[0], h[0], f2_mul(wj, f2_make(b0.x, b0.y)));
+          h[1] = f2_fma(a[1], h[1], f2_mul(wj, f2_make(b0.z, b0.w)));
+          if (kMode == kMain) {
+            const float4 c0 = lds128f(rowb + 64);
+            acc = f2_mul(f2_make(c0.x, c0.y), h[0]);
+            acc = f2_fma(f2_make(c0.z, c0.w), h[1], acc);
+          }
         }
+        if (kMode == kMain) py[j] = f2_lo(acc) + f2_hi(acc);
       }
       if (kMode != kMain) return;
-      // owner of step 2i + pl finishes it: (own half + partner half + D u) * SiLU(z)
-      float yo[4];
+      if constexpr (kLanes == 2) {
+        // owner of step 2i + pl finishes it: (own half + partner half + D u) * SiLU(z)
+        float yo[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float mine = pl ? py[2 * i + 1] : py[2 * i];
-        const float send = pl ? py[2 * i] : py[2 * i + 1];
-        const float other = __shfl_xor_sync(0xffffffffu, send, 1);
-        yo[i] = (mine + other + P.du[i]) * P.g[i];
-      }
-      // lane 0 stores steps 0..3, lane 1 steps 4..7 of this chunk
-      const float s1 = __shfl_xor_sync(0xffffffffu, pl ? yo[0] : yo[2], 1);   // lane0 gets y1, lane1 gets y4
-      const float s2 = __shfl_xor_sync(0xffffffffu, pl ? yo[1] : yo[3], 1);   // lane0 gets y3, lane1 gets y6
-      uint2 out;
-      if (pl == 0) {
-        out.x = pack_bf16x2(yo[0], s1);
-        out.y = pack_bf16x2(yo[1], s2);
+        for (int i = 0; i < 4; ++i) {
+          const float mine = pl ? py[2 * i + 1] : py[2 * i];
+          const float send = pl ? py[2 * i] : py[2 * i + 1];
+          const float other = __shfl_xor_sync(0xffffffffu, send, 1);
+          yo[i] = (mine + other + P.du[i]) * P.g[i];
+        }
+        // lane 0 stores steps 0..3, lane 1 steps 4..7 of this chunk
+        const float s1 = __shfl_xor_sync(0xffffffffu, pl ? yo[0] : yo[2], 1);   // lane0 gets y1, lane1 gets y4
+        const float s2 = __shfl_xor_sync(0xffffffffu, pl ? yo[1] : yo[3], 1);   // lane0 gets y3, lane1 gets y6
+        uint2 out;
+        if (pl == 0) {
+          out.x = pack_bf16x2(yo[0], s1);
+          out.y = pack_bf16x2(yo[1], s2);
+        } else {
+          out.x = pack_bf16x2(s1, yo[2]);
+          out.y = pack_bf16x2(s2, yo[3]);
+        }
+        if (valid) *reinterpret_cast<uint2*>(yrow + t0 + c * 8 + pl * 4) = out;
       } else {
-        out.x = pack_bf16x2(s1, yo[2]);
-        out.y = pack_bf16x2(s2, yo[3]);
+        // butterfly over the 4 lanes: after it, lane q holds the totals of steps 2q and 2q + 1
+        const bool up2 = (pl & 2) != 0;
+        float k4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float send = up2 ? py[i] : py[4 + i];
+          const float keep = up2 ? py[4 + i] : py[i];
+          k4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+        }
+        const bool up1 = (pl & 1) != 0;
+        float tot[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const float send = up1 ? k4[i] : k4[2 + i];
+          const float keep = up1 ? k4[2 + i] : k4[i];
+          tot[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+        }
+        const f2 y2 = f2_mul(f2_add(f2_make(tot[0], tot[1]), f2_make(P.du[0], P.du[1])), f2_make(P.g[0], P.g[1]));
+        if (valid) *reinterpret_cast<uint32_t*>(yrow + t0 + c * 8 + 2 * pl) = pack_bf16x2(f2_lo(y2), f2_hi(y2));
       }
-      if (valid) *reinterpret_cast<uint2*>(yrow + t0 + c * 8 + pl * 4) = out;
     };
 
     auto pipeline = [&](auto tag) {
-      Prep cur, nxt;
-      prep(tag, 0, cur);
+      Prep pa, pb;
+      prep(tag, 0, pa);
 #pragma unroll kUnrollChunks
-      for (int c = 0; c < nch; ++c) {
-        if (c + 1 < nch) prep(tag, c + 1, nxt);
-        run(tag, c, cur);
-        cur = nxt;
+      for (int c = 0; c < nch; c += 2) {
+        if (c + 1 < nch) prep(tag, c + 1, pb);
+        run(tag, c, pa);
+        if (c + 1 < nch) {
+          if (c + 2 < nch) prep(tag, c + 2, pa);
+          run(tag, c + 1, pb);
+        }
       }
     };
     if (nch > 0) {
@@ -503,7 +598,11 @@ __global__ void __launch_bounds__(kThr, 2) scan_fast_kernel(const __grid_constan
       }
     }
     // the pair's ΣΔ (every lane takes part in the shuffle, valid or not)
-    const float sd = (kMode == kAgg && chunk_end) ? sum_delta + __shfl_xor_sync(0xffffffffu, sum_delta, 1) : 0.0f;
+    float sd = 0.0f;
+    if (kMode == kAgg && chunk_end) {
+      sd = sum_delta + __shfl_xor_sync(0xffffffffu, sum_delta, 1);
+      if (kLanes == 4) sd += __shfl_xor_sync(0xffffffffu, sd, 2);
+    }
     if (kMode == kAgg && chunk_end && valid) {
       // aggregate of this chunk: P = exp(A ΣΔ), Q = h_end from a zero state
       const int64_t cbase = chunk_idx * p.h_in_chunk_stride + state_off(cur_b, cur_d);
@@ -533,13 +632,21 @@ __global__ void __launch_bounds__(kThr, 2) scan_fast_kernel(const __grid_constan
 int fast_channels_per_cta() { return kCh; }
 
 int fast_resident_ctas() {
+  static int cached[64] = {0};
   int occ = 0, dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return 0; }
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) { cudaGetLastError(); return 0; }
-  if (cudaFuncSetAttribute(scan_fast_kernel<kMain>, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemF::kTotal) !=
-      cudaSuccess) { cudaGetLastError(); return 0; }
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, scan_fast_kernel<kMain>, kThr, SmemF::kTotal) !=
-      cudaSuccess) { cudaGetLastError(); return 0; }
+  auto kern = scan_fast_kernel<kLanesDefault, kMain>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemF::kTotal) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kCh * kLanesDefault, SmemF::kTotal) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (dev >= 0 && dev < 64) cached[dev] = occ * sms;
   return occ * sms;
 }
 
@@ -552,6 +659,8 @@ cudaError_t fast_status_read_and_clear(unsigned int* out) {
 
 cudaError_t scan_fast_launch(const ScanParams& p, int nchunks, int balanced_ctas, cudaStream_t stream, char* err,
                              size_t errlen) {
+  constexpr int kL = kLanesDefault;
+  constexpr int kThreads = kCh * kL;
   Maps tm;
   memset(&tm, 0, sizeof(tm));
   const uint64_t rows = static_cast<uint64_t>(p.batch) * p.dim;
@@ -573,29 +682,31 @@ cudaError_t scan_fast_launch(const ScanParams& p, int nchunks, int balanced_ctas
   }
   const int gpb = (p.dim + kCh - 1) / kCh;
   const unsigned groups = static_cast<unsigned>(p.batch) * gpb;
+  auto kmain = scan_fast_kernel<kL, kMain>;
+  auto kagg = scan_fast_kernel<kL, kAgg>;
   cudaError_t e;
-  e = cudaFuncSetAttribute(scan_fast_kernel<kMain>, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemF::kTotal);
+  e = cudaFuncSetAttribute(kmain, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemF::kTotal);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(scan_fast_kernel<kAgg>, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemF::kTotal);
+  e = cudaFuncSetAttribute(kagg, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemF::kTotal);
   if (e != cudaSuccess) return e;
   if (balanced_ctas > 0) {
     e = cudaMemsetAsync(p.flags, 0, sizeof(unsigned) * balanced_ctas, stream);
     if (e != cudaSuccess) return e;
     void* args[] = {const_cast<Maps*>(&tm), const_cast<ScanParams*>(&p)};
-    return cudaLaunchCooperativeKernel(reinterpret_cast<void*>(scan_fast_kernel<kMain>), dim3(balanced_ctas),
-                                       dim3(kThr), args, SmemF::kTotal, stream);
+    return cudaLaunchCooperativeKernel(reinterpret_cast<void*>(kmain), dim3(balanced_ctas), dim3(kThreads), args,
+                                       SmemF::kTotal, stream);
   }
   if (nchunks > 1) {
     ScanParams pa = p;
     pa.h_in = nullptr;
     pa.h0 = nullptr;
-    scan_fast_kernel<kAgg><<<dim3(groups, nchunks - 1), kThr, SmemF::kTotal, stream>>>(tm, pa);
+    kagg<<<dim3(groups, nchunks - 1), kThreads, SmemF::kTotal, stream>>>(tm, pa);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     e = carry_launch_f32(p, nchunks, stream);
     if (e != cudaSuccess) return e;
   }
-  scan_fast_kernel<kMain><<<dim3(groups, nchunks), kThr, SmemF::kTotal, stream>>>(tm, p);
+  kmain<<<dim3(groups, nchunks), kThreads, SmemF::kTotal, stream>>>(tm, p);
   return cudaGetLastError();
 }
 
