@@ -289,6 +289,33 @@ def measure_decode(w, steps_tokens, dev, rank):
             "tokens_per_s": w.batch / (k_ms * 1e-3)}
 
 
+def measure_conv(w, dev, rank, reps=50):
+    """The conv1d + SiLU prefill kernel on the workload's x (batch, dim, L): event-timed per launch."""
+    import torch
+    from selective_state_space_139_b300 import ssm
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed + 17 + rank)
+    x = torch.randn((w.batch, w.dim, w.seqlen), generator=g, device=dev).to(torch.bfloat16)
+    cw = 0.5 * torch.randn((w.dim, 4), generator=g, device=dev)
+    st = torch.zeros((w.batch, w.dim, 3), device=dev)
+    u = torch.empty_like(x)
+    st_out = torch.empty_like(st)
+    for _ in range(3):
+        ssm.causal_conv1d_fwd(x, cw, st, out=u, final_state=st_out)
+    torch.cuda.synchronize(dev)
+    times = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        ssm.causal_conv1d_fwd(x, cw, st, out=u, final_state=st_out)
+        b.record()
+        torch.cuda.synchronize(dev)
+        times.append(a.elapsed_time(b))
+    ms = statistics.median(times)
+    nbytes = 2 * x.numel() * 2 + w.dim * 16 + 2 * st.numel() * 4
+    return {"ms": ms, "bytes": nbytes, "achieved_gbs": nbytes / (ms * 1e-3) / 1e9}
+
+
 # ----------------------------------------------------------------------------- distributed helpers
 
 _PG = None
@@ -388,6 +415,7 @@ def main():
         dw = W.WORKLOADS["decode-2.8b"]
         dec = measure_decode(dw, args.decode_steps, dev, rank)
         dec["ms_per_token_step"] = _max_over_ranks(dec["ms_per_token_step"])
+    conv = measure_conv(w, dev, rank)
     if rank != 0:
         return 0
     tokens_all = w.tokens * ws
@@ -414,6 +442,9 @@ def main():
                           "ms_per_token_step": dec["ms_per_token_step"], "achieved_gbs": dec["achieved_gbs"],
                           "frac": dec["achieved_gbs"] / peak, "bytes_per_step": dec["bytes_per_step"],
                           "steps": dec["steps"]}
+    line["conv1d"] = {"workload": w.name + " x (conv1d + SiLU prefill)", "ms": conv["ms"],
+                      "achieved_gbs": conv["achieved_gbs"], "frac": conv["achieved_gbs"] / peak,
+                      "bytes_per_launch": conv["bytes"]}
     if not args.no_cpu_baseline:
         v, cores, sample, _ = cpu_oracle_sample(w)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}

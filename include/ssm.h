@@ -184,6 +184,23 @@ SSM_API ssm_status ssm_scan_fwd_describe(int batch, int dim, int dstate, int64_t
                                          const ssm_scan_options* opts, ssm_scan_plan* plan);
 
 /*
+ * Prefill of the short convolution that feeds the scan: causal depthwise conv1d of width dconv (4)
+ * followed by SiLU ("Mamba и State Space Models", "Реализация MambaBlock"; "State Space Models: Mamba и
+ * альтернатива Transformer", "Mamba: Selective State Space"; the cache of "Модуль 8", §14):
+ *   u[b,d,t] = SiLU( Σ_{k<4} conv_w[d,k] · xpad[b,d,t+k] ),  xpad = [conv_state_in[b,d,0..2], x[b,d,:]]
+ *   conv_state_out[b,d,:] = the last three entries of xpad (oldest first), ready for ssm_state_update
+ *   x, u            : (batch, dim, seqlen) io_dtype
+ *   conv_w          : (dim, dconv) float32, no bias; conv_w[d, dconv-1] multiplies the newest input
+ *   conv_state_in   : (batch, dim, dconv-1) float32 or NULL (zeros: a fresh sequence)
+ *   conv_state_out  : (batch, dim, dconv-1) float32 or NULL; must not alias conv_state_in
+ *   apply_silu      : nonzero applies SiLU (the Mamba block does)
+ * dconv must be 4.  Float32 io is computed in double.
+ */
+SSM_API ssm_status ssm_causal_conv1d_fwd(const void* x, const float* conv_w, const float* conv_state_in, void* u,
+                                         float* conv_state_out, int batch, int dim, int64_t seqlen, int dconv,
+                                         int apply_silu, ssm_dtype io_dtype, cudaStream_t stream);
+
+/*
  * Reads and clears the device status word (synchronises `stream`).  Returns SSM_OK, SSM_ERR_TIMEOUT
  * if a kernel gave up a bounded wait since the last call, or SSM_ERR_CUDA.
  */

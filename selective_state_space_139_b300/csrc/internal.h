@@ -73,6 +73,21 @@ struct DecodeParams {
 
 cudaError_t state_update_launch(const DecodeParams& p, cudaStream_t stream);
 
+struct ConvParams {
+  const void* x;          // (batch, dim, L) io dtype
+  const float* w;         // (dim, 4)
+  const float* state_in;  // (batch, dim, 3) or null (zeros)
+  void* u;                // (batch, dim, L) io dtype
+  float* state_out;       // (batch, dim, 3) or null
+  int batch, dim;
+  int64_t L;
+  int silu;
+  int io_bf16;
+};
+
+// vec: L is a multiple of the 16-byte element count and x, u, w are 16-byte aligned
+cudaError_t conv1d_launch(const ConvParams& p, bool vec, cudaStream_t stream);
+
 // Sets the text returned by ssm_last_error_message() on the calling host thread (ssm_api.cu).
 void set_last_error(const char* fmt, ...);
 

@@ -439,6 +439,8 @@ ssm_status ssm_state_update(const void* x_t, const void* delta_t, const float* A
     return fail(SSM_ERR_INVALID_ARG, "bad sizes batch=%d dim=%d dstate=%d dconv=%d", batch, dim, dstate, dconv);
   if (dstate > 16) return fail(SSM_ERR_UNSUPPORTED, "dstate=%d > 16 is not supported", dstate);
   if (dconv != 4) return fail(SSM_ERR_UNSUPPORTED, "d_conv=%d is not supported (only 4)", dconv);
+  if (static_cast<int64_t>(batch) * dim >= (int64_t(1) << 31))
+    return fail(SSM_ERR_UNSUPPORTED, "batch * dim must be below 2^31");
   if (!x_t || !delta_t || !A || !B_t || !C_t || !state || !conv_state || !conv_w || !y_t)
     return fail(SSM_ERR_INVALID_ARG, "null required pointer");
   const size_t e = io_dtype == SSM_BF16 ? 2 : 4;
@@ -469,6 +471,54 @@ ssm_status ssm_state_update(const void* x_t, const void* delta_t, const float* A
             aligned(C_t, 8);
   cudaError_t ce = ssm::state_update_launch(p, stream);
   if (ce != cudaSuccess) return cuda_fail(ce, "state update launch");
+  return SSM_OK;
+}
+
+ssm_status ssm_causal_conv1d_fwd(const void* x, const float* conv_w, const float* conv_state_in, void* u,
+                                 float* conv_state_out, int batch, int dim, int64_t seqlen, int dconv, int apply_silu,
+                                 ssm_dtype io_dtype, cudaStream_t stream) {
+  g_err[0] = 0;
+  if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return fail(SSM_ERR_INVALID_ARG, "unknown io_dtype %d", io_dtype);
+  if (batch < 1 || dim < 1 || seqlen < 0 || dconv < 1)
+    return fail(SSM_ERR_INVALID_ARG, "bad sizes batch=%d dim=%d seqlen=%lld dconv=%d", batch, dim,
+                static_cast<long long>(seqlen), dconv);
+  if (dconv != 4) return fail(SSM_ERR_UNSUPPORTED, "d_conv=%d is not supported (only 4)", dconv);
+  if (static_cast<int64_t>(batch) * dim >= (int64_t(1) << 31))
+    return fail(SSM_ERR_UNSUPPORTED, "batch * dim must be below 2^31");
+  if (!conv_w || (seqlen > 0 && (!x || !u))) return fail(SSM_ERR_INVALID_ARG, "null required pointer (x, conv_w, u)");
+  const size_t e = io_dtype == SSM_BF16 ? 2 : 4;
+  for (const void* p : {x, static_cast<const void*>(u)})
+    if (p && !aligned(p, e)) return fail(SSM_ERR_INVALID_ARG, "io pointer not aligned to its element size");
+  for (const void* p : {static_cast<const void*>(conv_w), static_cast<const void*>(conv_state_in),
+                        static_cast<const void*>(conv_state_out)})
+    if (p && !aligned(p, 4)) return fail(SSM_ERR_INVALID_ARG, "float32 pointer not 4-byte aligned");
+  const size_t bdl = static_cast<size_t>(batch) * dim * seqlen * e;
+  const size_t st = static_cast<size_t>(batch) * dim * 3 * 4;
+  const Range outs[] = {range_of(u, bdl), range_of(conv_state_out, conv_state_out ? st : 0)};
+  const Range ins[] = {range_of(x, bdl), range_of(conv_w, static_cast<size_t>(dim) * 4 * 4),
+                       range_of(conv_state_in, conv_state_in ? st : 0)};
+  for (const Range& o : outs)
+    for (const Range& i : ins)
+      if (overlap(o, i)) return fail(SSM_ERR_INVALID_ARG, "an output overlaps an input");
+  if (overlap(outs[0], outs[1])) return fail(SSM_ERR_INVALID_ARG, "u overlaps conv_state_out");
+  if (seqlen == 0) {
+    if (conv_state_out) {
+      cudaError_t ce = conv_state_in ? cudaMemcpyAsync(conv_state_out, conv_state_in, st, cudaMemcpyDeviceToDevice, stream)
+                                     : cudaMemsetAsync(conv_state_out, 0, st, stream);
+      if (ce != cudaSuccess) return cuda_fail(ce, "seqlen 0 conv state copy");
+    }
+    return SSM_OK;
+  }
+  ssm::ConvParams p;
+  memset(&p, 0, sizeof(p));
+  p.x = x; p.w = conv_w; p.state_in = conv_state_in; p.u = u; p.state_out = conv_state_out;
+  p.batch = batch; p.dim = dim; p.L = seqlen; p.silu = apply_silu != 0; p.io_bf16 = io_dtype == SSM_BF16;
+  const int64_t vecn = static_cast<int64_t>(16 / e);
+  // the vectorised kernel indexes chunks with 32-bit integers
+  const bool vec = seqlen % vecn == 0 && aligned(x, 16) && aligned(u, 16) && aligned(conv_w, 16) &&
+                   static_cast<int64_t>(batch) * dim * (seqlen / vecn) < (int64_t(1) << 31);
+  cudaError_t ce = ssm::conv1d_launch(p, vec, stream);
+  if (ce != cudaSuccess) return cuda_fail(ce, "conv1d launch");
   return SSM_OK;
 }
 

@@ -27,15 +27,17 @@ template <typename IO, bool kFull16>
 __global__ void __launch_bounds__(kThreads) state_update_kernel(const DecodeParams p) {
   constexpr bool kFast = sizeof(IO) == 2;
   const int tid = threadIdx.x;
-  const int64_t c_raw = static_cast<int64_t>(blockIdx.x) * kChannelsPerBlock + tid / kLanesPerChannel;
+  // channel indices fit 32 bits (batch * dim < 2^31 is checked on the host): 32-bit division only
+  const int c_raw = static_cast<int>(blockIdx.x) * kChannelsPerBlock + tid / kLanesPerChannel;
   const int j = tid % kLanesPerChannel;
-  const int64_t nchan = static_cast<int64_t>(p.batch) * p.dim;
+  const int nchan = p.batch * p.dim;
   // lanes past the last channel still take part in the shuffles; they read a valid channel and
   // write nothing
   const bool live = c_raw < nchan;
-  const int64_t c = live ? c_raw : nchan - 1;
-  const int b = static_cast<int>(c / p.dim);
-  const int d = static_cast<int>(c % p.dim);
+  const int c32 = live ? c_raw : nchan - 1;
+  const int b = c32 / p.dim;
+  const int d = c32 - b * p.dim;
+  const int64_t c = c32;
   const int N = kFull16 ? 16 : p.N;
 
   // conv window [cs0, cs1, cs2, x_t] and its weights
@@ -146,9 +148,98 @@ __global__ void __launch_bounds__(kThreads) state_update_kernel(const DecodePara
   }
 }
 
+// bf16 io, dstate 16, aligned buffers: each thread serves kPer channels (slot + 64 k of its block),
+// issuing every load of all of them before any arithmetic and storing after, so that several
+// 16-byte state reads per thread are in flight (the step is bound by HBM latency x parallelism).
+constexpr int kPer = 2;
+
+__global__ void __launch_bounds__(kThreads) state_update_bf16_kernel(const DecodeParams p) {
+  using IO = __nv_bfloat16;
+  const int tid = threadIdx.x;
+  const int j = tid % kLanesPerChannel;
+  const int slot = tid / kLanesPerChannel;
+  const int nchan = p.batch * p.dim;
+  const int base = static_cast<int>(blockIdx.x) * (kChannelsPerBlock * kPer);
+  int cc[kPer];
+  bool live[kPer];
+  float4 h4[kPer], a4[kPer], w4[kPer];
+  uint2 braw[kPer], craw[kPer];
+  float xv[kPer], dv[kPer], zv[kPer], c0[kPer], c1[kPer], c2[kPer], Dv[kPer], bv[kPer];
+  // ---- loads
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int craw_i = base + slot + kChannelsPerBlock * k;
+    live[k] = craw_i < nchan;
+    const int c = live[k] ? craw_i : nchan - 1;
+    const int b = c / p.dim;
+    const int d = c - b * p.dim;
+    cc[k] = c;
+    const int64_t c64 = c;
+    h4[k] = *reinterpret_cast<const float4*>(p.state + c64 * 16 + 4 * j);
+    a4[k] = *reinterpret_cast<const float4*>(p.A + static_cast<int64_t>(d) * 16 + 4 * j);
+    w4[k] = *reinterpret_cast<const float4*>(p.conv_w + static_cast<int64_t>(d) * 4);
+    braw[k] = *reinterpret_cast<const uint2*>(static_cast<const IO*>(p.B) + static_cast<int64_t>(b) * 16 + 4 * j);
+    craw[k] = *reinterpret_cast<const uint2*>(static_cast<const IO*>(p.C) + static_cast<int64_t>(b) * 16 + 4 * j);
+    xv[k] = ld_io<IO>(p.x, c64);
+    dv[k] = ld_io<IO>(p.delta, c64);
+    zv[k] = p.z ? ld_io<IO>(p.z, c64) : 0.0f;
+    c0[k] = p.conv_state[c64 * 3 + 0];
+    c1[k] = p.conv_state[c64 * 3 + 1];
+    c2[k] = p.conv_state[c64 * 3 + 2];
+    Dv[k] = p.D ? p.D[d] : 0.0f;
+    bv[k] = p.bias ? p.bias[d] : 0.0f;
+  }
+  // ---- arithmetic
+  float yk[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const float4 w = w4[k];
+    const float s = fmaf(w.w, xv[k], fmaf(w.z, c2[k], fmaf(w.y, c1[k], w.x * c0[k])));
+    const float u = silu_fast(s);
+    const float v = dv[k] + bv[k];
+    const float dl = p.softplus ? softplus_fast(v) : v;
+    const float wu = dl * u;
+    const float av[4] = {a4[k].x, a4[k].y, a4[k].z, a4[k].w};
+    float hv[4] = {h4[k].x, h4[k].y, h4[k].z, h4[k].w};
+    const float bb[4] = {bf16lo_to_f32(braw[k].x), bf16hi_to_f32(braw[k].x), bf16lo_to_f32(braw[k].y),
+                         bf16hi_to_f32(braw[k].y)};
+    const float cv[4] = {bf16lo_to_f32(craw[k].x), bf16hi_to_f32(craw[k].x), bf16lo_to_f32(craw[k].y),
+                         bf16hi_to_f32(craw[k].y)};
+    float py = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float a = ex2_approx(dl * av[i] * kLog2e);
+      hv[i] = fmaf(a, hv[i], wu * bb[i]);
+      py = fmaf(cv[i], hv[i], py);
+    }
+    h4[k] = make_float4(hv[0], hv[1], hv[2], hv[3]);
+    py += __shfl_xor_sync(0xffffffffu, py, 1);
+    py += __shfl_xor_sync(0xffffffffu, py, 2);
+    float y = fmaf(Dv[k], u, py);
+    if (p.z) y *= silu_fast(zv[k]);
+    yk[k] = y;
+  }
+  // ---- stores (every lane read its channel's old conv window in the load phase)
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    if (!live[k]) continue;
+    const int64_t c64 = cc[k];
+    *reinterpret_cast<float4*>(p.state + c64 * 16 + 4 * j) = h4[k];
+    if (j < 3) p.conv_state[c64 * 3 + j] = j == 0 ? c1[k] : (j == 1 ? c2[k] : xv[k]);
+    if (j == 0) static_cast<IO*>(p.y)[c64] = IoTraits<IO>::from_f32(yk[k]);
+  }
+}
+
 template <typename IO>
 cudaError_t launch(const DecodeParams& p, cudaStream_t stream) {
   const int64_t nchan = static_cast<int64_t>(p.batch) * p.dim;
+  if (sizeof(IO) == 2 && p.vec16) {
+    const unsigned blocks =
+        static_cast<unsigned>((nchan + kChannelsPerBlock * kPer - 1) / (kChannelsPerBlock * kPer));
+    state_update_bf16_kernel<<<blocks, kThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+  }
   const unsigned blocks = static_cast<unsigned>((nchan + kChannelsPerBlock - 1) / kChannelsPerBlock);
   if (p.vec16) state_update_kernel<IO, true><<<blocks, kThreads, 0, stream>>>(p);
   else state_update_kernel<IO, false><<<blocks, kThreads, 0, stream>>>(p);

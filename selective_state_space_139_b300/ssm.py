@@ -73,6 +73,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ssm_state_update.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, vp]
     lib.ssm_scan_fwd_describe.restype = i32
     lib.ssm_scan_fwd_describe.argtypes = [i32, i32, i32, i64, i32, ctypes.POINTER(ScanOptions), ctypes.POINTER(ScanPlan)]
+    lib.ssm_causal_conv1d_fwd.restype = i32
+    lib.ssm_causal_conv1d_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i64, i32, i32, i32, vp]
     lib.ssm_device_status.restype = i32
     lib.ssm_device_status.argtypes = [vp]
     if path == _build.LIB:
@@ -230,6 +232,32 @@ def selective_state_update(x_t: torch.Tensor, delta_t: torch.Tensor, A: torch.Te
                                   _stream_handle(stream))
     _check(lib, st)
     return y
+
+
+def causal_conv1d_fwd(x: torch.Tensor, conv_w: torch.Tensor, conv_state: Optional[torch.Tensor] = None,
+                      silu: bool = True, return_final_state: bool = True, out: Optional[torch.Tensor] = None,
+                      final_state: Optional[torch.Tensor] = None, stream=None
+                      ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Causal depthwise conv (width 4) + SiLU over x (batch, dim, L) with weights (dim, 4) and an optional
+    incoming conv state (batch, dim, 3).  Returns (u, final conv state)."""
+    lib = load_library()
+    batch, dim, L = x.shape
+    K = conv_w.shape[1]
+    dev = x.device
+    _need(x, "x", (batch, dim, L), x.dtype, dev)
+    _need(conv_w, "conv_w", (dim, K), torch.float32, dev)
+    _need(conv_state, "conv_state", (batch, dim, K - 1), torch.float32, dev, optional=True)
+    u = torch.empty_like(x) if out is None else out
+    _need(u, "out", (batch, dim, L), x.dtype, dev)
+    if return_final_state and final_state is None:
+        final_state = torch.empty((batch, dim, K - 1), dtype=torch.float32, device=dev)
+    if final_state is not None:
+        _need(final_state, "final_state", (batch, dim, K - 1), torch.float32, dev)
+    with torch.cuda.device(dev):
+        st = lib.ssm_causal_conv1d_fwd(_ptr(x), _ptr(conv_w), _ptr(conv_state), _ptr(u), _ptr(final_state), batch, dim, L,
+                                       K, int(bool(silu)), _io_code(x.dtype), _stream_handle(stream))
+    _check(lib, st)
+    return u, final_state
 
 
 def device_status(stream=None) -> int:

@@ -112,3 +112,14 @@ def test_state_update_rejects_bad_arguments_on_host(lib):
     assert _upd(lib, x=P + 1) == ssm.SSM_ERR_INVALID_ARG
     assert _upd(lib, y=P + 0x5000000) == ssm.SSM_ERR_INVALID_ARG          # y aliases state
     assert _upd(lib, state=P + 0x2000000) == ssm.SSM_ERR_INVALID_ARG      # state aliases A
+
+
+def test_conv1d_rejects_bad_arguments_on_host(lib):
+    f = lib.ssm_causal_conv1d_fwd
+    assert f(P, P + 0x1000000, None, P + 0x2000000, None, 2, 8, 64, 3, 1, ssm.SSM_BF16, None) == ssm.SSM_ERR_UNSUPPORTED
+    assert f(P, None, None, P + 0x2000000, None, 2, 8, 64, 4, 1, ssm.SSM_BF16, None) == ssm.SSM_ERR_INVALID_ARG
+    assert f(P, P + 0x1000000, None, P + 0x10, None, 2, 8, 64, 4, 1, ssm.SSM_BF16, None) == ssm.SSM_ERR_INVALID_ARG
+    assert f(P + 1, P + 0x1000000, None, P + 0x2000000, None, 2, 8, 64, 4, 1, ssm.SSM_BF16, None) == ssm.SSM_ERR_INVALID_ARG
+    # the outgoing state may not alias the incoming one
+    assert f(P, P + 0x1000000, P + 0x3000000, P + 0x2000000, P + 0x3000000, 2, 8, 64, 4, 1, ssm.SSM_BF16,
+             None) == ssm.SSM_ERR_INVALID_ARG

@@ -1,0 +1,97 @@
+"""GPU parity of the causal depthwise conv1d + SiLU prefill kernel against the fp64 oracle
+(pinned to numpy.convolve in the oracle tests).  The outgoing conv state holds raw inputs, so it
+must match exactly."""
+import numpy as np
+import pytest
+import torch
+
+from selective_state_space_139_b300 import ssm
+from tests._helpers import max_rel_err, to64
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def _dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")
+
+
+def _inputs(batch, dim, L, dtype, seed, with_state, dev):
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    x = torch.randn((batch, dim, L), generator=g, device=dev).to(dtype)
+    w = 0.5 * torch.randn((dim, 4), generator=g, device=dev)
+    st = torch.randn((batch, dim, 3), generator=g, device=dev).to(dtype).float() if with_state else None
+    return x, w, st
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("shape", [(2, 130, 256), (1, 64, 33), (3, 20, 1), (1, 5, 2), (2, 48, 8), (1, 16, 3)])
+@pytest.mark.parametrize("with_state", [False, True])
+@pytest.mark.parametrize("silu", [True, False])
+def test_conv1d_every_element(shape, dtype, with_state, silu):
+    dev = _dev()
+    b, d, L = shape
+    x, w, st = _inputs(b, d, L, dtype, L * 7 + d, with_state, dev)
+    u, st_out = ssm.causal_conv1d_fwd(x, w, st, silu=silu)
+    torch.cuda.synchronize()
+    ru, rst = oracle.causal_conv1d(to64(x).reshape(b * d, L), np.tile(to64(w), (b, 1)),
+                                   None if st is None else to64(st).reshape(b * d, 3), silu=silu)
+    tol = 2e-5 if dtype == torch.float32 else 1e-2
+    assert max_rel_err(to64(u).reshape(b * d, L), ru) <= tol
+    np.testing.assert_array_equal(to64(st_out).reshape(b * d, 3), rst)
+
+
+def test_conv1d_mamba28b_rows_sampled():
+    dev = _dev()
+    x, w, st = _inputs(4, 5120, 4096, torch.bfloat16, 3, True, dev)
+    u, st_out = ssm.causal_conv1d_fwd(x, w, st)
+    torch.cuda.synchronize()
+    rows = [(0, 0), (0, 5119), (3, 17), (2, 4096), (1, 2500), (3, 5119)]
+    bi = torch.tensor([r[0] for r in rows])
+    di = torch.tensor([r[1] for r in rows])
+    ru, rst = oracle.causal_conv1d(to64(x[bi, di]), to64(w[di]), to64(st[bi, di]))
+    assert max_rel_err(to64(u[bi, di]), ru) <= 1e-2
+    np.testing.assert_array_equal(to64(st_out[bi, di]), rst)
+    assert torch.isfinite(u).all()
+
+
+def test_conv_then_scan_then_decode_equals_one_prefill():
+    """Prefill of L1 tokens on the GPU (conv kernel, then the scan), then L2 decode steps from the
+    conv state and SSM state it produced, equals the oracle's single prefill of L1 + L2 tokens.
+    Float32 io: the only storage point between the kernels is u, kept in the io dtype, and the
+    oracle chain rounds its u to float32 at the same point (with bf16 io that rounding alone moves
+    near-zero outputs by more than the metric's floor allows; the bf16 kernels are checked one by
+    one and by the 1000-token decode workload)."""
+    from selective_state_space_139_b300 import workloads as W
+    dev = _dev()
+    batch, dim, N, L1, L2 = 2, 192, 16, 640, 24
+    wk = W.DecodeWorkload("t", batch, dim, N, 4, L1 + L2, "f32", seed=91)
+    inp = W.make_decode_inputs(wk, device=dev)
+    x = inp["x"][:L1].permute(1, 2, 0).contiguous()
+    u, conv_state = ssm.causal_conv1d_fwd(x, inp["conv_w"])
+    per = lambda k: inp[k][:L1].permute(1, 2, 0).contiguous()
+    y1, state = ssm.selective_scan_fwd(u, per("delta"), inp["A"], per("B"), per("C"), D=inp["D"], z=per("z"),
+                                       delta_bias=inp["delta_bias"])
+    ys = torch.empty_like(inp["x"][L1:])
+    for t in range(L2):
+        ssm.selective_state_update(inp["x"][L1 + t], inp["delta"][L1 + t], inp["A"], inp["B"][L1 + t],
+                                   inp["C"][L1 + t], inp["D"], inp["z"][L1 + t], state, conv_state, inp["conv_w"],
+                                   delta_bias=inp["delta_bias"], out=ys[t])
+    torch.cuda.synchronize()
+    # oracle: conv over all L1 + L2 tokens, u of the first L1 rounded to float32 (the storage point),
+    # one scan over the whole stream
+    L = L1 + L2
+    xs = to64(inp["x"]).transpose(1, 2, 0).reshape(batch * dim, L)
+    ru, rtail = oracle.causal_conv1d(xs, np.tile(to64(inp["conv_w"]), (batch, 1)))
+    ru[:, :L1] = ru[:, :L1].astype(np.float32).astype(np.float64)
+    f = lambda k: to64(inp[k]).transpose(1, 2, 0)
+    ry, rh = oracle.selective_scan(ru.reshape(batch, dim, L), f("delta"), to64(inp["A"]), f("B"), f("C"),
+                                   D=to64(inp["D"]), z=f("z"), delta_bias=to64(inp["delta_bias"]))
+    got = torch.cat([y1, ys.permute(1, 2, 0)], dim=2)
+    assert max_rel_err(to64(got), ry) <= 2e-5
+    assert max_rel_err(to64(state), rh) <= 2e-5
+    np.testing.assert_array_equal(to64(conv_state).reshape(batch * dim, 3), rtail)
