@@ -18,6 +18,8 @@ What it computes (page title, section):
 * ``causal_conv1d`` -- the depthwise causal conv (width K, K-1 leading pad values) with SiLU.
 * ``state_update`` -- one decode step with the conv cache and the SSM cache ("Модуль 8", §6, §14).
 * ``compose_affine`` -- (a2, b2) ∘ (a1, b1) = (a2 a1, a2 b1 + b2), "later after earlier".
+* ``scan_backward`` -- gradients of sum(dy * y) by reverse-mode differentiation of the recurrence
+  (the pages' hardware-aware scan recomputes states for its backward; here the plain form).
 
 Pins: every function is checked in ``tests/test_oracle_pins.py`` against closed forms, brute
 force and the pages' worked examples (see the test module's docstring for the list).
@@ -67,6 +69,10 @@ def _load():
         lib.oracle_state_update.argtypes = [_D, _D, _D, _D, _D, _D, _D, _D, ctypes.c_int, _D, _D, _D,
                                             _D, _I64, ctypes.c_int64, ctypes.c_int, ctypes.c_int]
         lib.oracle_state_update.restype = ctypes.c_int
+        lib.oracle_scan_backward.argtypes = [_D, _D, _D, _D, _D, _D, _D, _D, ctypes.c_int, _D, _I64, _D, _D, _D, _D,
+                                             _D, _D, _D, _D, _D, ctypes.c_int64, ctypes.c_int, ctypes.c_int64,
+                                             ctypes.c_int]
+        lib.oracle_scan_backward.restype = ctypes.c_int
         lib.oracle_compose_affine.argtypes = [ctypes.c_double] * 4 + [_D, _D]
         lib.oracle_compose_affine.restype = None
         _lib = lib
@@ -223,3 +229,45 @@ def state_update(x_t, delta_t, A, B_t, C_t, bidx, state, conv_state, conv_w, D=N
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return y, st, cs
+
+
+def scan_backward(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softplus: bool = True, h0=None,
+                  threads: int = 0):
+    """Gradients of sum(dy * y) for the full-tensor scan (Δ·B input term).  Shapes as in
+    ``selective_scan``; returns a dict with du, ddelta, dz (batch, dim, L), dA (dim, N), dB, dC
+    (batch, N, L), dD, ddelta_bias (dim), summed over the batch where a parameter is shared."""
+    u = np.asarray(u, dtype=np.float64)
+    batch, dim, L = u.shape
+    A_c, D_c, b_c, z_c, h_c, bidx = _expand(u, A, D, delta_bias, z, h0)
+    n = batch * dim
+    N = A_c.shape[1]
+    uu = _f64(u.reshape(n, L))
+    dl = _f64(np.asarray(delta, np.float64).reshape(n, L))
+    A_c = _f64(A_c)
+    B = _f64(B)
+    C = _f64(C)
+    D_c = _f64(D_c)
+    z_c = _f64(z_c)
+    b_c = _f64(b_c)
+    h_c = _f64(h_c)
+    dyc = _f64(np.asarray(dy, np.float64).reshape(n, L))
+    bidx = np.ascontiguousarray(bidx)
+    du = np.empty((n, L))
+    dd = np.empty((n, L))
+    dz = np.empty((n, L)) if z_c is not None else None
+    dA = np.empty((n, N))
+    dD = np.empty(n)
+    dbias = np.empty(n)
+    dB = np.empty((n, N, L))
+    dC = np.empty((n, N, L))
+    rc = _load().oracle_scan_backward(_p(uu), _p(dl), _p(A_c), _p(B), _p(C), _p(D_c), _p(z_c), _p(b_c),
+                                      int(bool(delta_softplus)), _p(h_c), bidx.ctypes.data_as(_I64), _p(dyc), _p(du),
+                                      _p(dd), _p(dz), _p(dA), _p(dD), _p(dbias), _p(dB), _p(dC), n, N, L, threads)
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    out = {"du": du.reshape(batch, dim, L), "ddelta": dd.reshape(batch, dim, L),
+           "dz": None if dz is None else dz.reshape(batch, dim, L),
+           "dA": dA.reshape(batch, dim, N).sum(0), "dD": dD.reshape(batch, dim).sum(0),
+           "ddelta_bias": dbias.reshape(batch, dim).sum(0),
+           "dB": dB.reshape(batch, dim, N, L).sum(1), "dC": dC.reshape(batch, dim, N, L).sum(1)}
+    return out

@@ -340,3 +340,123 @@ ORACLE_API int oracle_state_update(const double* x_t, const double* delta_t, con
   }
   return 0;
 }
+
+/* ------------------------------------------------------------------------------------
+ * Backward of the selective scan (reverse-mode differentiation of the recurrence above).
+ * For one channel, with v_t = Δ_raw_t + bias, Δ_t = softplus(v_t) (or v_t), Ā = exp(Δ A),
+ * b_t = Δ_t B_t x_t, h_t = Ā_t ⊙ h_{t-1} + b_t, s_t = C_t·h_t + D x_t, y_t = s_t SiLU(z_t), and an
+ * upstream gradient dy:
+ *   ds_t   = dy_t SiLU(z_t);            dz_t = dy_t s_t SiLU'(z_t),  SiLU'(z) = σ(z)(1 + z(1 - σ(z)))
+ *   dh_t   = ds_t C_t + Ā_{t+1} ⊙ dh_{t+1}   (from the last step backwards; nothing after L-1)
+ *   dC_t  += ds_t h_t;   dB_t += dh_t Δ_t x_t
+ *   dΔ_t   = Σ_n dh_{t,n} (h_{t-1,n} Ā_{t,n} A_n + B_{t,n} x_t)
+ *   dA_n  += Σ_t dh_{t,n} h_{t-1,n} Ā_{t,n} Δ_t
+ *   dx_t   = ds_t D + Σ_n dh_{t,n} Δ_t B_{t,n};   dD += ds_t x_t
+ *   dv_t   = dΔ_t σ(v_t) (softplus' = sigmoid), or dΔ_t without softplus;  dΔ_raw_t = dv_t;  dbias += dv_t
+ * The Δ·B input term is differentiated (the ZOH variant is not).  Per channel c the results are
+ * dx, dΔ_raw, dz (n, L); dA (n, N); dD, dbias (n); and this channel's contributions to dB and dC,
+ * (n, N, L) -- the caller sums those over the channels of each batch row.
+ * ---------------------------------------------------------------------------------- */
+typedef struct {
+  const scan_problem* fwd;
+  const double* dy;   /* (n, L) */
+  double* du;         /* (n, L) */
+  double* ddelta;     /* (n, L) */
+  double* dz;         /* (n, L) or NULL when there is no gate */
+  double* dA;         /* (n, N) */
+  double* dD;         /* (n) */
+  double* dbias;      /* (n) */
+  double* dB;         /* (n, N, L) per-channel contribution */
+  double* dC;         /* (n, N, L) per-channel contribution */
+} bwd_problem;
+
+static double sigmoid(double v) { return 1.0 / (1.0 + exp(-v)); }
+
+static void backward_channel(const bwd_problem* q, int64_t c) {
+  const scan_problem* p = q->fwd;
+  const int N = p->N;
+  const int64_t L = p->L;
+  const double* Bb = p->B + p->bidx[c] * (int64_t)N * L;
+  const double* Cb = p->C + p->bidx[c] * (int64_t)N * L;
+  /* forward, keeping every state (h[t] = state after step t; hs[0] = initial) */
+  double* hs = (double*)malloc(sizeof(double) * (size_t)(L + 1) * N);
+  double* sv = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+  for (int n = 0; n < N; ++n) hs[n] = p->h0 ? p->h0[c * N + n] : 0.0;
+  for (int64_t t = 0; t < L; ++t) {
+    double dlt = delta_at(p, c, t);
+    double x = p->u[c * L + t];
+    double s = 0.0;
+    for (int n = 0; n < N; ++n) {
+      double abar = exp(dlt * p->A[c * N + n]);
+      double h = abar * hs[t * N + n] + dlt * Bb[(int64_t)n * L + t] * x;
+      hs[(t + 1) * N + n] = h;
+      s += Cb[(int64_t)n * L + t] * h;
+    }
+    if (p->D) s += p->D[c] * x;
+    sv[t] = s;
+  }
+  /* backward */
+  double dh[64], dAacc[64];
+  for (int n = 0; n < N; ++n) { dh[n] = 0.0; dAacc[n] = 0.0; }
+  double dD = 0.0, dbias = 0.0;
+  for (int64_t t = L - 1; t >= 0; --t) {
+    double dlt = delta_at(p, c, t);
+    double x = p->u[c * L + t];
+    double dyt = q->dy[c * L + t];
+    double ds = dyt;
+    if (p->z) {
+      double zz = p->z[c * L + t];
+      double sg = sigmoid(zz);
+      ds = dyt * silu(zz);
+      q->dz[c * L + t] = dyt * sv[t] * sg * (1.0 + zz * (1.0 - sg));
+    }
+    double dx = p->D ? ds * p->D[c] : 0.0;
+    dD += ds * x;
+    double ddl = 0.0;
+    for (int n = 0; n < N; ++n) {
+      double a = p->A[c * N + n];
+      double abar = exp(dlt * a);
+      double bn = Bb[(int64_t)n * L + t];
+      double cn = Cb[(int64_t)n * L + t];
+      /* dh_t = ds_t C_t + (Ā_{t+1} dh_{t+1}); the second term was folded into dh at step t+1 */
+      dh[n] += ds * cn;
+      q->dC[(c * N + n) * L + t] = ds * hs[(t + 1) * N + n];
+      q->dB[(c * N + n) * L + t] = dh[n] * dlt * x;
+      double hprev = hs[t * N + n];
+      ddl += dh[n] * (hprev * abar * a + bn * x);
+      dAacc[n] += dh[n] * hprev * abar * dlt;
+      dx += dh[n] * dlt * bn;
+      dh[n] *= abar;   /* carried to step t-1: Ā_t ⊙ dh_t */
+    }
+    double v = p->delta[c * L + t] + (p->bias ? p->bias[c] : 0.0);
+    double dv = p->softplus_flag ? ddl * sigmoid(v) : ddl;
+    q->du[c * L + t] = dx;
+    q->ddelta[c * L + t] = dv;
+    dbias += dv;
+  }
+  for (int n = 0; n < N; ++n) q->dA[c * N + n] = dAacc[n];
+  q->dD[c] = dD;
+  q->dbias[c] = dbias;
+  free(hs);
+  free(sv);
+}
+
+static void backward_fn(const void* q, int64_t c) { backward_channel((const bwd_problem*)q, c); }
+
+ORACLE_API int oracle_scan_backward(const double* u, const double* delta, const double* A, const double* B,
+                                    const double* C, const double* D, const double* z, const double* bias,
+                                    int softplus_flag, const double* h0, const int64_t* bidx, const double* dy,
+                                    double* du, double* ddelta, double* dz, double* dA, double* dD,
+                                    double* dbias, double* dB, double* dC, int64_t n, int N, int64_t L,
+                                    int threads) {
+  scan_problem p;
+  /* the forward outputs are not written here; du stands in for the y pointer the check wants */
+  if (fill_problem(&p, u, delta, A, B, C, D, z, bias, softplus_flag, 0, h0, bidx, du, NULL, n, N, L))
+    return -1;
+  if (!dy || !du || !ddelta || !dA || !dD || !dbias || !dB || !dC || (z && !dz)) return -1;
+  bwd_problem q;
+  q.fwd = &p; q.dy = dy; q.du = du; q.ddelta = ddelta; q.dz = dz; q.dA = dA; q.dD = dD; q.dbias = dbias;
+  q.dB = dB; q.dC = dC;
+  run_channels(backward_fn, &q, n, threads);
+  return 0;
+}

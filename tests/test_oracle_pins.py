@@ -12,7 +12,10 @@
 * invariants: zero input gives zero output and state; z = 0 gives y = 0; softplus(v) - softplus(-v) = v
   and SiLU(z) - SiLU(-z) = z; Δ = 0 keeps h; Δ|A| ≫ 1 resets h to ΔBu;
 * the chunked (aggregate/carry/re-run) form equals the sequential one for every chunk length;
-* a prefill followed by decode steps equals one longer prefill ("Модуль 8", §6/§14 caches).
+* a prefill followed by decode steps equals one longer prefill ("Модуль 8", §6/§14 caches);
+* the backward (reverse-mode) oracle against central finite differences of sum(dy * y) for every
+  input, with and without softplus, gate and skip, and against the exact gradient of the A = 0,
+  no-gate case (y is then linear in u).
 
 Each mistake a plausible bug would make (a dropped D term, a sign error in the exponent, reading
 before updating, swapping B and C, the gate before the D skip, the conv tap order) fails at
@@ -315,6 +318,63 @@ def test_prefill_then_decode_equals_longer_prefill():
     y = np.concatenate([y1, np.stack(ys, -1)], -1)
     np.testing.assert_allclose(y, y_ref, rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(h.reshape(batch, dim, N), h_ref, rtol=1e-12, atol=1e-13)
+
+
+# ---------------------------------------------------------------- backward: finite differences
+
+@pytest.mark.parametrize("softplus,gate,skip", [(True, True, True), (False, False, False), (True, False, True)])
+def test_backward_matches_central_differences(softplus, gate, skip):
+    rng = _rng(11)
+    b, d, N, L = 2, 3, 5, 12
+    u = rng.standard_normal((b, d, L))
+    dl = rng.standard_normal((b, d, L)) if softplus else rng.uniform(0.05, 0.5, (b, d, L))
+    A = -np.exp(rng.standard_normal((d, N)))
+    B = rng.standard_normal((b, N, L))
+    C = rng.standard_normal((b, N, L))
+    D = rng.standard_normal(d) if skip else None
+    z = rng.standard_normal((b, d, L)) if gate else None
+    bias = 0.3 * rng.standard_normal(d) if softplus else None
+    dy = rng.standard_normal((b, d, L))
+    g = oracle.scan_backward(u, dl, A, B, C, dy, D=D, z=z, delta_bias=bias, delta_softplus=softplus)
+    base = dict(u=u, delta=dl, A=A, B=B, C=C, D=D, z=z, delta_bias=bias, delta_softplus=softplus)
+
+    def loss(**kw):
+        y, _ = oracle.selective_scan(**dict(base, **kw))
+        return float((y * dy).sum())
+
+    eps = 1e-6
+    checks = [("u", "du"), ("delta", "ddelta"), ("A", "dA"), ("B", "dB"), ("C", "dC")]
+    if gate:
+        checks.append(("z", "dz"))
+    if skip:
+        checks.append(("D", "dD"))
+    if softplus:
+        checks.append(("delta_bias", "ddelta_bias"))
+    for name, key in checks:
+        arr = base[name]
+        for _ in range(6):
+            idx = tuple(int(rng.integers(n)) for n in arr.shape)
+            hi, lo = arr.copy(), arr.copy()
+            hi[idx] += eps
+            lo[idx] -= eps
+            fd = (loss(**{name: hi}) - loss(**{name: lo})) / (2 * eps)
+            assert abs(fd - g[key][idx]) <= 1e-7 * max(1.0, abs(fd)), (name, idx, fd, g[key][idx])
+
+
+def test_backward_of_a_linear_input_is_exact():
+    # y is linear in u when Δ does not depend on u: with A = 0, no gate and no D,
+    # dL/du_t = Σ_{s >= t} dy_s Δ_t C_s·B_t exactly (the prefix-sum closed form read backwards)
+    rng = _rng(12)
+    L, N = 10, 3
+    u = rng.standard_normal((1, 1, L))
+    dl = rng.uniform(0.1, 1.0, (1, 1, L))
+    B = rng.standard_normal((1, N, L))
+    C = rng.standard_normal((1, N, L))
+    dy = rng.standard_normal((1, 1, L))
+    g = oracle.scan_backward(u, dl, np.zeros((1, N)), B, C, dy, delta_softplus=False)
+    ref = np.array([sum(dy[0, 0, s] * dl[0, 0, t] * float(C[0, :, s] @ B[0, :, t]) for s in range(t, L))
+                    for t in range(L)])
+    np.testing.assert_allclose(g["du"][0, 0], ref, rtol=1e-12, atol=1e-13)
 
 
 # ---------------------------------------------------------------- the pins catch planted mistakes
