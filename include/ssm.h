@@ -201,6 +201,33 @@ SSM_API ssm_status ssm_causal_conv1d_fwd(const void* x, const float* conv_w, con
                                          int apply_silu, ssm_dtype io_dtype, cudaStream_t stream);
 
 /*
+ * Backward of the prefill scan: the gradients of sum(dy ⊙ y) with respect to every input of
+ * ssm_scan_fwd (zero initial state, Δ·B input term).  The pages define only the forward recurrence;
+ * this is its chain rule, computed with the states recomputed from checkpoints every 8 steps instead
+ * of stored (the recomputation of the hardware-aware scan: "Mamba: линейная альтернатива
+ * трансформеру", "Почему selectivity ломает старый трюк со свёрткой"; the ai.pinkoculture.com concept
+ * page, 硬件感知的实现).
+ *   inputs      : as ssm_scan_fwd, plus dy (batch, dim, seqlen) io_dtype, the gradient of y
+ *   du, ddelta  : (batch, dim, seqlen) io_dtype; ddelta is the gradient of the raw Δ input (before
+ *                 delta_bias and softplus)
+ *   dz          : (batch, dim, seqlen) io_dtype; required when z is given, NULL when z is NULL
+ *   dA          : (dim, dstate) float32, summed over the batch
+ *   dB, dC      : (batch, dstate, seqlen) float32, summed over the channels
+ *   dD          : (dim) float32 summed over the batch, or NULL (not computed)
+ *   ddelta_bias : (dim) float32 summed over the batch, or NULL (not computed)
+ * All outputs are overwritten (the call zeroes the accumulated ones itself).  The cross-channel sums
+ * use atomic adds, so their last bits can differ from run to run.  Float32 io is computed in double.
+ * workspace: ssm_scan_bwd_workspace_size() bytes, 256-byte aligned, no initial contents required.
+ */
+SSM_API size_t ssm_scan_bwd_workspace_size(int batch, int dim, int dstate, int64_t seqlen, ssm_dtype io_dtype);
+
+SSM_API ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                                const float* D, const void* z, const float* delta_bias, int softplus_flag,
+                                const void* dy, void* du, void* ddelta, void* dz, float* dA, float* dB, float* dC,
+                                float* dD, float* ddelta_bias, int batch, int dim, int dstate, int64_t seqlen,
+                                ssm_dtype io_dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Reads and clears the device status word (synchronises `stream`).  Returns SSM_OK, SSM_ERR_TIMEOUT
  * if a kernel gave up a bounded wait since the last call, or SSM_ERR_CUDA.
  */

@@ -231,6 +231,54 @@ def state_update(x_t, delta_t, A, B_t, C_t, bidx, state, conv_state, conv_w, D=N
     return y, st, cs
 
 
+def scan_backward_channels(u, delta, A, B, C, bidx, dy, D=None, z=None, delta_bias=None,
+                           delta_softplus: bool = True, h0=None, threads: int = 0, block: int = 512):
+    """Backward in channel-list form: rows ``u, delta, dy, z`` (n, L), ``A`` (n, N), ``D, delta_bias``
+    (n), ``h0`` (n, N), channel c reading ``B[bidx[c]], C[bidx[c]]`` (batch, N, L).  Returns per-channel
+    du, ddelta, dz (n, L), dA (n, N), dD, ddelta_bias (n), and dB, dC (batch, N, L) summed over the listed
+    channels of each batch row.  Channels are processed ``block`` at a time to bound memory."""
+    uu = np.ascontiguousarray(u, dtype=np.float64)
+    n, L = uu.shape
+    B = _f64(B)
+    C = _f64(C)
+    batch, N = B.shape[0], B.shape[1]
+    A = np.ascontiguousarray(A, dtype=np.float64)
+    dl = np.ascontiguousarray(delta, dtype=np.float64)
+    dyc = np.ascontiguousarray(dy, dtype=np.float64)
+    bidx = np.ascontiguousarray(bidx, dtype=np.int64)
+    opt = lambda a, shape: None if a is None else np.ascontiguousarray(np.asarray(a, np.float64).reshape(shape))
+    D = opt(D, (n,))
+    z = opt(z, (n, L))
+    delta_bias = opt(delta_bias, (n,))
+    h0 = opt(h0, (n, N))
+    out = {"du": np.empty((n, L)), "ddelta": np.empty((n, L)), "dz": None if z is None else np.empty((n, L)),
+           "dA": np.empty((n, N)), "dD": np.empty(n), "ddelta_bias": np.empty(n),
+           "dB": np.zeros((batch, N, L)), "dC": np.zeros((batch, N, L))}
+    for c0 in range(0, n, block):
+        c1 = min(n, c0 + block)
+        m = c1 - c0
+        sl = lambda a: None if a is None else np.ascontiguousarray(a[c0:c1])
+        dB = np.empty((m, N, L))
+        dC = np.empty((m, N, L))
+        du, dd, dA, dD, db = np.empty((m, L)), np.empty((m, L)), np.empty((m, N)), np.empty(m), np.empty(m)
+        dz = None if z is None else np.empty((m, L))
+        rc = _load().oracle_scan_backward(_p(sl(uu)), _p(sl(dl)), _p(sl(A)), _p(B), _p(C), _p(sl(D)), _p(sl(z)),
+                                          _p(sl(delta_bias)), int(bool(delta_softplus)), _p(sl(h0)),
+                                          sl(bidx).ctypes.data_as(_I64), _p(sl(dyc)), _p(du), _p(dd), _p(dz), _p(dA),
+                                          _p(dD), _p(db), _p(dB), _p(dC), m, N, L, threads)
+        if rc != 0:
+            raise ValueError("oracle rejected its arguments")
+        out["du"][c0:c1], out["ddelta"][c0:c1], out["dA"][c0:c1] = du, dd, dA
+        out["dD"][c0:c1], out["ddelta_bias"][c0:c1] = dD, db
+        if dz is not None:
+            out["dz"][c0:c1] = dz
+        bb = bidx[c0:c1]
+        for b in np.unique(bb):
+            out["dB"][b] += dB[bb == b].sum(0)
+            out["dC"][b] += dC[bb == b].sum(0)
+    return out
+
+
 def scan_backward(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softplus: bool = True, h0=None,
                   threads: int = 0):
     """Gradients of sum(dy * y) for the full-tensor scan (Δ·B input term).  Shapes as in
@@ -240,34 +288,11 @@ def scan_backward(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_
     batch, dim, L = u.shape
     A_c, D_c, b_c, z_c, h_c, bidx = _expand(u, A, D, delta_bias, z, h0)
     n = batch * dim
-    N = A_c.shape[1]
-    uu = _f64(u.reshape(n, L))
-    dl = _f64(np.asarray(delta, np.float64).reshape(n, L))
-    A_c = _f64(A_c)
-    B = _f64(B)
-    C = _f64(C)
-    D_c = _f64(D_c)
-    z_c = _f64(z_c)
-    b_c = _f64(b_c)
-    h_c = _f64(h_c)
-    dyc = _f64(np.asarray(dy, np.float64).reshape(n, L))
-    bidx = np.ascontiguousarray(bidx)
-    du = np.empty((n, L))
-    dd = np.empty((n, L))
-    dz = np.empty((n, L)) if z_c is not None else None
-    dA = np.empty((n, N))
-    dD = np.empty(n)
-    dbias = np.empty(n)
-    dB = np.empty((n, N, L))
-    dC = np.empty((n, N, L))
-    rc = _load().oracle_scan_backward(_p(uu), _p(dl), _p(A_c), _p(B), _p(C), _p(D_c), _p(z_c), _p(b_c),
-                                      int(bool(delta_softplus)), _p(h_c), bidx.ctypes.data_as(_I64), _p(dyc), _p(du),
-                                      _p(dd), _p(dz), _p(dA), _p(dD), _p(dbias), _p(dB), _p(dC), n, N, L, threads)
-    if rc != 0:
-        raise ValueError("oracle rejected its arguments")
-    out = {"du": du.reshape(batch, dim, L), "ddelta": dd.reshape(batch, dim, L),
-           "dz": None if dz is None else dz.reshape(batch, dim, L),
-           "dA": dA.reshape(batch, dim, N).sum(0), "dD": dD.reshape(batch, dim).sum(0),
-           "ddelta_bias": dbias.reshape(batch, dim).sum(0),
-           "dB": dB.reshape(batch, dim, N, L).sum(1), "dC": dC.reshape(batch, dim, N, L).sum(1)}
-    return out
+    g = scan_backward_channels(u.reshape(n, L), np.asarray(delta, np.float64).reshape(n, L), A_c, B, C, bidx,
+                               np.asarray(dy, np.float64).reshape(n, L), D=D_c, z=z_c, delta_bias=b_c,
+                               delta_softplus=delta_softplus, h0=h_c, threads=threads)
+    N = g["dA"].shape[1]
+    return {"du": g["du"].reshape(batch, dim, L), "ddelta": g["ddelta"].reshape(batch, dim, L),
+            "dz": None if g["dz"] is None else g["dz"].reshape(batch, dim, L),
+            "dA": g["dA"].reshape(batch, dim, N).sum(0), "dD": g["dD"].reshape(batch, dim).sum(0),
+            "ddelta_bias": g["ddelta_bias"].reshape(batch, dim).sum(0), "dB": g["dB"], "dC": g["dC"]}

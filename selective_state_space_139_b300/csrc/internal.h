@@ -88,6 +88,42 @@ struct ConvParams {
 // vec: L is a multiple of the 16-byte element count and x, u, w are 16-byte aligned
 cudaError_t conv1d_launch(const ConvParams& p, bool vec, cudaStream_t stream);
 
+// Backward of the prefill scan (scan_bwd.cu).  For bfloat16 io the cross-channel sums are
+// accumulated straight into the float32 outputs (acc_* == dA, dB, ...); for float32 io they are
+// accumulated in double in the workspace and converted at the end.
+struct BwdParams {
+  const void* u;
+  const void* delta;
+  const void* z;          // may be null
+  const void* B;
+  const void* C;
+  const float* A;
+  const float* D;         // may be null
+  const float* bias;      // may be null
+  const void* dy;
+  void* du;
+  void* ddelta;
+  void* dz;               // null iff z is null
+  float* dA;              // (dim, N)
+  float* dB;              // (batch, N, L)
+  float* dC;              // (batch, N, L)
+  float* dD;              // (dim) or null
+  float* dbias;           // (dim) or null
+  void* ckpt;             // (batch, dim, ceil(L / segment), 16) states, float (bf16 io) or double (f32 io)
+  void* acc_dA;
+  void* acc_dB;
+  void* acc_dC;
+  void* acc_dD;           // null when dD is null
+  void* acc_dbias;        // null when dbias is null
+  int batch, dim, N;
+  int64_t L;
+  int softplus;
+  int io_bf16;
+};
+
+int bwd_segment_steps();
+cudaError_t scan_bwd_launch(const BwdParams& p, cudaStream_t stream);
+
 // Sets the text returned by ssm_last_error_message() on the calling host thread (ssm_api.cu).
 void set_last_error(const char* fmt, ...);
 

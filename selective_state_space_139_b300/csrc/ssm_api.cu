@@ -531,3 +531,123 @@ ssm_status ssm_device_status(cudaStream_t stream) {
 }
 
 }  // extern "C"
+
+namespace {
+
+struct BwdLayout {
+  size_t ckpt = 0, acc_dA = 0, acc_dB = 0, acc_dC = 0, acc_dD = 0, acc_dbias = 0, total = 0;
+};
+
+// checkpoints (16 states per channel and segment), then for float32 io the double accumulators
+BwdLayout bwd_layout(int batch, int dim, int dstate, int64_t seqlen, ssm_dtype io) {
+  BwdLayout l;
+  const size_t ce = io == SSM_BF16 ? sizeof(float) : sizeof(double);
+  const int K = ssm::bwd_segment_steps();
+  const size_t nseg = static_cast<size_t>((seqlen + K - 1) / K);
+  size_t off = round_up(static_cast<size_t>(batch) * dim * nseg * 16 * ce, 256);
+  if (io == SSM_F32) {
+    l.acc_dA = off;
+    off += round_up(static_cast<size_t>(dim) * dstate * 8, 256);
+    l.acc_dB = off;
+    off += round_up(static_cast<size_t>(batch) * dstate * seqlen * 8, 256);
+    l.acc_dC = off;
+    off += round_up(static_cast<size_t>(batch) * dstate * seqlen * 8, 256);
+    l.acc_dD = off;
+    off += round_up(static_cast<size_t>(dim) * 8, 256);
+    l.acc_dbias = off;
+    off += round_up(static_cast<size_t>(dim) * 8, 256);
+  }
+  l.total = seqlen > 0 ? off : 0;
+  return l;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ssm_scan_bwd_workspace_size(int batch, int dim, int dstate, int64_t seqlen, ssm_dtype io_dtype) {
+  if (!sizes_ok(batch, dim, dstate, seqlen, io_dtype)) return 0;
+  return bwd_layout(batch, dim, dstate, seqlen, io_dtype).total;
+}
+
+ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                        const float* D, const void* z, const float* delta_bias, int softplus_flag, const void* dy,
+                        void* du, void* ddelta, void* dz, float* dA, float* dB, float* dC, float* dD,
+                        float* ddelta_bias, int batch, int dim, int dstate, int64_t seqlen, ssm_dtype io_dtype,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  g_err[0] = 0;
+  if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return fail(SSM_ERR_INVALID_ARG, "unknown io_dtype %d", io_dtype);
+  if (batch < 1 || dim < 1 || seqlen < 0 || dstate < 1)
+    return fail(SSM_ERR_INVALID_ARG, "bad sizes batch=%d dim=%d dstate=%d seqlen=%lld", batch, dim, dstate,
+                static_cast<long long>(seqlen));
+  if (dstate > 16) return fail(SSM_ERR_UNSUPPORTED, "dstate=%d > 16 is not supported", dstate);
+  if (batch > 65535) return fail(SSM_ERR_UNSUPPORTED, "batch=%d above 65535 is not supported", batch);
+  if (!A || !dA) return fail(SSM_ERR_INVALID_ARG, "null required pointer (A, dA)");
+  if (seqlen > 0 && (!u || !delta || !B || !C || !dy || !du || !ddelta || !dB || !dC))
+    return fail(SSM_ERR_INVALID_ARG, "null required pointer (u, delta, B, C, dy, du, ddelta, dB, dC)");
+  if ((z == nullptr) != (dz == nullptr)) return fail(SSM_ERR_INVALID_ARG, "dz must be given exactly when z is");
+  const size_t e = io_dtype == SSM_BF16 ? 2 : 4;
+  for (const void* q : {u, delta, z, B, C, dy, static_cast<const void*>(du), static_cast<const void*>(ddelta),
+                        static_cast<const void*>(dz)})
+    if (q && !aligned(q, e)) return fail(SSM_ERR_INVALID_ARG, "io pointer not aligned to its element size");
+  for (const void* q : {static_cast<const void*>(A), static_cast<const void*>(D), static_cast<const void*>(delta_bias),
+                        static_cast<const void*>(dA), static_cast<const void*>(dB), static_cast<const void*>(dC),
+                        static_cast<const void*>(dD), static_cast<const void*>(ddelta_bias)})
+    if (q && !aligned(q, 4)) return fail(SSM_ERR_INVALID_ARG, "float32 pointer not 4-byte aligned");
+  const size_t bdl = static_cast<size_t>(batch) * dim * seqlen * e;
+  const size_t bnl = static_cast<size_t>(batch) * dstate * seqlen * e;
+  const size_t bnl4 = static_cast<size_t>(batch) * dstate * seqlen * 4;
+  const size_t dn4 = static_cast<size_t>(dim) * dstate * 4;
+  const Range outs[] = {range_of(du, bdl), range_of(ddelta, bdl), range_of(dz, dz ? bdl : 0), range_of(dA, dn4),
+                        range_of(dB, bnl4), range_of(dC, bnl4), range_of(dD, dD ? dim * 4 : 0),
+                        range_of(ddelta_bias, ddelta_bias ? dim * 4 : 0)};
+  const Range ins[] = {range_of(u, bdl), range_of(delta, bdl), range_of(z, z ? bdl : 0), range_of(B, bnl),
+                       range_of(C, bnl), range_of(A, dn4), range_of(D, D ? dim * 4 : 0),
+                       range_of(delta_bias, delta_bias ? dim * 4 : 0), range_of(dy, bdl)};
+  for (const Range& o : outs)
+    for (const Range& i : ins)
+      if (overlap(o, i)) return fail(SSM_ERR_INVALID_ARG, "an output overlaps an input");
+  const int nouts = static_cast<int>(sizeof(outs) / sizeof(outs[0]));
+  for (int i = 0; i < nouts; ++i)
+    for (int j = i + 1; j < nouts; ++j)
+      if (overlap(outs[i], outs[j])) return fail(SSM_ERR_INVALID_ARG, "two outputs overlap");
+  const BwdLayout lay = bwd_layout(batch, dim, dstate, seqlen, io_dtype);
+  if (lay.total > 0) {
+    if (!workspace || workspace_bytes < lay.total)
+      return fail(SSM_ERR_INVALID_ARG, "workspace of %zu bytes required, %zu given", lay.total, workspace_bytes);
+    if (!aligned(workspace, 256)) return fail(SSM_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    const Range w = range_of(workspace, lay.total);
+    for (const Range& i : ins)
+      if (overlap(w, i)) return fail(SSM_ERR_INVALID_ARG, "workspace overlaps an input");
+    for (const Range& o : outs)
+      if (overlap(w, o)) return fail(SSM_ERR_INVALID_ARG, "workspace overlaps an output");
+  }
+  if (seqlen == 0) {
+    // no steps: every parameter gradient is zero
+    cudaError_t ce = cudaMemsetAsync(dA, 0, dn4, stream);
+    if (ce == cudaSuccess && dD) ce = cudaMemsetAsync(dD, 0, dim * 4, stream);
+    if (ce == cudaSuccess && ddelta_bias) ce = cudaMemsetAsync(ddelta_bias, 0, dim * 4, stream);
+    if (ce != cudaSuccess) return cuda_fail(ce, "seqlen 0 gradient clear");
+    return SSM_OK;
+  }
+  ssm::BwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.u = u; p.delta = delta; p.z = z; p.B = B; p.C = C; p.A = A; p.D = D; p.bias = delta_bias; p.dy = dy;
+  p.du = du; p.ddelta = ddelta; p.dz = dz; p.dA = dA; p.dB = dB; p.dC = dC; p.dD = dD; p.dbias = ddelta_bias;
+  p.batch = batch; p.dim = dim; p.N = dstate; p.L = seqlen;
+  p.softplus = softplus_flag != 0; p.io_bf16 = io_dtype == SSM_BF16;
+  char* ws = static_cast<char*>(workspace);
+  p.ckpt = ws + lay.ckpt;
+  if (io_dtype == SSM_BF16) {
+    p.acc_dA = dA; p.acc_dB = dB; p.acc_dC = dC; p.acc_dD = dD; p.acc_dbias = ddelta_bias;
+  } else {
+    p.acc_dA = ws + lay.acc_dA; p.acc_dB = ws + lay.acc_dB; p.acc_dC = ws + lay.acc_dC;
+    p.acc_dD = dD ? ws + lay.acc_dD : nullptr;
+    p.acc_dbias = ddelta_bias ? ws + lay.acc_dbias : nullptr;
+  }
+  cudaError_t ce = ssm::scan_bwd_launch(p, stream);
+  if (ce != cudaSuccess) return cuda_fail(ce, "scan backward launch");
+  return SSM_OK;
+}
+
+}  // extern "C"

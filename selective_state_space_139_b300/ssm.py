@@ -77,6 +77,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ssm_causal_conv1d_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i64, i32, i32, i32, vp]
     lib.ssm_device_status.restype = i32
     lib.ssm_device_status.argtypes = [vp]
+    lib.ssm_scan_bwd_workspace_size.restype = sz
+    lib.ssm_scan_bwd_workspace_size.argtypes = [i32, i32, i32, i64, i32]
+    lib.ssm_scan_bwd.restype = i32
+    lib.ssm_scan_bwd.argtypes = [vp] * 8 + [i32] + [vp] * 9 + [i32, i32, i32, i64, i32, vp, sz, vp]
     if path == _build.LIB:
         _lib = lib
     return lib
@@ -258,6 +262,52 @@ def causal_conv1d_fwd(x: torch.Tensor, conv_w: torch.Tensor, conv_state: Optiona
                                        K, int(bool(silu)), _io_code(x.dtype), _stream_handle(stream))
     _check(lib, st)
     return u, final_state
+
+
+def scan_bwd_workspace_size(batch: int, dim: int, dstate: int, seqlen: int, dtype=torch.bfloat16) -> int:
+    lib = load_library()
+    return int(lib.ssm_scan_bwd_workspace_size(batch, dim, dstate, seqlen, _io_code(dtype)))
+
+
+def selective_scan_bwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor, C: torch.Tensor,
+                       dy: torch.Tensor, D: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
+                       delta_bias: Optional[torch.Tensor] = None, delta_softplus: bool = True, *,
+                       workspace: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """Gradients of sum(dy * y) for the prefill scan (zero initial state).  Returns a dict with du,
+    ddelta, dz (batch, dim, L) in the io dtype (dz None without z), dA (dim, N), dB, dC (batch, N, L),
+    dD and ddelta_bias (dim,) in float32 (dD / ddelta_bias None when D / delta_bias is None)."""
+    lib = load_library()
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    dev = u.device
+    io = u.dtype
+    _need(u, "u", (batch, dim, L), io, dev)
+    _need(delta, "delta", (batch, dim, L), io, dev)
+    _need(z, "z", (batch, dim, L), io, dev, optional=True)
+    _need(A, "A", (dim, N), torch.float32, dev)
+    _need(B, "B", (batch, N, L), io, dev)
+    _need(C, "C", (batch, N, L), io, dev)
+    _need(dy, "dy", (batch, dim, L), io, dev)
+    _need(D, "D", (dim,), torch.float32, dev, optional=True)
+    _need(delta_bias, "delta_bias", (dim,), torch.float32, dev, optional=True)
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = {"du": torch.empty_like(u), "ddelta": torch.empty_like(u),
+         "dz": None if z is None else torch.empty_like(u),
+         "dA": torch.empty((dim, N), **f32), "dB": torch.empty((batch, N, L), **f32),
+         "dC": torch.empty((batch, N, L), **f32),
+         "dD": None if D is None else torch.empty((dim,), **f32),
+         "ddelta_bias": None if delta_bias is None else torch.empty((dim,), **f32)}
+    ws_bytes = int(lib.ssm_scan_bwd_workspace_size(batch, dim, N, L, _io_code(io)))
+    if ws_bytes and (workspace is None or workspace.numel() < ws_bytes):
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.ssm_scan_bwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+                              int(bool(delta_softplus)), _ptr(dy), _ptr(g["du"]), _ptr(g["ddelta"]), _ptr(g["dz"]),
+                              _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]), _ptr(g["ddelta_bias"]),
+                              batch, dim, N, L, _io_code(io), _ptr(workspace) if ws_bytes else None, ws_bytes,
+                              _stream_handle(stream))
+    _check(lib, st)
+    return g
 
 
 def device_status(stream=None) -> int:

@@ -143,6 +143,12 @@ def make_scan_inputs(w: ScanWorkload, device="cpu", seed: Optional[int] = None) 
     return out
 
 
+def make_cotangent(batch: int, dim: int, seqlen: int, dtype: torch.dtype, seed: int, device="cpu") -> torch.Tensor:
+    """dy (batch, dim, seqlen) ~ N(0, 1) in the io dtype: the incoming gradient of a backward call."""
+    g = _gen(seed * 104729 + 3, device)
+    return torch.randn((batch, dim, seqlen), generator=g, device=device, dtype=torch.float32).to(dtype).contiguous()
+
+
 def make_decode_inputs(w: DecodeWorkload, steps: Optional[int] = None, device="cpu",
                        seed: Optional[int] = None) -> Dict[str, torch.Tensor]:
     """Per-token inputs for ``steps`` tokens, stacked along a leading time axis:

@@ -123,3 +123,39 @@ def test_conv1d_rejects_bad_arguments_on_host(lib):
     # the outgoing state may not alias the incoming one
     assert f(P, P + 0x1000000, P + 0x3000000, P + 0x2000000, P + 0x3000000, 2, 8, 64, 4, 1, ssm.SSM_BF16,
              None) == ssm.SSM_ERR_INVALID_ARG
+
+
+def _bwd(lib, **kw):
+    a = dict(u=P, delta=P + 0x1000000, A=P + 0x2000000, B=P + 0x3000000, C=P + 0x4000000, D=None, z=None, bias=None,
+             softplus=1, dy=P + 0x5000000, du=P + 0x6000000, dd=P + 0x7000000, dz=None, dA=P + 0x8000000,
+             dB=P + 0x9000000, dC=P + 0xa000000, dD=None, dbias=None, batch=2, dim=8, dstate=16, seqlen=64,
+             io=ssm.SSM_BF16, ws=P + 0x10000000, wsb=1 << 24, stream=None)
+    a.update(kw)
+    return lib.ssm_scan_bwd(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"], a["bias"], a["softplus"],
+                            a["dy"], a["du"], a["dd"], a["dz"], a["dA"], a["dB"], a["dC"], a["dD"], a["dbias"],
+                            a["batch"], a["dim"], a["dstate"], a["seqlen"], a["io"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_scan_bwd_rejects_bad_arguments_on_host(lib):
+    assert _bwd(lib, dstate=17) == ssm.SSM_ERR_UNSUPPORTED
+    assert _bwd(lib, batch=0) == ssm.SSM_ERR_INVALID_ARG
+    assert _bwd(lib, io=5) == ssm.SSM_ERR_INVALID_ARG
+    assert _bwd(lib, dy=None) == ssm.SSM_ERR_INVALID_ARG
+    assert _bwd(lib, dA=None) == ssm.SSM_ERR_INVALID_ARG
+    assert _bwd(lib, z=P + 0xb000000) == ssm.SSM_ERR_INVALID_ARG                    # z without dz
+    assert _bwd(lib, dz=P + 0xb000000) == ssm.SSM_ERR_INVALID_ARG                   # dz without z
+    assert _bwd(lib, du=P + 1) == ssm.SSM_ERR_INVALID_ARG                           # misaligned
+    assert _bwd(lib, du=P + 0x10) == ssm.SSM_ERR_INVALID_ARG                        # du overlaps u
+    assert _bwd(lib, dB=P + 0xa000010) == ssm.SSM_ERR_INVALID_ARG                   # dB overlaps dC
+    assert _bwd(lib, wsb=16) == ssm.SSM_ERR_INVALID_ARG                             # short workspace
+    assert _bwd(lib, ws=P + 0x10000010) == ssm.SSM_ERR_INVALID_ARG                  # unaligned workspace
+    assert _bwd(lib, ws=P + 0x400) == ssm.SSM_ERR_INVALID_ARG                       # workspace overlaps u
+
+
+def test_scan_bwd_workspace_query(lib):
+    # bf16: one float checkpoint of 16 states per channel every 8 steps
+    assert lib.ssm_scan_bwd_workspace_size(2, 8, 16, 64, ssm.SSM_BF16) == 2 * 8 * 8 * 16 * 4
+    assert lib.ssm_scan_bwd_workspace_size(2, 8, 16, 0, ssm.SSM_BF16) == 0
+    assert lib.ssm_scan_bwd_workspace_size(2, 8, 17, 64, ssm.SSM_BF16) == 0
+    # float32: double checkpoints plus double accumulators
+    assert lib.ssm_scan_bwd_workspace_size(1, 128, 16, 64, ssm.SSM_F32) >= 128 * 8 * 16 * 8 + 2 * 16 * 64 * 8
