@@ -109,7 +109,9 @@ struct BwdParams {
   float* dC;              // (batch, N, L)
   float* dD;              // (dim) or null
   float* dbias;           // (dim) or null
-  void* ckpt;             // (batch, dim, ceil(L / segment), 16) states, float (bf16 io) or double (f32 io)
+  void* ckpt;             // (batch, dim, ceil(L / segment), 16) local states, float (bf16 io) or double (f32 io)
+  void* ckpt_s;           // (batch, dim, ceil(L / segment)) running sum of Δ within the chunk, same type
+  void* agg;              // (batch, dim, nchunks, 48) chunk aggregates, same type
   void* acc_dA;
   void* acc_dB;
   void* acc_dC;
@@ -117,11 +119,16 @@ struct BwdParams {
   void* acc_dbias;        // null when dbias is null
   int batch, dim, N;
   int64_t L;
+  int64_t chunk_len;      // steps per chunk, a multiple of the segment length
+  int nchunks;
   int softplus;
   int io_bf16;
+  int vec_io;             // L % 8 == 0 and every io row base 16-byte aligned
+  int vec_red;            // dB, dC 16-byte aligned and L % 4 == 0 (vector atomics)
 };
 
 int bwd_segment_steps();
+int bwd_aggregate_floats();
 cudaError_t scan_bwd_launch(const BwdParams& p, cudaStream_t stream);
 
 // Sets the text returned by ssm_last_error_message() on the calling host thread (ssm_api.cu).

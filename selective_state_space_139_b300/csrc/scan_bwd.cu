@@ -5,23 +5,31 @@
 // page, 硬件感知的实现: recomputation to save memory).  The pages give only the forward recurrence;
 // the derivatives below are its chain rule.
 //
-// Forward (per channel): v_t = Δ_raw_t + bias, Δ_t = softplus(v_t), Ā = exp(Δ A), h_t = Ā ⊙ h_{t-1} +
-// Δ_t B_t x_t, s_t = C_t·h_t + D x_t, y_t = s_t SiLU(z_t).  Backward from dy:
+// Forward (per channel): v_t = Δ_raw_t + bias, Δ_t = softplus(v_t), Ā_t = exp(Δ_t A), h_t = Ā_t ⊙ h_{t-1}
+// + Δ_t B_t x_t, s_t = C_t·h_t + D x_t, y_t = s_t SiLU(z_t).  Backward from dy:
 //   ds_t = dy_t SiLU(z_t);  dz_t = dy_t s_t SiLU'(z_t)
 //   dh_t = ds_t C_t + Ā_{t+1} ⊙ dh_{t+1}
 //   dC_t = Σ_channels ds_t h_t;  dB_t = Σ_channels dh_t Δ_t x_t
 //   dΔ_t = Σ_n dh_{t,n} (h_{t-1,n} Ā_{t,n} A_n + B_{t,n} x_t);  dA_n = Σ_{batch, t} dh_{t,n} h_{t-1,n} Ā_{t,n} Δ_t
 //   dx_t = ds_t D + Σ_n dh_{t,n} Δ_t B_{t,n};  dD = Σ ds_t x_t;  dΔ_raw_t = dΔ_t σ(v_t);  dbias = Σ dΔ_raw
 //
-// Two kernels.  (1) A forward pass (one thread per channel) writes the state at the start of every
-// 8-step segment.  (2) The backward pass walks the segments from the last to the first: it
-// recomputes the segment's 8 states from its checkpoint into shared memory (layout [step][state]
-// [thread], conflict free), then runs the 8 steps backwards.  dB and dC sum over the channels of a
-// batch row: per step a warp transpose-reduces its 32 values (16 of dB, 16 of dC), the four warps'
-// partials are added in shared memory and one global atomic per (step, state) and CTA adds them.
-// dA, dD and dbias accumulate per thread and are added once per channel.  bf16 io computes in
-// float32 with the MUFU approximations of the forward; float32 io computes in double and
-// accumulates its cross-channel sums in double (the same reasoning as the forward).
+// Time is cut into chunks so that (channel group, chunk) tiles run in parallel.  Both recurrences are
+// affine maps of the state, so a chunk is summarised by three vectors per channel (the same
+// composition as the forward's chunked schedule):
+//   P = Π_chunk Ā (the decay over the chunk),  Q = the chunk's end state from a zero start,
+//   G = Σ_t (Π_{r=chunk start..t} Ā_r) ⊙ C_t ds_t, the gradient reaching the state before the chunk from
+//       the chunk's own outputs.
+// Three kernels: (1) per tile, a forward pass from a zero state that writes P, Q, G and a
+// checkpoint (the local state and the running Σ Δ) every 8 steps; (2) per channel, the carries:
+// h_start(c+1) = P_c ⊙ h_start(c) + Q_c forwards, dh_in(c) = G_{c+1} + P_{c+1} ⊙ dh_in(c+1) backwards;
+// (3) per tile, the reverse pass: for each 8-step segment from the last, the true state at the
+// segment start is the checkpoint plus exp(A Σ Δ) ⊙ h_start, the segment's 8 states are recomputed into
+// shared memory (layout [step][state][thread], conflict free), and the 8 steps run backwards starting
+// from dh_in.  dB and dC sum over the channels of a batch row: per step a warp transpose-reduces its
+// 32 values (16 of dB, 16 of dC), the four warps' partials are added in shared memory and the CTA adds
+// them to global memory with vector atomics.  dA, dD and dbias accumulate per thread and are added
+// once per tile.  bf16 io computes in float32 with the MUFU approximations of the forward; float32
+// io computes in double and accumulates its cross-channel sums in double.
 #include <cstring>
 
 #include "internal.h"
@@ -31,26 +39,25 @@ namespace ssm {
 namespace {
 
 constexpr int kThreads = 128;   // channels per CTA
-constexpr int kSeg = 8;         // steps per segment
+constexpr int kSeg = 8;         // steps per segment (checkpoint interval)
 constexpr int kN = 16;
+constexpr int kAgg = 3 * kN;    // per (channel, chunk): [Q -> h_start | P | G -> dh_in]
 
 template <typename CT>
 struct Smem {
-  // B and C of the segment [step][B0..15 | C0..15] (float), the recomputed states, and the dB/dC
-  // partials of the four warps
-  static constexpr int kBC = kSeg * 32 * 4;
+  // B and C of the segment [step][B0..15 | C0..15] (float, two buffers), the recomputed states, the
+  // dB/dC partials of the four warps (two buffers) and the chunk start states
+  static constexpr int kBC = 2 * kSeg * 32 * 4;
   static constexpr int kH = kSeg * kN * kThreads * static_cast<int>(sizeof(CT));
-  static constexpr int kRed = 4 * kSeg * 32 * static_cast<int>(sizeof(CT));
-  static constexpr int kTotal = kBC + kH + kRed;
+  static constexpr int kRed = 2 * 4 * kSeg * 32 * static_cast<int>(sizeof(CT));
+  static constexpr int kHs = kN * kThreads * static_cast<int>(sizeof(CT));   // chunk start states
+  static constexpr int kTotal = kBC + kH + kRed + kHs;
 };
 
 template <typename CT>
-__device__ __forceinline__ CT sp(CT v, bool fast) {
-  if constexpr (sizeof(CT) == 4) {
-    return fast ? softplus_fast(v) : (v > 0.f ? v + log1pf(expf(-v)) : log1pf(expf(v)));
-  } else {
-    return v > 0.0 ? v + log1p(exp(-v)) : log1p(exp(v));
-  }
+__device__ __forceinline__ CT sp(CT v) {
+  if constexpr (sizeof(CT) == 4) return softplus_fast(v);
+  else return v > 0.0 ? v + log1p(exp(-v)) : log1p(exp(v));
 }
 
 template <typename CT>
@@ -65,58 +72,276 @@ __device__ __forceinline__ CT sigm(CT x) {
   else return 1.0 / (1.0 + exp(-x));
 }
 
+// Two states (n, n+1) of a channel.  float: one packed f32x2 register pair, so elementwise
+// arithmetic issues once per pair; double (the float32-io path): two scalars.  The exponent of Ā is
+// taken base 2 for float (A pre-scaled by log2 e) and base e for double.
+template <typename CT>
+struct Pair;
+
+template <>
+struct Pair<float> {
+  f2 v;
+  static constexpr float kExpScale = kLog2e;
+  __device__ static Pair make(float lo, float hi) { return {f2_make(lo, hi)}; }
+  __device__ static Pair splat(float a) { return {f2_splat(a)}; }
+  __device__ static Pair from_f2(f2 a) { return {a}; }
+  __device__ float lo() const { return f2_lo(v); }
+  __device__ float hi() const { return f2_hi(v); }
+};
+
+template <>
+struct Pair<double> {
+  double a, b;
+  static constexpr double kExpScale = 1.0;
+  __device__ static Pair make(double lo, double hi) { return {lo, hi}; }
+  __device__ static Pair splat(double x) { return {x, x}; }
+  __device__ static Pair from_f2(f2 x) { return {f2_lo(x), f2_hi(x)}; }
+  __device__ double lo() const { return a; }
+  __device__ double hi() const { return b; }
+};
+
+__device__ __forceinline__ Pair<float> pmul(Pair<float> x, Pair<float> y) { return {f2_mul(x.v, y.v)}; }
+__device__ __forceinline__ Pair<float> pfma(Pair<float> x, Pair<float> y, Pair<float> z) { return {f2_fma(x.v, y.v, z.v)}; }
+__device__ __forceinline__ Pair<float> padd(Pair<float> x, Pair<float> y) { return {f2_add(x.v, y.v)}; }
+// exp of the pre-scaled exponent: 2^x for float
+__device__ __forceinline__ Pair<float> pexp(Pair<float> x) { return Pair<float>::make(ex2_approx(x.lo()), ex2_approx(x.hi())); }
+
+__device__ __forceinline__ Pair<double> pmul(Pair<double> x, Pair<double> y) { return {x.a * y.a, x.b * y.b}; }
+__device__ __forceinline__ Pair<double> pfma(Pair<double> x, Pair<double> y, Pair<double> z) {
+  return {fma(x.a, y.a, z.a), fma(x.b, y.b, z.b)};
+}
+__device__ __forceinline__ Pair<double> padd(Pair<double> x, Pair<double> y) { return {x.a + y.a, x.b + y.b}; }
+__device__ __forceinline__ Pair<double> pexp(Pair<double> x) { return {exp(x.a), exp(x.b)}; }
+
+constexpr int kP = kN / 2;   // state pairs per channel
+
+// The io inputs of one 8-step segment of a channel, as raw 16-byte words: u, Δ_raw, dy, z.  Fetched
+// one segment ahead (software pipeline), unpacked when the segment is processed.
 template <typename IO>
-__device__ __forceinline__ float ld(const void* p, int64_t i) {
-  return IoTraits<IO>::to_f32(static_cast<const IO*>(p)[i]);
+struct SegRaw {
+  static constexpr int kW = kSeg * static_cast<int>(sizeof(IO)) / 16;   // 16-byte words per array
+  uint4 w[4][kW];
+};
+
+// vec: the row segment is 16-byte aligned and complete; otherwise scalar loads (zeros past nk)
+template <typename IO>
+__device__ __forceinline__ void fetch_one(const void* base, int64_t off, int nk, bool vec, uint4 (&w)[SegRaw<IO>::kW]) {
+  constexpr int kW = SegRaw<IO>::kW;
+  const IO* p = static_cast<const IO*>(base) + off;
+  if (vec && nk == kSeg) {
+#pragma unroll
+    for (int i = 0; i < kW; ++i) w[i] = __ldg(reinterpret_cast<const uint4*>(p) + i);
+  } else {
+    IO e[kSeg];
+#pragma unroll
+    for (int k = 0; k < kSeg; ++k) e[k] = k < nk ? p[k] : IoTraits<IO>::from_f32(0.0f);
+    static_assert(sizeof(e) == sizeof(w), "segment words");
+    memcpy(&w, e, sizeof(e));
+  }
 }
 
-// widen B and C of steps [t0, t0 + nk) of batch row b into the shared table (zeros past dstate / L)
 template <typename IO>
-__device__ __forceinline__ void load_bc(float* bc, const BwdParams& p, int b, int64_t t0, int nk) {
-  for (int i = threadIdx.x; i < kSeg * 32; i += kThreads) {
+__device__ __forceinline__ void fetch_seg(const BwdParams& p, int64_t off, int nk, SegRaw<IO>& r) {
+  fetch_one<IO>(p.u, off, nk, p.vec_io, r.w[0]);
+  fetch_one<IO>(p.delta, off, nk, p.vec_io, r.w[1]);
+  fetch_one<IO>(p.dy, off, nk, p.vec_io, r.w[2]);
+  if (p.z) fetch_one<IO>(p.z, off, nk, p.vec_io, r.w[3]);
+}
+
+template <typename IO, typename CT>
+__device__ __forceinline__ void unpack_one(const uint4 (&w)[SegRaw<IO>::kW], CT (&out)[kSeg]) {
+  if constexpr (sizeof(IO) == 2) {
+    float f[8];
+    unpack_chunk(w[0], f, IO());
+#pragma unroll
+    for (int k = 0; k < kSeg; ++k) out[k] = f[k];
+  } else {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      float f[4];
+      unpack_chunk(w[i], f, IO());
+#pragma unroll
+      for (int k = 0; k < 4; ++k) out[4 * i + k] = f[k];
+    }
+  }
+}
+
+template <typename IO, typename CT>
+__device__ __forceinline__ void store_seg(void* base, int64_t off, int nk, bool vec, const CT (&v)[kSeg]) {
+  IO* p = static_cast<IO*>(base) + off;
+  float f[kSeg];
+#pragma unroll
+  for (int k = 0; k < kSeg; ++k) f[k] = static_cast<float>(v[k]);
+  if (vec && nk == kSeg) {
+    if constexpr (sizeof(IO) == 2) {
+      *reinterpret_cast<uint4*>(p) = pack_chunk(f);
+    } else {
+      const float a[4] = {f[0], f[1], f[2], f[3]}, b[4] = {f[4], f[5], f[6], f[7]};
+      reinterpret_cast<uint4*>(p)[0] = pack_chunk(a);
+      reinterpret_cast<uint4*>(p)[1] = pack_chunk(b);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < kSeg; ++k)
+      if (k < nk) p[k] = IoTraits<IO>::from_f32(f[k]);
+  }
+}
+
+// B and C of steps [t0, t0 + nk) of batch row b, widened: each thread fetches 2 of the segment's
+// 8 x 32 table entries ([step][B0..15 | C0..15], zeros past dstate / nk) and later stores them
+__device__ __forceinline__ void fetch_bc(const BwdParams& p, int b, int64_t t0, int nk, float (&r)[2]) {
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int i = threadIdx.x + j * kThreads;
     const int k = i / 32, col = i % 32, arr = col / 16, n = col % 16;
     float v = 0.0f;
-    if (k < nk && n < p.N) v = ld<IO>(arr ? p.C : p.B, (static_cast<int64_t>(b) * p.N + n) * p.L + t0 + k);
-    bc[i] = v;
+    if (k < nk && n < p.N) {
+      const int64_t idx = (static_cast<int64_t>(b) * p.N + n) * p.L + t0 + k;
+      const void* src = arr ? p.C : p.B;
+      v = p.io_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(src)[idx])
+                    : static_cast<const float*>(src)[idx];
+    }
+    r[j] = v;
   }
 }
 
-// (1) forward with checkpoints: ckpt[(b, d), seg, :] = state entering segment seg
+__device__ __forceinline__ void store_bc(float* bc, const float (&r)[2]) {
+  bc[threadIdx.x] = r[0];
+  bc[threadIdx.x + kThreads] = r[1];
+}
+
+struct Tile {
+  int b, d, dd;
+  bool valid;
+  int64_t row;           // b * dim + dd
+  int64_t c0, c1;        // the chunk's steps [c0, c1)
+  int64_t ag;            // index of the (row, chunk) aggregate
+};
+
+__device__ __forceinline__ Tile tile_of(const BwdParams& p) {
+  Tile t;
+  t.b = blockIdx.y;
+  t.d = blockIdx.x * kThreads + threadIdx.x;
+  t.valid = t.d < p.dim;
+  t.dd = t.valid ? t.d : 0;
+  t.row = static_cast<int64_t>(t.b) * p.dim + t.dd;
+  t.c0 = static_cast<int64_t>(blockIdx.z) * p.chunk_len;
+  t.c1 = t.c0 + p.chunk_len < p.L ? t.c0 + p.chunk_len : p.L;
+  t.ag = (t.row * p.nchunks + blockIdx.z) * kAgg;
+  return t;
+}
+
+// (1) local forward of one tile: checkpoints every 8 steps and the chunk aggregates P, Q, G.
+// The next segment's inputs are fetched into registers while the current one is computed; B/C go
+// through a double-buffered shared table, so each segment needs one barrier.
 template <typename IO, typename CT>
-__global__ void __launch_bounds__(kThreads) bwd_ckpt_kernel(const BwdParams p) {
-  __shared__ float bc[kSeg * 32];
-  constexpr bool kFast = sizeof(CT) == 4;
-  const int b = blockIdx.y;
-  const int d = blockIdx.x * kThreads + threadIdx.x;
-  const bool valid = d < p.dim;
-  const int dd = valid ? d : 0;
-  const int64_t row = static_cast<int64_t>(b) * p.dim + dd;
-  CT A[kN], h[kN];
-#pragma unroll
-  for (int n = 0; n < kN; ++n) {
-    A[n] = n < p.N ? p.A[static_cast<int64_t>(dd) * p.N + n] : 0.0f;
-    h[n] = 0;
-  }
-  const CT bias = p.bias ? p.bias[dd] : 0.0f;
+__global__ void __launch_bounds__(kThreads, sizeof(CT) == 4 ? 4 : 1) bwd_chunk_fwd_kernel(const BwdParams p) {
+  using P = Pair<CT>;
+  __shared__ __align__(16) float bc_buf[2][kSeg * 32];
+  const Tile T = tile_of(p);
   const int64_t nseg = (p.L + kSeg - 1) / kSeg;
-  CT* ck = static_cast<CT*>(p.ckpt) + row * nseg * kN;
-  for (int64_t s = 0; s < nseg; ++s) {
-    const int64_t t0 = s * kSeg;
-    const int nk = static_cast<int>(p.L - t0 < kSeg ? p.L - t0 : kSeg);
-    __syncthreads();
-    load_bc<IO>(bc, p, b, t0, nk);
-    __syncthreads();
-    if (valid) {
+  P A2[kP], h[kP], E[kP], G[kP];
+  {
+    const float* Ad = p.A + static_cast<int64_t>(T.dd) * p.N;
 #pragma unroll
-      for (int n = 0; n < kN; ++n) ck[s * kN + n] = h[n];
+    for (int j = 0; j < kP; ++j) {
+      const CT a0 = 2 * j < p.N ? static_cast<CT>(Ad[2 * j]) : static_cast<CT>(0);
+      const CT a1 = 2 * j + 1 < p.N ? static_cast<CT>(Ad[2 * j + 1]) : static_cast<CT>(0);
+      A2[j] = P::make(a0 * P::kExpScale, a1 * P::kExpScale);
+      h[j] = P::splat(0);
+      E[j] = P::splat(1);
+      G[j] = P::splat(0);
     }
-    for (int k = 0; k < nk; ++k) {
-      const CT x = ld<IO>(p.u, row * p.L + t0 + k);
-      const CT v = ld<IO>(p.delta, row * p.L + t0 + k) + bias;
-      const CT dl = p.softplus ? sp<CT>(v, kFast) : v;
+  }
+  const CT bias = p.bias ? p.bias[T.dd] : 0.0f;
+  CT S = 0;
+  CT* ck = static_cast<CT*>(p.ckpt) + T.row * nseg * kN;
+  CT* cs = static_cast<CT*>(p.ckpt_s) + T.row * nseg;
+  auto seg_len = [&](int64_t t0) { return static_cast<int>(T.c1 - t0 < kSeg ? T.c1 - t0 : kSeg); };
+  SegRaw<IO> raw;
+  float bcr[2];
+  fetch_seg<IO>(p, T.row * p.L + T.c0, seg_len(T.c0), raw);
+  fetch_bc(p, T.b, T.c0, seg_len(T.c0), bcr);
+  store_bc(bc_buf[0], bcr);
+  __syncthreads();
+  int buf = 0;
+  for (int64_t t0 = T.c0; t0 < T.c1; t0 += kSeg) {
+    const int nk = seg_len(t0);
+    CT x[kSeg], v[kSeg], zz[kSeg], dyv[kSeg];
+    unpack_one<IO, CT>(raw.w[0], x);
+    unpack_one<IO, CT>(raw.w[1], v);
+    unpack_one<IO, CT>(raw.w[2], dyv);
+    if (p.z) unpack_one<IO, CT>(raw.w[3], zz);
+    const int64_t tn = t0 + kSeg;
+    const bool more = tn < T.c1;
+    if (more) {
+      fetch_seg<IO>(p, T.row * p.L + tn, seg_len(tn), raw);
+      fetch_bc(p, T.b, tn, seg_len(tn), bcr);
+    }
+    if (T.valid) {
+      const int64_t s = t0 / kSeg;
 #pragma unroll
-      for (int n = 0; n < kN; ++n) h[n] = expo<CT>(dl * A[n]) * h[n] + dl * static_cast<CT>(bc[k * 32 + n]) * x;
+      for (int j = 0; j < kP; ++j) {
+        ck[s * kN + 2 * j] = h[j].lo();
+        ck[s * kN + 2 * j + 1] = h[j].hi();
+      }
+      cs[s] = S;
     }
+    const f2* bc2 = reinterpret_cast<const f2*>(bc_buf[buf]);   // [k][B pairs 0..7 | C pairs 0..7]
+#pragma unroll
+    for (int k = 0; k < kSeg; ++k) {
+      if (k < nk) {
+        const CT dl = p.softplus ? sp<CT>(v[k] + bias) : v[k] + bias;
+        const CT ds = p.z ? dyv[k] * zz[k] * sigm<CT>(zz[k]) : dyv[k];
+        S += dl;
+        const P dlp = P::splat(dl), dlx = P::splat(dl * x[k]), dsp = P::splat(ds);
+#pragma unroll
+        for (int j = 0; j < kP; ++j) {
+          const P a = pexp(pmul(dlp, A2[j]));
+          h[j] = pfma(a, h[j], pmul(dlx, P::from_f2(bc2[k * 16 + j])));
+          E[j] = pmul(E[j], a);
+          G[j] = pfma(E[j], pmul(P::from_f2(bc2[k * 16 + 8 + j]), dsp), G[j]);
+        }
+      }
+    }
+    if (more) store_bc(bc_buf[buf ^ 1], bcr);
+    __syncthreads();
+    buf ^= 1;
+  }
+  if (T.valid) {
+    CT* ag = static_cast<CT*>(p.agg) + T.ag;
+#pragma unroll
+    for (int j = 0; j < kP; ++j) {
+      ag[2 * j] = h[j].lo();
+      ag[2 * j + 1] = h[j].hi();
+      ag[kN + 2 * j] = E[j].lo();
+      ag[kN + 2 * j + 1] = E[j].hi();
+      ag[2 * kN + 2 * j] = G[j].lo();
+      ag[2 * kN + 2 * j + 1] = G[j].hi();
+    }
+  }
+}
+
+// (2) carries across chunks, one thread per (channel, state): Q becomes h_start, G becomes dh_in
+template <typename CT>
+__global__ void bwd_carry_kernel(const BwdParams p) {
+  const int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  const int64_t rows = static_cast<int64_t>(p.batch) * p.dim;
+  if (i >= rows * kN) return;
+  const int64_t row = i / kN;
+  const int n = static_cast<int>(i % kN);
+  CT* ag = static_cast<CT*>(p.agg) + row * p.nchunks * kAgg + n;
+  CT h = 0;
+  for (int c = 0; c < p.nchunks; ++c) {
+    const CT q = ag[c * kAgg];
+    ag[c * kAgg] = h;
+    h = ag[c * kAgg + kN] * h + q;
+  }
+  CT g = 0;
+  for (int c = p.nchunks - 1; c >= 0; --c) {
+    const CT gc = ag[c * kAgg + 2 * kN];
+    ag[c * kAgg + 2 * kN] = g;
+    g = gc + ag[c * kAgg + kN] * g;
   }
 }
 
@@ -137,142 +362,209 @@ __device__ __forceinline__ CT warp_transpose_sum(CT (&v)[32]) {
   return v[0];
 }
 
-// (2) backward over segments in reverse
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+// (3) reverse pass of one tile.  Pipelined like (1): the previous segment's inputs, checkpoint and
+// B/C are fetched while the current one is computed; the dB/dC partials are double-buffered and
+// reduced one segment later by the first two warps.
 template <typename IO, typename CT>
-__global__ void __launch_bounds__(kThreads) bwd_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(kThreads) bwd_chunk_rev_kernel(const BwdParams p) {
+  using P = Pair<CT>;
   extern __shared__ __align__(16) uint8_t smem[];
-  float* bc = reinterpret_cast<float*>(smem);
-  CT* hbuf = reinterpret_cast<CT*>(smem + Smem<CT>::kBC);                  // [k][n][thread]
-  CT* red = reinterpret_cast<CT*>(smem + Smem<CT>::kBC + Smem<CT>::kH);    // [warp][k][32]
-  constexpr bool kFast = sizeof(CT) == 4;
+  float* bc_base = reinterpret_cast<float*>(smem);                                           // [2][k][32]
+  P* hbuf = reinterpret_cast<P*>(smem + Smem<CT>::kBC);                                      // [k][j][thread]
+  CT* red_base = reinterpret_cast<CT*>(smem + Smem<CT>::kBC + Smem<CT>::kH);                  // [2][warp][k][32]
+  P* hs_s = reinterpret_cast<P*>(smem + Smem<CT>::kBC + Smem<CT>::kH + Smem<CT>::kRed);      // [j][thread]
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.y;
-  const int d = blockIdx.x * kThreads + tid;
-  const bool valid = d < p.dim;
-  const int dd = valid ? d : 0;
-  const int64_t row = static_cast<int64_t>(b) * p.dim + dd;
-  CT A[kN], dh[kN], dA[kN];
-#pragma unroll
-  for (int n = 0; n < kN; ++n) {
-    A[n] = n < p.N ? p.A[static_cast<int64_t>(dd) * p.N + n] : 0.0f;
-    dh[n] = 0;
-    dA[n] = 0;
-  }
-  const CT bias = p.bias ? p.bias[dd] : 0.0f;
-  const CT Dd = p.D ? p.D[dd] : 0.0f;
-  CT dD = 0, dbias = 0;
+  const Tile T = tile_of(p);
   const int64_t nseg = (p.L + kSeg - 1) / kSeg;
-  const CT* ck = static_cast<const CT*>(p.ckpt) + row * nseg * kN;
-  for (int64_t s = nseg - 1; s >= 0; --s) {
-    const int64_t t0 = s * kSeg;
-    const int nk = static_cast<int>(p.L - t0 < kSeg ? p.L - t0 : kSeg);
-    __syncthreads();   // the previous segment is done with bc and red
-    load_bc<IO>(bc, p, b, t0, nk);
-    __syncthreads();
-    // inputs of the segment and the recomputed forward
-    CT x[kSeg], dl[kSeg], vv[kSeg], sv[kSeg], zz[kSeg], dyv[kSeg];
-    CT h0[kN];
+  P A2[kP], dh[kP], dA[kP];
+  {
+    const CT* ag = static_cast<const CT*>(p.agg) + T.ag;
+    const float* Ad = p.A + static_cast<int64_t>(T.dd) * p.N;
 #pragma unroll
-    for (int n = 0; n < kN; ++n) h0[n] = ck[s * kN + n];
-    {
-      CT h[kN];
+    for (int j = 0; j < kP; ++j) {
+      const CT a0 = 2 * j < p.N ? static_cast<CT>(Ad[2 * j]) : static_cast<CT>(0);
+      const CT a1 = 2 * j + 1 < p.N ? static_cast<CT>(Ad[2 * j + 1]) : static_cast<CT>(0);
+      A2[j] = P::make(a0 * P::kExpScale, a1 * P::kExpScale);
+      hs_s[j * kThreads + tid] = P::make(ag[2 * j], ag[2 * j + 1]);
+      dh[j] = T.valid ? P::make(ag[2 * kN + 2 * j], ag[2 * kN + 2 * j + 1]) : P::splat(0);
+      dA[j] = P::splat(0);
+    }
+  }
+  const CT bias = p.bias ? p.bias[T.dd] : 0.0f;
+  const CT Dd = p.D ? p.D[T.dd] : 0.0f;
+  CT dD = 0, dbias = 0;
+  const CT* ck = static_cast<const CT*>(p.ckpt) + T.row * nseg * kN;
+  const CT* cs = static_cast<const CT*>(p.ckpt_s) + T.row * nseg;
+  auto seg_len = [&](int64_t t0) { return static_cast<int>(T.c1 - t0 < kSeg ? T.c1 - t0 : kSeg); };
+  // adds the CTA's dB/dC partials of the segment at t0 (buffer rb) to global memory
+  auto flush_red = [&](const CT* rb, int64_t t0, int nk) {
+    if (tid >= 64) return;
+    const int col = tid & 31, half = tid >> 5, arr = col / 16, n = col % 16;
+    const int k0 = half * 4;
+    if (n >= p.N || k0 >= nk) return;
+    CT s4[4];
 #pragma unroll
-      for (int n = 0; n < kN; ++n) h[n] = h0[n];
-#pragma unroll
-      for (int k = 0; k < kSeg; ++k) {
-        if (k < nk) {
-          const int64_t i = row * p.L + t0 + k;
-          x[k] = ld<IO>(p.u, i);
-          vv[k] = ld<IO>(p.delta, i) + bias;
-          dl[k] = p.softplus ? sp<CT>(vv[k], kFast) : vv[k];
-          zz[k] = p.z ? ld<IO>(p.z, i) : 0.0f;
-          dyv[k] = ld<IO>(p.dy, i);
-          CT sacc = Dd * x[k];
-#pragma unroll
-          for (int n = 0; n < kN; ++n) {
-            h[n] = expo<CT>(dl[k] * A[n]) * h[n] + dl[k] * static_cast<CT>(bc[k * 32 + n]) * x[k];
-            hbuf[(k * kN + n) * kThreads + tid] = h[n];
-            sacc += static_cast<CT>(bc[k * 32 + 16 + n]) * h[n];
-          }
-          sv[k] = sacc;
-        } else {
-          x[k] = dl[k] = vv[k] = sv[k] = zz[k] = dyv[k] = 0;
-        }
+    for (int i = 0; i < 4; ++i)
+      s4[i] = (rb[(0 * kSeg + k0 + i) * 32 + col] + rb[(1 * kSeg + k0 + i) * 32 + col]) +
+              (rb[(2 * kSeg + k0 + i) * 32 + col] + rb[(3 * kSeg + k0 + i) * 32 + col]);
+    CT* dst = static_cast<CT*>(arr ? p.acc_dC : p.acc_dB) + (static_cast<int64_t>(T.b) * p.N + n) * p.L + t0 + k0;
+    if constexpr (sizeof(CT) == 4) {
+      if (p.vec_red && k0 + 4 <= nk) {
+        red_add_v4(dst, s4[0], s4[1], s4[2], s4[3]);
+        return;
       }
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (k0 + i < nk) atomicAdd(dst + i, s4[i]);
+  };
+  const int64_t last = T.c0 + ((T.c1 - T.c0 - 1) / kSeg) * kSeg;
+  SegRaw<IO> raw;
+  float bcr[2];
+  CT ckr[kN], ckS;
+  auto fetch_ck = [&](int64_t t0) {
+    const int64_t s = t0 / kSeg;
+#pragma unroll
+    for (int n = 0; n < kN; ++n) ckr[n] = ck[s * kN + n];
+    ckS = cs[s];
+  };
+  fetch_seg<IO>(p, T.row * p.L + last, seg_len(last), raw);
+  fetch_bc(p, T.b, last, seg_len(last), bcr);
+  fetch_ck(last);
+  store_bc(bc_base, bcr);
+  __syncthreads();
+  int buf = 0;
+  int64_t pend_t0 = -1;   // the segment whose dB/dC partials wait in the other red buffer
+  int pend_nk = 0;
+  for (int64_t t0 = last; t0 >= T.c0; t0 -= kSeg) {
+    const int nk = seg_len(t0);
+    const int64_t off = T.row * p.L + t0;
+    const f2* bc2 = reinterpret_cast<const f2*>(bc_base + buf * (kSeg * 32));   // [k][B pairs | C pairs]
+    CT* red = red_base + buf * (4 * kSeg * 32);
+    CT x[kSeg], v[kSeg], zz[kSeg], dyv[kSeg];
+    unpack_one<IO, CT>(raw.w[0], x);
+    unpack_one<IO, CT>(raw.w[1], v);
+    unpack_one<IO, CT>(raw.w[2], dyv);
+    if (p.z) unpack_one<IO, CT>(raw.w[3], zz);
+    // the true state entering the segment: local checkpoint + decayed chunk start state
+    P h0[kP];
+    {
+      const P Sp = P::splat(ckS);
+#pragma unroll
+      for (int j = 0; j < kP; ++j)
+        h0[j] = pfma(pexp(pmul(A2[j], Sp)), hs_s[j * kThreads + tid], P::make(ckr[2 * j], ckr[2 * j + 1]));
+    }
+    const int64_t tn = t0 - kSeg;
+    const bool more = tn >= T.c0;
+    if (more) {
+      fetch_seg<IO>(p, T.row * p.L + tn, seg_len(tn), raw);
+      fetch_bc(p, T.b, tn, seg_len(tn), bcr);
+      fetch_ck(tn);
+    }
+    if (pend_t0 >= 0) flush_red(red_base + (buf ^ 1) * (4 * kSeg * 32), pend_t0, pend_nk);
+    // recompute the segment forwards: states into shared memory, Δ, σ(v), ds; dz is final here
+    CT dl[kSeg], sg[kSeg], ds[kSeg], gdz[kSeg];
+    P hc[kP];   // the state after the step being differentiated (ends as the segment's last)
+#pragma unroll
+    for (int j = 0; j < kP; ++j) hc[j] = h0[j];
+#pragma unroll
+    for (int k = 0; k < kSeg; ++k) {
+      gdz[k] = 0;
+      if (k < nk) {
+        const CT vb = v[k] + bias;
+        dl[k] = p.softplus ? sp<CT>(vb) : vb;
+        sg[k] = p.softplus ? sigm<CT>(vb) : static_cast<CT>(1);
+        const P dlp = P::splat(dl[k]), dlx = P::splat(dl[k] * x[k]);
+        P sa[2] = {P::make(Dd * x[k], 0), P::splat(0)};   // C·h in four partial sums
+#pragma unroll
+        for (int j = 0; j < kP; ++j) {
+          hc[j] = pfma(pexp(pmul(dlp, A2[j])), hc[j], pmul(dlx, P::from_f2(bc2[k * 16 + j])));
+          if (k < kSeg - 1) hbuf[(k * kP + j) * kThreads + tid] = hc[j];
+          sa[j & 1] = pfma(P::from_f2(bc2[k * 16 + 8 + j]), hc[j], sa[j & 1]);
+        }
+        const P st = padd(sa[0], sa[1]);
+        const CT sacc = st.lo() + st.hi();
+        if (p.z) {
+          const CT sz = sigm<CT>(zz[k]);
+          ds[k] = dyv[k] * zz[k] * sz;
+          gdz[k] = dyv[k] * sacc * sz * (static_cast<CT>(1) + zz[k] * (static_cast<CT>(1) - sz));
+        } else {
+          ds[k] = dyv[k];
+        }
+        if (!T.valid) ds[k] = 0;
+      } else {
+        dl[k] = sg[k] = ds[k] = 0;
+      }
+    }
+    if (T.valid && p.z) store_seg<IO, CT>(p.dz, off, nk, p.vec_io, gdz);
     // backward over the segment's steps
-    CT gdu[kSeg], gdd[kSeg], gdz[kSeg];
+    CT gdu[kSeg], gdd[kSeg];
 #pragma unroll
     for (int k = kSeg - 1; k >= 0; --k) {
-      if (k >= nk) {
-        gdu[k] = gdd[k] = gdz[k] = 0;
-        continue;
-      }
-      CT ds = dyv[k];
-      gdz[k] = 0;
-      if (p.z) {
-        const CT sg = sigm<CT>(zz[k]);
-        ds = dyv[k] * zz[k] * sg;
-        gdz[k] = dyv[k] * sv[k] * sg * (static_cast<CT>(1) + zz[k] * (static_cast<CT>(1) - sg));
-      }
-      if (!valid) ds = 0;
-      CT dx = ds * Dd;
-      dD += ds * x[k];
-      CT ddl = 0;
-      CT vals[32];
+      gdu[k] = gdd[k] = 0;
+      if (k < nk) {
+        dD += ds[k] * x[k];
+        const P dlp = P::splat(dl[k]), dsp = P::splat(ds[k]), dlx = P::splat(dl[k] * x[k]);
+        P dq[2] = {P::splat(0), P::splat(0)}, db[2] = {P::splat(0), P::splat(0)};
+        CT vals[32];
 #pragma unroll
-      for (int n = 0; n < kN; ++n) {
-        const CT abar = expo<CT>(dl[k] * A[n]);
-        const CT bn = bc[k * 32 + n];
-        const CT cn = bc[k * 32 + 16 + n];
-        dh[n] += ds * cn;
-        const CT hk = hbuf[(k * kN + n) * kThreads + tid];
-        const CT hprev = k > 0 ? hbuf[((k - 1) * kN + n) * kThreads + tid] : h0[n];
-        vals[16 + n] = ds * hk;                 // dC contribution
-        vals[n] = dh[n] * dl[k] * x[k];         // dB contribution
-        ddl += dh[n] * (hprev * abar * A[n] + bn * x[k]);
-        dA[n] += dh[n] * hprev * abar * dl[k];
-        dx += dh[n] * dl[k] * bn;
-        dh[n] *= abar;
-      }
-      const CT dv = p.softplus ? ddl * sigm<CT>(vv[k]) : ddl;
-      gdu[k] = dx;
-      gdd[k] = dv;
-      dbias += dv;
-      const CT tot = warp_transpose_sum<CT>(vals);
-      red[(warp * kSeg + k) * 32 + lane] = tot;
-    }
-    // outputs of the segment
-    if (valid) {
-#pragma unroll
-      for (int k = 0; k < kSeg; ++k) {
-        if (k < nk) {
-          const int64_t i = row * p.L + t0 + k;
-          static_cast<IO*>(p.du)[i] = IoTraits<IO>::from_f32(static_cast<float>(gdu[k]));
-          static_cast<IO*>(p.ddelta)[i] = IoTraits<IO>::from_f32(static_cast<float>(gdd[k]));
-          if (p.z) static_cast<IO*>(p.dz)[i] = IoTraits<IO>::from_f32(static_cast<float>(gdz[k]));
+        for (int j = 0; j < kP; ++j) {
+          const P abar = pexp(pmul(dlp, A2[j]));
+          const P bn = P::from_f2(bc2[k * 16 + j]);
+          const P cn = P::from_f2(bc2[k * 16 + 8 + j]);
+          dh[j] = pfma(dsp, cn, dh[j]);
+          // the state after step k is hc; the one before it is h0 or recomputed in shared memory
+          const P hp = k > 0 ? hbuf[((k - 1) * kP + j) * kThreads + tid] : h0[j];
+          const P vc = pmul(dsp, hc[j]);            // dC contribution
+          const P vb = pmul(dh[j], dlx);            // dB contribution
+          vals[16 + 2 * j] = vc.lo();
+          vals[16 + 2 * j + 1] = vc.hi();
+          vals[2 * j] = vb.lo();
+          vals[2 * j + 1] = vb.hi();
+          const P w = pmul(pmul(dh[j], hp), abar);  // gradient of the exponent of Ā
+          dq[j & 1] = pfma(w, A2[j], dq[j & 1]);
+          dA[j] = pfma(w, dlp, dA[j]);
+          db[j & 1] = pfma(dh[j], bn, db[j & 1]);
+          dh[j] = pmul(dh[j], abar);
+          hc[j] = hp;
         }
+        const P dbt = padd(db[0], db[1]), dqt = padd(dq[0], dq[1]);
+        const CT dhb = dbt.lo() + dbt.hi();
+        // dq sums w·A·kExpScale: undo the exponent scale
+        const CT ddl = (dqt.lo() + dqt.hi()) * (static_cast<CT>(1) / P::kExpScale) + dhb * x[k];
+        const CT dv = ddl * sg[k];
+        gdu[k] = ds[k] * Dd + dhb * dl[k];
+        gdd[k] = dv;
+        dbias += dv;
+        red[(warp * kSeg + k) * 32 + lane] = warp_transpose_sum<CT>(vals);
       }
     }
+    if (T.valid) {
+      store_seg<IO, CT>(p.du, off, nk, p.vec_io, gdu);
+      store_seg<IO, CT>(p.ddelta, off, nk, p.vec_io, gdd);
+    }
+    if (more) store_bc(bc_base + (buf ^ 1) * (kSeg * 32), bcr);
     __syncthreads();
-    // the CTA's dB/dC partials of this segment: (k, col) pairs over the threads
-    for (int i = tid; i < kSeg * 32; i += kThreads) {
-      const int k = i / 32, col = i % 32, arr = col / 16, n = col % 16;
-      if (k < nk && n < p.N) {
-        const CT v = red[(0 * kSeg + k) * 32 + col] + red[(1 * kSeg + k) * 32 + col] +
-                     red[(2 * kSeg + k) * 32 + col] + red[(3 * kSeg + k) * 32 + col];
-        CT* dst = static_cast<CT*>(arr ? p.acc_dC : p.acc_dB);
-        atomicAdd(dst + (static_cast<int64_t>(b) * p.N + n) * p.L + t0 + k, v);
-      }
-    }
+    pend_t0 = t0;
+    pend_nk = nk;
+    buf ^= 1;
   }
-  if (valid) {
+  if (pend_t0 >= 0) flush_red(red_base + (buf ^ 1) * (4 * kSeg * 32), pend_t0, pend_nk);
+  if (T.valid) {
+    CT* accA = static_cast<CT*>(p.acc_dA) + static_cast<int64_t>(T.d) * p.N;
 #pragma unroll
-    for (int n = 0; n < kN; ++n)
-      if (n < p.N) atomicAdd(static_cast<CT*>(p.acc_dA) + static_cast<int64_t>(d) * p.N + n, dA[n]);
-    if (p.acc_dD) atomicAdd(static_cast<CT*>(p.acc_dD) + d, dD);
-    if (p.acc_dbias) atomicAdd(static_cast<CT*>(p.acc_dbias) + d, dbias);
+    for (int j = 0; j < kP; ++j) {
+      if (2 * j < p.N) atomicAdd(accA + 2 * j, dA[j].lo());
+      if (2 * j + 1 < p.N) atomicAdd(accA + 2 * j + 1, dA[j].hi());
+    }
+    if (p.acc_dD) atomicAdd(static_cast<CT*>(p.acc_dD) + T.d, dD);
+    if (p.acc_dbias) atomicAdd(static_cast<CT*>(p.acc_dbias) + T.d, dbias);
   }
 }
 
@@ -283,11 +575,14 @@ __global__ void double_to_float_kernel(const double* __restrict__ src, float* __
 
 template <typename IO, typename CT>
 cudaError_t launch(const BwdParams& p, cudaStream_t stream) {
-  const dim3 grid((p.dim + kThreads - 1) / kThreads, p.batch);
-  bwd_ckpt_kernel<IO, CT><<<grid, kThreads, 0, stream>>>(p);
+  const dim3 grid((p.dim + kThreads - 1) / kThreads, p.batch, p.nchunks);
+  bwd_chunk_fwd_kernel<IO, CT><<<grid, kThreads, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  auto k = bwd_kernel<IO, CT>;
+  const int64_t carry_threads = static_cast<int64_t>(p.batch) * p.dim * kN;
+  bwd_carry_kernel<CT><<<static_cast<unsigned>((carry_threads + 255) / 256), 256, 0, stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  auto k = bwd_chunk_rev_kernel<IO, CT>;
   e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<CT>::kTotal);
   if (e != cudaSuccess) return e;
   k<<<grid, kThreads, Smem<CT>::kTotal, stream>>>(p);
@@ -297,6 +592,7 @@ cudaError_t launch(const BwdParams& p, cudaStream_t stream) {
 }  // namespace
 
 int bwd_segment_steps() { return kSeg; }
+int bwd_aggregate_floats() { return kAgg; }
 
 cudaError_t scan_bwd_launch(const BwdParams& p, cudaStream_t stream) {
   // zero the accumulators (the float outputs for bf16 io, the double workspace for float32 io)
@@ -318,7 +614,7 @@ cudaError_t scan_bwd_launch(const BwdParams& p, cudaStream_t stream) {
   } pairs[5] = {{p.acc_dA, p.dA, nA}, {p.acc_dB, p.dB, nBC}, {p.acc_dC, p.dC, nBC},
                 {p.acc_dD, p.dD, static_cast<size_t>(p.dim)}, {p.acc_dbias, p.dbias, static_cast<size_t>(p.dim)}};
   for (const Pair& q : pairs) {
-    if (!q.src || !q.dst) continue;
+    if (!q.src || !q.dst || q.n == 0) continue;
     double_to_float_kernel<<<static_cast<unsigned>((q.n + 255) / 256), 256, 0, stream>>>(
         static_cast<const double*>(q.src), q.dst, static_cast<int64_t>(q.n));
     if ((ce = cudaGetLastError()) != cudaSuccess) return ce;

@@ -535,16 +535,41 @@ ssm_status ssm_device_status(cudaStream_t stream) {
 namespace {
 
 struct BwdLayout {
-  size_t ckpt = 0, acc_dA = 0, acc_dB = 0, acc_dC = 0, acc_dD = 0, acc_dbias = 0, total = 0;
+  size_t ckpt = 0, ckpt_s = 0, agg = 0, acc_dA = 0, acc_dB = 0, acc_dC = 0, acc_dD = 0, acc_dbias = 0, total = 0;
+  int64_t chunk_len = 0;
+  int nchunks = 1;
 };
 
-// checkpoints (16 states per channel and segment), then for float32 io the double accumulators
+// Time chunks: enough (channel group, chunk) tiles for several waves of resident CTAs, chunks a
+// multiple of the segment length and at least 64 steps.
+void bwd_chunks(int batch, int dim, int64_t seqlen, BwdLayout* l) {
+  const int K = ssm::bwd_segment_steps();
+  const int64_t groups = static_cast<int64_t>(batch) * ((dim + kChannelsPerCta - 1) / kChannelsPerCta);
+  const int64_t target_tiles = 24LL * sm_count();
+  int64_t nch = std::max<int64_t>(1, (target_tiles + groups - 1) / groups);
+  nch = std::min<int64_t>(nch, std::max<int64_t>(1, seqlen / 64));
+  nch = std::min<int64_t>(nch, 65535);
+  int64_t chunk = static_cast<int64_t>(round_up(static_cast<size_t>((seqlen + nch - 1) / nch), K));
+  if (chunk <= 0) chunk = K;
+  l->chunk_len = chunk;
+  l->nchunks = static_cast<int>((seqlen + chunk - 1) / chunk);
+}
+
+// checkpoints (16 local states and a Δ sum per channel and segment), chunk aggregates, then for
+// float32 io the double accumulators
 BwdLayout bwd_layout(int batch, int dim, int dstate, int64_t seqlen, ssm_dtype io) {
   BwdLayout l;
+  if (seqlen <= 0) return l;
+  bwd_chunks(batch, dim, seqlen, &l);
   const size_t ce = io == SSM_BF16 ? sizeof(float) : sizeof(double);
   const int K = ssm::bwd_segment_steps();
+  const size_t rows = static_cast<size_t>(batch) * dim;
   const size_t nseg = static_cast<size_t>((seqlen + K - 1) / K);
-  size_t off = round_up(static_cast<size_t>(batch) * dim * nseg * 16 * ce, 256);
+  size_t off = round_up(rows * nseg * 16 * ce, 256);
+  l.ckpt_s = off;
+  off += round_up(rows * nseg * ce, 256);
+  l.agg = off;
+  off += round_up(rows * l.nchunks * ssm::bwd_aggregate_floats() * ce, 256);
   if (io == SSM_F32) {
     l.acc_dA = off;
     off += round_up(static_cast<size_t>(dim) * dstate * 8, 256);
@@ -557,7 +582,7 @@ BwdLayout bwd_layout(int batch, int dim, int dstate, int64_t seqlen, ssm_dtype i
     l.acc_dbias = off;
     off += round_up(static_cast<size_t>(dim) * 8, 256);
   }
-  l.total = seqlen > 0 ? off : 0;
+  l.total = off;
   return l;
 }
 
@@ -636,8 +661,18 @@ ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A, const 
   p.du = du; p.ddelta = ddelta; p.dz = dz; p.dA = dA; p.dB = dB; p.dC = dC; p.dD = dD; p.dbias = ddelta_bias;
   p.batch = batch; p.dim = dim; p.N = dstate; p.L = seqlen;
   p.softplus = softplus_flag != 0; p.io_bf16 = io_dtype == SSM_BF16;
+  p.chunk_len = lay.chunk_len;
+  p.nchunks = lay.nchunks;
+  bool vec_io = seqlen % 8 == 0;
+  for (const void* q : {u, delta, z, dy, static_cast<const void*>(du), static_cast<const void*>(ddelta),
+                        static_cast<const void*>(dz)})
+    if (q && !aligned(q, 16)) vec_io = false;
+  p.vec_io = vec_io;
+  p.vec_red = seqlen % 4 == 0 && aligned(dB, 16) && aligned(dC, 16);
   char* ws = static_cast<char*>(workspace);
   p.ckpt = ws + lay.ckpt;
+  p.ckpt_s = ws + lay.ckpt_s;
+  p.agg = ws + lay.agg;
   if (io_dtype == SSM_BF16) {
     p.acc_dA = dA; p.acc_dB = dB; p.acc_dC = dC; p.acc_dD = dD; p.acc_dbias = ddelta_bias;
   } else {

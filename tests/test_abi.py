@@ -153,8 +153,9 @@ def test_scan_bwd_rejects_bad_arguments_on_host(lib):
 
 
 def test_scan_bwd_workspace_query(lib):
-    # bf16: one float checkpoint of 16 states per channel every 8 steps
-    assert lib.ssm_scan_bwd_workspace_size(2, 8, 16, 64, ssm.SSM_BF16) == 2 * 8 * 8 * 16 * 4
+    # bf16, one 64-step chunk: per channel 8 float checkpoints of 16 states and a Δ sum, and one
+    # 48-float chunk aggregate (each region rounded up to 256 bytes)
+    assert lib.ssm_scan_bwd_workspace_size(2, 8, 16, 64, ssm.SSM_BF16) == 2 * 8 * 8 * 16 * 4 + 512 + 2 * 8 * 48 * 4
     assert lib.ssm_scan_bwd_workspace_size(2, 8, 16, 0, ssm.SSM_BF16) == 0
     assert lib.ssm_scan_bwd_workspace_size(2, 8, 17, 64, ssm.SSM_BF16) == 0
     # float32: double checkpoints plus double accumulators
