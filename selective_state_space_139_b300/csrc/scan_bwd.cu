@@ -38,6 +38,10 @@
 namespace ssm {
 namespace {
 
+#ifndef SSM_BWD_FWD_MINB
+#define SSM_BWD_FWD_MINB 3   // resident CTAs per SM the local forward is compiled for (float state)
+#endif
+
 constexpr int kThreads = 128;   // channels per CTA
 constexpr int kSeg = 8;         // steps per segment (checkpoint interval)
 constexpr int kN = 16;
@@ -210,6 +214,35 @@ __device__ __forceinline__ void store_bc(float* bc, const float (&r)[2]) {
   bc[threadIdx.x + kThreads] = r[1];
 }
 
+// One checkpoint record: 16 states, 64 (float) or 128 (double) bytes, 16-byte aligned.
+__device__ __forceinline__ void store_ckpt(float* dst, const Pair<float> (&h)[kP]) {
+#pragma unroll
+  for (int i = 0; i < kP / 2; ++i)
+    reinterpret_cast<float4*>(dst)[i] = make_float4(h[2 * i].lo(), h[2 * i].hi(), h[2 * i + 1].lo(), h[2 * i + 1].hi());
+}
+__device__ __forceinline__ void store_ckpt(double* dst, const Pair<double> (&h)[kP]) {
+#pragma unroll
+  for (int j = 0; j < kP; ++j) reinterpret_cast<double2*>(dst)[j] = make_double2(h[j].a, h[j].b);
+}
+__device__ __forceinline__ void load_ckpt(const float* src, float (&r)[kN]) {
+#pragma unroll
+  for (int i = 0; i < kN / 4; ++i) {
+    const float4 q = __ldg(reinterpret_cast<const float4*>(src) + i);
+    r[4 * i] = q.x;
+    r[4 * i + 1] = q.y;
+    r[4 * i + 2] = q.z;
+    r[4 * i + 3] = q.w;
+  }
+}
+__device__ __forceinline__ void load_ckpt(const double* src, double (&r)[kN]) {
+#pragma unroll
+  for (int j = 0; j < kN / 2; ++j) {
+    const double2 q = __ldg(reinterpret_cast<const double2*>(src) + j);
+    r[2 * j] = q.x;
+    r[2 * j + 1] = q.y;
+  }
+}
+
 struct Tile {
   int b, d, dd;
   bool valid;
@@ -235,7 +268,7 @@ __device__ __forceinline__ Tile tile_of(const BwdParams& p) {
 // The next segment's inputs are fetched into registers while the current one is computed; B/C go
 // through a double-buffered shared table, so each segment needs one barrier.
 template <typename IO, typename CT>
-__global__ void __launch_bounds__(kThreads, sizeof(CT) == 4 ? 4 : 1) bwd_chunk_fwd_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(kThreads, sizeof(CT) == 4 ? SSM_BWD_FWD_MINB : 1) bwd_chunk_fwd_kernel(const BwdParams p) {
   using P = Pair<CT>;
   __shared__ __align__(16) float bc_buf[2][kSeg * 32];
   const Tile T = tile_of(p);
@@ -280,11 +313,7 @@ __global__ void __launch_bounds__(kThreads, sizeof(CT) == 4 ? 4 : 1) bwd_chunk_f
     }
     if (T.valid) {
       const int64_t s = t0 / kSeg;
-#pragma unroll
-      for (int j = 0; j < kP; ++j) {
-        ck[s * kN + 2 * j] = h[j].lo();
-        ck[s * kN + 2 * j + 1] = h[j].hi();
-      }
+      store_ckpt(ck + s * kN, h);
       cs[s] = S;
     }
     const f2* bc2 = reinterpret_cast<const f2*>(bc_buf[buf]);   // [k][B pairs 0..7 | C pairs 0..7]
@@ -430,8 +459,7 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_rev_kernel(const BwdParams
   CT ckr[kN], ckS;
   auto fetch_ck = [&](int64_t t0) {
     const int64_t s = t0 / kSeg;
-#pragma unroll
-    for (int n = 0; n < kN; ++n) ckr[n] = ck[s * kN + n];
+    load_ckpt(ck + s * kN, ckr);
     ckS = cs[s];
   };
   fetch_seg<IO>(p, T.row * p.L + last, seg_len(last), raw);

@@ -35,6 +35,10 @@ ssm_status cuda_fail(cudaError_t e, const char* what) {
   return fail(SSM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+#ifndef SSM_BWD_TILES_PER_SM
+#define SSM_BWD_TILES_PER_SM 24   // backward: (channel group, chunk) tiles to aim for per SM
+#endif
+
 constexpr int kChannelsPerCta = 128;
 constexpr int64_t kMinChunkTiles = 4;
 
@@ -545,7 +549,7 @@ struct BwdLayout {
 void bwd_chunks(int batch, int dim, int64_t seqlen, BwdLayout* l) {
   const int K = ssm::bwd_segment_steps();
   const int64_t groups = static_cast<int64_t>(batch) * ((dim + kChannelsPerCta - 1) / kChannelsPerCta);
-  const int64_t target_tiles = 24LL * sm_count();
+  const int64_t target_tiles = static_cast<int64_t>(SSM_BWD_TILES_PER_SM) * sm_count();
   int64_t nch = std::max<int64_t>(1, (target_tiles + groups - 1) / groups);
   nch = std::min<int64_t>(nch, std::max<int64_t>(1, seqlen / 64));
   nch = std::min<int64_t>(nch, 65535);
