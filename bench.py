@@ -4,8 +4,9 @@
 Default workload: the Mamba-2.8B layer scan (batch 4, d_inner 5120, d_state 16, L 4096, bf16 io,
 float32 state).  One step = one ssm_scan_fwd call over that batch (every prefill row of the hot
 path: load, softplus, discretise, recurrence, readout + D skip, gate, store, final state).
-The decode row (batch 256, d_inner 5120, 1000 tokens) is measured after it and reported in the
-same JSON line under "decode".
+The decode row (batch 256, d_inner 5120, 1000 tokens), the conv1d + SiLU prefill and the scan
+backward are measured after it and reported in the same JSON line under "decode", "conv1d" and
+"backward".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -135,38 +136,57 @@ def _ncu_traffic(kernel_key, workload):
 
 # ----------------------------------------------------------------------------- CPU oracle timing
 
-def cpu_oracle_sample(w, target_s: float = 12.0, min_channels: int = 2):
-    """Times the fp64 oracle on a bounded sample of channels of the workload; returns tokens/s of the
-    whole workload extrapolated from the sample, the cores used and a description."""
-    import torch
-    import oracle
-    from selective_state_space_139_b300 import workloads as W
+class OracleSample:
+    """A bounded sample of the workload for the fp64 oracle: ``nc`` channels (rows of the workload's
+    shape and distributions) run ``passes`` times, sized from a calibration so that one timing takes
+    about ``target_s`` seconds on all host cores."""
 
-    cores = os.cpu_count() or 1
-    n_total = w.batch * w.dim
-    # calibrate with one channel
-    g = np.random.default_rng(0)
+    def __init__(self, w, target_s: float, min_channels: int = 2):
+        self.w = w
+        self.cores = os.cpu_count() or 1
+        self.n_total = w.batch * w.dim
+        nc = min(self.cores, self.n_total)
+        secs = self._run(self._make(nc))
+        while secs < 0.5 and nc < self.n_total:       # calibrate on a sample that runs long enough to time
+            nc = min(self.n_total, nc * 4)
+            secs = self._run(self._make(nc))
+        want = max(min_channels, int(nc * target_s / max(secs, 1e-6)))
+        if want <= self.n_total:
+            self.nc, self.passes = want, 1
+        else:
+            self.nc, self.passes = self.n_total, max(1, round(want / self.n_total))
+        self.inputs = self._make(self.nc)
 
-    def make(nc):
+    def _make(self, nc):
+        from selective_state_space_139_b300 import workloads as W
+        w = self.w
         inp = W.random_scan_inputs(1, nc, w.dstate, w.seqlen, w.io_dtype, seed=1, a_scale=w.a_scale)
         f = lambda t: t.double().numpy()
         return (f(inp["u"][0]), f(inp["delta"][0]), f(inp["A"]), f(inp["B"]), f(inp["C"]), np.zeros(nc, np.int64),
                 f(inp["D"]), f(inp["z"][0]), f(inp["delta_bias"]))
 
-    def run(args):
+    def _run(self, args):
+        import oracle
         u, dl, A, B, C, bidx, D, z, bias = args
         t0 = time.perf_counter()
-        oracle.selective_scan_channels(u, dl, A, B, C, bidx, D=D, z=z, delta_bias=bias, threads=cores)
+        oracle.selective_scan_channels(u, dl, A, B, C, bidx, D=D, z=z, delta_bias=bias, threads=self.cores)
         return time.perf_counter() - t0
 
-    one = run(make(min(cores, n_total)))
-    per_round = max(one, 1e-4)
-    rounds = max(1, int(target_s / per_round))
-    nc = min(n_total, max(min_channels, rounds * min(cores, n_total)))
-    secs = run(make(nc))
-    tokens_per_s = (w.batch * w.seqlen) * (nc / n_total) / secs
-    sample = f"{nc} of {n_total} channels x {w.seqlen} steps (fp64 oracle, {secs:.1f} s)"
-    return tokens_per_s, cores, sample, secs
+    def time(self):
+        """Runs the sample once; returns (workload tokens/s extrapolated from it, seconds, description)."""
+        secs = sum(self._run(self.inputs) for _ in range(self.passes))
+        frac = self.nc * self.passes / self.n_total
+        tokens_per_s = self.w.batch * self.w.seqlen * frac / secs
+        what = f"{self.nc} of {self.n_total} channels" + (f" x {self.passes} passes" if self.passes > 1 else "")
+        return tokens_per_s, secs, f"{what} x {self.w.seqlen} steps (fp64 oracle, {secs:.1f} s)"
+
+
+def cpu_oracle_sample(w, target_s: float = 15.0):
+    """Times the fp64 oracle on a bounded sample of the workload; returns tokens/s of the whole
+    workload extrapolated from the sample, the cores used, a description and the seconds taken."""
+    s = OracleSample(w, target_s)
+    v, secs, what = s.time()
+    return v, s.cores, what, secs
 
 
 # ----------------------------------------------------------------------------- GPU measurement
@@ -316,6 +336,41 @@ def measure_conv(w, dev, rank, reps=50):
     return {"ms": ms, "bytes": nbytes, "achieved_gbs": nbytes / (ms * 1e-3) / 1e9}
 
 
+def measure_bwd(w, dev, rank, reps=10):
+    """The scan backward (ssm_scan_bwd) on the workload with a N(0, 1) dy: event-timed per call.
+    Algorithmic bytes: u, Δ, z, dy read and du, dΔ, dz written (io dtype) per (b, d, t), B and C read
+    (io dtype) and dB, dC written (float32) per (b, n, t), the per-channel parameters and dA."""
+    import torch
+    from selective_state_space_139_b300 import ssm
+    from selective_state_space_139_b300 import workloads as W
+    inp = W.make_scan_inputs(w, device=dev, seed=w.seed + rank)
+    dy = W.make_cotangent(w.batch, w.dim, w.seqlen, inp["u"].dtype, w.seed + rank, device=dev)
+    ws = torch.empty(ssm.scan_bwd_workspace_size(w.batch, w.dim, w.dstate, w.seqlen, inp["u"].dtype),
+                     dtype=torch.uint8, device=dev)
+
+    def call():
+        return ssm.selective_scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], dy, D=inp["D"],
+                                      z=inp["z"], delta_bias=inp["delta_bias"], workspace=ws)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize(dev)
+    times = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        b.record()
+        torch.cuda.synchronize(dev)
+        times.append(a.elapsed_time(b))
+    ms = statistics.median(times)
+    e = inp["u"].element_size()
+    bdl = w.batch * w.dim * w.seqlen
+    bnl = w.batch * w.dstate * w.seqlen
+    nbytes = 7 * bdl * e + bnl * (2 * e + 2 * 4) + w.dim * (3 * 4 + 2 * w.dstate * 4)
+    return {"ms": ms, "bytes": nbytes, "achieved_gbs": nbytes / (ms * 1e-3) / 1e9,
+            "tokens_per_s": w.batch * w.seqlen / (ms * 1e-3), "workspace_bytes": ws.numel()}
+
+
 # ----------------------------------------------------------------------------- distributed helpers
 
 _PG = None
@@ -357,12 +412,13 @@ def run_reference(args, ws, rank):
     if rank != 0:
         return 0
     w = W.WORKLOADS[args.workload]
-    values = []
-    sample = ""
-    cores = os.cpu_count() or 1
     budget = max(0.5, args.ref_budget / max(1, args.steps + args.warmup))
+    sample = OracleSample(w, target_s=budget)
+    cores = sample.cores
+    values = []
+    what = ""
     for i in range(args.warmup + args.steps):
-        v, cores, sample, secs = cpu_oracle_sample(w, target_s=budget)
+        v, secs, what = sample.time()
         if i >= args.warmup:
             values.append(v)
     value = statistics.mean(values)
@@ -372,7 +428,7 @@ def run_reference(args, ws, rank):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "batch": w.batch, "d_inner": w.dim, "d_state": w.dstate,
                        "seq_len": w.seqlen, "io": w.io_dtype},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": what},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -388,6 +444,7 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=150.0,
                     help="seconds of oracle work for the whole --impl reference run")
     args = ap.parse_args()
@@ -416,6 +473,7 @@ def main():
         dec = measure_decode(dw, args.decode_steps, dev, rank)
         dec["ms_per_token_step"] = _max_over_ranks(dec["ms_per_token_step"])
     conv = measure_conv(w, dev, rank)
+    bwd = None if args.no_backward else measure_bwd(w, dev, rank)
     if rank != 0:
         return 0
     tokens_all = w.tokens * ws
@@ -445,6 +503,11 @@ def main():
     line["conv1d"] = {"workload": w.name + " x (conv1d + SiLU prefill)", "ms": conv["ms"],
                       "achieved_gbs": conv["achieved_gbs"], "frac": conv["achieved_gbs"] / peak,
                       "bytes_per_launch": conv["bytes"]}
+    if bwd is not None:
+        line["backward"] = {"workload": w.name + " x (scan backward: local forward, carry, reverse pass)",
+                            "ms": bwd["ms"], "tokens_per_s": bwd["tokens_per_s"] * ws,
+                            "achieved_gbs": bwd["achieved_gbs"], "frac": bwd["achieved_gbs"] / peak,
+                            "bytes_per_call": bwd["bytes"], "workspace_bytes": bwd["workspace_bytes"]}
     if not args.no_cpu_baseline:
         v, cores, sample, _ = cpu_oracle_sample(w)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
