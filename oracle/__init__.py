@@ -20,6 +20,9 @@ What it computes (page title, section):
 * ``compose_affine`` -- (a2, b2) ∘ (a1, b1) = (a2 a1, a2 b1 + b2), "later after earlier".
 * ``scan_backward`` -- gradients of sum(dy * y) by reverse-mode differentiation of the recurrence
   (the pages' hardware-aware scan recomputes states for its backward; here the plain form).
+* ``ssd_scan`` -- Mamba-2 state space duality: a scalar decay per head and a (headdim, dstate) state
+  ("Mamba и State Space Models", "Mamba-2: State Space Duality (SSD)"; "Модуль 8", §7, §14), as the
+  recurrence and as the chunked block form.
 
 Pins: every function is checked in ``tests/test_oracle_pins.py`` against closed forms, brute
 force and the pages' worked examples (see the test module's docstring for the list).
@@ -73,6 +76,10 @@ def _load():
                                              _D, _D, _D, _D, _D, ctypes.c_int64, ctypes.c_int, ctypes.c_int64,
                                              ctypes.c_int]
         lib.oracle_scan_backward.restype = ctypes.c_int
+        lib.oracle_ssd_scan.argtypes = [_D] * 7 + [ctypes.c_int, _D, _D, _D, ctypes.c_int64, ctypes.c_int64,
+                                                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                   ctypes.c_int64, ctypes.c_int]
+        lib.oracle_ssd_scan.restype = ctypes.c_int
         lib.oracle_compose_affine.argtypes = [ctypes.c_double] * 4 + [_D, _D]
         lib.oracle_compose_affine.restype = None
         _lib = lib
@@ -296,3 +303,30 @@ def scan_backward(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_
             "dz": None if g["dz"] is None else g["dz"].reshape(batch, dim, L),
             "dA": g["dA"].reshape(batch, dim, N).sum(0), "dD": g["dD"].reshape(batch, dim).sum(0),
             "ddelta_bias": g["ddelta_bias"].reshape(batch, dim).sum(0), "dB": g["dB"], "dC": g["dC"]}
+
+
+def ssd_scan(x, dt, A, B, C, D=None, dt_bias=None, dt_softplus: bool = True, h0=None, chunk: Optional[int] = None,
+             threads: int = 0):
+    """Mamba-2 SSD with a scalar decay per head.  ``x`` (batch, L, nheads, headdim); ``dt`` (batch, L,
+    nheads) before bias and softplus; ``A, D, dt_bias`` (nheads); ``B, C`` (batch, L, ngroups, dstate);
+    ``h0`` (batch, nheads, headdim, dstate).  ``chunk=None`` runs the recurrence, an integer the
+    chunked block form.  Returns ``y`` (batch, L, nheads, headdim) and the final state, float64."""
+    x = _f64(x)
+    batch, L, nheads, headdim = x.shape
+    B = _f64(B)
+    ngroups, dstate = B.shape[2], B.shape[3]
+    dt = _f64(dt, (batch, L, nheads))
+    A = _f64(A, (nheads,))
+    B = _f64(B, (batch, L, ngroups, dstate))
+    C = _f64(C, (batch, L, ngroups, dstate))
+    D = _f64(D, (nheads,))
+    dt_bias = _f64(dt_bias, (nheads,))
+    h0 = _f64(h0, (batch, nheads, headdim, dstate))
+    y = np.empty((batch, L, nheads, headdim))
+    hT = np.empty((batch, nheads, headdim, dstate))
+    rc = _load().oracle_ssd_scan(_p(x), _p(dt), _p(A), _p(B), _p(C), _p(D), _p(dt_bias), int(bool(dt_softplus)),
+                                 _p(h0), _p(y), _p(hT), batch, L, nheads, headdim, dstate, ngroups,
+                                 int(chunk or 0), threads)
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return y, hT

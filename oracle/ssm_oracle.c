@@ -460,3 +460,163 @@ ORACLE_API int oracle_scan_backward(const double* u, const double* delta, const 
   run_channels(backward_fn, &q, n, threads);
   return 0;
 }
+
+/* ------------------------------------------------------------------------------------------
+ * Mamba-2 state space duality (SSD): scalar decay per head, matrix state per head.
+ *  [S1] "Mamba и State Space Models", "Mamba-2: State Space Duality (SSD)": A is a scalar
+ *       (A = -exp(A_log)), d_state 128, y = SS(A)·(B ⊗ X)·C.
+ *  [S2] "Модуль 8", §7: with transition a_t·I and a zero initial state the weight of input j in
+ *       output i ≥ j is M_ij = C_i^T B_j Π_{r=j+1..i} a_r; inside a chunk the block is computed as
+ *       a masked matrix product, between chunks only the state is passed; §14: the state has the
+ *       shape [batch, nheads, headdim, d_state] and the input term is Δ·B·x.
+ * Per batch b and head h, with P = headdim, N = dstate and the head's group g:
+ *   Δ_t = softplus(dt[b,t,h] + dt_bias[h]),  a_t = exp(Δ_t A[h])
+ *   H_t[p][n] = a_t H_{t-1}[p][n] + Δ_t x[b,t,h,p] B[b,t,g,n]
+ *   y[b,t,h,p] = Σ_n C[b,t,g,n] H_t[p][n] + D[h] x[b,t,h,p]
+ * Layouts: x, y (batch, L, nheads, headdim); dt (batch, L, nheads); B, C (batch, L, ngroups, dstate);
+ * A, D, dt_bias (nheads); h0, hT (batch, nheads, headdim, dstate).  Heads split evenly over groups.
+ * ------------------------------------------------------------------------------------------ */
+typedef struct {
+  const double *x, *dt, *A, *B, *C, *D, *dt_bias, *h0;
+  double *y, *hT;
+  int softplus_flag;
+  int64_t batch, L, chunk;
+  int nheads, headdim, dstate, ngroups;
+} ssd_problem;
+
+static double ssd_delta(const ssd_problem* p, int64_t b, int64_t t, int h) {
+  double v = p->dt[(b * p->L + t) * p->nheads + h];
+  if (p->dt_bias) v += p->dt_bias[h];
+  return p->softplus_flag ? softplus(v) : v;
+}
+
+static const double* ssd_x(const ssd_problem* p, int64_t b, int64_t t, int h) {
+  return p->x + ((b * p->L + t) * p->nheads + h) * p->headdim;
+}
+
+static const double* ssd_bc(const ssd_problem* p, const double* base, int64_t b, int64_t t, int h) {
+  const int g = h / (p->nheads / p->ngroups);
+  return base + ((b * p->L + t) * p->ngroups + g) * p->dstate;
+}
+
+static void ssd_init_state(const ssd_problem* p, int64_t b, int h, double* H) {
+  const int64_t PN = (int64_t)p->headdim * p->dstate;
+  for (int64_t i = 0; i < PN; ++i) H[i] = p->h0 ? p->h0[(b * p->nheads + h) * PN + i] : 0.0;
+}
+
+static void ssd_store_state(const ssd_problem* p, int64_t b, int h, const double* H) {
+  const int64_t PN = (int64_t)p->headdim * p->dstate;
+  if (p->hT)
+    for (int64_t i = 0; i < PN; ++i) p->hT[(b * p->nheads + h) * PN + i] = H[i];
+}
+
+/* the recurrence, one step at a time ([S2] §7, form 1) */
+static void ssd_sequential_pair(const ssd_problem* p, int64_t pair) {
+  const int64_t b = pair / p->nheads;
+  const int h = (int)(pair % p->nheads);
+  const int P = p->headdim, N = p->dstate;
+  double* H = (double*)malloc(sizeof(double) * (size_t)P * N);
+  ssd_init_state(p, b, h, H);
+  for (int64_t t = 0; t < p->L; ++t) {
+    const double dl = ssd_delta(p, b, t, h);
+    const double a = exp(dl * p->A[h]);
+    const double* x = ssd_x(p, b, t, h);
+    const double* Bt = ssd_bc(p, p->B, b, t, h);
+    const double* Ct = ssd_bc(p, p->C, b, t, h);
+    for (int i = 0; i < P; ++i)
+      for (int n = 0; n < N; ++n) H[i * N + n] = a * H[i * N + n] + dl * x[i] * Bt[n];
+    double* y = p->y + ((b * p->L + t) * p->nheads + h) * P;
+    for (int i = 0; i < P; ++i) {
+      double s = 0.0;
+      for (int n = 0; n < N; ++n) s += Ct[n] * H[i * N + n];
+      y[i] = s + (p->D ? p->D[h] * x[i] : 0.0);
+    }
+  }
+  ssd_store_state(p, b, h, H);
+  free(H);
+}
+
+/* the chunked block form ([S2] §7, form 3): inside a chunk, y_i = Σ_{j≤i} (C_i·B_j) Π_{r=j+1..i} a_r Δ_j x_j
+ * plus the state entering the chunk read through (Π_{r=start..i} a_r) C_i; between chunks only the
+ * state is passed: H_end = (Π_chunk a) H_start + Σ_j (Π_{r=j+1..end} a_r) Δ_j x_j B_j^T. */
+static void ssd_chunked_pair(const ssd_problem* p, int64_t pair) {
+  const int64_t b = pair / p->nheads;
+  const int h = (int)(pair % p->nheads);
+  const int P = p->headdim, N = p->dstate;
+  const int64_t Q = p->chunk;
+  double* H = (double*)malloc(sizeof(double) * (size_t)P * N);
+  double* Hn = (double*)malloc(sizeof(double) * (size_t)P * N);
+  double* a = (double*)malloc(sizeof(double) * (size_t)Q);
+  double* dl = (double*)malloc(sizeof(double) * (size_t)Q);
+  ssd_init_state(p, b, h, H);
+  for (int64_t s0 = 0; s0 < p->L; s0 += Q) {
+    const int64_t q = p->L - s0 < Q ? p->L - s0 : Q;
+    for (int64_t i = 0; i < q; ++i) {
+      dl[i] = ssd_delta(p, b, s0 + i, h);
+      a[i] = exp(dl[i] * p->A[h]);
+    }
+    for (int64_t i = 0; i < q; ++i) {
+      const double* Ci = ssd_bc(p, p->C, b, s0 + i, h);
+      double* y = p->y + ((b * p->L + s0 + i) * p->nheads + h) * P;
+      for (int k = 0; k < P; ++k) y[k] = 0.0;
+      double decay = 1.0;                       /* Π_{r=j+1..i} a_r */
+      for (int64_t j = i; j >= 0; --j) {
+        if (j < i) decay *= a[j + 1];
+        const double* Bj = ssd_bc(p, p->B, b, s0 + j, h);
+        double cb = 0.0;
+        for (int n = 0; n < N; ++n) cb += Ci[n] * Bj[n];
+        const double m = cb * decay * dl[j];
+        const double* xj = ssd_x(p, b, s0 + j, h);
+        for (int k = 0; k < P; ++k) y[k] += m * xj[k];
+      }
+      double into = 1.0;                        /* Π_{r=start..i} a_r */
+      for (int64_t r = 0; r <= i; ++r) into *= a[r];
+      const double* xi = ssd_x(p, b, s0 + i, h);
+      for (int k = 0; k < P; ++k) {
+        double s = 0.0;
+        for (int n = 0; n < N; ++n) s += Ci[n] * H[k * N + n];
+        y[k] += into * s + (p->D ? p->D[h] * xi[k] : 0.0);
+      }
+    }
+    double total = 1.0;
+    for (int64_t r = 0; r < q; ++r) total *= a[r];
+    for (int64_t i = 0; i < (int64_t)P * N; ++i) Hn[i] = total * H[i];
+    for (int64_t j = 0; j < q; ++j) {
+      double decay = 1.0;                       /* Π_{r=j+1..end} a_r */
+      for (int64_t r = j + 1; r < q; ++r) decay *= a[r];
+      const double* Bj = ssd_bc(p, p->B, b, s0 + j, h);
+      const double* xj = ssd_x(p, b, s0 + j, h);
+      for (int k = 0; k < P; ++k)
+        for (int n = 0; n < N; ++n) Hn[k * N + n] += decay * dl[j] * xj[k] * Bj[n];
+    }
+    memcpy(H, Hn, sizeof(double) * (size_t)P * N);
+  }
+  ssd_store_state(p, b, h, H);
+  free(H);
+  free(Hn);
+  free(a);
+  free(dl);
+}
+
+static void ssd_fn(const void* q, int64_t pair) {
+  const ssd_problem* p = (const ssd_problem*)q;
+  if (p->chunk > 0) ssd_chunked_pair(p, pair);
+  else ssd_sequential_pair(p, pair);
+}
+
+/* chunk = 0: the recurrence; chunk > 0: the chunked block form with that chunk length */
+ORACLE_API int oracle_ssd_scan(const double* x, const double* dt, const double* A, const double* B,
+                               const double* C, const double* D, const double* dt_bias, int softplus_flag,
+                               const double* h0, double* y, double* hT, int64_t batch, int64_t L, int nheads,
+                               int headdim, int dstate, int ngroups, int64_t chunk, int threads) {
+  if (!x || !dt || !A || !B || !C || !y || batch < 1 || L < 0 || nheads < 1 || headdim < 1 || dstate < 1 ||
+      ngroups < 1 || nheads % ngroups != 0 || chunk < 0)
+    return -1;
+  ssd_problem p;
+  p.x = x; p.dt = dt; p.A = A; p.B = B; p.C = C; p.D = D; p.dt_bias = dt_bias; p.h0 = h0;
+  p.y = y; p.hT = hT; p.softplus_flag = softplus_flag;
+  p.batch = batch; p.L = L; p.chunk = chunk;
+  p.nheads = nheads; p.headdim = headdim; p.dstate = dstate; p.ngroups = ngroups;
+  run_channels(ssd_fn, &p, batch * nheads, threads);
+  return 0;
+}

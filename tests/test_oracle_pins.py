@@ -15,7 +15,11 @@
 * a prefill followed by decode steps equals one longer prefill ("Модуль 8", §6/§14 caches);
 * the backward (reverse-mode) oracle against central finite differences of sum(dy * y) for every
   input, with and without softplus, gate and skip, and against the exact gradient of the A = 0,
-  no-gate case (y is then linear in u).
+  no-gate case (y is then linear in u);
+* the Mamba-2 SSD oracle (recurrence and chunked block form) against the semi-separable matrix
+  M_ij = C_i·B_j Π_{r=j+1..i} a_r Δ_j written out as an O(L²) brute force ("Модуль 8", §7), against
+  the already pinned Mamba-1 oracle (each (head, p) row is a Mamba-1 channel whose A row repeats the
+  head's scalar), and against numpy prefix sums when A = 0.
 
 Each mistake a plausible bug would make (a dropped D term, a sign error in the exponent, reading
 before updating, swapping B and C, the gate before the D skip, the conv tap order) fails at
@@ -377,6 +381,98 @@ def test_backward_of_a_linear_input_is_exact():
     np.testing.assert_allclose(g["du"][0, 0], ref, rtol=1e-12, atol=1e-13)
 
 
+# ---------------------------------------------------------------- Mamba-2 SSD ("Модуль 8", §7)
+
+def _ssd_inputs(seed, batch=2, L=29, nheads=4, headdim=3, dstate=5, ngroups=2, a_zero=False):
+    r = _rng(seed)
+    x = r.standard_normal((batch, L, nheads, headdim))
+    dt = r.standard_normal((batch, L, nheads))
+    A = np.zeros(nheads) if a_zero else -r.uniform(0.5, 2.0, nheads)
+    B = r.standard_normal((batch, L, ngroups, dstate))
+    C = r.standard_normal((batch, L, ngroups, dstate))
+    D = r.standard_normal(nheads)
+    bias = r.standard_normal(nheads) - 1.0
+    h0 = r.standard_normal((batch, nheads, headdim, dstate))
+    return x, dt, A, B, C, D, bias, h0
+
+
+def _ssd_bruteforce(x, dt, A, B, C, D, bias, h0):
+    """y = M x with M_ij = (C_i·B_j) Π_{r=j+1..i} a_r Δ_j for i ≥ j, plus the initial state read through
+    (Π_{r≤i} a_r) C_i, plus D x: the semi-separable matrix written out, O(L²) per head."""
+    batch, L, nheads, P = x.shape
+    G = B.shape[2]
+    y = np.zeros_like(x)
+    for b in range(batch):
+        for h in range(nheads):
+            g = h // (nheads // G)
+            dl = np.logaddexp(0.0, dt[b, :, h] + bias[h])
+            a = np.exp(dl * A[h])
+            for i in range(L):
+                for j in range(i + 1):
+                    m = float(C[b, i, g] @ B[b, j, g]) * float(np.prod(a[j + 1:i + 1])) * dl[j]
+                    y[b, i, h] += m * x[b, j, h]
+                y[b, i, h] += float(np.prod(a[:i + 1])) * (h0[b, h] @ C[b, i, g]) + D[h] * x[b, i, h]
+    return y
+
+
+def test_ssd_matches_semiseparable_bruteforce():
+    args = _ssd_inputs(31)
+    ref = _ssd_bruteforce(*args)
+    x, dt, A, B, C, D, bias, h0 = args
+    for chunk in (None, 4):
+        y, _ = oracle.ssd_scan(x, dt, A, B, C, D=D, dt_bias=bias, h0=h0, chunk=chunk)
+        assert np.max(np.abs(y - ref)) <= 1e-10 * max(1.0, np.max(np.abs(ref))), chunk
+
+
+def test_ssd_reduces_to_mamba1_channels():
+    """Each (head, p) row of the SSD is a Mamba-1 channel whose A row is the head's scalar repeated
+    over the states, with the head's Δ and the group's B and C."""
+    x, dt, A, B, C, D, bias, h0 = _ssd_inputs(32)
+    batch, L, nheads, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    y, hT = oracle.ssd_scan(x, dt, A, B, C, D=D, dt_bias=bias, h0=h0)
+    rows = [(b, h, q) for b in range(batch) for h in range(nheads) for q in range(P)]
+    u = np.array([x[b, :, h, q] for b, h, q in rows])
+    dl = np.array([dt[b, :, h] for b, h, q in rows])
+    Ar = np.array([np.full(N, A[h]) for b, h, q in rows])
+    Bm = np.stack([B[b, :, g].T for b in range(batch) for g in range(G)])     # (batch*G, N, L)
+    bidx = np.array([b * G + h // (nheads // G) for b, h, q in rows])
+    y1, h1 = oracle.selective_scan_channels(u, dl, Ar, Bm, np.stack([C[b, :, g].T for b in range(batch)
+                                                                     for g in range(G)]), bidx,
+                                            D=np.array([D[h] for b, h, q in rows]),
+                                            delta_bias=np.array([bias[h] for b, h, q in rows]),
+                                            h0=np.array([h0[b, h, q] for b, h, q in rows]))
+    got = np.array([y[b, :, h, q] for b, h, q in rows])
+    assert np.max(np.abs(got - y1)) <= 1e-12 * max(1.0, np.max(np.abs(y1)))
+    assert np.max(np.abs(np.array([hT[b, h, q] for b, h, q in rows]) - h1)) <= 1e-12 * max(1.0, np.max(np.abs(h1)))
+
+
+def test_ssd_a_zero_is_prefix_sum():
+    """A = 0: H_t = Σ_{s≤t} Δ_s x_s B_s^T (numpy cumsum), y_t = H_t C_t + D x_t."""
+    x, dt, A, B, C, D, bias, _ = _ssd_inputs(33, a_zero=True)
+    batch, L, nheads, P = x.shape
+    G = B.shape[2]
+    y, hT = oracle.ssd_scan(x, dt, A, B, C, D=D, dt_bias=bias)
+    for b in range(batch):
+        for h in range(nheads):
+            g = h // (nheads // G)
+            dl = np.logaddexp(0.0, dt[b, :, h] + bias[h])
+            terms = dl[:, None, None] * x[b, :, h][:, :, None] * B[b, :, g][:, None, :]    # (L, P, N)
+            Hs = np.cumsum(terms, axis=0)
+            ref = np.einsum("tpn,tn->tp", Hs, C[b, :, g]) + D[h] * x[b, :, h]
+            assert np.max(np.abs(y[b, :, h] - ref)) <= 1e-11 * max(1.0, np.max(np.abs(ref)))
+            assert np.max(np.abs(hT[b, h] - Hs[-1])) <= 1e-11 * max(1.0, np.max(np.abs(Hs[-1])))
+
+
+@pytest.mark.parametrize("chunk", [1, 3, 16, 29, 64])
+def test_ssd_chunked_equals_sequential(chunk):
+    x, dt, A, B, C, D, bias, h0 = _ssd_inputs(34)
+    y1, h1 = oracle.ssd_scan(x, dt, A, B, C, D=D, dt_bias=bias, h0=h0)
+    y2, h2 = oracle.ssd_scan(x, dt, A, B, C, D=D, dt_bias=bias, h0=h0, chunk=chunk)
+    assert np.max(np.abs(y1 - y2)) <= 1e-11 * max(1.0, np.max(np.abs(y1)))
+    assert np.max(np.abs(h1 - h2)) <= 1e-11 * max(1.0, np.max(np.abs(h1)))
+
+
 # ---------------------------------------------------------------- the pins catch planted mistakes
 
 _MUTATIONS = {
@@ -391,13 +487,19 @@ _MUTATIONS = {
                       "return v > 0.0 ? v + log1p(exp(v)) : log1p(exp(v));"),
     "conv_tap_order": ("s += w[c * K + k] * xpad[t + k];", "s += w[c * K + (K - 1 - k)] * xpad[t + k];"),
     "compose_order": ("*b_out = a2 * b1 + b2;", "*b_out = a1 * b2 + b1;"),
+    "ssd_decay_index": ("if (j < i) decay *= a[j + 1];", "if (j < i) decay *= a[j];"),
+    "ssd_group_index": ("const int g = h / (p->nheads / p->ngroups);", "const int g = h % p->ngroups;"),
+    "ssd_drop_D": ("y[i] = s + (p->D ? p->D[h] * x[i] : 0.0);", "y[i] = s;"),
+    "ssd_state_decay": ("H[i * N + n] = a * H[i * N + n] + dl * x[i] * Bt[n];",
+                        "H[i * N + n] = H[i * N + n] + dl * x[i] * Bt[n];"),
 }
 
 _PIN_TESTS = [test_compose_worked_example, test_zoh_epsilon_worked_example, test_a_zero_is_delta_weighted_prefix_sum,
               test_semiseparable_bruteforce_general_A, test_lti_reduces_to_convolution, test_zero_input_and_zero_gate,
               test_softplus_and_silu_identities, test_update_before_read_and_gate_after_skip,
               test_causal_conv_matches_numpy_convolve, test_decode_window_orientation,
-              test_prefill_then_decode_equals_longer_prefill]
+              test_prefill_then_decode_equals_longer_prefill, test_ssd_matches_semiseparable_bruteforce,
+              test_ssd_reduces_to_mamba1_channels, test_ssd_a_zero_is_prefix_sum]
 
 
 @pytest.mark.parametrize("name", sorted(_MUTATIONS))
