@@ -228,6 +228,29 @@ SSM_API ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A
                                 ssm_dtype io_dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Mamba-2 state space duality (SSD) forward: a scalar decay per head and a (headdim, dstate) state per
+ * head ("Mamba и State Space Models", "Mamba-2: State Space Duality (SSD)"; "Модуль 8", §7 and §14).
+ * Per batch b and head h, with g = h / (nheads / ngroups) the head's B/C group:
+ *     Δ_t = softplus(dt[b,t,h] + dt_bias[h])   (or dt + dt_bias when softplus_flag is 0)
+ *     H_t = exp(Δ_t A[h]) H_{t-1} + Δ_t x[b,t,h,:] B[b,t,g,:]^T,   H_{-1} = h0[b,h] (or zeros)
+ *     y[b,t,h,:] = H_t C[b,t,g,:] + D[h] x[b,t,h,:]
+ *   x, y          : (batch, seqlen, nheads, headdim) io_dtype
+ *   dt            : (batch, seqlen, nheads) io_dtype
+ *   B, C          : (batch, seqlen, ngroups, dstate) io_dtype
+ *   A, D, dt_bias : (nheads) float32; D and dt_bias may be NULL (zero)
+ *   h0            : (batch, nheads, headdim, dstate) float32 or NULL (zeros)
+ *   final_state   : (batch, nheads, headdim, dstate) float32 or NULL
+ * This build implements io_dtype SSM_BF16 with headdim 64 and dstate 128 (the pages' Mamba-2
+ * geometry); other values return SSM_ERR_UNSUPPORTED.  x, B, C and y must be 16-byte aligned, h0 and
+ * final_state 8-byte aligned.  Accumulation and the state are float32 (tensor-core products with the
+ * computed operand split into two bf16 terms); no workspace.
+ */
+SSM_API ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                               const float* D, const float* dt_bias, int softplus_flag, const float* h0, void* y,
+                               float* final_state, int batch, int64_t seqlen, int nheads, int headdim, int dstate,
+                               int ngroups, ssm_dtype io_dtype, cudaStream_t stream);
+
+/*
  * Reads and clears the device status word (synchronises `stream`).  Returns SSM_OK, SSM_ERR_TIMEOUT
  * if a kernel gave up a bounded wait since the last call, or SSM_ERR_CUDA.
  */

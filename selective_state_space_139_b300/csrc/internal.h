@@ -131,6 +131,27 @@ int bwd_segment_steps();
 int bwd_aggregate_floats();
 cudaError_t scan_bwd_launch(const BwdParams& p, cudaStream_t stream);
 
+// Mamba-2 SSD forward (ssd.cu): bf16 io, headdim 64, d_state 128.
+struct SsdParams {
+  const void* x;          // (batch, L, nheads, 64) bf16
+  const void* dt;         // (batch, L, nheads) bf16, before bias and softplus
+  const float* A;         // (nheads)
+  const void* B;          // (batch, L, ngroups, 128) bf16
+  const void* C;          // (batch, L, ngroups, 128) bf16
+  const float* D;         // (nheads) or null
+  const float* dt_bias;   // (nheads) or null
+  const float* h0;        // (batch, nheads, 64, 128) or null
+  void* y;                // (batch, L, nheads, 64) bf16
+  float* hT;              // (batch, nheads, 64, 128) or null
+  int batch, nheads, ngroups;
+  int64_t L;
+  int softplus;
+};
+
+int ssd_head_dim();
+int ssd_state_dim();
+cudaError_t ssd_fwd_launch(const SsdParams& p, cudaStream_t stream);
+
 // Sets the text returned by ssm_last_error_message() on the calling host thread (ssm_api.cu).
 void set_last_error(const char* fmt, ...);
 

@@ -690,3 +690,59 @@ ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A, const 
 }
 
 }  // extern "C"
+
+extern "C" {
+
+ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void* B, const void* C, const float* D,
+                       const float* dt_bias, int softplus_flag, const float* h0, void* y, float* final_state,
+                       int batch, int64_t seqlen, int nheads, int headdim, int dstate, int ngroups, ssm_dtype io_dtype,
+                       cudaStream_t stream) {
+  g_err[0] = 0;
+  if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return fail(SSM_ERR_INVALID_ARG, "unknown io_dtype %d", io_dtype);
+  if (batch < 1 || seqlen < 0 || nheads < 1 || headdim < 1 || dstate < 1 || ngroups < 1 || nheads % ngroups != 0)
+    return fail(SSM_ERR_INVALID_ARG, "bad sizes batch=%d seqlen=%lld nheads=%d headdim=%d dstate=%d ngroups=%d",
+                batch, static_cast<long long>(seqlen), nheads, headdim, dstate, ngroups);
+  if (io_dtype != SSM_BF16) return fail(SSM_ERR_UNSUPPORTED, "the SSD path supports bf16 io only");
+  if (headdim != ssm::ssd_head_dim() || dstate != ssm::ssd_state_dim())
+    return fail(SSM_ERR_UNSUPPORTED, "the SSD path supports headdim %d and dstate %d only", ssm::ssd_head_dim(),
+                ssm::ssd_state_dim());
+  if (batch > 65535) return fail(SSM_ERR_UNSUPPORTED, "batch=%d above 65535 is not supported", batch);
+  if (!A || (seqlen > 0 && (!x || !dt || !B || !C || !y)))
+    return fail(SSM_ERR_INVALID_ARG, "null required pointer (x, dt, A, B, C, y)");
+  for (const void* q : {x, B, C, static_cast<const void*>(y)})
+    if (q && !aligned(q, 16)) return fail(SSM_ERR_INVALID_ARG, "x, B, C and y must be 16-byte aligned");
+  if (dt && !aligned(dt, 2)) return fail(SSM_ERR_INVALID_ARG, "dt not aligned to its element size");
+  for (const void* q : {static_cast<const void*>(A), static_cast<const void*>(D), static_cast<const void*>(dt_bias)})
+    if (q && !aligned(q, 4)) return fail(SSM_ERR_INVALID_ARG, "float32 pointer not 4-byte aligned");
+  for (const void* q : {static_cast<const void*>(h0), static_cast<const void*>(final_state)})
+    if (q && !aligned(q, 8)) return fail(SSM_ERR_INVALID_ARG, "h0 and final_state must be 8-byte aligned");
+  const size_t e = 2;
+  const size_t xl = static_cast<size_t>(batch) * seqlen * nheads * headdim * e;
+  const size_t bcl = static_cast<size_t>(batch) * seqlen * ngroups * dstate * e;
+  const size_t st = static_cast<size_t>(batch) * nheads * headdim * dstate * 4;
+  const Range outs[] = {range_of(y, xl), range_of(final_state, final_state ? st : 0)};
+  const Range ins[] = {range_of(x, xl), range_of(dt, static_cast<size_t>(batch) * seqlen * nheads * e),
+                       range_of(B, bcl), range_of(C, bcl), range_of(A, nheads * 4), range_of(D, D ? nheads * 4 : 0),
+                       range_of(dt_bias, dt_bias ? nheads * 4 : 0), range_of(h0, h0 ? st : 0)};
+  for (const Range& o : outs)
+    for (const Range& i : ins)
+      if (overlap(o, i)) return fail(SSM_ERR_INVALID_ARG, "an output overlaps an input");
+  if (overlap(outs[0], outs[1])) return fail(SSM_ERR_INVALID_ARG, "y overlaps final_state");
+  if (seqlen == 0) {
+    if (final_state) {
+      cudaError_t ce = h0 ? cudaMemcpyAsync(final_state, h0, st, cudaMemcpyDeviceToDevice, stream)
+                          : cudaMemsetAsync(final_state, 0, st, stream);
+      if (ce != cudaSuccess) return cuda_fail(ce, "seqlen 0 state copy");
+    }
+    return SSM_OK;
+  }
+  ssm::SsdParams p;
+  memset(&p, 0, sizeof(p));
+  p.x = x; p.dt = dt; p.A = A; p.B = B; p.C = C; p.D = D; p.dt_bias = dt_bias; p.h0 = h0; p.y = y; p.hT = final_state;
+  p.batch = batch; p.nheads = nheads; p.ngroups = ngroups; p.L = seqlen; p.softplus = softplus_flag != 0;
+  cudaError_t ce = ssm::ssd_fwd_launch(p, stream);
+  if (ce != cudaSuccess) return cuda_fail(ce, "ssd launch");
+  return SSM_OK;
+}
+
+}  // extern "C"

@@ -77,6 +77,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ssm_causal_conv1d_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i64, i32, i32, i32, vp]
     lib.ssm_device_status.restype = i32
     lib.ssm_device_status.argtypes = [vp]
+    lib.ssm_ssd_fwd.restype = i32
+    lib.ssm_ssd_fwd.argtypes = [vp] * 7 + [i32, vp, vp, vp, i32, i64, i32, i32, i32, i32, i32, vp]
     lib.ssm_scan_bwd_workspace_size.restype = sz
     lib.ssm_scan_bwd_workspace_size.argtypes = [i32, i32, i32, i64, i32]
     lib.ssm_scan_bwd.restype = i32
@@ -308,6 +310,40 @@ def selective_scan_bwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B:
                               _stream_handle(stream))
     _check(lib, st)
     return g
+
+
+def ssd_fwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor, C: torch.Tensor,
+            D: Optional[torch.Tensor] = None, dt_bias: Optional[torch.Tensor] = None, dt_softplus: bool = True,
+            h0: Optional[torch.Tensor] = None, return_final_state: bool = True, *, out: Optional[torch.Tensor] = None,
+            final_state: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Mamba-2 SSD forward.  x (batch, L, nheads, headdim), dt (batch, L, nheads), B, C (batch, L,
+    ngroups, dstate) in bf16; A, D, dt_bias (nheads,) f32; h0 (batch, nheads, headdim, dstate) f32.
+    Returns (y, final state)."""
+    lib = load_library()
+    batch, L, nheads, headdim = x.shape
+    ngroups, dstate = B.shape[2], B.shape[3]
+    dev = x.device
+    io = x.dtype
+    _need(x, "x", (batch, L, nheads, headdim), io, dev)
+    _need(dt, "dt", (batch, L, nheads), io, dev)
+    _need(B, "B", (batch, L, ngroups, dstate), io, dev)
+    _need(C, "C", (batch, L, ngroups, dstate), io, dev)
+    _need(A, "A", (nheads,), torch.float32, dev)
+    _need(D, "D", (nheads,), torch.float32, dev, optional=True)
+    _need(dt_bias, "dt_bias", (nheads,), torch.float32, dev, optional=True)
+    _need(h0, "h0", (batch, nheads, headdim, dstate), torch.float32, dev, optional=True)
+    y = torch.empty_like(x) if out is None else out
+    _need(y, "out", (batch, L, nheads, headdim), io, dev)
+    if return_final_state and final_state is None:
+        final_state = torch.empty((batch, nheads, headdim, dstate), dtype=torch.float32, device=dev)
+    if final_state is not None:
+        _need(final_state, "final_state", (batch, nheads, headdim, dstate), torch.float32, dev)
+    with torch.cuda.device(dev):
+        st = lib.ssm_ssd_fwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(dt_bias),
+                             int(bool(dt_softplus)), _ptr(h0), _ptr(y), _ptr(final_state), batch, L, nheads, headdim,
+                             dstate, ngroups, _io_code(io), _stream_handle(stream))
+    _check(lib, st)
+    return y, final_state
 
 
 def device_status(stream=None) -> int:

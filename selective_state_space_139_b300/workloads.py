@@ -83,11 +83,47 @@ class DecodeWorkload:
                 self.dim * self.dstate * 4 + 2 * self.dim * 4)
 
 
+@dataclass(frozen=True)
+class SsdWorkload:
+    """Mamba-2 SSD layer: x (batch, L, nheads, headdim), B/C (batch, L, ngroups, dstate)."""
+    name: str
+    batch: int
+    seqlen: int
+    nheads: int
+    headdim: int
+    dstate: int
+    ngroups: int
+    seed: int
+    a_range: Tuple[float, float] = (1.0, 16.0)   # -A log-uniform in this range
+
+    @property
+    def tokens(self) -> int:
+        return self.batch * self.seqlen
+
+    def algorithmic_bytes(self) -> int:
+        """Reads of x, dt, B, C (bf16) and writes of y (bf16) and the final state (fp32), plus A, D, bias."""
+        bl = self.batch * self.seqlen
+        return (2 * bl * self.nheads * self.headdim + bl * self.nheads + 2 * bl * self.ngroups * self.dstate) * 2 + \
+            self.batch * self.nheads * self.headdim * self.dstate * 4 + 3 * self.nheads * 4
+
+    def flops(self) -> int:
+        """Multiply-adds x 2 of the chunked form with 64-step chunks: C B^T (causal half), the masked
+        product with x (causal half), C H^T and the state update, per (batch, head, chunk)."""
+        q, p_, n = 64, self.headdim, self.dstate
+        nch = (self.seqlen + q - 1) // q
+        per_chunk = q * q * n // 2 + q * q * p_ // 2 + q * n * p_ + q * p_ * n
+        return 2 * per_chunk * nch * self.batch * self.nheads
+
+
 WORKLOADS: Dict[str, object] = {
     "tiny-f32": ScanWorkload("tiny-f32", 1, 64, 16, 256, "f32", 1000),
     "mamba130m-layer": ScanWorkload("mamba130m-layer", 8, 1536, 16, 2048, "bf16", 1001),
     "mamba2.8b-layer": ScanWorkload("mamba2.8b-layer", 4, 5120, 16, 4096, "bf16", 1002, a_scale=(0.5, 2.0)),
     "long-dna": ScanWorkload("long-dna", 1, 1536, 16, 1 << 20, "bf16", 1003, symbol_alphabet=4),
+    # Mamba-2 geometry of "Модуль 8", §10: 8192 SSM channels in one B/C group, d_state 128
+    # (headdim 64, so 128 heads); batch and length as the 2.8B Mamba-1 layer
+    "mamba2-ssd-layer": SsdWorkload("mamba2-ssd-layer", 4, 4096, 128, 64, 128, 1, 1005),
+    "ssd-small": SsdWorkload("ssd-small", 2, 300, 6, 64, 128, 1, 1006),
     "decode-2.8b": DecodeWorkload("decode-2.8b", 256, 5120, 16, 4, 1000, "bf16", 1004, a_scale=(0.5, 2.0)),
 }
 
@@ -174,3 +210,22 @@ def random_scan_inputs(batch: int, dim: int, dstate: int, seqlen: int, io_dtype:
     w = ScanWorkload(f"adhoc-{batch}x{dim}x{dstate}x{seqlen}", batch, dim, dstate, seqlen, io_dtype, seed,
                      a_scale=a_scale)
     return make_scan_inputs(w, device=device)
+
+
+def make_ssd_inputs(w: SsdWorkload, device="cpu", seed: Optional[int] = None) -> Dict[str, torch.Tensor]:
+    """x, dt, B, C ~ N(0, 1) in bf16; A = -s with s log-uniform in ``a_range`` per head; D ~ N(0, 1);
+    dt_bias = log(expm1(s')) with s' log-uniform in [1e-3, 0.1] (softplus(dt_bias) = s'), all float32."""
+    seed = w.seed if seed is None else seed
+    g = _gen(seed, device)
+    bf = torch.bfloat16
+    out = {
+        "x": torch.randn((w.batch, w.seqlen, w.nheads, w.headdim), generator=g, device=device).to(bf),
+        "dt": torch.randn((w.batch, w.seqlen, w.nheads), generator=g, device=device).to(bf),
+        "B": torch.randn((w.batch, w.seqlen, w.ngroups, w.dstate), generator=g, device=device).to(bf),
+        "C": torch.randn((w.batch, w.seqlen, w.ngroups, w.dstate), generator=g, device=device).to(bf),
+    }
+    out["A"] = -_loguniform(w.nheads, w.a_range[0], w.a_range[1], g, device).to(torch.float32)
+    out["D"] = torch.randn(w.nheads, generator=g, device=device, dtype=torch.float32)
+    s = _loguniform(w.nheads, 1e-3, 1e-1, g, device)
+    out["dt_bias"] = torch.log(torch.expm1(s)).to(torch.float32)
+    return out

@@ -160,3 +160,24 @@ def test_scan_bwd_workspace_query(lib):
     assert lib.ssm_scan_bwd_workspace_size(2, 8, 17, 64, ssm.SSM_BF16) == 0
     # float32: double checkpoints plus double accumulators
     assert lib.ssm_scan_bwd_workspace_size(1, 128, 16, 64, ssm.SSM_F32) >= 128 * 8 * 16 * 8 + 2 * 16 * 64 * 8
+
+
+def test_ssd_rejects_bad_arguments_on_host(lib):
+    f = lib.ssm_ssd_fwd
+    base = dict(x=P, dt=P + 0x1000000, A=P + 0x2000000, B=P + 0x3000000, C=P + 0x4000000, D=None, bias=None, sp=1,
+                h0=None, y=P + 0x5000000, hT=None, batch=2, L=64, H=4, hd=64, N=128, G=1, io=ssm.SSM_BF16)
+
+    def call(**kw):
+        a = dict(base)
+        a.update(kw)
+        return f(a["x"], a["dt"], a["A"], a["B"], a["C"], a["D"], a["bias"], a["sp"], a["h0"], a["y"], a["hT"],
+                 a["batch"], a["L"], a["H"], a["hd"], a["N"], a["G"], a["io"], None)
+    assert call(io=ssm.SSM_F32) == ssm.SSM_ERR_UNSUPPORTED
+    assert call(hd=32) == ssm.SSM_ERR_UNSUPPORTED
+    assert call(N=64) == ssm.SSM_ERR_UNSUPPORTED
+    assert call(G=3) == ssm.SSM_ERR_INVALID_ARG          # 4 heads do not split into 3 groups
+    assert call(H=0) == ssm.SSM_ERR_INVALID_ARG
+    assert call(x=P + 8) == ssm.SSM_ERR_INVALID_ARG      # not 16-byte aligned
+    assert call(y=P + 0x100) == ssm.SSM_ERR_INVALID_ARG  # y overlaps x
+    assert call(dt=None) == ssm.SSM_ERR_INVALID_ARG
+    assert call(hT=P + 0x5000004) == ssm.SSM_ERR_INVALID_ARG   # misaligned final state

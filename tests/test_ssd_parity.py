@@ -1,0 +1,110 @@
+"""GPU parity of the Mamba-2 SSD forward (C ABI through the binding) against the fp64 oracle.
+
+bf16 io with float32 accumulation and state: max relative error (floor 1e-3 of the largest
+reference value) of 1e-2, the bound used for every bf16-io path.  Small and ragged shapes compare
+every output; the Mamba-2 layer compares sampled heads over all batch rows at full length, in the
+configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+from selective_state_space_139_b300 import ssm
+from selective_state_space_139_b300 import workloads as W
+from tests._helpers import max_rel_err, to64
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2
+
+
+def _dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")
+
+
+def _oracle(inp, heads=None, use_D=True, use_bias=True, softplus=True, h0=None):
+    sl = (lambda t: t) if heads is None else (lambda t: t[:, :, heads])
+    hs = (lambda t: t) if heads is None else (lambda t: t[heads])
+    return oracle.ssd_scan(to64(sl(inp["x"])), to64(sl(inp["dt"])), to64(hs(inp["A"])), to64(inp["B"]),
+                           to64(inp["C"]), D=to64(hs(inp["D"])) if use_D else None,
+                           dt_bias=to64(hs(inp["dt_bias"])) if use_bias else None, dt_softplus=softplus,
+                           h0=None if h0 is None else to64(h0 if heads is None else h0[:, heads]))
+
+
+def _run(inp, use_D=True, use_bias=True, softplus=True, h0=None):
+    y, hT = ssm.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], D=inp["D"] if use_D else None,
+                        dt_bias=inp["dt_bias"] if use_bias else None, dt_softplus=softplus, h0=h0)
+    torch.cuda.synchronize()
+    return y, hT
+
+
+def _check(y, hT, ry, rh):
+    ey, eh = max_rel_err(to64(y), ry), max_rel_err(to64(hT), rh)
+    assert ey <= TOL and eh <= TOL, (ey, eh)
+    return ey, eh
+
+
+def test_ssd_small_full():
+    dev = _dev()
+    inp = W.make_ssd_inputs(W.WORKLOADS["ssd-small"], device=dev)
+    y, hT = _run(inp)
+    _check(y, hT, *_oracle(inp))
+
+
+@pytest.mark.parametrize("L", [1, 63, 64, 65, 200])
+def test_ssd_ragged_lengths(L):
+    dev = _dev()
+    w = W.SsdWorkload("adhoc", 2, L, 3, 64, 128, 1, 2000 + L)
+    inp = W.make_ssd_inputs(w, device=dev)
+    y, hT = _run(inp)
+    _check(y, hT, *_oracle(inp))
+
+
+def test_ssd_groups_h0_and_options():
+    dev = _dev()
+    w = W.SsdWorkload("adhoc", 2, 150, 6, 64, 128, 3, 2101)
+    inp = W.make_ssd_inputs(w, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    h0 = torch.randn((2, 6, 64, 128), generator=g, device=dev)
+    y, hT = _run(inp, h0=h0)
+    _check(y, hT, *_oracle(inp, h0=h0))
+    y, hT = _run(inp, use_D=False, use_bias=False)
+    _check(y, hT, *_oracle(inp, use_D=False, use_bias=False))
+    inp["dt"] = (inp["dt"].float().abs() * 0.05).to(torch.bfloat16)      # positive steps without softplus
+    y, hT = _run(inp, softplus=False, use_bias=False)     # (the bias is negative: it would make Δ < 0)
+    _check(y, hT, *_oracle(inp, softplus=False, use_bias=False))
+
+
+def test_ssd_mamba2_layer_sampled_heads():
+    dev = _dev()
+    w = W.WORKLOADS["mamba2-ssd-layer"]
+    inp = W.make_ssd_inputs(w, device=dev)
+    y, hT = _run(inp)
+    heads = [0, 1, 77, w.nheads - 1]
+    ry, rh = _oracle(inp, heads=heads)
+    _check(y[:, :, heads], hT[:, heads], ry, rh)
+
+
+def test_ssd_seqlen_zero_passes_the_state_through():
+    dev = _dev()
+    w = W.SsdWorkload("adhoc", 1, 0, 2, 64, 128, 1, 2200)
+    inp = W.make_ssd_inputs(w, device=dev)
+    h0 = torch.randn((1, 2, 64, 128), device=dev)
+    y, hT = _run(inp, h0=h0)
+    assert y.numel() == 0 and torch.equal(hT, h0)
+
+
+def test_ssd_rejects_cpu_tensors_and_other_sizes():
+    dev = _dev()
+    w = W.SsdWorkload("adhoc", 1, 16, 2, 64, 128, 1, 2300)
+    cpu = W.make_ssd_inputs(w)
+    with pytest.raises(ValueError):
+        ssm.ssd_fwd(cpu["x"], cpu["dt"], cpu["A"], cpu["B"], cpu["C"])
+    inp = W.make_ssd_inputs(W.SsdWorkload("adhoc", 1, 16, 2, 32, 128, 1, 2301), device=dev)
+    with pytest.raises(ssm.SSMError):
+        ssm.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"])
