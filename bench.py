@@ -4,9 +4,9 @@
 Default workload: the Mamba-2.8B layer scan (batch 4, d_inner 5120, d_state 16, L 4096, bf16 io,
 float32 state).  One step = one ssm_scan_fwd call over that batch (every prefill row of the hot
 path: load, softplus, discretise, recurrence, readout + D skip, gate, store, final state).
-The decode row (batch 256, d_inner 5120, 1000 tokens), the conv1d + SiLU prefill and the scan
-backward are measured after it and reported in the same JSON line under "decode", "conv1d" and
-"backward".
+The decode row (batch 256, d_inner 5120, 1000 tokens), the conv1d + SiLU prefill, the scan
+backward and the Mamba-2 SSD layer are measured after it and reported in the same JSON line under
+"decode", "conv1d", "backward" and "ssd".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -43,6 +43,14 @@ def _peaks():
         return float(j["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def _bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (burst)"
+    except Exception:
+        return 1800.0, "fallback"
 
 
 def _dist():
@@ -191,7 +199,7 @@ def cpu_oracle_sample(w, target_s: float = 15.0):
 
 # ----------------------------------------------------------------------------- GPU measurement
 
-def measure_scan(w, steps, warmup, dev, rank, peak, peak_kind):
+def measure_scan(w, steps, warmup, dev, rank, peak, peak_kind, soak_s=1.0):
     import torch
     from selective_state_space_139_b300 import ssm
     from selective_state_space_139_b300 import workloads as W
@@ -211,7 +219,7 @@ def measure_scan(w, steps, warmup, dev, rank, peak, peak_kind):
 
     sampler = ClockSampler(dev.index if dev.index is not None else 0).start()
     # soak for ~1 s so that the clock record has samples under load, then the W warm-up steps
-    t_end = time.time() + 1.0
+    t_end = time.time() + soak_s
     while time.time() < t_end:
         step()
         torch.cuda.synchronize(dev)
@@ -371,6 +379,36 @@ def measure_bwd(w, dev, rank, reps=10):
             "tokens_per_s": w.batch * w.seqlen / (ms * 1e-3), "workspace_bytes": ws.numel()}
 
 
+def measure_ssd(dev, rank, reps=10):
+    """The Mamba-2 SSD forward on its layer workload: event-timed per call; algorithmic FLOPs of the
+    chunked form (64-step chunks) and algorithmic bytes as the workload defines them."""
+    import torch
+    from selective_state_space_139_b300 import ssm
+    from selective_state_space_139_b300 import workloads as W
+    w = W.WORKLOADS["mamba2-ssd-layer"]
+    inp = W.make_ssd_inputs(w, device=dev, seed=w.seed + rank)
+    y = torch.empty_like(inp["x"])
+    hT = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), device=dev)
+
+    def call():
+        ssm.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], D=inp["D"], dt_bias=inp["dt_bias"], out=y,
+                    final_state=hT)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize(dev)
+    times = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        b.record()
+        torch.cuda.synchronize(dev)
+        times.append(a.elapsed_time(b))
+    ms = statistics.median(times)
+    return {"workload": w, "ms": ms, "tokens_per_s": w.tokens / (ms * 1e-3),
+            "tflops": w.flops() / (ms * 1e-3) / 1e12, "achieved_gbs": w.algorithmic_bytes() / (ms * 1e-3) / 1e9}
+
+
 # ----------------------------------------------------------------------------- distributed helpers
 
 _PG = None
@@ -434,6 +472,27 @@ def run_reference(args, ws, rank):
     return 0
 
 
+def run_one_part(args, w, dev, rank, peak, peak_kind):
+    """One measured part alone (the command profiles are captured with): prints its numbers."""
+    from selective_state_space_139_b300 import workloads as W
+    if args.only == "scan":
+        r = measure_scan(w, args.steps, args.warmup, dev, rank, peak, peak_kind, soak_s=0.0 if args.no_soak else 1.0)
+        out = {"kernel_ms": r["kernel_ms"], "achieved_gbs": r["achieved_gbs"], "frac": r["achieved_gbs"] / peak}
+    elif args.only == "decode":
+        d = measure_decode(W.WORKLOADS["decode-2.8b"], args.decode_steps, dev, rank)
+        out = {"ms_per_token_step": d["ms_per_token_step"], "achieved_gbs": d["achieved_gbs"]}
+    elif args.only == "conv1d":
+        out = measure_conv(w, dev, rank, reps=args.steps)
+    elif args.only == "backward":
+        out = measure_bwd(w, dev, rank, reps=args.steps)
+    else:
+        out = measure_ssd(dev, rank, reps=args.steps)
+        out.pop("workload")
+    if rank == 0:
+        print(json.dumps({"part": args.only, "workload": w.name, **out}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -445,6 +504,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--no-ssd", action="store_true")
+    ap.add_argument("--only", default="all", choices=["all", "scan", "decode", "conv1d", "backward", "ssd"],
+                    help="measure one part alone (for profiler captures)")
+    ap.add_argument("--no-soak", action="store_true", help="skip the 1 s clock soak before the scan warm-up")
     ap.add_argument("--ref-budget", type=float, default=150.0,
                     help="seconds of oracle work for the whole --impl reference run")
     args = ap.parse_args()
@@ -466,7 +529,9 @@ def main():
     w = W.WORKLOADS[args.workload]
     if not isinstance(w, W.ScanWorkload):
         raise SystemExit("--workload must name a prefill workload; decode is reported under 'decode'")
-    r = measure_scan(w, args.steps, args.warmup, dev, rank, peak, peak_kind)
+    if args.only != "all":
+        return run_one_part(args, w, dev, rank, peak, peak_kind)
+    r = measure_scan(w, args.steps, args.warmup, dev, rank, peak, peak_kind, soak_s=0.0 if args.no_soak else 1.0)
     dec = None
     if not args.no_decode:
         dw = W.WORKLOADS["decode-2.8b"]
@@ -474,6 +539,7 @@ def main():
         dec["ms_per_token_step"] = _max_over_ranks(dec["ms_per_token_step"])
     conv = measure_conv(w, dev, rank)
     bwd = None if args.no_backward else measure_bwd(w, dev, rank)
+    ssd = None if args.no_ssd else measure_ssd(dev, rank)
     if rank != 0:
         return 0
     tokens_all = w.tokens * ws
@@ -508,6 +574,16 @@ def main():
                             "ms": bwd["ms"], "tokens_per_s": bwd["tokens_per_s"] * ws,
                             "achieved_gbs": bwd["achieved_gbs"], "frac": bwd["achieved_gbs"] / peak,
                             "bytes_per_call": bwd["bytes"], "workspace_bytes": bwd["workspace_bytes"]}
+    if ssd is not None:
+        sw = ssd["workload"]
+        tpeak, tkind = _bf16_peak()
+        line["ssd"] = {"workload": f"{sw.name} (batch {sw.batch}, L {sw.seqlen}, {sw.nheads} heads x {sw.headdim}, "
+                                   f"d_state {sw.dstate}, {sw.ngroups} group, bf16 io)",
+                       "ms": ssd["ms"], "tokens_per_s": ssd["tokens_per_s"] * ws,
+                       "roofline": {"bound": "tensor", "achieved": ssd["tflops"], "peak": tpeak, "unit": "TFLOP/s",
+                                    "frac": ssd["tflops"] / tpeak, "peak_source": tkind,
+                                    "flops_per_call": sw.flops()},
+                       "achieved_gbs": ssd["achieved_gbs"], "hbm_frac": ssd["achieved_gbs"] / peak}
     if not args.no_cpu_baseline:
         v, cores, sample, _ = cpu_oracle_sample(w)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}

@@ -134,23 +134,32 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_chunk_kernel(const SsdParams 
     }
   }
 
-  const int nchunks = static_cast<int>((L + kQ - 1) / kQ);
-  for (int c = 0; c < nchunks; ++c) {
-    const int64_t t0 = static_cast<int64_t>(c) * kQ;
-    // ---- loads of the chunk: x (64 rows x 128 B), B and C (64 rows x 256 B); zero rows past L
+  // chunk loads: x (64 rows x 128 B) and C, B (64 rows x 256 B); rows past L are zero-filled.  x and C
+  // of the next chunk are issued while the state update of the current one runs (they are free by
+  // then); B is used by that update and is loaded at the top of the next iteration.
+  auto load_x = [&](int64_t t0) {
     for (int i = tid; i < kQ * 8; i += kThreads) {
       const int j = i >> 3, q = i & 7;
       const bool ok = t0 + j < L;
       const __nv_bfloat16* src = xg + ((static_cast<int64_t>(b) * L + (ok ? t0 + j : 0)) * p.nheads + h) * kHd + q * 8;
       cp_async16(sb + SsdSmem::kX + j * kXPitch + q * 16, src, ok ? 16 : 0);
     }
+  };
+  auto load_bc = [&](int64_t t0, int off) {
+    const __nv_bfloat16* base = off == SsdSmem::kB ? Bg : Cg;
     for (int i = tid; i < kQ * 16; i += kThreads) {
       const int j = i >> 4, q = i & 15;
       const bool ok = t0 + j < L;
       const int64_t row = (static_cast<int64_t>(b) * L + (ok ? t0 + j : 0)) * p.ngroups + grp;
-      cp_async16(sb + SsdSmem::kB + j * kBPitch + q * 16, Bg + row * kNs + q * 8, ok ? 16 : 0);
-      cp_async16(sb + SsdSmem::kC + j * kBPitch + q * 16, Cg + row * kNs + q * 8, ok ? 16 : 0);
+      cp_async16(sb + off + j * kBPitch + q * 16, base + row * kNs + q * 8, ok ? 16 : 0);
     }
+  };
+  const int nchunks = static_cast<int>((L + kQ - 1) / kQ);
+  load_x(0);
+  load_bc(0, SsdSmem::kC);
+  for (int c = 0; c < nchunks; ++c) {
+    const int64_t t0 = static_cast<int64_t>(c) * kQ;
+    load_bc(t0, SsdSmem::kB);
     // ---- Δ and the inclusive prefix of Δ·A (log2 units) over the chunk: warps 0 and 1
     if (tid < kQ) {
       const int64_t t = t0 + tid;
@@ -189,15 +198,23 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_chunk_kernel(const SsdParams 
       ldsm_x4(a_addr(sb + SsdSmem::kC, kBPitch, warp * 16, ks * 16, lane), a[0], a[1], a[2], a[3]);
       // e^{cum_i} C H^T (the state entering the chunk), hi and lo parts of H
       if (have_state) {
+        // all fragments first, then the MMAs cycling over the eight accumulators (no back-to-back
+        // dependent MMAs)
+        uint32_t bh[4][4], bl[4][4];
 #pragma unroll
         for (int pt = 0; pt < 4; ++pt) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(b_addr(sb + SsdSmem::kHh, kBPitch, pt * 16, ks * 16, lane), b0, b1, b2, b3);
-          mma16816(acc[2 * pt], a, b0, b1);
-          mma16816(acc[2 * pt + 1], a, b2, b3);
-          ldsm_x4(b_addr(sb + SsdSmem::kHl, kBPitch, pt * 16, ks * 16, lane), b0, b1, b2, b3);
-          mma16816(acc[2 * pt], a, b0, b1);
-          mma16816(acc[2 * pt + 1], a, b2, b3);
+          ldsm_x4(b_addr(sb + SsdSmem::kHh, kBPitch, pt * 16, ks * 16, lane), bh[pt][0], bh[pt][1], bh[pt][2], bh[pt][3]);
+          ldsm_x4(b_addr(sb + SsdSmem::kHl, kBPitch, pt * 16, ks * 16, lane), bl[pt][0], bl[pt][1], bl[pt][2], bl[pt][3]);
+        }
+#pragma unroll
+        for (int pt = 0; pt < 4; ++pt) {
+          mma16816(acc[2 * pt], a, bh[pt][0], bh[pt][1]);
+          mma16816(acc[2 * pt + 1], a, bh[pt][2], bh[pt][3]);
+        }
+#pragma unroll
+        for (int pt = 0; pt < 4; ++pt) {
+          mma16816(acc[2 * pt], a, bl[pt][0], bl[pt][1]);
+          mma16816(acc[2 * pt + 1], a, bl[pt][2], bl[pt][3]);
         }
       }
       // G = C B^T for the causal j tiles 0 .. 2w+1
@@ -245,14 +262,19 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_chunk_kernel(const SsdParams 
         split2(m[2], m[3], ah[1], al[1]);
         split2(m[4], m[5], ah[2], al[2]);
         split2(m[6], m[7], ah[3], al[3]);
+        uint32_t bx[4][4];
+#pragma unroll
+        for (int pt = 0; pt < 4; ++pt)
+          ldsm_x4_t(b_addr_t(sb + SsdSmem::kX, kXPitch, pt * 16, s * 16, lane), bx[pt][0], bx[pt][1], bx[pt][2], bx[pt][3]);
 #pragma unroll
         for (int pt = 0; pt < 4; ++pt) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(b_addr_t(sb + SsdSmem::kX, kXPitch, pt * 16, s * 16, lane), b0, b1, b2, b3);
-          mma16816(acc[2 * pt], ah, b0, b1);
-          mma16816(acc[2 * pt + 1], ah, b2, b3);
-          mma16816(acc[2 * pt], al, b0, b1);
-          mma16816(acc[2 * pt + 1], al, b2, b3);
+          mma16816(acc[2 * pt], ah, bx[pt][0], bx[pt][1]);
+          mma16816(acc[2 * pt + 1], ah, bx[pt][2], bx[pt][3]);
+        }
+#pragma unroll
+        for (int pt = 0; pt < 4; ++pt) {
+          mma16816(acc[2 * pt], al, bx[pt][0], bx[pt][1]);
+          mma16816(acc[2 * pt + 1], al, bx[pt][2], bx[pt][3]);
         }
       }
     }
@@ -288,7 +310,11 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_chunk_kernel(const SsdParams 
         *reinterpret_cast<uint32_t*>(smem + SsdSmem::kWl + j * kXPitch + (p0 + 2 * q) * 2) = lo;
       }
     }
-    __syncthreads();   // (w ∘ x) complete; every warp is done reading H for the outputs
+    __syncthreads();   // (w ∘ x) complete; every warp is done reading H, x and C for the outputs
+    if (c + 1 < nchunks) {
+      load_x(t0 + kQ);
+      load_bc(t0 + kQ, SsdSmem::kC);
+    }
     {
       const float eE = ex2_approx(cum_end);
 #pragma unroll
@@ -305,13 +331,22 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_chunk_kernel(const SsdParams 
       ldsm_x4_t(a_addr_t(sb + SsdSmem::kWh, kXPitch, warp * 16, ks * 16, lane), ah[0], ah[1], ah[2], ah[3]);
       ldsm_x4_t(a_addr_t(sb + SsdSmem::kWl, kXPitch, warp * 16, ks * 16, lane), al[0], al[1], al[2], al[3]);
 #pragma unroll
-      for (int np = 0; np < 8; ++np) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(b_addr_t(sb + SsdSmem::kB, kBPitch, np * 16, ks * 16, lane), b0, b1, b2, b3);
-        mma16816(hacc[2 * np], ah, b0, b1);
-        mma16816(hacc[2 * np + 1], ah, b2, b3);
-        mma16816(hacc[2 * np], al, b0, b1);
-        mma16816(hacc[2 * np + 1], al, b2, b3);
+      for (int half = 0; half < 2; ++half) {   // 4 n-tile pairs at a time: hi MMAs over 8 accumulators, then lo
+        uint32_t bb[4][4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          ldsm_x4_t(b_addr_t(sb + SsdSmem::kB, kBPitch, (half * 4 + q) * 16, ks * 16, lane), bb[q][0], bb[q][1],
+                    bb[q][2], bb[q][3]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          mma16816(hacc[2 * (half * 4 + q)], ah, bb[q][0], bb[q][1]);
+          mma16816(hacc[2 * (half * 4 + q) + 1], ah, bb[q][2], bb[q][3]);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          mma16816(hacc[2 * (half * 4 + q)], al, bb[q][0], bb[q][1]);
+          mma16816(hacc[2 * (half * 4 + q) + 1], al, bb[q][2], bb[q][3]);
+        }
       }
     }
     // the new state as the hi/lo B operand of the next chunk
