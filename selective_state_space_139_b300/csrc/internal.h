@@ -151,6 +151,8 @@ struct SsdParams {
 int ssd_head_dim();
 int ssd_state_dim();
 cudaError_t ssd_fwd_launch(const SsdParams& p, cudaStream_t stream);
+cudaError_t ssd_tc_launch(const SsdParams& p, cudaStream_t stream);     // tcgen05 kernel (ssd_tc.cu)
+cudaError_t ssd_status_read_and_clear(unsigned int* out);
 
 // Sets the text returned by ssm_last_error_message() on the calling host thread (ssm_api.cu).
 void set_last_error(const char* fmt, ...);

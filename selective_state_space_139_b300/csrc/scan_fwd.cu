@@ -543,6 +543,10 @@ cudaError_t read_and_clear_device_status(unsigned int* out, cudaStream_t stream)
   unsigned int fast = 0;
   e = fast_status_read_and_clear(&fast);
   *out |= fast;
+  if (e != cudaSuccess) return e;
+  unsigned int ssd = 0;
+  e = ssd_status_read_and_clear(&ssd);
+  *out |= ssd;
   return e;
 }
 

@@ -22,6 +22,10 @@
 #include "internal.h"
 #include "ssm_device.cuh"
 
+#ifndef SSM_SSD_TCGEN05
+#define SSM_SSD_TCGEN05 1   // 1: the tcgen05 kernel (ssd_tc.cu); 0: this mma.sync kernel
+#endif
+
 namespace ssm {
 namespace {
 
@@ -383,6 +387,7 @@ int ssd_head_dim() { return kHd; }
 int ssd_state_dim() { return kNs; }
 
 cudaError_t ssd_fwd_launch(const SsdParams& p, cudaStream_t stream) {
+  if (SSM_SSD_TCGEN05) return ssd_tc_launch(p, stream);
   cudaError_t e = cudaFuncSetAttribute(ssd_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SsdSmem::kTot);
   if (e != cudaSuccess) return e;
   ssd_chunk_kernel<<<dim3(p.nheads, p.batch), kThreads, SsdSmem::kTot, stream>>>(p);

@@ -1,0 +1,445 @@
+// Mamba-2 SSD forward on the fifth-generation tensor cores (tcgen05, accumulators in tensor memory).
+// Same operator and chunked block form as ssd.cu ("Mamba и State Space Models", "Mamba-2: State Space
+// Duality (SSD)"; "Модуль 8. Альтернативы Transformer", §7 and §14):
+//   y_i = Σ_{j≤i} (C_i·B_j) e^{cum_i − cum_j} Δ_j x_j + e^{cum_i} C_i·H + D_h x_i
+//   H  <- e^{cum_end} H + Σ_j e^{cum_end − cum_j} Δ_j x_j B_j^T
+// over chunks of 64 steps, one CTA (4 warps) per (batch, head), two CTAs per SM.
+//
+// Per chunk, four tcgen05.mma groups (bf16 operands from 128-byte-swizzled shared tiles, fp32
+// accumulators in tensor memory):
+//   G   = C B^T          M 64 (i) x N 64 (j) x K 128 (n)   A: C [i][n] K-major, B: B [j][n] K-major
+//   Yo  = C H^T          M 64 (i) x N 64 (p) x K 128 (n)   B: H^T stored [n][p] (MN-major), hi + lo
+//   S^T = B^T (w ∘ x)    M 128 (n) x N 64 (p) x K 64 (j)   A: the same B tile read MN-major, B: (w ∘ x) [j][p]
+//   Yd  = M X            M 64 (i) x N 64 (p) x K 64 (j)    A: M [i][j] K-major (hi + lo), B: x [j][p] MN-major
+// The K-major 128-byte-swizzled tile of B[j][n] is byte for byte the MN-major tile of B^T, so one copy
+// serves both products and nothing is transposed.  The CUDA cores do the element-wise parts: Δ and its
+// prefix sum, M = G ∘ e^{cum_i − cum_j} Δ_j (causal) from the G accumulator, w ∘ x, the state update
+// H = e^{cum_end} H + S^T (thread n owns column n of H in registers) and the output y.
+// As in ssd.cu, x, B, C enter the MMAs exactly and every computed operand (M, H, w ∘ x) is split into
+// two bf16 terms, so products keep float32-level accuracy.
+// Tensor memory: columns [0, 64) G then Yd (M = 64 rows sit in lanes 32w .. 32w + 15 of warp w),
+// [64, 128) Yo, [128, 192) S^T (row n in lane n); 256 columns are allocated per CTA.
+// Every mbarrier wait is bounded; on a timeout the CTA records it, stops and frees its tensor memory.
+#include "internal.h"
+#include "ssm_device.cuh"
+
+namespace ssm {
+namespace {
+
+__device__ unsigned int g_ssd_status = 0;
+
+constexpr int kQ = 64;         // chunk length
+constexpr int kHd = 64;        // head dim
+constexpr int kNs = 128;       // d_state
+constexpr int kThreads = 128;
+constexpr uint32_t kTmemCols = 256;
+
+// tiles (byte offsets from a 1024-byte aligned base); every tile is 128-byte swizzled
+struct TcSmem {
+  static constexpr int kC = 0;        // C [i][n]: 2 atoms (n 0..63, 64..127) of 64 rows x 128 B
+  static constexpr int kB = 16384;    // B [j][n]: same layout
+  static constexpr int kX = 32768;    // x [j][p]: 64 rows x 128 B
+  static constexpr int kWh = 40960;   // (w ∘ x) hi [j][p]
+  static constexpr int kWl = 49152;   // (w ∘ x) lo
+  static constexpr int kMh = 57344;   // M hi [i][j]
+  static constexpr int kMl = 65536;   // M lo
+  static constexpr int kHh = 73728;   // H^T hi [n][p]: 128 rows x 128 B
+  static constexpr int kHl = 90112;   // H^T lo
+  static constexpr int kTiles = 106496;
+  static constexpr int kDynamic = kTiles + 1024;
+};
+
+// byte offset of the 16-byte chunk `c` (0..7 inside a 128-byte row) of row r in a 128-byte swizzled
+// tile region (rows of 128 B, 8-row groups of 1024 B)
+__device__ __forceinline__ uint32_t sw_chunk(int r, int c) {
+  return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// shared-memory matrix descriptor: start, leading and stride byte offsets, version 1, 128-byte swizzle
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
+}
+// instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, major-ness of A and B, N, M
+__device__ __forceinline__ uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+         (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// 32 consecutive fp32 columns of this thread's tensor-memory lane (warp-collective)
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// The M = 64 accumulator rows of this warp (16 rows in lanes 32w .. 32w + 15) in the m16n8 fragment
+// layout: with g = lane / 4 and t = lane % 4, v[4r .. 4r + 3] = rows (g, g, g + 8, g + 8), columns
+// (8r + 2t, 8r + 2t + 1, 8r + 2t, 8r + 2t + 1) for r = 0..7 (64 columns from `taddr`; warp-collective).
+__device__ __forceinline__ void tc_ld_frag64(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+// fp32 pair -> bf16x2 hi and bf16x2 of the remainders
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16x2(a, b);
+  lo = pack_bf16x2(a - bf16lo_to_f32(hi), b - bf16hi_to_f32(hi));
+}
+
+// 8 fp32 -> the hi and lo 16-byte chunks
+__device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo) {
+  split2(v[0], v[1], hi.x, lo.x);
+  split2(v[2], v[3], hi.y, lo.y);
+  split2(v[4], v[5], hi.z, lo.z);
+  split2(v[6], v[7], hi.w, lo.w);
+}
+
+__global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bars[3];
+  __shared__ uint32_t tmem_slot;
+  __shared__ __align__(16) float s_dl[kQ];
+  __shared__ __align__(16) float s_cum[kQ];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int grp = h / (p.nheads / p.ngroups);
+  const int64_t L = p.L;
+  const float A2 = p.A[h] * kLog2e;
+  const float bias = p.dt_bias ? p.dt_bias[h] : 0.0f;
+  const float Dh = p.D ? p.D[h] : 0.0f;
+  const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(p.x);
+  const __nv_bfloat16* dtg = static_cast<const __nv_bfloat16*>(p.dt);
+  const __nv_bfloat16* Bg = static_cast<const __nv_bfloat16*>(p.B);
+  const __nv_bfloat16* Cg = static_cast<const __nv_bfloat16*>(p.C);
+  __nv_bfloat16* yg = static_cast<__nv_bfloat16*>(p.y);
+
+  if (tid == 0) {
+    for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+
+  // the state: thread n holds column n of H (64 values of p) in fp32
+  const int n_own = tid;
+  float H[kHd];
+  bool have_state = p.h0 != nullptr;
+  {
+    const float* h0 = p.h0 ? p.h0 + (static_cast<int64_t>(b) * p.nheads + h) * kHd * kNs : nullptr;
+#pragma unroll
+    for (int q = 0; q < kHd; ++q) H[q] = h0 ? h0[q * kNs + n_own] : 0.0f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint4 hi, lo;
+      split8(&H[c * 8], hi, lo);
+      *reinterpret_cast<uint4*>(sm + TcSmem::kHh + sw_chunk(n_own, c)) = hi;
+      *reinterpret_cast<uint4*>(sm + TcSmem::kHl + sw_chunk(n_own, c)) = lo;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t t_lane = static_cast<uint32_t>(warp * 32) << 16;   // this warp's lane quadrant
+
+  const uint32_t id_g = idesc_bf16(64, 64, 0, 0);
+  const uint32_t id_yo = idesc_bf16(64, 64, 0, 1);
+  const uint32_t id_s = idesc_bf16(128, 64, 1, 1);
+  const uint32_t id_yd = idesc_bf16(64, 64, 0, 1);
+
+  // tile loaders (rows past L are zero-filled); each tile of chunk c + 1 is requested as soon as the
+  // tensor cores and the threads are done with that tile of chunk c
+  auto load_bc = [&](int64_t t0, int off, const __nv_bfloat16* src_base) {
+    for (int i = tid; i < kQ * 16; i += kThreads) {
+      const int r = i >> 4, q = i & 15;
+      const bool in = t0 + r < L;
+      const int64_t row = (static_cast<int64_t>(b) * L + (in ? t0 + r : 0)) * p.ngroups + grp;
+      cp_async16(sb + off + (q >> 3) * (kQ * 128) + sw_chunk(r, q & 7), src_base + row * kNs + q * 8, in ? 16 : 0);
+    }
+  };
+  auto load_x = [&](int64_t t0) {
+    for (int i = tid; i < kQ * 8; i += kThreads) {
+      const int r = i >> 3, q = i & 7;
+      const bool in = t0 + r < L;
+      const __nv_bfloat16* src = xg + ((static_cast<int64_t>(b) * L + (in ? t0 + r : 0)) * p.nheads + h) * kHd + q * 8;
+      cp_async16(sb + TcSmem::kX + sw_chunk(r, q), src, in ? 16 : 0);
+    }
+  };
+  auto load_dl = [&](int64_t t) -> float {
+    if (t >= L) return 0.0f;
+    const float v = __bfloat162float(dtg[(static_cast<int64_t>(b) * L + t) * p.nheads + h]) + bias;
+    return p.softplus ? softplus_fast(v) : v;
+  };
+  const int nchunks = static_cast<int>((L + kQ - 1) / kQ);
+  load_bc(0, TcSmem::kC, Cg);
+  load_bc(0, TcSmem::kB, Bg);
+  load_x(0);
+  float2 dt_next = warp == 0 ? make_float2(load_dl(2 * lane), load_dl(2 * lane + 1)) : make_float2(0.0f, 0.0f);
+  bool ok = true;
+  for (int c = 0; c < nchunks && ok; ++c) {
+    const int64_t t0 = static_cast<int64_t>(c) * kQ;
+    const uint32_t par = static_cast<uint32_t>(c & 1);
+    const bool ys = have_state;   // a state enters this chunk
+    // ---- P0: Δ and its inclusive prefix sum over the chunk, by warp 0 (two steps per lane); the
+    // chunk's tiles were requested during the previous chunk
+    if (warp == 0) {
+      const float d0 = dt_next.x, d1 = dt_next.y;
+      if (c + 1 < nchunks) dt_next = make_float2(load_dl(t0 + kQ + 2 * lane), load_dl(t0 + kQ + 2 * lane + 1));
+      const float a0 = d0 * A2;
+      float s2 = a0 + d1 * A2;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, s2, o);
+        if (lane >= o) s2 += u;
+      }
+      const float before = __shfl_up_sync(0xffffffffu, s2, 1);
+      const float base = lane > 0 ? before : 0.0f;
+      *reinterpret_cast<float2*>(&s_dl[2 * lane]) = make_float2(d0, d1);
+      *reinterpret_cast<float2*>(&s_cum[2 * lane]) = make_float2(base + a0, s2);
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---- P1: G = C B^T and Yo = C H^T on the tensor cores; meanwhile w ∘ x on the CUDA cores
+    if (tid == 0) {
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t ka = (ks >> 2) * (kQ * 128) + (ks & 3) * 32;
+        tc_mma(tmem + 0, sdesc(sb + TcSmem::kC + ka, 16, 1024), sdesc(sb + TcSmem::kB + ka, 16, 1024), id_g, ks > 0);
+      }
+      if (ys) {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t ka = (ks >> 2) * (kQ * 128) + (ks & 3) * 32;
+          tc_mma(tmem + 64, sdesc(sb + TcSmem::kC + ka, 16, 1024), sdesc(sb + TcSmem::kHh + ks * 2048, 16384, 1024),
+                 id_yo, ks > 0);
+        }
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t ka = (ks >> 2) * (kQ * 128) + (ks & 3) * 32;
+          tc_mma(tmem + 64, sdesc(sb + TcSmem::kC + ka, 16, 1024), sdesc(sb + TcSmem::kHl + ks * 2048, 16384, 1024),
+                 id_yo, 1);
+        }
+      }
+      tc_commit(&bars[0]);
+    }
+    const float cum_end = s_cum[kQ - 1];
+    {
+      const int j = tid >> 1, c0 = (tid & 1) * 4;
+      const float wj = ex2_approx(cum_end - s_cum[j]) * s_dl[j];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t o = sw_chunk(j, c0 + q);
+        float v[8];
+        unpack_chunk(*reinterpret_cast<const uint4*>(sm + TcSmem::kX + o), v, __nv_bfloat16());
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] *= wj;
+        uint4 hi, lo;
+        split8(v, hi, lo);
+        *reinterpret_cast<uint4*>(sm + TcSmem::kWh + o) = hi;
+        *reinterpret_cast<uint4*>(sm + TcSmem::kWl + o) = lo;
+      }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---- P2: S^T = B^T (w ∘ x) on the tensor cores; M = G ∘ e^{cum_i − cum_j} Δ_j on the CUDA cores
+    if (tid == 0) {
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        tc_mma(tmem + 128, sdesc(sb + TcSmem::kB + ks * 2048, kQ * 128, 1024),
+               sdesc(sb + TcSmem::kWh + ks * 2048, kQ * 128, 1024), id_s, ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        tc_mma(tmem + 128, sdesc(sb + TcSmem::kB + ks * 2048, kQ * 128, 1024),
+               sdesc(sb + TcSmem::kWl + ks * 2048, kQ * 128, 1024), id_s, 1);
+      tc_commit(&bars[1]);
+    }
+    ok = mbar_wait_bounded(&bars[0], par, &g_ssd_status);
+    ok = __all_sync(0xffffffffu, ok);   // the tensor-memory loads below are warp-collective
+    tc_fence_after();
+    if (ok && c + 1 < nchunks) load_bc(t0 + kQ, TcSmem::kC, Cg);   // G and Yo are done with C
+    const int fg = lane >> 2, ft = lane & 3;             // fragment row and column pair of this lane
+    const int ri0 = warp * 16 + fg, ri1 = ri0 + 8;       // its two rows of the M = 64 results
+    if (ok) {
+      const float cr0 = s_cum[ri0], cr1 = s_cum[ri1];
+      float g[32];
+      tc_ld_frag64(tmem + t_lane + 0, g);
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const int j = 8 * r + 2 * ft;
+        const float2 cj = *reinterpret_cast<const float2*>(&s_cum[j]);
+        const float2 dj = *reinterpret_cast<const float2*>(&s_dl[j]);
+        const float m00 = j <= ri0 ? g[4 * r] * ex2_approx(cr0 - cj.x) * dj.x : 0.0f;
+        const float m01 = j + 1 <= ri0 ? g[4 * r + 1] * ex2_approx(cr0 - cj.y) * dj.y : 0.0f;
+        const float m10 = j <= ri1 ? g[4 * r + 2] * ex2_approx(cr1 - cj.x) * dj.x : 0.0f;
+        const float m11 = j + 1 <= ri1 ? g[4 * r + 3] * ex2_approx(cr1 - cj.y) * dj.y : 0.0f;
+        uint32_t hi, lo;
+        const uint32_t o0 = sw_chunk(ri0, r) + 4 * ft, o1 = sw_chunk(ri1, r) + 4 * ft;
+        split2(m00, m01, hi, lo);
+        *reinterpret_cast<uint32_t*>(sm + TcSmem::kMh + o0) = hi;
+        *reinterpret_cast<uint32_t*>(sm + TcSmem::kMl + o0) = lo;
+        split2(m10, m11, hi, lo);
+        *reinterpret_cast<uint32_t*>(sm + TcSmem::kMh + o1) = hi;
+        *reinterpret_cast<uint32_t*>(sm + TcSmem::kMl + o1) = lo;
+      }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    ok = __syncthreads_and(ok) != 0;
+    tc_fence_after();
+    if (!ok) break;
+
+    // ---- P3: Yd = M X on the tensor cores; the state update on the CUDA cores
+    if (tid == 0) {
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        tc_mma(tmem + 0, sdesc(sb + TcSmem::kMh + ks * 32, 16, 1024), sdesc(sb + TcSmem::kX + ks * 2048, kQ * 128, 1024),
+               id_yd, ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        tc_mma(tmem + 0, sdesc(sb + TcSmem::kMl + ks * 32, 16, 1024), sdesc(sb + TcSmem::kX + ks * 2048, kQ * 128, 1024),
+               id_yd, 1);
+      tc_commit(&bars[2]);
+    }
+    ok = mbar_wait_bounded(&bars[1], par, &g_ssd_status);
+    ok = __all_sync(0xffffffffu, ok);   // the tensor-memory loads below are warp-collective
+    tc_fence_after();
+    if (ok && c + 1 < nchunks) load_bc(t0 + kQ, TcSmem::kB, Bg);   // G and S^T are done with B
+    if (ok) {
+      const float eE = ex2_approx(cum_end);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float s[32];
+        tc_ld32(tmem + t_lane + 128 + half * 32, s);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) H[half * 32 + q] = fmaf(eE, H[half * 32 + q], s[q]);
+      }
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        uint4 hi, lo;
+        split8(&H[c8 * 8], hi, lo);
+        *reinterpret_cast<uint4*>(sm + TcSmem::kHh + sw_chunk(n_own, c8)) = hi;
+        *reinterpret_cast<uint4*>(sm + TcSmem::kHl + sw_chunk(n_own, c8)) = lo;
+      }
+    }
+    have_state = true;
+
+    // ---- P4: y = Yd + e^{cum_i} Yo + D x.  The x values this lane needs are taken into registers
+    // first so that the next chunk's x can be requested before the output work.
+    ok = ok && mbar_wait_bounded(&bars[2], par, &g_ssd_status);
+    ok = __all_sync(0xffffffffu, ok);   // the tensor-memory loads below are warp-collective
+    uint32_t xw[16];   // x at this lane's fragment positions, bf16 pairs: [r][row half]
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      xw[2 * r] = *reinterpret_cast<const uint32_t*>(sm + TcSmem::kX + sw_chunk(ri0, r) + 4 * ft);
+      xw[2 * r + 1] = *reinterpret_cast<const uint32_t*>(sm + TcSmem::kX + sw_chunk(ri1, r) + 4 * ft);
+    }
+    tc_fence_before();
+    ok = __syncthreads_and(ok) != 0;   // Yd and every thread are done with x
+    tc_fence_after();
+    if (ok && c + 1 < nchunks) load_x(t0 + kQ);
+    if (ok) {
+      const float e0 = ex2_approx(s_cum[ri0]), e1 = ex2_approx(s_cum[ri1]);
+      float yd[32], yo[32];
+      tc_ld_frag64(tmem + t_lane + 0, yd);
+      if (ys) tc_ld_frag64(tmem + t_lane + 64, yo);
+      __nv_bfloat16* y0 = yg + ((static_cast<int64_t>(b) * L + t0 + ri0) * p.nheads + h) * kHd;
+      __nv_bfloat16* y1 = yg + ((static_cast<int64_t>(b) * L + t0 + ri1) * p.nheads + h) * kHd;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const int pc = 8 * r + 2 * ft;
+        float v00 = yd[4 * r] + Dh * bf16lo_to_f32(xw[2 * r]);
+        float v01 = yd[4 * r + 1] + Dh * bf16hi_to_f32(xw[2 * r]);
+        float v10 = yd[4 * r + 2] + Dh * bf16lo_to_f32(xw[2 * r + 1]);
+        float v11 = yd[4 * r + 3] + Dh * bf16hi_to_f32(xw[2 * r + 1]);
+        if (ys) {
+          v00 = fmaf(e0, yo[4 * r], v00);
+          v01 = fmaf(e0, yo[4 * r + 1], v01);
+          v10 = fmaf(e1, yo[4 * r + 2], v10);
+          v11 = fmaf(e1, yo[4 * r + 3], v11);
+        }
+        if (t0 + ri0 < L) *reinterpret_cast<uint32_t*>(y0 + pc) = pack_bf16x2(v00, v01);
+        if (t0 + ri1 < L) *reinterpret_cast<uint32_t*>(y1 + pc) = pack_bf16x2(v10, v11);
+      }
+    }
+    fence_async_smem();   // the new H tiles, for the next chunk's MMAs
+    tc_fence_before();
+    ok = __syncthreads_and(ok) != 0;
+    tc_fence_after();
+  }
+  if (ok && p.hT) {
+    float* hT = p.hT + (static_cast<int64_t>(b) * p.nheads + h) * kHd * kNs;
+#pragma unroll
+    for (int q = 0; q < kHd; ++q) hT[q * kNs + n_own] = H[q];
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+}
+
+}  // namespace
+
+cudaError_t ssd_tc_launch(const SsdParams& p, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(ssd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem::kDynamic);
+  if (e != cudaSuccess) return e;
+  ssd_tc_kernel<<<dim3(p.nheads, p.batch), kThreads, TcSmem::kDynamic, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t ssd_status_read_and_clear(unsigned int* out) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_ssd_status, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_ssd_status, &zero, sizeof(unsigned int));
+}
+
+}  // namespace ssm
