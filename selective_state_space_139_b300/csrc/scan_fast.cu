@@ -43,6 +43,12 @@
 #ifndef SSM_FAST_LANES
 #define SSM_FAST_LANES 2            // lanes per channel: 2 or 4
 #endif
+#ifndef SSM_FAST_STAGES
+#define SSM_FAST_STAGES 3           // TMA pipeline stages
+#endif
+#ifndef SSM_FAST_MINB
+#define SSM_FAST_MINB 2             // resident CTAs per SM the kernel is compiled for
+#endif
 #ifndef SSM_FAST_DECAYS_FIRST
 #define SSM_FAST_DECAYS_FIRST 0     // 1: compute the chunk's decay factors before its recurrence
 #endif
@@ -54,7 +60,7 @@ __device__ unsigned int g_fast_status = 0;
 
 constexpr int kCh = 64;    // channels per CTA
 constexpr int kLanesDefault = SSM_FAST_LANES;
-constexpr int kSt = 3;     // TMA stages
+constexpr int kSt = SSM_FAST_STAGES;     // TMA stages
 constexpr int kRow = 128;  // bytes of one tile row = 64 bf16 steps
 constexpr int kT = 64;     // steps per tile
 constexpr int kN = 16;     // state width
@@ -65,7 +71,7 @@ struct SmemF {
   static constexpr int kTileBC = kN * kRow;                 // 2 KB
   static constexpr int kStage = 3 * kTileIO + 2 * kTileBC;  // 28 KB
   static constexpr int kBC32 = kT * 2 * kN * 4;             // 8 KB
-  static constexpr int kBars = kSt * kStage + 2 * kBC32;    // 100 KB
+  static constexpr int kBars = kSt * kStage + 2 * kBC32;    // 100 KB with 3 stages
   static constexpr int kTotal = kBars + 64 + 1024;
 };
 
@@ -151,7 +157,7 @@ struct Lane {
 };
 
 template <int kLanes, int kMode>
-__global__ void __launch_bounds__(kCh * kLanes, 2) scan_fast_kernel(const __grid_constant__ Maps tm,
+__global__ void __launch_bounds__(kCh * kLanes, SSM_FAST_MINB) scan_fast_kernel(const __grid_constant__ Maps tm,
                                                                       const ScanParams p) {
   constexpr int kThr = kCh * kLanes;
   constexpr int kNh = kN / kLanes;      // states per lane
