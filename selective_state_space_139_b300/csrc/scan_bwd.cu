@@ -38,6 +38,9 @@
 namespace ssm {
 namespace {
 
+#ifndef SSM_BWD_TWO_LANES
+#define SSM_BWD_TWO_LANES 1   // bf16 io: reverse pass with two lanes per channel (1) or one (0)
+#endif
 #ifndef SSM_BWD_FWD_MINB
 #define SSM_BWD_FWD_MINB 3   // resident CTAs per SM the local forward is compiled for (float state)
 #endif
@@ -596,6 +599,245 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_rev_kernel(const BwdParams
   }
 }
 
+// (3') reverse pass with two lanes per channel (bfloat16 io, float32 arithmetic): lane pl of a channel
+// owns the states 8pl .. 8pl + 7, so a CTA of 128 threads covers 64 channels with half the per-thread
+// state of (3) and more resident warps.  The per-step scalars (Δ, σ, ds, the output gradients) are
+// computed by both lanes; the partial sums over states (C·h, the two reductions of the Δ gradient) are
+// completed with one lane exchange.  dB/dC: a 4-round butterfly over the 16 channels of a warp that share
+// the lane parity leaves lane l with the sum of value (l >> 1) & 15 of its half.
+constexpr int kCh2 = 64;       // channels per CTA of (3')
+constexpr int kP2 = 4;         // state pairs per lane
+
+struct Smem2 {
+  static constexpr int kBC = 2 * kSeg * 32 * 4;                 // B/C table, two buffers
+  static constexpr int kH = kSeg * kP2 * kThreads * 8;          // recomputed states [k][j][thread] (pairs)
+  static constexpr int kRed = 2 * 4 * kSeg * 32 * 4;            // dB/dC partials, two buffers
+  static constexpr int kHs = kP2 * kThreads * 8;                // chunk start states [j][thread]
+  static constexpr int kTotal = kBC + kH + kRed + kHs;
+};
+
+template <typename IO>
+__global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p) {
+  using P = Pair<float>;
+  extern __shared__ __align__(16) uint8_t smem[];
+  float* bc_base = reinterpret_cast<float*>(smem);
+  P* hbuf = reinterpret_cast<P*>(smem + Smem2::kBC);
+  float* red_base = reinterpret_cast<float*>(smem + Smem2::kBC + Smem2::kH);
+  P* hs_s = reinterpret_cast<P*>(smem + Smem2::kBC + Smem2::kH + Smem2::kRed);
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int pl = tid & 1;                       // which half of the states
+  const int b = blockIdx.y;
+  const int d = blockIdx.x * kCh2 + (tid >> 1);
+  const bool valid = d < p.dim;
+  const int dd = valid ? d : 0;
+  const int64_t row = static_cast<int64_t>(b) * p.dim + dd;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.z) * p.chunk_len;
+  const int64_t c1 = c0 + p.chunk_len < p.L ? c0 + p.chunk_len : p.L;
+  const int64_t nseg = (p.L + kSeg - 1) / kSeg;
+  const int n0 = 8 * pl;                        // first state of this lane
+  P A2[kP2], dh[kP2], dA[kP2];
+  {
+    const float* ag = static_cast<const float*>(p.agg) + (row * p.nchunks + blockIdx.z) * kAgg;
+    const float* Ad = p.A + static_cast<int64_t>(dd) * p.N;
+#pragma unroll
+    for (int j = 0; j < kP2; ++j) {
+      const int n = n0 + 2 * j;
+      const float a0 = n < p.N ? Ad[n] : 0.0f;
+      const float a1 = n + 1 < p.N ? Ad[n + 1] : 0.0f;
+      A2[j] = P::make(a0 * kLog2e, a1 * kLog2e);
+      hs_s[j * kThreads + tid] = P::make(ag[n], ag[n + 1]);
+      dh[j] = valid ? P::make(ag[2 * kN + n], ag[2 * kN + n + 1]) : P::splat(0.0f);
+      dA[j] = P::splat(0.0f);
+    }
+  }
+  const float bias = p.bias ? p.bias[dd] : 0.0f;
+  const float Dd = p.D ? p.D[dd] : 0.0f;
+  float dD = 0.0f, dbias = 0.0f;
+  const float* ck = static_cast<const float*>(p.ckpt) + row * nseg * kN + n0;
+  const float* cs = static_cast<const float*>(p.ckpt_s) + row * nseg;
+  auto seg_len = [&](int64_t t0) { return static_cast<int>(c1 - t0 < kSeg ? c1 - t0 : kSeg); };
+  auto flush_red = [&](const float* rb, int64_t t0, int nk) {
+    if (tid >= 64) return;
+    const int col = tid & 31, half = tid >> 5, arr = col / 16, n = col % 16;
+    const int k0 = half * 4;
+    if (n >= p.N || k0 >= nk) return;
+    float s4[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      s4[i] = (rb[(0 * kSeg + k0 + i) * 32 + col] + rb[(1 * kSeg + k0 + i) * 32 + col]) +
+              (rb[(2 * kSeg + k0 + i) * 32 + col] + rb[(3 * kSeg + k0 + i) * 32 + col]);
+    float* dst = static_cast<float*>(arr ? p.acc_dC : p.acc_dB) + (static_cast<int64_t>(b) * p.N + n) * p.L + t0 + k0;
+    if (p.vec_red && k0 + 4 <= nk) {
+      red_add_v4(dst, s4[0], s4[1], s4[2], s4[3]);
+      return;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (k0 + i < nk) atomicAdd(dst + i, s4[i]);
+  };
+  const int64_t last = c0 + ((c1 - c0 - 1) / kSeg) * kSeg;
+  SegRaw<IO> raw;
+  float bcr[2];
+  float4 ckr0, ckr1;
+  float ckS;
+  auto fetch_ck = [&](int64_t t0) {
+    const int64_t sgi = t0 / kSeg;
+    ckr0 = __ldg(reinterpret_cast<const float4*>(ck + sgi * kN));
+    ckr1 = __ldg(reinterpret_cast<const float4*>(ck + sgi * kN) + 1);
+    ckS = cs[sgi];
+  };
+  fetch_seg<IO>(p, row * p.L + last, seg_len(last), raw);
+  fetch_bc(p, b, last, seg_len(last), bcr);
+  fetch_ck(last);
+  store_bc(bc_base, bcr);
+  __syncthreads();
+  int buf = 0;
+  int64_t pend_t0 = -1;
+  int pend_nk = 0;
+  // the column of the dB/dC table this lane's butterfly result belongs to
+  const int ridx = (lane >> 1) & 15;
+  const int rcol = ridx < 8 ? n0 + ridx : 16 + n0 + (ridx - 8);
+  for (int64_t t0 = last; t0 >= c0; t0 -= kSeg) {
+    const int nk = seg_len(t0);
+    const int64_t off = row * p.L + t0;
+    const f2* bc2 = reinterpret_cast<const f2*>(bc_base + buf * (kSeg * 32));
+    float* red = red_base + buf * (4 * kSeg * 32);
+    float x[kSeg], v[kSeg], zz[kSeg], dyv[kSeg];
+    unpack_one<IO, float>(raw.w[0], x);
+    unpack_one<IO, float>(raw.w[1], v);
+    unpack_one<IO, float>(raw.w[2], dyv);
+    if (p.z) unpack_one<IO, float>(raw.w[3], zz);
+    P h0[kP2];
+    {
+      const P Sp = P::splat(ckS);
+      const float ckv[8] = {ckr0.x, ckr0.y, ckr0.z, ckr0.w, ckr1.x, ckr1.y, ckr1.z, ckr1.w};
+#pragma unroll
+      for (int j = 0; j < kP2; ++j)
+        h0[j] = pfma(pexp(pmul(A2[j], Sp)), hs_s[j * kThreads + tid], P::make(ckv[2 * j], ckv[2 * j + 1]));
+    }
+    const int64_t tn = t0 - kSeg;
+    const bool more = tn >= c0;
+    if (more) {
+      fetch_seg<IO>(p, row * p.L + tn, seg_len(tn), raw);
+      fetch_bc(p, b, tn, seg_len(tn), bcr);
+      fetch_ck(tn);
+    }
+    if (pend_t0 >= 0) flush_red(red_base + (buf ^ 1) * (4 * kSeg * 32), pend_t0, pend_nk);
+    // recompute the segment (this lane's 8 states), finish C·h with the partner lane
+    float dl[kSeg], sg[kSeg], ds[kSeg], gdz[kSeg];
+    P hc[kP2];
+#pragma unroll
+    for (int j = 0; j < kP2; ++j) hc[j] = h0[j];
+#pragma unroll
+    for (int k = 0; k < kSeg; ++k) {
+      gdz[k] = 0.0f;
+      if (k < nk) {
+        const float vb = v[k] + bias;
+        dl[k] = p.softplus ? softplus_fast(vb) : vb;
+        sg[k] = p.softplus ? rcp_approx(1.0f + ex2_approx(-vb * kLog2e)) : 1.0f;
+        const P dlp = P::splat(dl[k]), dlx = P::splat(dl[k] * x[k]);
+        P sa = P::splat(0.0f);
+#pragma unroll
+        for (int j = 0; j < kP2; ++j) {
+          hc[j] = pfma(pexp(pmul(dlp, A2[j])), hc[j], pmul(dlx, P::from_f2(bc2[k * 16 + 4 * pl + j])));
+          if (k < kSeg - 1) hbuf[(k * kP2 + j) * kThreads + tid] = hc[j];
+          sa = pfma(P::from_f2(bc2[k * 16 + 8 + 4 * pl + j]), hc[j], sa);
+        }
+        const float part = sa.lo() + sa.hi();
+        const float sacc = part + __shfl_xor_sync(0xffffffffu, part, 1) + Dd * x[k];
+        if (p.z) {
+          const float sz = rcp_approx(1.0f + ex2_approx(-zz[k] * kLog2e));
+          ds[k] = dyv[k] * zz[k] * sz;
+          gdz[k] = dyv[k] * sacc * sz * (1.0f + zz[k] * (1.0f - sz));
+        } else {
+          ds[k] = dyv[k];
+        }
+        if (!valid) ds[k] = 0.0f;
+      } else {
+        dl[k] = sg[k] = ds[k] = 0.0f;
+        // keep the partner exchange uniform: the partner lane runs the same k with the same nk
+      }
+    }
+    if (valid && p.z && pl == 1) store_seg<IO, float>(p.dz, off, nk, p.vec_io, gdz);
+    float gdu[kSeg], gdd[kSeg];
+#pragma unroll
+    for (int k = kSeg - 1; k >= 0; --k) {
+      gdu[k] = gdd[k] = 0.0f;
+      if (k < nk) {
+        dD += ds[k] * x[k];
+        const P dlp = P::splat(dl[k]), dsp = P::splat(ds[k]), dlx = P::splat(dl[k] * x[k]);
+        P dq = P::splat(0.0f), db = P::splat(0.0f);
+        float vals[16];
+#pragma unroll
+        for (int j = 0; j < kP2; ++j) {
+          const P abar = pexp(pmul(dlp, A2[j]));
+          const P bn = P::from_f2(bc2[k * 16 + 4 * pl + j]);
+          const P cn = P::from_f2(bc2[k * 16 + 8 + 4 * pl + j]);
+          dh[j] = pfma(dsp, cn, dh[j]);
+          const P hp = k > 0 ? hbuf[((k - 1) * kP2 + j) * kThreads + tid] : h0[j];
+          const P vc = pmul(dsp, hc[j]);
+          const P vbb = pmul(dh[j], dlx);
+          vals[8 + 2 * j] = vc.lo();
+          vals[8 + 2 * j + 1] = vc.hi();
+          vals[2 * j] = vbb.lo();
+          vals[2 * j + 1] = vbb.hi();
+          const P w = pmul(pmul(dh[j], hp), abar);
+          dq = pfma(w, A2[j], dq);
+          dA[j] = pfma(w, dlp, dA[j]);
+          db = pfma(dh[j], bn, db);
+          dh[j] = pmul(dh[j], abar);
+          hc[j] = hp;
+        }
+        const float dbm = db.lo() + db.hi(), dqm = dq.lo() + dq.hi();
+        const float dhb = dbm + __shfl_xor_sync(0xffffffffu, dbm, 1);
+        const float dqs = dqm + __shfl_xor_sync(0xffffffffu, dqm, 1);
+        const float ddl = dqs * kLn2 + dhb * x[k];
+        const float dv = ddl * sg[k];
+        gdu[k] = ds[k] * Dd + dhb * dl[k];
+        gdd[k] = dv;
+        dbias += dv;
+        // butterfly over the 16 channels sharing this lane's parity
+#pragma unroll
+        for (int w = 16, cnt = 16; w >= 2; w >>= 1, cnt >>= 1) {
+          const bool upper = (lane & w) != 0;
+          const int half = cnt / 2;
+#pragma unroll
+          for (int i = 0; i < half; ++i) {
+            const float send = upper ? vals[i] : vals[i + half];
+            const float keep = upper ? vals[i + half] : vals[i];
+            vals[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+          }
+        }
+        red[(warp * kSeg + k) * 32 + rcol] = vals[0];
+      }
+    }
+    if (valid && pl == 0) {
+      store_seg<IO, float>(p.du, off, nk, p.vec_io, gdu);
+      store_seg<IO, float>(p.ddelta, off, nk, p.vec_io, gdd);
+    }
+    if (more) store_bc(bc_base + (buf ^ 1) * (kSeg * 32), bcr);
+    __syncthreads();
+    pend_t0 = t0;
+    pend_nk = nk;
+    buf ^= 1;
+  }
+  if (pend_t0 >= 0) flush_red(red_base + (buf ^ 1) * (4 * kSeg * 32), pend_t0, pend_nk);
+  if (valid) {
+    float* accA = static_cast<float*>(p.acc_dA) + static_cast<int64_t>(d) * p.N;
+#pragma unroll
+    for (int j = 0; j < kP2; ++j) {
+      const int n = n0 + 2 * j;
+      if (n < p.N) atomicAdd(accA + n, dA[j].lo());
+      if (n + 1 < p.N) atomicAdd(accA + n + 1, dA[j].hi());
+    }
+    if (pl == 0) {
+      if (p.acc_dD) atomicAdd(static_cast<float*>(p.acc_dD) + d, dD);
+      if (p.acc_dbias) atomicAdd(static_cast<float*>(p.acc_dbias) + d, dbias);
+    }
+  }
+}
+
 __global__ void double_to_float_kernel(const double* __restrict__ src, float* __restrict__ dst, int64_t n) {
   const int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
   if (i < n) dst[i] = static_cast<float>(src[i]);
@@ -610,6 +852,16 @@ cudaError_t launch(const BwdParams& p, cudaStream_t stream) {
   const int64_t carry_threads = static_cast<int64_t>(p.batch) * p.dim * kN;
   bwd_carry_kernel<CT><<<static_cast<unsigned>((carry_threads + 255) / 256), 256, 0, stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if constexpr (sizeof(CT) == 4) {
+    if (SSM_BWD_TWO_LANES) {
+      auto k2 = bwd_rev2_kernel<IO>;
+      e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem2::kTotal);
+      if (e != cudaSuccess) return e;
+      const dim3 grid2((p.dim + kCh2 - 1) / kCh2, p.batch, p.nchunks);
+      k2<<<grid2, kThreads, Smem2::kTotal, stream>>>(p);
+      return cudaGetLastError();
+    }
+  }
   auto k = bwd_chunk_rev_kernel<IO, CT>;
   e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<CT>::kTotal);
   if (e != cudaSuccess) return e;
