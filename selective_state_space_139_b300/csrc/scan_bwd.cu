@@ -354,9 +354,108 @@ __global__ void __launch_bounds__(kThreads, sizeof(CT) == 4 ? SSM_BWD_FWD_MINB :
   }
 }
 
-// (2) carries across chunks, one thread per (channel, state): Q becomes h_start, G becomes dh_in
+// (1') local forward with two lanes per channel (bfloat16 io): lane pl of a channel runs the states
+// 8pl .. 8pl + 7; both lanes evaluate the per-step scalars.  Same outputs as (1).
+template <typename IO>
+__global__ void __launch_bounds__(kThreads, 4) bwd_fwd2_kernel(const BwdParams p) {
+  using P = Pair<float>;
+  __shared__ __align__(16) float bc_buf[2][kSeg * 32];
+  const int tid = threadIdx.x;
+  const int pl = tid & 1;
+  const int b = blockIdx.y;
+  const int d = blockIdx.x * 64 + (tid >> 1);
+  const bool valid = d < p.dim;
+  const int dd = valid ? d : 0;
+  const int64_t row = static_cast<int64_t>(b) * p.dim + dd;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.z) * p.chunk_len;
+  const int64_t c1 = c0 + p.chunk_len < p.L ? c0 + p.chunk_len : p.L;
+  const int64_t nseg = (p.L + kSeg - 1) / kSeg;
+  const int n0 = 8 * pl;
+  P A2[4], h[4], E[4], G[4];
+  {
+    const float* Ad = p.A + static_cast<int64_t>(dd) * p.N;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + 2 * j;
+      A2[j] = P::make((n < p.N ? Ad[n] : 0.0f) * kLog2e, (n + 1 < p.N ? Ad[n + 1] : 0.0f) * kLog2e);
+      h[j] = P::splat(0.0f);
+      E[j] = P::splat(1.0f);
+      G[j] = P::splat(0.0f);
+    }
+  }
+  const float bias = p.bias ? p.bias[dd] : 0.0f;
+  float S = 0.0f;
+  float* ck = static_cast<float*>(p.ckpt) + row * nseg * kN + n0;
+  float* cs = static_cast<float*>(p.ckpt_s) + row * nseg;
+  auto seg_len = [&](int64_t t0) { return static_cast<int>(c1 - t0 < kSeg ? c1 - t0 : kSeg); };
+  SegRaw<IO> raw;
+  float bcr[2];
+  fetch_seg<IO>(p, row * p.L + c0, seg_len(c0), raw);
+  fetch_bc(p, b, c0, seg_len(c0), bcr);
+  store_bc(bc_buf[0], bcr);
+  __syncthreads();
+  int buf = 0;
+  for (int64_t t0 = c0; t0 < c1; t0 += kSeg) {
+    const int nk = seg_len(t0);
+    float x[kSeg], v[kSeg], zz[kSeg], dyv[kSeg];
+    unpack_one<IO, float>(raw.w[0], x);
+    unpack_one<IO, float>(raw.w[1], v);
+    unpack_one<IO, float>(raw.w[2], dyv);
+    if (p.z) unpack_one<IO, float>(raw.w[3], zz);
+    const int64_t tn = t0 + kSeg;
+    const bool more = tn < c1;
+    if (more) {
+      fetch_seg<IO>(p, row * p.L + tn, seg_len(tn), raw);
+      fetch_bc(p, b, tn, seg_len(tn), bcr);
+    }
+    if (valid) {
+      const int64_t sgi = t0 / kSeg;
+      reinterpret_cast<float4*>(ck + sgi * kN)[0] = make_float4(h[0].lo(), h[0].hi(), h[1].lo(), h[1].hi());
+      reinterpret_cast<float4*>(ck + sgi * kN)[1] = make_float4(h[2].lo(), h[2].hi(), h[3].lo(), h[3].hi());
+      if (pl == 0) cs[sgi] = S;
+    }
+    const f2* bc2 = reinterpret_cast<const f2*>(bc_buf[buf]);
+#pragma unroll
+    for (int k = 0; k < kSeg; ++k) {
+      if (k < nk) {
+        const float vb = v[k] + bias;
+        const float dl = p.softplus ? softplus_fast(vb) : vb;
+        const float ds = p.z ? dyv[k] * zz[k] * rcp_approx(1.0f + ex2_approx(-zz[k] * kLog2e)) : dyv[k];
+        S += dl;
+        const P dlp = P::splat(dl), dlx = P::splat(dl * x[k]), dsp = P::splat(ds);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const P a = pexp(pmul(dlp, A2[j]));
+          h[j] = pfma(a, h[j], pmul(dlx, P::from_f2(bc2[k * 16 + 4 * pl + j])));
+          E[j] = pmul(E[j], a);
+          G[j] = pfma(E[j], pmul(P::from_f2(bc2[k * 16 + 8 + 4 * pl + j]), dsp), G[j]);
+        }
+      }
+    }
+    if (more) store_bc(bc_buf[buf ^ 1], bcr);
+    __syncthreads();
+    buf ^= 1;
+  }
+  if (valid) {
+    float* ag = static_cast<float*>(p.agg) + (row * p.nchunks + blockIdx.z) * kAgg + n0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      ag[2 * j] = h[j].lo();
+      ag[2 * j + 1] = h[j].hi();
+      ag[kN + 2 * j] = E[j].lo();
+      ag[kN + 2 * j + 1] = E[j].hi();
+      ag[2 * kN + 2 * j] = G[j].lo();
+      ag[2 * kN + 2 * j + 1] = G[j].hi();
+    }
+  }
+}
+
+// (2) carries across chunks, one thread per (channel, state): Q becomes h_start, G becomes dh_in.
+// The aggregates are read 8 chunks at a time ahead of the serial composition, so that the loads of
+// a batch are in flight together.
 template <typename CT>
 __global__ void bwd_carry_kernel(const BwdParams p) {
+  constexpr int kB8 = 8;
   const int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
   const int64_t rows = static_cast<int64_t>(p.batch) * p.dim;
   if (i >= rows * kN) return;
@@ -364,16 +463,40 @@ __global__ void bwd_carry_kernel(const BwdParams p) {
   const int n = static_cast<int>(i % kN);
   CT* ag = static_cast<CT*>(p.agg) + row * p.nchunks * kAgg + n;
   CT h = 0;
-  for (int c = 0; c < p.nchunks; ++c) {
-    const CT q = ag[c * kAgg];
-    ag[c * kAgg] = h;
-    h = ag[c * kAgg + kN] * h + q;
+  for (int c0 = 0; c0 < p.nchunks; c0 += kB8) {
+    CT q[kB8], P[kB8];
+#pragma unroll
+    for (int k = 0; k < kB8; ++k) {
+      const int c = c0 + k;
+      q[k] = c < p.nchunks ? ag[c * kAgg] : CT(0);
+      P[k] = c < p.nchunks ? ag[c * kAgg + kN] : CT(0);
+    }
+#pragma unroll
+    for (int k = 0; k < kB8; ++k) {
+      const int c = c0 + k;
+      if (c < p.nchunks) {
+        ag[c * kAgg] = h;
+        h = P[k] * h + q[k];
+      }
+    }
   }
   CT g = 0;
-  for (int c = p.nchunks - 1; c >= 0; --c) {
-    const CT gc = ag[c * kAgg + 2 * kN];
-    ag[c * kAgg + 2 * kN] = g;
-    g = gc + ag[c * kAgg + kN] * g;
+  for (int c0 = p.nchunks - 1; c0 >= 0; c0 -= kB8) {
+    CT gc[kB8], P[kB8];
+#pragma unroll
+    for (int k = 0; k < kB8; ++k) {
+      const int c = c0 - k;
+      gc[k] = c >= 0 ? ag[c * kAgg + 2 * kN] : CT(0);
+      P[k] = c >= 0 ? ag[c * kAgg + kN] : CT(0);
+    }
+#pragma unroll
+    for (int k = 0; k < kB8; ++k) {
+      const int c = c0 - k;
+      if (c >= 0) {
+        ag[c * kAgg + 2 * kN] = g;
+        g = gc[k] + P[k] * g;
+      }
+    }
   }
 }
 
@@ -846,7 +969,15 @@ __global__ void double_to_float_kernel(const double* __restrict__ src, float* __
 template <typename IO, typename CT>
 cudaError_t launch(const BwdParams& p, cudaStream_t stream) {
   const dim3 grid((p.dim + kThreads - 1) / kThreads, p.batch, p.nchunks);
-  bwd_chunk_fwd_kernel<IO, CT><<<grid, kThreads, 0, stream>>>(p);
+  const dim3 grid2((p.dim + kCh2 - 1) / kCh2, p.batch, p.nchunks);
+  bool two_lanes = false;
+  if constexpr (sizeof(CT) == 4) {
+    if (SSM_BWD_TWO_LANES) {
+      bwd_fwd2_kernel<IO><<<grid2, kThreads, 0, stream>>>(p);
+      two_lanes = true;
+    }
+  }
+  if (!two_lanes) bwd_chunk_fwd_kernel<IO, CT><<<grid, kThreads, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t carry_threads = static_cast<int64_t>(p.batch) * p.dim * kN;
@@ -857,7 +988,6 @@ cudaError_t launch(const BwdParams& p, cudaStream_t stream) {
       auto k2 = bwd_rev2_kernel<IO>;
       e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem2::kTotal);
       if (e != cudaSuccess) return e;
-      const dim3 grid2((p.dim + kCh2 - 1) / kCh2, p.batch, p.nchunks);
       k2<<<grid2, kThreads, Smem2::kTotal, stream>>>(p);
       return cudaGetLastError();
     }
