@@ -43,6 +43,9 @@
 #ifndef SSM_FAST_LANES
 #define SSM_FAST_LANES 2            // lanes per channel: 2 or 4
 #endif
+#ifndef SSM_FAST_PINGPONG
+#define SSM_FAST_PINGPONG 0         // 1: prepare chunk c+1 while running chunk c (two Prep buffers); 0 measured faster
+#endif
 #ifndef SSM_FAST_STAGES
 #define SSM_FAST_STAGES 3           // TMA pipeline stages
 #endif
@@ -351,8 +354,9 @@ __global__ void __launch_bounds__(kCh * kLanes, SSM_FAST_MINB) scan_fast_kernel(
 
     // Per chunk of 8 steps: "prep" reads the inputs, computes the scalars of the steps this lane owns
     // and broadcasts them to the channel's lanes; "run" does the recurrence, the readout, the
-    // reduction over the channel's lanes and the store.  The loop prepares chunk c+1 while it runs
-    // chunk c (two Prep buffers used in turn), so the two latency chains overlap.
+    // reduction over the channel's lanes and the store.  By default they run one after the other
+    // (168 registers); the ping-pong variant prepares chunk c+1 while it runs chunk c (two Prep
+    // buffers, 234 registers) and measured slower.
     struct Prep {
       float qs[8], ws[8], dls[8];
       float g[8 / kLanes], du[8 / kLanes];   // SiLU(z) and D·u of this lane's own steps
@@ -561,6 +565,7 @@ __global__ void __launch_bounds__(kCh * kLanes, SSM_FAST_MINB) scan_fast_kernel(
     };
 
     auto pipeline = [&](auto tag) {
+#if SSM_FAST_PINGPONG
       Prep pa, pb;
       prep(tag, 0, pa);
 #pragma unroll kUnrollChunks
@@ -572,6 +577,13 @@ __global__ void __launch_bounds__(kCh * kLanes, SSM_FAST_MINB) scan_fast_kernel(
           run(tag, c + 1, pb);
         }
       }
+#else
+      for (int c = 0; c < nch; ++c) {
+        Prep pa;
+        prep(tag, c, pa);
+        run(tag, c, pa);
+      }
+#endif
     };
     if (nch > 0) {
       if (warp_structured) pipeline(std::true_type());
