@@ -131,7 +131,7 @@ int bwd_segment_steps();
 int bwd_aggregate_floats();
 cudaError_t scan_bwd_launch(const BwdParams& p, cudaStream_t stream);
 
-// Mamba-2 SSD forward (ssd.cu): bf16 io, headdim 64, d_state 128.
+// Mamba-2 SSD forward (ssd_tc.cu): bf16 io, headdim 64, d_state 128.
 struct SsdParams {
   const void* x;          // (batch, L, nheads, 64) bf16
   const void* dt;         // (batch, L, nheads) bf16, before bias and softplus
@@ -151,7 +151,6 @@ struct SsdParams {
 int ssd_head_dim();
 int ssd_state_dim();
 cudaError_t ssd_fwd_launch(const SsdParams& p, cudaStream_t stream);
-cudaError_t ssd_tc_launch(const SsdParams& p, cudaStream_t stream);     // tcgen05 kernel (ssd_tc.cu)
 cudaError_t ssd_status_read_and_clear(unsigned int* out);
 
 // Sets the text returned by ssm_last_error_message() on the calling host thread (ssm_api.cu).

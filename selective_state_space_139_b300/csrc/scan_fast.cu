@@ -38,7 +38,7 @@
 #define SSM_FAST_SOFTPLUS_LOG 0     // 1: ln2 * log2(1 + e^v) everywhere below v = 15 (no series branch)
 #endif
 #ifndef SSM_FAST_UNROLL
-#define SSM_FAST_UNROLL 1           // unroll factor of the chunk-pair loop
+#define SSM_FAST_UNROLL 1           // unroll factor of the chunk-pair loop (ping-pong variant)
 #endif
 #ifndef SSM_FAST_LANES
 #define SSM_FAST_LANES 2            // lanes per channel: 2 or 4
@@ -67,7 +67,9 @@ constexpr int kSt = SSM_FAST_STAGES;     // TMA stages
 constexpr int kRow = 128;  // bytes of one tile row = 64 bf16 steps
 constexpr int kT = 64;     // steps per tile
 constexpr int kN = 16;     // state width
+#if SSM_FAST_PINGPONG
 constexpr int kUnrollChunks = SSM_FAST_UNROLL;
+#endif
 
 struct SmemF {
   static constexpr int kTileIO = kCh * kRow;                // 8 KB
@@ -132,11 +134,13 @@ __device__ __forceinline__ float prmt_half(uint32_t word, uint32_t sel) {
 }
 
 // fast softplus on a packed pair (MUFU per element)
+#if SSM_FAST_SOFTPLUS_LOG
 __device__ __forceinline__ float softplus_log(float v) {
   const float e = ex2_approx(v * kLog2e);
   const float r = kLn2 * lg2_approx(1.0f + e);
   return v > 15.0f ? v : r;
 }
+#endif
 __device__ __forceinline__ f2 softplus2(f2 v) {
 #if SSM_FAST_SOFTPLUS_LOG
   return f2_make(softplus_log(f2_lo(v)), softplus_log(f2_hi(v)));

@@ -396,6 +396,7 @@ __global__ void __launch_bounds__(kCH, 1)
 
     auto one = [&](auto structured_tag, int c, int j, const float* uu, const float* dd, const float* zz) -> float {
       constexpr bool kS = decltype(structured_tag)::value;
+      (void)kS;   // used by the float path only
       const uint32_t row = bcb + (c * TL::kVec + j) * 128;
       if constexpr (kFast) {
         BC x;

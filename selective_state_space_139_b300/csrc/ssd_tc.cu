@@ -1,6 +1,8 @@
-// Mamba-2 SSD forward on the fifth-generation tensor cores (tcgen05, accumulators in tensor memory).
-// Same operator and chunked block form as ssd.cu ("Mamba и State Space Models", "Mamba-2: State Space
-// Duality (SSD)"; "Модуль 8. Альтернативы Transformer", §7 and §14):
+// Mamba-2 SSD forward on the fifth-generation tensor cores (tcgen05, accumulators in tensor memory),
+// chunked block form ("Mamba и State Space Models", "Mamba-2: State Space Duality (SSD)": a scalar A per
+// head, d_state 128, the SSM as a product with a semi-separable matrix; "Модуль 8. Альтернативы
+// Transformer", §7: M_ij = C_i·B_j Π_{r=j+1..i} a_r as a masked matrix product inside a chunk, only the
+// state passed between chunks; §14: state [batch, nheads, headdim, d_state], input term Δ·B·x):
 //   y_i = Σ_{j≤i} (C_i·B_j) e^{cum_i − cum_j} Δ_j x_j + e^{cum_i} C_i·H + D_h x_i
 //   H  <- e^{cum_end} H + Σ_j e^{cum_end − cum_j} Δ_j x_j B_j^T
 // over chunks of 64 steps, one CTA (4 warps) per (batch, head), two CTAs per SM.
@@ -15,8 +17,9 @@
 // serves both products and nothing is transposed.  The CUDA cores do the element-wise parts: Δ and its
 // prefix sum, M = G ∘ e^{cum_i − cum_j} Δ_j (causal) from the G accumulator, w ∘ x, the state update
 // H = e^{cum_end} H + S^T (thread n owns column n of H in registers) and the output y.
-// As in ssd.cu, x, B, C enter the MMAs exactly and every computed operand (M, H, w ∘ x) is split into
-// two bf16 terms, so products keep float32-level accuracy.
+// x, B, C enter the MMAs exactly (bf16 inputs) and every computed operand (M, H, w ∘ x) is split into
+// two bf16 terms (about 16 significant bits), so products keep float32-level accuracy rather than
+// bf16's 8 bits.
 // Tensor memory: columns [0, 64) G then Yd (M = 64 rows sit in lanes 32w .. 32w + 15 of warp w),
 // [64, 128) Yo, [128, 192) S^T (row n in lane n); 256 columns are allocated per CTA.
 // Every mbarrier wait is bounded; on a timeout the CTA records it, stops and frees its tensor memory.
@@ -428,7 +431,10 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
 
 }  // namespace
 
-cudaError_t ssd_tc_launch(const SsdParams& p, cudaStream_t stream) {
+int ssd_head_dim() { return kHd; }
+int ssd_state_dim() { return kNs; }
+
+cudaError_t ssd_fwd_launch(const SsdParams& p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(ssd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem::kDynamic);
   if (e != cudaSuccess) return e;
   ssd_tc_kernel<<<dim3(p.nheads, p.batch), kThreads, TcSmem::kDynamic, stream>>>(p);

@@ -16,13 +16,6 @@ namespace {
 
 thread_local char g_err[512] = {0};
 
-void set_err(const char* fmt, ...) {
-  va_list ap;
-  va_start(ap, fmt);
-  vsnprintf(g_err, sizeof(g_err), fmt, ap);
-  va_end(ap);
-}
-
 ssm_status fail(ssm_status s, const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
