@@ -311,14 +311,54 @@ def measure_decode(w, steps_tokens, dev, rank):
         evs[t][1].record(stream)
     torch.cuda.synchronize(dev)
     per = [a.elapsed_time(b) for a, b in evs]
-    k_ms = statistics.mean(per[5:]) if len(per) > 10 else statistics.mean(per)
-    return {"steps": steps_tokens, "ms_per_token_step": k_ms, "bytes_per_step": w.bytes_per_step(),
-            "achieved_gbs": w.bytes_per_step() / (k_ms * 1e-3) / 1e9,
+    eager_ms = statistics.mean(per[5:]) if len(per) > 10 else statistics.mean(per)
+    # the same token steps launched from a CUDA graph (how a serving loop issues decode steps): one
+    # replay runs every step back to back, so the per-step time is the GPU's, not the Python call's
+    state.zero_()
+    conv_state.zero_()
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g, stream=cap):
+            for t in range(steps_tokens):
+                tok(t)
+    stream.wait_stream(cap)
+    state.zero_()
+    conv_state.zero_()
+    g.replay()
+    torch.cuda.synchronize(dev)
+    state.zero_()
+    conv_state.zero_()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    g.replay()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    k_ms = a.elapsed_time(b) / steps_tokens
+    return {"steps": steps_tokens, "ms_per_token_step": k_ms, "eager_ms_per_token_step": eager_ms,
+            "bytes_per_step": w.bytes_per_step(), "achieved_gbs": w.bytes_per_step() / (k_ms * 1e-3) / 1e9,
             "tokens_per_s": w.batch / (k_ms * 1e-3)}
 
 
+def _time_back_to_back(call, reps, dev):
+    """Milliseconds per call of `reps` calls issued back to back on the current stream (no host sync in
+    between, so the host's per-call work overlaps the GPU's), from CUDA events around the batch."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    a.record(stream)
+    for _ in range(reps):
+        call()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    return a.elapsed_time(b) / reps
+
+
 def measure_conv(w, dev, rank, reps=50):
-    """The conv1d + SiLU prefill kernel on the workload's x (batch, dim, L): event-timed per launch."""
+    """The conv1d + SiLU prefill kernel on the workload's x (batch, dim, L), calls back to back
+    (inputs larger than L2)."""
     import torch
     from selective_state_space_139_b300 import ssm
     g = torch.Generator(device=dev)
@@ -331,21 +371,13 @@ def measure_conv(w, dev, rank, reps=50):
     for _ in range(3):
         ssm.causal_conv1d_fwd(x, cw, st, out=u, final_state=st_out)
     torch.cuda.synchronize(dev)
-    times = []
-    for _ in range(reps):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        ssm.causal_conv1d_fwd(x, cw, st, out=u, final_state=st_out)
-        b.record()
-        torch.cuda.synchronize(dev)
-        times.append(a.elapsed_time(b))
-    ms = statistics.median(times)
+    ms = _time_back_to_back(lambda: ssm.causal_conv1d_fwd(x, cw, st, out=u, final_state=st_out), reps, dev)
     nbytes = 2 * x.numel() * 2 + w.dim * 16 + 2 * st.numel() * 4
     return {"ms": ms, "bytes": nbytes, "achieved_gbs": nbytes / (ms * 1e-3) / 1e9}
 
 
 def measure_bwd(w, dev, rank, reps=10):
-    """The scan backward (ssm_scan_bwd) on the workload with a N(0, 1) dy: event-timed per call.
+    """The scan backward (ssm_scan_bwd) on the workload with a N(0, 1) dy, calls back to back.
     Algorithmic bytes: u, Δ, z, dy read and du, dΔ, dz written (io dtype) per (b, d, t), B and C read
     (io dtype) and dB, dC written (float32) per (b, n, t), the per-channel parameters and dA."""
     import torch
@@ -361,16 +393,7 @@ def measure_bwd(w, dev, rank, reps=10):
                                       z=inp["z"], delta_bias=inp["delta_bias"], workspace=ws)
     for _ in range(3):
         call()
-    torch.cuda.synchronize(dev)
-    times = []
-    for _ in range(reps):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        call()
-        b.record()
-        torch.cuda.synchronize(dev)
-        times.append(a.elapsed_time(b))
-    ms = statistics.median(times)
+    ms = _time_back_to_back(call, reps, dev)
     e = inp["u"].element_size()
     bdl = w.batch * w.dim * w.seqlen
     bnl = w.batch * w.dstate * w.seqlen
@@ -380,7 +403,7 @@ def measure_bwd(w, dev, rank, reps=10):
 
 
 def measure_ssd(dev, rank, reps=10):
-    """The Mamba-2 SSD forward on its layer workload: event-timed per call; algorithmic FLOPs of the
+    """The Mamba-2 SSD forward on its layer workload, calls back to back; algorithmic FLOPs of the
     chunked form (64-step chunks) and algorithmic bytes as the workload defines them."""
     import torch
     from selective_state_space_139_b300 import ssm
@@ -395,16 +418,7 @@ def measure_ssd(dev, rank, reps=10):
                     final_state=hT)
     for _ in range(3):
         call()
-    torch.cuda.synchronize(dev)
-    times = []
-    for _ in range(reps):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        call()
-        b.record()
-        torch.cuda.synchronize(dev)
-        times.append(a.elapsed_time(b))
-    ms = statistics.median(times)
+    ms = _time_back_to_back(call, reps, dev)
     return {"workload": w, "ms": ms, "tokens_per_s": w.tokens / (ms * 1e-3),
             "tflops": w.flops() / (ms * 1e-3) / 1e12, "achieved_gbs": w.algorithmic_bytes() / (ms * 1e-3) / 1e9}
 
@@ -563,7 +577,9 @@ def main():
     }
     if dec is not None:
         line["decode"] = {"workload": "decode-2.8b", "tokens_per_s": 256 * ws / (dec["ms_per_token_step"] * 1e-3),
-                          "ms_per_token_step": dec["ms_per_token_step"], "achieved_gbs": dec["achieved_gbs"],
+                          "ms_per_token_step": dec["ms_per_token_step"], "launch": "CUDA graph of all token steps",
+                          "eager_ms_per_token_step": dec["eager_ms_per_token_step"],
+                          "achieved_gbs": dec["achieved_gbs"],
                           "frac": dec["achieved_gbs"] / peak, "bytes_per_step": dec["bytes_per_step"],
                           "steps": dec["steps"]}
     line["conv1d"] = {"workload": w.name + " x (conv1d + SiLU prefill)", "ms": conv["ms"],
