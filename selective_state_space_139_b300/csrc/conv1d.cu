@@ -24,11 +24,17 @@ __device__ __forceinline__ float io_at(const IO* p, int64_t i) {
 
 // vectorised path: L % kVec == 0 and 16-byte aligned rows.  A persistent grid walks the flat
 // (row, chunk) index space with a grid-sized stride; each iteration a thread issues the loads of
-// kPer chunks (one stride apart) before any arithmetic, so several 16-byte requests per thread are
-// in flight.  Consecutive lanes hold consecutive flat chunks, so the three inputs before a chunk
+// kPer chunks (one stride apart) before any arithmetic (one per iteration measured fastest, with 16
+// blocks of the grid per SM).  Consecutive lanes hold consecutive flat chunks, so the three inputs before a chunk
 // come from the previous lane by a shuffle (lane 0 re-reads them).  Flat indices fit 32 bits
 // (checked on the host).
-constexpr int kPer = 4;
+#ifndef SSM_CONV_PER
+#define SSM_CONV_PER 1            // chunks per thread and iteration (1 measured fastest)
+#endif
+#ifndef SSM_CONV_BLOCKS_PER_SM
+#define SSM_CONV_BLOCKS_PER_SM 16 // blocks of the grid-stride loop per SM
+#endif
+constexpr int kPer = SSM_CONV_PER;
 
 template <typename IO>
 __global__ void __launch_bounds__(256) conv1d_vec_kernel(const ConvParams p) {
@@ -163,7 +169,8 @@ cudaError_t launch(const ConvParams& p, bool vec, cudaStream_t stream) {
       if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
       const int64_t total = nrows * (p.L / IoTraits<IO>::kVec);
       const int64_t want = (total + 256 * kPer - 1) / (256 * kPer);
-      const unsigned blocks = static_cast<unsigned>(want < 8 * sms ? want : 8 * sms);
+      const int64_t cap = static_cast<int64_t>(SSM_CONV_BLOCKS_PER_SM) * sms;
+      const unsigned blocks = static_cast<unsigned>(want < cap ? want : cap);
       conv1d_vec_kernel<IO><<<blocks, 256, 0, stream>>>(q);
     } else {
       const int64_t n = nrows * p.L;

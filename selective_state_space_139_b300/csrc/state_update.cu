@@ -149,9 +149,12 @@ __global__ void __launch_bounds__(kThreads) state_update_kernel(const DecodePara
 }
 
 // bf16 io, dstate 16, aligned buffers: each thread serves kPer channels (slot + 64 k of its block),
-// issuing every load of all of them before any arithmetic and storing after, so that several
-// 16-byte state reads per thread are in flight (the step is bound by HBM latency x parallelism).
-constexpr int kPer = 2;
+// issuing every load before any arithmetic and storing after.  One channel per thread (32
+// registers, full occupancy) measured fastest: the bytes in flight come from resident warps.
+#ifndef SSM_DECODE_PER
+#define SSM_DECODE_PER 1   // channels per thread of the bf16 decode kernel (1 measured fastest)
+#endif
+constexpr int kPer = SSM_DECODE_PER;
 
 __global__ void __launch_bounds__(kThreads) state_update_bf16_kernel(const DecodeParams p) {
   using IO = __nv_bfloat16;
