@@ -28,8 +28,10 @@
 // from dh_in.  dB and dC sum over the channels of a batch row: per step a warp transpose-reduces its
 // 32 values (16 of dB, 16 of dC), the four warps' partials are added in shared memory and the CTA adds
 // them to global memory with vector atomics.  dA, dD and dbias accumulate per thread and are added
-// once per tile.  bf16 io computes in float32 with the MUFU approximations of the forward; float32
-// io computes in double and accumulates its cross-channel sums in double.
+// once per tile.  bf16 io computes in float32 with the MUFU approximations of the forward and runs
+// (1) and (3) with two lanes per channel ((1') and (3') below: eight states per lane, 64 channels per
+// CTA); float32 io computes in double, one channel per thread, and accumulates its cross-channel sums
+// in double.
 #include <cstring>
 
 #include "internal.h"
@@ -39,7 +41,7 @@ namespace ssm {
 namespace {
 
 #ifndef SSM_BWD_TWO_LANES
-#define SSM_BWD_TWO_LANES 1   // bf16 io: reverse pass with two lanes per channel (1) or one (0)
+#define SSM_BWD_TWO_LANES 1   // bf16 io: local forward and reverse pass with two lanes per channel (1) or one (0)
 #endif
 #ifndef SSM_BWD_FWD_MINB
 #define SSM_BWD_FWD_MINB 3   // resident CTAs per SM the local forward is compiled for (float state)
