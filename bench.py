@@ -5,8 +5,8 @@ Default workload: the Mamba-2.8B layer scan (batch 4, d_inner 5120, d_state 16, 
 float32 state).  One step = one ssm_scan_fwd call over that batch (every prefill row of the hot
 path: load, softplus, discretise, recurrence, readout + D skip, gate, store, final state).
 The decode row (batch 256, d_inner 5120, 1000 tokens), the conv1d + SiLU prefill, the scan
-backward and the Mamba-2 SSD layer are measured after it and reported in the same JSON line under
-"decode", "conv1d", "backward" and "ssd".
+backward, the Mamba-2 SSD layer and the Mamba-2 decode step are measured after it and reported in the
+same JSON line under "decode", "conv1d", "backward", "ssd" and "ssd_decode".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -423,6 +423,45 @@ def measure_ssd(dev, rank, reps=10):
             "tflops": w.flops() / (ms * 1e-3) / 1e12, "achieved_gbs": w.algorithmic_bytes() / (ms * 1e-3) / 1e9}
 
 
+def measure_ssd_decode(dev, rank):
+    """The Mamba-2 decode step on its workload (64 sequences x 128 heads, state 268 MB): the token
+    steps launched from a CUDA graph, as a serving loop issues them."""
+    import torch
+    from selective_state_space_139_b300 import ssm
+    from selective_state_space_139_b300 import workloads as W
+    w = W.WORKLOADS["mamba2-decode"]
+    d = W.make_ssd_decode_inputs(w, device=dev, seed=w.seed + rank)
+    state = torch.zeros((w.batch, w.nheads, w.headdim, w.dstate), device=dev)
+    y = torch.empty((w.batch, w.nheads, w.headdim), device=dev, dtype=torch.bfloat16)
+
+    def tok(t):
+        ssm.ssd_state_update(d["x"][t], d["dt"][t], d["A"], d["B"][t], d["C"][t], state, D=d["D"],
+                             dt_bias=d["dt_bias"], out=y)
+    for t in range(5):
+        tok(t)
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g, stream=cap):
+            for t in range(w.seqlen):
+                tok(t)
+    stream.wait_stream(cap)
+    g.replay()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    g.replay()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / w.seqlen
+    nbytes = W.ssd_decode_bytes_per_step(w)
+    return {"workload": w, "ms": ms, "bytes": nbytes, "achieved_gbs": nbytes / (ms * 1e-3) / 1e9,
+            "tokens_per_s": w.batch / (ms * 1e-3)}
+
+
 # ----------------------------------------------------------------------------- distributed helpers
 
 _PG = None
@@ -499,6 +538,9 @@ def run_one_part(args, w, dev, rank, peak, peak_kind):
         out = measure_conv(w, dev, rank, reps=args.steps)
     elif args.only == "backward":
         out = measure_bwd(w, dev, rank, reps=args.steps)
+    elif args.only == "ssd_decode":
+        out = measure_ssd_decode(dev, rank)
+        out.pop("workload")
     else:
         out = measure_ssd(dev, rank, reps=args.steps)
         out.pop("workload")
@@ -519,7 +561,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-ssd", action="store_true")
-    ap.add_argument("--only", default="all", choices=["all", "scan", "decode", "conv1d", "backward", "ssd"],
+    ap.add_argument("--only", default="all", choices=["all", "scan", "decode", "conv1d", "backward", "ssd", "ssd_decode"],
                     help="measure one part alone (for profiler captures)")
     ap.add_argument("--no-soak", action="store_true", help="skip the 1 s clock soak before the scan warm-up")
     ap.add_argument("--ref-budget", type=float, default=150.0,
@@ -554,6 +596,7 @@ def main():
     conv = measure_conv(w, dev, rank)
     bwd = None if args.no_backward else measure_bwd(w, dev, rank)
     ssd = None if args.no_ssd else measure_ssd(dev, rank)
+    ssd_dec = None if args.no_ssd else measure_ssd_decode(dev, rank)
     if rank != 0:
         return 0
     tokens_all = w.tokens * ws
@@ -600,6 +643,13 @@ def main():
                                     "frac": ssd["tflops"] / tpeak, "peak_source": tkind,
                                     "flops_per_call": sw.flops()},
                        "achieved_gbs": ssd["achieved_gbs"], "hbm_frac": ssd["achieved_gbs"] / peak}
+    if ssd_dec is not None:
+        dw = ssd_dec["workload"]
+        line["ssd_decode"] = {"workload": f"{dw.name} (batch {dw.batch}, {dw.nheads} heads x {dw.headdim}, "
+                                          f"d_state {dw.dstate}, fp32 state, {dw.seqlen} token steps)",
+                              "ms_per_token_step": ssd_dec["ms"], "launch": "CUDA graph of all token steps",
+                              "tokens_per_s": ssd_dec["tokens_per_s"] * ws, "achieved_gbs": ssd_dec["achieved_gbs"],
+                              "frac": ssd_dec["achieved_gbs"] / peak, "bytes_per_step": ssd_dec["bytes"]}
     if not args.no_cpu_baseline:
         v, cores, sample, _ = cpu_oracle_sample(w)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}

@@ -251,6 +251,24 @@ SSM_API ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, co
                                int ngroups, ssm_dtype io_dtype, cudaStream_t stream);
 
 /*
+ * One-token decode step of a Mamba-2 (SSD) layer, updating its state cache in place ("Модуль 8", §14:
+ * the Mamba-2 state [batch, nheads, headdim, d_state]; "Mamba и State Space Models", "Mamba-2: State
+ * Space Duality (SSD)").  Per batch b and head h (B/C group g = h / (nheads / ngroups)):
+ *     Δ = softplus(dt[b,h] + dt_bias[h]);   H = exp(Δ A[h]) H + Δ x[b,h,:] B[b,g,:]^T
+ *     y[b,h,:] = H C[b,g,:] + D[h] x[b,h,:]
+ *   x_t, y_t  : (batch, nheads, headdim) io_dtype       dt_t : (batch, nheads) io_dtype
+ *   B_t, C_t  : (batch, ngroups, dstate) io_dtype       A, D, dt_bias : (nheads) float32 (D, dt_bias may be NULL)
+ *   state     : (batch, nheads, headdim, dstate) float32, read and written in place
+ * The same recurrence ssm_ssd_fwd computes (equal up to rounding), one step at a time, so decode steps
+ * from a prefill's final state continue its sequence.  This build implements io_dtype SSM_BF16, headdim 64,
+ * dstate 128 (others SSM_ERR_UNSUPPORTED); state 16-byte aligned, B_t and C_t 16-byte aligned.
+ */
+SSM_API ssm_status ssm_ssd_state_update(const void* x_t, const void* dt_t, const float* A, const void* B_t,
+                                        const void* C_t, const float* D, const float* dt_bias, int softplus_flag,
+                                        float* state, void* y_t, int batch, int nheads, int headdim, int dstate,
+                                        int ngroups, ssm_dtype io_dtype, cudaStream_t stream);
+
+/*
  * Reads and clears the device status word (synchronises `stream`).  Returns SSM_OK, SSM_ERR_TIMEOUT
  * if a kernel gave up a bounded wait since the last call, or SSM_ERR_CUDA.
  */

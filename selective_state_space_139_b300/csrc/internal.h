@@ -151,6 +151,22 @@ struct SsdParams {
 int ssd_head_dim();
 int ssd_state_dim();
 cudaError_t ssd_fwd_launch(const SsdParams& p, cudaStream_t stream);
+
+// Mamba-2 decode step (ssd_decode.cu): one token, state (batch, nheads, 64, 128) float32 in place.
+struct SsdDecodeParams {
+  const void* x;          // (batch, nheads, 64) bf16
+  const void* dt;         // (batch, nheads) bf16
+  const float* A;         // (nheads)
+  const void* B;          // (batch, ngroups, 128) bf16
+  const void* C;          // (batch, ngroups, 128) bf16
+  const float* D;         // (nheads) or null
+  const float* dt_bias;   // (nheads) or null
+  float* state;           // (batch, nheads, 64, 128)
+  void* y;                // (batch, nheads, 64) bf16
+  int batch, nheads, ngroups;
+  int softplus;
+};
+cudaError_t ssd_decode_launch(const SsdDecodeParams& p, cudaStream_t stream);
 cudaError_t ssd_status_read_and_clear(unsigned int* out);
 
 // Sets the text returned by ssm_last_error_message() on the calling host thread (ssm_api.cu).

@@ -739,3 +739,48 @@ ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void
 }
 
 }  // extern "C"
+
+extern "C" {
+
+ssm_status ssm_ssd_state_update(const void* x_t, const void* dt_t, const float* A, const void* B_t, const void* C_t,
+                                const float* D, const float* dt_bias, int softplus_flag, float* state, void* y_t,
+                                int batch, int nheads, int headdim, int dstate, int ngroups, ssm_dtype io_dtype,
+                                cudaStream_t stream) {
+  g_err[0] = 0;
+  if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return fail(SSM_ERR_INVALID_ARG, "unknown io_dtype %d", io_dtype);
+  if (batch < 1 || nheads < 1 || headdim < 1 || dstate < 1 || ngroups < 1 || nheads % ngroups != 0)
+    return fail(SSM_ERR_INVALID_ARG, "bad sizes batch=%d nheads=%d headdim=%d dstate=%d ngroups=%d", batch, nheads,
+                headdim, dstate, ngroups);
+  if (io_dtype != SSM_BF16) return fail(SSM_ERR_UNSUPPORTED, "the SSD decode step supports bf16 io only");
+  if (headdim != ssm::ssd_head_dim() || dstate != ssm::ssd_state_dim())
+    return fail(SSM_ERR_UNSUPPORTED, "the SSD decode step supports headdim %d and dstate %d only", ssm::ssd_head_dim(),
+                ssm::ssd_state_dim());
+  if (batch > 65535) return fail(SSM_ERR_UNSUPPORTED, "batch=%d above 65535 is not supported", batch);
+  if (!x_t || !dt_t || !A || !B_t || !C_t || !state || !y_t)
+    return fail(SSM_ERR_INVALID_ARG, "null required pointer (x_t, dt_t, A, B_t, C_t, state, y_t)");
+  for (const void* q : {x_t, dt_t, static_cast<const void*>(y_t)})
+    if (!aligned(q, 2)) return fail(SSM_ERR_INVALID_ARG, "io pointer not aligned to its element size");
+  for (const void* q : {B_t, C_t, static_cast<const void*>(state)})
+    if (!aligned(q, 16)) return fail(SSM_ERR_INVALID_ARG, "B_t, C_t and state must be 16-byte aligned");
+  for (const void* q : {static_cast<const void*>(A), static_cast<const void*>(D), static_cast<const void*>(dt_bias)})
+    if (q && !aligned(q, 4)) return fail(SSM_ERR_INVALID_ARG, "float32 pointer not 4-byte aligned");
+  const size_t bh = static_cast<size_t>(batch) * nheads;
+  const size_t bg = static_cast<size_t>(batch) * ngroups;
+  const Range outs[] = {range_of(y_t, bh * headdim * 2), range_of(state, bh * headdim * dstate * 4)};
+  const Range ins[] = {range_of(x_t, bh * headdim * 2), range_of(dt_t, bh * 2), range_of(B_t, bg * dstate * 2),
+                       range_of(C_t, bg * dstate * 2), range_of(A, nheads * 4), range_of(D, D ? nheads * 4 : 0),
+                       range_of(dt_bias, dt_bias ? nheads * 4 : 0)};
+  for (const Range& o : outs)
+    for (const Range& i : ins)
+      if (overlap(o, i)) return fail(SSM_ERR_INVALID_ARG, "an output or the state overlaps an input");
+  if (overlap(outs[0], outs[1])) return fail(SSM_ERR_INVALID_ARG, "y_t overlaps the state");
+  ssm::SsdDecodeParams p;
+  memset(&p, 0, sizeof(p));
+  p.x = x_t; p.dt = dt_t; p.A = A; p.B = B_t; p.C = C_t; p.D = D; p.dt_bias = dt_bias; p.state = state; p.y = y_t;
+  p.batch = batch; p.nheads = nheads; p.ngroups = ngroups; p.softplus = softplus_flag != 0;
+  cudaError_t ce = ssm::ssd_decode_launch(p, stream);
+  if (ce != cudaSuccess) return cuda_fail(ce, "ssd decode launch");
+  return SSM_OK;
+}
+
+}  // extern "C"

@@ -77,6 +77,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ssm_causal_conv1d_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i64, i32, i32, i32, vp]
     lib.ssm_device_status.restype = i32
     lib.ssm_device_status.argtypes = [vp]
+    lib.ssm_ssd_state_update.restype = i32
+    lib.ssm_ssd_state_update.argtypes = [vp] * 7 + [i32, vp, vp, i32, i32, i32, i32, i32, i32, vp]
     lib.ssm_ssd_fwd.restype = i32
     lib.ssm_ssd_fwd.argtypes = [vp] * 7 + [i32, vp, vp, vp, i32, i64, i32, i32, i32, i32, i32, vp]
     lib.ssm_scan_bwd_workspace_size.restype = sz
@@ -344,6 +346,35 @@ def ssd_fwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
                              dstate, ngroups, _io_code(io), _stream_handle(stream))
     _check(lib, st)
     return y, final_state
+
+
+def ssd_state_update(x_t: torch.Tensor, dt_t: torch.Tensor, A: torch.Tensor, B_t: torch.Tensor, C_t: torch.Tensor,
+                     state: torch.Tensor, D: Optional[torch.Tensor] = None, dt_bias: Optional[torch.Tensor] = None,
+                     dt_softplus: bool = True, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """One Mamba-2 decode step; updates ``state`` (batch, nheads, headdim, dstate) f32 in place.
+    x_t (batch, nheads, headdim), dt_t (batch, nheads), B_t, C_t (batch, ngroups, dstate) in bf16;
+    A, D, dt_bias (nheads,) f32.  Returns y_t (batch, nheads, headdim)."""
+    lib = load_library()
+    batch, nheads, headdim = x_t.shape
+    ngroups, dstate = B_t.shape[1], B_t.shape[2]
+    dev = x_t.device
+    io = x_t.dtype
+    _need(x_t, "x_t", (batch, nheads, headdim), io, dev)
+    _need(dt_t, "dt_t", (batch, nheads), io, dev)
+    _need(B_t, "B_t", (batch, ngroups, dstate), io, dev)
+    _need(C_t, "C_t", (batch, ngroups, dstate), io, dev)
+    _need(A, "A", (nheads,), torch.float32, dev)
+    _need(D, "D", (nheads,), torch.float32, dev, optional=True)
+    _need(dt_bias, "dt_bias", (nheads,), torch.float32, dev, optional=True)
+    _need(state, "state", (batch, nheads, headdim, dstate), torch.float32, dev)
+    y = torch.empty_like(x_t) if out is None else out
+    _need(y, "out", (batch, nheads, headdim), io, dev)
+    with torch.cuda.device(dev):
+        st = lib.ssm_ssd_state_update(_ptr(x_t), _ptr(dt_t), _ptr(A), _ptr(B_t), _ptr(C_t), _ptr(D), _ptr(dt_bias),
+                                      int(bool(dt_softplus)), _ptr(state), _ptr(y), batch, nheads, headdim, dstate,
+                                      ngroups, _io_code(io), _stream_handle(stream))
+    _check(lib, st)
+    return y
 
 
 def device_status(stream=None) -> int:

@@ -124,6 +124,8 @@ WORKLOADS: Dict[str, object] = {
     # (headdim 64, so 128 heads); batch and length as the 2.8B Mamba-1 layer
     "mamba2-ssd-layer": SsdWorkload("mamba2-ssd-layer", 4, 4096, 128, 64, 128, 1, 1005),
     "ssd-small": SsdWorkload("ssd-small", 2, 300, 6, 64, 128, 1, 1006),
+    # Mamba-2 decode: the SSD layer's heads, 64 sequences, 200 token steps (state 268 MB > L2)
+    "mamba2-decode": SsdWorkload("mamba2-decode", 64, 200, 128, 64, 128, 1, 1007),
     "decode-2.8b": DecodeWorkload("decode-2.8b", 256, 5120, 16, 4, 1000, "bf16", 1004, a_scale=(0.5, 2.0)),
 }
 
@@ -229,3 +231,20 @@ def make_ssd_inputs(w: SsdWorkload, device="cpu", seed: Optional[int] = None) ->
     s = _loguniform(w.nheads, 1e-3, 1e-1, g, device)
     out["dt_bias"] = torch.log(torch.expm1(s)).to(torch.float32)
     return out
+
+
+def make_ssd_decode_inputs(w: SsdWorkload, device="cpu", seed: Optional[int] = None) -> Dict[str, torch.Tensor]:
+    """Per-token inputs of ``w.seqlen`` Mamba-2 decode steps, stacked along a leading step axis:
+    x (steps, batch, nheads, headdim), dt (steps, batch, nheads), B, C (steps, batch, ngroups, dstate),
+    drawn as ``make_ssd_inputs`` draws them; A, D, dt_bias as there."""
+    full = make_ssd_inputs(w, device=device, seed=seed)
+    out = {k: full[k].transpose(0, 1).contiguous() for k in ("x", "dt", "B", "C")}
+    out.update({k: full[k] for k in ("A", "D", "dt_bias")})
+    return out
+
+
+def ssd_decode_bytes_per_step(w: SsdWorkload) -> int:
+    """State read + write (fp32), per-token x, dt, B, C and y (bf16), A, D, dt_bias."""
+    bh = w.batch * w.nheads
+    return 2 * bh * w.headdim * w.dstate * 4 + (2 * bh * w.headdim + bh + 2 * w.batch * w.ngroups * w.dstate) * 2 + \
+        3 * w.nheads * 4

@@ -181,3 +181,21 @@ def test_ssd_rejects_bad_arguments_on_host(lib):
     assert call(y=P + 0x100) == ssm.SSM_ERR_INVALID_ARG  # y overlaps x
     assert call(dt=None) == ssm.SSM_ERR_INVALID_ARG
     assert call(hT=P + 0x5000004) == ssm.SSM_ERR_INVALID_ARG   # misaligned final state
+
+
+def test_ssd_state_update_rejects_bad_arguments_on_host(lib):
+    f = lib.ssm_ssd_state_update
+    base = dict(x=P, dt=P + 0x100000, A=P + 0x200000, B=P + 0x300000, C=P + 0x400000, D=None, bias=None, sp=1,
+                st=P + 0x1000000, y=P + 0x500000, batch=2, H=4, hd=64, N=128, G=1, io=ssm.SSM_BF16)
+
+    def call(**kw):
+        a = dict(base)
+        a.update(kw)
+        return f(a["x"], a["dt"], a["A"], a["B"], a["C"], a["D"], a["bias"], a["sp"], a["st"], a["y"], a["batch"],
+                 a["H"], a["hd"], a["N"], a["G"], a["io"], None)
+    assert call(io=ssm.SSM_F32) == ssm.SSM_ERR_UNSUPPORTED
+    assert call(N=16) == ssm.SSM_ERR_UNSUPPORTED
+    assert call(G=3) == ssm.SSM_ERR_INVALID_ARG
+    assert call(st=None) == ssm.SSM_ERR_INVALID_ARG
+    assert call(st=P + 0x1000008) == ssm.SSM_ERR_INVALID_ARG   # state not 16-byte aligned
+    assert call(y=P + 0x1000000) == ssm.SSM_ERR_INVALID_ARG    # y overlaps the state

@@ -108,3 +108,61 @@ def test_ssd_rejects_cpu_tensors_and_other_sizes():
     inp = W.make_ssd_inputs(W.SsdWorkload("adhoc", 1, 16, 2, 32, 128, 1, 2301), device=dev)
     with pytest.raises(ssm.SSMError):
         ssm.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"])
+
+
+# ---------------------------------------------------------------- the Mamba-2 decode step
+
+def _decode_steps(d, state, first, count, use_D=True, use_bias=True):
+    ys = []
+    for t in range(first, first + count):
+        ys.append(ssm.ssd_state_update(d["x"][t], d["dt"][t], d["A"], d["B"][t], d["C"][t], state,
+                                       D=d["D"] if use_D else None, dt_bias=d["dt_bias"] if use_bias else None))
+    torch.cuda.synchronize()
+    return torch.stack(ys, dim=1)   # (batch, steps, nheads, headdim)
+
+
+@pytest.mark.parametrize("groups", [1, 2])
+def test_ssd_decode_steps_match_the_recurrence(groups):
+    dev = _dev()
+    w = W.SsdWorkload("adhoc", 3, 20, 6, 64, 128, groups, 2400 + groups)
+    d = W.make_ssd_decode_inputs(w, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(9)
+    h0 = torch.randn((3, 6, 64, 128), generator=g, device=dev)
+    state = h0.clone()
+    y = _decode_steps(d, state, 0, w.seqlen)
+    full = {k: d[k].transpose(0, 1) for k in ("x", "dt", "B", "C")}
+    ry, rh = oracle.ssd_scan(to64(full["x"]), to64(full["dt"]), to64(d["A"]), to64(full["B"]), to64(full["C"]),
+                             D=to64(d["D"]), dt_bias=to64(d["dt_bias"]), h0=to64(h0))
+    _check(y, state, ry, rh)
+
+
+def test_ssd_prefill_then_decode_equals_longer_prefill():
+    """ssm_ssd_fwd over 150 tokens, then 30 decode steps from its final state, against the oracle
+    recurrence over all 180 tokens."""
+    dev = _dev()
+    w = W.SsdWorkload("adhoc", 2, 180, 4, 64, 128, 1, 2500)
+    inp = W.make_ssd_inputs(w, device=dev)
+    L1 = 150
+    pre = {k: inp[k][:, :L1].contiguous() for k in ("x", "dt", "B", "C")}
+    y1, state = ssm.ssd_fwd(pre["x"], pre["dt"], inp["A"], pre["B"], pre["C"], D=inp["D"], dt_bias=inp["dt_bias"])
+    dec = {k: inp[k][:, L1:].transpose(0, 1).contiguous() for k in ("x", "dt", "B", "C")}
+    dec.update({k: inp[k] for k in ("A", "D", "dt_bias")})
+    y2 = _decode_steps(dec, state, 0, w.seqlen - L1)
+    ry, rh = oracle.ssd_scan(to64(inp["x"]), to64(inp["dt"]), to64(inp["A"]), to64(inp["B"]), to64(inp["C"]),
+                             D=to64(inp["D"]), dt_bias=to64(inp["dt_bias"]))
+    _check(torch.cat([y1, y2], dim=1), state, ry, rh)
+
+
+def test_ssd_decode_workload_sampled_heads():
+    dev = _dev()
+    w = W.WORKLOADS["mamba2-decode"]
+    d = W.make_ssd_decode_inputs(w, device=dev)
+    state = torch.zeros((w.batch, w.nheads, w.headdim, w.dstate), device=dev)
+    steps = 40
+    y = _decode_steps(d, state, 0, steps)
+    heads = [0, 63, w.nheads - 1]
+    full = {k: d[k][:steps].transpose(0, 1) for k in ("x", "dt", "B", "C")}
+    ry, rh = oracle.ssd_scan(to64(full["x"][:, :, heads]), to64(full["dt"][:, :, heads]), to64(d["A"][heads]),
+                             to64(full["B"]), to64(full["C"]), D=to64(d["D"][heads]), dt_bias=to64(d["dt_bias"][heads]))
+    _check(y[:, :, heads], state[:, heads], ry, rh)
