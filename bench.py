@@ -540,12 +540,11 @@ def run_one_part(args, w, dev, rank, peak, peak_kind):
         out = measure_bwd(w, dev, rank, reps=args.steps)
     elif args.only == "ssd_decode":
         out = measure_ssd_decode(dev, rank)
-        out.pop("workload")
     else:
         out = measure_ssd(dev, rank, reps=args.steps)
-        out.pop("workload")
+    name = getattr(out.pop("workload", w), "name", w.name)
     if rank == 0:
-        print(json.dumps({"part": args.only, "workload": w.name, **out}), flush=True)
+        print(json.dumps({"part": args.only, "workload": name, **out}), flush=True)
     return 0
 
 
