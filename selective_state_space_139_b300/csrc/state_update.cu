@@ -5,9 +5,10 @@
 //   Δ = softplus(Δ_raw + bias);  h <- exp(Δ A) ⊙ h + Δ B_t u;  y = (C_t·h + D u) · SiLU(z_t)
 //
 // The step is bound by HBM traffic on the float32 state (read + write 64 bytes per channel for
-// dstate 16).  Four lanes share a channel, each owning four consecutive states, so a warp moves
-// 8 channels x 64 contiguous bytes with 128-bit accesses; the per-channel scalars are computed
-// redundantly by the four lanes and the readout is reduced with two shuffles.
+// dstate 16).  The bf16 kernel gives each thread whole state rows (below); the general kernel (float32
+// io, dstate < 16 or unaligned buffers) lets four lanes share a channel, each owning four consecutive
+// states, so a warp moves 8 channels x 64 contiguous bytes, with the per-channel scalars computed by
+// the four lanes and the readout reduced with two shuffles.
 #include "internal.h"
 #include "ssm_device.cuh"
 
@@ -148,89 +149,100 @@ __global__ void __launch_bounds__(kThreads) state_update_kernel(const DecodePara
   }
 }
 
-// bf16 io, dstate 16, aligned buffers: each thread serves kPer channels (slot + 64 k of its block),
-// issuing every load before any arithmetic and storing after.  One channel per thread (32
-// registers, full occupancy) measured fastest: the bytes in flight come from resident warps.
-#ifndef SSM_DECODE_PER
-#define SSM_DECODE_PER 1   // channels per thread of the bf16 decode kernel (1 measured fastest)
+// bf16 io, dstate 16, aligned buffers: one thread per channel d and kBpt batch rows.  The thread
+// issues every load first (kBpt whole 64-byte state rows, the A row once for all its rows, B/C rows,
+// conv window and scalars), so a warp keeps 4 KB of state in flight, and it computes the conv,
+// softplus and gate once per channel.  Measured on the 256 x 5120 decode step: 44.2 us with four
+// lanes per channel (512 bytes in flight per warp), 39.5 us with one row per thread, 35.9 us with
+// two, 35.4 us with three, 38.9 us with four (210 registers).
+constexpr int kThreads1 = 128;
+#ifndef SSM_DECODE_BPT
+#define SSM_DECODE_BPT 2    // batch rows per thread
 #endif
-constexpr int kPer = SSM_DECODE_PER;
+constexpr int kBpt = SSM_DECODE_BPT;
 
-__global__ void __launch_bounds__(kThreads) state_update_bf16_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads1) state_update_bf16_kernel(const DecodeParams p) {
   using IO = __nv_bfloat16;
-  const int tid = threadIdx.x;
-  const int j = tid % kLanesPerChannel;
-  const int slot = tid / kLanesPerChannel;
-  const int nchan = p.batch * p.dim;
-  const int base = static_cast<int>(blockIdx.x) * (kChannelsPerBlock * kPer);
-  int cc[kPer];
-  bool live[kPer];
-  float4 h4[kPer], a4[kPer], w4[kPer];
-  uint2 braw[kPer], craw[kPer];
-  float xv[kPer], dv[kPer], zv[kPer], c0[kPer], c1[kPer], c2[kPer], Dv[kPer], bv[kPer];
-  // ---- loads
+  const int pairs = ((p.batch + kBpt - 1) / kBpt) * p.dim;
+  const int t_raw = static_cast<int>(blockIdx.x) * kThreads1 + threadIdx.x;
+  if (t_raw >= pairs) return;
+  const int bq = t_raw / p.dim;
+  const int d = t_raw - bq * p.dim;
+  // ---- loads: every state row, the A row, conv weights, B/C rows and the per-channel scalars
+  const float4* arow = reinterpret_cast<const float4*>(p.A + static_cast<int64_t>(d) * 16);
+  float4 a4[4];
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int craw_i = base + slot + kChannelsPerBlock * k;
-    live[k] = craw_i < nchan;
-    const int c = live[k] ? craw_i : nchan - 1;
-    const int b = c / p.dim;
-    const int d = c - b * p.dim;
+  for (int q = 0; q < 4; ++q) a4[q] = arow[q];
+  const float4 w = *reinterpret_cast<const float4*>(p.conv_w + static_cast<int64_t>(d) * 4);
+  const float Dv = p.D ? p.D[d] : 0.0f;
+  const float bv = p.bias ? p.bias[d] : 0.0f;
+  float4 h4[kBpt][4];
+  uint4 braw[kBpt][2], craw[kBpt][2];
+  float xv[kBpt], dv[kBpt], zv[kBpt], c0[kBpt], c1[kBpt], c2[kBpt];
+  bool live[kBpt];
+  int64_t cc[kBpt];
+#pragma unroll
+  for (int k = 0; k < kBpt; ++k) {
+    const int b0 = bq * kBpt + k;
+    live[k] = b0 < p.batch;
+    const int b = live[k] ? b0 : p.batch - 1;
+    const int64_t c = static_cast<int64_t>(b) * p.dim + d;
     cc[k] = c;
-    const int64_t c64 = c;
-    h4[k] = *reinterpret_cast<const float4*>(p.state + c64 * 16 + 4 * j);
-    a4[k] = *reinterpret_cast<const float4*>(p.A + static_cast<int64_t>(d) * 16 + 4 * j);
-    w4[k] = *reinterpret_cast<const float4*>(p.conv_w + static_cast<int64_t>(d) * 4);
-    braw[k] = *reinterpret_cast<const uint2*>(static_cast<const IO*>(p.B) + static_cast<int64_t>(b) * 16 + 4 * j);
-    craw[k] = *reinterpret_cast<const uint2*>(static_cast<const IO*>(p.C) + static_cast<int64_t>(b) * 16 + 4 * j);
-    xv[k] = ld_io<IO>(p.x, c64);
-    dv[k] = ld_io<IO>(p.delta, c64);
-    zv[k] = p.z ? ld_io<IO>(p.z, c64) : 0.0f;
-    c0[k] = p.conv_state[c64 * 3 + 0];
-    c1[k] = p.conv_state[c64 * 3 + 1];
-    c2[k] = p.conv_state[c64 * 3 + 2];
-    Dv[k] = p.D ? p.D[d] : 0.0f;
-    bv[k] = p.bias ? p.bias[d] : 0.0f;
-  }
-  // ---- arithmetic
-  float yk[kPer];
+    const float4* srow = reinterpret_cast<const float4*>(p.state + c * 16);
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const float4 w = w4[k];
+    for (int q = 0; q < 4; ++q) h4[k][q] = srow[q];
+    const uint4* brow = reinterpret_cast<const uint4*>(static_cast<const IO*>(p.B) + static_cast<int64_t>(b) * 16);
+    const uint4* crow = reinterpret_cast<const uint4*>(static_cast<const IO*>(p.C) + static_cast<int64_t>(b) * 16);
+    braw[k][0] = brow[0]; braw[k][1] = brow[1];
+    craw[k][0] = crow[0]; craw[k][1] = crow[1];
+    xv[k] = ld_io<IO>(p.x, c);
+    dv[k] = ld_io<IO>(p.delta, c);
+    zv[k] = p.z ? ld_io<IO>(p.z, c) : 0.0f;
+    const float* cs = p.conv_state + c * 3;
+    c0[k] = cs[0]; c1[k] = cs[1]; c2[k] = cs[2];
+  }
+  // ---- arithmetic and stores
+#pragma unroll
+  for (int k = 0; k < kBpt; ++k) {
     const float s = fmaf(w.w, xv[k], fmaf(w.z, c2[k], fmaf(w.y, c1[k], w.x * c0[k])));
     const float u = silu_fast(s);
-    const float v = dv[k] + bv[k];
+    const float v = dv[k] + bv;
     const float dl = p.softplus ? softplus_fast(v) : v;
     const float wu = dl * u;
-    const float av[4] = {a4[k].x, a4[k].y, a4[k].z, a4[k].w};
-    float hv[4] = {h4[k].x, h4[k].y, h4[k].z, h4[k].w};
-    const float bb[4] = {bf16lo_to_f32(braw[k].x), bf16hi_to_f32(braw[k].x), bf16lo_to_f32(braw[k].y),
-                         bf16hi_to_f32(braw[k].y)};
-    const float cv[4] = {bf16lo_to_f32(craw[k].x), bf16hi_to_f32(craw[k].x), bf16lo_to_f32(craw[k].y),
-                         bf16hi_to_f32(craw[k].y)};
-    float py = 0.0f;
+    const float dl2 = dl * kLog2e;
+    const uint32_t bw[8] = {braw[k][0].x, braw[k][0].y, braw[k][0].z, braw[k][0].w,
+                            braw[k][1].x, braw[k][1].y, braw[k][1].z, braw[k][1].w};
+    const uint32_t cw[8] = {craw[k][0].x, craw[k][0].y, craw[k][0].z, craw[k][0].w,
+                            craw[k][1].x, craw[k][1].y, craw[k][1].z, craw[k][1].w};
+    float py0 = 0.0f, py1 = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float a = ex2_approx(dl * av[i] * kLog2e);
-      hv[i] = fmaf(a, hv[i], wu * bb[i]);
-      py = fmaf(cv[i], hv[i], py);
+    for (int q = 0; q < 4; ++q) {
+      float hv[4] = {h4[k][q].x, h4[k][q].y, h4[k][q].z, h4[k][q].w};
+      const float av[4] = {a4[q].x, a4[q].y, a4[q].z, a4[q].w};
+      const float bb[4] = {bf16lo_to_f32(bw[2 * q]), bf16hi_to_f32(bw[2 * q]), bf16lo_to_f32(bw[2 * q + 1]),
+                           bf16hi_to_f32(bw[2 * q + 1])};
+      const float ccv[4] = {bf16lo_to_f32(cw[2 * q]), bf16hi_to_f32(cw[2 * q]), bf16lo_to_f32(cw[2 * q + 1]),
+                            bf16hi_to_f32(cw[2 * q + 1])};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        hv[i] = fmaf(ex2_approx(dl2 * av[i]), hv[i], wu * bb[i]);
+        if (i & 1) py1 = fmaf(ccv[i], hv[i], py1);
+        else py0 = fmaf(ccv[i], hv[i], py0);
+      }
+      h4[k][q] = make_float4(hv[0], hv[1], hv[2], hv[3]);
     }
-    h4[k] = make_float4(hv[0], hv[1], hv[2], hv[3]);
-    py += __shfl_xor_sync(0xffffffffu, py, 1);
-    py += __shfl_xor_sync(0xffffffffu, py, 2);
-    float y = fmaf(Dv[k], u, py);
+    float y = fmaf(Dv, u, py0 + py1);
     if (p.z) y *= silu_fast(zv[k]);
-    yk[k] = y;
-  }
-  // ---- stores (every lane read its channel's old conv window in the load phase)
-  __syncwarp();
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) {
     if (!live[k]) continue;
-    const int64_t c64 = cc[k];
-    *reinterpret_cast<float4*>(p.state + c64 * 16 + 4 * j) = h4[k];
-    if (j < 3) p.conv_state[c64 * 3 + j] = j == 0 ? c1[k] : (j == 1 ? c2[k] : xv[k]);
-    if (j == 0) static_cast<IO*>(p.y)[c64] = IoTraits<IO>::from_f32(yk[k]);
+    const int64_t c = cc[k];
+    float4* sw = reinterpret_cast<float4*>(p.state + c * 16);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) sw[q] = h4[k][q];
+    float* cs = p.conv_state + c * 3;
+    cs[0] = c1[k];
+    cs[1] = c2[k];
+    cs[2] = xv[k];
+    static_cast<IO*>(p.y)[c] = IoTraits<IO>::from_f32(y);
   }
 }
 
@@ -238,9 +250,9 @@ template <typename IO>
 cudaError_t launch(const DecodeParams& p, cudaStream_t stream) {
   const int64_t nchan = static_cast<int64_t>(p.batch) * p.dim;
   if (sizeof(IO) == 2 && p.vec16) {
-    const unsigned blocks =
-        static_cast<unsigned>((nchan + kChannelsPerBlock * kPer - 1) / (kChannelsPerBlock * kPer));
-    state_update_bf16_kernel<<<blocks, kThreads, 0, stream>>>(p);
+    const int64_t threads = ((p.batch + kBpt - 1) / kBpt) * static_cast<int64_t>(p.dim);
+    const unsigned blocks = static_cast<unsigned>((threads + kThreads1 - 1) / kThreads1);
+    state_update_bf16_kernel<<<blocks, kThreads1, 0, stream>>>(p);
     return cudaGetLastError();
   }
   const unsigned blocks = static_cast<unsigned>((nchan + kChannelsPerBlock - 1) / kChannelsPerBlock);
