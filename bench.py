@@ -173,12 +173,21 @@ class OracleSample:
         return (f(inp["u"][0]), f(inp["delta"][0]), f(inp["A"]), f(inp["B"]), f(inp["C"]), np.zeros(nc, np.int64),
                 f(inp["D"]), f(inp["z"][0]), f(inp["delta_bias"]))
 
-    def _run(self, args):
+    def _run(self, args, threads=None):
         import oracle
         u, dl, A, B, C, bidx, D, z, bias = args
         t0 = time.perf_counter()
-        oracle.selective_scan_channels(u, dl, A, B, C, bidx, D=D, z=z, delta_bias=bias, threads=self.cores)
+        oracle.selective_scan_channels(u, dl, A, B, C, bidx, D=D, z=z, delta_bias=bias,
+                                       threads=self.cores if threads is None else threads)
         return time.perf_counter() - t0
+
+    def time_single_thread(self, multi_tokens_per_s: float, target_s: float = 4.0):
+        """The same oracle on one host thread, on a sample sized for about ``target_s`` seconds."""
+        channels_per_s = multi_tokens_per_s * self.n_total / (self.w.batch * self.w.seqlen) / self.cores
+        nc = int(max(1, min(self.n_total, target_s * channels_per_s)))
+        secs = self._run(self._make(nc), threads=1)
+        tokens_per_s = self.w.batch * self.w.seqlen * (nc / self.n_total) / secs
+        return tokens_per_s, f"{nc} channels x {self.w.seqlen} steps on 1 thread ({secs:.1f} s)"
 
     def time(self):
         """Runs the sample once; returns (workload tokens/s extrapolated from it, seconds, description)."""
@@ -194,7 +203,8 @@ def cpu_oracle_sample(w, target_s: float = 15.0):
     workload extrapolated from the sample, the cores used, a description and the seconds taken."""
     s = OracleSample(w, target_s)
     v, secs, what = s.time()
-    return v, s.cores, what, secs
+    v1, what1 = s.time_single_thread(v)
+    return v, s.cores, what, secs, v1, what1
 
 
 # ----------------------------------------------------------------------------- GPU measurement
@@ -697,8 +707,9 @@ def main():
                               "tokens_per_s": ssd_dec["tokens_per_s"] * ws, "achieved_gbs": ssd_dec["achieved_gbs"],
                               "frac": ssd_dec["achieved_gbs"] / peak, "bytes_per_step": ssd_dec["bytes"]}
     if not args.no_cpu_baseline:
-        v, cores, sample, _ = cpu_oracle_sample(w)
-        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+        v, cores, sample, _, v1, sample1 = cpu_oracle_sample(w)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+                                "single_thread": {"value": v1, "unit": UNIT, "cores": 1, "sample": sample1}}
     print(json.dumps(line), flush=True)
     return 0
 
