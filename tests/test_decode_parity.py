@@ -1,8 +1,9 @@
 """GPU parity of the one-token decode step against the fp64 oracle.
 
 The full-size workload (batch 256, d_inner 5120, dstate 16, 1000 tokens) runs 1000 steps on the
-GPU and must match, on sampled channels, one 1000-token prefill of the same inputs by the oracle
-(causal conv + SiLU, then the selective scan); the final SSM state and conv state must match too.
+GPU and must match, over every channel and step, one 1000-token prefill of the same inputs by the
+oracle (causal conv + SiLU, then the selective scan); the final SSM state and conv state must match
+too.
 Small shapes (ragged dim, dstate < 16, float32 io) are compared over every channel.
 """
 import numpy as np
@@ -11,7 +12,7 @@ import torch
 
 from selective_state_space_139_b300 import ssm
 from selective_state_space_139_b300 import workloads as W
-from tests._helpers import max_rel_err, sample_channels, to64
+from tests._helpers import max_rel_err, to64
 
 import oracle
 
@@ -52,17 +53,35 @@ def _oracle_prefill(inp, chans, steps):
     return y, hL, conv_tail, bi, di
 
 
+def _rel_err_on_device(y, ref):
+    """The parity metric computed on the GPU (float64), for outputs too large to hold twice on the host."""
+    y = y.double()
+    ref = ref.double()
+    scale = max(float(ref.abs().max()), 1e-30)
+    return float(((y - ref).abs() / torch.clamp(ref.abs(), min=1e-3 * scale)).max())
+
+
 def test_decode_2p8b_1000_tokens_matches_prefill():
+    """Every output of 1000 decode steps (batch 256, d_inner 5120) against one 1000-token oracle
+    prefill: the oracle runs on blocks of channels and its results are gathered on the device (y
+    rounded to float32, a 6e-8 relative change; state in float64; conv state exact)."""
     dev = _dev()
     w = W.WORKLOADS["decode-2.8b"]
     inp = W.make_decode_inputs(w, device=dev)
     ys, state, conv_state = _decode_all(inp, w.steps, w.batch, w.dim, w.dstate, dev)
-    chans = sample_channels(w.batch, w.dim, 48, seed=4)
-    ry, rh, rc, bi, di = _oracle_prefill(inp, chans, w.steps)
-    assert max_rel_err(to64(ys[:, bi, di].T), ry) <= 1e-2
-    assert max_rel_err(to64(state[bi, di]), rh) <= 1e-2
-    np.testing.assert_array_equal(to64(conv_state[bi, di]), rc)   # raw inputs, kept exactly
     assert torch.isfinite(ys).all() and torch.isfinite(state).all()
+    ref_y = torch.empty(ys.shape, dtype=torch.float32, device=dev)           # (steps, batch, dim)
+    ref_h = torch.empty(state.shape, dtype=torch.float64, device=dev)
+    chans = [(b, d) for b in range(w.batch) for d in range(w.dim)]
+    block = 32768
+    for i in range(0, len(chans), block):
+        part = chans[i:i + block]
+        ry, rh, rc, bi, di = _oracle_prefill(inp, part, w.steps)
+        ref_y[:, bi, di] = torch.from_numpy(ry.T.copy()).to(dev, torch.float32)
+        ref_h[bi, di] = torch.from_numpy(rh).to(dev)
+        np.testing.assert_array_equal(to64(conv_state[bi, di]), rc)   # raw inputs, kept exactly
+    assert _rel_err_on_device(ys, ref_y) <= 1e-2
+    assert _rel_err_on_device(state, ref_h) <= 1e-2
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])

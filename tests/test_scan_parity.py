@@ -2,8 +2,9 @@
 
 Tolerances: max relative error (with a floor of 1e-3 of the largest reference value) of 2e-5 for
 float32 io and 1e-2 for bfloat16 io with float32 state.  Small shapes are compared element by
-element over every output; the full-size workloads are compared on sampled channels, in the launch
-configuration the benchmark times (algorithm "auto").
+element over every output; the full-size workloads are compared over every output too (the oracle runs
+on all host cores, in channel blocks for the 2^20-step sequence), in the launch configuration the
+benchmark times (algorithm "auto").
 """
 import numpy as np
 import pytest
@@ -62,32 +63,60 @@ def test_mamba130m_layer_full(algorithm):
     _check_full(inp, y, hL, TOL[torch.bfloat16])
 
 
+_ORACLE_CACHE = {}
+
+
+def _rel_err_on_device(y, ref):
+    """The parity metric computed on the GPU (float64), for outputs too large to hold twice on the host."""
+    y = y.double()
+    ref = ref.double()
+    scale = max(float(ref.abs().max()), 1e-30)
+    return float(((y - ref).abs() / torch.clamp(ref.abs(), min=1e-3 * scale)).max())
+
+
+def _blockwise_errors(inp, y, hL, batch, dim, block):
+    """The parity metric over every channel: the oracle runs on blocks of channels (host memory stays
+    bounded for long sequences) and its results are gathered on the device, rounded to float32 for y
+    (a 6e-8 relative change, far below the 1e-2 bound) and kept in float64 for the final state."""
+    dev = y.device
+    ref_y = torch.empty(y.shape, dtype=torch.float32, device=dev)
+    ref_h = torch.empty(hL.shape, dtype=torch.float64, device=dev)
+    chans = [(b, d) for b in range(batch) for d in range(dim)]
+    for i in range(0, len(chans), block):
+        part = chans[i:i + block]
+        ry, rh = oracle_channels(inp, part)
+        bi = torch.tensor([c[0] for c in part])
+        di = torch.tensor([c[1] for c in part])
+        ref_y[bi, di] = torch.from_numpy(ry).to(dev, torch.float32)
+        ref_h[bi, di] = torch.from_numpy(rh).to(dev)
+    return _rel_err_on_device(y, ref_y), _rel_err_on_device(hL, ref_h)
+
+
 @pytest.mark.parametrize("algorithm", ["auto", "chunked"])
-def test_mamba28b_layer_sampled(algorithm):
+def test_mamba28b_layer_full(algorithm):
+    """Every output of the Mamba-2.8B layer (batch 4, d_inner 5120, L 4096) against the oracle."""
     dev = _dev()
     w = W.WORKLOADS["mamba2.8b-layer"]
     inp = W.make_scan_inputs(w, device=dev)
     y, hL = _run(inp, algorithm=algorithm)
-    chans = sample_channels(w.batch, w.dim, 96, seed=2)
-    ry, rh = oracle_channels(inp, chans)
-    bi = torch.tensor([c[0] for c in chans])
-    di = torch.tensor([c[1] for c in chans])
-    assert max_rel_err(to64(y[bi, di]), ry) <= 1e-2
-    assert max_rel_err(to64(hL[bi, di]), rh) <= 1e-2
     assert torch.isfinite(y).all()
+    if w.name not in _ORACLE_CACHE:
+        _ORACLE_CACHE[w.name] = _full_oracle(inp)
+    ry, rh = _ORACLE_CACHE[w.name]
+    assert max_rel_err(to64(y), ry) <= 1e-2
+    assert max_rel_err(to64(hL), rh) <= 1e-2
 
 
-def test_long_dna_sampled():
+def test_long_dna_full():
+    """Every output of the long-sequence workload (batch 1, d_inner 1536, L 2^20), oracle on blocks of
+    channels."""
     dev = _dev()
     w = W.WORKLOADS["long-dna"]
     inp = W.make_scan_inputs(w, device=dev)
     y, hL = _run(inp)
-    chans = sample_channels(w.batch, w.dim, 6, seed=3)
-    ry, rh = oracle_channels(inp, chans)
-    bi = torch.tensor([c[0] for c in chans])
-    di = torch.tensor([c[1] for c in chans])
-    assert max_rel_err(to64(y[bi, di]), ry) <= 1e-2
-    assert max_rel_err(to64(hL[bi, di]), rh) <= 1e-2
+    assert torch.isfinite(y).all()
+    ey, eh = _blockwise_errors(inp, y, hL, w.batch, w.dim, block=96)
+    assert ey <= 1e-2 and eh <= 1e-2, (ey, eh)
 
 
 SHAPES = [  # batch, dim, dstate, L
