@@ -211,16 +211,26 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
       cp_async16(sb + TcSmem::kX + sw_chunk(r, q), src, in ? 16 : 0);
     }
   };
-  auto load_dl = [&](int64_t t) -> float {
+  // dt of the next chunk is fetched as raw bf16 bits one chunk ahead and only converted (softplus)
+  // when that chunk starts, so the load's latency is not waited for
+  const unsigned short* dtr = reinterpret_cast<const unsigned short*>(dtg);
+  auto load_dt_raw = [&](int64_t t) -> uint32_t {
+    return t < L ? static_cast<uint32_t>(dtr[(static_cast<int64_t>(b) * L + t) * p.nheads + h]) : 0u;
+  };
+  auto dl_of = [&](uint32_t raw, int64_t t) -> float {
     if (t >= L) return 0.0f;
-    const float v = __bfloat162float(dtg[(static_cast<int64_t>(b) * L + t) * p.nheads + h]) + bias;
+    const float v = __uint_as_float(raw << 16) + bias;
     return p.softplus ? softplus_fast(v) : v;
   };
   const int nchunks = static_cast<int>((L + kQ - 1) / kQ);
   load_bc(0, TcSmem::kC, Cg);
   load_bc(0, TcSmem::kB, Bg);
   load_x(0);
-  float2 dt_next = warp == 0 ? make_float2(load_dl(2 * lane), load_dl(2 * lane + 1)) : make_float2(0.0f, 0.0f);
+  uint32_t dt_raw0 = 0u, dt_raw1 = 0u;
+  if (warp == 0) {
+    dt_raw0 = load_dt_raw(2 * lane);
+    dt_raw1 = load_dt_raw(2 * lane + 1);
+  }
   bool ok = true;
   for (int c = 0; c < nchunks && ok; ++c) {
     const int64_t t0 = static_cast<int64_t>(c) * kQ;
@@ -229,8 +239,11 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     // ---- P0: Δ and its inclusive prefix sum over the chunk, by warp 0 (two steps per lane); the
     // chunk's tiles were requested during the previous chunk
     if (warp == 0) {
-      const float d0 = dt_next.x, d1 = dt_next.y;
-      if (c + 1 < nchunks) dt_next = make_float2(load_dl(t0 + kQ + 2 * lane), load_dl(t0 + kQ + 2 * lane + 1));
+      const float d0 = dl_of(dt_raw0, t0 + 2 * lane), d1 = dl_of(dt_raw1, t0 + 2 * lane + 1);
+      if (c + 1 < nchunks) {
+        dt_raw0 = load_dt_raw(t0 + kQ + 2 * lane);
+        dt_raw1 = load_dt_raw(t0 + kQ + 2 * lane + 1);
+      }
       const float a0 = d0 * A2;
       float s2 = a0 + d1 * A2;
 #pragma unroll
