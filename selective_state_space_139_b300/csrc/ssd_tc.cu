@@ -5,23 +5,27 @@
 // state passed between chunks; §14: state [batch, nheads, headdim, d_state], input term Δ·B·x):
 //   y_i = Σ_{j≤i} (C_i·B_j) e^{cum_i − cum_j} Δ_j x_j + e^{cum_i} C_i·H + D_h x_i
 //   H  <- e^{cum_end} H + Σ_j e^{cum_end − cum_j} Δ_j x_j B_j^T
-// over chunks of 64 steps, one CTA (4 warps) per (batch, head), two CTAs per SM.
+// over chunks of 64 steps, one CTA (8 warps) per (batch, head), two CTAs per SM.
 //
 // Per chunk, four tcgen05.mma groups (bf16 operands from 128-byte-swizzled shared tiles, fp32
 // accumulators in tensor memory):
 //   G   = C B^T          M 64 (i) x N 64 (j) x K 128 (n)   A: C [i][n] K-major, B: B [j][n] K-major
-//   Yo  = C H^T          M 64 (i) x N 64 (p) x K 128 (n)   B: H^T stored [n][p] (MN-major), hi + lo
+//   Yo  = C H^T          M 64 (i) x N 128 x K 128 (n)      B: H^T hi and lo tiles [n][p] (MN-major) side by
+//                                                          side as one N = 128 operand; the halves are added
+//                                                          when Yo is read
 //   S^T = B^T (w ∘ x)    M 128 (n) x N 64 (p) x K 64 (j)   A: the same B tile read MN-major, B: (w ∘ x) [j][p]
 //   Yd  = M X            M 64 (i) x N 64 (p) x K 64 (j)    A: M [i][j] K-major (hi + lo), B: x [j][p] MN-major
 // The K-major 128-byte-swizzled tile of B[j][n] is byte for byte the MN-major tile of B^T, so one copy
 // serves both products and nothing is transposed.  The CUDA cores do the element-wise parts: Δ and its
 // prefix sum, M = G ∘ e^{cum_i − cum_j} Δ_j (causal) from the G accumulator, w ∘ x, the state update
-// H = e^{cum_end} H + S^T (thread n owns column n of H in registers) and the output y.
+// H = e^{cum_end} H + S^T (threads n and n + 128 own the two halves of column n of H in registers) and the
+// output y.  Warps w and w + 4 share tensor-memory lane quadrant w and split the 64 accumulator columns.
 // x, B, C enter the MMAs exactly (bf16 inputs) and every computed operand (M, H, w ∘ x) is split into
 // two bf16 terms (about 16 significant bits), so products keep float32-level accuracy rather than
 // bf16's 8 bits.
 // Tensor memory: columns [0, 64) G then Yd (M = 64 rows sit in lanes 32w .. 32w + 15 of warp w),
-// [64, 128) Yo, [128, 192) S^T (row n in lane n); 256 columns are allocated per CTA.
+// [64, 192) Yo (C H_hi^T then C H_lo^T), [192, 256) S^T (row n in lane n); 256 columns are allocated
+// per CTA.
 // Every mbarrier wait is bounded; on a timeout the CTA records it, stops and frees its tensor memory.
 #include "internal.h"
 #include "ssm_device.cuh"
@@ -34,7 +38,7 @@ __device__ unsigned int g_ssd_status = 0;
 constexpr int kQ = 64;         // chunk length
 constexpr int kHd = 64;        // head dim
 constexpr int kNs = 128;       // d_state
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 256;
 
 // tiles (byte offsets from a 1024-byte aligned base); every tile is 128-byte swizzled
@@ -63,6 +67,9 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
   return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16) |
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
 }
+// The descriptor of a tile `off` bytes further on: the start address field holds address >> 4 in 14 bits,
+// and every tile lies below 256 KB from the 1024-byte aligned base, so the field never carries.
+__device__ __forceinline__ uint64_t dadd(uint64_t base, uint32_t off) { return base + (off >> 4); }
 // instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, major-ness of A and B, N, M
 __device__ __forceinline__ uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
@@ -99,22 +106,20 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
 
-// The M = 64 accumulator rows of this warp (16 rows in lanes 32w .. 32w + 15) in the m16n8 fragment
-// layout: with g = lane / 4 and t = lane % 4, v[4r .. 4r + 3] = rows (g, g, g + 8, g + 8), columns
-// (8r + 2t, 8r + 2t + 1, 8r + 2t, 8r + 2t + 1) for r = 0..7 (64 columns from `taddr`; warp-collective).
-__device__ __forceinline__ void tc_ld_frag64(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
+// The M = 64 accumulator rows of a warp (16 rows in lanes 32q .. 32q + 15 of its lane quadrant q) in the
+// m16n8 fragment layout, 32 columns from `taddr`: with g = lane / 4 and t = lane % 4, v[4r .. 4r + 3] =
+// rows (g, g, g + 8, g + 8), columns (8r + 2t, 8r + 2t + 1, 8r + 2t, 8r + 2t + 1) for r = 0..3
+// (warp-collective).
+__device__ __forceinline__ void tc_ld_frag32(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
   asm volatile(
-      "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
-      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
@@ -166,30 +171,36 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
 
-  // the state: thread n holds column n of H (64 values of p) in fp32
-  const int n_own = tid;
-  float H[kHd];
+  // the state: thread n (< 128) holds H[p][n] for p < 32, thread n + 128 for p >= 32, in fp32
+  const int quad = warp & 3, half = warp >> 2;   // tensor-memory lane quadrant and column half
+  const int n_own = tid & 127;
+  const int pbase = 32 * half;
+  float H[kHd / 2];
   bool have_state = p.h0 != nullptr;
   {
     const float* h0 = p.h0 ? p.h0 + (static_cast<int64_t>(b) * p.nheads + h) * kHd * kNs : nullptr;
 #pragma unroll
-    for (int q = 0; q < kHd; ++q) H[q] = h0 ? h0[q * kNs + n_own] : 0.0f;
+    for (int q = 0; q < kHd / 2; ++q) H[q] = h0 ? h0[(pbase + q) * kNs + n_own] : 0.0f;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < 4; ++c) {
       uint4 hi, lo;
       split8(&H[c * 8], hi, lo);
-      *reinterpret_cast<uint4*>(sm + TcSmem::kHh + sw_chunk(n_own, c)) = hi;
-      *reinterpret_cast<uint4*>(sm + TcSmem::kHl + sw_chunk(n_own, c)) = lo;
+      *reinterpret_cast<uint4*>(sm + TcSmem::kHh + sw_chunk(n_own, 4 * half + c)) = hi;
+      *reinterpret_cast<uint4*>(sm + TcSmem::kHl + sw_chunk(n_own, 4 * half + c)) = lo;
     }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const uint32_t t_lane = static_cast<uint32_t>(warp * 32) << 16;   // this warp's lane quadrant
+  const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;   // this warp's lane quadrant
 
+  // base descriptors of the three operand layouts, built once (the MMA issue adds constant offsets)
+  const uint64_t dK = sdesc(sb, 16, 1024);          // K-major tiles: C, B, M
+  const uint64_t dH = sdesc(sb, 16384, 1024);       // H^T as an MN-major operand (128 rows of n)
+  const uint64_t dN = sdesc(sb, kQ * 128, 1024);    // MN-major 64-row tiles: B^T, w ∘ x, x
   const uint32_t id_g = idesc_bf16(64, 64, 0, 0);
-  const uint32_t id_yo = idesc_bf16(64, 64, 0, 1);
+  const uint32_t id_yo = idesc_bf16(64, 128, 0, 1);   // the H^T lo tile is the next MN atom of the hi tile
   const uint32_t id_s = idesc_bf16(128, 64, 1, 1);
   const uint32_t id_yd = idesc_bf16(64, 64, 0, 1);
 
@@ -267,30 +278,23 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         const uint32_t ka = (ks >> 2) * (kQ * 128) + (ks & 3) * 32;
-        tc_mma(tmem + 0, sdesc(sb + TcSmem::kC + ka, 16, 1024), sdesc(sb + TcSmem::kB + ka, 16, 1024), id_g, ks > 0);
+        tc_mma(tmem + 0, dadd(dK, TcSmem::kC + ka), dadd(dK, TcSmem::kB + ka), id_g, ks > 0);
       }
       if (ys) {
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t ka = (ks >> 2) * (kQ * 128) + (ks & 3) * 32;
-          tc_mma(tmem + 64, sdesc(sb + TcSmem::kC + ka, 16, 1024), sdesc(sb + TcSmem::kHh + ks * 2048, 16384, 1024),
-                 id_yo, ks > 0);
-        }
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t ka = (ks >> 2) * (kQ * 128) + (ks & 3) * 32;
-          tc_mma(tmem + 64, sdesc(sb + TcSmem::kC + ka, 16, 1024), sdesc(sb + TcSmem::kHl + ks * 2048, 16384, 1024),
-                 id_yo, 1);
+          tc_mma(tmem + 64, dadd(dK, TcSmem::kC + ka), dadd(dH, TcSmem::kHh + ks * 2048), id_yo, ks > 0);
         }
       }
       tc_commit(&bars[0]);
     }
     const float cum_end = s_cum[kQ - 1];
     {
-      const int j = tid >> 1, c0 = (tid & 1) * 4;
+      const int j = tid >> 2, c0 = (tid & 3) * 2;
       const float wj = ex2_approx(cum_end - s_cum[j]) * s_dl[j];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 2; ++q) {
         const uint32_t o = sw_chunk(j, c0 + q);
         float v[8];
         unpack_chunk(*reinterpret_cast<const uint4*>(sm + TcSmem::kX + o), v, __nv_bfloat16());
@@ -311,12 +315,10 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     if (tid == 0) {
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        tc_mma(tmem + 128, sdesc(sb + TcSmem::kB + ks * 2048, kQ * 128, 1024),
-               sdesc(sb + TcSmem::kWh + ks * 2048, kQ * 128, 1024), id_s, ks > 0);
+        tc_mma(tmem + 192, dadd(dN, TcSmem::kB + ks * 2048), dadd(dN, TcSmem::kWh + ks * 2048), id_s, ks > 0);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        tc_mma(tmem + 128, sdesc(sb + TcSmem::kB + ks * 2048, kQ * 128, 1024),
-               sdesc(sb + TcSmem::kWl + ks * 2048, kQ * 128, 1024), id_s, 1);
+        tc_mma(tmem + 192, dadd(dN, TcSmem::kB + ks * 2048), dadd(dN, TcSmem::kWl + ks * 2048), id_s, 1);
       tc_commit(&bars[1]);
     }
     ok = mbar_wait_bounded(&bars[0], par, &g_ssd_status);
@@ -324,20 +326,21 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     tc_fence_after();
     if (ok && c + 1 < nchunks) load_bc(t0 + kQ, TcSmem::kC, Cg);   // G and Yo are done with C
     const int fg = lane >> 2, ft = lane & 3;             // fragment row and column pair of this lane
-    const int ri0 = warp * 16 + fg, ri1 = ri0 + 8;       // its two rows of the M = 64 results
+    const int ri0 = quad * 16 + fg, ri1 = ri0 + 8;       // its two rows of the M = 64 results
     if (ok) {
       const float cr0 = s_cum[ri0], cr1 = s_cum[ri1];
-      float g[32];
-      tc_ld_frag64(tmem + t_lane + 0, g);
+      float g[16];
+      tc_ld_frag32(tmem + t_lane + pbase, g);
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
+      for (int rr = 0; rr < 4; ++rr) {
+        const int r = 4 * half + rr;                     // 16-byte column chunk of the row
         const int j = 8 * r + 2 * ft;
         const float2 cj = *reinterpret_cast<const float2*>(&s_cum[j]);
         const float2 dj = *reinterpret_cast<const float2*>(&s_dl[j]);
-        const float m00 = j <= ri0 ? g[4 * r] * ex2_approx(cr0 - cj.x) * dj.x : 0.0f;
-        const float m01 = j + 1 <= ri0 ? g[4 * r + 1] * ex2_approx(cr0 - cj.y) * dj.y : 0.0f;
-        const float m10 = j <= ri1 ? g[4 * r + 2] * ex2_approx(cr1 - cj.x) * dj.x : 0.0f;
-        const float m11 = j + 1 <= ri1 ? g[4 * r + 3] * ex2_approx(cr1 - cj.y) * dj.y : 0.0f;
+        const float m00 = j <= ri0 ? g[4 * rr] * ex2_approx(cr0 - cj.x) * dj.x : 0.0f;
+        const float m01 = j + 1 <= ri0 ? g[4 * rr + 1] * ex2_approx(cr0 - cj.y) * dj.y : 0.0f;
+        const float m10 = j <= ri1 ? g[4 * rr + 2] * ex2_approx(cr1 - cj.x) * dj.x : 0.0f;
+        const float m11 = j + 1 <= ri1 ? g[4 * rr + 3] * ex2_approx(cr1 - cj.y) * dj.y : 0.0f;
         uint32_t hi, lo;
         const uint32_t o0 = sw_chunk(ri0, r) + 4 * ft, o1 = sw_chunk(ri1, r) + 4 * ft;
         split2(m00, m01, hi, lo);
@@ -358,11 +361,11 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     if (tid == 0) {
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        tc_mma(tmem + 0, sdesc(sb + TcSmem::kMh + ks * 32, 16, 1024), sdesc(sb + TcSmem::kX + ks * 2048, kQ * 128, 1024),
+        tc_mma(tmem + 0, dadd(dK, TcSmem::kMh + ks * 32), dadd(dN, TcSmem::kX + ks * 2048),
                id_yd, ks > 0);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        tc_mma(tmem + 0, sdesc(sb + TcSmem::kMl + ks * 32, 16, 1024), sdesc(sb + TcSmem::kX + ks * 2048, kQ * 128, 1024),
+        tc_mma(tmem + 0, dadd(dK, TcSmem::kMl + ks * 32), dadd(dN, TcSmem::kX + ks * 2048),
                id_yd, 1);
       tc_commit(&bars[2]);
     }
@@ -372,19 +375,18 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     if (ok && c + 1 < nchunks) load_bc(t0 + kQ, TcSmem::kB, Bg);   // G and S^T are done with B
     if (ok) {
       const float eE = ex2_approx(cum_end);
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      {
         float s[32];
-        tc_ld32(tmem + t_lane + 128 + half * 32, s);
+        tc_ld32(tmem + t_lane + 192 + pbase, s);
 #pragma unroll
-        for (int q = 0; q < 32; ++q) H[half * 32 + q] = fmaf(eE, H[half * 32 + q], s[q]);
+        for (int q = 0; q < 32; ++q) H[q] = fmaf(eE, H[q], s[q]);
       }
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
+      for (int c8 = 0; c8 < 4; ++c8) {
         uint4 hi, lo;
         split8(&H[c8 * 8], hi, lo);
-        *reinterpret_cast<uint4*>(sm + TcSmem::kHh + sw_chunk(n_own, c8)) = hi;
-        *reinterpret_cast<uint4*>(sm + TcSmem::kHl + sw_chunk(n_own, c8)) = lo;
+        *reinterpret_cast<uint4*>(sm + TcSmem::kHh + sw_chunk(n_own, 4 * half + c8)) = hi;
+        *reinterpret_cast<uint4*>(sm + TcSmem::kHl + sw_chunk(n_own, 4 * half + c8)) = lo;
       }
     }
     have_state = true;
@@ -393,11 +395,11 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     // first so that the next chunk's x can be requested before the output work.
     ok = ok && mbar_wait_bounded(&bars[2], par, &g_ssd_status);
     ok = __all_sync(0xffffffffu, ok);   // the tensor-memory loads below are warp-collective
-    uint32_t xw[16];   // x at this lane's fragment positions, bf16 pairs: [r][row half]
+    uint32_t xw[8];   // x at this lane's fragment positions, bf16 pairs: [r][row half]
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      xw[2 * r] = *reinterpret_cast<const uint32_t*>(sm + TcSmem::kX + sw_chunk(ri0, r) + 4 * ft);
-      xw[2 * r + 1] = *reinterpret_cast<const uint32_t*>(sm + TcSmem::kX + sw_chunk(ri1, r) + 4 * ft);
+    for (int rr = 0; rr < 4; ++rr) {
+      xw[2 * rr] = *reinterpret_cast<const uint32_t*>(sm + TcSmem::kX + sw_chunk(ri0, 4 * half + rr) + 4 * ft);
+      xw[2 * rr + 1] = *reinterpret_cast<const uint32_t*>(sm + TcSmem::kX + sw_chunk(ri1, 4 * half + rr) + 4 * ft);
     }
     tc_fence_before();
     ok = __syncthreads_and(ok) != 0;   // Yd and every thread are done with x
@@ -405,14 +407,20 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     if (ok && c + 1 < nchunks) load_x(t0 + kQ);
     if (ok) {
       const float e0 = ex2_approx(s_cum[ri0]), e1 = ex2_approx(s_cum[ri1]);
-      float yd[32], yo[32];
-      tc_ld_frag64(tmem + t_lane + 0, yd);
-      if (ys) tc_ld_frag64(tmem + t_lane + 64, yo);
+      float yd[16], yo[16];
+      tc_ld_frag32(tmem + t_lane + pbase, yd);
+      if (ys) {
+        float yl[16];
+        tc_ld_frag32(tmem + t_lane + 64 + pbase, yo);
+        tc_ld_frag32(tmem + t_lane + 128 + pbase, yl);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) yo[q] += yl[q];
+      }
       __nv_bfloat16* y0 = yg + ((static_cast<int64_t>(b) * L + t0 + ri0) * p.nheads + h) * kHd;
       __nv_bfloat16* y1 = yg + ((static_cast<int64_t>(b) * L + t0 + ri1) * p.nheads + h) * kHd;
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const int pc = 8 * r + 2 * ft;
+      for (int r = 0; r < 4; ++r) {
+        const int pc = pbase + 8 * r + 2 * ft;
         float v00 = yd[4 * r] + Dh * bf16lo_to_f32(xw[2 * r]);
         float v01 = yd[4 * r + 1] + Dh * bf16hi_to_f32(xw[2 * r]);
         float v10 = yd[4 * r + 2] + Dh * bf16lo_to_f32(xw[2 * r + 1]);
@@ -435,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
   if (ok && p.hT) {
     float* hT = p.hT + (static_cast<int64_t>(b) * p.nheads + h) * kHd * kNs;
 #pragma unroll
-    for (int q = 0; q < kHd; ++q) hT[q * kNs + n_own] = H[q];
+    for (int q = 0; q < kHd / 2; ++q) hT[(pbase + q) * kNs + n_own] = H[q];
   }
   tc_fence_before();
   __syncthreads();
