@@ -22,17 +22,18 @@ __device__ __forceinline__ float io_at(const IO* p, int64_t i) {
   return IoTraits<IO>::to_f32(p[i]);
 }
 
-// vectorised path: L % kVec == 0 and 16-byte aligned rows.  A persistent grid walks the flat
-// (row, chunk) index space with a grid-sized stride; each iteration a thread issues the loads of
-// kPer chunks (one stride apart) before any arithmetic (one per iteration measured fastest, with 16
-// blocks of the grid per SM).  Consecutive lanes hold consecutive flat chunks, so the three inputs before a chunk
-// come from the previous lane by a shuffle (lane 0 re-reads them).  Flat indices fit 32 bits
-// (checked on the host).
+// vectorised path: L % kVec == 0 and 16-byte aligned rows.  A grid of SSM_CONV_BLOCKS_PER_SM blocks per
+// SM walks the flat (row, chunk) index space with a grid-sized stride; each iteration a thread issues
+// the loads of kPer chunks (one stride apart) before any arithmetic (one per iteration measured
+// fastest; two or four chunks, or requesting the next chunk before computing the current one, were
+// slower).  Consecutive lanes hold consecutive flat chunks, so the three inputs before a chunk come
+// from the previous lane by a shuffle (lane 0 re-reads them).  Flat indices fit 32 bits (checked on
+// the host).
 #ifndef SSM_CONV_PER
 #define SSM_CONV_PER 1            // chunks per thread and iteration (1 measured fastest)
 #endif
 #ifndef SSM_CONV_BLOCKS_PER_SM
-#define SSM_CONV_BLOCKS_PER_SM 16 // blocks of the grid-stride loop per SM
+#define SSM_CONV_BLOCKS_PER_SM 32 // blocks of the grid-stride loop per SM (8: 73.9 us, 16: 71.9, 32: 69.8, 64: 69.8)
 #endif
 constexpr int kPer = SSM_CONV_PER;
 
