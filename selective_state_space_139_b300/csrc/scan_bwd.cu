@@ -70,12 +70,6 @@ __device__ __forceinline__ CT sp(CT v) {
 }
 
 template <typename CT>
-__device__ __forceinline__ CT expo(CT x) {
-  if constexpr (sizeof(CT) == 4) return ex2_approx(x * kLog2e);
-  else return exp(x);
-}
-
-template <typename CT>
 __device__ __forceinline__ CT sigm(CT x) {
   if constexpr (sizeof(CT) == 4) return rcp_approx(1.0f + ex2_approx(-x * kLog2e));
   else return 1.0 / (1.0 + exp(-x));
