@@ -190,27 +190,29 @@ __device__ __forceinline__ void store_seg(void* base, int64_t off, int nk, bool 
   }
 }
 
-// B and C of steps [t0, t0 + nk) of batch row b, widened: each thread fetches 2 of the segment's
-// 8 x 32 table entries ([step][B0..15 | C0..15], zeros past dstate / nk) and later stores them
-__device__ __forceinline__ void fetch_bc(const BwdParams& p, int b, int64_t t0, int nk, float (&r)[2]) {
+// B and C of steps [t0, t0 + nk) of batch row b: each thread fetches 2 of the segment's 8 x 32 table
+// entries ([step][B0..15 | C0..15], zeros past dstate / nk) one segment ahead and stores them, widened
+// to float, when that segment starts.  The loads keep their raw bits until then (bf16: the 16-bit
+// pattern), so no instruction waits for them while the current segment is computed.
+__device__ __forceinline__ void fetch_bc(const BwdParams& p, int b, int64_t t0, int nk, uint32_t (&r)[2]) {
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     const int i = threadIdx.x + j * kThreads;
     const int k = i / 32, col = i % 32, arr = col / 16, n = col % 16;
-    float v = 0.0f;
+    uint32_t v = 0u;
     if (k < nk && n < p.N) {
       const int64_t idx = (static_cast<int64_t>(b) * p.N + n) * p.L + t0 + k;
       const void* src = arr ? p.C : p.B;
-      v = p.io_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(src)[idx])
-                    : static_cast<const float*>(src)[idx];
+      v = p.io_bf16 ? static_cast<uint32_t>(static_cast<const unsigned short*>(src)[idx])
+                    : static_cast<const uint32_t*>(src)[idx];
     }
     r[j] = v;
   }
 }
 
-__device__ __forceinline__ void store_bc(float* bc, const float (&r)[2]) {
-  bc[threadIdx.x] = r[0];
-  bc[threadIdx.x + kThreads] = r[1];
+__device__ __forceinline__ void store_bc(float* bc, const uint32_t (&r)[2], bool bf16) {
+  bc[threadIdx.x] = __uint_as_float(bf16 ? r[0] << 16 : r[0]);
+  bc[threadIdx.x + kThreads] = __uint_as_float(bf16 ? r[1] << 16 : r[1]);
 }
 
 // One checkpoint record: 16 states, 64 (float) or 128 (double) bytes, 16-byte aligned.
@@ -291,10 +293,10 @@ __global__ void __launch_bounds__(kThreads, sizeof(CT) == 4 ? SSM_BWD_FWD_MINB :
   CT* cs = static_cast<CT*>(p.ckpt_s) + T.row * nseg;
   auto seg_len = [&](int64_t t0) { return static_cast<int>(T.c1 - t0 < kSeg ? T.c1 - t0 : kSeg); };
   SegRaw<IO> raw;
-  float bcr[2];
+  uint32_t bcr[2];
   fetch_seg<IO>(p, T.row * p.L + T.c0, seg_len(T.c0), raw);
   fetch_bc(p, T.b, T.c0, seg_len(T.c0), bcr);
-  store_bc(bc_buf[0], bcr);
+  store_bc(bc_buf[0], bcr, p.io_bf16);
   __syncthreads();
   int buf = 0;
   for (int64_t t0 = T.c0; t0 < T.c1; t0 += kSeg) {
@@ -332,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, sizeof(CT) == 4 ? SSM_BWD_FWD_MINB :
         }
       }
     }
-    if (more) store_bc(bc_buf[buf ^ 1], bcr);
+    if (more) store_bc(bc_buf[buf ^ 1], bcr, p.io_bf16);
     __syncthreads();
     buf ^= 1;
   }
@@ -385,10 +387,10 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_fwd2_kernel(const BwdParams p
   float* cs = static_cast<float*>(p.ckpt_s) + row * nseg;
   auto seg_len = [&](int64_t t0) { return static_cast<int>(c1 - t0 < kSeg ? c1 - t0 : kSeg); };
   SegRaw<IO> raw;
-  float bcr[2];
+  uint32_t bcr[2];
   fetch_seg<IO>(p, row * p.L + c0, seg_len(c0), raw);
   fetch_bc(p, b, c0, seg_len(c0), bcr);
-  store_bc(bc_buf[0], bcr);
+  store_bc(bc_buf[0], bcr, p.io_bf16);
   __syncthreads();
   int buf = 0;
   for (int64_t t0 = c0; t0 < c1; t0 += kSeg) {
@@ -428,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_fwd2_kernel(const BwdParams p
         }
       }
     }
-    if (more) store_bc(bc_buf[buf ^ 1], bcr);
+    if (more) store_bc(bc_buf[buf ^ 1], bcr, p.io_bf16);
     __syncthreads();
     buf ^= 1;
   }
@@ -577,7 +579,7 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_rev_kernel(const BwdParams
   };
   const int64_t last = T.c0 + ((T.c1 - T.c0 - 1) / kSeg) * kSeg;
   SegRaw<IO> raw;
-  float bcr[2];
+  uint32_t bcr[2];
   CT ckr[kN], ckS;
   auto fetch_ck = [&](int64_t t0) {
     const int64_t s = t0 / kSeg;
@@ -587,7 +589,7 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_rev_kernel(const BwdParams
   fetch_seg<IO>(p, T.row * p.L + last, seg_len(last), raw);
   fetch_bc(p, T.b, last, seg_len(last), bcr);
   fetch_ck(last);
-  store_bc(bc_base, bcr);
+  store_bc(bc_base, bcr, p.io_bf16);
   __syncthreads();
   int buf = 0;
   int64_t pend_t0 = -1;   // the segment whose dB/dC partials wait in the other red buffer
@@ -699,7 +701,7 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_rev_kernel(const BwdParams
       store_seg<IO, CT>(p.du, off, nk, p.vec_io, gdu);
       store_seg<IO, CT>(p.ddelta, off, nk, p.vec_io, gdd);
     }
-    if (more) store_bc(bc_base + (buf ^ 1) * (kSeg * 32), bcr);
+    if (more) store_bc(bc_base + (buf ^ 1) * (kSeg * 32), bcr, p.io_bf16);
     __syncthreads();
     pend_t0 = t0;
     pend_nk = nk;
@@ -797,7 +799,7 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
   };
   const int64_t last = c0 + ((c1 - c0 - 1) / kSeg) * kSeg;
   SegRaw<IO> raw;
-  float bcr[2];
+  uint32_t bcr[2];
   float4 ckr0, ckr1;
   float ckS;
   auto fetch_ck = [&](int64_t t0) {
@@ -809,7 +811,7 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
   fetch_seg<IO>(p, row * p.L + last, seg_len(last), raw);
   fetch_bc(p, b, last, seg_len(last), bcr);
   fetch_ck(last);
-  store_bc(bc_base, bcr);
+  store_bc(bc_base, bcr, p.io_bf16);
   __syncthreads();
   int buf = 0;
   int64_t pend_t0 = -1;
@@ -935,7 +937,7 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
       store_seg<IO, float>(p.du, off, nk, p.vec_io, gdu);
       store_seg<IO, float>(p.ddelta, off, nk, p.vec_io, gdd);
     }
-    if (more) store_bc(bc_base + (buf ^ 1) * (kSeg * 32), bcr);
+    if (more) store_bc(bc_base + (buf ^ 1) * (kSeg * 32), bcr, p.io_bf16);
     __syncthreads();
     pend_t0 = t0;
     pend_nk = nk;
