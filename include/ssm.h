@@ -269,6 +269,19 @@ SSM_API ssm_status ssm_ssd_state_update(const void* x_t, const void* dt_t, const
                                         int ngroups, ssm_dtype io_dtype, cudaStream_t stream);
 
 /*
+ * Diagnostic of the device failure path; the pages have no counterpart.  Enqueues one small kernel
+ * that performs a bounded wait which nothing can satisfy and gives up after limit_ns nanoseconds
+ * (clamped to 1 ms .. 2 s), recording a timeout in the device status word exactly as the library's
+ * kernels do when one of their waits runs out:
+ *   which = 0: an mbarrier phase that never completes (the wait of the TMA pipelines);
+ *   which = 1: a global flag that nothing sets (the wait of the balanced schedule's carry).
+ * The next ssm_device_status() then returns SSM_ERR_TIMEOUT and clears the word; the CUDA context
+ * stays usable.  Nothing faults, traps or waits without a limit.  Returns SSM_ERR_INVALID_ARG for
+ * another `which` (before enqueuing anything) and SSM_ERR_CUDA if the launch fails.
+ */
+SSM_API ssm_status ssm_selftest_bounded_wait(int which, int64_t limit_ns, cudaStream_t stream);
+
+/*
  * Reads and clears the device status word (synchronises `stream`).  Returns SSM_OK, SSM_ERR_TIMEOUT
  * if a kernel gave up a bounded wait since the last call, or SSM_ERR_CUDA.
  */

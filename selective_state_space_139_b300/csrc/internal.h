@@ -172,6 +172,10 @@ cudaError_t ssd_status_read_and_clear(unsigned int* out);
 // Sets the text returned by ssm_last_error_message() on the calling host thread (ssm_api.cu).
 void set_last_error(const char* fmt, ...);
 
+// Self-test of the device failure path (selftest.cu): which 0 = an mbarrier wait, 1 = a flag poll.
+cudaError_t selftest_bounded_wait_launch(int which, unsigned long long limit_ns, cudaStream_t stream);
+cudaError_t selftest_status_read_and_clear(unsigned int* out);
+
 // Device status word access (scan_fwd.cu owns the symbol).
 cudaError_t read_and_clear_device_status(unsigned int* out, cudaStream_t stream);
 

@@ -548,6 +548,10 @@ cudaError_t read_and_clear_device_status(unsigned int* out, cudaStream_t stream)
   unsigned int ssd = 0;
   e = ssd_status_read_and_clear(&ssd);
   *out |= ssd;
+  if (e != cudaSuccess) return e;
+  unsigned int st = 0;
+  e = selftest_status_read_and_clear(&st);
+  *out |= st;
   return e;
 }
 

@@ -519,6 +519,15 @@ ssm_status ssm_causal_conv1d_fwd(const void* x, const float* conv_w, const float
   return SSM_OK;
 }
 
+ssm_status ssm_selftest_bounded_wait(int which, int64_t limit_ns, cudaStream_t stream) {
+  g_err[0] = 0;
+  if (which != 0 && which != 1) return fail(SSM_ERR_INVALID_ARG, "which must be 0 (mbarrier) or 1 (flag), got %d", which);
+  const int64_t lim = limit_ns < 1000000 ? 1000000 : (limit_ns > 2000000000 ? 2000000000 : limit_ns);
+  cudaError_t ce = ssm::selftest_bounded_wait_launch(which, static_cast<unsigned long long>(lim), stream);
+  if (ce != cudaSuccess) return cuda_fail(ce, "self-test launch");
+  return SSM_OK;
+}
+
 ssm_status ssm_device_status(cudaStream_t stream) {
   unsigned int word = 0;
   cudaError_t ce = ssm::read_and_clear_device_status(&word, stream);

@@ -199,3 +199,8 @@ def test_ssd_state_update_rejects_bad_arguments_on_host(lib):
     assert call(st=None) == ssm.SSM_ERR_INVALID_ARG
     assert call(st=P + 0x1000008) == ssm.SSM_ERR_INVALID_ARG   # state not 16-byte aligned
     assert call(y=P + 0x1000000) == ssm.SSM_ERR_INVALID_ARG    # y overlaps the state
+
+
+def test_selftest_rejects_unknown_wait_kind_on_host(lib):
+    assert lib.ssm_selftest_bounded_wait(2, 1000000, None) == ssm.SSM_ERR_INVALID_ARG
+    assert lib.ssm_selftest_bounded_wait(-1, 1000000, None) == ssm.SSM_ERR_INVALID_ARG
