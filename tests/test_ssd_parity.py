@@ -2,8 +2,8 @@
 
 bf16 io with float32 accumulation and state: max relative error (floor 1e-3 of the largest
 reference value) of 1e-2, the bound used for every bf16-io path.  Small and ragged shapes compare
-every output; the Mamba-2 layer compares sampled heads over all batch rows at full length, in the
-configuration the benchmark times.
+every output; so do the full Mamba-2 layer and the full decode workload, in the configurations the
+benchmark times.
 """
 import numpy as np
 import pytest
@@ -26,13 +26,10 @@ def _dev():
     return torch.device("cuda:0")
 
 
-def _oracle(inp, heads=None, use_D=True, use_bias=True, softplus=True, h0=None):
-    sl = (lambda t: t) if heads is None else (lambda t: t[:, :, heads])
-    hs = (lambda t: t) if heads is None else (lambda t: t[heads])
-    return oracle.ssd_scan(to64(sl(inp["x"])), to64(sl(inp["dt"])), to64(hs(inp["A"])), to64(inp["B"]),
-                           to64(inp["C"]), D=to64(hs(inp["D"])) if use_D else None,
-                           dt_bias=to64(hs(inp["dt_bias"])) if use_bias else None, dt_softplus=softplus,
-                           h0=None if h0 is None else to64(h0 if heads is None else h0[:, heads]))
+def _oracle(inp, use_D=True, use_bias=True, softplus=True, h0=None):
+    return oracle.ssd_scan(to64(inp["x"]), to64(inp["dt"]), to64(inp["A"]), to64(inp["B"]), to64(inp["C"]),
+                           D=to64(inp["D"]) if use_D else None, dt_bias=to64(inp["dt_bias"]) if use_bias else None,
+                           dt_softplus=softplus, h0=None if h0 is None else to64(h0))
 
 
 def _run(inp, use_D=True, use_bias=True, softplus=True, h0=None):
@@ -80,14 +77,14 @@ def test_ssd_groups_h0_and_options():
     _check(y, hT, *_oracle(inp, softplus=False, use_bias=False))
 
 
-def test_ssd_mamba2_layer_sampled_heads():
+def test_ssd_mamba2_layer_full():
+    """Every output of the Mamba-2 SSD layer (batch 4, L 4096, 128 heads x 64, d_state 128)."""
     dev = _dev()
     w = W.WORKLOADS["mamba2-ssd-layer"]
     inp = W.make_ssd_inputs(w, device=dev)
     y, hT = _run(inp)
-    heads = [0, 1, 77, w.nheads - 1]
-    ry, rh = _oracle(inp, heads=heads)
-    _check(y[:, :, heads], hT[:, heads], ry, rh)
+    assert torch.isfinite(y).all()
+    _check(y, hT, *_oracle(inp))
 
 
 def test_ssd_seqlen_zero_passes_the_state_through():
@@ -154,15 +151,15 @@ def test_ssd_prefill_then_decode_equals_longer_prefill():
     _check(torch.cat([y1, y2], dim=1), state, ry, rh)
 
 
-def test_ssd_decode_workload_sampled_heads():
+def test_ssd_decode_workload_full():
+    """Every output of the Mamba-2 decode workload (64 sequences x 128 heads, 200 token steps) against
+    one oracle prefill of the same token stream."""
     dev = _dev()
     w = W.WORKLOADS["mamba2-decode"]
     d = W.make_ssd_decode_inputs(w, device=dev)
     state = torch.zeros((w.batch, w.nheads, w.headdim, w.dstate), device=dev)
-    steps = 40
-    y = _decode_steps(d, state, 0, steps)
-    heads = [0, 63, w.nheads - 1]
-    full = {k: d[k][:steps].transpose(0, 1) for k in ("x", "dt", "B", "C")}
-    ry, rh = oracle.ssd_scan(to64(full["x"][:, :, heads]), to64(full["dt"][:, :, heads]), to64(d["A"][heads]),
-                             to64(full["B"]), to64(full["C"]), D=to64(d["D"][heads]), dt_bias=to64(d["dt_bias"][heads]))
-    _check(y[:, :, heads], state[:, heads], ry, rh)
+    y = _decode_steps(d, state, 0, w.seqlen)
+    full = {k: d[k].transpose(0, 1) for k in ("x", "dt", "B", "C")}
+    ry, rh = oracle.ssd_scan(to64(full["x"]), to64(full["dt"]), to64(d["A"]), to64(full["B"]), to64(full["C"]),
+                             D=to64(d["D"]), dt_bias=to64(d["dt_bias"]))
+    _check(y, state, ry, rh)
