@@ -9,6 +9,13 @@ backward, the Mamba-2 SSD layer and the Mamba-2 decode step are measured after i
 same JSON line under "decode", "conv1d", "backward", "ssd" and "ssd_decode".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+                    [--only scan|decode|conv1d|backward|ssd|ssd_decode]
+
+The scan's inputs (674 MB per step) are larger than L2.  "e2e" repeats the measurement through the
+binding with pinned host inputs copied in and y / the final state copied out every step (consecutive
+steps overlap on three streams).  The decode roofline times each step after flushing L2 (its working
+set fits in L2); the CUDA-graph time of back-to-back steps is reported beside it.  "cpu_baseline"
+times the fp64 oracle on all host cores and on one thread.
 
 Under torchrun every rank runs its own replica (its own batch of the workload, no collective on the
 data path); value = tokens of all ranks / the slowest rank's time ("scaling": "weak").
