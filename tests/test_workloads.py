@@ -45,3 +45,32 @@ def test_decode_inputs_shapes():
     x = W.make_decode_inputs(d)
     assert x["x"].shape == (5, 3, 10) and x["B"].shape == (5, 3, 16) and x["conv_w"].shape == (10, 4)
     assert abs(float(x["conv_w"].std()) - 0.5) < 0.25
+
+
+def test_ssd_generators_shapes_ranges_and_determinism():
+    w = W.WORKLOADS["ssd-small"]
+    a = W.make_ssd_inputs(w)
+    b = W.make_ssd_inputs(w)
+    assert a["x"].shape == (w.batch, w.seqlen, w.nheads, w.headdim) and a["x"].dtype == torch.bfloat16
+    assert a["dt"].shape == (w.batch, w.seqlen, w.nheads)
+    assert a["B"].shape == a["C"].shape == (w.batch, w.seqlen, w.ngroups, w.dstate)
+    for k in ("A", "D", "dt_bias"):
+        assert a[k].shape == (w.nheads,) and a[k].dtype == torch.float32
+    for k in a:
+        assert torch.equal(a[k], b[k])                        # same seed, same tensors
+    assert (a["A"] < 0).all() and (a["A"] >= -16).all() and (a["A"] <= -1).all()
+    s = torch.nn.functional.softplus(a["dt_bias"].double())   # softplus(dt_bias) is the drawn step size
+    assert (s >= 1e-3 * (1 - 1e-5)).all() and (s <= 0.1 * (1 + 1e-5)).all()
+    assert not torch.equal(W.make_ssd_inputs(w, seed=w.seed + 1)["x"], a["x"])
+
+
+def test_ssd_decode_inputs_are_the_prefill_stream_step_major():
+    w = W.WORKLOADS["ssd-small"]
+    full = W.make_ssd_inputs(w)
+    d = W.make_ssd_decode_inputs(w)
+    assert d["x"].shape == (w.seqlen, w.batch, w.nheads, w.headdim)
+    for k in ("x", "dt", "B", "C"):
+        assert torch.equal(d[k].transpose(0, 1), full[k])
+    bh = w.batch * w.nheads
+    expect = 2 * bh * 64 * 128 * 4 + (2 * bh * 64 + bh + 2 * w.batch * w.ngroups * 128) * 2 + 3 * w.nheads * 4
+    assert W.ssd_decode_bytes_per_step(w) == expect
