@@ -102,6 +102,9 @@ SSM_API size_t ssm_scan_fwd_workspace_size_ex(int batch, int dim, int dstate, in
  *                    aligned; may be NULL when that size is 0.
  * Precision: y matches the exact recurrence to about 1e-6 relative for float32 io and to bf16
  * rounding (plus about 1e-4 relative) for bfloat16 io; the state is kept in float32 throughout.
+ * y and last_state are defined once ssm_device_status() has returned SSM_OK for the stream: the
+ * balanced schedule hands states from one CTA to the next behind a bounded wait, and a wait that
+ * gives up (status SSM_ERR_TIMEOUT) leaves the rest of that CTA's range computed from a zero state.
  */
 SSM_API ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B, const void* C,
                         const float* D, const void* z, const float* delta_bias, int softplus_flag,
@@ -168,7 +171,8 @@ SSM_API size_t ssm_scan_fwd_noalloc_max_scratch(void);
 /* How a prefill call with these sizes and options would run (filled by ssm_scan_fwd_describe). */
 typedef struct {
   int struct_size;           /* set to sizeof(ssm_scan_plan) before the call */
-  int path;                  /* 0: general kernel (float32 io, exact ZOH, or layouts TMA cannot use); 1: bf16 fast path */
+  int path;                  /* 0: general kernel (float32 io, exact ZOH, or layouts TMA cannot use);
+                                1: bf16 two-lane kernel; 2: bf16 rescaled-state kernel, one thread per channel */
   int schedule;              /* 0: one CTA per channel tile; 1: balanced persistent ranges; 2: chunked (aggregates, carry, re-run) */
   int nchunks;               /* time chunks (1 unless schedule 2) */
   int64_t chunk_len;         /* steps per chunk */
@@ -280,6 +284,19 @@ SSM_API ssm_status ssm_ssd_state_update(const void* x_t, const void* dt_t, const
  * another `which` (before enqueuing anything) and SSM_ERR_CUDA if the launch fails.
  */
 SSM_API ssm_status ssm_selftest_bounded_wait(int which, int64_t limit_ns, cudaStream_t stream);
+
+/*
+ * Diagnostic of the balanced schedule's carry wait, on the real prefill kernels; the pages have no
+ * counterpart.  Arms a one-shot fault for the next ssm_scan_fwd / ssm_scan_fwd_ex call made on the
+ * calling host thread: if that call runs the balanced schedule (ssm_scan_fwd_describe: schedule 1),
+ * CTA `cta` computes and writes its carry but never raises the flag that publishes it, and the carry
+ * wait of every CTA is limited to limit_ns nanoseconds (clamped to 1 ms .. 2 s).  CTA cta + 1 then
+ * gives up its wait, records a timeout in the device status word and finishes its range from a zero
+ * state; the next ssm_device_status() returns SSM_ERR_TIMEOUT.  Nothing faults or waits without a
+ * limit, and the context stays usable.  A call with another schedule consumes the arming without
+ * effect.  Returns SSM_ERR_INVALID_ARG for cta < 0.
+ */
+SSM_API ssm_status ssm_selftest_withhold_carry(int cta, int64_t limit_ns);
 
 /*
  * Reads and clears the device status word (synchronises `stream`).  Returns SSM_OK, SSM_ERR_TIMEOUT

@@ -37,8 +37,12 @@ struct ScanParams {
   // bf16 fast path, balanced persistent schedule
   int sched_balanced;     // 1: one range of (group, tile) work per resident CTA
   int64_t range_tiles;    // tiles per CTA range
-  float* carry;           // (ctas, 64, 16) states handed from one CTA to the next
+  float* carry;           // (ctas, channels per CTA, 16) states handed from one CTA to the next
   unsigned* flags;        // (ctas) publication flags
+  // Diagnostics (ssm_selftest_withhold_carry): the CTA whose carry publication is withheld (-1: none)
+  // and the limit of the carry wait in ns (0: the default 2 s).
+  int test_withhold_cta;
+  uint64_t carry_wait_ns;
 };
 
 // Steps per time tile for an io element size (64 for bf16, 32 for float32).
@@ -182,7 +186,14 @@ cudaError_t read_and_clear_device_status(unsigned int* out, cudaStream_t stream)
 // Carry pass of the chunked algorithm over float carries (scan_fwd.cu).
 cudaError_t carry_launch_f32(const ScanParams& p, int nchunks, cudaStream_t stream);
 
-// bf16 fast path (scan_fast.cu).
+// bf16 prefill on the rescaled state, one thread per channel (scan_scaled.cu).
+int scaled_channels_per_cta();
+int scaled_resident_ctas();   // co-resident CTAs on the current device (0 if unknown)
+cudaError_t scaled_status_read_and_clear(unsigned int* out);
+cudaError_t scan_scaled_launch(const ScanParams& p, int nchunks, int balanced_ctas, cudaStream_t stream, char* err,
+                               size_t errlen);
+
+// bf16 fast path, two lanes per channel (scan_fast.cu).
 int fast_channels_per_cta();
 int fast_resident_ctas();   // co-resident CTAs on the current device (0 if unknown)
 cudaError_t fast_status_read_and_clear(unsigned int* out);

@@ -28,6 +28,7 @@
 #include <cstring>
 
 #include "internal.h"
+#include "scan_walk.cuh"
 #include "ssm_device.cuh"
 
 // Build-time variants (the defaults are the measured best).
@@ -85,49 +86,6 @@ enum { kMain = 0, kAgg = 1 };
 struct Maps {
   CUtensorMap u, dt, z, B, C;
 };
-
-// The (group, tile) sequence one CTA walks, in processing order.
-struct Walk {
-  int64_t g_head;   // partial head group (tiles [0, tb)), -1 if none
-  int64_t tb;
-  int64_t gf0, gf1; // complete groups [gf0, gf1)
-  int64_t g_tail;   // tail group (tiles [ta, Lt)), -1 if none
-  int64_t ta;
-  int64_t n_head, n_full, n_tail;   // tile counts of the three parts
-  int64_t Lt;
-  __device__ int64_t total() const { return n_head + n_full + n_tail; }
-  // tile k of the walk -> (group, tile within group)
-  __device__ void at(int64_t k, int64_t& g, int64_t& t) const {
-    if (k < n_head) { g = g_head; t = k; return; }
-    k -= n_head;
-    if (k < n_full) { g = gf0 + k / Lt; t = k % Lt; return; }
-    k -= n_full;
-    g = g_tail; t = ta + k;
-  }
-};
-
-__device__ Walk make_walk_balanced(int64_t cta, int64_t R, int64_t total_tiles, int64_t Lt) {
-  Walk w;
-  w.Lt = Lt;
-  const int64_t A = cta * R;
-  const int64_t Bn = A + R < total_tiles ? A + R : total_tiles;
-  w.g_head = -1; w.g_tail = -1; w.tb = 0; w.ta = 0; w.n_head = 0; w.n_tail = 0;
-  w.gf0 = w.gf1 = 0; w.n_full = 0;
-  if (Bn <= A) return w;
-  const int64_t g0 = A / Lt, ta = A % Lt;
-  const int64_t g1 = (Bn - 1) / Lt, tb = (Bn - 1) % Lt + 1;
-  int64_t f0 = g0, f1 = g1 + 1;   // candidate complete groups
-  if (ta > 0) {                   // g0 starts mid-group: it is the tail (needs the carry)
-    w.g_tail = g0; w.ta = ta; w.n_tail = Lt - ta; f0 = g0 + 1;
-    if (g1 == g0) { f1 = f0; }    // a single tail segment (it runs to the group end)
-  }
-  if (tb < Lt && !(g1 == g0 && ta > 0)) {   // g1 ends mid-group: its head is run first
-    w.g_head = g1; w.tb = tb; w.n_head = tb; f1 = g1;
-  }
-  if (f1 < f0) f1 = f0;
-  w.gf0 = f0; w.gf1 = f1; w.n_full = (f1 - f0) * Lt;
-  return w;
-}
 
 __device__ __forceinline__ float prmt_half(uint32_t word, uint32_t sel) {
   return __uint_as_float(__byte_perm(word, 0u, sel));
@@ -190,14 +148,8 @@ __global__ void __launch_bounds__(kCh * kLanes, SSM_FAST_MINB) scan_fast_kernel(
     w = make_walk_balanced(blockIdx.x, p.range_tiles, static_cast<int64_t>(p.batch) * gpb * Lt, Lt);
   } else {
     // one (group, chunk): a single segment started from h0 / the carried-in state
-    const int64_t g = blockIdx.x;
     chunk_idx = blockIdx.y;
-    const int64_t ct = (p.chunk_len + kT - 1) / kT;
-    const int64_t t0 = chunk_idx * ct;
-    const int64_t t1 = t0 + ct < Lt ? t0 + ct : Lt;
-    w.Lt = Lt; w.g_head = -1; w.tb = 0; w.n_head = 0; w.g_tail = -1; w.ta = 0; w.n_tail = 0;
-    if (t0 == 0 && t1 == Lt) { w.gf0 = g; w.gf1 = g + 1; w.n_full = Lt; }
-    else { w.gf0 = w.gf1 = 0; w.n_full = 0; w.g_tail = g; w.ta = t0; w.n_tail = t1 - t0; }
+    w = make_walk_grid(blockIdx.x, chunk_idx, (p.chunk_len + kT - 1) / kT, Lt);
   }
   const int64_t ntiles = w.total();
 
@@ -288,7 +240,7 @@ __global__ void __launch_bounds__(kCh * kLanes, SSM_FAST_MINB) scan_fast_kernel(
             unsigned v;
             asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
             if (v != 0u) { got = 1; break; }
-            if (globaltimer_ns() - t0 > 2000000000ull) break;
+            if (globaltimer_ns() - t0 > (p.carry_wait_ns ? p.carry_wait_ns : 2000000000ull)) break;
             __nanosleep(200);
           }
           if (!got) atomicOr(&g_fast_status, kStatusTimeout);
@@ -607,7 +559,7 @@ __global__ void __launch_bounds__(kCh * kLanes, SSM_FAST_MINB) scan_fast_kernel(
         dst[2 * i + 1] = f2_hi(h[i]);
       }
       __syncthreads();
-      if (tid == 0) {
+      if (tid == 0 && static_cast<int>(blockIdx.x) != p.test_withhold_cta) {
         __threadfence();
         asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.flags + blockIdx.x), "r"(1u) : "memory");
       }

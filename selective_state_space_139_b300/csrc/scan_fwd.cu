@@ -545,6 +545,10 @@ cudaError_t read_and_clear_device_status(unsigned int* out, cudaStream_t stream)
   e = fast_status_read_and_clear(&fast);
   *out |= fast;
   if (e != cudaSuccess) return e;
+  unsigned int scaled = 0;
+  e = scaled_status_read_and_clear(&scaled);
+  *out |= scaled;
+  if (e != cudaSuccess) return e;
   unsigned int ssd = 0;
   e = ssd_status_read_and_clear(&ssd);
   *out |= ssd;

@@ -16,6 +16,14 @@ namespace {
 
 thread_local char g_err[512] = {0};
 
+// One-shot diagnostic of the balanced schedule's carry wait (ssm_selftest_withhold_carry).
+struct Withhold {
+  bool armed = false;
+  int cta = -1;
+  int64_t limit_ns = 0;
+};
+thread_local Withhold g_withhold;
+
 ssm_status fail(ssm_status s, const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
@@ -60,7 +68,8 @@ int sm_count() {
 }
 
 struct Plan {
-  int path = 0;           // 0: general kernel (float32 io, ZOH, layouts TMA cannot describe); 1: bf16 fast path
+  int path = 0;           // 0: general kernel (float32 io, ZOH, layouts TMA cannot describe); 1: bf16 two-lane
+                          // kernel; 2: bf16 rescaled-state kernel (one thread per channel)
   int nchunks = 1;
   int64_t chunk_len = 0;
   int balanced_ctas = 0;  // fast path: > 0 selects the balanced persistent schedule
@@ -99,6 +108,25 @@ bool make_plan(int batch, int dim, int dstate, int64_t seqlen, ssm_dtype io, con
   }
   const int sms = sm_count();
   *pl = Plan();
+  if (fast_eligible(batch, dim, seqlen, io, disc) && seqlen % 16 == 0 && algo != SSM_ALGO_CHUNKED) {
+    // rescaled-state kernel under the balanced schedule when there are at least as many 128-channel
+    // groups as resident CTAs
+    const int64_t cpc = ssm::scaled_channels_per_cta();
+    const int64_t G = static_cast<int64_t>(batch) * ((dim + cpc - 1) / cpc);
+    const int64_t Lt = (seqlen + 63) / 64;
+    const int64_t S = ssm::scaled_resident_ctas();
+    if (S > 0 && G >= S) {
+      pl->path = 2;
+      pl->balanced_ctas = static_cast<int>(S);
+      pl->range_tiles = (G * Lt + S - 1) / S;
+      pl->nchunks = 1;
+      pl->chunk_len = seqlen;
+      pl->off_carry = 0;
+      pl->off_flags = round_up(static_cast<size_t>(S) * cpc * 16 * sizeof(float), 256);
+      pl->workspace = pl->off_flags + round_up(static_cast<size_t>(S) * sizeof(unsigned), 256);
+      return true;
+    }
+  }
   if (fast_eligible(batch, dim, seqlen, io, disc)) {
     pl->path = 1;
     const int64_t cpc = ssm::fast_channels_per_cta();
@@ -274,7 +302,8 @@ ssm_status ssm_scan_fwd_describe(int batch, int dim, int dstate, int64_t seqlen,
   plan->nchunks = pl.nchunks;
   plan->chunk_len = pl.chunk_len;
   plan->workspace_bytes = pl.workspace;
-  const int64_t cpc = pl.path == 1 ? ssm::fast_channels_per_cta() : kChannelsPerCta;
+  const int64_t cpc = pl.path == 1 ? ssm::fast_channels_per_cta()
+                      : pl.path == 2 ? ssm::scaled_channels_per_cta() : kChannelsPerCta;
   const int64_t groups = static_cast<int64_t>(batch) * ((dim + cpc - 1) / cpc);
   if (pl.balanced_ctas > 0) {
     plan->schedule = 1;
@@ -370,8 +399,26 @@ ssm_status ssm_scan_fwd_ex(const void* u, const void* delta, const float* A, con
   bool aligned16 = true;
   for (const void* q : {u, delta, z, B, C, static_cast<const void*>(y)})
     if (q && !aligned(q, 16)) aligned16 = false;
+  p.test_withhold_cta = -1;
+  p.carry_wait_ns = 0;
+  if (g_withhold.armed) {
+    // one-shot diagnostic armed by ssm_selftest_withhold_carry on this host thread
+    p.test_withhold_cta = g_withhold.cta;
+    p.carry_wait_ns = static_cast<uint64_t>(g_withhold.limit_ns);
+    g_withhold.armed = false;
+  }
   char err[256] = {0};
   char* ws = static_cast<char*>(workspace);
+  if (pl.path == 2 && aligned16) {
+    p.sched_balanced = 1;
+    p.range_tiles = pl.range_tiles;
+    p.carry = reinterpret_cast<float*>(ws + pl.off_carry);
+    p.flags = reinterpret_cast<unsigned*>(ws + pl.off_flags);
+    p.chunk_len = seqlen;
+    cudaError_t ce = ssm::scan_scaled_launch(p, 1, pl.balanced_ctas, stream, err, sizeof(err));
+    if (ce != cudaSuccess) return cuda_fail(ce, err[0] ? err : "scan launch");
+    return SSM_OK;
+  }
   if (pl.path == 1 && aligned16) {
     if (pl.balanced_ctas > 0) {
       p.sched_balanced = 1;
@@ -525,6 +572,15 @@ ssm_status ssm_selftest_bounded_wait(int which, int64_t limit_ns, cudaStream_t s
   const int64_t lim = limit_ns < 1000000 ? 1000000 : (limit_ns > 2000000000 ? 2000000000 : limit_ns);
   cudaError_t ce = ssm::selftest_bounded_wait_launch(which, static_cast<unsigned long long>(lim), stream);
   if (ce != cudaSuccess) return cuda_fail(ce, "self-test launch");
+  return SSM_OK;
+}
+
+ssm_status ssm_selftest_withhold_carry(int cta, int64_t limit_ns) {
+  g_err[0] = 0;
+  if (cta < 0) return fail(SSM_ERR_INVALID_ARG, "cta must be >= 0, got %d", cta);
+  g_withhold.armed = true;
+  g_withhold.cta = cta;
+  g_withhold.limit_ns = limit_ns < 1000000 ? 1000000 : (limit_ns > 2000000000 ? 2000000000 : limit_ns);
   return SSM_OK;
 }
 

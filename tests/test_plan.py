@@ -61,14 +61,15 @@ def test_bad_plans_are_refused():
 
 @pytest.mark.gpu
 def test_full_size_workloads_run_the_balanced_and_chunked_schedules():
-    """With the device's resident-CTA count known: the 2.8B layer (320 groups of 64 channels, at
-    least as many as two CTAs on each SM) runs the balanced persistent schedule in one launch; the
-    130M layer (192 groups) has too few groups and splits time into chunks."""
+    """With the device's resident-CTA count known: the 2.8B layer (160 groups of 128 channels, at
+    least one per SM) runs the rescaled-state kernel under the balanced persistent schedule in one
+    launch, one CTA per SM; the 130M layer (96 groups of 128, 192 of 64) has too few groups and
+    splits time into chunks."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     big = ssm.describe_scan(4, 5120, 16, 4096, dtype=BF16)
-    assert (big["path"], big["schedule"], big["kernel_launches"]) == ("fast", "balanced", 1)
-    assert big["ctas"] == 2 * sms and big["workspace_bytes"] > 0
+    assert (big["path"], big["schedule"], big["kernel_launches"]) == ("scaled", "balanced", 1)
+    assert big["ctas"] == sms and big["workspace_bytes"] > 0
     small = ssm.describe_scan(8, 1536, 16, 2048, dtype=BF16)
     assert (small["path"], small["schedule"]) == ("fast", "chunked") and small["nchunks"] > 1
