@@ -1,4 +1,4 @@
-// Prefill selective scan on a rescaled state: bf16 io, one thread per channel, sm_103a.
+// Prefill selective scan on a rescaled state: bf16 io, two lanes per channel, sm_103a.
 //
 // Operator ("Mamba и State Space Models", "Selective Scan (core algorithm)"; "State Space Models:
 // Mamba и альтернатива Transformer", "Mamba: Selective State Space"):
@@ -12,20 +12,24 @@
 // step there are three float32 operations (the decay ρ_t exp(Δ_t A[d,n]), the state FMA with the
 // table value ln2·B_t[n], the readout FMA) instead of four.  ρ_t folds into the decay for free: with
 // A[d,n] = (n+1)·A[d,0] the decays are ρ_t r^(n+1), r = exp(Δ_t A[d,0]), a multiply tree rooted at
-// ρ_t r.  The segment starts from g = h_init (σ_init = 1) and ends with h = σ_last·g.  |σ_t| below
-// 1e-20 (u_t = 0, or Δ_t underflowing to 0) is replaced by 1e-20, which adds at most 1e-20·ln2·|B_t|
-// to the state where the exact input term is smaller than that.
+// ρ_t r.  A segment starts from g = h_init (σ_init = 1) and ends with h = σ_last·g.  |σ_t| below 1e-20
+// (u_t = 0, or Δ_t underflowing to 0) is replaced by 1e-20, which adds at most 1e-20·ln2·|B_t| to the
+// state where the exact input term is smaller than that.
 //
 // Layout of the work:
-//  * A CTA is 128 threads and owns 128 consecutive channels of one batch row (a "group"): one
-//    channel per thread, all 16 states in registers (8 packed f32x2 pairs), one CTA per SM.
+//  * A CTA is 256 threads and owns 128 consecutive channels of one batch row (a "group"), one CTA
+//    per SM.  Two adjacent lanes share a channel: lane p holds the states n = p, p+2, .., p+14 (its
+//    k-th value is state p + 2k) as four packed f32x2 pairs, so that both lanes' decays are ρ r^(p+1)
+//    times powers of r^2 and need the same two numbers per step, r and ρ.
 //  * u, Δ_raw, z tiles [128 channels x 64 steps] and B, C tiles [dstate x 64 steps] arrive by TMA
 //    with a 128-byte swizzle through a 4-stage mbarrier pipeline.  At the start of tile k the CTA
-//    widens tile k+1's B and C into a float32 table [step][ln2·B_0..15 | C_0..15], read by every
-//    thread with broadcast 128-bit loads.
-//  * Per 8-step chunk a thread computes the chunk's per-step scalars (ℓ, ρ, σ·SiLU(z), D u·SiLU(z))
-//    one chunk ahead of the recurrence that consumes them, so that their MUFU chains overlap the
-//    previous chunk's state updates.
+//    widens tile k+1's B and C into a float32 table [step][ln2·B | C], each half with the even states
+//    first and the odd states after, read by the two lanes of a channel with 128-bit loads.
+//  * Steps are processed in chunks of 8.  Lane p owns steps 4p..4p+3 of each chunk: it computes their
+//    scalars (ℓ, r or ℓ, σ, ρ, σ·SiLU(z), D u·SiLU(z)) one chunk ahead, in phases placed between the
+//    steps of the current chunk's recurrence so that their load and MUFU chains overlap it; r and ρ
+//    reach both lanes by shuffles; each step's readout is the sum of the two lanes' halves, and the
+//    owner of the step finishes, rounds and stores it.
 //  * Scheduling: the balanced persistent schedule or the grid schedule of scan_walk.cuh, with the
 //    CTA-to-CTA carry of the balanced schedule behind a bounded wait.
 //  * Aggregate mode (chunked schedule): per (group, chunk) from a zero state, the chunk's decay
@@ -37,32 +41,18 @@
 #include "scan_walk.cuh"
 #include "ssm_device.cuh"
 
-#ifndef SSM_SCALED_SCALARS_AFTER
-#define SSM_SCALED_SCALARS_AFTER 0    // 1: the next chunk's scalars after this chunk's recurrence in program order
-#endif
-#ifndef SSM_SCALED_CHUNK
-#define SSM_SCALED_CHUNK 8            // steps per chunk: 8 or 4
-#endif
-#ifndef SSM_SCALED_LANES
-#define SSM_SCALED_LANES 2            // lanes per channel: 1 (16 states per thread) or 2 (8 states each)
-#endif
-#ifndef SSM_SCALED_PLAIN_BC_LOADS
-#define SSM_SCALED_PLAIN_BC_LOADS 0   // 1: table reads as plain C++ loads (the compiler may hoist them)
-#endif
-
 namespace ssm {
 namespace {
 
 __device__ unsigned int g_scaled_status = 0;
 
-constexpr int kCh = 128;    // channels (threads) per CTA
-constexpr int kT = 64;      // steps per tile
-constexpr int kSt = 4;      // TMA stages
-constexpr int kRow = 128;   // bytes of one tile row (64 bf16 steps)
-constexpr int kN = 16;      // register state width
-constexpr int kC = SSM_SCALED_CHUNK;   // steps per chunk
-constexpr int kLanesDefault = SSM_SCALED_LANES;
-constexpr int kCP = kC / 2;            // step pairs per chunk
+constexpr int kCh = 128;        // channels per CTA
+constexpr int kThreads = 256;   // two lanes per channel
+constexpr int kT = 64;          // steps per tile
+constexpr int kC = 8;           // steps per chunk
+constexpr int kSt = 4;          // TMA stages
+constexpr int kRow = 128;       // bytes of one tile row (64 bf16 steps)
+constexpr int kN = 16;          // state width
 constexpr float kSigmaMin = 1e-20f;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
@@ -81,14 +71,14 @@ struct MapsS {
   CUtensorMap u, dt, z, B, C;
 };
 
-// Per-step scalars of one 8-step chunk of one channel, as pairs of consecutive steps.
+// Scalars of one 8-step chunk as one lane sees them.
 struct Sc {
-  f2 l2[kCP];    // ℓ = Δ/ln2
-  f2 rho[kCP];   // σ_{t-1}/σ_t
-  f2 al[kCP];    // σ_t·SiLU(z_t)            (main mode)
-  f2 be[kCP];    // D·u_t·SiLU(z_t)          (main mode)
-  float sig;   // σ of the chunk's last step
-  float lsum;  // Σ ℓ over the chunk       (aggregate mode)
+  float q[8];      // per step: r = 2^(ℓ·A[d,0]) (A[d,n] = (n+1)·A[d,0]) or ℓ (other A)
+  float rho[8];    // per step: σ_{t-1}/σ_t
+  f2 al[2];        // own steps: σ_t·SiLU(z_t)
+  f2 be[2];        // own steps: D·u_t·SiLU(z_t)
+  float sig;       // σ of the chunk's last step (both lanes)
+  float lsum;      // Σ ℓ over the own steps (aggregate mode)
 };
 
 // Per-channel constants of a segment.
@@ -98,186 +88,50 @@ struct Chan {
   float A0;      // A[d,0]
   int b, d;
   bool valid;
-  bool structured;   // warp-uniform: every lane's row has A[d,n] = (n+1)·A[d,0]
+  bool structured;   // warp-uniform: every channel of the warp has A[d,n] = (n+1)·A[d,0]
 };
 
 __device__ __forceinline__ float pick(f2 v, int j) { return (j & 1) ? f2_hi(v) : f2_lo(v); }
 
-// Scalars of chunk c of the tile whose u row (this thread's channel) starts at `urow` in shared memory.
+// The scalars of a chunk (a lane's own steps 4p..4p+3, read from its channel's row of the stage),
+// computed in phases: load, then for each own step pair softplus and σ (a, b), the gate (gate), and
+// the exchange of r and ρ between the two lanes (exchange).
 template <int kMode>
-__device__ __forceinline__ void chunk_scalars(Sc& s, uint32_t urow, int c, int sw, float bias2, float D, float sig_prev,
-                                              bool softplus, bool has_z) {
-  // this chunk's steps inside the 16-byte (8-step) swizzled unit of the row
-  const uint32_t off = static_cast<uint32_t>((((c * kC) >> 3) ^ sw) << 4) + ((c * kC) & 7) * 2;
-  uint32_t uu[kCP], dd[kCP], zz[kCP];
-  if (kC == 8) {
-    const uint4 uw = lds128(urow + off);
-    const uint4 dw = lds128(urow + SmemS::kTileIO + off);
-    uint4 zw = make_uint4(0u, 0u, 0u, 0u);
-    if (kMode == kMain && has_z) zw = lds128(urow + 2 * SmemS::kTileIO + off);
-    const uint32_t a[4] = {uw.x, uw.y, uw.z, uw.w}, b[4] = {dw.x, dw.y, dw.z, dw.w}, e[4] = {zw.x, zw.y, zw.z, zw.w};
-#pragma unroll
-    for (int q = 0; q < kCP; ++q) { uu[q] = a[q]; dd[q] = b[q]; zz[q] = e[q]; }
-  } else {
+struct Phases {
+  uint32_t uu[2], dd[2], zz[2];
+  f2 x[2], l2v[2], u2v[2];
+  float qo[4], sg[4], rs[4];
+  float lsum = 0.0f;
+
+  __device__ __forceinline__ void load(uint32_t urow, int c, int sw, int pl, bool has_z) {
+    const uint32_t off = static_cast<uint32_t>((c ^ sw) << 4) + 8u * pl;   // own 4 steps: 8 bytes of the unit
     const uint2 uw = lds64(urow + off);
     const uint2 dw = lds64(urow + SmemS::kTileIO + off);
     uint2 zw = make_uint2(0u, 0u);
     if (kMode == kMain && has_z) zw = lds64(urow + 2 * SmemS::kTileIO + off);
-    const uint32_t a[2] = {uw.x, uw.y}, b[2] = {dw.x, dw.y}, e[2] = {zw.x, zw.y};
-#pragma unroll
-    for (int q = 0; q < kCP; ++q) { uu[q] = a[q % 2]; dd[q] = b[q % 2]; zz[q] = e[q % 2]; }
+    uu[0] = uw.x; uu[1] = uw.y; dd[0] = dw.x; dd[1] = dw.y; zz[0] = zw.x; zz[1] = zw.y;
   }
-  f2 lsum2 = f2_splat(0.0f);
-#pragma unroll
-  for (int q = 0; q < kCP; ++q) {
-    const f2 u2 = f2_make(bf16lo_to_f32(uu[q]), bf16hi_to_f32(uu[q]));
+  // (Δ_raw + bias)·log2(e), and 1 + 2^x for the softplus
+  __device__ __forceinline__ void a(int q, float bias2, bool softplus) {
+    u2v[q] = f2_make(bf16lo_to_f32(uu[q]), bf16hi_to_f32(uu[q]));
     const f2 v2 = f2_make(bf16lo_to_f32(dd[q]), bf16hi_to_f32(dd[q]));
-    const f2 x = f2_fma(v2, f2_splat(kLog2e), f2_splat(bias2));   // (Δ_raw + bias)·log2(e)
-    f2 l2 = x;
+    x[q] = f2_fma(v2, f2_splat(kLog2e), f2_splat(bias2));
+    l2v[q] = x[q];
     if (softplus) {
-      // ℓ = log2(1 + 2^x) = softplus(v)/ln2; max(., x) covers x > 64, where 2^x is clamped
-      const f2 e = f2_make(ex2_approx(fminf(f2_lo(x), 64.0f)), ex2_approx(fminf(f2_hi(x), 64.0f)));
-      const f2 w = f2_add(e, f2_splat(1.0f));
-      l2 = f2_make(fmaxf(lg2_approx(f2_lo(w)), f2_lo(x)), fmaxf(lg2_approx(f2_hi(w)), f2_hi(x)));
-    }
-    s.l2[q] = l2;
-    if (kMode == kAgg) lsum2 = f2_add(lsum2, l2);
-    const f2 sg = f2_mul(l2, u2);
-    float s0 = f2_lo(sg), s1 = f2_hi(sg);
-    s0 = fabsf(s0) < kSigmaMin ? kSigmaMin : s0;
-    s1 = fabsf(s1) < kSigmaMin ? kSigmaMin : s1;
-    s.rho[q] = f2_mul(f2_make(sig_prev, s0), f2_make(rcp_approx(s0), rcp_approx(s1)));
-    sig_prev = s1;
-    if (kMode == kMain) {
-      f2 g = f2_splat(1.0f);
-      if (has_z) {
-        const f2 z2 = f2_make(bf16lo_to_f32(zz[q]), bf16hi_to_f32(zz[q]));
-        const f2 t = f2_mul(z2, f2_splat(-kLog2e));
-        const f2 den = f2_add(f2_make(ex2_approx(f2_lo(t)), ex2_approx(f2_hi(t))), f2_splat(1.0f));
-        g = f2_mul(z2, f2_make(rcp_approx(f2_lo(den)), rcp_approx(f2_hi(den))));
-      }
-      s.al[q] = f2_mul(f2_make(s0, s1), g);
-      s.be[q] = f2_mul(f2_mul(f2_splat(D), u2), g);
+      const f2 e = f2_make(ex2_approx(fminf(f2_lo(x[q]), 64.0f)), ex2_approx(fminf(f2_hi(x[q]), 64.0f)));
+      l2v[q] = f2_add(e, f2_splat(1.0f));
     }
   }
-  s.sig = sig_prev;
-  if (kMode == kAgg) s.lsum = f2_lo(lsum2) + f2_hi(lsum2);
-}
-
-__device__ __forceinline__ float4 tab_load(uint32_t addr) {
-#if SSM_SCALED_PLAIN_BC_LOADS
-  float4 v;
-  asm("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
-  return v;
-#else
-  return lds128f(addr);
-#endif
-}
-
-// The recurrence over one 8-step chunk: g ← ρ exp(ΔA) ⊙ g + ln2·B, then (main mode) the readout
-// y = σ·SiLU(z)·(C·g) + D·u·SiLU(z) for each step, returned packed as eight bf16 values.
-template <int kMode, bool kS>
-__device__ __forceinline__ uint4 chunk_run(f2 (&h)[8], const Sc& s, uint32_t tab, const Chan& k, const float* Arow,
-                                           int N) {
-  float Ag[kN];
-  if (!kS) {
-#pragma unroll
-    for (int n = 0; n < kN; ++n) Ag[n] = n < N ? __ldg(Arow + n) : 0.0f;
-  }
-  float y[kC];
-#pragma unroll
-  for (int j = 0; j < kC; ++j) {
-    const float l2 = pick(s.l2[j >> 1], j);
-    const float rho = pick(s.rho[j >> 1], j);
-    const uint32_t row = tab + j * 128;
-    f2 P[8];
-    if (kS) {
-      // ρ r^(n+1), n = 0..15, r = exp(Δ A[d,0]) = 2^(ℓ A[d,0])
-      const float r = ex2_approx(l2 * k.A0);
-      const float r2 = r * r, r4 = r2 * r2, r8 = r4 * r4;
-      const float c0 = rho * r;
-      P[0] = f2_make(c0, c0 * r);
-      P[1] = f2_mul(P[0], f2_splat(r2));
-      P[2] = f2_mul(P[0], f2_splat(r4));
-      P[3] = f2_mul(P[1], f2_splat(r4));
-#pragma unroll
-      for (int i = 0; i < 4; ++i) P[4 + i] = f2_mul(P[i], f2_splat(r8));
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        P[i] = f2_make(rho * ex2_approx(l2 * Ag[2 * i]), rho * ex2_approx(l2 * Ag[2 * i + 1]));
-    }
-    const float4 b0 = tab_load(row), b1 = tab_load(row + 16), b2 = tab_load(row + 32), b3 = tab_load(row + 48);
-    h[0] = f2_fma(P[0], h[0], f2_make(b0.x, b0.y));
-    h[1] = f2_fma(P[1], h[1], f2_make(b0.z, b0.w));
-    h[2] = f2_fma(P[2], h[2], f2_make(b1.x, b1.y));
-    h[3] = f2_fma(P[3], h[3], f2_make(b1.z, b1.w));
-    h[4] = f2_fma(P[4], h[4], f2_make(b2.x, b2.y));
-    h[5] = f2_fma(P[5], h[5], f2_make(b2.z, b2.w));
-    h[6] = f2_fma(P[6], h[6], f2_make(b3.x, b3.y));
-    h[7] = f2_fma(P[7], h[7], f2_make(b3.z, b3.w));
-    if (kMode == kMain) {
-      const float4 c0v = tab_load(row + 64), c1v = tab_load(row + 80), c2v = tab_load(row + 96),
-                   c3v = tab_load(row + 112);
-      f2 a0 = f2_mul(f2_make(c0v.x, c0v.y), h[0]);
-      f2 a1 = f2_mul(f2_make(c0v.z, c0v.w), h[1]);
-      a0 = f2_fma(f2_make(c1v.x, c1v.y), h[2], a0);
-      a1 = f2_fma(f2_make(c1v.z, c1v.w), h[3], a1);
-      a0 = f2_fma(f2_make(c2v.x, c2v.y), h[4], a0);
-      a1 = f2_fma(f2_make(c2v.z, c2v.w), h[5], a1);
-      a0 = f2_fma(f2_make(c3v.x, c3v.y), h[6], a0);
-      a1 = f2_fma(f2_make(c3v.z, c3v.w), h[7], a1);
-      const f2 sum = f2_add(a0, a1);
-      y[j] = fmaf(pick(s.al[j >> 1], j), f2_lo(sum) + f2_hi(sum), pick(s.be[j >> 1], j));
-    }
-  }
-  if (kMode != kMain) return make_uint4(0u, 0u, 0u, 0u);
-  if (kC == 8)
-    return make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5 % kC]),
-                      pack_bf16x2(y[6 % kC], y[7 % kC]));
-  return make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), 0u, 0u);
-}
-
-// ---------------------------------------------------------------- two lanes per channel
-// Lane p of a channel holds states [8p, 8p+8) and owns steps [4p, 4p+4) of every 8-step chunk: it
-// computes those steps' scalars and finishes their outputs.  Each step's decay exponent and ρ reach
-// both lanes by shuffles; each step's readout is the sum of the two lanes' halves.
-struct Sc2 {
-  float q[8];      // per step: ℓ·A[d,0] (structured A) or ℓ (general A)
-  float rho[8];    // per step: σ_{t-1}/σ_t
-  f2 al[2];        // own steps: σ_t·SiLU(z_t)
-  f2 be[2];        // own steps: D·u_t·SiLU(z_t)
-  float sig;       // σ of the chunk's last step (both lanes)
-  float lsum;      // Σ ℓ over the own steps (aggregate mode)
-};
-
-template <int kMode>
-__device__ __forceinline__ void chunk_scalars2(Sc2& s, uint32_t urow, int c, int sw, int pl, float bias2, float D,
-                                               float qmul, float sig_prev, bool softplus, bool has_z) {
-  const uint32_t off = static_cast<uint32_t>((c ^ sw) << 4) + 8u * pl;   // own 4 steps: 8 bytes of the unit
-  const uint2 uw = lds64(urow + off);
-  const uint2 dw = lds64(urow + SmemS::kTileIO + off);
-  uint2 zw = make_uint2(0u, 0u);
-  if (kMode == kMain && has_z) zw = lds64(urow + 2 * SmemS::kTileIO + off);
-  const uint32_t uu[2] = {uw.x, uw.y}, dd[2] = {dw.x, dw.y}, zz[2] = {zw.x, zw.y};
-  float qo[4], sg[4], rs[4];
-  float lsum = 0.0f;
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const f2 u2 = f2_make(bf16lo_to_f32(uu[q]), bf16hi_to_f32(uu[q]));
-    const f2 v2 = f2_make(bf16lo_to_f32(dd[q]), bf16hi_to_f32(dd[q]));
-    const f2 x = f2_fma(v2, f2_splat(kLog2e), f2_splat(bias2));
-    f2 l2 = x;
-    if (softplus) {
-      const f2 e = f2_make(ex2_approx(fminf(f2_lo(x), 64.0f)), ex2_approx(fminf(f2_hi(x), 64.0f)));
-      const f2 w = f2_add(e, f2_splat(1.0f));
-      l2 = f2_make(fmaxf(lg2_approx(f2_lo(w)), f2_lo(x)), fmaxf(lg2_approx(f2_hi(w)), f2_hi(x)));
-    }
+  // ℓ = log2(1 + 2^x) = softplus(v)/ln2 (max(., x) covers x > 64, where 2^x is clamped), r, σ, 1/σ
+  __device__ __forceinline__ void b(int q, float A0, bool structured, bool softplus) {
+    f2 l2 = l2v[q];
+    if (softplus)
+      l2 = f2_make(fmaxf(lg2_approx(f2_lo(l2)), f2_lo(x[q])), fmaxf(lg2_approx(f2_hi(l2)), f2_hi(x[q])));
     if (kMode == kAgg) lsum += f2_lo(l2) + f2_hi(l2);
-    const f2 qq = f2_mul(l2, f2_splat(qmul));
-    qo[2 * q] = f2_lo(qq);
-    qo[2 * q + 1] = f2_hi(qq);
-    const f2 sgm = f2_mul(l2, u2);
+    const f2 qq = f2_mul(l2, f2_splat(A0));
+    qo[2 * q] = structured ? ex2_approx(f2_lo(qq)) : f2_lo(l2);
+    qo[2 * q + 1] = structured ? ex2_approx(f2_hi(qq)) : f2_hi(l2);
+    const f2 sgm = f2_mul(l2, u2v[q]);
     float s0 = f2_lo(sgm), s1 = f2_hi(sgm);
     s0 = fabsf(s0) < kSigmaMin ? kSigmaMin : s0;
     s1 = fabsf(s1) < kSigmaMin ? kSigmaMin : s1;
@@ -285,47 +139,54 @@ __device__ __forceinline__ void chunk_scalars2(Sc2& s, uint32_t urow, int c, int
     sg[2 * q + 1] = s1;
     rs[2 * q] = rcp_approx(s0);
     rs[2 * q + 1] = rcp_approx(s1);
-    if (kMode == kMain) {
-      f2 g = f2_splat(1.0f);
-      if (has_z) {
-        const f2 z2 = f2_make(bf16lo_to_f32(zz[q]), bf16hi_to_f32(zz[q]));
-        const f2 t = f2_mul(z2, f2_splat(-kLog2e));
-        const f2 den = f2_add(f2_make(ex2_approx(f2_lo(t)), ex2_approx(f2_hi(t))), f2_splat(1.0f));
-        g = f2_mul(z2, f2_make(rcp_approx(f2_lo(den)), rcp_approx(f2_hi(den))));
-      }
-      s.al[q] = f2_mul(f2_make(s0, s1), g);
-      s.be[q] = f2_mul(f2_mul(f2_splat(D), u2), g);
+  }
+  // σ·SiLU(z) and D·u·SiLU(z)
+  __device__ __forceinline__ void gate(int q, Sc& ns, float D, bool has_z) {
+    if (kMode != kMain) return;
+    f2 g = f2_splat(1.0f);
+    if (has_z) {
+      const f2 z2 = f2_make(bf16lo_to_f32(zz[q]), bf16hi_to_f32(zz[q]));
+      const f2 t = f2_mul(z2, f2_splat(-kLog2e));
+      const f2 den = f2_add(f2_make(ex2_approx(f2_lo(t)), ex2_approx(f2_hi(t))), f2_splat(1.0f));
+      g = f2_mul(z2, f2_make(rcp_approx(f2_lo(den)), rcp_approx(f2_hi(den))));
     }
+    ns.al[q] = f2_mul(f2_make(sg[2 * q], sg[2 * q + 1]), g);
+    ns.be[q] = f2_mul(f2_mul(f2_splat(D), u2v[q]), g);
   }
-  // σ before the first own step: lane 1 takes step 3 from lane 0; lane 0 takes the previous chunk's
-  // step 7 (sig_prev), which lane 1 handed over at the end of that chunk
-  const float s3x = __shfl_xor_sync(0xffffffffu, sg[3], 1);
-  const float first_prev = pl ? s3x : sig_prev;
-  float ro[4];
-  ro[0] = first_prev * rs[0];
-  ro[1] = sg[0] * rs[1];
-  ro[2] = sg[1] * rs[2];
-  ro[3] = sg[2] * rs[3];
-  s.sig = pl ? sg[3] : s3x;
-  const int base = (threadIdx.x & 31) & ~1;
+  // ρ of the own steps and the exchange: σ before the first own step is, for lane 1, step 3 from
+  // lane 0 and, for lane 0, the previous chunk's step 7 (sig_prev); then r and ρ of every step reach
+  // both lanes from the step's owner
+  __device__ __forceinline__ void exchange(Sc& ns, int pl, float sig_prev) {
+    const float s3x = __shfl_xor_sync(0xffffffffu, sg[3], 1);
+    const float first_prev = pl ? s3x : sig_prev;
+    float ro[4];
+    ro[0] = first_prev * rs[0];
+    ro[1] = sg[0] * rs[1];
+    ro[2] = sg[1] * rs[2];
+    ro[3] = sg[2] * rs[3];
+    ns.sig = pl ? sg[3] : s3x;
+    const int base = (threadIdx.x & 31) & ~1;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    s.q[j] = __shfl_sync(0xffffffffu, qo[j & 3], base | (j >> 2));
-    s.rho[j] = __shfl_sync(0xffffffffu, ro[j & 3], base | (j >> 2));
+    for (int j = 0; j < 8; ++j) {
+      ns.q[j] = __shfl_sync(0xffffffffu, qo[j & 3], base | (j >> 2));
+      ns.rho[j] = __shfl_sync(0xffffffffu, ro[j & 3], base | (j >> 2));
+    }
+    ns.lsum = lsum;
   }
-  s.lsum = lsum;
-}
+};
 
-// The recurrence of one lane's 8 states over one 8-step chunk; returns the lane's four own outputs
-// packed as bf16 (main mode).
+// One 8-step chunk of one lane: the recurrence of the current chunk (scalars in s) with the next
+// chunk's scalars computed into ns in phases placed between the steps, so that their load and MUFU
+// chains overlap the state updates (0.381 ms against 0.403 ms with the scalars computed as one block
+// on the 2.8B layer).  urow, c, sig_prev and the channel constants describe the next chunk.  Returns
+// the lane's four own outputs packed as bf16 (main mode).
 template <int kMode, bool kS>
-__device__ __forceinline__ uint2 chunk_run2(f2 (&h)[4], const Sc2& s, uint32_t tab, int pl, float kb,
-                                            const float* Arow, int N) {
-  float Ah[8];
-  if (!kS) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) Ah[i] = 8 * pl + i < N ? __ldg(Arow + 8 * pl + i) : 0.0f;
-  }
+__device__ __forceinline__ uint2 chunk_step(f2 (&h)[4], const Sc& s, Sc& ns, uint32_t tab, int pl,
+                                            const float (&Ah)[8], uint32_t urow, int c, int sw, float bias2,
+                                            float D, float A0, bool structured, float sig_prev, bool softplus,
+                                            bool has_z) {
+  Phases<kMode> ph;
+  ph.load(urow, c, sw, pl, has_z);
   float part[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -334,25 +195,25 @@ __device__ __forceinline__ uint2 chunk_run2(f2 (&h)[4], const Sc2& s, uint32_t t
     const uint32_t row = tab + j * 128 + pl * 32;
     f2 a[4];
     if (kS) {
-      // ρ r^(8p+1) .. ρ r^(8p+8), r = 2^q
-      const float r = ex2_approx(q);
-      const float c0 = rho * ex2_approx(q * kb);
-      const float r2 = r * r, r4 = r2 * r2;
-      a[0] = f2_make(c0, c0 * r);
-      a[1] = f2_mul(a[0], f2_splat(r2));
-      a[2] = f2_mul(a[0], f2_splat(r4));
-      a[3] = f2_mul(a[1], f2_splat(r4));
+      // ρ r^(p+1+2k), k = 0..7
+      const float r = q;
+      const float r2 = r * r, r4 = r2 * r2, r8 = r4 * r4;
+      const float c0 = rho * (pl ? r2 : r);
+      a[0] = f2_make(c0, c0 * r2);
+      a[1] = f2_mul(a[0], f2_splat(r4));
+      a[2] = f2_mul(a[0], f2_splat(r8));
+      a[3] = f2_mul(a[1], f2_splat(r8));
     } else {
 #pragma unroll
       for (int i = 0; i < 4; ++i) a[i] = f2_make(rho * ex2_approx(q * Ah[2 * i]), rho * ex2_approx(q * Ah[2 * i + 1]));
     }
-    const float4 b0 = tab_load(row), b1 = tab_load(row + 16);
+    const float4 b0 = lds128f(row), b1 = lds128f(row + 16);
     h[0] = f2_fma(a[0], h[0], f2_make(b0.x, b0.y));
     h[1] = f2_fma(a[1], h[1], f2_make(b0.z, b0.w));
     h[2] = f2_fma(a[2], h[2], f2_make(b1.x, b1.y));
     h[3] = f2_fma(a[3], h[3], f2_make(b1.z, b1.w));
     if (kMode == kMain) {
-      const float4 c0v = tab_load(row + 64), c1v = tab_load(row + 80);
+      const float4 c0v = lds128f(row + 64), c1v = lds128f(row + 80);
       f2 a0 = f2_mul(f2_make(c0v.x, c0v.y), h[0]);
       f2 a1 = f2_mul(f2_make(c0v.z, c0v.w), h[1]);
       a0 = f2_fma(f2_make(c1v.x, c1v.y), h[2], a0);
@@ -360,29 +221,46 @@ __device__ __forceinline__ uint2 chunk_run2(f2 (&h)[4], const Sc2& s, uint32_t t
       const f2 sum = f2_add(a0, a1);
       part[j] = f2_lo(sum) + f2_hi(sum);
     }
+    // a phase of the next chunk's scalars
+    if (j == 0 || j == 2) ph.a(j >> 1, bias2, softplus);
+    if (j == 1 || j == 3) ph.b(j >> 1, A0, structured, softplus);
+    if (j == 4 || j == 5) ph.gate(j - 4, ns, D, has_z);
+    if (j == 6) ph.exchange(ns, pl, sig_prev);
   }
   if constexpr (kMode != kMain) {
     return make_uint2(0u, 0u);
-  }
-  // each lane finishes its own four steps: its half plus the partner's half
-  float y[4];
+  } else {
+    // lane p finishes steps 4p..4p+3: its half plus the partner's half
+    float y[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float send = pl ? part[i] : part[4 + i];
-    const float mine = pl ? part[4 + i] : part[i];
-    const float tot = mine + __shfl_xor_sync(0xffffffffu, send, 1);
-    y[i] = fmaf(pick(s.al[i >> 1], i), tot, pick(s.be[i >> 1], i));
+    for (int i = 0; i < 4; ++i) {
+      const float send = pl ? part[i] : part[4 + i];
+      const float mine = pl ? part[4 + i] : part[i];
+      const float tot = mine + __shfl_xor_sync(0xffffffffu, send, 1);
+      y[i] = fmaf(pick(s.al[i >> 1], i), tot, pick(s.be[i >> 1], i));
+    }
+    return make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
   }
-  return make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
 }
 
-template <int kMode, int kLanes>
-__global__ void __launch_bounds__(kCh * kLanes, 1) scan_scaled_kernel(const __grid_constant__ MapsS tm,
-                                                                        const ScanParams p) {
-  constexpr int kThr = kCh * kLanes;
-  constexpr int kNs = kN / kLanes;     // states per lane
-  static_assert(kLanes == 1 || (kLanes == 2 && kC == 8), "two lanes per channel need 8-step chunks");
-  using ScT = typename std::conditional<kLanes == 1, Sc, Sc2>::type;
+// The scalars of a chunk on their own (the first chunk of a CTA's walk).
+template <int kMode>
+__device__ __forceinline__ void chunk_scalars(Sc& ns, uint32_t urow, int c, int sw, int pl, float bias2, float D,
+                                              float A0, bool structured, float sig_prev, bool softplus, bool has_z) {
+  Phases<kMode> ph;
+  ph.load(urow, c, sw, pl, has_z);
+  ph.a(0, bias2, softplus);
+  ph.a(1, bias2, softplus);
+  ph.b(0, A0, structured, softplus);
+  ph.b(1, A0, structured, softplus);
+  ph.gate(0, ns, D, has_z);
+  ph.gate(1, ns, D, has_z);
+  ph.exchange(ns, pl, sig_prev);
+}
+
+template <int kMode>
+__global__ void __launch_bounds__(kThreads, 1) scan_scaled_kernel(const __grid_constant__ MapsS tm, const ScanParams p) {
+  constexpr int kNs = kN / 2;     // states per lane
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // table of tile k: tab_at(k)
@@ -391,9 +269,10 @@ __global__ void __launch_bounds__(kCh * kLanes, 1) scan_scaled_kernel(const __gr
   __shared__ int s_carry_ok;
 
   const int tid = threadIdx.x;
-  const int ch = tid / kLanes;                     // channel within the group
-  const int pl = tid % kLanes;                     // lane within the channel
-  const int n0 = pl * kNs;                         // this lane's first state
+  const int ch = tid >> 1;                         // channel within the group
+  const int pl = tid & 1;                          // lane within the channel
+  auto sidx = [&](int k) { return pl + 2 * k; };   // this lane's k-th state
+  const int n0 = pl * kNs;                         // this lane's slot in a CTA-to-CTA carry row
   const int sw = ch & 7;                           // 128-byte swizzle of this channel's tile row
   const int64_t Lt = (p.L + kT - 1) / kT;
   const int gpb = (p.dim + kCh - 1) / kCh;         // groups per batch row
@@ -449,28 +328,28 @@ __global__ void __launch_bounds__(kCh * kLanes, 1) scan_scaled_kernel(const __gr
   }
 
   // Widens tile k's B and C (stage k % kSt) into table k & 1: ln2·B in columns 0..15, C in 16..31,
-  // zero rows for n >= dstate.  256 jobs (array, n, 8-step chunk) over the CTA; a warp's 32 threads
-  // store 32 consecutive words.
+  // zero rows for n >= dstate.  256 jobs (array, n, 8-step chunk), one per thread; a warp's 32
+  // threads store 32 consecutive words.
   auto widen = [&](int64_t k) {
     const uint32_t src = smem_u32(smem + (k % kSt) * SmemS::kStage + 3 * SmemS::kTileIO);
     float* tab = tab_at(k);
-#pragma unroll
-    for (int rep = 0; rep < 256 / kThr; ++rep) {
-      const int job = tid + rep * kThr;
+    {
+      const int job = tid;
       const int arr = (job >> 4) & 1;
       const int n = job & 15;
       const int c = job >> 5;
-      if (arr == 1 && kMode != kMain) continue;
       float vals[8];
-      if (n < p.N) {
+      if (n < p.N && (arr == 0 || kMode == kMain)) {
         unpack_chunk(lds128(src + arr * SmemS::kTileBC + n * kRow + ((c ^ (n & 7)) << 4)), vals, __nv_bfloat16());
       } else {
 #pragma unroll
         for (int j = 0; j < 8; ++j) vals[j] = 0.0f;
       }
       const float scale = arr == 0 ? kLn2 : 1.0f;
+      // even states in columns 0..7 of each half, odd states in 8..15 (one block per lane)
+      const int col = (n & 1) * 8 + (n >> 1);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) tab[(c * 8 + j) * 32 + arr * 16 + n] = vals[j] * scale;
+      for (int j = 0; j < 8; ++j) tab[(c * 8 + j) * 32 + arr * 16 + col] = vals[j] * scale;
     }
   };
 
@@ -489,16 +368,6 @@ __global__ void __launch_bounds__(kCh * kLanes, 1) scan_scaled_kernel(const __gr
     cc.D = p.D ? p.D[cc.d] : 0.0f;
     cc.bias2 = (p.bias ? p.bias[cc.d] : 0.0f) * kLog2e;
   };
-  // scalars of chunk c of the tile in the stage whose row starts at urow; sig_prev = σ before it
-  auto scalars = [&](ScT& sc, uint32_t urow, int c, const Chan& cc, float sig_prev) {
-    if constexpr (kLanes == 1) {
-      chunk_scalars<kMode>(sc, urow, c, sw, cc.bias2, cc.D, sig_prev, softplus, has_z);
-    } else {
-      chunk_scalars2<kMode>(sc, urow, c, sw, pl, cc.bias2, cc.D, cc.structured ? cc.A0 : 1.0f, sig_prev, softplus,
-                            has_z);
-    }
-  };
-
   // prologue: tile 0's table and channel constants, the first chunk's scalars
   bool ok = mbar_wait_bounded(&full[0], 0u, &g_scaled_status);
   if (ok) widen(0);
@@ -507,9 +376,9 @@ __global__ void __launch_bounds__(kCh * kLanes, 1) scan_scaled_kernel(const __gr
   w.at(0, gk, tk);
   Chan cur, nxt;
   tile_chan(gk, cur);
-  ScT sc_a, sc_b;   // scalar buffers: sc_a holds the scalars of the next chunk to run
-  const uint32_t stage0 = smem_u32(smem);
-  scalars(sc_a, stage0 + ch * kRow, 0, cur, 1.0f);
+  Sc sc_a, sc_b;   // scalar buffers: sc_a holds the scalars of the next chunk to run
+  chunk_scalars<kMode>(sc_a, smem_u32(smem) + ch * kRow, 0, sw, pl, cur.bias2, cur.D, cur.A0, cur.structured, 1.0f,
+                       softplus, has_z);
 
   f2 h[kNs / 2];   // this lane's rescaled states
 #pragma unroll
@@ -575,11 +444,11 @@ __global__ void __launch_bounds__(kCh * kLanes, 1) scan_scaled_kernel(const __gr
         const float* src = static_cast<const float*>(p.h_in) + chunk_idx * p.h_in_chunk_stride + soff;
 #pragma unroll
         for (int i = 0; i < kNs; ++i)
-          if (n0 + i < p.N) init[i] = src[n0 + i];
+          if (sidx(i) < p.N) init[i] = src[sidx(i)];
       } else if (p.h0 != nullptr && t == 0) {
 #pragma unroll
         for (int i = 0; i < kNs; ++i)
-          if (n0 + i < p.N) init[i] = p.h0[soff + n0 + i];
+          if (sidx(i) < p.N) init[i] = p.h0[soff + sidx(i)];
       }
 #pragma unroll
       for (int i = 0; i < kNs / 2; ++i) h[i] = f2_make(init[2 * i], init[2 * i + 1]);
@@ -594,37 +463,26 @@ __global__ void __launch_bounds__(kCh * kLanes, 1) scan_scaled_kernel(const __gr
     __nv_bfloat16* yrow = nullptr;
     if (kMode == kMain && cur.valid)
       yrow = static_cast<__nv_bfloat16*>(p.y) + (static_cast<int64_t>(cur.b) * p.dim + cur.d) * p.L + t0;
-    const float* Arow = p.A + static_cast<int64_t>(cur.d) * p.N;
-    const float kb = static_cast<float>(8 * pl + 1);
+    float Ah[8];   // this lane's row of A (A not of the form (n+1)·A[d,0])
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      Ah[i] = (!cur.structured && sidx(i) < p.N) ? p.A[static_cast<int64_t>(cur.d) * p.N + sidx(i)] : 0.0f;
     float sig_end = 1.0f;
     // Chunks in pairs with two scalar buffers (the tile's chunk count is even): chunk c runs on the
     // buffer filled during chunk c - 1, and the other buffer takes chunk c + 1 (or the next tile's
     // first chunk), so no scalar set is copied.
     auto chunks = [&](auto tag) {
       constexpr bool kS = decltype(tag)::value;
-      auto one = [&](ScT& run_sc, ScT& fill_sc, int c) {
+      auto one = [&](Sc& run_sc, Sc& fill_sc, int c) {
         // the next chunk's scalars: chunk c + 1 of this tile or chunk 0 of the next tile, chosen by
         // selects so that they share one basic block with this chunk's recurrence (past the last
         // tile they are computed from a stale stage and never used)
         const bool in_tile = c + 1 < nch;
-#if !SSM_SCALED_SCALARS_AFTER
-        scalars(fill_sc, in_tile ? urow : urow_next, in_tile ? c + 1 : 0, in_tile ? cur : nxt,
-                (in_tile || !next_new) ? run_sc.sig : 1.0f);
-#endif
-        if constexpr (kLanes == 1) {
-          const uint4 yv = chunk_run<kMode, kS>(h, run_sc, tab + c * kC * 128, cur, Arow, p.N);
-          if (kMode == kMain && yrow) {
-            if (kC == 8) *reinterpret_cast<uint4*>(yrow + c * kC) = yv;
-            else *reinterpret_cast<uint2*>(yrow + c * kC) = make_uint2(yv.x, yv.y);
-          }
-        } else {
-          const uint2 yv = chunk_run2<kMode, kS>(h, run_sc, tab + c * kC * 128, pl, kb, Arow, p.N);
-          if (kMode == kMain && yrow) *reinterpret_cast<uint2*>(yrow + c * kC + 4 * pl) = yv;
-        }
-#if SSM_SCALED_SCALARS_AFTER
-        scalars(fill_sc, in_tile ? urow : urow_next, in_tile ? c + 1 : 0, in_tile ? cur : nxt,
-                (in_tile || !next_new) ? run_sc.sig : 1.0f);
-#endif
+        const Chan& cc = in_tile ? cur : nxt;
+        const uint2 yv = chunk_step<kMode, kS>(h, run_sc, fill_sc, tab + c * kC * 128, pl, Ah, in_tile ? urow : urow_next,
+                                               in_tile ? c + 1 : 0, sw, cc.bias2, cc.D, cc.A0, cc.structured,
+                                               (in_tile || !next_new) ? run_sc.sig : 1.0f, softplus, has_z);
+        if (kMode == kMain && yrow) *reinterpret_cast<uint2*>(yrow + c * kC + 4 * pl) = yv;
         if (kMode == kAgg) lsum += run_sc.lsum;
         sig_end = run_sc.sig;
       };
@@ -660,21 +518,21 @@ __global__ void __launch_bounds__(kCh * kLanes, 1) scan_scaled_kernel(const __gr
       } else if (kMode == kMain && t == Lt - 1 && cur.valid && p.last_state) {
 #pragma unroll
         for (int i = 0; i < kNs; ++i)
-          if (n0 + i < p.N) p.last_state[soff + n0 + i] = hv[i];
+          if (sidx(i) < p.N) p.last_state[soff + sidx(i)] = hv[i];
       }
       if (kMode == kAgg && !p.sched_balanced) {
         // aggregate of this chunk: P = exp(A ΣΔ) = 2^(A Σℓ), Q = h_end from a zero state
         float ls = lsum;
-        if (kLanes == 2) ls += __shfl_xor_sync(0xffffffffu, ls, 1);
+        ls += __shfl_xor_sync(0xffffffffu, ls, 1);
         if (cur.valid) {
           const int64_t cbase = chunk_idx * p.h_in_chunk_stride + soff;
           float* Pa = static_cast<float*>(p.agg_P);
           float* Qa = static_cast<float*>(p.agg_Q);
 #pragma unroll
           for (int i = 0; i < kNs; ++i) {
-            if (n0 + i < p.N) {
-              Pa[cbase + n0 + i] = ex2_approx(p.A[static_cast<int64_t>(cur.d) * p.N + n0 + i] * ls);
-              Qa[cbase + n0 + i] = hv[i];
+            if (sidx(i) < p.N) {
+              Pa[cbase + sidx(i)] = ex2_approx(p.A[static_cast<int64_t>(cur.d) * p.N + sidx(i)] * ls);
+              Qa[cbase + sidx(i)] = hv[i];
             }
           }
         }
@@ -703,12 +561,12 @@ int scaled_resident_ctas() {
   if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return 0; }
   if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) { cudaGetLastError(); return 0; }
-  auto kern = scan_scaled_kernel<kMain, kLanesDefault>;
+  auto kern = scan_scaled_kernel<kMain>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemS::kTotal) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kCh * kLanesDefault, SmemS::kTotal) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, SmemS::kTotal) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -746,9 +604,8 @@ cudaError_t scan_scaled_launch(const ScanParams& p, int nchunks, int balanced_ct
   }
   const int gpb = (p.dim + kCh - 1) / kCh;
   const unsigned groups = static_cast<unsigned>(p.batch) * gpb;
-  auto kmain = scan_scaled_kernel<kMain, kLanesDefault>;
-  auto kagg = scan_scaled_kernel<kAgg, kLanesDefault>;
-  constexpr int kThreads = kCh * kLanesDefault;
+  auto kmain = scan_scaled_kernel<kMain>;
+  auto kagg = scan_scaled_kernel<kAgg>;
   cudaError_t e;
   e = cudaFuncSetAttribute(kmain, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemS::kTotal);
   if (e != cudaSuccess) return e;
