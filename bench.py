@@ -60,6 +60,28 @@ def _bf16_peak():
         return 1800.0, "fallback"
 
 
+# FP32 lane-operations per clock per SM (4 sub-partitions x 32 lanes; packed f32x2 instructions do not
+# raise it) and the SM count: the peak of the FP32 pipe at the sampled SM clock.
+FP32_LANE_OPS_PER_CLK_SM = 128
+# Minimum float32 lane-operations per state-step of the rescaled recurrence: the decay factor, the
+# state FMA and the readout FMA.
+FP32_OPS_PER_STATE_STEP = 3
+
+
+def _fp32_peak(clocks, dev_index=0):
+    """Peak FP32 lane-ops/s at the median SM clock sampled under load (max clock if none)."""
+    import torch
+    sms = torch.cuda.get_device_properties(dev_index).multi_processor_count
+    mhz = None
+    try:
+        mhz = float(clocks.get("sm_mhz")) if clocks else None
+    except Exception:
+        mhz = None
+    if not mhz:
+        mhz = 2032.0
+    return sms * FP32_LANE_OPS_PER_CLK_SM * mhz * 1e6, sms, mhz
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -560,6 +582,41 @@ def _max_over_ranks(x: float) -> float:
 
 # ----------------------------------------------------------------------------- main
 
+def _config(w, n_gpus):
+    """The workload as both arms name it (no kernel or plan details)."""
+    return {"workload": w.name, "batch": w.batch, "d_inner": w.dim, "d_state": w.dstate, "seq_len": w.seqlen,
+            "io": w.io_dtype, "l2": "inputs larger than L2 (%.0f MB per step vs 126 MB)" % (w.algorithmic_bytes() / 1e6),
+            "parallelism": f"replicas x{n_gpus}"}
+
+
+def measure_scan_kernel(w, dev, rank, reps=10):
+    """Another prefill workload: the scan's device time alone (mean of back-to-back calls)."""
+    import torch
+    from selective_state_space_139_b300 import ssm
+    from selective_state_space_139_b300 import workloads as W
+
+    inp = W.make_scan_inputs(w, device=dev, seed=w.seed + rank)
+    y = torch.empty_like(inp["u"])
+    hL = torch.empty((w.batch, w.dim, w.dstate), device=dev, dtype=torch.float32)
+    plan = ssm.describe_scan(w.batch, w.dim, w.dstate, w.seqlen, inp["u"].dtype)
+    ws = torch.empty(max(plan["workspace_bytes"], 1), dtype=torch.uint8, device=dev)
+
+    def call():
+        ssm.selective_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], D=inp["D"], z=inp["z"],
+                               delta_bias=inp["delta_bias"], out=y, last_state=hL, workspace=ws)
+
+    ms = _time_back_to_back(call, reps, dev)
+    assert ssm.device_status() == ssm.SSM_OK
+    bytes_alg = w.algorithmic_bytes()
+    out = {"workload": w.name, "shape": f"batch {w.batch}, d_inner {w.dim}, d_state {w.dstate}, L {w.seqlen}",
+           "ms": ms, "tokens_per_s": w.tokens / (ms * 1e-3), "achieved_gbs": bytes_alg / (ms * 1e-3) / 1e9,
+           "bytes_per_call": bytes_alg, "plan": f"{plan['path']}/{plan['schedule']}, {plan['nchunks']} chunk(s), "
+                                                f"{plan['kernel_launches']} launch(es)"}
+    del inp, y, hL, ws
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_reference(args, ws, rank):
     from selective_state_space_139_b300 import workloads as W
     if rank != 0:
@@ -579,8 +636,7 @@ def run_reference(args, ws, rank):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "batch": w.batch, "d_inner": w.dim, "d_state": w.dstate,
-                       "seq_len": w.seqlen, "io": w.io_dtype},
+            "config": _config(w, args.gpus),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": what},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -624,6 +680,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-ssd", action="store_true")
+    ap.add_argument("--no-other-scans", action="store_true", help="skip the 130M-layer and long-sequence scans")
     ap.add_argument("--only", default="all", choices=["all", "scan", "decode", "conv1d", "backward", "ssd", "ssd_decode"],
                     help="measure one part alone (for profiler captures)")
     ap.add_argument("--no-soak", action="store_true", help="skip the 1 s clock soak before the scan warm-up")
@@ -660,22 +717,34 @@ def main():
     bwd = None if args.no_backward else measure_bwd(w, dev, rank)
     ssd = None if args.no_ssd else measure_ssd(dev, rank)
     ssd_dec = None if args.no_ssd else measure_ssd_decode(dev, rank)
+    others = []
+    if not args.no_other_scans:
+        for name in ("mamba130m-layer", "long-dna"):
+            if name != w.name:
+                others.append(measure_scan_kernel(W.WORKLOADS[name], dev, rank, reps=10 if name != "long-dna" else 5))
     if rank != 0:
         return 0
     tokens_all = w.tokens * ws
     value = tokens_all / (r["ms_per_step"] * 1e-3)
+    fp32_ops = FP32_OPS_PER_STATE_STEP * w.batch * w.dim * w.dstate * w.seqlen
+    fp32_peak, fp32_sms, fp32_mhz = _fp32_peak(r["clocks"], dev.index or 0)
     traffic = _ncu_traffic("scan_fwd", w.name)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": r["ms_per_step"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32 (bf16 io)", "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch, "d_inner": w.dim, "d_state": w.dstate, "seq_len": w.seqlen,
-                   "io": w.io_dtype, "kernel": r["algorithm"], "ctas": r["ctas"],
-                   "l2": "inputs larger than L2 (%.0f MB per step vs 126 MB)" % (r["bytes_alg"] / 1e6),
-                   "parallelism": f"replicas x{ws}"},
+        "config": _config(w, ws),
+        "plan": {"kernel": r["algorithm"], "ctas": r["ctas"]},
         "roofline": {"bound": "hbm", "achieved": r["achieved_gbs"], "peak": peak, "unit": "GB/s",
                      "frac": r["achieved_gbs"] / peak, "traffic": traffic, "peak_source": peak_kind,
                      "kernel_ms": r["kernel_ms"], "bytes_per_launch": r["bytes_alg"]},
+        "roofline_fp32": {"bound": "alu", "achieved": fp32_ops / (r["kernel_ms"] * 1e-3) / 1e12, "peak": fp32_peak / 1e12,
+                          "unit": "T lane-ops/s", "frac": fp32_ops / (r["kernel_ms"] * 1e-3) / fp32_peak,
+                          "ops_per_launch": fp32_ops,
+                          "peak_source": f"{FP32_LANE_OPS_PER_CLK_SM} FP32 lane-ops/clk/SM x {fp32_sms} SMs x "
+                                         f"{fp32_mhz:.0f} MHz (median SM clock sampled during the timed steps)",
+                          "ops": f"{FP32_OPS_PER_STATE_STEP} per state-step (decay, state FMA, readout FMA) x batch x "
+                                 f"d_inner x d_state x L"},
         "clocks": r["clocks"],
         "e2e": {"value": tokens_all / (r["e2e_ms"] * 1e-3), "unit": UNIT, "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"],
@@ -718,6 +787,10 @@ def main():
                               "l2": "state larger than L2 (268 MB)",
                               "tokens_per_s": ssd_dec["tokens_per_s"] * ws, "achieved_gbs": ssd_dec["achieved_gbs"],
                               "frac": ssd_dec["achieved_gbs"] / peak, "bytes_per_step": ssd_dec["bytes"]}
+    for o in others:
+        o["frac"] = o["achieved_gbs"] / peak
+        o["tokens_per_s"] *= ws
+        line.setdefault("other_scans", {})[o["workload"]] = o
     if not args.no_cpu_baseline:
         v, cores, sample, _, v1, sample1 = cpu_oracle_sample(w)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,

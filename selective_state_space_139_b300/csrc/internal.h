@@ -193,12 +193,4 @@ cudaError_t scaled_status_read_and_clear(unsigned int* out);
 cudaError_t scan_scaled_launch(const ScanParams& p, int nchunks, int balanced_ctas, cudaStream_t stream, char* err,
                                size_t errlen);
 
-// bf16 fast path, two lanes per channel (scan_fast.cu).
-int fast_channels_per_cta();
-int fast_resident_ctas();   // co-resident CTAs on the current device (0 if unknown)
-cudaError_t fast_status_read_and_clear(unsigned int* out);
-// balanced_ctas > 0: balanced persistent schedule; else one CTA per (group, chunk)
-cudaError_t scan_fast_launch(const ScanParams& p, int nchunks, int balanced_ctas, cudaStream_t stream, char* err,
-                             size_t errlen);
-
 }  // namespace ssm

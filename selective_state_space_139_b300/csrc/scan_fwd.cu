@@ -541,10 +541,6 @@ cudaError_t read_and_clear_device_status(unsigned int* out, cudaStream_t stream)
   const unsigned int zero = 0;
   e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(unsigned int));
   if (e != cudaSuccess) return e;
-  unsigned int fast = 0;
-  e = fast_status_read_and_clear(&fast);
-  *out |= fast;
-  if (e != cudaSuccess) return e;
   unsigned int scaled = 0;
   e = scaled_status_read_and_clear(&scaled);
   *out |= scaled;

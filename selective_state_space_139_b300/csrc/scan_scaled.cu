@@ -468,9 +468,10 @@ __global__ void __launch_bounds__(kThreads, 1) scan_scaled_kernel(const __grid_c
     for (int i = 0; i < 8; ++i)
       Ah[i] = (!cur.structured && sidx(i) < p.N) ? p.A[static_cast<int64_t>(cur.d) * p.N + sidx(i)] : 0.0f;
     float sig_end = 1.0f;
-    // Chunks in pairs with two scalar buffers (the tile's chunk count is even): chunk c runs on the
-    // buffer filled during chunk c - 1, and the other buffer takes chunk c + 1 (or the next tile's
-    // first chunk), so no scalar set is copied.
+    // Chunks in pairs with two scalar buffers: chunk c runs on the buffer filled during chunk c - 1,
+    // and the other buffer takes chunk c + 1 (or the next tile's first chunk), so no scalar set is
+    // copied.  A tile with an odd chunk count (the last tile when L is an odd multiple of 8) ends
+    // with one chunk on sc_a and a copy back into sc_a.
     auto chunks = [&](auto tag) {
       constexpr bool kS = decltype(tag)::value;
       auto one = [&](Sc& run_sc, Sc& fill_sc, int c) {
@@ -486,9 +487,14 @@ __global__ void __launch_bounds__(kThreads, 1) scan_scaled_kernel(const __grid_c
         if (kMode == kAgg) lsum += run_sc.lsum;
         sig_end = run_sc.sig;
       };
-      for (int c = 0; c < nch; c += 2) {
+      int c = 0;
+      for (; c + 1 < nch; c += 2) {
         one(sc_a, sc_b, c);
         one(sc_b, sc_a, c + 1);
+      }
+      if (c < nch) {
+        one(sc_a, sc_b, c);
+        sc_a = sc_b;
       }
     };
     if (cur.structured) chunks(std::true_type());

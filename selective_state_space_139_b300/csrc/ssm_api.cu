@@ -68,8 +68,7 @@ int sm_count() {
 }
 
 struct Plan {
-  int path = 0;           // 0: general kernel (float32 io, ZOH, layouts TMA cannot describe); 1: bf16 two-lane
-                          // kernel; 2: bf16 rescaled-state kernel (one thread per channel)
+  int path = 0;           // 0: general kernel (float32 io, ZOH, layouts TMA cannot describe); 1: bf16 fast path
   int nchunks = 1;
   int64_t chunk_len = 0;
   int balanced_ctas = 0;  // fast path: > 0 selects the balanced persistent schedule
@@ -82,10 +81,10 @@ struct Plan {
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // The bf16 fast path needs: bf16 io, the Δ·B input term, rows TMA can describe (L a multiple of 8,
-// at least one 64-step tile, at least 64 rows).  Pointer alignment is checked at call time.
+// at least one 64-step tile, at least 128 rows).  Pointer alignment is checked at call time.
 bool fast_eligible(int batch, int dim, int64_t seqlen, ssm_dtype io, int disc) {
   return io == SSM_BF16 && disc == SSM_DISC_DELTA_B && seqlen % 8 == 0 && seqlen >= 64 &&
-         static_cast<int64_t>(batch) * dim >= 64;
+         static_cast<int64_t>(batch) * dim >= 128;
 }
 
 void layout_chunked(Plan* pl, int batch, int dim, int dstate, size_t carry_bytes) {
@@ -94,6 +93,31 @@ void layout_chunked(Plan* pl, int batch, int dim, int dstate, size_t carry_bytes
   pl->off_Q = round_up(per_chunk * (pl->nchunks - 1), 256);
   pl->off_hin = pl->off_Q + round_up(per_chunk * (pl->nchunks - 1), 256);
   pl->workspace = pl->off_hin + round_up(per_chunk * pl->nchunks, 256);
+}
+
+// The chunk length (a multiple of 64, at least 256; 0 = one pass) that minimises the estimated
+// time of the grid and chunked schedules for G channel groups on `slots` co-resident CTAs: time in
+// units of one CTA running one step of its group, the main pass taking ceil(G n / slots) waves of a
+// chunk plus a pipeline fill of about one tile per wave, the aggregate pass (no readout, no outputs)
+// about 0.6 of that.  With need_chunks, at least two chunks.
+int64_t best_chunk(int64_t G, int64_t slots, int64_t seqlen, bool need_chunks) {
+  const int64_t Lt = (seqlen + 63) / 64;
+  double best = 0.0;
+  int64_t best_c = 0;
+  for (int64_t n = need_chunks ? 2 : 1; n <= Lt && n <= 65535; ++n) {
+    const int64_t c = static_cast<int64_t>(round_up(static_cast<size_t>((seqlen + n - 1) / n), 64));
+    const int64_t nn = (seqlen + c - 1) / c;
+    if (nn != n) continue;   // the same chunk length as a smaller n
+    if (nn > 1 && c < 256) break;
+    const double main = static_cast<double>((G * nn + slots - 1) / slots) * (c + 64);
+    const double agg = nn > 1 ? 0.6 * static_cast<double>((G * (nn - 1) + slots - 1) / slots) * (c + 64) : 0.0;
+    const double t = main + agg;
+    if (best_c == 0 || t < best * 0.999) {
+      best = t;
+      best_c = nn > 1 ? c : -1;
+    }
+  }
+  return best_c > 0 ? best_c : 0;
 }
 
 // Decides the kernel path and schedule and lays out the workspace.  Returns false on bad options.
@@ -108,15 +132,16 @@ bool make_plan(int batch, int dim, int dstate, int64_t seqlen, ssm_dtype io, con
   }
   const int sms = sm_count();
   *pl = Plan();
-  if (fast_eligible(batch, dim, seqlen, io, disc) && seqlen % 16 == 0 && algo != SSM_ALGO_CHUNKED) {
-    // rescaled-state kernel under the balanced schedule when there are at least as many 128-channel
-    // groups as resident CTAs
+  if (fast_eligible(batch, dim, seqlen, io, disc)) {
+    // rescaled-state kernel: the balanced schedule when there are at least as many 128-channel
+    // groups as resident CTAs, otherwise one pass per group or time chunks, whichever the wave
+    // count makes faster
+    pl->path = 1;
     const int64_t cpc = ssm::scaled_channels_per_cta();
     const int64_t G = static_cast<int64_t>(batch) * ((dim + cpc - 1) / cpc);
     const int64_t Lt = (seqlen + 63) / 64;
-    const int64_t S = ssm::scaled_resident_ctas();
-    if (S > 0 && G >= S) {
-      pl->path = 2;
+    const int64_t S = ssm::scaled_resident_ctas();   // 0 when unknown (no device)
+    if (algo == SSM_ALGO_AUTO && S > 0 && G >= S) {
       pl->balanced_ctas = static_cast<int>(S);
       pl->range_tiles = (G * Lt + S - 1) / S;
       pl->nchunks = 1;
@@ -126,41 +151,17 @@ bool make_plan(int batch, int dim, int dstate, int64_t seqlen, ssm_dtype io, con
       pl->workspace = pl->off_flags + round_up(static_cast<size_t>(S) * sizeof(unsigned), 256);
       return true;
     }
-  }
-  if (fast_eligible(batch, dim, seqlen, io, disc)) {
-    pl->path = 1;
-    const int64_t cpc = ssm::fast_channels_per_cta();
-    const int64_t G = static_cast<int64_t>(batch) * ((dim + cpc - 1) / cpc);
-    const int64_t Lt = (seqlen + 63) / 64;
-    const int64_t S = ssm::fast_resident_ctas();     // 0 when unknown (no device)
     int64_t chunk = 0;
-    if (algo == SSM_ALGO_CHUNKED) {
+    if (algo == SSM_ALGO_CHUNKED && user_chunk > 0) {
       chunk = user_chunk;
-      if (chunk == 0) {
-        const int64_t target = std::max<int64_t>(2, (2 * std::max<int64_t>(S, sms) + G - 1) / G);
-        chunk = round_up(static_cast<size_t>((seqlen + target - 1) / target), 64);
-      }
-    } else if (S > 0 && G >= S) {
-      // enough groups for every resident CTA: balanced persistent schedule
-      pl->balanced_ctas = static_cast<int>(S);
-      pl->range_tiles = (G * Lt + S - 1) / S;
-      pl->nchunks = 1;
-      pl->chunk_len = seqlen;
-      pl->off_carry = 0;
-      pl->off_flags = round_up(static_cast<size_t>(S) * cpc * 16 * sizeof(float), 256);
-      pl->workspace = pl->off_flags + round_up(static_cast<size_t>(S) * sizeof(unsigned), 256);
-      return true;
-    } else if (algo == SSM_ALGO_AUTO && Lt >= 8) {
-      // too few groups: split time into chunks (aggregates, carry, re-run)
-      const int64_t slots = std::max<int64_t>(S, sms);
-      const int64_t target = (2 * slots + G - 1) / G;
-      chunk = std::max<int64_t>(round_up(static_cast<size_t>((seqlen + target - 1) / target), 64), 4 * 64);
+    } else if (algo != SSM_ALGO_SINGLE_PASS) {
+      chunk = best_chunk(G, S > 0 ? S : sms, seqlen, algo == SSM_ALGO_CHUNKED);
     }
     if (chunk > 0 && (seqlen + chunk - 1) / chunk > 65535)
       chunk = round_up(static_cast<size_t>((seqlen + 65534) / 65535), 64);
     if (chunk <= 0 || chunk >= seqlen) {
       pl->nchunks = 1;
-      pl->chunk_len = static_cast<int64_t>(round_up(static_cast<size_t>(seqlen), 64));
+      pl->chunk_len = seqlen;
       pl->workspace = 0;
       return true;
     }
@@ -302,8 +303,7 @@ ssm_status ssm_scan_fwd_describe(int batch, int dim, int dstate, int64_t seqlen,
   plan->nchunks = pl.nchunks;
   plan->chunk_len = pl.chunk_len;
   plan->workspace_bytes = pl.workspace;
-  const int64_t cpc = pl.path == 1 ? ssm::fast_channels_per_cta()
-                      : pl.path == 2 ? ssm::scaled_channels_per_cta() : kChannelsPerCta;
+  const int64_t cpc = pl.path == 1 ? ssm::scaled_channels_per_cta() : kChannelsPerCta;
   const int64_t groups = static_cast<int64_t>(batch) * ((dim + cpc - 1) / cpc);
   if (pl.balanced_ctas > 0) {
     plan->schedule = 1;
@@ -409,16 +409,6 @@ ssm_status ssm_scan_fwd_ex(const void* u, const void* delta, const float* A, con
   }
   char err[256] = {0};
   char* ws = static_cast<char*>(workspace);
-  if (pl.path == 2 && aligned16) {
-    p.sched_balanced = 1;
-    p.range_tiles = pl.range_tiles;
-    p.carry = reinterpret_cast<float*>(ws + pl.off_carry);
-    p.flags = reinterpret_cast<unsigned*>(ws + pl.off_flags);
-    p.chunk_len = seqlen;
-    cudaError_t ce = ssm::scan_scaled_launch(p, 1, pl.balanced_ctas, stream, err, sizeof(err));
-    if (ce != cudaSuccess) return cuda_fail(ce, err[0] ? err : "scan launch");
-    return SSM_OK;
-  }
   if (pl.path == 1 && aligned16) {
     if (pl.balanced_ctas > 0) {
       p.sched_balanced = 1;
@@ -435,7 +425,7 @@ ssm_status ssm_scan_fwd_ex(const void* u, const void* delta, const float* A, con
     } else {
       p.chunk_len = pl.chunk_len;
     }
-    cudaError_t ce = ssm::scan_fast_launch(p, pl.nchunks, pl.balanced_ctas, stream, err, sizeof(err));
+    cudaError_t ce = ssm::scan_scaled_launch(p, pl.nchunks, pl.balanced_ctas, stream, err, sizeof(err));
     if (ce != cudaSuccess) return cuda_fail(ce, err[0] ? err : "scan launch");
     return SSM_OK;
   }

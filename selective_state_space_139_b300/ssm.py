@@ -161,7 +161,7 @@ def describe_scan(batch: int, dim: int, dstate: int, seqlen: int, dtype=torch.bf
     pl = ScanPlan()
     pl.struct_size = ctypes.sizeof(ScanPlan)
     _check(lib, lib.ssm_scan_fwd_describe(batch, dim, dstate, seqlen, _io_code(dtype), ctypes.byref(o), ctypes.byref(pl)))
-    return {"path": ("general", "fast", "scaled")[pl.path], "schedule": ("grid", "balanced", "chunked")[pl.schedule],
+    return {"path": ("general", "fast")[pl.path], "schedule": ("grid", "balanced", "chunked")[pl.schedule],
             "nchunks": pl.nchunks, "chunk_len": pl.chunk_len, "ctas": pl.ctas, "kernel_launches": pl.kernel_launches,
             "workspace_bytes": pl.workspace_bytes}
 

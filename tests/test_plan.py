@@ -42,9 +42,9 @@ def test_kernel_path_choice():
 def test_explicit_schedules():
     pl = ssm.describe_scan(4, 512, 16, 4096, dtype=BF16, algorithm="chunked", chunk_len=512)
     assert (pl["schedule"], pl["nchunks"], pl["chunk_len"], pl["kernel_launches"]) == ("chunked", 8, 512, 3)
-    assert pl["ctas"] == 4 * (512 // 64) * 8
+    assert pl["ctas"] == 4 * (512 // 128) * 8
     pl = ssm.describe_scan(4, 5120, 16, 4096, dtype=BF16, algorithm="single_pass")
-    assert (pl["schedule"], pl["nchunks"], pl["workspace_bytes"], pl["ctas"]) == ("grid", 1, 0, 4 * 5120 // 64)
+    assert (pl["schedule"], pl["nchunks"], pl["workspace_bytes"], pl["ctas"]) == ("grid", 1, 0, 4 * 5120 // 128)
     assert ssm.describe_scan(2, 256, 16, 0, dtype=BF16)["kernel_launches"] == 0
 
 
@@ -62,14 +62,16 @@ def test_bad_plans_are_refused():
 @pytest.mark.gpu
 def test_full_size_workloads_run_the_balanced_and_chunked_schedules():
     """With the device's resident-CTA count known: the 2.8B layer (160 groups of 128 channels, at
-    least one per SM) runs the rescaled-state kernel under the balanced persistent schedule in one
-    launch, one CTA per SM; the 130M layer (96 groups of 128, 192 of 64) has too few groups and
-    splits time into chunks."""
+    least one per SM) runs the balanced persistent schedule in one launch, one CTA per SM; the 130M
+    layer (96 groups) runs one pass per group, which the wave count makes faster than time chunks;
+    the 2^20-step sequence (12 groups) splits time into chunks."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     big = ssm.describe_scan(4, 5120, 16, 4096, dtype=BF16)
-    assert (big["path"], big["schedule"], big["kernel_launches"]) == ("scaled", "balanced", 1)
+    assert (big["path"], big["schedule"], big["kernel_launches"]) == ("fast", "balanced", 1)
     assert big["ctas"] == sms and big["workspace_bytes"] > 0
     small = ssm.describe_scan(8, 1536, 16, 2048, dtype=BF16)
-    assert (small["path"], small["schedule"]) == ("fast", "chunked") and small["nchunks"] > 1
+    assert (small["path"], small["schedule"], small["ctas"]) == ("fast", "grid", 96)
+    long = ssm.describe_scan(1, 1536, 16, 1 << 20, dtype=BF16)
+    assert (long["path"], long["schedule"]) == ("fast", "chunked") and long["nchunks"] > 1

@@ -237,10 +237,10 @@ def test_binding_rejects_cpu_tensors():
         ssm.selective_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"])
 
 
-BALANCED_SHAPES = [  # enough 64-channel groups for every resident CTA: balanced persistent schedule
-    (8, 2400, 16, 200),     # 304 groups, 4 tiles per group, a ragged last tile (L % 64 = 8)
-    (64, 512, 16, 256),     # 512 groups
-    (5, 4100, 16, 136),     # ragged dim (4100 = 64 * 64 + 4)
+BALANCED_SHAPES = [  # at least one 128-channel group per resident CTA: balanced persistent schedule
+    (8, 2400, 16, 200),     # 152 groups, 4 tiles per group, a ragged last tile of one 8-step chunk
+    (64, 512, 16, 256),     # 256 groups
+    (5, 4100, 16, 136),     # ragged dim (4100 = 32 * 128 + 4), last tile of one 8-step chunk
     (8, 2400, 7, 128),      # dstate 7
 ]
 
