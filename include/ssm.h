@@ -152,8 +152,9 @@ SSM_API ssm_status ssm_state_update(const void* x_t, const void* delta_t, const 
  *    passes every input and output buffer.
  *  - Shapes whose schedule needs more scratch than the fixed size return SSM_ERR_UNSUPPORTED
  *    with a message naming the size; use ssm_scan_fwd with a caller workspace for those.
- *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
- *    that device current; make that first call before any stream capture.
+ *  - The first call in a CUDA context (the first on each device, and the first after a
+ *    cudaDeviceReset) looks up the array's device address (cudaGetSymbolAddress) with that context
+ *    current; make that first call before any stream capture.
  *  - All calls on a device share the one array and it keeps the last call's contents (each call
  *    writes the scratch words it reads, so results do not depend on them).  Two calls whose
  *    kernels overlap on the GPU (different streams, or host threads without ordering) race on

@@ -8,6 +8,8 @@
 // afford an allocation on its latency path.  ssm_scan_fwd_noalloc serves them: its scratch is a
 // fixed array in this library's device memory, reserved when the library's module loads on a GPU
 // and held until the process exits.  The call itself allocates nothing.
+#include <cudaTypedefs.h>
+
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
@@ -21,10 +23,73 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;   // 8 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// The array's device address, looked up once per device with that device current.
-constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {};
+// The array's device address, looked up once per CUDA context with that context current.  The
+// context is identified by its driver-assigned unique id, which is never reused: after a
+// cudaDeviceReset, or in another context of the same device, the module is loaded anew and the
+// array may sit elsewhere, so a new id triggers a new lookup.
+struct ScratchEntry {
+  unsigned long long ctx_id;
+  void* addr;
+};
+constexpr int kCacheEntries = 64;
+ScratchEntry g_cache[kCacheEntries] = {};
+int g_cache_next = 0;
 std::mutex g_scratch_mu;
+
+using PfnCtxGetCurrent = CUresult (*)(CUcontext*);
+using PfnCtxGetId = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context, or 0 if there is none or it cannot be read.
+unsigned long long current_context_id() {
+  static PfnCtxGetCurrent get_current = nullptr;
+  static PfnCtxGetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PfnCtxGetCurrent>(f);
+    else
+      cudaGetLastError();
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PfnCtxGetId>(f);
+    else
+      cudaGetLastError();
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// The array's device address in the current context (set-up on the first call in a context).
+cudaError_t scratch_address(void** out) {
+  const unsigned long long id = current_context_id();
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (id != 0) {
+    for (const ScratchEntry& e : g_cache)
+      if (e.ctx_id == id) {
+        *out = e.addr;
+        return cudaSuccess;
+      }
+  }
+  // the host-side name of the array is not a device pointer: translate it with the context current
+  void* addr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
+  if (e != cudaSuccess) return e;
+  // the runtime creates the context on its first call: the id may only be readable now
+  const unsigned long long id2 = id != 0 ? id : current_context_id();
+  if (id2 != 0) {
+    g_cache[g_cache_next] = ScratchEntry{id2, addr};
+    g_cache_next = (g_cache_next + 1) % kCacheEntries;
+  }
+  *out = addr;
+  return cudaSuccess;
+}
 
 }  // namespace
 
@@ -44,31 +109,11 @@ ssm_status ssm_scan_fwd_noalloc(const void* u, const void* delta, const float* A
                         need, kNoAllocScratchBytes);
     return SSM_ERR_UNSUPPORTED;
   }
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) {
-    ssm::set_last_error("ssm_scan_fwd_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
-    return SSM_ERR_CUDA;
-  }
-  if (dev < 0 || dev >= kMaxDevices) {
-    ssm::set_last_error("ssm_scan_fwd_noalloc: device ordinal %d above %d", dev, kMaxDevices - 1);
-    return SSM_ERR_UNSUPPORTED;
-  }
   void* scratch = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
-      // first call on this device: translate the symbol to its device address (the host-side name
-      // of the array is not a device pointer)
-      void* addr = nullptr;
-      e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
-      if (e != cudaSuccess) {
-        ssm::set_last_error("ssm_scan_fwd_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-        return SSM_ERR_CUDA;
-      }
-      g_scratch_addr[dev] = addr;
-    }
-    scratch = g_scratch_addr[dev];
+  const cudaError_t e = scratch_address(&scratch);
+  if (e != cudaSuccess) {
+    ssm::set_last_error("ssm_scan_fwd_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    return SSM_ERR_CUDA;
   }
   // The existing entry point does the rest: its schedules write every scratch word they read in the
   // same call (the balanced schedule clears its flags first; the chunked one writes its aggregates

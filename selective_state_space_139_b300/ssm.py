@@ -73,6 +73,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ssm_state_update.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, vp]
     lib.ssm_selftest_bounded_wait.restype = i32
     lib.ssm_selftest_bounded_wait.argtypes = [i32, i64, vp]
+    lib.ssm_selftest_withhold_carry.restype = i32
+    lib.ssm_selftest_withhold_carry.argtypes = [i32, i64]
     lib.ssm_scan_fwd_describe.restype = i32
     lib.ssm_scan_fwd_describe.argtypes = [i32, i32, i32, i64, i32, ctypes.POINTER(ScanOptions), ctypes.POINTER(ScanPlan)]
     lib.ssm_causal_conv1d_fwd.restype = i32
