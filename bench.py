@@ -23,6 +23,7 @@ data path); value = tokens of all ranks / the slowest rank's time ("scaling": "w
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -589,21 +590,26 @@ def _config(w, n_gpus):
             "parallelism": f"replicas x{n_gpus}"}
 
 
-def measure_scan_kernel(w, dev, rank, reps=10):
-    """Another prefill workload: the scan's device time alone (mean of back-to-back calls)."""
+def measure_scan_kernel(w, dev, rank, reps=10, discretization="delta_b", general_A=False):
+    """Another prefill workload (or option): the scan's device time alone (mean of back-to-back calls).
+    general_A replaces A by -exp(U[0, 3)) per (d, n), which is not of the form (n+1)·A[d,0]."""
     import torch
     from selective_state_space_139_b300 import ssm
     from selective_state_space_139_b300 import workloads as W
 
     inp = W.make_scan_inputs(w, device=dev, seed=w.seed + rank)
+    if general_A:
+        g = torch.Generator(device=dev).manual_seed(w.seed + 17)
+        inp["A"] = -torch.exp(3.0 * torch.rand(inp["A"].shape, generator=g, device=dev))
     y = torch.empty_like(inp["u"])
     hL = torch.empty((w.batch, w.dim, w.dstate), device=dev, dtype=torch.float32)
-    plan = ssm.describe_scan(w.batch, w.dim, w.dstate, w.seqlen, inp["u"].dtype)
+    plan = ssm.describe_scan(w.batch, w.dim, w.dstate, w.seqlen, inp["u"].dtype, discretization=discretization)
     ws = torch.empty(max(plan["workspace_bytes"], 1), dtype=torch.uint8, device=dev)
 
     def call():
         ssm.selective_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], D=inp["D"], z=inp["z"],
-                               delta_bias=inp["delta_bias"], out=y, last_state=hL, workspace=ws)
+                               delta_bias=inp["delta_bias"], out=y, last_state=hL, workspace=ws,
+                               discretization=discretization)
 
     ms = _time_back_to_back(call, reps, dev)
     assert ssm.device_status() == ssm.SSM_OK
@@ -718,10 +724,17 @@ def main():
     ssd = None if args.no_ssd else measure_ssd(dev, rank)
     ssd_dec = None if args.no_ssd else measure_ssd_decode(dev, rank)
     others = []
+    variants = {}
     if not args.no_other_scans:
         for name in ("mamba130m-layer", "long-dna"):
             if name != w.name:
                 others.append(measure_scan_kernel(W.WORKLOADS[name], dev, rank, reps=10 if name != "long-dna" else 5))
+        # the options that run the general kernel: the exact ZOH input term (bf16 io) on this workload,
+        # and float32 io (computed in double) on the 130M-layer shape
+        variants["general_A"] = measure_scan_kernel(w, dev, rank, reps=10, general_A=True)
+        variants["zoh"] = measure_scan_kernel(w, dev, rank, reps=3, discretization="zoh")
+        variants["f32_io"] = measure_scan_kernel(dataclasses.replace(W.WORKLOADS["mamba130m-layer"], io_dtype="f32"),
+                                                 dev, rank, reps=3)
     if rank != 0:
         return 0
     tokens_all = w.tokens * ws
@@ -791,6 +804,14 @@ def main():
         o["frac"] = o["achieved_gbs"] / peak
         o["tokens_per_s"] *= ws
         line.setdefault("other_scans", {})[o["workload"]] = o
+    for k, o in variants.items():
+        o["frac"] = o["achieved_gbs"] / peak
+        o["tokens_per_s"] *= ws
+    if variants:
+        variants["general_A"]["what"] = "A = -exp(U[0,3)) per (d, n): one ex2 per state and step (fast path)"
+        variants["zoh"]["what"] = "exact zero-order-hold input term, bf16 io (general kernel, one thread per channel)"
+        variants["f32_io"]["what"] = "float32 io: coefficients, state and readout in double (general kernel)"
+        line["variants"] = variants
     if not args.no_cpu_baseline:
         v, cores, sample, _, v1, sample1 = cpu_oracle_sample(w)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
