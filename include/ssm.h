@@ -45,7 +45,8 @@ typedef enum {
   SSM_ERR_INVALID_ARG = 1,   /* null pointer, bad size, bad flag, aliasing, short workspace */
   SSM_ERR_UNSUPPORTED = 2,   /* valid but outside what this build implements (dstate > 16, d_conv != 4) */
   SSM_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
-  SSM_ERR_TIMEOUT = 4        /* reported by ssm_device_status(): a device wait gave up */
+  SSM_ERR_TIMEOUT = 4,       /* reported by ssm_device_status(): a device wait gave up */
+  SSM_ERR_CHECK = 5          /* reported by ssm_device_status() of the checked build: an index check failed */
 } ssm_status;
 
 typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
@@ -72,6 +73,15 @@ typedef struct {
 
 /* ABI version of this header (increments on any signature change). */
 SSM_API int ssm_abi_version(void);
+
+/*
+ * 1 for the checked debug build (libssm_b300_check.so, compiled with -DSSM_CHECK=1), 0 otherwise.
+ * In the checked build every global load and store of the kernels goes through an index check
+ * against the buffer's element count; an access outside it is not made (loads read a zeroed sink,
+ * stores go to it), the kernel carries on, and the next ssm_device_status() returns SSM_ERR_CHECK.
+ * Nothing traps.  The checks cost time: the checked build is for tests, not for measurement.
+ */
+SSM_API int ssm_checked_build(void);
 
 /* Human-readable name of a status code (static string). */
 SSM_API const char* ssm_status_string(ssm_status s);
@@ -300,8 +310,18 @@ SSM_API ssm_status ssm_selftest_bounded_wait(int which, int64_t limit_ns, cudaSt
 SSM_API ssm_status ssm_selftest_withhold_carry(int cta, int64_t limit_ns);
 
 /*
- * Reads and clears the device status word (synchronises `stream`).  Returns SSM_OK, SSM_ERR_TIMEOUT
- * if a kernel gave up a bounded wait since the last call, or SSM_ERR_CUDA.
+ * Self-test of the index checks (checked build only): enqueues on `stream` one kernel that stores to
+ * the element one past a 32-element device buffer through the index check, which redirects the store
+ * to a sink inside the library and records the failure; the next ssm_device_status() returns
+ * SSM_ERR_CHECK and clears it.  No memory outside the library's own buffers is touched.  The ordinary
+ * build returns SSM_ERR_UNSUPPORTED and enqueues nothing.
+ */
+SSM_API ssm_status ssm_selftest_index_check(cudaStream_t stream);
+
+/*
+ * Reads and clears the device status word (synchronises `stream`).  Returns SSM_OK, SSM_ERR_CHECK if
+ * (checked build only) an index check failed since the last call, else SSM_ERR_TIMEOUT if a kernel
+ * gave up a bounded wait since the last call, or SSM_ERR_CUDA.
  */
 SSM_API ssm_status ssm_device_status(cudaStream_t stream);
 

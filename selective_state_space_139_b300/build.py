@@ -9,6 +9,8 @@ import os
 import shutil
 import subprocess
 import sys
+import tempfile
+from concurrent.futures import ThreadPoolExecutor
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
@@ -16,6 +18,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIB_DIR, "libssm_b300.so")
+# The checked debug build: every kernel's global accesses go through index checks that report
+# SSM_ERR_CHECK through ssm_device_status() instead of touching memory outside their buffers.
+LIB_CHECK = os.path.join(LIB_DIR, "libssm_b300_check.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -35,28 +40,43 @@ def deps():
         [os.path.join(INCLUDE, "ssm.h"), os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    """Compiles each kernel file to an object in parallel, then links the shared library."""
+    lib = LIB_CHECK if checked else LIB
+    if not force and up_to_date(lib):
+        return lib
     os.makedirs(LIB_DIR, exist_ok=True)
-    tmp = LIB + ".tmp"
-    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC,-fvisibility=hidden",
-           "-Xcompiler", "-Wall", "-I", INCLUDE, "-I", CSRC, "-o", tmp, *sources()]
+    flags = [*ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden", "-Xcompiler", "-Wall",
+             "-I", INCLUDE, "-I", CSRC]
+    if checked:
+        flags.append("-DSSM_CHECK=1")
     if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-        print(" ".join(cmd))
-    subprocess.check_call(cmd)
-    os.replace(tmp, LIB)
-    return LIB
+        flags.append("-Xptxas=-v")
+    with tempfile.TemporaryDirectory(prefix="ssm_obj_") as obj_dir:
+        def compile_one(src: str) -> str:
+            obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
+            cmd = [nvcc(), *flags, "-c", "-o", obj, src]
+            if verbose:
+                print(" ".join(cmd))
+            subprocess.check_call(cmd)
+            return obj
+
+        srcs = sources()
+        with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as pool:
+            objs = list(pool.map(compile_one, srcs))
+        tmp = lib + ".tmp"
+        subprocess.check_call([nvcc(), *ARCH, "-shared", "-o", tmp, *objs])
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose="-v" in sys.argv)
-    print(LIB)
+    for chk in (False, True):
+        print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, checked=chk))

@@ -47,6 +47,8 @@ __global__ void __launch_bounds__(256) conv1d_vec_kernel(const ConvParams p) {
   const uint32_t stride = gridDim.x * blockDim.x;
   const int lane = threadIdx.x & 31;
   const IO* __restrict__ xg = static_cast<const IO*>(p.x);     // x and u never overlap (checked on the host)
+  const int64_t nRows = static_cast<int64_t>(p.batch) * p.dim;  // buffer sizes for the checks of checked builds
+  const int64_t nIO = nRows * p.L;
   IO* __restrict__ ug = static_cast<IO*>(p.u);
   for (uint32_t f0 = blockIdx.x * blockDim.x + threadIdx.x; f0 - lane < total; f0 += kPer * stride) {
     uint32_t row[kPer], c[kPer];
@@ -59,7 +61,7 @@ __global__ void __launch_bounds__(256) conv1d_vec_kernel(const ConvParams p) {
       const uint32_t fl = live[i] ? f : total - 1;   // lanes past the end mirror the last chunk
       row[i] = fl / cpr;
       c[i] = fl - row[i] * cpr;
-      raw[i] = __ldg(reinterpret_cast<const uint4*>(xg + static_cast<int64_t>(fl) * V));
+      raw[i] = __ldg(reinterpret_cast<const uint4*>(checked(xg, static_cast<int64_t>(fl) * V, nIO, V)));
     }
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
@@ -75,14 +77,15 @@ __global__ void __launch_bounds__(256) conv1d_vec_kernel(const ConvParams p) {
         prev[0] = up[0]; prev[1] = up[1]; prev[2] = up[2];
       } else if (c[i] > 0) {
         float pv[V];
-        unpack_chunk(__ldg(reinterpret_cast<const uint4*>(xg + rbase + (c[i] - 1) * V)), pv, IO());
+        unpack_chunk(__ldg(reinterpret_cast<const uint4*>(checked(xg, rbase + (c[i] - 1) * V, nIO, V))), pv, IO());
         prev[0] = pv[V - 3]; prev[1] = pv[V - 2]; prev[2] = pv[V - 1];
       } else if (p.state_in) {
-        prev[0] = p.state_in[row[i] * 3 + 0]; prev[1] = p.state_in[row[i] * 3 + 1]; prev[2] = p.state_in[row[i] * 3 + 2];
+        const float* si = checked(p.state_in, static_cast<int64_t>(row[i]) * 3, nRows * 3, 3);
+        prev[0] = si[0]; prev[1] = si[1]; prev[2] = si[2];
       } else {
         prev[0] = prev[1] = prev[2] = 0.0f;
       }
-      const float4 w = *reinterpret_cast<const float4*>(p.w + static_cast<int64_t>(d) * 4);
+      const float4 w = *reinterpret_cast<const float4*>(checked(p.w, static_cast<int64_t>(d) * 4, static_cast<int64_t>(p.dim) * 4, 4));
       float win[V + 3];
       win[0] = prev[0]; win[1] = prev[1]; win[2] = prev[2];
 #pragma unroll
@@ -100,11 +103,12 @@ __global__ void __launch_bounds__(256) conv1d_vec_kernel(const ConvParams p) {
         }
       }
       if (live[i]) {
-        *reinterpret_cast<uint4*>(ug + rbase + c[i] * V) = pack_chunk(out);
+        *reinterpret_cast<uint4*>(checked(ug, rbase + c[i] * V, nIO, V)) = pack_chunk(out);
         if (p.state_out && c[i] == cpr - 1) {
-          p.state_out[row[i] * 3 + 0] = xv[V - 3];
-          p.state_out[row[i] * 3 + 1] = xv[V - 2];
-          p.state_out[row[i] * 3 + 2] = xv[V - 1];
+          float* so = checked(p.state_out, static_cast<int64_t>(row[i]) * 3, nRows * 3, 3);
+          so[0] = xv[V - 3];
+          so[1] = xv[V - 2];
+          so[2] = xv[V - 1];
         }
       }
     }
@@ -126,10 +130,10 @@ __global__ void __launch_bounds__(256) conv1d_scalar_kernel(const ConvParams p) 
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int64_t tt = t - 3 + k;   // position in x; negative -> the incoming state
-    if (tt >= 0) win[k] = io_at(xr, tt);
-    else win[k] = p.state_in ? p.state_in[row * 3 + (tt + 3)] : 0.0f;
+    if (tt >= 0) win[k] = IoTraits<IO>::to_f32(*checked(static_cast<const IO*>(p.x), row * p.L + tt, nrows * p.L));
+    else win[k] = p.state_in ? *checked(p.state_in, row * 3 + (tt + 3), nrows * 3) : 0.0f;
   }
-  const float* w = p.w + static_cast<int64_t>(d) * 4;
+  const float* w = checked(p.w, static_cast<int64_t>(d) * 4, static_cast<int64_t>(p.dim) * 4, 4);
   float o;
   if constexpr (kFast) {
     const float s = fmaf(w[3], win[3], fmaf(w[2], win[2], fmaf(w[1], win[1], w[0] * win[0])));
@@ -139,10 +143,10 @@ __global__ void __launch_bounds__(256) conv1d_scalar_kernel(const ConvParams p) 
                      static_cast<double>(w[2]) * win[2] + static_cast<double>(w[3]) * win[3];
     o = static_cast<float>(p.silu ? s / (1.0 + exp(-s)) : s);
   }
-  static_cast<IO*>(p.u)[row * p.L + t] = IoTraits<IO>::from_f32(o);
+  *checked(static_cast<IO*>(p.u), row * p.L + t, nrows * p.L) = IoTraits<IO>::from_f32(o);
   if (p.state_out && t >= p.L - 3) {
     // the last three entries of xpad (L >= 3 here; shorter sequences are handled by the host)
-    p.state_out[row * 3 + (t - (p.L - 3))] = io_at(xr, t);
+    *checked(p.state_out, row * 3 + (t - (p.L - 3)), nrows * 3) = io_at(xr, t);
   }
 }
 
@@ -188,6 +192,8 @@ cudaError_t launch(const ConvParams& p, bool vec, cudaStream_t stream) {
 }
 
 }  // namespace
+
+cudaError_t conv1d_check_read_and_clear(unsigned int* out) { return tu_check_read_and_clear(out); }
 
 cudaError_t conv1d_launch(const ConvParams& p, bool vec, cudaStream_t stream) {
   return p.io_bf16 ? launch<__nv_bfloat16>(p, vec, stream) : launch<float>(p, vec, stream);

@@ -6,7 +6,16 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#ifndef SSM_CHECK
+#define SSM_CHECK 0   // 1 in the checked debug build (libssm_b300_check.so)
+#endif
+
 namespace ssm {
+
+// Bits of the device status word read by ssm_device_status(): a bounded wait gave up; an index
+// check of the checked build failed.
+constexpr unsigned kStatusTimeout = 1u;
+constexpr unsigned kStatusBounds = 2u;
 
 // Everything a prefill pass needs; filled and validated by the API layer.
 struct ScanParams {
@@ -129,8 +138,16 @@ struct BwdParams {
   int io_bf16;
   int vec_io;             // L % 8 == 0 and every io row base 16-byte aligned
   int vec_red;            // dB, dC 16-byte aligned and L % 4 == 0 (vector atomics)
+  int vec_bc;             // L % 8 == 0 and B, C 16-byte aligned (16-byte loads of 8 steps of a B/C row)
 };
 
+// bfloat16-io backward (scan_bwd_bf16.cu): 128-channel tiles, the local forward, the carries and
+// the reverse pass; the accumulators (dA, dB, dC, dD, dbias) must be zero on entry.
+constexpr int kBwd16ChannelsPerCta = 128;
+constexpr int kBwd16CtasPerSm = 2;   // resident reverse-pass CTAs per SM (109 KB of shared memory each)
+cudaError_t bwd16_launch(const BwdParams& p, cudaStream_t stream);
+// The carries of the chunk aggregates (float), shared by both backward implementations.
+cudaError_t bwd_carry_launch_f32(const BwdParams& p, cudaStream_t stream);
 int bwd_segment_steps();
 int bwd_aggregate_floats();
 cudaError_t scan_bwd_launch(const BwdParams& p, cudaStream_t stream);
@@ -179,9 +196,23 @@ void set_last_error(const char* fmt, ...);
 // Self-test of the device failure path (selftest.cu): which 0 = an mbarrier wait, 1 = a flag poll.
 cudaError_t selftest_bounded_wait_launch(int which, unsigned long long limit_ns, cudaStream_t stream);
 cudaError_t selftest_status_read_and_clear(unsigned int* out);
+// Checked build only: a store one past a buffer, caught by its index check (cudaErrorNotSupported in
+// the ordinary build, which launches nothing).
+cudaError_t selftest_index_check_launch(cudaStream_t stream);
 
 // Device status word access (scan_fwd.cu owns the symbol).
 cudaError_t read_and_clear_device_status(unsigned int* out, cudaStream_t stream);
+
+// Index-check words of the checked build (-DSSM_CHECK=1), one per kernel file; each reads its word
+// and clears it, and reports 0 in the ordinary build.
+cudaError_t general_check_read_and_clear(unsigned int* out);
+cudaError_t scaled_check_read_and_clear(unsigned int* out);
+cudaError_t decode_check_read_and_clear(unsigned int* out);
+cudaError_t conv1d_check_read_and_clear(unsigned int* out);
+cudaError_t ssd_check_read_and_clear(unsigned int* out);
+cudaError_t ssd_decode_check_read_and_clear(unsigned int* out);
+cudaError_t bwd_check_read_and_clear(unsigned int* out);
+cudaError_t bwd16_check_read_and_clear(unsigned int* out);
 
 // Carry pass of the chunked algorithm over float carries (scan_fwd.cu).
 cudaError_t carry_launch_f32(const ScanParams& p, int nchunks, cudaStream_t stream);

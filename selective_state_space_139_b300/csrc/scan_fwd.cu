@@ -239,7 +239,8 @@ __device__ void fill_stage_plain(uint8_t* stage, const ScanParams& p, int b, int
       const int d = d0 + r;
       const int64_t tt = t0 + t;
       IO v = IoTraits<IO>::from_f32(0.0f);
-      if (d < p.dim && tt < p.L) v = srcs[a][(static_cast<int64_t>(b) * p.dim + d) * p.L + tt];
+      if (d < p.dim && tt < p.L)
+        v = *checked(srcs[a], (static_cast<int64_t>(b) * p.dim + d) * p.L + tt, static_cast<int64_t>(p.batch) * p.dim * p.L);
       const int chunk = t / TL::kVec, e = t % TL::kVec;
       tile[(r * kRowBytes + (((chunk ^ (r & 7)) << 4))) / IoTraits<IO>::kBytes + e] = v;
     }
@@ -252,7 +253,7 @@ __device__ void fill_stage_plain(uint8_t* stage, const ScanParams& p, int b, int
       const int n = idx / TL::kT, t = idx % TL::kT;
       const int64_t tt = t0 + t;
       IO v = IoTraits<IO>::from_f32(0.0f);
-      if (tt < p.L) v = bcs[a][(static_cast<int64_t>(b) * p.N + n) * p.L + tt];
+      if (tt < p.L) v = *checked(bcs[a], (static_cast<int64_t>(b) * p.N + n) * p.L + tt, static_cast<int64_t>(p.batch) * p.N * p.L);
       const int chunk = t / TL::kVec, e = t % TL::kVec;
       tile[(n * kRowBytes + (((chunk ^ (n & 7)) << 4))) / IoTraits<IO>::kBytes + e] = v;
     }
@@ -322,17 +323,18 @@ __global__ void __launch_bounds__(kCH, 1)
   ChanD chd;
   ch.structured = true;
   {
-    const float a0 = valid ? p.A[static_cast<int64_t>(d) * p.N] : 0.0f;
+    const int64_t nA = static_cast<int64_t>(p.dim) * p.N;
+    const float a0 = valid ? *checked(p.A, static_cast<int64_t>(d) * p.N, nA) : 0.0f;
 #pragma unroll
     for (int n = 0; n < kNmax; ++n) {
-      const float an = (valid && n < p.N) ? p.A[static_cast<int64_t>(d) * p.N + n] : 0.0f;
+      const float an = (valid && n < p.N) ? *checked(p.A, static_cast<int64_t>(d) * p.N + n, nA) : 0.0f;
       ch.AL2[n] = an * kLog2e;
       ch.invA[n] = an != 0.0f ? 1.0f / an : 0.0f;
       chd.A[n] = an;
       if (n < p.N && an != static_cast<float>(n + 1) * a0) ch.structured = false;
     }
-    ch.D = (valid && p.D) ? p.D[d] : 0.0f;
-    ch.bias = (valid && p.bias) ? p.bias[d] : 0.0f;
+    ch.D = (valid && p.D) ? *checked(p.D, d, p.dim) : 0.0f;
+    ch.bias = (valid && p.bias) ? *checked(p.bias, d, p.dim) : 0.0f;
     chd.D = ch.D;
     chd.bias = ch.bias;
   }
@@ -349,8 +351,10 @@ __global__ void __launch_bounds__(kCH, 1)
     for (int n = 0; n < kNmax; ++n) {
       double v = 0.0;
       if (p.h_in && valid && n < p.N) {
-        v = p.carry_f64 ? static_cast<const double*>(p.h_in)[coff + base + n]
-                        : static_cast<double>(static_cast<const float*>(p.h_in)[coff + base + n]);
+        // chunked schedule: nchunks carried-in states; single pass: h0 in h_in (one)
+        const int64_t nh = static_cast<int64_t>(gridDim.z) * (p.h_in_chunk_stride ? p.h_in_chunk_stride : base + p.N);
+        v = p.carry_f64 ? *checked(static_cast<const double*>(p.h_in), coff + base + n, nh)
+                        : static_cast<double>(*checked(static_cast<const float*>(p.h_in), coff + base + n, nh));
       }
       hd[n] = v;
     }
@@ -427,10 +431,10 @@ __global__ void __launch_bounds__(kCH, 1)
           if (kMode == kModeMain && valid) {
             const int64_t t = t0 + c * TL::kVec;
             if (vec_store) {
-              *reinterpret_cast<uint4*>(yrow + t) = pack_chunk(yy);
+              *reinterpret_cast<uint4*>(checked(yrow, t, p.L - 0, TL::kVec)) = pack_chunk(yy);
             } else {
 #pragma unroll
-              for (int j = 0; j < TL::kVec; ++j) yrow[t + j] = IoTraits<IO>::from_f32(yy[j]);
+              for (int j = 0; j < TL::kVec; ++j) *checked(yrow, t + j, p.L) = IoTraits<IO>::from_f32(yy[j]);
             }
           }
         } else {
@@ -438,7 +442,7 @@ __global__ void __launch_bounds__(kCH, 1)
           for (int j = 0; j < TL::kVec; ++j) {
             if (j < nvalid) {
               yy[j] = one(structured_tag, c, j, uu, dd, zz);
-              if (kMode == kModeMain && valid) yrow[t0 + c * TL::kVec + j] = IoTraits<IO>::from_f32(yy[j]);
+              if (kMode == kModeMain && valid) *checked(yrow, t0 + c * TL::kVec + j, p.L) = IoTraits<IO>::from_f32(yy[j]);
             }
           }
         }
@@ -471,7 +475,7 @@ __global__ void __launch_bounds__(kCH, 1)
     if (p.last_state && chunk == static_cast<int>(gridDim.z) - 1) {
 #pragma unroll
       for (int n = 0; n < kNmax; ++n)
-        if (n < p.N) p.last_state[sbase + n] = static_cast<float>(hd[n]);
+        if (n < p.N) *checked(p.last_state, sbase + n, static_cast<int64_t>(p.batch) * p.dim * p.N) = static_cast<float>(hd[n]);
     }
   } else {
     // aggregate of this chunk: P = Π exp(Δ A) = exp(A ΣΔ) (one accurate exp per state), Q = h_end
@@ -479,13 +483,14 @@ __global__ void __launch_bounds__(kCH, 1)
 #pragma unroll
     for (int n = 0; n < kNmax; ++n) {
       if (n < p.N) {
-        const float an = p.A[static_cast<int64_t>(d) * p.N + n];
+        const float an = *checked(p.A, static_cast<int64_t>(d) * p.N + n, static_cast<int64_t>(p.dim) * p.N);
+        const int64_t nagg = static_cast<int64_t>(gridDim.z) * p.h_in_chunk_stride;
         if (p.carry_f64) {
-          static_cast<double*>(p.agg_P)[cbase + n] = exp(static_cast<double>(an) * sum_delta_d);
-          static_cast<double*>(p.agg_Q)[cbase + n] = hd[n];
+          *checked(static_cast<double*>(p.agg_P), cbase + n, nagg) = exp(static_cast<double>(an) * sum_delta_d);
+          *checked(static_cast<double*>(p.agg_Q), cbase + n, nagg) = hd[n];
         } else {
-          static_cast<float*>(p.agg_P)[cbase + n] = expf(an * sum_delta);
-          static_cast<float*>(p.agg_Q)[cbase + n] = static_cast<float>(hd[n]);
+          *checked(static_cast<float*>(p.agg_P), cbase + n, nagg) = expf(an * sum_delta);
+          *checked(static_cast<float*>(p.agg_Q), cbase + n, nagg) = static_cast<float>(hd[n]);
         }
       }
     }
@@ -533,6 +538,8 @@ cudaError_t launch_pass(const TensorMaps& tm, const ScanParams& p, int nchunks, 
 
 int scan_tile_steps(int io_bytes) { return kRowBytes / io_bytes; }
 
+cudaError_t general_check_read_and_clear(unsigned int* out) { return tu_check_read_and_clear(out); }
+
 cudaError_t read_and_clear_device_status(unsigned int* out, cudaStream_t stream) {
   cudaError_t e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return e;
@@ -552,7 +559,19 @@ cudaError_t read_and_clear_device_status(unsigned int* out, cudaStream_t stream)
   unsigned int st = 0;
   e = selftest_status_read_and_clear(&st);
   *out |= st;
-  return e;
+  if (e != cudaSuccess) return e;
+  // index checks of the checked build (each reader returns 0 in the ordinary build)
+  cudaError_t (*const readers[])(unsigned int*) = {general_check_read_and_clear, scaled_check_read_and_clear,
+                                                    decode_check_read_and_clear,  conv1d_check_read_and_clear,
+                                                    ssd_check_read_and_clear,     ssd_decode_check_read_and_clear,
+                                                    bwd_check_read_and_clear,     bwd16_check_read_and_clear};
+  for (auto* r : readers) {
+    unsigned int c = 0;
+    e = r(&c);
+    *out |= c;
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t carry_launch_f32(const ScanParams& p, int nchunks, cudaStream_t stream) {

@@ -278,6 +278,11 @@ __global__ void __launch_bounds__(kThreads, 1) scan_scaled_kernel(const __grid_c
   const int gpb = (p.dim + kCh - 1) / kCh;         // groups per batch row
   const bool has_z = kMode == kMain && p.z != nullptr;
   const bool softplus = p.softplus != 0;
+  // buffer sizes (elements) for the index checks of checked builds
+  const int64_t nA = static_cast<int64_t>(p.dim) * p.N;
+  const int64_t nState = static_cast<int64_t>(p.batch) * p.dim * p.N;
+  const int64_t nIO = static_cast<int64_t>(p.batch) * p.dim * p.L;
+  const int64_t nCarry = static_cast<int64_t>(gridDim.x) * kCh * kN;
 
   Walk w;
   int64_t chunk_idx = 0;
@@ -360,13 +365,13 @@ __global__ void __launch_bounds__(kThreads, 1) scan_scaled_kernel(const __grid_c
     cc.valid = d < p.dim;
     cc.d = cc.valid ? d : 0;
     const int64_t arow = static_cast<int64_t>(cc.d) * p.N;
-    cc.A0 = p.A[arow];
+    cc.A0 = *checked(p.A, arow, nA);
     bool st_ok = true;
     for (int n = 1; n < p.N; ++n)
-      if (p.A[arow + n] != static_cast<float>(n + 1) * cc.A0) st_ok = false;
+      if (*checked(p.A, arow + n, nA) != static_cast<float>(n + 1) * cc.A0) st_ok = false;
     cc.structured = __all_sync(0xffffffffu, st_ok) != 0;
-    cc.D = p.D ? p.D[cc.d] : 0.0f;
-    cc.bias2 = (p.bias ? p.bias[cc.d] : 0.0f) * kLog2e;
+    cc.D = p.D ? *checked(p.D, cc.d, p.dim) : 0.0f;
+    cc.bias2 = (p.bias ? *checked(p.bias, cc.d, p.dim) : 0.0f) * kLog2e;
   };
   // prologue: tile 0's table and channel constants, the first chunk's scalars
   bool ok = mbar_wait_bounded(&full[0], 0u, &g_scaled_status);
@@ -394,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_scaled_kernel(const __grid_c
     const bool tail_start = w.is_tail_start(k);
     if (tail_start && p.sched_balanced && tid == 0) {
       // the state carried in from the previous CTA, which ran the head of this group first
-      const unsigned* flag = p.flags + (blockIdx.x - 1);
+      const unsigned* flag = checked(p.flags, static_cast<int64_t>(blockIdx.x) - 1, gridDim.x);
       const uint64_t limit = p.carry_wait_ns ? p.carry_wait_ns : kWaitNs;
       const uint64_t t0 = globaltimer_ns();
       int got = 0;
@@ -433,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_scaled_kernel(const __grid_c
       if (tail_start && p.sched_balanced) {
         if (s_carry_ok) {
           const float4* src = reinterpret_cast<const float4*>(
-              p.carry + (static_cast<int64_t>(blockIdx.x) - 1) * kCh * kN + ch * kN + n0);
+              checked(p.carry, (static_cast<int64_t>(blockIdx.x) - 1) * kCh * kN + ch * kN + n0, nCarry, 8));
 #pragma unroll
           for (int i = 0; i < kNs / 4; ++i) {
             const float4 v = __ldcg(src + i);
@@ -444,11 +449,12 @@ __global__ void __launch_bounds__(kThreads, 1) scan_scaled_kernel(const __grid_c
         const float* src = static_cast<const float*>(p.h_in) + chunk_idx * p.h_in_chunk_stride + soff;
 #pragma unroll
         for (int i = 0; i < kNs; ++i)
-          if (sidx(i) < p.N) init[i] = src[sidx(i)];
+          if (sidx(i) < p.N)
+            init[i] = *checked(src, sidx(i), (static_cast<int64_t>(gridDim.y) - chunk_idx) * p.h_in_chunk_stride - soff);
       } else if (p.h0 != nullptr && t == 0) {
 #pragma unroll
         for (int i = 0; i < kNs; ++i)
-          if (sidx(i) < p.N) init[i] = p.h0[soff + sidx(i)];
+          if (sidx(i) < p.N) init[i] = *checked(p.h0, soff + sidx(i), nState);
       }
 #pragma unroll
       for (int i = 0; i < kNs / 2; ++i) h[i] = f2_make(init[2 * i], init[2 * i + 1]);
@@ -462,11 +468,12 @@ __global__ void __launch_bounds__(kThreads, 1) scan_scaled_kernel(const __grid_c
     const uint32_t tab = smem_u32(tab_at(k));
     __nv_bfloat16* yrow = nullptr;
     if (kMode == kMain && cur.valid)
-      yrow = static_cast<__nv_bfloat16*>(p.y) + (static_cast<int64_t>(cur.b) * p.dim + cur.d) * p.L + t0;
+      yrow = checked(static_cast<__nv_bfloat16*>(p.y), (static_cast<int64_t>(cur.b) * p.dim + cur.d) * p.L + t0, nIO,
+                     nch * kC);
     float Ah[8];   // this lane's row of A (A not of the form (n+1)·A[d,0])
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      Ah[i] = (!cur.structured && sidx(i) < p.N) ? p.A[static_cast<int64_t>(cur.d) * p.N + sidx(i)] : 0.0f;
+      Ah[i] = (!cur.structured && sidx(i) < p.N) ? *checked(p.A, static_cast<int64_t>(cur.d) * p.N + sidx(i), nA) : 0.0f;
     float sig_end = 1.0f;
     // Chunks in pairs with two scalar buffers: chunk c runs on the buffer filled during chunk c - 1,
     // and the other buffer takes chunk c + 1 (or the next tile's first chunk), so no scalar set is
@@ -513,7 +520,8 @@ __global__ void __launch_bounds__(kThreads, 1) scan_scaled_kernel(const __grid_c
       if (p.sched_balanced && k == w.n_head - 1) {
         // publish the state at the end of the head for the next CTA, once every thread has
         // written its part
-        float4* dst = reinterpret_cast<float4*>(p.carry + static_cast<int64_t>(blockIdx.x) * kCh * kN + ch * kN + n0);
+        float4* dst = reinterpret_cast<float4*>(
+            checked(p.carry, static_cast<int64_t>(blockIdx.x) * kCh * kN + ch * kN + n0, nCarry, 8));
 #pragma unroll
         for (int i = 0; i < kNs / 4; ++i) dst[i] = make_float4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
         __syncthreads();
@@ -524,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_scaled_kernel(const __grid_c
       } else if (kMode == kMain && t == Lt - 1 && cur.valid && p.last_state) {
 #pragma unroll
         for (int i = 0; i < kNs; ++i)
-          if (sidx(i) < p.N) p.last_state[soff + sidx(i)] = hv[i];
+          if (sidx(i) < p.N) *checked(p.last_state, soff + sidx(i), nState) = hv[i];
       }
       if (kMode == kAgg && !p.sched_balanced) {
         // aggregate of this chunk: P = exp(A ΣΔ) = 2^(A Σℓ), Q = h_end from a zero state
@@ -537,8 +545,9 @@ __global__ void __launch_bounds__(kThreads, 1) scan_scaled_kernel(const __grid_c
 #pragma unroll
           for (int i = 0; i < kNs; ++i) {
             if (sidx(i) < p.N) {
-              Pa[cbase + sidx(i)] = ex2_approx(p.A[static_cast<int64_t>(cur.d) * p.N + sidx(i)] * ls);
-              Qa[cbase + sidx(i)] = hv[i];
+              const int64_t nAgg = static_cast<int64_t>(gridDim.y) * p.h_in_chunk_stride;
+              *checked(Pa, cbase + sidx(i), nAgg) = ex2_approx(*checked(p.A, static_cast<int64_t>(cur.d) * p.N + sidx(i), nA) * ls);
+              *checked(Qa, cbase + sidx(i), nAgg) = hv[i];
             }
           }
         }
@@ -579,6 +588,8 @@ int scaled_resident_ctas() {
   if (dev >= 0 && dev < 64) cached[dev] = occ * sms;
   return occ * sms;
 }
+
+cudaError_t scaled_check_read_and_clear(unsigned int* out) { return tu_check_read_and_clear(out); }
 
 cudaError_t scaled_status_read_and_clear(unsigned int* out) {
   cudaError_t e = cudaMemcpyFromSymbol(out, g_scaled_status, sizeof(unsigned int));

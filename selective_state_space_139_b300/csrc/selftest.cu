@@ -6,6 +6,10 @@
 // the CUDA context stays usable.  Those waits never run out in correct operation; this kernel makes
 // each kind run out on purpose, with the same helpers and the same status word protocol, so that the
 // path can be tested without faulting, trapping or hanging a GPU.
+//
+// In the checked build a second kernel asks checked() for an index one past a 32-element buffer: the
+// check redirects the store to its sink and records kStatusBounds, which the next
+// ssm_device_status() reports as SSM_ERR_CHECK.  The ordinary build has no such kernel.
 #include "internal.h"
 #include "ssm_device.cuh"
 
@@ -39,7 +43,25 @@ __global__ void bounded_wait_selftest_kernel(int which, unsigned long long limit
   }
 }
 
+#if SSM_CHECK
+__device__ float g_check_probe[32];
+
+__global__ void index_check_selftest_kernel() {
+  *checked(g_check_probe, 32 + static_cast<int64_t>(threadIdx.x), 32) = 1.0f;
+}
+#endif
+
 }  // namespace
+
+cudaError_t selftest_index_check_launch(cudaStream_t stream) {
+#if SSM_CHECK
+  index_check_selftest_kernel<<<1, 1, 0, stream>>>();
+  return cudaGetLastError();
+#else
+  (void)stream;
+  return cudaErrorNotSupported;
+#endif
+}
 
 cudaError_t selftest_bounded_wait_launch(int which, unsigned long long limit_ns, cudaStream_t stream) {
   bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>(which, limit_ns);
@@ -50,7 +72,12 @@ cudaError_t selftest_status_read_and_clear(unsigned int* out) {
   cudaError_t e = cudaMemcpyFromSymbol(out, g_selftest_status, sizeof(unsigned int));
   if (e != cudaSuccess) return e;
   const unsigned int zero = 0;
-  return cudaMemcpyToSymbol(g_selftest_status, &zero, sizeof(unsigned int));
+  e = cudaMemcpyToSymbol(g_selftest_status, &zero, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  unsigned int c = 0;
+  e = tu_check_read_and_clear(&c);
+  *out |= c;
+  return e;
 }
 
 }  // namespace ssm

@@ -24,21 +24,26 @@ __global__ void __launch_bounds__(kThreads) ssd_decode_kernel(const SsdDecodePar
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int grp = h / (p.nheads / p.ngroups);
   const int64_t bh = static_cast<int64_t>(b) * p.nheads + h;
-  float4* st = reinterpret_cast<float4*>(p.state + bh * kHd * kNs) + lane;   // row r: st[r * 32]
+  const int64_t nHead = p.nheads, nBH = static_cast<int64_t>(p.batch) * p.nheads;
+  const int64_t nState4 = nBH * kHd * kNs / 4, nBC = static_cast<int64_t>(p.batch) * p.ngroups * kNs;
+  float4* const st4 = reinterpret_cast<float4*>(p.state);
+  const int64_t st0 = bh * kHd * kNs / 4 + lane;   // row r: st4[st0 + r * 32]
   const int64_t bg = (static_cast<int64_t>(b) * p.ngroups + grp) * kNs + 4 * lane;
   // ---- loads
   float4 hv[kRows];
 #pragma unroll
-  for (int i = 0; i < kRows; ++i) hv[i] = st[(warp + 4 * i) * 32];
-  const uint2 braw = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.B) + bg));
-  const uint2 craw = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.C) + bg));
-  const __nv_bfloat16* xr = static_cast<const __nv_bfloat16*>(p.x) + bh * kHd;
+  for (int i = 0; i < kRows; ++i) hv[i] = *checked(st4, st0 + (warp + 4 * i) * 32, nState4);
+  const uint2 braw = __ldg(reinterpret_cast<const uint2*>(checked(static_cast<const __nv_bfloat16*>(p.B), bg, nBC, 4)));
+  const uint2 craw = __ldg(reinterpret_cast<const uint2*>(checked(static_cast<const __nv_bfloat16*>(p.C), bg, nBC, 4)));
+  const __nv_bfloat16* const xg = static_cast<const __nv_bfloat16*>(p.x);
+  const int64_t nX = nBH * kHd;
   float xv[kRows];
 #pragma unroll
-  for (int i = 0; i < kRows; ++i) xv[i] = __bfloat162float(xr[warp + 4 * i]);
-  const float v = __bfloat162float(static_cast<const __nv_bfloat16*>(p.dt)[bh]) + (p.dt_bias ? p.dt_bias[h] : 0.0f);
-  const float Ah = p.A[h];
-  const float Dh = p.D ? p.D[h] : 0.0f;
+  for (int i = 0; i < kRows; ++i) xv[i] = __bfloat162float(*checked(xg, bh * kHd + warp + 4 * i, nX));
+  const float v = __bfloat162float(*checked(static_cast<const __nv_bfloat16*>(p.dt), bh, nBH)) +
+                  (p.dt_bias ? *checked(p.dt_bias, h, nHead) : 0.0f);
+  const float Ah = *checked(p.A, h, nHead);
+  const float Dh = p.D ? *checked(p.D, h, nHead) : 0.0f;
   // ---- arithmetic
   const float dl = p.softplus ? softplus_fast(v) : v;
   const float a = ex2_approx(dl * Ah * kLog2e);
@@ -60,7 +65,7 @@ __global__ void __launch_bounds__(kThreads) ssd_decode_kernel(const SsdDecodePar
   // ---- stores of the state, then the readouts: butterfly over lane bits 4..1 (16 values -> 1) and a
   // last exchange over bit 0; lane l then holds the sum of row warp + 4 ((l >> 1) & 15)
 #pragma unroll
-  for (int i = 0; i < kRows; ++i) st[(warp + 4 * i) * 32] = hv[i];
+  for (int i = 0; i < kRows; ++i) *checked(st4, st0 + (warp + 4 * i) * 32, nState4) = hv[i];
 #pragma unroll
   for (int w = 16, cnt = kRows; w >= 2; w >>= 1, cnt >>= 1) {
     const bool upper = (lane & w) != 0;
@@ -76,7 +81,8 @@ __global__ void __launch_bounds__(kThreads) ssd_decode_kernel(const SsdDecodePar
   if ((lane & 1) == 0) {
     const int i = (lane >> 1) & 15;
     const int r = warp + 4 * i;
-    static_cast<__nv_bfloat16*>(p.y)[bh * kHd + r] = __float2bfloat16_rn(part[0] + Dh * __bfloat162float(xr[r]));
+    *checked(static_cast<__nv_bfloat16*>(p.y), bh * kHd + r, nX) =
+        __float2bfloat16_rn(part[0] + Dh * __bfloat162float(*checked(xg, bh * kHd + r, nX)));
   }
 }
 
@@ -86,5 +92,7 @@ cudaError_t ssd_decode_launch(const SsdDecodeParams& p, cudaStream_t stream) {
   ssd_decode_kernel<<<dim3(p.nheads, p.batch), kThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
+
+cudaError_t ssd_decode_check_read_and_clear(unsigned int* out) { return tu_check_read_and_clear(out); }
 
 }  // namespace ssm

@@ -152,9 +152,13 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
   const int h = blockIdx.x, b = blockIdx.y;
   const int grp = h / (p.nheads / p.ngroups);
   const int64_t L = p.L;
-  const float A2 = p.A[h] * kLog2e;
-  const float bias = p.dt_bias ? p.dt_bias[h] : 0.0f;
-  const float Dh = p.D ? p.D[h] : 0.0f;
+  // element counts of the buffers, for the index checks of the checked build
+  const int64_t nHead = p.nheads, nBH = static_cast<int64_t>(p.batch) * p.nheads;
+  const int64_t nRowX = static_cast<int64_t>(p.batch) * L * p.nheads, nX = nRowX * kHd;
+  const int64_t nBC = static_cast<int64_t>(p.batch) * L * p.ngroups * kNs, nState = nBH * kHd * kNs;
+  const float A2 = *checked(p.A, h, nHead) * kLog2e;
+  const float bias = p.dt_bias ? *checked(p.dt_bias, h, nHead) : 0.0f;
+  const float Dh = p.D ? *checked(p.D, h, nHead) : 0.0f;
   const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(p.x);
   const __nv_bfloat16* dtg = static_cast<const __nv_bfloat16*>(p.dt);
   const __nv_bfloat16* Bg = static_cast<const __nv_bfloat16*>(p.B);
@@ -178,9 +182,9 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
   float H[kHd / 2];
   bool have_state = p.h0 != nullptr;
   {
-    const float* h0 = p.h0 ? p.h0 + (static_cast<int64_t>(b) * p.nheads + h) * kHd * kNs : nullptr;
+    const int64_t h0_base = (static_cast<int64_t>(b) * p.nheads + h) * kHd * kNs;
 #pragma unroll
-    for (int q = 0; q < kHd / 2; ++q) H[q] = h0 ? h0[(pbase + q) * kNs + n_own] : 0.0f;
+    for (int q = 0; q < kHd / 2; ++q) H[q] = p.h0 ? *checked(p.h0, h0_base + (pbase + q) * kNs + n_own, nState) : 0.0f;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint4 hi, lo;
@@ -211,14 +215,16 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
       const int r = i >> 4, q = i & 15;
       const bool in = t0 + r < L;
       const int64_t row = (static_cast<int64_t>(b) * L + (in ? t0 + r : 0)) * p.ngroups + grp;
-      cp_async16(sb + off + (q >> 3) * (kQ * 128) + sw_chunk(r, q & 7), src_base + row * kNs + q * 8, in ? 16 : 0);
+      cp_async16(sb + off + (q >> 3) * (kQ * 128) + sw_chunk(r, q & 7), checked(src_base, row * kNs + q * 8, nBC, 8),
+                 in ? 16 : 0);
     }
   };
   auto load_x = [&](int64_t t0) {
     for (int i = tid; i < kQ * 8; i += kThreads) {
       const int r = i >> 3, q = i & 7;
       const bool in = t0 + r < L;
-      const __nv_bfloat16* src = xg + ((static_cast<int64_t>(b) * L + (in ? t0 + r : 0)) * p.nheads + h) * kHd + q * 8;
+      const __nv_bfloat16* src =
+          checked(xg, ((static_cast<int64_t>(b) * L + (in ? t0 + r : 0)) * p.nheads + h) * kHd + q * 8, nX, 8);
       cp_async16(sb + TcSmem::kX + sw_chunk(r, q), src, in ? 16 : 0);
     }
   };
@@ -226,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
   // when that chunk starts, so the load's latency is not waited for
   const unsigned short* dtr = reinterpret_cast<const unsigned short*>(dtg);
   auto load_dt_raw = [&](int64_t t) -> uint32_t {
-    return t < L ? static_cast<uint32_t>(dtr[(static_cast<int64_t>(b) * L + t) * p.nheads + h]) : 0u;
+    return t < L ? static_cast<uint32_t>(*checked(dtr, (static_cast<int64_t>(b) * L + t) * p.nheads + h, nRowX)) : 0u;
   };
   auto dl_of = [&](uint32_t raw, int64_t t) -> float {
     if (t >= L) return 0.0f;
@@ -416,8 +422,8 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
 #pragma unroll
         for (int q = 0; q < 16; ++q) yo[q] += yl[q];
       }
-      __nv_bfloat16* y0 = yg + ((static_cast<int64_t>(b) * L + t0 + ri0) * p.nheads + h) * kHd;
-      __nv_bfloat16* y1 = yg + ((static_cast<int64_t>(b) * L + t0 + ri1) * p.nheads + h) * kHd;
+      const int64_t y0 = ((static_cast<int64_t>(b) * L + t0 + ri0) * p.nheads + h) * kHd;
+      const int64_t y1 = ((static_cast<int64_t>(b) * L + t0 + ri1) * p.nheads + h) * kHd;
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int pc = pbase + 8 * r + 2 * ft;
@@ -431,8 +437,8 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
           v10 = fmaf(e1, yo[4 * r + 2], v10);
           v11 = fmaf(e1, yo[4 * r + 3], v11);
         }
-        if (t0 + ri0 < L) *reinterpret_cast<uint32_t*>(y0 + pc) = pack_bf16x2(v00, v01);
-        if (t0 + ri1 < L) *reinterpret_cast<uint32_t*>(y1 + pc) = pack_bf16x2(v10, v11);
+        if (t0 + ri0 < L) *reinterpret_cast<uint32_t*>(checked(yg, y0 + pc, nX, 2)) = pack_bf16x2(v00, v01);
+        if (t0 + ri1 < L) *reinterpret_cast<uint32_t*>(checked(yg, y1 + pc, nX, 2)) = pack_bf16x2(v10, v11);
       }
     }
     fence_async_smem();   // the new H tiles, for the next chunk's MMAs
@@ -441,9 +447,9 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     tc_fence_after();
   }
   if (ok && p.hT) {
-    float* hT = p.hT + (static_cast<int64_t>(b) * p.nheads + h) * kHd * kNs;
+    const int64_t hT_base = (static_cast<int64_t>(b) * p.nheads + h) * kHd * kNs;
 #pragma unroll
-    for (int q = 0; q < kHd / 2; ++q) hT[(pbase + q) * kNs + n_own] = H[q];
+    for (int q = 0; q < kHd / 2; ++q) *checked(p.hT, hT_base + (pbase + q) * kNs + n_own, nState) = H[q];
   }
   tc_fence_before();
   __syncthreads();
@@ -468,5 +474,7 @@ cudaError_t ssd_status_read_and_clear(unsigned int* out) {
   const unsigned int zero = 0;
   return cudaMemcpyToSymbol(g_ssd_status, &zero, sizeof(unsigned int));
 }
+
+cudaError_t ssd_check_read_and_clear(unsigned int* out) { return tu_check_read_and_clear(out); }
 
 }  // namespace ssm

@@ -8,12 +8,50 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "internal.h"
+
 namespace ssm {
 
 // ------------------------------------------------------------------ status word
-// Bit 0: a pipeline wait gave up.  The word lives in scan_fwd.cu and is read and cleared by
-// ssm_device_status().
-constexpr unsigned kStatusTimeout = 1u;
+// kStatusTimeout (internal.h): a pipeline wait gave up.  The word lives in scan_fwd.cu and is read and
+// cleared by ssm_device_status().
+
+// ------------------------------------------------------------------ checked builds
+// Built with -DSSM_CHECK=1 (libssm_b300_check.so), every global-memory access whose index a kernel
+// computes goes through checked(): an index outside its buffer sets kStatusBounds in this
+// translation unit's check word and the access is redirected to a small sink inside this library's
+// device image, so that the kernel carries on without touching memory it does not own.  The result
+// of that call is then wrong, and ssm_device_status() reports SSM_ERR_CHECK.  Without SSM_CHECK the
+// helper is the plain pointer arithmetic.
+#if SSM_CHECK
+static __device__ unsigned int g_tu_check_status = 0;
+static __device__ __align__(16) unsigned char g_tu_check_sink[256];
+#endif
+
+// &base[idx], valid for `width` elements, in a buffer of n elements.
+template <typename T>
+__device__ __forceinline__ T* checked(T* base, int64_t idx, int64_t n, int width = 1) {
+#if SSM_CHECK
+  if (base == nullptr || idx < 0 || idx + width > n || width * static_cast<int64_t>(sizeof(T)) > 256) {
+    atomicOr(&g_tu_check_status, kStatusBounds);
+    return reinterpret_cast<T*>(g_tu_check_sink);
+  }
+#endif
+  return base + idx;
+}
+
+// Reads and clears this translation unit's check word (0 in unchecked builds).
+static inline cudaError_t tu_check_read_and_clear(unsigned int* out) {
+#if SSM_CHECK
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_tu_check_status, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_tu_check_status, &zero, sizeof(unsigned int));
+#else
+  *out = 0;
+  return cudaSuccess;
+#endif
+}
 
 // ------------------------------------------------------------------ shared memory / mbarrier
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

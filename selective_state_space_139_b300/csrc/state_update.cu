@@ -19,11 +19,6 @@ constexpr int kLanesPerChannel = 4;
 constexpr int kThreads = 256;
 constexpr int kChannelsPerBlock = kThreads / kLanesPerChannel;
 
-template <typename IO>
-__device__ __forceinline__ float ld_io(const void* p, int64_t i) {
-  return IoTraits<IO>::to_f32(static_cast<const IO*>(p)[i]);
-}
-
 template <typename IO, bool kFull16>
 __global__ void __launch_bounds__(kThreads) state_update_kernel(const DecodeParams p) {
   constexpr bool kFast = sizeof(IO) == 2;
@@ -42,35 +37,38 @@ __global__ void __launch_bounds__(kThreads) state_update_kernel(const DecodePara
   const int N = kFull16 ? 16 : p.N;
 
   // conv window [cs0, cs1, cs2, x_t] and its weights
-  const float x = ld_io<IO>(p.x, c);
-  float* cs = p.conv_state + c * 3;
+  const float x = IoTraits<IO>::to_f32(*checked(static_cast<const IO*>(p.x), c, nchan));
+  float* cs = checked(p.conv_state, c * 3, static_cast<int64_t>(nchan) * 3, 3);
   const float cs0 = cs[0], cs1 = cs[1], cs2 = cs[2];
   float4 w;
+  const float* wr = checked(p.conv_w, static_cast<int64_t>(d) * 4, static_cast<int64_t>(p.dim) * 4, 4);
   if (kFull16) {
-    w = *reinterpret_cast<const float4*>(p.conv_w + static_cast<int64_t>(d) * 4);
+    w = *reinterpret_cast<const float4*>(wr);
   } else {
-    const float* wr = p.conv_w + static_cast<int64_t>(d) * 4;
     w = make_float4(wr[0], wr[1], wr[2], wr[3]);
   }
   const float s = fmaf(w.w, x, fmaf(w.z, cs2, fmaf(w.y, cs1, w.x * cs0)));
   const float u = kFast ? silu_fast(s) : silu_accurate(s);
 
-  const float v = ld_io<IO>(p.delta, c) + (p.bias ? p.bias[d] : 0.0f);
+  const float v = IoTraits<IO>::to_f32(*checked(static_cast<const IO*>(p.delta), c, nchan)) +
+                  (p.bias ? *checked(p.bias, d, p.dim) : 0.0f);
   const float dl = p.softplus ? (kFast ? softplus_fast(v) : softplus_accurate(v)) : v;
   const float wu = dl * u;
 
   float hv[4], av[4], bv[4], cv[4];
-  float* srow = p.state + c * N;
-  const float* arow = p.A + static_cast<int64_t>(d) * N;
+  float* srow = checked(p.state, c * N, static_cast<int64_t>(nchan) * N, N);
+  const float* arow = checked(p.A, static_cast<int64_t>(d) * N, static_cast<int64_t>(p.dim) * N, N);
   const int64_t bcrow = static_cast<int64_t>(b) * N;
+  const IO* Brow = checked(static_cast<const IO*>(p.B), bcrow, static_cast<int64_t>(p.batch) * N, N);
+  const IO* Crow = checked(static_cast<const IO*>(p.C), bcrow, static_cast<int64_t>(p.batch) * N, N);
   if (kFull16) {
     const float4 h4 = *reinterpret_cast<const float4*>(srow + 4 * j);
     const float4 a4 = *reinterpret_cast<const float4*>(arow + 4 * j);
     hv[0] = h4.x; hv[1] = h4.y; hv[2] = h4.z; hv[3] = h4.w;
     av[0] = a4.x; av[1] = a4.y; av[2] = a4.z; av[3] = a4.w;
     if (kFast) {
-      const uint2 braw = *reinterpret_cast<const uint2*>(static_cast<const IO*>(p.B) + bcrow + 4 * j);
-      const uint2 craw = *reinterpret_cast<const uint2*>(static_cast<const IO*>(p.C) + bcrow + 4 * j);
+      const uint2 braw = *reinterpret_cast<const uint2*>(Brow + 4 * j);
+      const uint2 craw = *reinterpret_cast<const uint2*>(Crow + 4 * j);
       bv[0] = bf16lo_to_f32(braw.x); bv[1] = bf16hi_to_f32(braw.x);
       bv[2] = bf16lo_to_f32(braw.y); bv[3] = bf16hi_to_f32(braw.y);
       cv[0] = bf16lo_to_f32(craw.x); cv[1] = bf16hi_to_f32(craw.x);
@@ -78,8 +76,8 @@ __global__ void __launch_bounds__(kThreads) state_update_kernel(const DecodePara
     } else {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        bv[i] = ld_io<IO>(p.B, bcrow + 4 * j + i);
-        cv[i] = ld_io<IO>(p.C, bcrow + 4 * j + i);
+        bv[i] = IoTraits<IO>::to_f32(Brow[4 * j + i]);
+        cv[i] = IoTraits<IO>::to_f32(Crow[4 * j + i]);
       }
     }
   } else {
@@ -89,8 +87,8 @@ __global__ void __launch_bounds__(kThreads) state_update_kernel(const DecodePara
       const bool in = n < N;
       hv[i] = in ? srow[n] : 0.0f;
       av[i] = in ? arow[n] : 0.0f;
-      bv[i] = in ? ld_io<IO>(p.B, bcrow + n) : 0.0f;
-      cv[i] = in ? ld_io<IO>(p.C, bcrow + n) : 0.0f;
+      bv[i] = in ? IoTraits<IO>::to_f32(Brow[n]) : 0.0f;
+      cv[i] = in ? IoTraits<IO>::to_f32(Crow[n]) : 0.0f;
     }
   }
 
@@ -110,7 +108,8 @@ __global__ void __launch_bounds__(kThreads) state_update_kernel(const DecodePara
     const double sd = static_cast<double>(w.w) * x + static_cast<double>(w.z) * cs2 +
                       static_cast<double>(w.y) * cs1 + static_cast<double>(w.x) * cs0;
     ud = sd / (1.0 + exp(-sd));
-    const double vd = static_cast<double>(ld_io<IO>(p.delta, c)) + (p.bias ? p.bias[d] : 0.0f);
+    const double vd = static_cast<double>(IoTraits<IO>::to_f32(*checked(static_cast<const IO*>(p.delta), c, nchan))) +
+                      (p.bias ? *checked(p.bias, d, p.dim) : 0.0f);
     const double dld = p.softplus ? (vd > 0.0 ? vd + log1p(exp(-vd)) : log1p(exp(vd))) : vd;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -135,16 +134,16 @@ __global__ void __launch_bounds__(kThreads) state_update_kernel(const DecodePara
   if (j < 3) cs[j] = j == 0 ? cs1 : (j == 1 ? cs2 : x);
   if (j == 0) {
     if constexpr (kFast) {
-      float y = fmaf(p.D ? p.D[d] : 0.0f, u, py);
-      if (p.z) y *= silu_fast(ld_io<IO>(p.z, c));
-      static_cast<IO*>(p.y)[c] = IoTraits<IO>::from_f32(y);
+      float y = fmaf(p.D ? *checked(p.D, d, p.dim) : 0.0f, u, py);
+      if (p.z) y *= silu_fast(IoTraits<IO>::to_f32(*checked(static_cast<const IO*>(p.z), c, nchan)));
+      *checked(static_cast<IO*>(p.y), c, nchan) = IoTraits<IO>::from_f32(y);
     } else {
-      double y = pyd + (p.D ? static_cast<double>(p.D[d]) : 0.0) * ud;
+      double y = pyd + (p.D ? static_cast<double>(*checked(p.D, d, p.dim)) : 0.0) * ud;
       if (p.z) {
-        const double z = ld_io<IO>(p.z, c);
+        const double z = IoTraits<IO>::to_f32(*checked(static_cast<const IO*>(p.z), c, nchan));
         y *= z / (1.0 + exp(-z));
       }
-      static_cast<IO*>(p.y)[c] = IoTraits<IO>::from_f32(static_cast<float>(y));
+      *checked(static_cast<IO*>(p.y), c, nchan) = IoTraits<IO>::from_f32(static_cast<float>(y));
     }
   }
 }
@@ -168,14 +167,16 @@ __global__ void __launch_bounds__(kThreads1) state_update_bf16_kernel(const Deco
   if (t_raw >= pairs) return;
   const int bq = t_raw / p.dim;
   const int d = t_raw - bq * p.dim;
+  // buffer sizes (elements) for the index checks of checked builds
+  const int64_t nBD = static_cast<int64_t>(p.batch) * p.dim;
   // ---- loads: every state row, the A row, conv weights, B/C rows and the per-channel scalars
-  const float4* arow = reinterpret_cast<const float4*>(p.A + static_cast<int64_t>(d) * 16);
+  const float4* arow = reinterpret_cast<const float4*>(checked(p.A, static_cast<int64_t>(d) * 16, static_cast<int64_t>(p.dim) * 16, 16));
   float4 a4[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) a4[q] = arow[q];
-  const float4 w = *reinterpret_cast<const float4*>(p.conv_w + static_cast<int64_t>(d) * 4);
-  const float Dv = p.D ? p.D[d] : 0.0f;
-  const float bv = p.bias ? p.bias[d] : 0.0f;
+  const float4 w = *reinterpret_cast<const float4*>(checked(p.conv_w, static_cast<int64_t>(d) * 4, static_cast<int64_t>(p.dim) * 4, 4));
+  const float Dv = p.D ? *checked(p.D, d, p.dim) : 0.0f;
+  const float bv = p.bias ? *checked(p.bias, d, p.dim) : 0.0f;
   float4 h4[kBpt][4];
   uint4 braw[kBpt][2], craw[kBpt][2];
   float xv[kBpt], dv[kBpt], zv[kBpt], c0[kBpt], c1[kBpt], c2[kBpt];
@@ -188,17 +189,19 @@ __global__ void __launch_bounds__(kThreads1) state_update_bf16_kernel(const Deco
     const int b = live[k] ? b0 : p.batch - 1;
     const int64_t c = static_cast<int64_t>(b) * p.dim + d;
     cc[k] = c;
-    const float4* srow = reinterpret_cast<const float4*>(p.state + c * 16);
+    const float4* srow = reinterpret_cast<const float4*>(checked(p.state, c * 16, nBD * 16, 16));
 #pragma unroll
     for (int q = 0; q < 4; ++q) h4[k][q] = srow[q];
-    const uint4* brow = reinterpret_cast<const uint4*>(static_cast<const IO*>(p.B) + static_cast<int64_t>(b) * 16);
-    const uint4* crow = reinterpret_cast<const uint4*>(static_cast<const IO*>(p.C) + static_cast<int64_t>(b) * 16);
+    const uint4* brow = reinterpret_cast<const uint4*>(
+        checked(static_cast<const IO*>(p.B), static_cast<int64_t>(b) * 16, static_cast<int64_t>(p.batch) * 16, 16));
+    const uint4* crow = reinterpret_cast<const uint4*>(
+        checked(static_cast<const IO*>(p.C), static_cast<int64_t>(b) * 16, static_cast<int64_t>(p.batch) * 16, 16));
     braw[k][0] = brow[0]; braw[k][1] = brow[1];
     craw[k][0] = crow[0]; craw[k][1] = crow[1];
-    xv[k] = ld_io<IO>(p.x, c);
-    dv[k] = ld_io<IO>(p.delta, c);
-    zv[k] = p.z ? ld_io<IO>(p.z, c) : 0.0f;
-    const float* cs = p.conv_state + c * 3;
+    xv[k] = IoTraits<IO>::to_f32(*checked(static_cast<const IO*>(p.x), c, nBD));
+    dv[k] = IoTraits<IO>::to_f32(*checked(static_cast<const IO*>(p.delta), c, nBD));
+    zv[k] = p.z ? IoTraits<IO>::to_f32(*checked(static_cast<const IO*>(p.z), c, nBD)) : 0.0f;
+    const float* cs = checked(p.conv_state, c * 3, nBD * 3, 3);
     c0[k] = cs[0]; c1[k] = cs[1]; c2[k] = cs[2];
   }
   // ---- arithmetic and stores
@@ -235,14 +238,14 @@ __global__ void __launch_bounds__(kThreads1) state_update_bf16_kernel(const Deco
     if (p.z) y *= silu_fast(zv[k]);
     if (!live[k]) continue;
     const int64_t c = cc[k];
-    float4* sw = reinterpret_cast<float4*>(p.state + c * 16);
+    float4* sw = reinterpret_cast<float4*>(checked(p.state, c * 16, nBD * 16, 16));
 #pragma unroll
     for (int q = 0; q < 4; ++q) sw[q] = h4[k][q];
-    float* cs = p.conv_state + c * 3;
+    float* cs = checked(p.conv_state, c * 3, nBD * 3, 3);
     cs[0] = c1[k];
     cs[1] = c2[k];
     cs[2] = xv[k];
-    static_cast<IO*>(p.y)[c] = IoTraits<IO>::from_f32(y);
+    *checked(static_cast<IO*>(p.y), c, nBD) = IoTraits<IO>::from_f32(y);
   }
 }
 
@@ -262,6 +265,8 @@ cudaError_t launch(const DecodeParams& p, cudaStream_t stream) {
 }
 
 }  // namespace
+
+cudaError_t decode_check_read_and_clear(unsigned int* out) { return tu_check_read_and_clear(out); }
 
 cudaError_t state_update_launch(const DecodeParams& p, cudaStream_t stream) {
   return p.io_bf16 ? launch<__nv_bfloat16>(p, stream) : launch<float>(p, stream);

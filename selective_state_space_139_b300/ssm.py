@@ -6,15 +6,16 @@ library is missing or a tensor is not on a CUDA device, the call raises.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
-from typing import Optional, Tuple
+from typing import Iterator, Optional, Tuple
 
 import torch
 
 from . import build as _build
 
-SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_TIMEOUT = range(5)
+SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_TIMEOUT, SSM_ERR_CHECK = range(6)
 SSM_F32, SSM_BF16 = 0, 1
 ALGORITHMS = {"auto": 0, "single_pass": 1, "chunked": 2}
 DISCRETIZATIONS = {"delta_b": 0, "zoh": 1}
@@ -56,6 +57,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
     lib.ssm_abi_version.restype = i32
     lib.ssm_abi_version.argtypes = []
+    lib.ssm_checked_build.restype = i32
+    lib.ssm_checked_build.argtypes = []
     lib.ssm_status_string.restype = ctypes.c_char_p
     lib.ssm_status_string.argtypes = [i32]
     lib.ssm_last_error_message.restype = ctypes.c_char_p
@@ -75,6 +78,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ssm_selftest_bounded_wait.argtypes = [i32, i64, vp]
     lib.ssm_selftest_withhold_carry.restype = i32
     lib.ssm_selftest_withhold_carry.argtypes = [i32, i64]
+    lib.ssm_selftest_index_check.restype = i32
+    lib.ssm_selftest_index_check.argtypes = [vp]
     lib.ssm_scan_fwd_describe.restype = i32
     lib.ssm_scan_fwd_describe.argtypes = [i32, i32, i32, i64, i32, ctypes.POINTER(ScanOptions), ctypes.POINTER(ScanPlan)]
     lib.ssm_causal_conv1d_fwd.restype = i32
@@ -94,9 +99,28 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     return lib
 
 
+@contextlib.contextmanager
+def use_checked_library() -> Iterator[ctypes.CDLL]:
+    """Routes every call in the block through the checked debug build (libssm_b300_check.so).
+
+    Its kernels check each global index against the buffer's size; a failed check is reported by
+    ``device_status()`` as SSM_ERR_CHECK instead of touching memory outside the buffer.
+    """
+    global _lib
+    plain = load_library()
+    checked = load_library(_build.LIB_CHECK)
+    if checked.ssm_checked_build() != 1:
+        raise ImportError(f"{_build.LIB_CHECK} is not a checked build")
+    _lib = checked
+    try:
+        yield checked
+    finally:
+        _lib = plain
+
+
 def _status_name(s: int) -> str:
     return {0: "SSM_OK", 1: "SSM_ERR_INVALID_ARG", 2: "SSM_ERR_UNSUPPORTED", 3: "SSM_ERR_CUDA",
-            4: "SSM_ERR_TIMEOUT"}.get(s, f"status {s}")
+            4: "SSM_ERR_TIMEOUT", 5: "SSM_ERR_CHECK"}.get(s, f"status {s}")
 
 
 def _check(lib, status: int):

@@ -204,3 +204,19 @@ def test_ssd_state_update_rejects_bad_arguments_on_host(lib):
 def test_selftest_rejects_unknown_wait_kind_on_host(lib):
     assert lib.ssm_selftest_bounded_wait(2, 1000000, None) == ssm.SSM_ERR_INVALID_ARG
     assert lib.ssm_selftest_bounded_wait(-1, 1000000, None) == ssm.SSM_ERR_INVALID_ARG
+
+
+def test_checked_build_exports_the_same_entry_points(lib):
+    """libssm_b300_check.so (-DSSM_CHECK=1) is a drop-in for the ordinary library."""
+    build.build(checked=True)
+    chk = ssm.load_library(build.LIB_CHECK)
+    for n in _declared_functions():
+        assert hasattr(chk, n), f"{n} declared in ssm.h but not exported by the checked build"
+    assert lib.ssm_checked_build() == 0
+    assert chk.ssm_checked_build() == 1
+    assert chk.ssm_status_string(ssm.SSM_ERR_CHECK) == b"SSM_ERR_CHECK"
+
+
+def test_index_check_selftest_needs_the_checked_build(lib):
+    # the ordinary build has no checks to exercise: refused before any CUDA call
+    assert lib.ssm_selftest_index_check(None) == ssm.SSM_ERR_UNSUPPORTED

@@ -45,18 +45,22 @@ def test_conv1d_every_element(shape, dtype, with_state, silu):
     np.testing.assert_array_equal(to64(st_out).reshape(b * d, 3), rst)
 
 
-def test_conv1d_mamba28b_rows_sampled():
+def test_conv1d_mamba28b_every_element():
+    """The 2.8B-layer shape (4 x 5120 x 4096, bf16, with a carried-in state), every output element and
+    every returned state, in blocks of rows so that host memory stays bounded."""
     dev = _dev()
-    x, w, st = _inputs(4, 5120, 4096, torch.bfloat16, 3, True, dev)
+    b, d, L = 4, 5120, 4096
+    x, w, st = _inputs(b, d, L, torch.bfloat16, 3, True, dev)
     u, st_out = ssm.causal_conv1d_fwd(x, w, st)
     torch.cuda.synchronize()
-    rows = [(0, 0), (0, 5119), (3, 17), (2, 4096), (1, 2500), (3, 5119)]
-    bi = torch.tensor([r[0] for r in rows])
-    di = torch.tensor([r[1] for r in rows])
-    ru, rst = oracle.causal_conv1d(to64(x[bi, di]), to64(w[di]), to64(st[bi, di]))
-    assert max_rel_err(to64(u[bi, di]), ru) <= 1e-2
-    np.testing.assert_array_equal(to64(st_out[bi, di]), rst)
-    assert torch.isfinite(u).all()
+    worst = 0.0
+    for bb in range(b):
+        for d0 in range(0, d, 1280):
+            sl = slice(d0, d0 + 1280)
+            ru, rst = oracle.causal_conv1d(to64(x[bb, sl]), to64(w[sl]), to64(st[bb, sl]))
+            worst = max(worst, max_rel_err(to64(u[bb, sl]), ru))
+            np.testing.assert_array_equal(to64(st_out[bb, sl]), rst)
+    assert worst <= 1e-2, worst
 
 
 def test_conv_then_scan_then_decode_equals_one_prefill():

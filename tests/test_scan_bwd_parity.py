@@ -100,33 +100,25 @@ def test_backward_mamba130m_layer_full():
     _compare(g, _oracle(inp), TOL[torch.bfloat16])
 
 
-def test_backward_mamba2p8b_layer_sampled_dims():
+def test_backward_mamba2p8b_layer_full():
+    """Every output of the 2.8B-layer backward against the oracle, in the launch configuration the
+    benchmark times: du, dΔ, dz of every channel and step, the batch-summed dA, dD, dbias, and the
+    channel-summed dB, dC of every (batch row, state, step)."""
     dev = _dev()
     w = W.WORKLOADS["mamba2.8b-layer"]
     inp = W.make_scan_inputs(w, device=dev)
     inp["dy"] = W.make_cotangent(w.batch, w.dim, w.seqlen, inp["u"].dtype, w.seed, device=dev)
     g = _gpu(inp)
-    rng = np.random.default_rng(5)
-    dims = sorted({0, w.dim - 1, 127, 128} | set(int(d) for d in rng.integers(0, w.dim, 12)))
-    di = torch.as_tensor(dims)
-    bs = np.repeat(np.arange(w.batch), len(dims))
-    ds = np.tile(np.array(dims), w.batch)
-    bi_t, di_t = torch.as_tensor(bs), torch.as_tensor(ds)
-    rows = lambda t: to64(t[bi_t, di_t])
-    r = oracle.scan_backward_channels(rows(inp["u"]), rows(inp["delta"]), to64(inp["A"][di_t]), to64(inp["B"]),
-                                      to64(inp["C"]), bs, rows(inp["dy"]), D=to64(inp["D"][di_t]), z=rows(inp["z"]),
-                                      delta_bias=to64(inp["delta_bias"][di_t]))
+    r = _oracle(inp)
     tol = TOL[torch.bfloat16]
-    errs = {k: max_rel_err(to64(g[k][bi_t, di_t]), r[k]) for k in ("du", "ddelta", "dz")}
-    nd = len(dims)
-    errs["dA"] = max_rel_err(to64(g["dA"][di]), r["dA"].reshape(w.batch, nd, -1).sum(0))
-    errs["dD"] = max_rel_err(to64(g["dD"][di]), r["dD"].reshape(w.batch, nd).sum(0))
-    errs["ddelta_bias"] = max_rel_err(to64(g["ddelta_bias"][di]), r["ddelta_bias"].reshape(w.batch, nd).sum(0))
+    errs = {}
+    for k in KEYS:
+        if r.get(k) is None:
+            continue
+        errs[k] = max_rel_err(to64(g[k]), r[k])
+        r[k] = None   # bounded host memory: one full-size pair at a time
     bad = {k: e for k, e in errs.items() if not e <= tol}
     assert not bad, (bad, errs)
-    # the cross-channel sums are finite and of the expected size everywhere
-    for k in ("dB", "dC"):
-        assert torch.isfinite(g[k]).all(), k
 
 
 def test_backward_seqlen_zero_gives_zero_parameter_gradients():
