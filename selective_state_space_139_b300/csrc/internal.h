@@ -138,16 +138,8 @@ struct BwdParams {
   int io_bf16;
   int vec_io;             // L % 8 == 0 and every io row base 16-byte aligned
   int vec_red;            // dB, dC 16-byte aligned and L % 4 == 0 (vector atomics)
-  int vec_bc;             // L % 8 == 0 and B, C 16-byte aligned (16-byte loads of 8 steps of a B/C row)
 };
 
-// bfloat16-io backward (scan_bwd_bf16.cu): 128-channel tiles, the local forward, the carries and
-// the reverse pass; the accumulators (dA, dB, dC, dD, dbias) must be zero on entry.
-constexpr int kBwd16ChannelsPerCta = 128;
-constexpr int kBwd16CtasPerSm = 2;   // resident reverse-pass CTAs per SM (109 KB of shared memory each)
-cudaError_t bwd16_launch(const BwdParams& p, cudaStream_t stream);
-// The carries of the chunk aggregates (float), shared by both backward implementations.
-cudaError_t bwd_carry_launch_f32(const BwdParams& p, cudaStream_t stream);
 int bwd_segment_steps();
 int bwd_aggregate_floats();
 cudaError_t scan_bwd_launch(const BwdParams& p, cudaStream_t stream);
@@ -212,7 +204,6 @@ cudaError_t conv1d_check_read_and_clear(unsigned int* out);
 cudaError_t ssd_check_read_and_clear(unsigned int* out);
 cudaError_t ssd_decode_check_read_and_clear(unsigned int* out);
 cudaError_t bwd_check_read_and_clear(unsigned int* out);
-cudaError_t bwd16_check_read_and_clear(unsigned int* out);
 
 // Carry pass of the chunked algorithm over float carries (scan_fwd.cu).
 cudaError_t carry_launch_f32(const ScanParams& p, int nchunks, cudaStream_t stream);

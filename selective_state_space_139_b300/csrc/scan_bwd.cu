@@ -1001,11 +1001,6 @@ cudaError_t launch(const BwdParams& p, cudaStream_t stream) {
 
 int bwd_segment_steps() { return kSeg; }
 
-cudaError_t bwd_carry_launch_f32(const BwdParams& p, cudaStream_t stream) {
-  const int64_t carry_threads = static_cast<int64_t>(p.batch) * p.dim * kN;
-  bwd_carry_kernel<float><<<static_cast<unsigned>((carry_threads + 255) / 256), 256, 0, stream>>>(p);
-  return cudaGetLastError();
-}
 int bwd_aggregate_floats() { return kAgg; }
 
 cudaError_t scan_bwd_launch(const BwdParams& p, cudaStream_t stream) {

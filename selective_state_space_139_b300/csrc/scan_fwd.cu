@@ -564,7 +564,7 @@ cudaError_t read_and_clear_device_status(unsigned int* out, cudaStream_t stream)
   cudaError_t (*const readers[])(unsigned int*) = {general_check_read_and_clear, scaled_check_read_and_clear,
                                                     decode_check_read_and_clear,  conv1d_check_read_and_clear,
                                                     ssd_check_read_and_clear,     ssd_decode_check_read_and_clear,
-                                                    bwd_check_read_and_clear,     bwd16_check_read_and_clear};
+                                                    bwd_check_read_and_clear};
   for (auto* r : readers) {
     unsigned int c = 0;
     e = r(&c);

@@ -602,33 +602,12 @@ struct BwdLayout {
   size_t ckpt = 0, ckpt_s = 0, agg = 0, acc_dA = 0, acc_dB = 0, acc_dC = 0, acc_dD = 0, acc_dbias = 0, total = 0;
   int64_t chunk_len = 0;
   int nchunks = 1;
-  bool bf16 = false;
 };
 
 // Time chunks: enough (channel group, chunk) tiles for several waves of resident CTAs, chunks a
 // multiple of the segment length and at least 64 steps.
 void bwd_chunks(int batch, int dim, int64_t seqlen, BwdLayout* l) {
   const int K = ssm::bwd_segment_steps();
-  if (l->bf16) {
-    // bfloat16 io: 128-channel tiles, two resident reverse-pass CTAs per SM.  The chunk count is the
-    // one whose wave count times the chunk length (plus a per-tile overhead of 24 steps) is least.
-    const int64_t groups = static_cast<int64_t>(batch) * ((dim + ssm::kBwd16ChannelsPerCta - 1) / ssm::kBwd16ChannelsPerCta);
-    const int64_t slots = static_cast<int64_t>(ssm::kBwd16CtasPerSm) * sm_count();
-    const int64_t max_nch = std::max<int64_t>(1, std::min<int64_t>(4096, seqlen / 64));
-    int64_t best_chunk = round_up(static_cast<size_t>(seqlen), K), best_cost = -1;
-    for (int64_t nch = 1; nch <= max_nch; ++nch) {
-      const int64_t chunk = static_cast<int64_t>(round_up(static_cast<size_t>((seqlen + nch - 1) / nch), K));
-      const int64_t n = (seqlen + chunk - 1) / chunk;
-      const int64_t cost = ((groups * n + slots - 1) / slots) * (chunk + 24);
-      if (best_cost < 0 || cost < best_cost) {
-        best_cost = cost;
-        best_chunk = chunk;
-      }
-    }
-    l->chunk_len = std::max<int64_t>(best_chunk, K);
-    l->nchunks = static_cast<int>((seqlen + l->chunk_len - 1) / l->chunk_len);
-    return;
-  }
   const int64_t groups = static_cast<int64_t>(batch) * ((dim + kChannelsPerCta - 1) / kChannelsPerCta);
   const int64_t target_tiles = static_cast<int64_t>(SSM_BWD_TILES_PER_SM) * sm_count();
   int64_t nch = std::max<int64_t>(1, (target_tiles + groups - 1) / groups);
@@ -645,7 +624,6 @@ void bwd_chunks(int batch, int dim, int64_t seqlen, BwdLayout* l) {
 BwdLayout bwd_layout(int batch, int dim, int dstate, int64_t seqlen, ssm_dtype io) {
   BwdLayout l;
   if (seqlen <= 0) return l;
-  l.bf16 = false;   // the 128-channel bf16 kernels are not dispatched yet
   bwd_chunks(batch, dim, seqlen, &l);
   const size_t ce = io == SSM_BF16 ? sizeof(float) : sizeof(double);
   const int K = ssm::bwd_segment_steps();
@@ -755,7 +733,6 @@ ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A, const 
     if (q && !aligned(q, 16)) vec_io = false;
   p.vec_io = vec_io;
   p.vec_red = seqlen % 4 == 0 && aligned(dB, 16) && aligned(dC, 16);
-  p.vec_bc = seqlen % 8 == 0 && aligned(B, 16) && aligned(C, 16);
   char* ws = static_cast<char*>(workspace);
   p.ckpt = ws + lay.ckpt;
   p.ckpt_s = ws + lay.ckpt_s;
