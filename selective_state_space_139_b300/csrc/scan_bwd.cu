@@ -128,9 +128,10 @@ struct SegRaw {
 
 // vec: the row segment is 16-byte aligned and complete; otherwise scalar loads (zeros past nk)
 template <typename IO>
-__device__ __forceinline__ void fetch_one(const void* base, int64_t off, int nk, bool vec, uint4 (&w)[SegRaw<IO>::kW]) {
+__device__ __forceinline__ void fetch_one(const void* base, int64_t off, int nk, bool vec, uint4 (&w)[SegRaw<IO>::kW],
+                                          int64_t n_total) {
   constexpr int kW = SegRaw<IO>::kW;
-  const IO* p = static_cast<const IO*>(base) + off;
+  const IO* p = checked(static_cast<const IO*>(base), off, n_total, nk);   // the segment's nk elements
   if (vec && nk == kSeg) {
 #pragma unroll
     for (int i = 0; i < kW; ++i) w[i] = __ldg(reinterpret_cast<const uint4*>(p) + i);
@@ -145,10 +146,11 @@ __device__ __forceinline__ void fetch_one(const void* base, int64_t off, int nk,
 
 template <typename IO>
 __device__ __forceinline__ void fetch_seg(const BwdParams& p, int64_t off, int nk, SegRaw<IO>& r) {
-  fetch_one<IO>(p.u, off, nk, p.vec_io, r.w[0]);
-  fetch_one<IO>(p.delta, off, nk, p.vec_io, r.w[1]);
-  fetch_one<IO>(p.dy, off, nk, p.vec_io, r.w[2]);
-  if (p.z) fetch_one<IO>(p.z, off, nk, p.vec_io, r.w[3]);
+  const int64_t n_io = static_cast<int64_t>(p.batch) * p.dim * p.L;
+  fetch_one<IO>(p.u, off, nk, p.vec_io, r.w[0], n_io);
+  fetch_one<IO>(p.delta, off, nk, p.vec_io, r.w[1], n_io);
+  fetch_one<IO>(p.dy, off, nk, p.vec_io, r.w[2], n_io);
+  if (p.z) fetch_one<IO>(p.z, off, nk, p.vec_io, r.w[3], n_io);
 }
 
 template <typename IO, typename CT>
@@ -170,8 +172,8 @@ __device__ __forceinline__ void unpack_one(const uint4 (&w)[SegRaw<IO>::kW], CT 
 }
 
 template <typename IO, typename CT>
-__device__ __forceinline__ void store_seg(void* base, int64_t off, int nk, bool vec, const CT (&v)[kSeg]) {
-  IO* p = static_cast<IO*>(base) + off;
+__device__ __forceinline__ void store_seg(void* base, int64_t off, int nk, bool vec, const CT (&v)[kSeg], int64_t n_total) {
+  IO* p = checked(static_cast<IO*>(base), off, n_total, nk);   // the segment's nk elements
   float f[kSeg];
 #pragma unroll
   for (int k = 0; k < kSeg; ++k) f[k] = static_cast<float>(v[k]);
@@ -202,9 +204,10 @@ __device__ __forceinline__ void fetch_bc(const BwdParams& p, int b, int64_t t0, 
     uint32_t v = 0u;
     if (k < nk && n < p.N) {
       const int64_t idx = (static_cast<int64_t>(b) * p.N + n) * p.L + t0 + k;
+      const int64_t nbc = static_cast<int64_t>(p.batch) * p.N * p.L;
       const void* src = arr ? p.C : p.B;
-      v = p.io_bf16 ? static_cast<uint32_t>(static_cast<const unsigned short*>(src)[idx])
-                    : static_cast<const uint32_t*>(src)[idx];
+      v = p.io_bf16 ? static_cast<uint32_t>(*checked(static_cast<const unsigned short*>(src), idx, nbc))
+                    : *checked(static_cast<const uint32_t*>(src), idx, nbc);
     }
     r[j] = v;
   }
@@ -252,6 +255,24 @@ struct Tile {
   int64_t ag;            // index of the (row, chunk) aggregate
 };
 
+// element counts of the buffers, for the index checks of the checked build
+struct Sizes {
+  int64_t nA, nDim, nIO, nBC, nCk, nCs, nAgg;
+};
+__device__ __forceinline__ Sizes sizes_of(const BwdParams& p) {
+  Sizes z{};
+  if (!SSM_CHECK) return z;   // the ordinary build checks nothing
+  const int64_t rows = static_cast<int64_t>(p.batch) * p.dim, nseg = (p.L + kSeg - 1) / kSeg;
+  z.nA = static_cast<int64_t>(p.dim) * p.N;
+  z.nDim = p.dim;
+  z.nIO = rows * p.L;
+  z.nBC = static_cast<int64_t>(p.batch) * p.N * p.L;
+  z.nCk = rows * nseg * kN;
+  z.nCs = rows * nseg;
+  z.nAgg = rows * p.nchunks * kAgg;
+  return z;
+}
+
 __device__ __forceinline__ Tile tile_of(const BwdParams& p) {
   Tile t;
   t.b = blockIdx.y;
@@ -273,10 +294,11 @@ __global__ void __launch_bounds__(kThreads, sizeof(CT) == 4 ? SSM_BWD_FWD_MINB :
   using P = Pair<CT>;
   __shared__ __align__(16) float bc_buf[2][kSeg * 32];
   const Tile T = tile_of(p);
+  const Sizes Z = sizes_of(p);
   const int64_t nseg = (p.L + kSeg - 1) / kSeg;
   P A2[kP], h[kP], E[kP], G[kP];
   {
-    const float* Ad = p.A + static_cast<int64_t>(T.dd) * p.N;
+    const float* Ad = checked(p.A, static_cast<int64_t>(T.dd) * p.N, Z.nA, p.N);
 #pragma unroll
     for (int j = 0; j < kP; ++j) {
       const CT a0 = 2 * j < p.N ? static_cast<CT>(Ad[2 * j]) : static_cast<CT>(0);
@@ -287,10 +309,10 @@ __global__ void __launch_bounds__(kThreads, sizeof(CT) == 4 ? SSM_BWD_FWD_MINB :
       G[j] = P::splat(0);
     }
   }
-  const CT bias = p.bias ? p.bias[T.dd] : 0.0f;
+  const CT bias = p.bias ? *checked(p.bias, T.dd, Z.nDim) : 0.0f;
   CT S = 0;
-  CT* ck = static_cast<CT*>(p.ckpt) + T.row * nseg * kN;
-  CT* cs = static_cast<CT*>(p.ckpt_s) + T.row * nseg;
+  CT* const ck = static_cast<CT*>(p.ckpt) + T.row * nseg * kN;
+  CT* const cs = static_cast<CT*>(p.ckpt_s) + T.row * nseg;
   auto seg_len = [&](int64_t t0) { return static_cast<int>(T.c1 - t0 < kSeg ? T.c1 - t0 : kSeg); };
   SegRaw<IO> raw;
   uint32_t bcr[2];
@@ -314,8 +336,8 @@ __global__ void __launch_bounds__(kThreads, sizeof(CT) == 4 ? SSM_BWD_FWD_MINB :
     }
     if (T.valid) {
       const int64_t s = t0 / kSeg;
-      store_ckpt(ck + s * kN, h);
-      cs[s] = S;
+      store_ckpt(checked(ck, s * kN, Z.nCk - T.row * nseg * kN, kN), h);
+      *checked(cs, s, Z.nCs - T.row * nseg) = S;
     }
     const f2* bc2 = reinterpret_cast<const f2*>(bc_buf[buf]);   // [k][B pairs 0..7 | C pairs 0..7]
 #pragma unroll
@@ -339,15 +361,18 @@ __global__ void __launch_bounds__(kThreads, sizeof(CT) == 4 ? SSM_BWD_FWD_MINB :
     buf ^= 1;
   }
   if (T.valid) {
-    CT* ag = static_cast<CT*>(p.agg) + T.ag;
+    CT* const base = static_cast<CT*>(p.agg);
+    CT* const aq = checked(base, T.ag, Z.nAgg, kN);
+    CT* const ap = checked(base, T.ag + kN, Z.nAgg, kN);
+    CT* const agg = checked(base, T.ag + 2 * kN, Z.nAgg, kN);
 #pragma unroll
     for (int j = 0; j < kP; ++j) {
-      ag[2 * j] = h[j].lo();
-      ag[2 * j + 1] = h[j].hi();
-      ag[kN + 2 * j] = E[j].lo();
-      ag[kN + 2 * j + 1] = E[j].hi();
-      ag[2 * kN + 2 * j] = G[j].lo();
-      ag[2 * kN + 2 * j + 1] = G[j].hi();
+      aq[2 * j] = h[j].lo();
+      aq[2 * j + 1] = h[j].hi();
+      ap[2 * j] = E[j].lo();
+      ap[2 * j + 1] = E[j].hi();
+      agg[2 * j] = G[j].lo();
+      agg[2 * j + 1] = G[j].hi();
     }
   }
 }
@@ -368,10 +393,11 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_fwd2_kernel(const BwdParams p
   const int64_t c0 = static_cast<int64_t>(blockIdx.z) * p.chunk_len;
   const int64_t c1 = c0 + p.chunk_len < p.L ? c0 + p.chunk_len : p.L;
   const int64_t nseg = (p.L + kSeg - 1) / kSeg;
+  const Sizes Z = sizes_of(p);
   const int n0 = 8 * pl;
   P A2[4], h[4], E[4], G[4];
   {
-    const float* Ad = p.A + static_cast<int64_t>(dd) * p.N;
+    const float* Ad = checked(p.A, static_cast<int64_t>(dd) * p.N, Z.nA, p.N);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int n = n0 + 2 * j;
@@ -381,10 +407,11 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_fwd2_kernel(const BwdParams p
       G[j] = P::splat(0.0f);
     }
   }
-  const float bias = p.bias ? p.bias[dd] : 0.0f;
+  const float bias = p.bias ? *checked(p.bias, dd, Z.nDim) : 0.0f;
   float S = 0.0f;
-  float* ck = static_cast<float*>(p.ckpt) + row * nseg * kN + n0;
-  float* cs = static_cast<float*>(p.ckpt_s) + row * nseg;
+  const int64_t ck_row = row * nseg * kN + n0, cs_row = row * nseg;
+  float* const ck = static_cast<float*>(p.ckpt) + ck_row;   // this lane's checkpoint row
+  float* const cs = static_cast<float*>(p.ckpt_s) + cs_row;
   auto seg_len = [&](int64_t t0) { return static_cast<int>(c1 - t0 < kSeg ? c1 - t0 : kSeg); };
   SegRaw<IO> raw;
   uint32_t bcr[2];
@@ -408,9 +435,10 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_fwd2_kernel(const BwdParams p
     }
     if (valid) {
       const int64_t sgi = t0 / kSeg;
-      reinterpret_cast<float4*>(ck + sgi * kN)[0] = make_float4(h[0].lo(), h[0].hi(), h[1].lo(), h[1].hi());
-      reinterpret_cast<float4*>(ck + sgi * kN)[1] = make_float4(h[2].lo(), h[2].hi(), h[3].lo(), h[3].hi());
-      if (pl == 0) cs[sgi] = S;
+      float4* const cq = reinterpret_cast<float4*>(checked(ck, sgi * kN, Z.nCk - ck_row, 8));
+      cq[0] = make_float4(h[0].lo(), h[0].hi(), h[1].lo(), h[1].hi());
+      cq[1] = make_float4(h[2].lo(), h[2].hi(), h[3].lo(), h[3].hi());
+      if (pl == 0) *checked(cs, sgi, Z.nCs - cs_row) = S;
     }
     const f2* bc2 = reinterpret_cast<const f2*>(bc_buf[buf]);
 #pragma unroll
@@ -435,15 +463,19 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_fwd2_kernel(const BwdParams p
     buf ^= 1;
   }
   if (valid) {
-    float* ag = static_cast<float*>(p.agg) + (row * p.nchunks + blockIdx.z) * kAgg + n0;
+    float* const base = static_cast<float*>(p.agg);
+    const int64_t a0 = (row * p.nchunks + blockIdx.z) * kAgg + n0;
+    float* const aq = checked(base, a0, Z.nAgg, 8);
+    float* const ap = checked(base, a0 + kN, Z.nAgg, 8);
+    float* const agg = checked(base, a0 + 2 * kN, Z.nAgg, 8);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      ag[2 * j] = h[j].lo();
-      ag[2 * j + 1] = h[j].hi();
-      ag[kN + 2 * j] = E[j].lo();
-      ag[kN + 2 * j + 1] = E[j].hi();
-      ag[2 * kN + 2 * j] = G[j].lo();
-      ag[2 * kN + 2 * j + 1] = G[j].hi();
+      aq[2 * j] = h[j].lo();
+      aq[2 * j + 1] = h[j].hi();
+      ap[2 * j] = E[j].lo();
+      ap[2 * j + 1] = E[j].hi();
+      agg[2 * j] = G[j].lo();
+      agg[2 * j + 1] = G[j].hi();
     }
   }
 }
@@ -459,21 +491,24 @@ __global__ void bwd_carry_kernel(const BwdParams p) {
   if (i >= rows * kN) return;
   const int64_t row = i / kN;
   const int n = static_cast<int>(i % kN);
-  CT* ag = static_cast<CT*>(p.agg) + row * p.nchunks * kAgg + n;
+  const Sizes Z = sizes_of(p);
+  CT* const base = static_cast<CT*>(p.agg);
+  const int64_t a0 = row * p.nchunks * kAgg + n;
+  auto ag = [&](int64_t off) -> CT& { return *checked(base, a0 + off, Z.nAgg); };
   CT h = 0;
   for (int c0 = 0; c0 < p.nchunks; c0 += kB8) {
     CT q[kB8], P[kB8];
 #pragma unroll
     for (int k = 0; k < kB8; ++k) {
       const int c = c0 + k;
-      q[k] = c < p.nchunks ? ag[c * kAgg] : CT(0);
-      P[k] = c < p.nchunks ? ag[c * kAgg + kN] : CT(0);
+      q[k] = c < p.nchunks ? ag(static_cast<int64_t>(c) * kAgg) : CT(0);
+      P[k] = c < p.nchunks ? ag(static_cast<int64_t>(c) * kAgg + kN) : CT(0);
     }
 #pragma unroll
     for (int k = 0; k < kB8; ++k) {
       const int c = c0 + k;
       if (c < p.nchunks) {
-        ag[c * kAgg] = h;
+        ag(static_cast<int64_t>(c) * kAgg) = h;
         h = P[k] * h + q[k];
       }
     }
@@ -484,14 +519,14 @@ __global__ void bwd_carry_kernel(const BwdParams p) {
 #pragma unroll
     for (int k = 0; k < kB8; ++k) {
       const int c = c0 - k;
-      gc[k] = c >= 0 ? ag[c * kAgg + 2 * kN] : CT(0);
-      P[k] = c >= 0 ? ag[c * kAgg + kN] : CT(0);
+      gc[k] = c >= 0 ? ag(static_cast<int64_t>(c) * kAgg + 2 * kN) : CT(0);
+      P[k] = c >= 0 ? ag(static_cast<int64_t>(c) * kAgg + kN) : CT(0);
     }
 #pragma unroll
     for (int k = 0; k < kB8; ++k) {
       const int c = c0 - k;
       if (c >= 0) {
-        ag[c * kAgg + 2 * kN] = g;
+        ag(static_cast<int64_t>(c) * kAgg + 2 * kN) = g;
         g = gc[k] + P[k] * g;
       }
     }
@@ -534,26 +569,29 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_rev_kernel(const BwdParams
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const Tile T = tile_of(p);
+  const Sizes Z = sizes_of(p);
   const int64_t nseg = (p.L + kSeg - 1) / kSeg;
   P A2[kP], dh[kP], dA[kP];
   {
-    const CT* ag = static_cast<const CT*>(p.agg) + T.ag;
-    const float* Ad = p.A + static_cast<int64_t>(T.dd) * p.N;
+    const CT* const agb = static_cast<const CT*>(p.agg);
+    const CT* const aq = checked(agb, T.ag, Z.nAgg, kN);
+    const CT* const agd = checked(agb, T.ag + 2 * kN, Z.nAgg, kN);
+    const float* Ad = checked(p.A, static_cast<int64_t>(T.dd) * p.N, Z.nA, p.N);
 #pragma unroll
     for (int j = 0; j < kP; ++j) {
       const CT a0 = 2 * j < p.N ? static_cast<CT>(Ad[2 * j]) : static_cast<CT>(0);
       const CT a1 = 2 * j + 1 < p.N ? static_cast<CT>(Ad[2 * j + 1]) : static_cast<CT>(0);
       A2[j] = P::make(a0 * P::kExpScale, a1 * P::kExpScale);
-      hs_s[j * kThreads + tid] = P::make(ag[2 * j], ag[2 * j + 1]);
-      dh[j] = T.valid ? P::make(ag[2 * kN + 2 * j], ag[2 * kN + 2 * j + 1]) : P::splat(0);
+      hs_s[j * kThreads + tid] = P::make(aq[2 * j], aq[2 * j + 1]);
+      dh[j] = T.valid ? P::make(agd[2 * j], agd[2 * j + 1]) : P::splat(0);
       dA[j] = P::splat(0);
     }
   }
-  const CT bias = p.bias ? p.bias[T.dd] : 0.0f;
-  const CT Dd = p.D ? p.D[T.dd] : 0.0f;
+  const CT bias = p.bias ? *checked(p.bias, T.dd, Z.nDim) : 0.0f;
+  const CT Dd = p.D ? *checked(p.D, T.dd, Z.nDim) : 0.0f;
   CT dD = 0, dbias = 0;
-  const CT* ck = static_cast<const CT*>(p.ckpt) + T.row * nseg * kN;
-  const CT* cs = static_cast<const CT*>(p.ckpt_s) + T.row * nseg;
+  const CT* const ck = static_cast<const CT*>(p.ckpt) + T.row * nseg * kN;
+  const CT* const cs = static_cast<const CT*>(p.ckpt_s) + T.row * nseg;
   auto seg_len = [&](int64_t t0) { return static_cast<int>(T.c1 - t0 < kSeg ? T.c1 - t0 : kSeg); };
   // adds the CTA's dB/dC partials of the segment at t0 (buffer rb) to global memory
   auto flush_red = [&](const CT* rb, int64_t t0, int nk) {
@@ -566,7 +604,8 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_rev_kernel(const BwdParams
     for (int i = 0; i < 4; ++i)
       s4[i] = (rb[(0 * kSeg + k0 + i) * 32 + col] + rb[(1 * kSeg + k0 + i) * 32 + col]) +
               (rb[(2 * kSeg + k0 + i) * 32 + col] + rb[(3 * kSeg + k0 + i) * 32 + col]);
-    CT* dst = static_cast<CT*>(arr ? p.acc_dC : p.acc_dB) + (static_cast<int64_t>(T.b) * p.N + n) * p.L + t0 + k0;
+    CT* dst = checked(static_cast<CT*>(arr ? p.acc_dC : p.acc_dB), (static_cast<int64_t>(T.b) * p.N + n) * p.L + t0 + k0,
+                      Z.nBC, nk - k0 < 4 ? nk - k0 : 4);
     if constexpr (sizeof(CT) == 4) {
       if (p.vec_red && k0 + 4 <= nk) {
         red_add_v4(dst, s4[0], s4[1], s4[2], s4[3]);
@@ -583,8 +622,8 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_rev_kernel(const BwdParams
   CT ckr[kN], ckS;
   auto fetch_ck = [&](int64_t t0) {
     const int64_t s = t0 / kSeg;
-    load_ckpt(ck + s * kN, ckr);
-    ckS = cs[s];
+    load_ckpt(checked(ck, s * kN, Z.nCk - T.row * nseg * kN, kN), ckr);
+    ckS = *checked(cs, s, Z.nCs - T.row * nseg);
   };
   fetch_seg<IO>(p, T.row * p.L + last, seg_len(last), raw);
   fetch_bc(p, T.b, last, seg_len(last), bcr);
@@ -654,7 +693,7 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_rev_kernel(const BwdParams
         dl[k] = sg[k] = ds[k] = 0;
       }
     }
-    if (T.valid && p.z) store_seg<IO, CT>(p.dz, off, nk, p.vec_io, gdz);
+    if (T.valid && p.z) store_seg<IO, CT>(p.dz, off, nk, p.vec_io, gdz, Z.nIO);
     // backward over the segment's steps
     CT gdu[kSeg], gdd[kSeg];
 #pragma unroll
@@ -698,8 +737,8 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_rev_kernel(const BwdParams
       }
     }
     if (T.valid) {
-      store_seg<IO, CT>(p.du, off, nk, p.vec_io, gdu);
-      store_seg<IO, CT>(p.ddelta, off, nk, p.vec_io, gdd);
+      store_seg<IO, CT>(p.du, off, nk, p.vec_io, gdu, Z.nIO);
+      store_seg<IO, CT>(p.ddelta, off, nk, p.vec_io, gdd, Z.nIO);
     }
     if (more) store_bc(bc_base + (buf ^ 1) * (kSeg * 32), bcr, p.io_bf16);
     __syncthreads();
@@ -709,14 +748,14 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_rev_kernel(const BwdParams
   }
   if (pend_t0 >= 0) flush_red(red_base + (buf ^ 1) * (4 * kSeg * 32), pend_t0, pend_nk);
   if (T.valid) {
-    CT* accA = static_cast<CT*>(p.acc_dA) + static_cast<int64_t>(T.d) * p.N;
+    CT* accA = checked(static_cast<CT*>(p.acc_dA), static_cast<int64_t>(T.d) * p.N, Z.nA, p.N);
 #pragma unroll
     for (int j = 0; j < kP; ++j) {
       if (2 * j < p.N) atomicAdd(accA + 2 * j, dA[j].lo());
       if (2 * j + 1 < p.N) atomicAdd(accA + 2 * j + 1, dA[j].hi());
     }
-    if (p.acc_dD) atomicAdd(static_cast<CT*>(p.acc_dD) + T.d, dD);
-    if (p.acc_dbias) atomicAdd(static_cast<CT*>(p.acc_dbias) + T.d, dbias);
+    if (p.acc_dD) atomicAdd(checked(static_cast<CT*>(p.acc_dD), T.d, Z.nDim), dD);
+    if (p.acc_dbias) atomicAdd(checked(static_cast<CT*>(p.acc_dbias), T.d, Z.nDim), dbias);
   }
 }
 
@@ -757,26 +796,31 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
   const int64_t c1 = c0 + p.chunk_len < p.L ? c0 + p.chunk_len : p.L;
   const int64_t nseg = (p.L + kSeg - 1) / kSeg;
   const int n0 = 8 * pl;                        // first state of this lane
+  const Sizes Z = sizes_of(p);
   P A2[kP2], dh[kP2], dA[kP2];
   {
-    const float* ag = static_cast<const float*>(p.agg) + (row * p.nchunks + blockIdx.z) * kAgg;
-    const float* Ad = p.A + static_cast<int64_t>(dd) * p.N;
+    const float* const agb = static_cast<const float*>(p.agg);
+    const int64_t a0i = (row * p.nchunks + blockIdx.z) * kAgg;
+    const float* const aq = checked(agb, a0i, Z.nAgg, kN);
+    const float* const agd = checked(agb, a0i + 2 * kN, Z.nAgg, kN);
+    const float* Ad = checked(p.A, static_cast<int64_t>(dd) * p.N, Z.nA, p.N);
 #pragma unroll
     for (int j = 0; j < kP2; ++j) {
       const int n = n0 + 2 * j;
       const float a0 = n < p.N ? Ad[n] : 0.0f;
       const float a1 = n + 1 < p.N ? Ad[n + 1] : 0.0f;
       A2[j] = P::make(a0 * kLog2e, a1 * kLog2e);
-      hs_s[j * kThreads + tid] = P::make(ag[n], ag[n + 1]);
-      dh[j] = valid ? P::make(ag[2 * kN + n], ag[2 * kN + n + 1]) : P::splat(0.0f);
+      hs_s[j * kThreads + tid] = P::make(aq[n], aq[n + 1]);
+      dh[j] = valid ? P::make(agd[n], agd[n + 1]) : P::splat(0.0f);
       dA[j] = P::splat(0.0f);
     }
   }
-  const float bias = p.bias ? p.bias[dd] : 0.0f;
-  const float Dd = p.D ? p.D[dd] : 0.0f;
+  const float bias = p.bias ? *checked(p.bias, dd, Z.nDim) : 0.0f;
+  const float Dd = p.D ? *checked(p.D, dd, Z.nDim) : 0.0f;
   float dD = 0.0f, dbias = 0.0f;
-  const float* ck = static_cast<const float*>(p.ckpt) + row * nseg * kN + n0;
-  const float* cs = static_cast<const float*>(p.ckpt_s) + row * nseg;
+  const int64_t ck_row = row * nseg * kN + n0, cs_row = row * nseg;
+  const float* const ck = static_cast<const float*>(p.ckpt) + ck_row;   // this lane's checkpoint row
+  const float* const cs = static_cast<const float*>(p.ckpt_s) + cs_row;
   auto seg_len = [&](int64_t t0) { return static_cast<int>(c1 - t0 < kSeg ? c1 - t0 : kSeg); };
   auto flush_red = [&](const float* rb, int64_t t0, int nk) {
     if (tid >= 64) return;
@@ -788,7 +832,8 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
     for (int i = 0; i < 4; ++i)
       s4[i] = (rb[(0 * kSeg + k0 + i) * 32 + col] + rb[(1 * kSeg + k0 + i) * 32 + col]) +
               (rb[(2 * kSeg + k0 + i) * 32 + col] + rb[(3 * kSeg + k0 + i) * 32 + col]);
-    float* dst = static_cast<float*>(arr ? p.acc_dC : p.acc_dB) + (static_cast<int64_t>(b) * p.N + n) * p.L + t0 + k0;
+    float* dst = checked(static_cast<float*>(arr ? p.acc_dC : p.acc_dB), (static_cast<int64_t>(b) * p.N + n) * p.L + t0 + k0,
+                         Z.nBC, nk - k0 < 4 ? nk - k0 : 4);
     if (p.vec_red && k0 + 4 <= nk) {
       red_add_v4(dst, s4[0], s4[1], s4[2], s4[3]);
       return;
@@ -804,9 +849,10 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
   float ckS;
   auto fetch_ck = [&](int64_t t0) {
     const int64_t sgi = t0 / kSeg;
-    ckr0 = __ldg(reinterpret_cast<const float4*>(ck + sgi * kN));
-    ckr1 = __ldg(reinterpret_cast<const float4*>(ck + sgi * kN) + 1);
-    ckS = cs[sgi];
+    const float4* const cq = reinterpret_cast<const float4*>(checked(ck, sgi * kN, Z.nCk - ck_row, 8));
+    ckr0 = __ldg(cq);
+    ckr1 = __ldg(cq + 1);
+    ckS = *checked(cs, sgi, Z.nCs - cs_row);
   };
   fetch_seg<IO>(p, row * p.L + last, seg_len(last), raw);
   fetch_bc(p, b, last, seg_len(last), bcr);
@@ -880,7 +926,7 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
         // keep the partner exchange uniform: the partner lane runs the same k with the same nk
       }
     }
-    if (valid && p.z && pl == 1) store_seg<IO, float>(p.dz, off, nk, p.vec_io, gdz);
+    if (valid && p.z && pl == 1) store_seg<IO, float>(p.dz, off, nk, p.vec_io, gdz, Z.nIO);
     float gdu[kSeg], gdd[kSeg];
 #pragma unroll
     for (int k = kSeg - 1; k >= 0; --k) {
@@ -934,8 +980,8 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
       }
     }
     if (valid && pl == 0) {
-      store_seg<IO, float>(p.du, off, nk, p.vec_io, gdu);
-      store_seg<IO, float>(p.ddelta, off, nk, p.vec_io, gdd);
+      store_seg<IO, float>(p.du, off, nk, p.vec_io, gdu, Z.nIO);
+      store_seg<IO, float>(p.ddelta, off, nk, p.vec_io, gdd, Z.nIO);
     }
     if (more) store_bc(bc_base + (buf ^ 1) * (kSeg * 32), bcr, p.io_bf16);
     __syncthreads();
@@ -945,7 +991,7 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
   }
   if (pend_t0 >= 0) flush_red(red_base + (buf ^ 1) * (4 * kSeg * 32), pend_t0, pend_nk);
   if (valid) {
-    float* accA = static_cast<float*>(p.acc_dA) + static_cast<int64_t>(d) * p.N;
+    float* accA = checked(static_cast<float*>(p.acc_dA), static_cast<int64_t>(d) * p.N, Z.nA, p.N);
 #pragma unroll
     for (int j = 0; j < kP2; ++j) {
       const int n = n0 + 2 * j;
@@ -953,8 +999,8 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
       if (n + 1 < p.N) atomicAdd(accA + n + 1, dA[j].hi());
     }
     if (pl == 0) {
-      if (p.acc_dD) atomicAdd(static_cast<float*>(p.acc_dD) + d, dD);
-      if (p.acc_dbias) atomicAdd(static_cast<float*>(p.acc_dbias) + d, dbias);
+      if (p.acc_dD) atomicAdd(checked(static_cast<float*>(p.acc_dD), d, Z.nDim), dD);
+      if (p.acc_dbias) atomicAdd(checked(static_cast<float*>(p.acc_dbias), d, Z.nDim), dbias);
     }
   }
 }
