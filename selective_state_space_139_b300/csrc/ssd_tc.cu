@@ -146,7 +146,9 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
   __shared__ uint32_t tmem_slot;
   __shared__ __align__(16) float s_dl[kQ];
   __shared__ __align__(16) float s_cum[kQ];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned tile base, derived by pointer arithmetic on the shared array so that the compiler
+  // keeps shared-space loads and stores (an integer round trip would make them generic)
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(sm);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int h = blockIdx.x, b = blockIdx.y;
@@ -210,22 +212,31 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
 
   // tile loaders (rows past L are zero-filled); each tile of chunk c + 1 is requested as soon as the
   // tensor cores and the threads are done with that tile of chunk c
+  // Each thread's rows and 16-byte columns of the tile loads are the same in every chunk: B/C rows
+  // bc_r0 + 16k (k < 4) at column bc_q, x rows x_r0 + 32k (k < 2) at column x_q.  Row r0 + 16k of a
+  // swizzled tile sits 2048k bytes after row r0 (the swizzle depends on r & 7 only), so the shared
+  // offsets are constants plus immediates and the global index advances by a fixed stride.  Rows past
+  // L are zero-filled from a valid address (step 0 of the sequence).
+  const int bc_r0 = tid >> 4, bc_q = tid & 15, x_r0 = tid >> 3, x_q = tid & 7;
+  const uint32_t bc_dst = static_cast<uint32_t>((bc_q >> 3) * (kQ * 128)) + sw_chunk(bc_r0, bc_q & 7);
+  const uint32_t x_dst = TcSmem::kX + sw_chunk(x_r0, x_q);
+  const int64_t bc_step = static_cast<int64_t>(p.ngroups) * kNs, x_step = static_cast<int64_t>(p.nheads) * kHd;
+  const int64_t bc_col = (static_cast<int64_t>(b) * L * p.ngroups + grp) * kNs + bc_q * 8;   // step 0
+  const int64_t x_col = (static_cast<int64_t>(b) * L * p.nheads + h) * kHd + x_q * 8;
   auto load_bc = [&](int64_t t0, int off, const __nv_bfloat16* src_base) {
-    for (int i = tid; i < kQ * 16; i += kThreads) {
-      const int r = i >> 4, q = i & 15;
-      const bool in = t0 + r < L;
-      const int64_t row = (static_cast<int64_t>(b) * L + (in ? t0 + r : 0)) * p.ngroups + grp;
-      cp_async16(sb + off + (q >> 3) * (kQ * 128) + sw_chunk(r, q & 7), checked(src_base, row * kNs + q * 8, nBC, 8),
-                 in ? 16 : 0);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t r = t0 + bc_r0 + 16 * k;
+      const bool in = r < L;
+      cp_async16(sb + off + bc_dst + 2048 * k, checked(src_base, bc_col + (in ? r : 0) * bc_step, nBC, 8), in ? 16 : 0);
     }
   };
   auto load_x = [&](int64_t t0) {
-    for (int i = tid; i < kQ * 8; i += kThreads) {
-      const int r = i >> 3, q = i & 7;
-      const bool in = t0 + r < L;
-      const __nv_bfloat16* src =
-          checked(xg, ((static_cast<int64_t>(b) * L + (in ? t0 + r : 0)) * p.nheads + h) * kHd + q * 8, nX, 8);
-      cp_async16(sb + TcSmem::kX + sw_chunk(r, q), src, in ? 16 : 0);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int64_t r = t0 + x_r0 + 32 * k;
+      const bool in = r < L;
+      cp_async16(sb + x_dst + 4096 * k, checked(xg, x_col + (in ? r : 0) * x_step, nX, 8), in ? 16 : 0);
     }
   };
   // dt of the next chunk is fetched as raw bf16 bits one chunk ahead and only converted (softplus)
