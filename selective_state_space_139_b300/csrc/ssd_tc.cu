@@ -259,6 +259,20 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     dt_raw0 = load_dt_raw(2 * lane);
     dt_raw1 = load_dt_raw(2 * lane + 1);
   }
+  // Shared-tile offsets that are the same in every chunk.  Row r's 16-byte chunk c sits at
+  // sw_chunk(r, c); for the fragment rows ri0 = 16·quad + fg (and ri1 = ri0 + 8, 1024 bytes further) and
+  // chunk 4·half + rr this is frag_off + ((rr ^ (fg & 3)) << 4), for the state row n_own and chunk
+  // 4·half + c8 it is state_off + ((c8 ^ (n_own & 3)) << 4) (4·half and rr occupy disjoint bits).
+  const int fg = lane >> 2, ft = lane & 3;             // fragment row and column pair of this lane
+  const int ri0 = quad * 16 + fg, ri1 = ri0 + 8;       // its two rows of the M = 64 results
+  const uint32_t frag_off = static_cast<uint32_t>(quad * 2048 + fg * 128 + (((4 * half) ^ (fg & 4)) << 4) + 4 * ft);
+  const int f3 = fg & 3;
+  const uint32_t state_off = static_cast<uint32_t>((n_own >> 3) * 1024 + (n_own & 7) * 128 + (((4 * half) ^ (n_own & 4)) << 4));
+  const int s3 = n_own & 3;
+  const int jw = tid >> 2;                             // the w ∘ x row of this thread, chunks cw and cw + 1
+  const uint32_t w_off0 = sw_chunk(jw, (tid & 3) * 2), w_off1 = sw_chunk(jw, (tid & 3) * 2 + 1);
+  const int64_t y_step = static_cast<int64_t>(p.nheads) * kHd;   // elements per time step of x and y
+  const int64_t y_row0 = ((static_cast<int64_t>(b) * L + ri0) * p.nheads + h) * kHd;
   bool ok = true;
   for (int c = 0; c < nchunks && ok; ++c) {
     const int64_t t0 = static_cast<int64_t>(c) * kQ;
@@ -308,11 +322,10 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     }
     const float cum_end = s_cum[kQ - 1];
     {
-      const int j = tid >> 2, c0 = (tid & 3) * 2;
-      const float wj = ex2_approx(cum_end - s_cum[j]) * s_dl[j];
+      const float wj = ex2_approx(cum_end - s_cum[jw]) * s_dl[jw];
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        const uint32_t o = sw_chunk(j, c0 + q);
+        const uint32_t o = q ? w_off1 : w_off0;
         float v[8];
         unpack_chunk(*reinterpret_cast<const uint4*>(sm + TcSmem::kX + o), v, __nv_bfloat16());
 #pragma unroll
@@ -342,8 +355,6 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     ok = __all_sync(0xffffffffu, ok);   // the tensor-memory loads below are warp-collective
     tc_fence_after();
     if (ok && c + 1 < nchunks) load_bc(t0 + kQ, TcSmem::kC, Cg);   // G and Yo are done with C
-    const int fg = lane >> 2, ft = lane & 3;             // fragment row and column pair of this lane
-    const int ri0 = quad * 16 + fg, ri1 = ri0 + 8;       // its two rows of the M = 64 results
     if (ok) {
       const float cr0 = s_cum[ri0], cr1 = s_cum[ri1];
       float g[16];
@@ -359,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
         const float m10 = j <= ri1 ? g[4 * rr + 2] * ex2_approx(cr1 - cj.x) * dj.x : 0.0f;
         const float m11 = j + 1 <= ri1 ? g[4 * rr + 3] * ex2_approx(cr1 - cj.y) * dj.y : 0.0f;
         uint32_t hi, lo;
-        const uint32_t o0 = sw_chunk(ri0, r) + 4 * ft, o1 = sw_chunk(ri1, r) + 4 * ft;
+        const uint32_t o0 = frag_off + ((rr ^ f3) << 4), o1 = o0 + 1024;
         split2(m00, m01, hi, lo);
         *reinterpret_cast<uint32_t*>(sm + TcSmem::kMh + o0) = hi;
         *reinterpret_cast<uint32_t*>(sm + TcSmem::kMl + o0) = lo;
@@ -402,8 +413,9 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
       for (int c8 = 0; c8 < 4; ++c8) {
         uint4 hi, lo;
         split8(&H[c8 * 8], hi, lo);
-        *reinterpret_cast<uint4*>(sm + TcSmem::kHh + sw_chunk(n_own, 4 * half + c8)) = hi;
-        *reinterpret_cast<uint4*>(sm + TcSmem::kHl + sw_chunk(n_own, 4 * half + c8)) = lo;
+        const uint32_t o = state_off + ((c8 ^ s3) << 4);
+        *reinterpret_cast<uint4*>(sm + TcSmem::kHh + o) = hi;
+        *reinterpret_cast<uint4*>(sm + TcSmem::kHl + o) = lo;
       }
     }
     have_state = true;
@@ -415,8 +427,9 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     uint32_t xw[8];   // x at this lane's fragment positions, bf16 pairs: [r][row half]
 #pragma unroll
     for (int rr = 0; rr < 4; ++rr) {
-      xw[2 * rr] = *reinterpret_cast<const uint32_t*>(sm + TcSmem::kX + sw_chunk(ri0, 4 * half + rr) + 4 * ft);
-      xw[2 * rr + 1] = *reinterpret_cast<const uint32_t*>(sm + TcSmem::kX + sw_chunk(ri1, 4 * half + rr) + 4 * ft);
+      const uint32_t o0 = frag_off + ((rr ^ f3) << 4);
+      xw[2 * rr] = *reinterpret_cast<const uint32_t*>(sm + TcSmem::kX + o0);
+      xw[2 * rr + 1] = *reinterpret_cast<const uint32_t*>(sm + TcSmem::kX + o0 + 1024);
     }
     tc_fence_before();
     ok = __syncthreads_and(ok) != 0;   // Yd and every thread are done with x
@@ -433,8 +446,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
 #pragma unroll
         for (int q = 0; q < 16; ++q) yo[q] += yl[q];
       }
-      const int64_t y0 = ((static_cast<int64_t>(b) * L + t0 + ri0) * p.nheads + h) * kHd;
-      const int64_t y1 = ((static_cast<int64_t>(b) * L + t0 + ri1) * p.nheads + h) * kHd;
+      const int64_t y0 = y_row0 + t0 * y_step, y1 = y0 + 8 * y_step;
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int pc = pbase + 8 * r + 2 * ft;
