@@ -729,10 +729,11 @@ def main():
         for name in ("mamba130m-layer", "long-dna"):
             if name != w.name:
                 others.append(measure_scan_kernel(W.WORKLOADS[name], dev, rank, reps=10 if name != "long-dna" else 5))
-        # the options that run the general kernel: the exact ZOH input term (bf16 io) on this workload,
-        # and float32 io (computed in double) on the 130M-layer shape
+        # other options on this workload: A without the (n+1) structure, the exact ZOH input term (with
+        # both kinds of A); float32 io (the general kernel, computed in double) on the 130M-layer shape
         variants["general_A"] = measure_scan_kernel(w, dev, rank, reps=10, general_A=True)
-        variants["zoh"] = measure_scan_kernel(w, dev, rank, reps=3, discretization="zoh")
+        variants["zoh"] = measure_scan_kernel(w, dev, rank, reps=10, discretization="zoh")
+        variants["zoh_general_A"] = measure_scan_kernel(w, dev, rank, reps=5, discretization="zoh", general_A=True)
         variants["f32_io"] = measure_scan_kernel(dataclasses.replace(W.WORKLOADS["mamba130m-layer"], io_dtype="f32"),
                                                  dev, rank, reps=3)
     if rank != 0:
@@ -809,7 +810,10 @@ def main():
         o["tokens_per_s"] *= ws
     if variants:
         variants["general_A"]["what"] = "A = -exp(U[0,3)) per (d, n): one ex2 per state and step (fast path)"
-        variants["zoh"]["what"] = "exact zero-order-hold input term, bf16 io (general kernel, one thread per channel)"
+        variants["zoh"]["what"] = ("exact zero-order-hold input term, bf16 io (fast path: k = h/(-u/A[d,0]), "
+                                   "two FMAs per state)")
+        variants["zoh_general_A"]["what"] = ("exact zero-order-hold input term with A = -exp(U[0,3)) (fast path, "
+                                             "one ex2 and one input coefficient per state)")
         variants["f32_io"]["what"] = "float32 io: coefficients, state and readout in double (general kernel)"
         line["variants"] = variants
     if not args.no_cpu_baseline:

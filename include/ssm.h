@@ -182,8 +182,9 @@ SSM_API size_t ssm_scan_fwd_noalloc_max_scratch(void);
 /* How a prefill call with these sizes and options would run (filled by ssm_scan_fwd_describe). */
 typedef struct {
   int struct_size;           /* set to sizeof(ssm_scan_plan) before the call */
-  int path;                  /* 0: general kernel (float32 io, exact ZOH, or layouts TMA cannot use);
-                                1: bf16 fast path (rescaled-state kernel, two lanes per channel) */
+  int path;                  /* 0: general kernel (float32 io, or layouts TMA cannot use);
+                                1: bf16 fast path (rescaled-state kernel, two lanes per channel;
+                                   Δ·B or exact-ZOH input term) */
   int schedule;              /* 0: one CTA per channel tile; 1: balanced persistent ranges; 2: chunked (aggregates, carry, re-run) */
   int nchunks;               /* time chunks (1 unless schedule 2) */
   int64_t chunk_len;         /* steps per chunk */

@@ -16,6 +16,17 @@
 // (u_t = 0, or Δ_t underflowing to 0) is replaced by 1e-20, which adds at most 1e-20·ln2·|B_t| to the
 // state where the exact input term is smaller than that.
 //
+// Exact zero-order hold ("Модуль 8", §4: the input term (exp(ΔA) - 1)/A · B u).  With
+// A[d,n] = (n+1)·A[d,0] and a_n = exp(Δ_t A[d,n]) the input term is (a_n - 1)·B̃_n·u_t/A[d,0] with
+// B̃_n = B_t[n]/(n+1), so the kernel takes σ_t = -u_t/A[d,0] and carries k_t = h_t/σ_t:
+//   k_t = a_n ρ_t k_{t-1} + (1 - a_n) B̃_n = B̃_n - a_n·(B̃_n - ρ_t k_{t-1}),
+// two FMAs per state whose addend is the same table value B̃_n (the table holds B/(n+1) instead of
+// ln2·B; ρ_t and the decay powers are kept negated so that neither FMA needs a sign change).  The
+// readout and the segment ends are those of the Δ·B form.  Warps whose A is not of that form, or
+// whose A[d,0] is 0, carry g_t = h_t/u_t with one input coefficient per state,
+// (n+1)(a_n - 1)/A[d,n], or its series in Δ A[d,n] where |Δ A[d,n]| < 1/32 (the A -> 0 limit Δ·B
+// included).
+//
 // Layout of the work:
 //  * A CTA is 256 threads and owns 128 consecutive channels of one batch row (a "group"), one CTA
 //    per SM.  Two adjacent lanes share a channel: lane p holds the states n = p, p+2, .., p+14 (its
@@ -74,7 +85,7 @@ struct MapsS {
 // Scalars of one 8-step chunk as one lane sees them.
 struct Sc {
   float q[8];      // per step: r = 2^(ℓ·A[d,0]) (A[d,n] = (n+1)·A[d,0]) or ℓ (other A)
-  float rho[8];    // per step: σ_{t-1}/σ_t
+  float rho[8];    // per step: σ_{t-1}/σ_t (exact-ZOH mode: -σ_{t-1}/σ_t)
   f2 al[2];        // own steps: σ_t·SiLU(z_t)
   f2 be[2];        // own steps: D·u_t·SiLU(z_t)
   float sig;       // σ of the chunk's last step (both lanes)
@@ -86,6 +97,7 @@ struct Chan {
   float bias2;   // bias·log2(e)
   float D;
   float A0;      // A[d,0]
+  float sA;      // exact-ZOH mode: σ_t = sA·u_t (-1/A[d,0] for structured warps, 1 otherwise)
   int b, d;
   bool valid;
   bool structured;   // warp-uniform: every channel of the warp has A[d,n] = (n+1)·A[d,0]
@@ -96,7 +108,7 @@ __device__ __forceinline__ float pick(f2 v, int j) { return (j & 1) ? f2_hi(v) :
 // The scalars of a chunk (a lane's own steps 4p..4p+3, read from its channel's row of the stage),
 // computed in phases: load, then for each own step pair softplus and σ (a, b), the gate (gate), and
 // the exchange of r and ρ between the two lanes (exchange).
-template <int kMode>
+template <int kMode, bool kZoh>
 struct Phases {
   uint32_t uu[2], dd[2], zz[2];
   f2 x[2], l2v[2], u2v[2];
@@ -123,7 +135,7 @@ struct Phases {
     }
   }
   // ℓ = log2(1 + 2^x) = softplus(v)/ln2 (max(., x) covers x > 64, where 2^x is clamped), r, σ, 1/σ
-  __device__ __forceinline__ void b(int q, float A0, bool structured, bool softplus) {
+  __device__ __forceinline__ void b(int q, float A0, float sA, bool structured, bool softplus) {
     f2 l2 = l2v[q];
     if (softplus)
       l2 = f2_make(fmaxf(lg2_approx(f2_lo(l2)), f2_lo(x[q])), fmaxf(lg2_approx(f2_hi(l2)), f2_hi(x[q])));
@@ -131,7 +143,7 @@ struct Phases {
     const f2 qq = f2_mul(l2, f2_splat(A0));
     qo[2 * q] = structured ? ex2_approx(f2_lo(qq)) : f2_lo(l2);
     qo[2 * q + 1] = structured ? ex2_approx(f2_hi(qq)) : f2_hi(l2);
-    const f2 sgm = f2_mul(l2, u2v[q]);
+    const f2 sgm = kZoh ? f2_mul(u2v[q], f2_splat(sA)) : f2_mul(l2, u2v[q]);
     float s0 = f2_lo(sgm), s1 = f2_hi(sgm);
     s0 = fabsf(s0) < kSigmaMin ? kSigmaMin : s0;
     s1 = fabsf(s1) < kSigmaMin ? kSigmaMin : s1;
@@ -164,6 +176,10 @@ struct Phases {
     ro[1] = sg[0] * rs[1];
     ro[2] = sg[1] * rs[2];
     ro[3] = sg[2] * rs[3];
+    if (kZoh) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ro[i] = -ro[i];
+    }
     ns.sig = pl ? sg[3] : s3x;
     const int base = (threadIdx.x & 31) & ~1;
 #pragma unroll
@@ -180,12 +196,12 @@ struct Phases {
 // chains overlap the state updates (0.381 ms against 0.403 ms with the scalars computed as one block
 // on the 2.8B layer).  urow, c, sig_prev and the channel constants describe the next chunk.  Returns
 // the lane's four own outputs packed as bf16 (main mode).
-template <int kMode, bool kS>
+template <int kMode, bool kS, bool kZoh>
 __device__ __forceinline__ uint2 chunk_step(f2 (&h)[4], const Sc& s, Sc& ns, uint32_t tab, int pl,
-                                            const float (&Ah)[8], uint32_t urow, int c, int sw, float bias2,
-                                            float D, float A0, bool structured, float sig_prev, bool softplus,
-                                            bool has_z) {
-  Phases<kMode> ph;
+                                            const float (&Ah)[8], const float (&Wz)[8], uint32_t urow, int c,
+                                            int sw, float bias2, float D, float A0, float sA, bool structured,
+                                            float sig_prev, bool softplus, bool has_z) {
+  Phases<kMode, kZoh> ph;
   ph.load(urow, c, sw, pl, has_z);
   float part[8];
 #pragma unroll
@@ -195,23 +211,46 @@ __device__ __forceinline__ uint2 chunk_step(f2 (&h)[4], const Sc& s, Sc& ns, uin
     const uint32_t row = tab + j * 128 + pl * 32;
     f2 a[4];
     if (kS) {
-      // ρ r^(p+1+2k), k = 0..7
       const float r = q;
       const float r2 = r * r, r4 = r2 * r2, r8 = r4 * r4;
-      const float c0 = rho * (pl ? r2 : r);
+      // Δ·B: ρ r^(p+1+2k), k = 0..7.  Exact ZOH: -r^(p+1+2k) (ρ enters through t below)
+      const float c0 = kZoh ? -(pl ? r2 : r) : rho * (pl ? r2 : r);
       a[0] = f2_make(c0, c0 * r2);
       a[1] = f2_mul(a[0], f2_splat(r4));
       a[2] = f2_mul(a[0], f2_splat(r8));
       a[3] = f2_mul(a[1], f2_splat(r8));
-    } else {
+    } else if (!kZoh) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) a[i] = f2_make(rho * ex2_approx(q * Ah[2 * i]), rho * ex2_approx(q * Ah[2 * i + 1]));
     }
     const float4 b0 = lds128f(row), b1 = lds128f(row + 16);
-    h[0] = f2_fma(a[0], h[0], f2_make(b0.x, b0.y));
-    h[1] = f2_fma(a[1], h[1], f2_make(b0.z, b0.w));
-    h[2] = f2_fma(a[2], h[2], f2_make(b1.x, b1.y));
-    h[3] = f2_fma(a[3], h[3], f2_make(b1.z, b1.w));
+    const f2 bt[4] = {f2_make(b0.x, b0.y), f2_make(b0.z, b0.w), f2_make(b1.x, b1.y), f2_make(b1.z, b1.w)};
+    if (!kZoh) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) h[i] = f2_fma(a[i], h[i], bt[i]);
+    } else if (kS) {
+      // k_t = B̃ - a·(B̃ - ρ k_{t-1}) with rho = -ρ, a[i] = -a
+#pragma unroll
+      for (int i = 0; i < 4; ++i) h[i] = f2_fma(a[i], f2_fma(f2_splat(rho), h[i], bt[i]), bt[i]);
+    } else {
+      // exact ZOH, any A: g_t = ρ e g_{t-1} + m B̃ with e = 2^(ℓ A[d,n]) = exp(y), y = Δ A[d,n], and
+      // m = (n+1)(e - 1)/A[d,n] = Wz·(e - 1), e - 1 taken from its series y(1 + y/2 + y²/6 + y³/24)
+      // where |y| < 1/32, free of the cancellation in e - 1.  A[d,n] = 0 is held as 2^-60 (Ah, Wz),
+      // where the series gives m = (n+1)·Δ, the A -> 0 limit, and e = 1.
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const f2 x = f2_mul(f2_splat(q), f2_make(Ah[2 * i], Ah[2 * i + 1]));
+        const f2 e = f2_make(ex2_approx(f2_lo(x)), ex2_approx(f2_hi(x)));
+        const f2 y = f2_mul(x, f2_splat(kLn2));
+        const f2 poly = f2_mul(y, f2_fma(y, f2_fma(y, f2_fma(y, f2_splat(1.0f / 24.0f), f2_splat(1.0f / 6.0f)),
+                                                       f2_splat(0.5f)), f2_splat(1.0f)));
+        const f2 em = f2_add(e, f2_splat(-1.0f));
+        const f2 em1 = f2_make(fabsf(f2_lo(y)) < 0.03125f ? f2_lo(poly) : f2_lo(em),
+                               fabsf(f2_hi(y)) < 0.03125f ? f2_hi(poly) : f2_hi(em));
+        const f2 m = f2_mul(em1, f2_make(Wz[2 * i], Wz[2 * i + 1]));
+        h[i] = f2_fma(f2_mul(f2_splat(-rho), e), h[i], f2_mul(m, bt[i]));   // rho = -ρ
+      }
+    }
     if (kMode == kMain) {
       const float4 c0v = lds128f(row + 64), c1v = lds128f(row + 80);
       f2 a0 = f2_mul(f2_make(c0v.x, c0v.y), h[0]);
@@ -223,7 +262,7 @@ __device__ __forceinline__ uint2 chunk_step(f2 (&h)[4], const Sc& s, Sc& ns, uin
     }
     // a phase of the next chunk's scalars
     if (j == 0 || j == 2) ph.a(j >> 1, bias2, softplus);
-    if (j == 1 || j == 3) ph.b(j >> 1, A0, structured, softplus);
+    if (j == 1 || j == 3) ph.b(j >> 1, A0, sA, structured, softplus);
     if (j == 4 || j == 5) ph.gate(j - 4, ns, D, has_z);
     if (j == 6) ph.exchange(ns, pl, sig_prev);
   }
@@ -244,21 +283,22 @@ __device__ __forceinline__ uint2 chunk_step(f2 (&h)[4], const Sc& s, Sc& ns, uin
 }
 
 // The scalars of a chunk on their own (the first chunk of a CTA's walk).
-template <int kMode>
+template <int kMode, bool kZoh>
 __device__ __forceinline__ void chunk_scalars(Sc& ns, uint32_t urow, int c, int sw, int pl, float bias2, float D,
-                                              float A0, bool structured, float sig_prev, bool softplus, bool has_z) {
-  Phases<kMode> ph;
+                                              float A0, float sA, bool structured, float sig_prev, bool softplus,
+                                              bool has_z) {
+  Phases<kMode, kZoh> ph;
   ph.load(urow, c, sw, pl, has_z);
   ph.a(0, bias2, softplus);
   ph.a(1, bias2, softplus);
-  ph.b(0, A0, structured, softplus);
-  ph.b(1, A0, structured, softplus);
+  ph.b(0, A0, sA, structured, softplus);
+  ph.b(1, A0, sA, structured, softplus);
   ph.gate(0, ns, D, has_z);
   ph.gate(1, ns, D, has_z);
   ph.exchange(ns, pl, sig_prev);
 }
 
-template <int kMode>
+template <int kMode, bool kZoh>
 __global__ void __launch_bounds__(kThreads, 1) scan_scaled_kernel(const __grid_constant__ MapsS tm, const ScanParams p) {
   constexpr int kNs = kN / 2;     // states per lane
   extern __shared__ uint8_t smem_raw[];
@@ -332,8 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1) scan_scaled_kernel(const __grid_c
     issued = ntiles < kSt - 1 ? ntiles : kSt - 1;
   }
 
-  // Widens tile k's B and C (stage k % kSt) into table k & 1: ln2·B in columns 0..15, C in 16..31,
-  // zero rows for n >= dstate.  256 jobs (array, n, 8-step chunk), one per thread; a warp's 32
+  // Widens tile k's B and C (stage k % kSt) into table k & 1: ln2·B (exact-ZOH mode: B/(n+1)) in
+  // columns 0..15, C in 16..31, zero rows for n >= dstate.  256 jobs (array, n, 8-step chunk), one per thread; a warp's 32
   // threads store 32 consecutive words.
   auto widen = [&](int64_t k) {
     const uint32_t src = smem_u32(smem + (k % kSt) * SmemS::kStage + 3 * SmemS::kTileIO);
@@ -350,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_scaled_kernel(const __grid_c
 #pragma unroll
         for (int j = 0; j < 8; ++j) vals[j] = 0.0f;
       }
-      const float scale = arr == 0 ? kLn2 : 1.0f;
+      const float scale = arr == 0 ? (kZoh ? 1.0f / static_cast<float>(n + 1) : kLn2) : 1.0f;
       // even states in columns 0..7 of each half, odd states in 8..15 (one block per lane)
       const int col = (n & 1) * 8 + (n >> 1);
 #pragma unroll
@@ -366,10 +406,12 @@ __global__ void __launch_bounds__(kThreads, 1) scan_scaled_kernel(const __grid_c
     cc.d = cc.valid ? d : 0;
     const int64_t arow = static_cast<int64_t>(cc.d) * p.N;
     cc.A0 = *checked(p.A, arow, nA);
-    bool st_ok = true;
+    // exact ZOH divides by A[d,0]: a zero row takes the per-state path, which has the A -> 0 limit
+    bool st_ok = !kZoh || cc.A0 != 0.0f;
     for (int n = 1; n < p.N; ++n)
       if (*checked(p.A, arow + n, nA) != static_cast<float>(n + 1) * cc.A0) st_ok = false;
     cc.structured = __all_sync(0xffffffffu, st_ok) != 0;
+    cc.sA = kZoh && cc.structured ? -1.0f / cc.A0 : 1.0f;
     cc.D = p.D ? *checked(p.D, cc.d, p.dim) : 0.0f;
     cc.bias2 = (p.bias ? *checked(p.bias, cc.d, p.dim) : 0.0f) * kLog2e;
   };
@@ -382,8 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1) scan_scaled_kernel(const __grid_c
   Chan cur, nxt;
   tile_chan(gk, cur);
   Sc sc_a, sc_b;   // scalar buffers: sc_a holds the scalars of the next chunk to run
-  chunk_scalars<kMode>(sc_a, smem_u32(smem) + ch * kRow, 0, sw, pl, cur.bias2, cur.D, cur.A0, cur.structured, 1.0f,
-                       softplus, has_z);
+  chunk_scalars<kMode, kZoh>(sc_a, smem_u32(smem) + ch * kRow, 0, sw, pl, cur.bias2, cur.D, cur.A0, cur.sA,
+                             cur.structured, 1.0f, softplus, has_z);
 
   f2 h[kNs / 2];   // this lane's rescaled states
 #pragma unroll
@@ -470,10 +512,6 @@ __global__ void __launch_bounds__(kThreads, 1) scan_scaled_kernel(const __grid_c
     if (kMode == kMain && cur.valid)
       yrow = checked(static_cast<__nv_bfloat16*>(p.y), (static_cast<int64_t>(cur.b) * p.dim + cur.d) * p.L + t0, nIO,
                      nch * kC);
-    float Ah[8];   // this lane's row of A (A not of the form (n+1)·A[d,0])
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      Ah[i] = (!cur.structured && sidx(i) < p.N) ? *checked(p.A, static_cast<int64_t>(cur.d) * p.N + sidx(i), nA) : 0.0f;
     float sig_end = 1.0f;
     // Chunks in pairs with two scalar buffers: chunk c runs on the buffer filled during chunk c - 1,
     // and the other buffer takes chunk c + 1 (or the next tile's first chunk), so no scalar set is
@@ -481,15 +519,24 @@ __global__ void __launch_bounds__(kThreads, 1) scan_scaled_kernel(const __grid_c
     // with one chunk on sc_a and a copy back into sc_a.
     auto chunks = [&](auto tag) {
       constexpr bool kS = decltype(tag)::value;
+      float Ah[8];   // this lane's row of A (A not of the form (n+1)·A[d,0])
+      float Wz[8];   // exact-ZOH mode: (n+1)/A[d,n], with A[d,n] = 0 held as 2^-60 in Ah and Wz
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        Ah[i] = (!kS && sidx(i) < p.N) ? *checked(p.A, static_cast<int64_t>(cur.d) * p.N + sidx(i), nA) : 0.0f;
+        if (kZoh && Ah[i] == 0.0f) Ah[i] = 0x1p-60f;
+        Wz[i] = (!kS && kZoh) ? static_cast<float>(sidx(i) + 1) / Ah[i] : 0.0f;
+      }
       auto one = [&](Sc& run_sc, Sc& fill_sc, int c) {
         // the next chunk's scalars: chunk c + 1 of this tile or chunk 0 of the next tile, chosen by
         // selects so that they share one basic block with this chunk's recurrence (past the last
         // tile they are computed from a stale stage and never used)
         const bool in_tile = c + 1 < nch;
         const Chan& cc = in_tile ? cur : nxt;
-        const uint2 yv = chunk_step<kMode, kS>(h, run_sc, fill_sc, tab + c * kC * 128, pl, Ah, in_tile ? urow : urow_next,
-                                               in_tile ? c + 1 : 0, sw, cc.bias2, cc.D, cc.A0, cc.structured,
-                                               (in_tile || !next_new) ? run_sc.sig : 1.0f, softplus, has_z);
+        const uint2 yv = chunk_step<kMode, kS, kZoh>(h, run_sc, fill_sc, tab + c * kC * 128, pl, Ah, Wz,
+                                                     in_tile ? urow : urow_next, in_tile ? c + 1 : 0, sw, cc.bias2,
+                                                     cc.D, cc.A0, cc.sA, cc.structured,
+                                                     (in_tile || !next_new) ? run_sc.sig : 1.0f, softplus, has_z);
         if (kMode == kMain && yrow) *reinterpret_cast<uint2*>(yrow + c * kC + 4 * pl) = yv;
         if (kMode == kAgg) lsum += run_sc.lsum;
         sig_end = run_sc.sig;
@@ -576,7 +623,7 @@ int scaled_resident_ctas() {
   if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return 0; }
   if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) { cudaGetLastError(); return 0; }
-  auto kern = scan_scaled_kernel<kMain>;
+  auto kern = scan_scaled_kernel<kMain, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemS::kTotal) != cudaSuccess) {
     cudaGetLastError();
     return 0;
@@ -621,8 +668,8 @@ cudaError_t scan_scaled_launch(const ScanParams& p, int nchunks, int balanced_ct
   }
   const int gpb = (p.dim + kCh - 1) / kCh;
   const unsigned groups = static_cast<unsigned>(p.batch) * gpb;
-  auto kmain = scan_scaled_kernel<kMain>;
-  auto kagg = scan_scaled_kernel<kAgg>;
+  auto kmain = p.disc == 1 ? scan_scaled_kernel<kMain, true> : scan_scaled_kernel<kMain, false>;
+  auto kagg = p.disc == 1 ? scan_scaled_kernel<kAgg, true> : scan_scaled_kernel<kAgg, false>;
   cudaError_t e;
   e = cudaFuncSetAttribute(kmain, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemS::kTotal);
   if (e != cudaSuccess) return e;

@@ -68,7 +68,7 @@ int sm_count() {
 }
 
 struct Plan {
-  int path = 0;           // 0: general kernel (float32 io, ZOH, layouts TMA cannot describe); 1: bf16 fast path
+  int path = 0;           // 0: general kernel (float32 io, layouts TMA cannot describe); 1: bf16 fast path
   int nchunks = 1;
   int64_t chunk_len = 0;
   int balanced_ctas = 0;  // fast path: > 0 selects the balanced persistent schedule
@@ -80,11 +80,12 @@ struct Plan {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// The bf16 fast path needs: bf16 io, the Δ·B input term, rows TMA can describe (L a multiple of 8,
-// at least one 64-step tile, at least 128 rows).  Pointer alignment is checked at call time.
+// The bf16 fast path needs: bf16 io, the Δ·B or the exact-ZOH input term, rows TMA can describe (L a
+// multiple of 8, at least one 64-step tile, at least 128 rows).  Pointer alignment is checked at call
+// time.
 bool fast_eligible(int batch, int dim, int64_t seqlen, ssm_dtype io, int disc) {
-  return io == SSM_BF16 && disc == SSM_DISC_DELTA_B && seqlen % 8 == 0 && seqlen >= 64 &&
-         static_cast<int64_t>(batch) * dim >= 128;
+  return io == SSM_BF16 && (disc == SSM_DISC_DELTA_B || disc == SSM_DISC_ZOH) && seqlen % 8 == 0 &&
+         seqlen >= 64 && static_cast<int64_t>(batch) * dim >= 128;
 }
 
 void layout_chunked(Plan* pl, int batch, int dim, int dstate, size_t carry_bytes) {

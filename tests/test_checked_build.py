@@ -52,6 +52,17 @@ def test_scan_options_general_A_and_zoh(checked, dtype):
     scan_t.test_chunked_with_initial_state(64, dtype)
 
 
+@pytest.mark.parametrize("shape", [scan_t.ZOH_FAST_SHAPES[2], scan_t.ZOH_FAST_SHAPES[3]])
+def test_scan_zoh_fast_path(checked, shape):
+    scan_t.test_zoh_fast_path(shape)
+
+
+def test_scan_zoh_fast_path_general_A_chunked_balanced(checked):
+    scan_t.test_zoh_fast_path_general_A_and_zero_rows()
+    scan_t.test_zoh_fast_path_chunked(64)
+    scan_t.test_zoh_fast_path_balanced_sampled()
+
+
 @pytest.mark.parametrize("shape,chunk", [((2, 140, 16, 512), 256), ((3, 100, 7, 1000), 192),
                                          ((1, 130, 16, 136), 64)])
 def test_scan_bf16_chunked_schedule(checked, shape, chunk):

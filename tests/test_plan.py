@@ -34,7 +34,9 @@ def test_plan_workspace_matches_the_workspace_query(shape, dtype, algorithm):
 def test_kernel_path_choice():
     assert ssm.describe_scan(4, 512, 16, 4096, dtype=BF16)["path"] == "fast"
     assert ssm.describe_scan(4, 512, 16, 4096, dtype=F32)["path"] == "general"          # float32 io
-    assert ssm.describe_scan(4, 512, 16, 4096, dtype=BF16, discretization="zoh")["path"] == "general"
+    assert ssm.describe_scan(4, 512, 16, 4096, dtype=BF16, discretization="zoh")["path"] == "fast"
+    assert ssm.describe_scan(4, 512, 16, 4096, dtype=F32, discretization="zoh")["path"] == "general"
+    assert ssm.describe_scan(4, 512, 16, 4100, dtype=BF16, discretization="zoh")["path"] == "general"
     assert ssm.describe_scan(4, 512, 16, 4100, dtype=BF16)["path"] == "general"          # L not a multiple of 8
     assert ssm.describe_scan(4, 512, 16, 32, dtype=BF16)["path"] == "general"            # shorter than a tile
 

@@ -186,6 +186,89 @@ def test_zoh_discretization(dtype):
     _check_full(inp, y, hL, TOL[dtype], discretization="zoh")
 
 
+ZOH_FAST_SHAPES = [  # batch, dim, dstate, L: bf16 shapes the fast kernel takes (L a multiple of 8, >= 64)
+    (2, 256, 16, 512), (1, 128, 16, 64), (3, 129, 16, 136), (2, 300, 5, 200), (1, 200, 1, 72),
+]
+
+
+@pytest.mark.parametrize("shape", ZOH_FAST_SHAPES)
+def test_zoh_fast_path(shape):
+    """The exact-ZOH input term on the bf16 fast kernel (structured A: the rescaled k = h/(-u/A[d,0])
+    form), every output, with an initial state."""
+    dev = _dev()
+    b, d, n, L = shape
+    assert ssm.describe_scan(b, d, n, L, dtype=torch.bfloat16, discretization="zoh")["path"] == "fast"
+    inp = W.random_scan_inputs(b, d, n, L, "bf16", seed=31 + L, a_scale=(0.5, 2.0), device=dev)
+    h0 = torch.randn((b, d, n), device=dev)
+    y, hL = _run(inp, discretization="zoh", h0=h0)
+    _check_full(inp, y, hL, TOL[torch.bfloat16], discretization="zoh", h0=h0)
+
+
+def test_zoh_fast_path_general_A_and_zero_rows():
+    """Exact ZOH on the fast kernel's per-state path: A without the (n+1) structure, single zero
+    entries (the A -> 0 limit Δ·B) and whole zero rows (structured but A[d,0] = 0), next to
+    structured warps."""
+    dev = _dev()
+    inp = W.random_scan_inputs(2, 256, 16, 320, "bf16", seed=41, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(6)
+    A = -torch.exp(torch.randn((256, 16), generator=g, device=dev))
+    A[:64] = -0.5 * torch.arange(1, 17, device=dev, dtype=torch.float32)   # structured warps
+    A[70, 3] = 0.0
+    A[100, 0] = 0.0
+    A[160:192] = 0.0                                                        # zero rows, one whole warp
+    A[200, :] = 0.0                                                         # a zero row in a mixed warp
+    A[230, 5] = -1e-6                                                       # |Δ A| far below 1/32
+    inp["A"] = A
+    h0 = torch.randn((2, 256, 16), device=dev)
+    y, hL = _run(inp, discretization="zoh", h0=h0)
+    _check_full(inp, y, hL, TOL[torch.bfloat16], discretization="zoh", h0=h0)
+
+
+@pytest.mark.parametrize("chunk", [64, 192])
+def test_zoh_fast_path_chunked(chunk):
+    """Exact ZOH through the chunked schedule: aggregate pass, carry pass, main pass."""
+    dev = _dev()
+    inp = W.random_scan_inputs(2, 140, 16, 512, "bf16", seed=chunk + 3, device=dev)
+    h0 = torch.randn((2, 140, 16), device=dev)
+    y, hL = _run(inp, algorithm="chunked", chunk_len=chunk, discretization="zoh", h0=h0)
+    _check_full(inp, y, hL, TOL[torch.bfloat16], discretization="zoh", h0=h0)
+
+
+def test_zoh_fast_path_balanced_sampled():
+    """Exact ZOH through the balanced persistent schedule (CTA-to-CTA carries), sampled channels."""
+    dev = _dev()
+    b, d, n, L = 8, 2400, 16, 200
+    inp = W.random_scan_inputs(b, d, n, L, "bf16", seed=77, a_scale=(0.5, 2.0), device=dev)
+    assert ssm.describe_scan(b, d, n, L, dtype=torch.bfloat16, discretization="zoh")["schedule"] == "balanced"
+    h0 = torch.randn((b, d, n), device=dev)
+    y, hL = _run(inp, discretization="zoh", h0=h0)
+    chans = sorted(set(sample_channels(b, d, 160, seed=5) + [(bb, dd) for bb in (0, b - 1) for dd in (127, 128, d - 1)]))
+    ry, rh = oracle_channels(inp, chans, h0=h0, discretization="zoh")
+    bi = torch.tensor([c[0] for c in chans])
+    di = torch.tensor([c[1] for c in chans])
+    assert max_rel_err(to64(y[bi, di]), ry) <= 1e-2
+    assert max_rel_err(to64(hL[bi, di]), rh) <= 1e-2
+    assert torch.isfinite(y).all() and torch.isfinite(hL).all()
+    assert ssm.device_status() == ssm.SSM_OK
+
+
+def test_zoh_mamba28b_layer_sampled():
+    """Exact ZOH on the Mamba-2.8B layer (batch 4, d_inner 5120, L 4096) in the benchmark's launch
+    configuration, 256 sampled channels against the oracle."""
+    dev = _dev()
+    w = W.WORKLOADS["mamba2.8b-layer"]
+    inp = W.make_scan_inputs(w, device=dev)
+    y, hL = _run(inp, discretization="zoh")
+    chans = sample_channels(w.batch, w.dim, 256, seed=12)
+    ry, rh = oracle_channels(inp, chans, discretization="zoh")
+    bi = torch.tensor([c[0] for c in chans])
+    di = torch.tensor([c[1] for c in chans])
+    assert max_rel_err(to64(y[bi, di]), ry) <= 1e-2
+    assert max_rel_err(to64(hL[bi, di]), rh) <= 1e-2
+    assert torch.isfinite(y).all()
+
+
 def test_outputs_fully_overwritten_and_status_clean():
     dev = _dev()
     inp = W.random_scan_inputs(2, 200, 16, 333, "bf16", seed=3, device=dev)
