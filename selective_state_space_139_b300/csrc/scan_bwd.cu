@@ -796,6 +796,10 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
   const int64_t c1 = c0 + p.chunk_len < p.L ? c0 + p.chunk_len : p.L;
   const int64_t nseg = (p.L + kSeg - 1) / kSeg;
   const int n0 = 8 * pl;                        // first state of this lane
+  // Pair slot j of this lane holds the states n0 + 2·(j ^ pm) and the next one: the XOR with lane
+  // bits 4 and 3 places the pairs that the first two rounds of the dB/dC butterfly keep in the lower
+  // slots, so those rounds need no selects
+  const int pm = (((lane >> 4) & 1) << 1) | ((lane >> 3) & 1);
   const Sizes Z = sizes_of(p);
   P A2[kP2], dh[kP2], dA[kP2];
   {
@@ -806,7 +810,7 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
     const float* Ad = checked(p.A, static_cast<int64_t>(dd) * p.N, Z.nA, p.N);
 #pragma unroll
     for (int j = 0; j < kP2; ++j) {
-      const int n = n0 + 2 * j;
+      const int n = n0 + 2 * (j ^ pm);
       const float a0 = n < p.N ? Ad[n] : 0.0f;
       const float a1 = n + 1 < p.N ? Ad[n + 1] : 0.0f;
       A2[j] = P::make(a0 * kLog2e, a1 * kLog2e);
@@ -845,13 +849,13 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
   const int64_t last = c0 + ((c1 - c0 - 1) / kSeg) * kSeg;
   SegRaw<IO> raw;
   uint32_t bcr[2];
-  float4 ckr0, ckr1;
+  float2 ckp[kP2];   // checkpoint pairs, in slot order
   float ckS;
   auto fetch_ck = [&](int64_t t0) {
     const int64_t sgi = t0 / kSeg;
-    const float4* const cq = reinterpret_cast<const float4*>(checked(ck, sgi * kN, Z.nCk - ck_row, 8));
-    ckr0 = __ldg(cq);
-    ckr1 = __ldg(cq + 1);
+    const float2* const cq = reinterpret_cast<const float2*>(checked(ck, sgi * kN, Z.nCk - ck_row, 8));
+#pragma unroll
+    for (int j = 0; j < kP2; ++j) ckp[j] = __ldg(cq + (j ^ pm));
     ckS = *checked(cs, sgi, Z.nCs - cs_row);
   };
   fetch_seg<IO>(p, row * p.L + last, seg_len(last), raw);
@@ -862,13 +866,14 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
   int buf = 0;
   int64_t pend_t0 = -1;
   int pend_nk = 0;
-  // the column of the dB/dC table this lane's butterfly result belongs to
-  const int ridx = (lane >> 1) & 15;
-  const int rcol = ridx < 8 ? n0 + ridx : 16 + n0 + (ridx - 8);
+  // the column of the dB/dC table this lane's butterfly result belongs to: pair pm, dB or dC by lane
+  // bit 2, low or high state of the pair by lane bit 1
+  const int rcol = ((lane >> 2) & 1) * 16 + n0 + 2 * pm + ((lane >> 1) & 1);
   for (int64_t t0 = last; t0 >= c0; t0 -= kSeg) {
     const int nk = seg_len(t0);
     const int64_t off = row * p.L + t0;
-    const f2* bc2 = reinterpret_cast<const f2*>(bc_base + buf * (kSeg * 32));
+    // this lane's B pairs at bcl[k * 16 + (j ^ pm)], C pairs 8 further
+    const f2* bcl = reinterpret_cast<const f2*>(bc_base + buf * (kSeg * 32)) + 4 * pl;
     float* red = red_base + buf * (4 * kSeg * 32);
     float x[kSeg], v[kSeg], zz[kSeg], dyv[kSeg];
     unpack_one<IO, float>(raw.w[0], x);
@@ -878,10 +883,9 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
     P h0[kP2];
     {
       const P Sp = P::splat(ckS);
-      const float ckv[8] = {ckr0.x, ckr0.y, ckr0.z, ckr0.w, ckr1.x, ckr1.y, ckr1.z, ckr1.w};
 #pragma unroll
       for (int j = 0; j < kP2; ++j)
-        h0[j] = pfma(pexp(pmul(A2[j], Sp)), hs_s[j * kThreads + tid], P::make(ckv[2 * j], ckv[2 * j + 1]));
+        h0[j] = pfma(pexp(pmul(A2[j], Sp)), hs_s[j * kThreads + tid], P::make(ckp[j].x, ckp[j].y));
     }
     const int64_t tn = t0 - kSeg;
     const bool more = tn >= c0;
@@ -907,9 +911,9 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
         P sa = P::splat(0.0f);
 #pragma unroll
         for (int j = 0; j < kP2; ++j) {
-          hc[j] = pfma(pexp(pmul(dlp, A2[j])), hc[j], pmul(dlx, P::from_f2(bc2[k * 16 + 4 * pl + j])));
+          hc[j] = pfma(pexp(pmul(dlp, A2[j])), hc[j], pmul(dlx, P::from_f2(bcl[k * 16 + (j ^ pm)])));
           if (k < kSeg - 1) hbuf[(k * kP2 + j) * kThreads + tid] = hc[j];
-          sa = pfma(P::from_f2(bc2[k * 16 + 8 + 4 * pl + j]), hc[j], sa);
+          sa = pfma(P::from_f2(bcl[k * 16 + 8 + (j ^ pm)]), hc[j], sa);
         }
         const float part = sa.lo() + sa.hi();
         const float sacc = part + __shfl_xor_sync(0xffffffffu, part, 1) + Dd * x[k];
@@ -939,16 +943,16 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
 #pragma unroll
         for (int j = 0; j < kP2; ++j) {
           const P abar = pexp(pmul(dlp, A2[j]));
-          const P bn = P::from_f2(bc2[k * 16 + 4 * pl + j]);
-          const P cn = P::from_f2(bc2[k * 16 + 8 + 4 * pl + j]);
+          const P bn = P::from_f2(bcl[k * 16 + (j ^ pm)]);
+          const P cn = P::from_f2(bcl[k * 16 + 8 + (j ^ pm)]);
           dh[j] = pfma(dsp, cn, dh[j]);
           const P hp = k > 0 ? hbuf[((k - 1) * kP2 + j) * kThreads + tid] : h0[j];
           const P vc = pmul(dsp, hc[j]);
           const P vbb = pmul(dh[j], dlx);
-          vals[8 + 2 * j] = vc.lo();
-          vals[8 + 2 * j + 1] = vc.hi();
-          vals[2 * j] = vbb.lo();
-          vals[2 * j + 1] = vbb.hi();
+          vals[4 * j] = vbb.lo();
+          vals[4 * j + 1] = vbb.hi();
+          vals[4 * j + 2] = vc.lo();
+          vals[4 * j + 3] = vc.hi();
           const P w = pmul(pmul(dh[j], hp), abar);
           dq = pfma(w, A2[j], dq);
           dA[j] = pfma(w, dlp, dA[j]);
@@ -964,11 +968,16 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
         gdu[k] = ds[k] * Dd + dhb * dl[k];
         gdd[k] = dv;
         dbias += dv;
-        // butterfly over the 16 channels sharing this lane's parity
+        // butterfly over the 16 channels sharing this lane's parity.  Lane bits 4 and 3: the slot
+        // order already puts the kept pairs first (slots 0-1 of the partner across bit 4 hold the
+        // pairs of this lane's slots 2-3, and so on); lane bit 2: dB or dC; lane bit 1: low or high
 #pragma unroll
-        for (int w = 16, cnt = 16; w >= 2; w >>= 1, cnt >>= 1) {
+        for (int i = 0; i < 8; ++i) vals[i] += __shfl_xor_sync(0xffffffffu, vals[i + 8], 16);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) vals[i] += __shfl_xor_sync(0xffffffffu, vals[i + 4], 8);
+#pragma unroll
+        for (int w = 4, half = 2; w >= 2; w >>= 1, half >>= 1) {
           const bool upper = (lane & w) != 0;
-          const int half = cnt / 2;
 #pragma unroll
           for (int i = 0; i < half; ++i) {
             const float send = upper ? vals[i] : vals[i + half];
@@ -994,7 +1003,7 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
     float* accA = checked(static_cast<float*>(p.acc_dA), static_cast<int64_t>(d) * p.N, Z.nA, p.N);
 #pragma unroll
     for (int j = 0; j < kP2; ++j) {
-      const int n = n0 + 2 * j;
+      const int n = n0 + 2 * (j ^ pm);
       if (n < p.N) atomicAdd(accA + n, dA[j].lo());
       if (n + 1 < p.N) atomicAdd(accA + n + 1, dA[j].hi());
     }
