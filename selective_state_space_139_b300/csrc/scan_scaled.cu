@@ -298,7 +298,11 @@ __device__ __forceinline__ void chunk_scalars(Sc& ns, uint32_t urow, int c, int 
   ph.exchange(ns, pl, sig_prev);
 }
 
-template <int kMode, bool kZoh>
+// kZ (a gate z is given) and kSp (softplus on Δ) are template parameters rather than run-time flags:
+// tested at run time they split each chunk's body into basic blocks that the compiler does not
+// schedule across, and the next chunk's scalar phases stop overlapping the recurrence (0.369 ms
+// against 0.335 ms on the 2.8B layer).
+template <int kMode, bool kZoh, bool kZ, bool kSp>
 __global__ void __launch_bounds__(kThreads, 1) scan_scaled_kernel(const __grid_constant__ MapsS tm, const ScanParams p) {
   constexpr int kNs = kN / 2;     // states per lane
   extern __shared__ uint8_t smem_raw[];
@@ -316,8 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1) scan_scaled_kernel(const __grid_c
   const int sw = ch & 7;                           // 128-byte swizzle of this channel's tile row
   const int64_t Lt = (p.L + kT - 1) / kT;
   const int gpb = (p.dim + kCh - 1) / kCh;         // groups per batch row
-  const bool has_z = kMode == kMain && p.z != nullptr;
-  const bool softplus = p.softplus != 0;
+  constexpr bool has_z = kMode == kMain && kZ;
+  constexpr bool softplus = kSp;
   // buffer sizes (elements) for the index checks of checked builds
   const int64_t nA = static_cast<int64_t>(p.dim) * p.N;
   const int64_t nState = static_cast<int64_t>(p.batch) * p.dim * p.N;
@@ -613,6 +617,22 @@ __global__ void __launch_bounds__(kThreads, 1) scan_scaled_kernel(const __grid_c
   }
 }
 
+using ScaledKernel = void (*)(MapsS, ScanParams);
+
+template <int kMode, bool kZoh, bool kZ>
+ScaledKernel pick_sp(bool sp) {
+  return sp ? scan_scaled_kernel<kMode, kZoh, kZ, true> : scan_scaled_kernel<kMode, kZoh, kZ, false>;
+}
+
+// The instance for these parameters (the aggregate pass reads no z).
+template <int kMode>
+ScaledKernel pick_kernel(const ScanParams& p) {
+  const bool z = kMode == kMain && p.z != nullptr;
+  const bool sp = p.softplus != 0;
+  if (p.disc == 1) return z ? pick_sp<kMode, true, kMode == kMain>(sp) : pick_sp<kMode, true, false>(sp);
+  return z ? pick_sp<kMode, false, kMode == kMain>(sp) : pick_sp<kMode, false, false>(sp);
+}
+
 }  // namespace
 
 int scaled_channels_per_cta() { return kCh; }
@@ -623,7 +643,7 @@ int scaled_resident_ctas() {
   if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return 0; }
   if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) { cudaGetLastError(); return 0; }
-  auto kern = scan_scaled_kernel<kMain, false>;
+  auto kern = scan_scaled_kernel<kMain, false, true, true>;   // every instance has the same shared memory
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemS::kTotal) != cudaSuccess) {
     cudaGetLastError();
     return 0;
@@ -668,8 +688,8 @@ cudaError_t scan_scaled_launch(const ScanParams& p, int nchunks, int balanced_ct
   }
   const int gpb = (p.dim + kCh - 1) / kCh;
   const unsigned groups = static_cast<unsigned>(p.batch) * gpb;
-  auto kmain = p.disc == 1 ? scan_scaled_kernel<kMain, true> : scan_scaled_kernel<kMain, false>;
-  auto kagg = p.disc == 1 ? scan_scaled_kernel<kAgg, true> : scan_scaled_kernel<kAgg, false>;
+  const ScaledKernel kmain = pick_kernel<kMain>(p);
+  const ScaledKernel kagg = pick_kernel<kAgg>(p);
   cudaError_t e;
   e = cudaFuncSetAttribute(kmain, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemS::kTotal);
   if (e != cudaSuccess) return e;

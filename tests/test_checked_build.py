@@ -57,6 +57,13 @@ def test_scan_zoh_fast_path(checked, shape):
     scan_t.test_zoh_fast_path(shape)
 
 
+@pytest.mark.parametrize("discretization", ["delta_b", "zoh"])
+def test_scan_fast_kernel_flag_instances(checked, discretization):
+    for use_z in (True, False):
+        for softplus in (True, False):
+            scan_t.test_fast_kernel_flag_instances(discretization, use_z, softplus)
+
+
 def test_scan_zoh_fast_path_general_A_chunked_balanced(checked):
     scan_t.test_zoh_fast_path_general_A_and_zero_rows()
     scan_t.test_zoh_fast_path_chunked(64)

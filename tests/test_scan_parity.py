@@ -150,6 +150,28 @@ def test_optional_operands_and_softplus_off(dtype):
     _check_full(pos, y, hL, TOL[dtype], softplus=False)
 
 
+@pytest.mark.parametrize("discretization", ["delta_b", "zoh"])
+@pytest.mark.parametrize("use_z", [True, False])
+@pytest.mark.parametrize("softplus", [True, False])
+def test_fast_kernel_flag_instances(discretization, use_z, softplus):
+    """Every compiled instance of the bf16 fast kernel (gate or none, softplus on or off, Δ·B or
+    exact ZOH), in the grid schedule and in the chunked schedule (its aggregate pass included)."""
+    dev = _dev()
+    b, d, n, L = 2, 136, 16, 256
+    assert ssm.describe_scan(b, d, n, L, dtype=torch.bfloat16, discretization=discretization)["path"] == "fast"
+    inp = W.random_scan_inputs(b, d, n, L, "bf16", seed=3 + 2 * use_z + softplus, device=dev)
+    if not use_z:
+        inp = dict(inp, z=None)
+    if not softplus:
+        # Δ = Δ_raw must be non-negative without softplus: 0.1|Δ_raw|, no bias
+        inp = dict(inp, delta=(inp["delta"].float().abs() * 0.1).to(inp["delta"].dtype), delta_bias=None)
+    h0 = torch.randn((b, d, n), device=dev)
+    for algo, chunk in (("single_pass", 0), ("chunked", 64)):
+        y, hL = _run(inp, delta_softplus=softplus, discretization=discretization, h0=h0, algorithm=algo,
+                     chunk_len=chunk)
+        _check_full(inp, y, hL, TOL[torch.bfloat16], softplus=softplus, discretization=discretization, h0=h0)
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("chunk", [64, 128, 192])
 def test_chunked_with_initial_state(chunk, dtype):
