@@ -379,7 +379,10 @@ __global__ void __launch_bounds__(kThreads, sizeof(CT) == 4 ? SSM_BWD_FWD_MINB :
 
 // (1') local forward with two lanes per channel (bfloat16 io): lane pl of a channel runs the states
 // 8pl .. 8pl + 7; both lanes evaluate the per-step scalars.  Same outputs as (1).
-template <typename IO>
+// kZ (a gate is given), kSp (softplus on Δ) and kFull (every 8-step segment full: L and the chunk
+// length multiples of 8) are template parameters: tested at run time inside the unrolled steps they
+// split the segment's body into basic blocks the compiler does not schedule across.
+template <typename IO, bool kZ, bool kSp, bool kFull>
 __global__ void __launch_bounds__(kThreads, 4) bwd_fwd2_kernel(const BwdParams p) {
   using P = Pair<float>;
   __shared__ __align__(16) float bc_buf[2][kSeg * 32];
@@ -421,12 +424,12 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_fwd2_kernel(const BwdParams p
   __syncthreads();
   int buf = 0;
   for (int64_t t0 = c0; t0 < c1; t0 += kSeg) {
-    const int nk = seg_len(t0);
+    const int nk = kFull ? kSeg : seg_len(t0);
     float x[kSeg], v[kSeg], zz[kSeg], dyv[kSeg];
     unpack_one<IO, float>(raw.w[0], x);
     unpack_one<IO, float>(raw.w[1], v);
     unpack_one<IO, float>(raw.w[2], dyv);
-    if (p.z) unpack_one<IO, float>(raw.w[3], zz);
+    if (kZ) unpack_one<IO, float>(raw.w[3], zz);
     const int64_t tn = t0 + kSeg;
     const bool more = tn < c1;
     if (more) {
@@ -445,8 +448,8 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_fwd2_kernel(const BwdParams p
     for (int k = 0; k < kSeg; ++k) {
       if (k < nk) {
         const float vb = v[k] + bias;
-        const float dl = p.softplus ? softplus_fast(vb) : vb;
-        const float ds = p.z ? dyv[k] * zz[k] * rcp_approx(1.0f + ex2_approx(-zz[k] * kLog2e)) : dyv[k];
+        const float dl = kSp ? softplus_fast(vb) : vb;
+        const float ds = kZ ? dyv[k] * zz[k] * rcp_approx(1.0f + ex2_approx(-zz[k] * kLog2e)) : dyv[k];
         S += dl;
         const P dlp = P::splat(dl), dlx = P::splat(dl * x[k]), dsp = P::splat(ds);
 #pragma unroll
@@ -776,7 +779,7 @@ struct Smem2 {
   static constexpr int kTotal = kBC + kH + kRed + kHs;
 };
 
-template <typename IO>
+template <typename IO, bool kZ, bool kSp>
 __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p) {
   using P = Pair<float>;
   extern __shared__ __align__(16) uint8_t smem[];
@@ -879,7 +882,7 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
     unpack_one<IO, float>(raw.w[0], x);
     unpack_one<IO, float>(raw.w[1], v);
     unpack_one<IO, float>(raw.w[2], dyv);
-    if (p.z) unpack_one<IO, float>(raw.w[3], zz);
+    if (kZ) unpack_one<IO, float>(raw.w[3], zz);
     P h0[kP2];
     {
       const P Sp = P::splat(ckS);
@@ -905,8 +908,8 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
       gdz[k] = 0.0f;
       if (k < nk) {
         const float vb = v[k] + bias;
-        dl[k] = p.softplus ? softplus_fast(vb) : vb;
-        sg[k] = p.softplus ? rcp_approx(1.0f + ex2_approx(-vb * kLog2e)) : 1.0f;
+        dl[k] = kSp ? softplus_fast(vb) : vb;
+        sg[k] = kSp ? rcp_approx(1.0f + ex2_approx(-vb * kLog2e)) : 1.0f;
         const P dlp = P::splat(dl[k]), dlx = P::splat(dl[k] * x[k]);
         P sa = P::splat(0.0f);
 #pragma unroll
@@ -917,7 +920,7 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
         }
         const float part = sa.lo() + sa.hi();
         const float sacc = part + __shfl_xor_sync(0xffffffffu, part, 1) + Dd * x[k];
-        if (p.z) {
+        if (kZ) {
           const float sz = rcp_approx(1.0f + ex2_approx(-zz[k] * kLog2e));
           ds[k] = dyv[k] * zz[k] * sz;
           gdz[k] = dyv[k] * sacc * sz * (1.0f + zz[k] * (1.0f - sz));
@@ -930,7 +933,7 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
         // keep the partner exchange uniform: the partner lane runs the same k with the same nk
       }
     }
-    if (valid && p.z && pl == 1) store_seg<IO, float>(p.dz, off, nk, p.vec_io, gdz, Z.nIO);
+    if (valid && kZ && pl == 1) store_seg<IO, float>(p.dz, off, nk, p.vec_io, gdz, Z.nIO);
     float gdu[kSeg], gdd[kSeg];
 #pragma unroll
     for (int k = kSeg - 1; k >= 0; --k) {
@@ -1019,6 +1022,26 @@ __global__ void double_to_float_kernel(const double* __restrict__ src, float* __
   if (i < n) dst[i] = static_cast<float>(src[i]);
 }
 
+using BwdKernel = void (*)(BwdParams);
+
+template <typename IO, bool kZ, bool kSp>
+BwdKernel pick_fwd2_full(const BwdParams& p) {
+  const bool full = p.L % kSeg == 0 && p.chunk_len % kSeg == 0;
+  return full ? bwd_fwd2_kernel<IO, kZ, kSp, true> : bwd_fwd2_kernel<IO, kZ, kSp, false>;
+}
+
+template <typename IO>
+BwdKernel pick_fwd2(const BwdParams& p) {
+  if (p.z) return p.softplus ? pick_fwd2_full<IO, true, true>(p) : pick_fwd2_full<IO, true, false>(p);
+  return p.softplus ? pick_fwd2_full<IO, false, true>(p) : pick_fwd2_full<IO, false, false>(p);
+}
+
+template <typename IO>
+BwdKernel pick_rev2(const BwdParams& p) {
+  if (p.z) return p.softplus ? bwd_rev2_kernel<IO, true, true> : bwd_rev2_kernel<IO, true, false>;
+  return p.softplus ? bwd_rev2_kernel<IO, false, true> : bwd_rev2_kernel<IO, false, false>;
+}
+
 template <typename IO, typename CT>
 cudaError_t launch(const BwdParams& p, cudaStream_t stream) {
   const dim3 grid((p.dim + kThreads - 1) / kThreads, p.batch, p.nchunks);
@@ -1026,7 +1049,7 @@ cudaError_t launch(const BwdParams& p, cudaStream_t stream) {
   bool two_lanes = false;
   if constexpr (sizeof(CT) == 4) {
     if (SSM_BWD_TWO_LANES) {
-      bwd_fwd2_kernel<IO><<<grid2, kThreads, 0, stream>>>(p);
+      pick_fwd2<IO>(p)<<<grid2, kThreads, 0, stream>>>(p);
       two_lanes = true;
     }
   }
@@ -1038,7 +1061,7 @@ cudaError_t launch(const BwdParams& p, cudaStream_t stream) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if constexpr (sizeof(CT) == 4) {
     if (SSM_BWD_TWO_LANES) {
-      auto k2 = bwd_rev2_kernel<IO>;
+      auto k2 = pick_rev2<IO>(p);
       e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem2::kTotal);
       if (e != cudaSuccess) return e;
       k2<<<grid2, kThreads, Smem2::kTotal, stream>>>(p);

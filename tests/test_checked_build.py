@@ -117,6 +117,13 @@ def test_ssd_decode_steps(checked, groups):
     ssd_t.test_ssd_decode_steps_match_the_recurrence(groups)
 
 
+@pytest.mark.parametrize("L", [200, 203])
+def test_backward_flag_instances(checked, L):
+    for use_z in (True, False):
+        for softplus in (True, False):
+            bwd_t.test_backward_flag_instances(use_z, softplus, L)
+
+
 @pytest.mark.parametrize("shape,io", [((2, 200, 13, 333), "f32"), ((3, 130, 16, 77), "bf16"),
                                       ((2, 256, 16, 512), "bf16"), ((1, 5, 1, 9), "f32"), ((2, 129, 16, 1), "bf16")])
 def test_backward_small_and_ragged(checked, shape, io):

@@ -91,6 +91,22 @@ def test_backward_optional_operands(io, opts):
     _compare(g, r, TOL[inp["u"].dtype])
 
 
+@pytest.mark.parametrize("use_z", [True, False])
+@pytest.mark.parametrize("softplus", [True, False])
+@pytest.mark.parametrize("L", [200, 203])
+def test_backward_flag_instances(use_z, softplus, L):
+    """Every compiled instance of the bf16 two-lane backward kernels: gate or none, softplus on or
+    off, every 8-step segment full (L = 200) or a ragged last segment (L = 203)."""
+    dev = _dev()
+    inp = _inputs(2, 96, 16, L, "bf16", seed=L + 2 * use_z + softplus, dev=dev)
+    if not softplus:
+        # Δ = Δ_raw without softplus: positive steps 0.05|Δ_raw| and no bias (the generated biases are
+        # negative, softplus^-1 of steps below 0.1)
+        inp["delta"] = (inp["delta"].float().abs() * 0.05).to(inp["delta"].dtype)
+    g = _gpu(inp, use_z=use_z, use_bias=softplus, softplus=softplus)
+    _compare(g, _oracle(inp, use_z=use_z, use_bias=softplus, softplus=softplus), TOL[inp["u"].dtype])
+
+
 def test_backward_mamba130m_layer_full():
     dev = _dev()
     w = W.WORKLOADS["mamba130m-layer"]
