@@ -221,8 +221,12 @@ __device__ __forceinline__ uint2 chunk_step(f2 (&h)[4], const Sc& s, Sc& ns, uin
       a[2] = f2_mul(a[1], R4);
       a[3] = f2_mul(a[2], R4);
     } else if (!kZoh) {
+      const f2 q2 = f2_splat(q);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = f2_make(rho * ex2_approx(q * Ah[2 * i]), rho * ex2_approx(q * Ah[2 * i + 1]));
+      for (int i = 0; i < 4; ++i) {
+        const f2 x = f2_mul(q2, f2_make(Ah[2 * i], Ah[2 * i + 1]));
+        a[i] = f2_make(rho * ex2_approx(f2_lo(x)), rho * ex2_approx(f2_hi(x)));
+      }
     }
     const float4 b0 = lds128f(row), b1 = lds128f(row + 16);
     const f2 bt[4] = {f2_make(b0.x, b0.y), f2_make(b0.z, b0.w), f2_make(b1.x, b1.y), f2_make(b1.z, b1.w)};
