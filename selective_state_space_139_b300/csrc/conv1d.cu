@@ -24,23 +24,25 @@ __device__ __forceinline__ float io_at(const IO* p, int64_t i) {
 
 // vectorised path: L % kVec == 0 and 16-byte aligned rows.  A grid of SSM_CONV_BLOCKS_PER_SM blocks per
 // SM walks the flat (row, chunk) index space with a grid-sized stride; each iteration a thread issues
-// the loads of kPer chunks (one stride apart) before any arithmetic (one per iteration measured
-// fastest; two or four chunks, or requesting the next chunk before computing the current one, were
-// slower).  Consecutive lanes hold consecutive flat chunks, so the three inputs before a chunk come
+// the loads of kPer chunks (one stride apart) before any arithmetic: one with SiLU, whose arithmetic
+// makes the kernel issue-bound (two or four chunks, requesting the next chunk before computing the
+// current one, or a SiLU with one MUFU operation and a Newton reciprocal were all slower), two without
+// it (59.4 us against 62.8 us for one on the 2.8B layer's x).  Consecutive lanes hold consecutive flat chunks, so the three inputs before a chunk come
 // from the previous lane by a shuffle (lane 0 re-reads them).  Flat indices fit 32 bits (checked on
 // the host).
-#ifndef SSM_CONV_PER
-#define SSM_CONV_PER 1            // chunks per thread and iteration (1 measured fastest)
-#endif
 #ifndef SSM_CONV_BLOCKS_PER_SM
 #define SSM_CONV_BLOCKS_PER_SM 32 // blocks of the grid-stride loop per SM (8: 73.9 us, 16: 71.9, 32: 69.8, 64: 69.8)
 #endif
-constexpr int kPer = SSM_CONV_PER;
+template <bool kSilu>
+__host__ __device__ constexpr int per_thread() { return kSilu ? 1 : 2; }   // chunks per thread and iteration
 
-template <typename IO>
+// kSilu is a template parameter: tested at run time inside the unrolled outputs it splits the body
+// into basic blocks.
+template <typename IO, bool kSilu>
 __global__ void __launch_bounds__(256) conv1d_vec_kernel(const ConvParams p) {
   using T = IoTraits<IO>;
   constexpr int V = T::kVec;
+  constexpr int kPer = per_thread<kSilu>();
   constexpr bool kFast = sizeof(IO) == 2;
   const uint32_t cpr = static_cast<uint32_t>(p.L / V);
   const uint32_t total = static_cast<uint32_t>(p.batch) * p.dim * cpr;
@@ -95,11 +97,11 @@ __global__ void __launch_bounds__(256) conv1d_vec_kernel(const ConvParams p) {
       for (int j = 0; j < V; ++j) {
         if constexpr (kFast) {
           const float s = fmaf(w.w, win[j + 3], fmaf(w.z, win[j + 2], fmaf(w.y, win[j + 1], w.x * win[j])));
-          out[j] = p.silu ? silu_fast(s) : s;
+          out[j] = kSilu ? silu_fast(s) : s;
         } else {
           const double s = static_cast<double>(w.x) * win[j] + static_cast<double>(w.y) * win[j + 1] +
                            static_cast<double>(w.z) * win[j + 2] + static_cast<double>(w.w) * win[j + 3];
-          out[j] = static_cast<float>(p.silu ? s / (1.0 + exp(-s)) : s);
+          out[j] = static_cast<float>(kSilu ? s / (1.0 + exp(-s)) : s);
         }
       }
       if (live[i]) {
@@ -173,10 +175,12 @@ cudaError_t launch(const ConvParams& p, bool vec, cudaStream_t stream) {
       int dev = 0, sms = 148;
       if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
       const int64_t total = nrows * (p.L / IoTraits<IO>::kVec);
-      const int64_t want = (total + 256 * kPer - 1) / (256 * kPer);
+      const int per = p.silu ? per_thread<true>() : per_thread<false>();
+      const int64_t want = (total + 256 * per - 1) / (256 * per);
       const int64_t cap = static_cast<int64_t>(SSM_CONV_BLOCKS_PER_SM) * sms;
       const unsigned blocks = static_cast<unsigned>(want < cap ? want : cap);
-      conv1d_vec_kernel<IO><<<blocks, 256, 0, stream>>>(q);
+      if (p.silu) conv1d_vec_kernel<IO, true><<<blocks, 256, 0, stream>>>(q);
+      else conv1d_vec_kernel<IO, false><<<blocks, 256, 0, stream>>>(q);
     } else {
       const int64_t n = nrows * p.L;
       conv1d_scalar_kernel<IO><<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(q);
