@@ -160,6 +160,9 @@ constexpr int kThreads1 = 128;
 #endif
 constexpr int kBpt = SSM_DECODE_BPT;
 
+// kZ (a gate is given) and kSp (softplus on Δ) are template parameters, so the per-row arithmetic
+// is one basic block.
+template <bool kZ, bool kSp>
 __global__ void __launch_bounds__(kThreads1) state_update_bf16_kernel(const DecodeParams p) {
   using IO = __nv_bfloat16;
   const int pairs = ((p.batch + kBpt - 1) / kBpt) * p.dim;
@@ -200,7 +203,7 @@ __global__ void __launch_bounds__(kThreads1) state_update_bf16_kernel(const Deco
     craw[k][0] = crow[0]; craw[k][1] = crow[1];
     xv[k] = IoTraits<IO>::to_f32(*checked(static_cast<const IO*>(p.x), c, nBD));
     dv[k] = IoTraits<IO>::to_f32(*checked(static_cast<const IO*>(p.delta), c, nBD));
-    zv[k] = p.z ? IoTraits<IO>::to_f32(*checked(static_cast<const IO*>(p.z), c, nBD)) : 0.0f;
+    zv[k] = kZ ? IoTraits<IO>::to_f32(*checked(static_cast<const IO*>(p.z), c, nBD)) : 0.0f;
     const float* cs = checked(p.conv_state, c * 3, nBD * 3, 3);
     c0[k] = cs[0]; c1[k] = cs[1]; c2[k] = cs[2];
   }
@@ -210,7 +213,7 @@ __global__ void __launch_bounds__(kThreads1) state_update_bf16_kernel(const Deco
     const float s = fmaf(w.w, xv[k], fmaf(w.z, c2[k], fmaf(w.y, c1[k], w.x * c0[k])));
     const float u = silu_fast(s);
     const float v = dv[k] + bv;
-    const float dl = p.softplus ? softplus_fast(v) : v;
+    const float dl = kSp ? softplus_fast(v) : v;
     const float wu = dl * u;
     const float dl2 = dl * kLog2e;
     const uint32_t bw[8] = {braw[k][0].x, braw[k][0].y, braw[k][0].z, braw[k][0].w,
@@ -235,7 +238,7 @@ __global__ void __launch_bounds__(kThreads1) state_update_bf16_kernel(const Deco
       h4[k][q] = make_float4(hv[0], hv[1], hv[2], hv[3]);
     }
     float y = fmaf(Dv, u, py0 + py1);
-    if (p.z) y *= silu_fast(zv[k]);
+    if (kZ) y *= silu_fast(zv[k]);
     if (!live[k]) continue;
     const int64_t c = cc[k];
     float4* sw = reinterpret_cast<float4*>(checked(p.state, c * 16, nBD * 16, 16));
@@ -255,7 +258,13 @@ cudaError_t launch(const DecodeParams& p, cudaStream_t stream) {
   if (sizeof(IO) == 2 && p.vec16) {
     const int64_t threads = ((p.batch + kBpt - 1) / kBpt) * static_cast<int64_t>(p.dim);
     const unsigned blocks = static_cast<unsigned>((threads + kThreads1 - 1) / kThreads1);
-    state_update_bf16_kernel<<<blocks, kThreads1, 0, stream>>>(p);
+    if (p.z) {
+      if (p.softplus) state_update_bf16_kernel<true, true><<<blocks, kThreads1, 0, stream>>>(p);
+      else state_update_bf16_kernel<true, false><<<blocks, kThreads1, 0, stream>>>(p);
+    } else {
+      if (p.softplus) state_update_bf16_kernel<false, true><<<blocks, kThreads1, 0, stream>>>(p);
+      else state_update_bf16_kernel<false, false><<<blocks, kThreads1, 0, stream>>>(p);
+    }
     return cudaGetLastError();
   }
   const unsigned blocks = static_cast<unsigned>((nchan + kChannelsPerBlock - 1) / kChannelsPerBlock);

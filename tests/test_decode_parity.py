@@ -98,3 +98,40 @@ def test_decode_small_shapes_every_channel(shape, io):
     assert max_rel_err(to64(ys[:, bi, di].T), ry) <= tol
     assert max_rel_err(to64(state[bi, di]), rh) <= tol
     np.testing.assert_array_equal(to64(conv_state[bi, di]), rc)
+
+
+@pytest.mark.parametrize("use_z", [True, False])
+@pytest.mark.parametrize("softplus", [True, False])
+def test_decode_flag_instances(use_z, softplus):
+    """Every compiled instance of the bf16 decode kernel (gate or none, softplus on or off) against the
+    oracle's decode step, token by token, over every channel."""
+    dev = _dev()
+    batch, dim, N, steps = 3, 64, 16, 20
+    wk = W.DecodeWorkload("t", batch, dim, N, 4, steps, "bf16", seed=5 + 2 * use_z + softplus)
+    inp = W.make_decode_inputs(wk, device=dev)
+    bias = inp["delta_bias"]
+    if not softplus:
+        # Δ = Δ_raw without softplus: positive steps 0.05|Δ_raw| and no bias
+        inp["delta"] = (inp["delta"].float().abs() * 0.05).to(inp["delta"].dtype)
+        bias = None
+    state = torch.zeros((batch, dim, N), device=dev)
+    conv_state = torch.zeros((batch, dim, 3), device=dev)
+    bidx = np.repeat(np.arange(batch, dtype=np.int64), dim)
+    didx = np.tile(np.arange(dim, dtype=np.int64), batch)
+    di = torch.as_tensor(didx)
+    st_o = np.zeros((batch * dim, N))
+    cs_o = np.zeros((batch * dim, 3))
+    for t in range(steps):
+        z_t = inp["z"][t] if use_z else None
+        y = ssm.selective_state_update(inp["x"][t], inp["delta"][t], inp["A"], inp["B"][t], inp["C"][t], inp["D"], z_t,
+                                       state, conv_state, inp["conv_w"], delta_bias=bias, delta_softplus=softplus)
+        ry, st_o, cs_o = oracle.state_update(to64(inp["x"][t]).reshape(-1), to64(inp["delta"][t]).reshape(-1),
+                                             to64(inp["A"])[didx], to64(inp["B"][t]), to64(inp["C"][t]), bidx, st_o, cs_o,
+                                             to64(inp["conv_w"])[didx], D=to64(inp["D"])[didx],
+                                             z_t=None if z_t is None else to64(z_t).reshape(-1),
+                                             delta_bias=None if bias is None else to64(bias)[didx],
+                                             delta_softplus=softplus)
+        torch.cuda.synchronize()
+        assert max_rel_err(to64(y).reshape(-1), ry) <= 1e-2, t
+    assert max_rel_err(to64(state).reshape(batch * dim, N), st_o) <= 1e-2
+    np.testing.assert_array_equal(to64(conv_state).reshape(batch * dim, 3), cs_o)
