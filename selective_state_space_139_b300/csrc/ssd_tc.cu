@@ -280,10 +280,8 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     // chunk's tiles were requested during the previous chunk
     if (warp == 0) {
       const float d0 = dl_of(dt_raw0, t0 + 2 * lane), d1 = dl_of(dt_raw1, t0 + 2 * lane + 1);
-      if (c + 1 < nchunks) {
-        dt_raw0 = load_dt_raw(t0 + kQ + 2 * lane);
-        dt_raw1 = load_dt_raw(t0 + kQ + 2 * lane + 1);
-      }
+      dt_raw0 = load_dt_raw(t0 + kQ + 2 * lane);   // zero past L
+      dt_raw1 = load_dt_raw(t0 + kQ + 2 * lane + 1);
       const float a0 = d0 * A2;
       float s2 = a0 + d1 * A2;
 #pragma unroll
@@ -352,7 +350,9 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     ok = mbar_wait_bounded(&bars[0], par, &g_ssd_status);
     ok = __all_sync(0xffffffffu, ok);   // the tensor-memory loads below are warp-collective
     tc_fence_after();
-    if (ok && c + 1 < nchunks) load_bc(t0 + kQ, TcSmem::kC, Cg);   // G and Yo are done with C
+    // the next chunk's tiles, requested unconditionally: past the last chunk every row is zero-filled
+    // from a valid address and nothing reads the result
+    load_bc(t0 + kQ, TcSmem::kC, Cg);   // G and Yo are done with C
     // The element-wise phases run whether or not the wait before them succeeded: after a failed
     // wait they read allocated tensor memory and write in-bounds shared and global memory (y is
     // undefined once the status word reports a timeout), and the loop leaves at the next barrier.
@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     ok = mbar_wait_bounded(&bars[1], par, &g_ssd_status);
     ok = __all_sync(0xffffffffu, ok);   // the tensor-memory loads below are warp-collective
     tc_fence_after();
-    if (ok && c + 1 < nchunks) load_bc(t0 + kQ, TcSmem::kB, Bg);   // G and S^T are done with B
+    load_bc(t0 + kQ, TcSmem::kB, Bg);   // G and S^T are done with B
     {
       const float eE = ex2_approx(cum_end);
       {
@@ -435,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     tc_fence_before();
     ok = __syncthreads_and(ok) != 0;   // Yd and every thread are done with x
     tc_fence_after();
-    if (ok && c + 1 < nchunks) load_x(t0 + kQ);
+    load_x(t0 + kQ);
     {
       const float e0 = ex2_approx(s_cum[ri0]), e1 = ex2_approx(s_cum[ri1]);
       float yd[16], yo[16];
@@ -468,6 +468,9 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     ok = __syncthreads_and(ok) != 0;
     tc_fence_after();
   }
+  // every tile copy this thread requested has landed before the CTA's shared memory is released
+  // (a loop left after a failed wait may have copies in flight)
+  asm volatile("cp.async.wait_all;" ::: "memory");
   if (ok && p.hT) {
     const int64_t hT_base = (static_cast<int64_t>(b) * p.nheads + h) * kHd * kNs;
 #pragma unroll
