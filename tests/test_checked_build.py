@@ -96,6 +96,12 @@ def test_decode_small_shapes(checked, shape, io):
     decode_t.test_decode_small_shapes_every_channel(shape, io)
 
 
+def test_decode_flag_instances(checked):
+    for use_z in (True, False):
+        for softplus in (True, False):
+            decode_t.test_decode_flag_instances(use_z, softplus)
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("shape", [(2, 130, 256), (1, 64, 33), (3, 20, 1), (1, 5, 2), (1, 16, 3)])
 def test_conv1d_small_shapes(checked, shape, dtype):
