@@ -259,7 +259,10 @@ SSM_API ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A
  * This build implements io_dtype SSM_BF16 with headdim 64 and dstate 128 (the pages' Mamba-2
  * geometry); other values return SSM_ERR_UNSUPPORTED.  x, B, C and y must be 16-byte aligned, h0 and
  * final_state 8-byte aligned.  Accumulation and the state are float32 (tensor-core products with the
- * computed operand split into two bf16 terms); no workspace.
+ * computed operand split into two bf16 terms); no workspace.  The kernel's waits for its tensor-core
+ * results are bounded: y and final_state are defined once ssm_device_status() has returned SSM_OK for
+ * the stream (SSM_ERR_TIMEOUT: a wait gave up; y and final_state are then undefined, and no other
+ * memory is written).
  */
 SSM_API ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void* B, const void* C,
                                const float* D, const float* dt_bias, int softplus_flag, const float* h0, void* y,
