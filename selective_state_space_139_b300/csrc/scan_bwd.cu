@@ -773,7 +773,7 @@ constexpr int kP2 = 4;         // state pairs per lane
 
 struct Smem2 {
   static constexpr int kBC = 2 * kSeg * 32 * 4;                 // B/C table, two buffers
-  static constexpr int kH = kSeg * kP2 * kThreads * 8;          // recomputed states [k][j][thread] (pairs)
+  static constexpr int kH = kSeg * kP2 * kThreads * 8;          // recomputed states [k][j/2][thread][2] (pairs)
   static constexpr int kRed = 2 * 4 * kSeg * 32 * 4;            // dB/dC partials, two buffers
   static constexpr int kHs = kP2 * kThreads * 8;                // chunk start states [j][thread]
   static constexpr int kTotal = kBC + kH + kRed + kHs;
@@ -915,8 +915,14 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
 #pragma unroll
         for (int j = 0; j < kP2; ++j) {
           hc[j] = pfma(pexp(pmul(dlp, A2[j])), hc[j], pmul(dlx, P::from_f2(bcl[k * 16 + (j ^ pm)])));
-          if (k < kSeg - 1) hbuf[(k * kP2 + j) * kThreads + tid] = hc[j];
           sa = pfma(P::from_f2(bcl[k * 16 + 8 + (j ^ pm)]), hc[j], sa);
+        }
+        if (k < kSeg - 1) {
+          // slots 2jj and 2jj + 1 side by side: one 16-byte store each ([k][jj][thread][2] pairs)
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj)
+            *reinterpret_cast<float4*>(&hbuf[((k * 2 + jj) * kThreads + tid) * 2]) =
+                make_float4(hc[2 * jj].lo(), hc[2 * jj].hi(), hc[2 * jj + 1].lo(), hc[2 * jj + 1].hi());
         }
         const float part = sa.lo() + sa.hi();
         const float sacc = part + __shfl_xor_sync(0xffffffffu, part, 1) + Dd * x[k];
@@ -943,13 +949,25 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
         const P dlp = P::splat(dl[k]), dsp = P::splat(ds[k]), dlx = P::splat(dl[k] * x[k]);
         P dq = P::splat(0.0f), db = P::splat(0.0f);
         float vals[16];
+        P hpv[kP2];   // the state before step k: h0 or recomputed in shared memory
+        if (k > 0) {
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj) {
+            const float4 v4 = *reinterpret_cast<const float4*>(&hbuf[(((k - 1) * 2 + jj) * kThreads + tid) * 2]);
+            hpv[2 * jj] = P::make(v4.x, v4.y);
+            hpv[2 * jj + 1] = P::make(v4.z, v4.w);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < kP2; ++j) hpv[j] = h0[j];
+        }
 #pragma unroll
         for (int j = 0; j < kP2; ++j) {
           const P abar = pexp(pmul(dlp, A2[j]));
           const P bn = P::from_f2(bcl[k * 16 + (j ^ pm)]);
           const P cn = P::from_f2(bcl[k * 16 + 8 + (j ^ pm)]);
           dh[j] = pfma(dsp, cn, dh[j]);
-          const P hp = k > 0 ? hbuf[((k - 1) * kP2 + j) * kThreads + tid] : h0[j];
+          const P hp = hpv[j];
           const P vc = pmul(dsp, hc[j]);
           const P vbb = pmul(dh[j], dlx);
           vals[4 * j] = vbb.lo();
