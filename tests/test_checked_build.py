@@ -12,6 +12,7 @@ import torch
 
 from selective_state_space_139_b300 import ssm
 from selective_state_space_139_b300 import workloads as W
+from tests._helpers import max_rel_err, to64
 from tests import test_conv1d_parity as conv_t
 from tests import test_decode_parity as decode_t
 from tests import test_scan_bwd_parity as bwd_t
@@ -134,3 +135,69 @@ def test_backward_flag_instances(checked, L):
                                       ((2, 256, 16, 512), "bf16"), ((1, 5, 1, 9), "f32"), ((2, 129, 16, 1), "bf16")])
 def test_backward_small_and_ragged(checked, shape, io):
     bwd_t.test_backward_small_and_ragged(shape, io)
+
+
+def _close(a, b, tol):
+    assert max_rel_err(to64(a), to64(b)) <= tol
+
+
+def test_full_size_workloads_stay_in_bounds():
+    """The full-size workloads through the checked build: every global index of the prefill (balanced
+    and chunked schedules, exact ZOH), the backward, conv1d, the decode step, the SSD forward and its
+    decode step stays inside its buffer, and the results agree with the ordinary build's (the same
+    arithmetic: equal up to the order of the backward's cross-channel atomics)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    dev = torch.device("cuda:0")
+    w = W.WORKLOADS["mamba2.8b-layer"]
+    inp = W.make_scan_inputs(w, device=dev)
+    dy = W.make_cotangent(w.batch, w.dim, w.seqlen, inp["u"].dtype, w.seed, device=dev)
+    conv_w = torch.randn((w.dim, 4), device=dev) * 0.5
+    conv_s = torch.randn((w.batch, w.dim, 3), device=dev)
+    sw = W.WORKLOADS["mamba2-ssd-layer"]
+    sin = W.make_ssd_inputs(sw, device=dev)
+    dw = W.WORKLOADS["decode-2.8b"]
+    din = W.make_decode_inputs(dw, steps=3, device=dev)
+    mw = W.WORKLOADS["mamba2-decode"]
+    mdin = W.make_ssd_decode_inputs(mw, device=dev)
+
+    def run_all():
+        a = dict(D=inp["D"], z=inp["z"], delta_bias=inp["delta_bias"])
+        out = {"scan": ssm.selective_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], **a),
+               "chunked": ssm.selective_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"],
+                                                 algorithm="chunked", **a),
+               "zoh": ssm.selective_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"],
+                                             discretization="zoh", **a),
+               "bwd": ssm.selective_scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], dy, **a),
+               "conv": ssm.causal_conv1d_fwd(inp["u"], conv_w, conv_state=conv_s),
+               "ssd": ssm.ssd_fwd(sin["x"], sin["dt"], sin["A"], sin["B"], sin["C"], D=sin["D"],
+                                  dt_bias=sin["dt_bias"])}
+        state = torch.zeros((dw.batch, dw.dim, dw.dstate), device=dev)
+        cst = torch.zeros((dw.batch, dw.dim, 3), device=dev)
+        out["decode"] = [ssm.selective_state_update(din["x"][t], din["delta"][t], din["A"], din["B"][t], din["C"][t],
+                                                    din["D"], din["z"][t], state, cst, din["conv_w"],
+                                                    delta_bias=din["delta_bias"]) for t in range(3)] + [state, cst]
+        mstate = torch.zeros((mw.batch, mw.nheads, mw.headdim, mw.dstate), device=dev)
+        out["ssd_decode"] = [ssm.ssd_state_update(mdin["x"][t], mdin["dt"][t], mdin["A"], mdin["B"][t], mdin["C"][t],
+                                                  mstate, D=mdin["D"], dt_bias=mdin["dt_bias"]) for t in range(3)]
+        out["ssd_decode"].append(mstate)
+        torch.cuda.synchronize()
+        return out
+
+    ref = run_all()
+    assert ssm.device_status() == ssm.SSM_OK
+    with ssm.use_checked_library():
+        assert ssm.device_status() == ssm.SSM_OK
+        got = run_all()
+        assert ssm.device_status() == ssm.SSM_OK, "an index check failed at full size"
+    for k in ("scan", "chunked", "zoh", "conv", "ssd"):
+        for a, b in zip(got[k], ref[k]):
+            if a is not None:
+                _close(a, b, 1e-5)
+    for name, g in got["bwd"].items():
+        if g is not None:
+            _close(g, ref["bwd"][name], 1e-3)
+    for a, b in zip(got["decode"], ref["decode"]):
+        _close(a, b, 1e-5)
+    for a, b in zip(got["ssd_decode"], ref["ssd_decode"]):
+        _close(a, b, 1e-5)
