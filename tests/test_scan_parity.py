@@ -119,6 +119,26 @@ def test_long_dna_full():
     assert ey <= 1e-2 and eh <= 1e-2, (ey, eh)
 
 
+def test_long_sequence_beyond_2_31_elements():
+    """The long-sequence workload with two batch rows: 3.2e9 elements per io tensor, so the offsets of
+    the second row exceed 2^31.  Sampled channels of both rows (the last channel of the last row
+    included) against the oracle, every output finite, status clean."""
+    import dataclasses
+    dev = _dev()
+    w = dataclasses.replace(W.WORKLOADS["long-dna"], name="long-dna-x2", batch=2, seed=1013)
+    assert w.batch * w.dim * w.seqlen > 2 ** 31
+    inp = W.make_scan_inputs(w, device=dev)
+    y, hL = _run(inp)
+    assert torch.isfinite(y).all() and torch.isfinite(hL).all()
+    assert ssm.device_status() == ssm.SSM_OK
+    chans = sorted(set(sample_channels(w.batch, w.dim, 24, seed=3) + [(1, w.dim - 1), (1, 0), (0, w.dim - 1)]))
+    ry, rh = oracle_channels(inp, chans)
+    bi = torch.tensor([c[0] for c in chans])
+    di = torch.tensor([c[1] for c in chans])
+    assert max_rel_err(to64(y[bi, di]), ry) <= 1e-2
+    assert max_rel_err(to64(hL[bi, di]), rh) <= 1e-2
+
+
 SHAPES = [  # batch, dim, dstate, L
     (1, 64, 16, 1), (1, 64, 16, 7), (2, 130, 16, 33), (1, 200, 5, 257), (3, 129, 16, 100),
     (2, 256, 16, 64), (1, 128, 16, 512), (2, 300, 1, 130),
