@@ -91,7 +91,7 @@ __device__ __forceinline__ void decays_structured(float r, f2 (&a)[kNmax / 2]) {
 // Per-channel constants.
 struct Chan {
   float AL2[kNmax];   // A[d,n]·log2(e) (fast path) or A[d,n] (accurate path)
-  float invA[kNmax];  // 1/A[d,n] for the ZOH input term (0 where A == 0)
+  float invA[kNmax];  // 1/A[d,n] for the ZOH input term (0 where |A| < 2^-60)
   float D, bias;
   bool structured;
 };
@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(kCH, 1)
     for (int n = 0; n < kNmax; ++n) {
       const float an = (valid && n < p.N) ? *checked(p.A, static_cast<int64_t>(d) * p.N + n, nA) : 0.0f;
       ch.AL2[n] = an * kLog2e;
-      ch.invA[n] = an != 0.0f ? 1.0f / an : 0.0f;
+      ch.invA[n] = fabsf(an) >= 0x1p-60f ? 1.0f / an : 0.0f;   // below 2^-60: the A -> 0 limit Δ·B
       chd.A[n] = an;
       if (n < p.N && an != static_cast<float>(n + 1) * a0) ch.structured = false;
     }

@@ -240,8 +240,9 @@ __device__ __forceinline__ uint2 chunk_step(f2 (&h)[4], const Sc& s, Sc& ns, uin
     } else {
       // exact ZOH, any A: g_t = ρ e g_{t-1} + m B̃ with e = 2^(ℓ A[d,n]) = exp(y), y = Δ A[d,n], and
       // m = (n+1)(e - 1)/A[d,n] = Wz·(e - 1), e - 1 taken from its series y(1 + y/2 + y²/6 + y³/24)
-      // where |y| < 1/32, free of the cancellation in e - 1.  A[d,n] = 0 is held as 2^-60 (Ah, Wz),
-      // where the series gives m = (n+1)·Δ, the A -> 0 limit, and e = 1.
+      // where |y| < 1/32, free of the cancellation in e - 1.  |A[d,n]| < 2^-60 (zero or denormal,
+      // where 1/A would overflow) is held as 2^-60 (Ah, Wz): the series then gives m = (n+1)·Δ, the
+      // A -> 0 limit, and e = 1, both exact to float32 precision.
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const f2 x = f2_mul(f2_splat(q), f2_make(Ah[2 * i], Ah[2 * i + 1]));
@@ -414,8 +415,9 @@ __global__ void __launch_bounds__(kThreads, 1) scan_scaled_kernel(const __grid_c
     cc.d = cc.valid ? d : 0;
     const int64_t arow = static_cast<int64_t>(cc.d) * p.N;
     cc.A0 = *checked(p.A, arow, nA);
-    // exact ZOH divides by A[d,0]: a zero row takes the per-state path, which has the A -> 0 limit
-    bool st_ok = !kZoh || cc.A0 != 0.0f;
+    // exact ZOH divides by A[d,0]: a row with |A[d,0]| < 2^-60 (zero or denormal, where 1/A would
+    // overflow) takes the per-state path, which has the A -> 0 limit
+    bool st_ok = !kZoh || fabsf(cc.A0) >= 0x1p-60f;
     for (int n = 1; n < p.N; ++n)
       if (*checked(p.A, arow + n, nA) != static_cast<float>(n + 1) * cc.A0) st_ok = false;
     cc.structured = __all_sync(0xffffffffu, st_ok) != 0;
@@ -528,11 +530,11 @@ __global__ void __launch_bounds__(kThreads, 1) scan_scaled_kernel(const __grid_c
     auto chunks = [&](auto tag) {
       constexpr bool kS = decltype(tag)::value;
       float Ah[8];   // this lane's row of A (A not of the form (n+1)·A[d,0])
-      float Wz[8];   // exact-ZOH mode: (n+1)/A[d,n], with A[d,n] = 0 held as 2^-60 in Ah and Wz
+      float Wz[8];   // exact-ZOH mode: (n+1)/A[d,n], with |A[d,n]| < 2^-60 held as 2^-60 in Ah and Wz
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         Ah[i] = (!kS && sidx(i) < p.N) ? *checked(p.A, static_cast<int64_t>(cur.d) * p.N + sidx(i), nA) : 0.0f;
-        if (kZoh && Ah[i] == 0.0f) Ah[i] = 0x1p-60f;
+        if (kZoh && fabsf(Ah[i]) < 0x1p-60f) Ah[i] = 0x1p-60f;   // same decay and limit to float32 precision
         Wz[i] = (!kS && kZoh) ? static_cast<float>(sidx(i) + 1) / Ah[i] : 0.0f;
       }
       auto one = [&](Sc& run_sc, Sc& fill_sc, int c) {

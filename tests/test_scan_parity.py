@@ -267,6 +267,25 @@ def test_zoh_fast_path_general_A_and_zero_rows():
     _check_full(inp, y, hL, TOL[torch.bfloat16], discretization="zoh", h0=h0)
 
 
+@pytest.mark.parametrize("L", [256, 150])
+def test_zoh_tiny_and_denormal_A(L):
+    """Exact ZOH where 1/A would overflow: zero, tiny (1e-30) and denormal (1e-40) entries of A, and a
+    structured row whose A[d,0] is denormal.  Both kernels (L = 256: the fast kernel; L = 150: the
+    general one) must give the A -> 0 limit Δ·B for those states, finite everywhere."""
+    dev = _dev()
+    inp = W.random_scan_inputs(2, 136, 16, L, "bf16", seed=53 + L, device=dev)
+    A = inp["A"].clone()
+    A[3, 2] = 0.0
+    A[10, 5] = -1e-30
+    A[20, 7] = -1e-40
+    A[21, 0] = 1e-40
+    A[40, :] = 1e-39 * torch.arange(1, 17, device=dev, dtype=torch.float32)   # structured, denormal A[d,0]
+    inp["A"] = A
+    y, hL = _run(inp, discretization="zoh")
+    assert torch.isfinite(y).all() and torch.isfinite(hL).all()
+    _check_full(inp, y, hL, TOL[torch.bfloat16], discretization="zoh")
+
+
 @pytest.mark.parametrize("chunk", [64, 192])
 def test_zoh_fast_path_chunked(chunk):
     """Exact ZOH through the chunked schedule: aggregate pass, carry pass, main pass."""
