@@ -65,6 +65,13 @@ bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* bas
                           uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows, char* err,
                           size_t errlen);
 
+// Builds a 3D tiled tensor map (`outer` blocks of `rows` rows of `inner` elements, 128-byte swizzle,
+// zero fill; boxes of box_inner x box_rows x 1): coordinates past `rows` read zeros instead of the
+// next block's rows.
+bool encode_tensor_map_3d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint64_t inner, uint64_t rows,
+                          uint64_t outer, uint64_t row_pitch_bytes, uint64_t outer_pitch_bytes, uint32_t box_inner,
+                          uint32_t box_rows, char* err, size_t errlen);
+
 struct DecodeParams {
   const void* x;
   const void* delta;

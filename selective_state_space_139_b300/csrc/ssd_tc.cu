@@ -27,6 +27,8 @@
 // [64, 192) Yo (C H_hi^T then C H_lo^T), [192, 256) S^T (row n in lane n); 256 columns are allocated
 // per CTA.
 // Every mbarrier wait is bounded; on a timeout the CTA records it, stops and frees its tensor memory.
+#include <cstring>
+
 #include "internal.h"
 #include "ssm_device.cuh"
 
@@ -122,10 +124,6 @@ __device__ __forceinline__ void tc_ld_frag32(uint32_t taddr, float (&v)[16]) {
   for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-
 // fp32 pair -> bf16x2 hi and bf16x2 of the remainders
 __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
   hi = pack_bf16x2(a, b);
@@ -140,9 +138,18 @@ __device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo) {
   split2(v[6], v[7], hi.w, lo.w);
 }
 
-__global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) {
+// Tensor maps of the C, B and x tiles: (batch, L, columns) with boxes of 64 columns x 64 steps, so a
+// chunk's rows past L read zeros rather than the next batch row's.
+struct SsdMaps {
+  CUtensorMap C, B, x;
+};
+
+constexpr int kLoader = 32;   // warp 1, lane 0 issues the tile loads (thread 0 issues the MMAs)
+
+__global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_constant__ SsdMaps tm, const SsdParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bars[3];
+  __shared__ uint64_t tbar[3];   // the C, B and x tiles of a chunk have landed
   __shared__ uint32_t tmem_slot;
   __shared__ __align__(16) float s_dl[kQ];
   __shared__ __align__(16) float s_cum[kQ];
@@ -157,18 +164,16 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
   // element counts of the buffers, for the index checks of the checked build
   const int64_t nHead = p.nheads, nBH = static_cast<int64_t>(p.batch) * p.nheads;
   const int64_t nRowX = static_cast<int64_t>(p.batch) * L * p.nheads, nX = nRowX * kHd;
-  const int64_t nBC = static_cast<int64_t>(p.batch) * L * p.ngroups * kNs, nState = nBH * kHd * kNs;
+  const int64_t nState = nBH * kHd * kNs;
   const float A2 = *checked(p.A, h, nHead) * kLog2e;
   const float bias = p.dt_bias ? *checked(p.dt_bias, h, nHead) : 0.0f;
   const float Dh = p.D ? *checked(p.D, h, nHead) : 0.0f;
-  const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(p.x);
   const __nv_bfloat16* dtg = static_cast<const __nv_bfloat16*>(p.dt);
-  const __nv_bfloat16* Bg = static_cast<const __nv_bfloat16*>(p.B);
-  const __nv_bfloat16* Cg = static_cast<const __nv_bfloat16*>(p.C);
   __nv_bfloat16* yg = static_cast<__nv_bfloat16*>(p.y);
 
   if (tid == 0) {
     for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < 3; ++i) mbar_init(&tbar[i], 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -209,34 +214,23 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
   const uint32_t id_s = idesc_bf16(128, 64, 1, 1);
   const uint32_t id_yd = idesc_bf16(64, 64, 0, 1);
 
-  // tile loaders (rows past L are zero-filled); each tile of chunk c + 1 is requested as soon as the
-  // tensor cores and the threads are done with that tile of chunk c
-  // Each thread's rows and 16-byte columns of the tile loads are the same in every chunk: B/C rows
-  // bc_r0 + 16k (k < 4) at column bc_q, x rows x_r0 + 32k (k < 2) at column x_q.  Row r0 + 16k of a
-  // swizzled tile sits 2048k bytes after row r0 (the swizzle depends on r & 7 only), so the shared
-  // offsets are constants plus immediates and the global index advances by a fixed stride.  Rows past
-  // L are zero-filled from a valid address (step 0 of the sequence).
-  const int bc_r0 = tid >> 4, bc_q = tid & 15, x_r0 = tid >> 3, x_q = tid & 7;
-  const uint32_t bc_dst = static_cast<uint32_t>((bc_q >> 3) * (kQ * 128)) + sw_chunk(bc_r0, bc_q & 7);
-  const uint32_t x_dst = TcSmem::kX + sw_chunk(x_r0, x_q);
-  const int64_t bc_step = static_cast<int64_t>(p.ngroups) * kNs, x_step = static_cast<int64_t>(p.nheads) * kHd;
-  const int64_t bc_col = (static_cast<int64_t>(b) * L * p.ngroups + grp) * kNs + bc_q * 8;   // step 0
-  const int64_t x_col = (static_cast<int64_t>(b) * L * p.nheads + h) * kHd + x_q * 8;
-  auto load_bc = [&](int64_t t0, int off, const __nv_bfloat16* src_base) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int64_t r = t0 + bc_r0 + 16 * k;
-      const bool in = r < L;
-      cp_async16(sb + off + bc_dst + 2048 * k, checked(src_base, bc_col + (in ? r : 0) * bc_step, nBC, 8), in ? 16 : 0);
-    }
+  // Tile loads by TMA, issued by one thread: each tile of chunk c + 1 is requested as soon as the
+  // tensor cores and the threads are done with that tile of chunk c.  C and B are two boxes of 64
+  // columns (the two 128-byte atoms of the 128 state columns), x one box of the head's 64 columns;
+  // rows past L are zero-filled by the tensor map.
+  auto issue_c = [&](int64_t t0) {
+    mbar_arrive_expect_tx(&tbar[0], 2 * kQ * 128);
+    tma_load_3d(sm + TcSmem::kC, &tm.C, &tbar[0], grp * kNs, static_cast<int>(t0), b);
+    tma_load_3d(sm + TcSmem::kC + kQ * 128, &tm.C, &tbar[0], grp * kNs + 64, static_cast<int>(t0), b);
   };
-  auto load_x = [&](int64_t t0) {
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int64_t r = t0 + x_r0 + 32 * k;
-      const bool in = r < L;
-      cp_async16(sb + x_dst + 4096 * k, checked(xg, x_col + (in ? r : 0) * x_step, nX, 8), in ? 16 : 0);
-    }
+  auto issue_b = [&](int64_t t0) {
+    mbar_arrive_expect_tx(&tbar[1], 2 * kQ * 128);
+    tma_load_3d(sm + TcSmem::kB, &tm.B, &tbar[1], grp * kNs, static_cast<int>(t0), b);
+    tma_load_3d(sm + TcSmem::kB + kQ * 128, &tm.B, &tbar[1], grp * kNs + 64, static_cast<int>(t0), b);
+  };
+  auto issue_x = [&](int64_t t0) {
+    mbar_arrive_expect_tx(&tbar[2], kQ * 128);
+    tma_load_3d(sm + TcSmem::kX, &tm.x, &tbar[2], h * kHd, static_cast<int>(t0), b);
   };
   // dt of the next chunk is fetched as raw bf16 bits one chunk ahead and only converted (softplus)
   // when that chunk starts, so the load's latency is not waited for
@@ -250,9 +244,18 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     return p.softplus ? softplus_fast(v) : v;
   };
   const int nchunks = static_cast<int>((L + kQ - 1) / kQ);
-  load_bc(0, TcSmem::kC, Cg);
-  load_bc(0, TcSmem::kB, Bg);
-  load_x(0);
+  // tiles armed per barrier (loader thread) and chunks whose tiles every thread has waited for
+  int armed[3] = {0, 0, 0};
+  int started = 0;
+  if (tid == kLoader) {
+    prefetch_tensormap(&tm.C);
+    prefetch_tensormap(&tm.B);
+    prefetch_tensormap(&tm.x);
+    issue_c(0);
+    issue_b(0);
+    issue_x(0);
+    armed[0] = armed[1] = armed[2] = 1;
+  }
   uint32_t dt_raw0 = 0u, dt_raw1 = 0u;
   if (warp == 0) {
     dt_raw0 = load_dt_raw(2 * lane);
@@ -294,7 +297,10 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
       *reinterpret_cast<float2*>(&s_dl[2 * lane]) = make_float2(d0, d1);
       *reinterpret_cast<float2*>(&s_cum[2 * lane]) = make_float2(base + a0, s2);
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
+    ok = ok && mbar_wait_bounded(&tbar[0], par, &g_ssd_status);
+    ok = ok && mbar_wait_bounded(&tbar[1], par, &g_ssd_status);
+    ok = ok && mbar_wait_bounded(&tbar[2], par, &g_ssd_status);
+    started = c + 1;
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -350,9 +356,10 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     ok = mbar_wait_bounded(&bars[0], par, &g_ssd_status);
     ok = __all_sync(0xffffffffu, ok);   // the tensor-memory loads below are warp-collective
     tc_fence_after();
-    // the next chunk's tiles, requested unconditionally: past the last chunk every row is zero-filled
-    // from a valid address and nothing reads the result
-    load_bc(t0 + kQ, TcSmem::kC, Cg);   // G and Yo are done with C
+    if (tid == kLoader && c + 1 < nchunks) {   // G and Yo are done with C
+      issue_c(t0 + kQ);
+      ++armed[0];
+    }
     // The element-wise phases run whether or not the wait before them succeeded: after a failed
     // wait they read allocated tensor memory and write in-bounds shared and global memory (y is
     // undefined once the status word reports a timeout), and the loop leaves at the next barrier.
@@ -402,7 +409,10 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     ok = mbar_wait_bounded(&bars[1], par, &g_ssd_status);
     ok = __all_sync(0xffffffffu, ok);   // the tensor-memory loads below are warp-collective
     tc_fence_after();
-    load_bc(t0 + kQ, TcSmem::kB, Bg);   // G and S^T are done with B
+    if (tid == kLoader && c + 1 < nchunks) {   // G and S^T are done with B
+      issue_b(t0 + kQ);
+      ++armed[1];
+    }
     {
       const float eE = ex2_approx(cum_end);
       {
@@ -435,7 +445,11 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     tc_fence_before();
     ok = __syncthreads_and(ok) != 0;   // Yd and every thread are done with x
     tc_fence_after();
-    load_x(t0 + kQ);
+    if (tid == kLoader && c + 1 < nchunks) {   // Yd and every thread are done with x
+      fence_async_smem();
+      issue_x(t0 + kQ);
+      ++armed[2];
+    }
     {
       const float e0 = ex2_approx(s_cum[ri0]), e1 = ex2_approx(s_cum[ri1]);
       float yd[16], yo[16];
@@ -468,9 +482,13 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const SsdParams p) 
     ok = __syncthreads_and(ok) != 0;
     tc_fence_after();
   }
-  // every tile copy this thread requested has landed before the CTA's shared memory is released
-  // (a loop left after a failed wait may have copies in flight)
-  asm volatile("cp.async.wait_all;" ::: "memory");
+  // every tile load the loader requested has landed before the CTA's shared memory is released (a
+  // loop left after a failed wait may have loads in flight)
+  if (tid == kLoader) {
+    for (int i = 0; i < 3; ++i)
+      for (int k = started; k < armed[i]; ++k)
+        (void)mbar_wait_bounded(&tbar[i], static_cast<uint32_t>(k & 1), &g_ssd_status, 100000000ull);
+  }
   if (ok && p.hT) {
     const int64_t hT_base = (static_cast<int64_t>(b) * p.nheads + h) * kHd * kNs;
 #pragma unroll
@@ -487,9 +505,24 @@ int ssd_head_dim() { return kHd; }
 int ssd_state_dim() { return kNs; }
 
 cudaError_t ssd_fwd_launch(const SsdParams& p, cudaStream_t stream) {
+  if (p.L > 0x7fffffffLL) return cudaErrorInvalidValue;   // TMA row coordinates are 32-bit
+  SsdMaps tm;
+  memset(&tm, 0, sizeof(tm));
+  char err[160];
+  const uint64_t L = static_cast<uint64_t>(p.L), bcw = static_cast<uint64_t>(p.ngroups) * kNs,
+                 xw = static_cast<uint64_t>(p.nheads) * kHd;
+  if (!encode_tensor_map_3d(&tm.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(p.C), bcw, L, p.batch, bcw * 2,
+                            L * bcw * 2, 64, kQ, err, sizeof(err)) ||
+      !encode_tensor_map_3d(&tm.B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(p.B), bcw, L, p.batch, bcw * 2,
+                            L * bcw * 2, 64, kQ, err, sizeof(err)) ||
+      !encode_tensor_map_3d(&tm.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(p.x), xw, L, p.batch, xw * 2,
+                            L * xw * 2, 64, kQ, err, sizeof(err))) {
+    set_last_error("ssd tensor maps: %s", err);
+    return cudaErrorInvalidValue;
+  }
   cudaError_t e = cudaFuncSetAttribute(ssd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem::kDynamic);
   if (e != cudaSuccess) return e;
-  ssd_tc_kernel<<<dim3(p.nheads, p.batch), kThreads, TcSmem::kDynamic, stream>>>(p);
+  ssd_tc_kernel<<<dim3(p.nheads, p.batch), kThreads, TcSmem::kDynamic, stream>>>(tm, p);
   return cudaGetLastError();
 }
 

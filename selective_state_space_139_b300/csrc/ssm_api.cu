@@ -259,6 +259,28 @@ bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* bas
   return true;
 }
 
+bool encode_tensor_map_3d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint64_t inner, uint64_t rows,
+                          uint64_t outer, uint64_t row_pitch_bytes, uint64_t outer_pitch_bytes, uint32_t box_inner,
+                          uint32_t box_rows, char* err, size_t errlen) {
+  auto enc = tensor_map_encoder();
+  if (!enc) {
+    snprintf(err, errlen, "cuTensorMapEncodeTiled is not available");
+    return false;
+  }
+  const cuuint64_t dims[3] = {inner, rows, outer};
+  const cuuint64_t strides[2] = {row_pitch_bytes, outer_pitch_bytes};
+  const cuuint32_t box[3] = {box_inner, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, dtype, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(err, errlen, "cuTensorMapEncodeTiled failed with %d", static_cast<int>(r));
+    return false;
+  }
+  return true;
+}
+
 }  // namespace ssm
 
 extern "C" {
