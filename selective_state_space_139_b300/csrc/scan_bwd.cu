@@ -218,6 +218,52 @@ __device__ __forceinline__ void store_bc(float* bc, const uint32_t (&r)[2], bool
   bc[threadIdx.x + kThreads] = __uint_as_float(bf16 ? r[1] << 16 : r[1]);
 }
 
+// The B and C rows of one 8-step segment for the two-lane (bf16) kernels.  With 16-byte rows (L a
+// multiple of 8, B and C 16-byte aligned) and a full segment, thread t < 32 loads the segment's 8 steps
+// of row t % 16 of B (t < 16) or C (t >= 16) in one 16-byte load; otherwise every thread fetches two
+// elements as fetch_bc does (held in .x and .y).
+struct BcSeg {
+  uint4 v;
+  bool vec;
+};
+
+__device__ __forceinline__ bool bc_rows_vec(const BwdParams& p) {
+  return p.io_bf16 && p.L % kSeg == 0 &&
+         ((reinterpret_cast<uintptr_t>(p.B) | reinterpret_cast<uintptr_t>(p.C)) & 15u) == 0;
+}
+
+__device__ __forceinline__ void fetch_bc2(const BwdParams& p, int b, int64_t t0, int nk, bool rows_vec, BcSeg& r) {
+  r.vec = rows_vec && nk == kSeg;
+  if (r.vec) {
+    const int t = threadIdx.x, n = t & 15;
+    r.v = make_uint4(0u, 0u, 0u, 0u);
+    if (t < 32 && n < p.N) {
+      const int64_t idx = (static_cast<int64_t>(b) * p.N + n) * p.L + t0;
+      const int64_t nbc = static_cast<int64_t>(p.batch) * p.N * p.L;
+      const unsigned short* src = static_cast<const unsigned short*>(t < 16 ? p.B : p.C);
+      r.v = __ldg(reinterpret_cast<const uint4*>(checked(src, idx, nbc, kSeg)));
+    }
+  } else {
+    uint32_t e[2];
+    fetch_bc(p, b, t0, nk, e);
+    r.v = make_uint4(e[0], e[1], 0u, 0u);
+  }
+}
+
+__device__ __forceinline__ void store_bc2(float* bc, const BcSeg& r) {
+  if (r.vec) {
+    if (threadIdx.x < 32) {
+      float f[kSeg];
+      unpack_chunk(r.v, f, __nv_bfloat16());
+#pragma unroll
+      for (int k = 0; k < kSeg; ++k) bc[k * 32 + threadIdx.x] = f[k];
+    }
+  } else {
+    const uint32_t e[2] = {r.v.x, r.v.y};
+    store_bc(bc, e, true);
+  }
+}
+
 // One checkpoint record: 16 states, 64 (float) or 128 (double) bytes, 16-byte aligned.
 __device__ __forceinline__ void store_ckpt(float* dst, const Pair<float> (&h)[kP]) {
 #pragma unroll
@@ -417,10 +463,11 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_fwd2_kernel(const BwdParams p
   float* const cs = static_cast<float*>(p.ckpt_s) + cs_row;
   auto seg_len = [&](int64_t t0) { return static_cast<int>(c1 - t0 < kSeg ? c1 - t0 : kSeg); };
   SegRaw<IO> raw;
-  uint32_t bcr[2];
+  BcSeg bcr;
+  const bool rows_vec = bc_rows_vec(p);
   fetch_seg<IO>(p, row * p.L + c0, seg_len(c0), raw);
-  fetch_bc(p, b, c0, seg_len(c0), bcr);
-  store_bc(bc_buf[0], bcr, p.io_bf16);
+  fetch_bc2(p, b, c0, seg_len(c0), rows_vec, bcr);
+  store_bc2(bc_buf[0], bcr);
   __syncthreads();
   int buf = 0;
   for (int64_t t0 = c0; t0 < c1; t0 += kSeg) {
@@ -434,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_fwd2_kernel(const BwdParams p
     const bool more = tn < c1;
     if (more) {
       fetch_seg<IO>(p, row * p.L + tn, seg_len(tn), raw);
-      fetch_bc(p, b, tn, seg_len(tn), bcr);
+      fetch_bc2(p, b, tn, seg_len(tn), rows_vec, bcr);
     }
     if (valid) {
       const int64_t sgi = t0 / kSeg;
@@ -461,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_fwd2_kernel(const BwdParams p
         }
       }
     }
-    if (more) store_bc(bc_buf[buf ^ 1], bcr, p.io_bf16);
+    if (more) store_bc2(bc_buf[buf ^ 1], bcr);
     __syncthreads();
     buf ^= 1;
   }
@@ -851,7 +898,8 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
   };
   const int64_t last = c0 + ((c1 - c0 - 1) / kSeg) * kSeg;
   SegRaw<IO> raw;
-  uint32_t bcr[2];
+  BcSeg bcr;
+  const bool rows_vec = bc_rows_vec(p);
   float2 ckp[kP2];   // checkpoint pairs, in slot order
   float ckS;
   auto fetch_ck = [&](int64_t t0) {
@@ -862,9 +910,9 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
     ckS = *checked(cs, sgi, Z.nCs - cs_row);
   };
   fetch_seg<IO>(p, row * p.L + last, seg_len(last), raw);
-  fetch_bc(p, b, last, seg_len(last), bcr);
+  fetch_bc2(p, b, last, seg_len(last), rows_vec, bcr);
   fetch_ck(last);
-  store_bc(bc_base, bcr, p.io_bf16);
+  store_bc2(bc_base, bcr);
   __syncthreads();
   int buf = 0;
   int64_t pend_t0 = -1;
@@ -894,7 +942,7 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
     const bool more = tn >= c0;
     if (more) {
       fetch_seg<IO>(p, row * p.L + tn, seg_len(tn), raw);
-      fetch_bc(p, b, tn, seg_len(tn), bcr);
+      fetch_bc2(p, b, tn, seg_len(tn), rows_vec, bcr);
       fetch_ck(tn);
     }
     if (pend_t0 >= 0) flush_red(red_base + (buf ^ 1) * (4 * kSeg * 32), pend_t0, pend_nk);
@@ -1013,7 +1061,7 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_rev2_kernel(const BwdParams p
       store_seg<IO, float>(p.du, off, nk, p.vec_io, gdu, Z.nIO);
       store_seg<IO, float>(p.ddelta, off, nk, p.vec_io, gdd, Z.nIO);
     }
-    if (more) store_bc(bc_base + (buf ^ 1) * (kSeg * 32), bcr, p.io_bf16);
+    if (more) store_bc2(bc_base + (buf ^ 1) * (kSeg * 32), bcr);
     __syncthreads();
     pend_t0 = t0;
     pend_nk = nk;
