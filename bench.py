@@ -497,15 +497,18 @@ def measure_ssd(dev, rank, reps=10):
     inp = W.make_ssd_inputs(w, device=dev, seed=w.seed + rank)
     y = torch.empty_like(inp["x"])
     hT = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), device=dev)
+    ws_bytes = ssm.ssd_workspace_size(w.batch, w.seqlen, w.nheads)   # balanced schedule: carries and flags
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
 
     def call():
         ssm.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], D=inp["D"], dt_bias=inp["dt_bias"], out=y,
-                    final_state=hT)
+                    final_state=hT, workspace=ws)
     for _ in range(3):
         call()
     ms = _time_back_to_back(call, reps, dev)
     return {"workload": w, "ms": ms, "tokens_per_s": w.tokens / (ms * 1e-3),
-            "tflops": w.flops() / (ms * 1e-3) / 1e12, "achieved_gbs": w.algorithmic_bytes() / (ms * 1e-3) / 1e9}
+            "tflops": w.flops() / (ms * 1e-3) / 1e12, "achieved_gbs": w.algorithmic_bytes() / (ms * 1e-3) / 1e9,
+            "schedule": "balanced" if ws_bytes else "one CTA per sequence", "workspace_bytes": ws_bytes}
 
 
 def measure_ssd_decode(dev, rank):
@@ -792,7 +795,8 @@ def main():
                        "roofline": {"bound": "tensor", "achieved": ssd["tflops"], "peak": tpeak, "unit": "TFLOP/s",
                                     "frac": ssd["tflops"] / tpeak, "peak_source": tkind,
                                     "flops_per_call": sw.flops()},
-                       "achieved_gbs": ssd["achieved_gbs"], "hbm_frac": ssd["achieved_gbs"] / peak}
+                       "achieved_gbs": ssd["achieved_gbs"], "hbm_frac": ssd["achieved_gbs"] / peak,
+                       "schedule": ssd["schedule"], "workspace_bytes": ssd["workspace_bytes"]}
     if ssd_dec is not None:
         dw = ssd_dec["workload"]
         line["ssd_decode"] = {"workload": f"{dw.name} (batch {dw.batch}, {dw.nheads} heads x {dw.headdim}, "

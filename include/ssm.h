@@ -259,15 +259,49 @@ SSM_API ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A
  * This build implements io_dtype SSM_BF16 with headdim 64 and dstate 128 (the pages' Mamba-2
  * geometry); other values return SSM_ERR_UNSUPPORTED.  x, B, C and y must be 16-byte aligned, h0 and
  * final_state 8-byte aligned.  Accumulation and the state are float32 (tensor-core products with the
- * computed operand split into two bf16 terms); no workspace.  The kernel's waits for its tensor-core
- * results are bounded: y and final_state are defined once ssm_device_status() has returned SSM_OK for
- * the stream (SSM_ERR_TIMEOUT: a wait gave up; y and final_state are then undefined, and no other
- * memory is written).
+ * computed operand split into two bf16 terms).  One CTA per (batch, head) sequence, no workspace (see
+ * ssm_ssd_fwd_ex for the balanced schedule).  The kernel's waits for its tensor-core results are
+ * bounded: y and final_state are defined once ssm_device_status() has returned SSM_OK for the stream
+ * (SSM_ERR_TIMEOUT: a wait gave up; y and final_state are then undefined, and no other memory is
+ * written).
  */
 SSM_API ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void* B, const void* C,
                                const float* D, const float* dt_bias, int softplus_flag, const float* h0, void* y,
                                float* final_state, int batch, int64_t seqlen, int nheads, int headdim, int dstate,
                                int ngroups, ssm_dtype io_dtype, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace ssm_ssd_fwd_ex needs for its balanced schedule on the current device:
+ * nonzero when there are more (batch, head) sequences than CTAs of the kernel fit on the device at
+ * once (or than `ctas`, when ctas > 0), 0 when one CTA per sequence runs (the workspace is then not
+ * used).  Returns 0 for invalid sizes or without a device.
+ */
+SSM_API size_t ssm_ssd_fwd_workspace_size(int batch, int64_t seqlen, int nheads, int ctas);
+
+/*
+ * ssm_ssd_fwd with a balanced schedule.  One CTA per sequence leaves the last wave of CTAs partly
+ * empty when the sequences outnumber the co-resident CTAs (512 sequences on 296 resident CTAs: two
+ * waves, the second 73 % full).  Given a workspace, the (sequence, 64-step chunk) units laid end to
+ * end are cut into equal ranges, one per co-resident CTA; a sequence split between two ranges passes
+ * its state from one CTA to the next through the workspace (the chunk-to-chunk state passing of
+ * "Модуль 8", §7), published behind a flag and waited for with a 2 s limit (SSM_ERR_TIMEOUT from
+ * ssm_device_status() if it runs out).  CTAs take their ranges in the order they start, so a CTA
+ * only waits for one that is already running.
+ *   workspace, workspace_bytes : NULL (one CTA per sequence, as ssm_ssd_fwd), or a device buffer of
+ *                                at least ssm_ssd_fwd_workspace_size(batch, seqlen, nheads, ctas)
+ *                                bytes, 256-byte aligned, no initial contents, not overlapping the
+ *                                inputs or outputs; owned by the caller and not used after the
+ *                                stream reaches the end of the call
+ *   ctas                       : 0 = one range per co-resident CTA; > 0 = at most that many ranges
+ * Results equal ssm_ssd_fwd's up to rounding order (the same arithmetic per chunk).  Other arguments,
+ * the requirements and the status as ssm_ssd_fwd; SSM_ERR_INVALID_ARG also for ctas < 0, a too small
+ * or misaligned workspace, or one that overlaps y or final_state.
+ */
+SSM_API ssm_status ssm_ssd_fwd_ex(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                                  const float* D, const float* dt_bias, int softplus_flag, const float* h0, void* y,
+                                  float* final_state, int batch, int64_t seqlen, int nheads, int headdim, int dstate,
+                                  int ngroups, ssm_dtype io_dtype, void* workspace, size_t workspace_bytes, int ctas,
+                                  cudaStream_t stream);
 
 /*
  * One-token decode step of a Mamba-2 (SSD) layer, updating its state cache in place ("Модуль 8", §14:
@@ -301,15 +335,16 @@ SSM_API ssm_status ssm_ssd_state_update(const void* x_t, const void* dt_t, const
 SSM_API ssm_status ssm_selftest_bounded_wait(int which, int64_t limit_ns, cudaStream_t stream);
 
 /*
- * Diagnostic of the balanced schedule's carry wait, on the real prefill kernels; the pages have no
- * counterpart.  Arms a one-shot fault for the next ssm_scan_fwd / ssm_scan_fwd_ex call made on the
- * calling host thread: if that call runs the balanced schedule (ssm_scan_fwd_describe: schedule 1),
- * CTA `cta` computes and writes its carry but never raises the flag that publishes it, and the carry
- * wait of every CTA is limited to limit_ns nanoseconds (clamped to 1 ms .. 2 s).  CTA cta + 1 then
- * gives up its wait, records a timeout in the device status word and finishes its range from a zero
- * state; the next ssm_device_status() returns SSM_ERR_TIMEOUT.  Nothing faults or waits without a
- * limit, and the context stays usable.  A call with another schedule consumes the arming without
- * effect.  Returns SSM_ERR_INVALID_ARG for cta < 0.
+ * Diagnostic of the balanced schedule's carry wait, on the real prefill and SSD kernels; the pages
+ * have no counterpart.  Arms a one-shot fault for the next ssm_scan_fwd / ssm_scan_fwd_ex /
+ * ssm_ssd_fwd / ssm_ssd_fwd_ex call made on the calling host thread: if that call runs a balanced
+ * schedule (ssm_scan_fwd_describe: schedule 1; ssm_ssd_fwd_ex with a workspace), CTA `cta` computes
+ * and writes its carry but never raises the flag that publishes it, and the carry wait of every CTA
+ * is limited to limit_ns nanoseconds (clamped to 1 ms .. 2 s).  CTA cta + 1 then gives up its wait,
+ * records a timeout in the device status word and finishes its range from a zero state; the next
+ * ssm_device_status() returns SSM_ERR_TIMEOUT.  Nothing faults or waits without a limit, and the
+ * context stays usable.  A call with another schedule consumes the arming without effect.  Returns
+ * SSM_ERR_INVALID_ARG for cta < 0.
  */
 SSM_API ssm_status ssm_selftest_withhold_carry(int cta, int64_t limit_ns);
 

@@ -166,11 +166,21 @@ struct SsdParams {
   int batch, nheads, ngroups;
   int64_t L;
   int softplus;
+  // balanced persistent schedule (0: one CTA per sequence)
+  int balanced;
+  int64_t range;            // (sequence, chunk) units per CTA
+  float* carry;             // (ranges, 64, 128): each range's state at the end of its head
+  unsigned* flags;          // (ranges + 1): the carry is published; then the range counter; cleared
+                            // before the launch
+  int test_withhold_cta;    // diagnostic: this range never publishes its carry (-1: none)
+  uint64_t carry_wait_ns;   // limit of the carry wait (0: 2 s)
 };
 
 int ssd_head_dim();
 int ssd_state_dim();
-cudaError_t ssd_fwd_launch(const SsdParams& p, cudaStream_t stream);
+int ssd_resident_ctas();   // co-resident CTAs of the SSD kernel on the current device (0 if unknown)
+// balanced_ctas: the ranges (and CTAs) of the balanced schedule (p.balanced), ignored otherwise
+cudaError_t ssd_fwd_launch(const SsdParams& p, int balanced_ctas, cudaStream_t stream);
 
 // Mamba-2 decode step (ssd_decode.cu): one token, state (batch, nheads, 64, 128) float32 in place.
 struct SsdDecodeParams {

@@ -5,7 +5,8 @@
 // state passed between chunks; §14: state [batch, nheads, headdim, d_state], input term Δ·B·x):
 //   y_i = Σ_{j≤i} (C_i·B_j) e^{cum_i − cum_j} Δ_j x_j + e^{cum_i} C_i·H + D_h x_i
 //   H  <- e^{cum_end} H + Σ_j e^{cum_end − cum_j} Δ_j x_j B_j^T
-// over chunks of 64 steps, one CTA (8 warps) per (batch, head), two CTAs per SM.
+// over chunks of 64 steps, one CTA (8 warps) per (batch, head) or per balanced range of chunks, two CTAs
+// per SM.
 //
 // Per chunk, four tcgen05.mma groups (bf16 operands from 128-byte-swizzled shared tiles, fp32
 // accumulators in tensor memory):
@@ -27,9 +28,11 @@
 // [64, 192) Yo (C H_hi^T then C H_lo^T), [192, 256) S^T (row n in lane n); 256 columns are allocated
 // per CTA.
 // Every mbarrier wait is bounded; on a timeout the CTA records it, stops and frees its tensor memory.
+#include <algorithm>
 #include <cstring>
 
 #include "internal.h"
+#include "scan_walk.cuh"
 #include "ssm_device.cuh"
 
 namespace ssm {
@@ -145,31 +148,88 @@ struct SsdMaps {
 };
 
 constexpr int kLoader = 32;   // warp 1, lane 0 issues the tile loads (thread 0 issues the MMAs)
+constexpr uint64_t kCarryWaitNs = 2000000000ull;
 
+// A sequence (batch row b, head h) of the walk and its per-head constants.
+struct SsdSeq {
+  int b, h, grp;
+  float A2;     // A[h]·log2(e)
+  float bias;   // dt_bias[h]
+  float Dh;     // D[h]
+};
+
+// One CTA walks a list of (sequence, chunk) units in order: one whole sequence (kBal false: one CTA per
+// sequence), or one of the equal ranges of the balanced schedule (kBal true; scan_walk.cuh: the
+// sequences' chunks laid end to end, one range per resident CTA; the head of the range's last sequence
+// first, its state published for the range after it, then the complete sequences, then the tail of
+// the first sequence from the state the range before it published).  512 sequences of the 4 x 128-head
+// layer on 296 resident CTAs are otherwise two waves, the second 73 % full.  A CTA takes its range
+// index from a counter when it starts, so the range it waits for belongs to a CTA that started earlier
+// and runs its head before anything it could wait for: no deadlock, whether or not every CTA is
+// resident at once.
+template <bool kBal>
 __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_constant__ SsdMaps tm, const SsdParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bars[3];
   __shared__ uint64_t tbar[3];   // the C, B and x tiles of a chunk have landed
   __shared__ uint32_t tmem_slot;
+  __shared__ int s_carry_ok;
+  __shared__ int s_range;
   __shared__ __align__(16) float s_dl[kQ];
   __shared__ __align__(16) float s_cum[kQ];
+  const int64_t L = p.L;
+  const int nchunks = static_cast<int>((L + kQ - 1) / kQ);
+  const int64_t nseq = static_cast<int64_t>(p.batch) * p.nheads;
+  int range = blockIdx.x;
+  if (kBal) {
+    if (threadIdx.x == 0) s_range = static_cast<int>(atomicAdd(p.flags + gridDim.x, 1u));
+    __syncthreads();
+    range = s_range;
+  }
+  const Walk w = kBal ? make_walk_balanced(range, p.range, nseq * nchunks, nchunks)
+                      : make_walk_grid(range, 0, nchunks, nchunks);
+  if (w.total() <= 0) return;
   // 1024-byte aligned tile base, derived by pointer arithmetic on the shared array so that the compiler
   // keeps shared-space loads and stores (an integer round trip would make them generic)
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(sm);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int h = blockIdx.x, b = blockIdx.y;
-  const int grp = h / (p.nheads / p.ngroups);
-  const int64_t L = p.L;
   // element counts of the buffers, for the index checks of the checked build
-  const int64_t nHead = p.nheads, nBH = static_cast<int64_t>(p.batch) * p.nheads;
+  const int64_t nHead = p.nheads;
   const int64_t nRowX = static_cast<int64_t>(p.batch) * L * p.nheads, nX = nRowX * kHd;
-  const int64_t nState = nBH * kHd * kNs;
-  const float A2 = *checked(p.A, h, nHead) * kLog2e;
-  const float bias = p.dt_bias ? *checked(p.dt_bias, h, nHead) : 0.0f;
-  const float Dh = p.D ? *checked(p.D, h, nHead) : 0.0f;
+  const int64_t nState = nseq * kHd * kNs;
+  const int64_t nCarry = static_cast<int64_t>(gridDim.x) * kHd * kNs;
+  const int hpg = p.nheads / p.ngroups;
   const __nv_bfloat16* dtg = static_cast<const __nv_bfloat16*>(p.dt);
   __nv_bfloat16* yg = static_cast<__nv_bfloat16*>(p.y);
+  auto seq_of = [&](int64_t g, SsdSeq& s) {
+    s.b = static_cast<int>(g / p.nheads);
+    s.h = static_cast<int>(g - static_cast<int64_t>(s.b) * p.nheads);
+    s.grp = s.h / hpg;
+    s.A2 = *checked(p.A, s.h, nHead) * kLog2e;
+    s.bias = p.dt_bias ? *checked(p.dt_bias, s.h, nHead) : 0.0f;
+    s.Dh = p.D ? *checked(p.D, s.h, nHead) : 0.0f;
+  };
+  // The walk as segments, each one sequence's chunks [c0, c1): the head, the complete sequences, the
+  // tail (any of them may be absent).
+  const int64_t n_whole = w.n_full / nchunks;
+  const int64_t nseg = kBal ? (w.n_head > 0 ? 1 : 0) + n_whole + (w.n_tail > 0 ? 1 : 0) : 1;
+  auto seg_at = [&](int64_t si, int64_t& gs, int& c0, int& c1) {
+    if (!kBal) { gs = range; c0 = 0; c1 = nchunks; return; }
+    if (w.n_head > 0) {
+      if (si == 0) { gs = w.g_head; c0 = 0; c1 = static_cast<int>(w.tb); return; }
+      --si;
+    }
+    if (si < n_whole) { gs = w.gf0 + si; c0 = 0; c1 = nchunks; return; }
+    gs = w.g_tail; c0 = static_cast<int>(w.ta); c1 = nchunks;
+  };
+  auto is_head = [&](int64_t si) { return kBal && w.n_head > 0 && si == 0; };
+  auto is_tail = [&](int64_t si) { return kBal && w.n_tail > 0 && si == nseg - 1; };
+  int64_t gs = 0;   // the current segment: sequence gs, chunks [c0, c1)
+  int c0 = 0, c1 = 0;
+  seg_at(0, gs, c0, c1);
+  SsdSeq cur;
+  seq_of(gs, cur);
 
   if (tid == 0) {
     for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
@@ -187,18 +247,77 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
   const int n_own = tid & 127;
   const int pbase = 32 * half;
   float H[kHd / 2];
-  {
-    const int64_t h0_base = (static_cast<int64_t>(b) * p.nheads + h) * kHd * kNs;
-#pragma unroll
-    for (int q = 0; q < kHd / 2; ++q) H[q] = p.h0 ? *checked(p.h0, h0_base + (pbase + q) * kNs + n_own, nState) : 0.0f;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint4 hi, lo;
-      split8(&H[c * 8], hi, lo);
-      *reinterpret_cast<uint4*>(sm + TcSmem::kHh + sw_chunk(n_own, 4 * half + c)) = hi;
-      *reinterpret_cast<uint4*>(sm + TcSmem::kHl + sw_chunk(n_own, 4 * half + c)) = lo;
+  bool ok = true;
+  // The state entering segment si (sequence sg): the state the previous CTA published (the tail of a
+  // balanced range; zero if that wait gives up), h0 of the sequence, or zero.
+  auto init_state = [&](int64_t si, int64_t sg) {
+    const float* src = nullptr;
+    bool carried = false;
+    if (is_tail(si)) {
+      if (tid == 0) {
+        const unsigned* flag = checked(p.flags, static_cast<int64_t>(range) - 1, gridDim.x);
+        const uint64_t limit = p.carry_wait_ns ? p.carry_wait_ns : kCarryWaitNs;
+        const uint64_t t_start = globaltimer_ns();
+        int got = 0;
+        while (true) {
+          unsigned v;
+          asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+          if (v != 0u) { got = 1; break; }
+          if (globaltimer_ns() - t_start > limit) break;
+          __nanosleep(256);
+        }
+        if (!got) atomicOr(&g_ssd_status, kStatusTimeout);
+        s_carry_ok = got;
+      }
+      __syncthreads();
+      if (s_carry_ok) {
+        src = p.carry + (static_cast<int64_t>(range) - 1) * kHd * kNs;
+        carried = true;
+      }
+    } else if (p.h0) {
+      src = p.h0 + sg * kHd * kNs;
     }
-  }
+#pragma unroll
+    for (int q = 0; q < kHd / 2; ++q) {
+      const int64_t i = (pbase + q) * kNs + n_own;
+      H[q] = !src ? 0.0f
+                  : carried ? __ldcg(checked(src, i, nCarry - (static_cast<int64_t>(range) - 1) * kHd * kNs))
+                            : *checked(src, i, nState - sg * kHd * kNs);
+    }
+  };
+  // The state leaving segment si (sequence sg): published for the next CTA (the head of a balanced
+  // range) once every thread has written its part, or written to final_state.
+  auto finish_state = [&](int64_t si, int64_t sg) {
+    if (is_head(si)) {
+      const int64_t base = static_cast<int64_t>(range) * kHd * kNs;
+#pragma unroll
+      for (int q = 0; q < kHd / 2; ++q) *checked(p.carry, base + (pbase + q) * kNs + n_own, nCarry) = H[q];
+      __syncthreads();
+      if (tid == 0 && range != p.test_withhold_cta) {
+        __threadfence();
+        asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.flags + range), "r"(1u) : "memory");
+      }
+    } else if (ok && p.hT) {
+#pragma unroll
+      for (int q = 0; q < kHd / 2; ++q) *checked(p.hT, sg * kHd * kNs + (pbase + q) * kNs + n_own, nState) = H[q];
+    }
+  };
+  // the state tiles H^T hi and lo [n][p] the next C·H^T product reads
+  auto store_state_tiles = [&](uint32_t state_off, int s3) {
+#pragma unroll
+    for (int c8 = 0; c8 < 4; ++c8) {
+      uint4 hi, lo;
+      split8(&H[c8 * 8], hi, lo);
+      const uint32_t o = state_off + ((c8 ^ s3) << 4);
+      *reinterpret_cast<uint4*>(sm + TcSmem::kHh + o) = hi;
+      *reinterpret_cast<uint4*>(sm + TcSmem::kHl + o) = lo;
+    }
+  };
+  const uint32_t state_off =
+      static_cast<uint32_t>((n_own >> 3) * 1024 + (n_own & 7) * 128 + (((4 * half) ^ (n_own & 4)) << 4));
+  const int s3 = n_own & 3;
+  init_state(0, gs);
+  store_state_tiles(state_off, s3);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -214,52 +333,51 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
   const uint32_t id_s = idesc_bf16(128, 64, 1, 1);
   const uint32_t id_yd = idesc_bf16(64, 64, 0, 1);
 
-  // Tile loads by TMA, issued by one thread: each tile of chunk c + 1 is requested as soon as the
-  // tensor cores and the threads are done with that tile of chunk c.  C and B are two boxes of 64
+  // Tile loads by TMA, issued by one thread: each tile of unit k + 1 is requested as soon as the
+  // tensor cores and the threads are done with that tile of unit k.  C and B are two boxes of 64
   // columns (the two 128-byte atoms of the 128 state columns), x one box of the head's 64 columns;
   // rows past L are zero-filled by the tensor map.
-  auto issue_c = [&](int64_t t0) {
+  auto issue_c = [&](int grp, int b, int t0) {
     mbar_arrive_expect_tx(&tbar[0], 2 * kQ * 128);
-    tma_load_3d(sm + TcSmem::kC, &tm.C, &tbar[0], grp * kNs, static_cast<int>(t0), b);
-    tma_load_3d(sm + TcSmem::kC + kQ * 128, &tm.C, &tbar[0], grp * kNs + 64, static_cast<int>(t0), b);
+    tma_load_3d(sm + TcSmem::kC, &tm.C, &tbar[0], grp * kNs, t0, b);
+    tma_load_3d(sm + TcSmem::kC + kQ * 128, &tm.C, &tbar[0], grp * kNs + 64, t0, b);
   };
-  auto issue_b = [&](int64_t t0) {
+  auto issue_b = [&](int grp, int b, int t0) {
     mbar_arrive_expect_tx(&tbar[1], 2 * kQ * 128);
-    tma_load_3d(sm + TcSmem::kB, &tm.B, &tbar[1], grp * kNs, static_cast<int>(t0), b);
-    tma_load_3d(sm + TcSmem::kB + kQ * 128, &tm.B, &tbar[1], grp * kNs + 64, static_cast<int>(t0), b);
+    tma_load_3d(sm + TcSmem::kB, &tm.B, &tbar[1], grp * kNs, t0, b);
+    tma_load_3d(sm + TcSmem::kB + kQ * 128, &tm.B, &tbar[1], grp * kNs + 64, t0, b);
   };
-  auto issue_x = [&](int64_t t0) {
+  auto issue_x = [&](int h, int b, int t0) {
     mbar_arrive_expect_tx(&tbar[2], kQ * 128);
-    tma_load_3d(sm + TcSmem::kX, &tm.x, &tbar[2], h * kHd, static_cast<int>(t0), b);
+    tma_load_3d(sm + TcSmem::kX, &tm.x, &tbar[2], h * kHd, t0, b);
   };
-  // dt of the next chunk is fetched as raw bf16 bits one chunk ahead and only converted (softplus)
-  // when that chunk starts, so the load's latency is not waited for
+  // dt of the next unit is fetched as raw bf16 bits one unit ahead and only converted (softplus)
+  // when that unit starts, so the load's latency is not waited for
   const unsigned short* dtr = reinterpret_cast<const unsigned short*>(dtg);
-  auto load_dt_raw = [&](int64_t t) -> uint32_t {
-    return t < L ? static_cast<uint32_t>(*checked(dtr, (static_cast<int64_t>(b) * L + t) * p.nheads + h, nRowX)) : 0u;
+  auto load_dt_raw = [&](int b, int h, int64_t tt) -> uint32_t {
+    return tt < L ? static_cast<uint32_t>(*checked(dtr, (static_cast<int64_t>(b) * L + tt) * p.nheads + h, nRowX)) : 0u;
   };
-  auto dl_of = [&](uint32_t raw, int64_t t) -> float {
-    if (t >= L) return 0.0f;
-    const float v = __uint_as_float(raw << 16) + bias;
+  auto dl_of = [&](uint32_t raw, int64_t tt) -> float {
+    if (tt >= L) return 0.0f;
+    const float v = __uint_as_float(raw << 16) + cur.bias;
     return p.softplus ? softplus_fast(v) : v;
   };
-  const int nchunks = static_cast<int>((L + kQ - 1) / kQ);
-  // tiles armed per barrier (loader thread) and chunks whose tiles every thread has waited for
-  int armed[3] = {0, 0, 0};
-  int started = 0;
+  // tiles armed per barrier (loader thread) and units whose tiles every thread has waited for
+  int64_t armed[3] = {0, 0, 0};
+  int64_t started = 0;
   if (tid == kLoader) {
     prefetch_tensormap(&tm.C);
     prefetch_tensormap(&tm.B);
     prefetch_tensormap(&tm.x);
-    issue_c(0);
-    issue_b(0);
-    issue_x(0);
+    issue_c(cur.grp, cur.b, c0 * kQ);
+    issue_b(cur.grp, cur.b, c0 * kQ);
+    issue_x(cur.h, cur.b, c0 * kQ);
     armed[0] = armed[1] = armed[2] = 1;
   }
   uint32_t dt_raw0 = 0u, dt_raw1 = 0u;
   if (warp == 0) {
-    dt_raw0 = load_dt_raw(2 * lane);
-    dt_raw1 = load_dt_raw(2 * lane + 1);
+    dt_raw0 = load_dt_raw(cur.b, cur.h, static_cast<int64_t>(c0) * kQ + 2 * lane);
+    dt_raw1 = load_dt_raw(cur.b, cur.h, static_cast<int64_t>(c0) * kQ + 2 * lane + 1);
   }
   // Shared-tile offsets that are the same in every chunk.  Row r's 16-byte chunk c sits at
   // sw_chunk(r, c); for the fragment rows ri0 = 16·quad + fg (and ri1 = ri0 + 8, 1024 bytes further) and
@@ -269,230 +387,247 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
   const int ri0 = quad * 16 + fg, ri1 = ri0 + 8;       // its two rows of the M = 64 results
   const uint32_t frag_off = static_cast<uint32_t>(quad * 2048 + fg * 128 + (((4 * half) ^ (fg & 4)) << 4) + 4 * ft);
   const int f3 = fg & 3;
-  const uint32_t state_off = static_cast<uint32_t>((n_own >> 3) * 1024 + (n_own & 7) * 128 + (((4 * half) ^ (n_own & 4)) << 4));
-  const int s3 = n_own & 3;
   const int jw = tid >> 2;                             // the w ∘ x row of this thread, chunks cw and cw + 1
   const uint32_t w_off0 = sw_chunk(jw, (tid & 3) * 2), w_off1 = sw_chunk(jw, (tid & 3) * 2 + 1);
   const int64_t y_step = static_cast<int64_t>(p.nheads) * kHd;   // elements per time step of x and y
-  const int64_t y_row0 = ((static_cast<int64_t>(b) * L + ri0) * p.nheads + h) * kHd;
-  bool ok = true;
-  for (int c = 0; c < nchunks && ok; ++c) {
-    const int64_t t0 = static_cast<int64_t>(c) * kQ;
-    const uint32_t par = static_cast<uint32_t>(c & 1);
-    // ---- P0: Δ and its inclusive prefix sum over the chunk, by warp 0 (two steps per lane); the
-    // chunk's tiles were requested during the previous chunk
-    if (warp == 0) {
-      const float d0 = dl_of(dt_raw0, t0 + 2 * lane), d1 = dl_of(dt_raw1, t0 + 2 * lane + 1);
-      dt_raw0 = load_dt_raw(t0 + kQ + 2 * lane);   // zero past L
-      dt_raw1 = load_dt_raw(t0 + kQ + 2 * lane + 1);
-      const float a0 = d0 * A2;
-      float s2 = a0 + d1 * A2;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float u = __shfl_up_sync(0xffffffffu, s2, o);
-        if (lane >= o) s2 += u;
-      }
-      const float before = __shfl_up_sync(0xffffffffu, s2, 1);
-      const float base = lane > 0 ? before : 0.0f;
-      *reinterpret_cast<float2*>(&s_dl[2 * lane]) = make_float2(d0, d1);
-      *reinterpret_cast<float2*>(&s_cum[2 * lane]) = make_float2(base + a0, s2);
+  int64_t k = 0;   // units (chunks) run so far: the parity of every barrier phase
+  for (int64_t si = 0; si < nseg && ok; ++si) {
+    // the next segment, whose first chunk is requested during this segment's last one
+    const bool more_seg = si + 1 < nseg;
+    int64_t gs_n = gs;
+    int c0_n = 0, c1_n = 0;
+    SsdSeq nx = cur;
+    if (more_seg) {
+      seg_at(si + 1, gs_n, c0_n, c1_n);
+      seq_of(gs_n, nx);
     }
-    ok = ok && mbar_wait_bounded(&tbar[0], par, &g_ssd_status);
-    ok = ok && mbar_wait_bounded(&tbar[1], par, &g_ssd_status);
-    ok = ok && mbar_wait_bounded(&tbar[2], par, &g_ssd_status);
-    started = c + 1;
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
+    const int64_t y_base = ((static_cast<int64_t>(cur.b) * L + ri0) * p.nheads + cur.h) * kHd;
+    for (int c = c0; c < c1 && ok; ++c, ++k) {
+      const int64_t t0 = static_cast<int64_t>(c) * kQ;
+      const uint32_t par = static_cast<uint32_t>(k & 1);
+      // the next unit: chunk c + 1 of this sequence, or the next segment's first chunk
+      const bool last = c + 1 == c1;
+      const bool more = !last || more_seg;
+      const int nb = last ? nx.b : cur.b, nh = last ? nx.h : cur.h, ngrp = last ? nx.grp : cur.grp;
+      const int nt0 = (last ? c0_n : c + 1) * kQ;
+      // ---- P0: Δ and its inclusive prefix sum over the chunk, by warp 0 (two steps per lane); the
+      // chunk's tiles were requested during the previous unit
+      if (warp == 0) {
+        const float d0 = dl_of(dt_raw0, t0 + 2 * lane), d1 = dl_of(dt_raw1, t0 + 2 * lane + 1);
+        if (more) {
+          dt_raw0 = load_dt_raw(nb, nh, nt0 + 2 * lane);   // zero past L
+          dt_raw1 = load_dt_raw(nb, nh, nt0 + 2 * lane + 1);
+        }
+        const float a0 = d0 * cur.A2;
+        float s2 = a0 + d1 * cur.A2;
+  #pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float u = __shfl_up_sync(0xffffffffu, s2, o);
+          if (lane >= o) s2 += u;
+        }
+        const float before = __shfl_up_sync(0xffffffffu, s2, 1);
+        const float base = lane > 0 ? before : 0.0f;
+        *reinterpret_cast<float2*>(&s_dl[2 * lane]) = make_float2(d0, d1);
+        *reinterpret_cast<float2*>(&s_cum[2 * lane]) = make_float2(base + a0, s2);
+      }
+      ok = ok && mbar_wait_bounded(&tbar[0], par, &g_ssd_status);
+      ok = ok && mbar_wait_bounded(&tbar[1], par, &g_ssd_status);
+      ok = ok && mbar_wait_bounded(&tbar[2], par, &g_ssd_status);
+      started = k + 1;
+      fence_async_smem();
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
 
-    // ---- P1: G = C B^T and Yo = C H^T on the tensor cores; meanwhile w ∘ x on the CUDA cores
-    if (tid == 0) {
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t ka = (ks >> 2) * (kQ * 128) + (ks & 3) * 32;
-        tc_mma(tmem + 0, dadd(dK, TcSmem::kC + ka), dadd(dK, TcSmem::kB + ka), id_g, ks > 0);
+      // ---- P1: G = C B^T and Yo = C H^T on the tensor cores; meanwhile w ∘ x on the CUDA cores
+      if (tid == 0) {
+  #pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t ka = (ks >> 2) * (kQ * 128) + (ks & 3) * 32;
+          tc_mma(tmem + 0, dadd(dK, TcSmem::kC + ka), dadd(dK, TcSmem::kB + ka), id_g, ks > 0);
+        }
+        // Yo = C H^T in every chunk, a segment's first one included (its H tiles are h0, the carried
+        // state or zero): one fewer run-time branch in the issue and output phases (0.548 -> 0.540 ms,
+        // outputs identical)
+  #pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t ka = (ks >> 2) * (kQ * 128) + (ks & 3) * 32;
+          tc_mma(tmem + 64, dadd(dK, TcSmem::kC + ka), dadd(dH, TcSmem::kHh + ks * 2048), id_yo, ks > 0);
+        }
+        tc_commit(&bars[0]);
       }
-      // Yo = C H^T in every chunk, the first one included (its H tiles are h0 or zero): one fewer
-      // run-time branch in the issue and output phases (0.548 -> 0.540 ms, outputs identical)
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t ka = (ks >> 2) * (kQ * 128) + (ks & 3) * 32;
-        tc_mma(tmem + 64, dadd(dK, TcSmem::kC + ka), dadd(dH, TcSmem::kHh + ks * 2048), id_yo, ks > 0);
-      }
-      tc_commit(&bars[0]);
-    }
-    const float cum_end = s_cum[kQ - 1];
-    {
-      const float wj = ex2_approx(cum_end - s_cum[jw]) * s_dl[jw];
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const uint32_t o = q ? w_off1 : w_off0;
-        float v[8];
-        unpack_chunk(*reinterpret_cast<const uint4*>(sm + TcSmem::kX + o), v, __nv_bfloat16());
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] *= wj;
-        uint4 hi, lo;
-        split8(v, hi, lo);
-        *reinterpret_cast<uint4*>(sm + TcSmem::kWh + o) = hi;
-        *reinterpret_cast<uint4*>(sm + TcSmem::kWl + o) = lo;
-      }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    // ---- P2: S^T = B^T (w ∘ x) on the tensor cores; M = G ∘ e^{cum_i − cum_j} Δ_j on the CUDA cores
-    if (tid == 0) {
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        tc_mma(tmem + 192, dadd(dN, TcSmem::kB + ks * 2048), dadd(dN, TcSmem::kWh + ks * 2048), id_s, ks > 0);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        tc_mma(tmem + 192, dadd(dN, TcSmem::kB + ks * 2048), dadd(dN, TcSmem::kWl + ks * 2048), id_s, 1);
-      tc_commit(&bars[1]);
-    }
-    ok = mbar_wait_bounded(&bars[0], par, &g_ssd_status);
-    ok = __all_sync(0xffffffffu, ok);   // the tensor-memory loads below are warp-collective
-    tc_fence_after();
-    if (tid == kLoader && c + 1 < nchunks) {   // G and Yo are done with C
-      issue_c(t0 + kQ);
-      ++armed[0];
-    }
-    // The element-wise phases run whether or not the wait before them succeeded: after a failed
-    // wait they read allocated tensor memory and write in-bounds shared and global memory (y is
-    // undefined once the status word reports a timeout), and the loop leaves at the next barrier.
-    // Without the run-time branches around them: 0.540 -> 0.527 ms.
-    {
-      const float cr0 = s_cum[ri0], cr1 = s_cum[ri1];
-      float g[16];
-      tc_ld_frag32(tmem + t_lane + pbase, g);
-#pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
-        const int r = 4 * half + rr;                     // 16-byte column chunk of the row
-        const int j = 8 * r + 2 * ft;
-        const float2 cj = *reinterpret_cast<const float2*>(&s_cum[j]);
-        const float2 dj = *reinterpret_cast<const float2*>(&s_dl[j]);
-        const float m00 = j <= ri0 ? g[4 * rr] * ex2_approx(cr0 - cj.x) * dj.x : 0.0f;
-        const float m01 = j + 1 <= ri0 ? g[4 * rr + 1] * ex2_approx(cr0 - cj.y) * dj.y : 0.0f;
-        const float m10 = j <= ri1 ? g[4 * rr + 2] * ex2_approx(cr1 - cj.x) * dj.x : 0.0f;
-        const float m11 = j + 1 <= ri1 ? g[4 * rr + 3] * ex2_approx(cr1 - cj.y) * dj.y : 0.0f;
-        uint32_t hi, lo;
-        const uint32_t o0 = frag_off + ((rr ^ f3) << 4), o1 = o0 + 1024;
-        split2(m00, m01, hi, lo);
-        *reinterpret_cast<uint32_t*>(sm + TcSmem::kMh + o0) = hi;
-        *reinterpret_cast<uint32_t*>(sm + TcSmem::kMl + o0) = lo;
-        split2(m10, m11, hi, lo);
-        *reinterpret_cast<uint32_t*>(sm + TcSmem::kMh + o1) = hi;
-        *reinterpret_cast<uint32_t*>(sm + TcSmem::kMl + o1) = lo;
-      }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    ok = __syncthreads_and(ok) != 0;
-    tc_fence_after();
-    if (!ok) break;
-
-    // ---- P3: Yd = M X on the tensor cores; the state update on the CUDA cores
-    if (tid == 0) {
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        tc_mma(tmem + 0, dadd(dK, TcSmem::kMh + ks * 32), dadd(dN, TcSmem::kX + ks * 2048),
-               id_yd, ks > 0);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        tc_mma(tmem + 0, dadd(dK, TcSmem::kMl + ks * 32), dadd(dN, TcSmem::kX + ks * 2048),
-               id_yd, 1);
-      tc_commit(&bars[2]);
-    }
-    ok = mbar_wait_bounded(&bars[1], par, &g_ssd_status);
-    ok = __all_sync(0xffffffffu, ok);   // the tensor-memory loads below are warp-collective
-    tc_fence_after();
-    if (tid == kLoader && c + 1 < nchunks) {   // G and S^T are done with B
-      issue_b(t0 + kQ);
-      ++armed[1];
-    }
-    {
-      const float eE = ex2_approx(cum_end);
+      const float cum_end = s_cum[kQ - 1];
       {
+        const float wj = ex2_approx(cum_end - s_cum[jw]) * s_dl[jw];
+  #pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const uint32_t o = q ? w_off1 : w_off0;
+          float v[8];
+          unpack_chunk(*reinterpret_cast<const uint4*>(sm + TcSmem::kX + o), v, __nv_bfloat16());
+  #pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] *= wj;
+          uint4 hi, lo;
+          split8(v, hi, lo);
+          *reinterpret_cast<uint4*>(sm + TcSmem::kWh + o) = hi;
+          *reinterpret_cast<uint4*>(sm + TcSmem::kWl + o) = lo;
+        }
+      }
+      fence_async_smem();
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+
+      // ---- P2: S^T = B^T (w ∘ x) on the tensor cores; M = G ∘ e^{cum_i − cum_j} Δ_j on the CUDA cores
+      if (tid == 0) {
+  #pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          tc_mma(tmem + 192, dadd(dN, TcSmem::kB + ks * 2048), dadd(dN, TcSmem::kWh + ks * 2048), id_s, ks > 0);
+  #pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          tc_mma(tmem + 192, dadd(dN, TcSmem::kB + ks * 2048), dadd(dN, TcSmem::kWl + ks * 2048), id_s, 1);
+        tc_commit(&bars[1]);
+      }
+      ok = mbar_wait_bounded(&bars[0], par, &g_ssd_status);
+      ok = __all_sync(0xffffffffu, ok);   // the tensor-memory loads below are warp-collective
+      tc_fence_after();
+      if (tid == kLoader && more) {   // G and Yo are done with C
+        issue_c(ngrp, nb, nt0);
+        ++armed[0];
+      }
+      // The element-wise phases run whether or not the wait before them succeeded: after a failed
+      // wait they read allocated tensor memory and write in-bounds shared and global memory (y is
+      // undefined once the status word reports a timeout), and the loop leaves at the next barrier.
+      // Without the run-time branches around them: 0.540 -> 0.527 ms.
+      {
+        const float cr0 = s_cum[ri0], cr1 = s_cum[ri1];
+        float gv[16];
+        tc_ld_frag32(tmem + t_lane + pbase, gv);
+  #pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+          const int r = 4 * half + rr;                     // 16-byte column chunk of the row
+          const int j = 8 * r + 2 * ft;
+          const float2 cj = *reinterpret_cast<const float2*>(&s_cum[j]);
+          const float2 dj = *reinterpret_cast<const float2*>(&s_dl[j]);
+          const float m00 = j <= ri0 ? gv[4 * rr] * ex2_approx(cr0 - cj.x) * dj.x : 0.0f;
+          const float m01 = j + 1 <= ri0 ? gv[4 * rr + 1] * ex2_approx(cr0 - cj.y) * dj.y : 0.0f;
+          const float m10 = j <= ri1 ? gv[4 * rr + 2] * ex2_approx(cr1 - cj.x) * dj.x : 0.0f;
+          const float m11 = j + 1 <= ri1 ? gv[4 * rr + 3] * ex2_approx(cr1 - cj.y) * dj.y : 0.0f;
+          uint32_t hi, lo;
+          const uint32_t o0 = frag_off + ((rr ^ f3) << 4), o1 = o0 + 1024;
+          split2(m00, m01, hi, lo);
+          *reinterpret_cast<uint32_t*>(sm + TcSmem::kMh + o0) = hi;
+          *reinterpret_cast<uint32_t*>(sm + TcSmem::kMl + o0) = lo;
+          split2(m10, m11, hi, lo);
+          *reinterpret_cast<uint32_t*>(sm + TcSmem::kMh + o1) = hi;
+          *reinterpret_cast<uint32_t*>(sm + TcSmem::kMl + o1) = lo;
+        }
+      }
+      fence_async_smem();
+      tc_fence_before();
+      ok = __syncthreads_and(ok) != 0;
+      tc_fence_after();
+      if (!ok) break;
+
+      // ---- P3: Yd = M X on the tensor cores; the state update on the CUDA cores
+      if (tid == 0) {
+  #pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          tc_mma(tmem + 0, dadd(dK, TcSmem::kMh + ks * 32), dadd(dN, TcSmem::kX + ks * 2048),
+                 id_yd, ks > 0);
+  #pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          tc_mma(tmem + 0, dadd(dK, TcSmem::kMl + ks * 32), dadd(dN, TcSmem::kX + ks * 2048),
+                 id_yd, 1);
+        tc_commit(&bars[2]);
+      }
+      ok = mbar_wait_bounded(&bars[1], par, &g_ssd_status);
+      ok = __all_sync(0xffffffffu, ok);   // the tensor-memory loads below are warp-collective
+      tc_fence_after();
+      if (tid == kLoader && more) {   // G and S^T are done with B
+        issue_b(ngrp, nb, nt0);
+        ++armed[1];
+      }
+      {
+        const float eE = ex2_approx(cum_end);
         float s[32];
         tc_ld32(tmem + t_lane + 192 + pbase, s);
-#pragma unroll
+  #pragma unroll
         for (int q = 0; q < 32; ++q) H[q] = fmaf(eE, H[q], s[q]);
       }
-#pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) {
-        uint4 hi, lo;
-        split8(&H[c8 * 8], hi, lo);
-        const uint32_t o = state_off + ((c8 ^ s3) << 4);
-        *reinterpret_cast<uint4*>(sm + TcSmem::kHh + o) = hi;
-        *reinterpret_cast<uint4*>(sm + TcSmem::kHl + o) = lo;
-      }
-    }
+      store_state_tiles(state_off, s3);
 
-    // ---- P4: y = Yd + e^{cum_i} Yo + D x.  The x values this lane needs are taken into registers
-    // first so that the next chunk's x can be requested before the output work.
-    ok = ok && mbar_wait_bounded(&bars[2], par, &g_ssd_status);
-    ok = __all_sync(0xffffffffu, ok);   // the tensor-memory loads below are warp-collective
-    uint32_t xw[8];   // x at this lane's fragment positions, bf16 pairs: [r][row half]
-#pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
-      const uint32_t o0 = frag_off + ((rr ^ f3) << 4);
-      xw[2 * rr] = *reinterpret_cast<const uint32_t*>(sm + TcSmem::kX + o0);
-      xw[2 * rr + 1] = *reinterpret_cast<const uint32_t*>(sm + TcSmem::kX + o0 + 1024);
-    }
-    tc_fence_before();
-    ok = __syncthreads_and(ok) != 0;   // Yd and every thread are done with x
-    tc_fence_after();
-    if (tid == kLoader && c + 1 < nchunks) {   // Yd and every thread are done with x
-      fence_async_smem();
-      issue_x(t0 + kQ);
-      ++armed[2];
-    }
-    {
-      const float e0 = ex2_approx(s_cum[ri0]), e1 = ex2_approx(s_cum[ri1]);
-      float yd[16], yo[16];
-      tc_ld_frag32(tmem + t_lane + pbase, yd);
+      // ---- P4: y = Yd + e^{cum_i} Yo + D x.  The x values this lane needs are taken into registers
+      // first so that the next unit's x can be requested before the output work.
+      ok = ok && mbar_wait_bounded(&bars[2], par, &g_ssd_status);
+      ok = __all_sync(0xffffffffu, ok);   // the tensor-memory loads below are warp-collective
+      uint32_t xw[8];   // x at this lane's fragment positions, bf16 pairs: [r][row half]
+  #pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const uint32_t o0 = frag_off + ((rr ^ f3) << 4);
+        xw[2 * rr] = *reinterpret_cast<const uint32_t*>(sm + TcSmem::kX + o0);
+        xw[2 * rr + 1] = *reinterpret_cast<const uint32_t*>(sm + TcSmem::kX + o0 + 1024);
+      }
+      tc_fence_before();
+      ok = __syncthreads_and(ok) != 0;   // Yd and every thread are done with x
+      tc_fence_after();
+      if (tid == kLoader && more) {   // Yd and every thread are done with x
+        fence_async_smem();
+        issue_x(nh, nb, nt0);
+        ++armed[2];
+      }
       {
-        float yl[16];
-        tc_ld_frag32(tmem + t_lane + 64 + pbase, yo);
-        tc_ld_frag32(tmem + t_lane + 128 + pbase, yl);
-#pragma unroll
-        for (int q = 0; q < 16; ++q) yo[q] += yl[q];
+        const float e0 = ex2_approx(s_cum[ri0]), e1 = ex2_approx(s_cum[ri1]);
+        float yd[16], yo[16];
+        tc_ld_frag32(tmem + t_lane + pbase, yd);
+        {
+          float yl[16];
+          tc_ld_frag32(tmem + t_lane + 64 + pbase, yo);
+          tc_ld_frag32(tmem + t_lane + 128 + pbase, yl);
+  #pragma unroll
+          for (int q = 0; q < 16; ++q) yo[q] += yl[q];
+        }
+        const int64_t y0 = y_base + t0 * y_step, y1 = y0 + 8 * y_step;
+  #pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int pc = pbase + 8 * r + 2 * ft;
+          float v00 = yd[4 * r] + cur.Dh * bf16lo_to_f32(xw[2 * r]);
+          float v01 = yd[4 * r + 1] + cur.Dh * bf16hi_to_f32(xw[2 * r]);
+          float v10 = yd[4 * r + 2] + cur.Dh * bf16lo_to_f32(xw[2 * r + 1]);
+          float v11 = yd[4 * r + 3] + cur.Dh * bf16hi_to_f32(xw[2 * r + 1]);
+          v00 = fmaf(e0, yo[4 * r], v00);
+          v01 = fmaf(e0, yo[4 * r + 1], v01);
+          v10 = fmaf(e1, yo[4 * r + 2], v10);
+          v11 = fmaf(e1, yo[4 * r + 3], v11);
+          if (t0 + ri0 < L) *reinterpret_cast<uint32_t*>(checked(yg, y0 + pc, nX, 2)) = pack_bf16x2(v00, v01);
+          if (t0 + ri1 < L) *reinterpret_cast<uint32_t*>(checked(yg, y1 + pc, nX, 2)) = pack_bf16x2(v10, v11);
+        }
       }
-      const int64_t y0 = y_row0 + t0 * y_step, y1 = y0 + 8 * y_step;
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int pc = pbase + 8 * r + 2 * ft;
-        float v00 = yd[4 * r] + Dh * bf16lo_to_f32(xw[2 * r]);
-        float v01 = yd[4 * r + 1] + Dh * bf16hi_to_f32(xw[2 * r]);
-        float v10 = yd[4 * r + 2] + Dh * bf16lo_to_f32(xw[2 * r + 1]);
-        float v11 = yd[4 * r + 3] + Dh * bf16hi_to_f32(xw[2 * r + 1]);
-        v00 = fmaf(e0, yo[4 * r], v00);
-        v01 = fmaf(e0, yo[4 * r + 1], v01);
-        v10 = fmaf(e1, yo[4 * r + 2], v10);
-        v11 = fmaf(e1, yo[4 * r + 3], v11);
-        if (t0 + ri0 < L) *reinterpret_cast<uint32_t*>(checked(yg, y0 + pc, nX, 2)) = pack_bf16x2(v00, v01);
-        if (t0 + ri1 < L) *reinterpret_cast<uint32_t*>(checked(yg, y1 + pc, nX, 2)) = pack_bf16x2(v10, v11);
-      }
+      fence_async_smem();   // the new H tiles, for the next unit's MMAs
+      tc_fence_before();
+      ok = __syncthreads_and(ok) != 0;
+      tc_fence_after();
     }
-    fence_async_smem();   // the new H tiles, for the next chunk's MMAs
-    tc_fence_before();
-    ok = __syncthreads_and(ok) != 0;
-    tc_fence_after();
+    if (!ok) break;
+    // The segment ends: its state leaves, the next segment's state replaces it in the H tiles (read
+    // first by the next chunk's C·H^T, after that chunk's barrier and proxy fence).  Kept out of the
+    // chunk loop so that its straight-line phases are not split at a branch (CTA-uniform: every thread
+    // reaches the barriers inside).
+    finish_state(si, gs);
+    if (more_seg) {
+      init_state(si + 1, gs_n);
+      store_state_tiles(state_off, s3);
+    }
+    gs = gs_n;
+    c0 = c0_n;
+    c1 = c1_n;
+    cur = nx;
   }
   // every tile load the loader requested has landed before the CTA's shared memory is released (a
   // loop left after a failed wait may have loads in flight)
   if (tid == kLoader) {
     for (int i = 0; i < 3; ++i)
-      for (int k = started; k < armed[i]; ++k)
+      for (int64_t k = started; k < armed[i]; ++k)
         (void)mbar_wait_bounded(&tbar[i], static_cast<uint32_t>(k & 1), &g_ssd_status, 100000000ull);
-  }
-  if (ok && p.hT) {
-    const int64_t hT_base = (static_cast<int64_t>(b) * p.nheads + h) * kHd * kNs;
-#pragma unroll
-    for (int q = 0; q < kHd / 2; ++q) *checked(p.hT, hT_base + (pbase + q) * kNs + n_own, nState) = H[q];
   }
   tc_fence_before();
   __syncthreads();
@@ -504,7 +639,48 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
 int ssd_head_dim() { return kHd; }
 int ssd_state_dim() { return kNs; }
 
-cudaError_t ssd_fwd_launch(const SsdParams& p, cudaStream_t stream) {
+static cudaError_t set_smem_attributes() {
+  for (const void* k : {reinterpret_cast<const void*>(ssd_tc_kernel<false>),
+                        reinterpret_cast<const void*>(ssd_tc_kernel<true>)}) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem::kDynamic);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// CTAs of the SSD kernel that fit on the current device at once, from its registers, shared memory and
+// threads per SM and the tensor-memory columns each CTA allocates (512 per SM).  The runtime's
+// occupancy query reports one CTA per SM for this kernel (measured on a B300, even with no dynamic
+// shared memory), while two run side by side (the time of 296 sequences is 1.3 times that of 148); the
+// balanced schedule does not depend on the number for correctness.
+int ssd_resident_ctas() {
+  static int cached[64] = {0};
+  int dev = 0, sms = 0, smem = 0, reserved = 0, regs = 0, threads = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return 0; }
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  cudaFuncAttributes fa;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&regs, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&threads, cudaDevAttrMaxThreadsPerMultiProcessor, dev) != cudaSuccess ||
+      cudaFuncGetAttributes(&fa, ssd_tc_kernel<true>) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  const int warps = kThreads / 32;
+  const int regs_per_warp = (fa.numRegs * 32 + 255) / 256 * 256;   // allocated per warp in units of 256
+  int per_sm = 512 / static_cast<int>(kTmemCols);
+  per_sm = std::min(per_sm, smem / (TcSmem::kDynamic + static_cast<int>(fa.sharedSizeBytes) + reserved));
+  per_sm = std::min(per_sm, regs / (warps * regs_per_warp));
+  per_sm = std::min(per_sm, threads / kThreads);
+  per_sm = std::min(per_sm, 2);   // the kernel's launch bounds
+  if (per_sm < 1) per_sm = 1;
+  if (dev >= 0 && dev < 64) cached[dev] = per_sm * sms;
+  return per_sm * sms;
+}
+
+cudaError_t ssd_fwd_launch(const SsdParams& p, int balanced_ctas, cudaStream_t stream) {
   if (p.L > 0x7fffffffLL) return cudaErrorInvalidValue;   // TMA row coordinates are 32-bit
   SsdMaps tm;
   memset(&tm, 0, sizeof(tm));
@@ -520,9 +696,18 @@ cudaError_t ssd_fwd_launch(const SsdParams& p, cudaStream_t stream) {
     set_last_error("ssd tensor maps: %s", err);
     return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(ssd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem::kDynamic);
+  cudaError_t e = set_smem_attributes();
   if (e != cudaSuccess) return e;
-  ssd_tc_kernel<<<dim3(p.nheads, p.batch), kThreads, TcSmem::kDynamic, stream>>>(tm, p);
+  if (p.balanced) {
+    // the publication flags and the range counter after them start at zero
+    e = cudaMemsetAsync(p.flags, 0, sizeof(unsigned) * (balanced_ctas + 1), stream);
+    if (e != cudaSuccess) return e;
+    ssd_tc_kernel<true><<<balanced_ctas, kThreads, TcSmem::kDynamic, stream>>>(tm, p);
+    return cudaGetLastError();
+  }
+  const int64_t nseq = static_cast<int64_t>(p.batch) * p.nheads;
+  if (nseq > 0x7fffffffLL) return cudaErrorInvalidValue;
+  ssd_tc_kernel<false><<<static_cast<unsigned>(nseq), kThreads, TcSmem::kDynamic, stream>>>(tm, p);
   return cudaGetLastError();
 }
 

@@ -80,6 +80,32 @@ struct Plan {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// The balanced schedule of the SSD forward (ssd_tc.cu) for these sizes: CTAs (0: one CTA per
+// sequence, when the sequences fit in one wave of resident CTAs or no workspace is given), units of
+// (sequence, 64-step chunk) per CTA, and the workspace: the ranges' carried states, then their flags
+// and the range counter.
+struct SsdPlan {
+  int ctas = 0;
+  int64_t range = 0;
+  size_t carry = 0, workspace = 0;
+};
+SsdPlan ssd_plan(int batch, int nheads, int64_t seqlen, int ctas) {
+  SsdPlan pl;
+  if (seqlen <= 0) return pl;
+  const int64_t nseq = static_cast<int64_t>(batch) * nheads;
+  const int64_t nchunks = (seqlen + 63) / 64;
+  const int64_t slots = ssm::ssd_resident_ctas();
+  const int64_t G = ctas > 0 ? std::min<int64_t>(ctas, slots) : slots;
+  if (G <= 0 || G >= nseq) return pl;
+  // G < nseq, so every range is longer than a sequence: a CTA's tail never waits for long
+  const int64_t total = nseq * nchunks;
+  pl.range = (total + G - 1) / G;
+  pl.ctas = static_cast<int>((total + pl.range - 1) / pl.range);
+  pl.carry = round_up(static_cast<size_t>(pl.ctas) * ssm::ssd_head_dim() * ssm::ssd_state_dim() * sizeof(float), 256);
+  pl.workspace = pl.carry + round_up(static_cast<size_t>(pl.ctas + 1) * sizeof(unsigned), 256);
+  return pl;
+}
+
 // The bf16 fast path needs: bf16 io, the Δ·B or the exact-ZOH input term, rows TMA can describe (L a
 // multiple of 8, at least one 64-step tile, at least 128 rows).  Pointer alignment is checked at call
 // time.
@@ -776,10 +802,10 @@ ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A, const 
 
 extern "C" {
 
-ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void* B, const void* C, const float* D,
+ssm_status ssm_ssd_fwd_ex(const void* x, const void* dt, const float* A, const void* B, const void* C, const float* D,
                        const float* dt_bias, int softplus_flag, const float* h0, void* y, float* final_state,
-                       int batch, int64_t seqlen, int nheads, int headdim, int dstate, int ngroups, ssm_dtype io_dtype,
-                       cudaStream_t stream) {
+                          int batch, int64_t seqlen, int nheads, int headdim, int dstate, int ngroups,
+                          ssm_dtype io_dtype, void* workspace, size_t workspace_bytes, int ctas, cudaStream_t stream) {
   g_err[0] = 0;
   if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return fail(SSM_ERR_INVALID_ARG, "unknown io_dtype %d", io_dtype);
   if (batch < 1 || seqlen < 0 || nheads < 1 || headdim < 1 || dstate < 1 || ngroups < 1 || nheads % ngroups != 0)
@@ -803,14 +829,23 @@ ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void
   const size_t xl = static_cast<size_t>(batch) * seqlen * nheads * headdim * e;
   const size_t bcl = static_cast<size_t>(batch) * seqlen * ngroups * dstate * e;
   const size_t st = static_cast<size_t>(batch) * nheads * headdim * dstate * 4;
-  const Range outs[] = {range_of(y, xl), range_of(final_state, final_state ? st : 0)};
+  if (ctas < 0) return fail(SSM_ERR_INVALID_ARG, "ctas must be >= 0, got %d", ctas);
+  const SsdPlan plan = workspace ? ssd_plan(batch, nheads, seqlen, ctas) : SsdPlan();
+  if (plan.ctas > 0 && workspace_bytes < plan.workspace)
+    return fail(SSM_ERR_INVALID_ARG, "workspace of %zu bytes, the balanced schedule needs %zu", workspace_bytes,
+                plan.workspace);
+  if (plan.ctas > 0 && !aligned(workspace, 256)) return fail(SSM_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  const Range outs[] = {range_of(y, xl), range_of(final_state, final_state ? st : 0),
+                        range_of(workspace, plan.ctas > 0 ? plan.workspace : 0)};
   const Range ins[] = {range_of(x, xl), range_of(dt, static_cast<size_t>(batch) * seqlen * nheads * e),
                        range_of(B, bcl), range_of(C, bcl), range_of(A, nheads * 4), range_of(D, D ? nheads * 4 : 0),
                        range_of(dt_bias, dt_bias ? nheads * 4 : 0), range_of(h0, h0 ? st : 0)};
   for (const Range& o : outs)
     for (const Range& i : ins)
       if (overlap(o, i)) return fail(SSM_ERR_INVALID_ARG, "an output overlaps an input");
-  if (overlap(outs[0], outs[1])) return fail(SSM_ERR_INVALID_ARG, "y overlaps final_state");
+  for (int i = 0; i < 3; ++i)
+    for (int j = i + 1; j < 3; ++j)
+      if (overlap(outs[i], outs[j])) return fail(SSM_ERR_INVALID_ARG, "y, final_state and the workspace overlap");
   if (seqlen == 0) {
     if (final_state) {
       cudaError_t ce = h0 ? cudaMemcpyAsync(final_state, h0, st, cudaMemcpyDeviceToDevice, stream)
@@ -823,9 +858,39 @@ ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void
   memset(&p, 0, sizeof(p));
   p.x = x; p.dt = dt; p.A = A; p.B = B; p.C = C; p.D = D; p.dt_bias = dt_bias; p.h0 = h0; p.y = y; p.hT = final_state;
   p.batch = batch; p.nheads = nheads; p.ngroups = ngroups; p.L = seqlen; p.softplus = softplus_flag != 0;
-  cudaError_t ce = ssm::ssd_fwd_launch(p, stream);
+  p.test_withhold_cta = -1;
+  p.carry_wait_ns = 0;
+  if (plan.ctas > 0) {
+    p.balanced = 1;
+    p.range = plan.range;
+    p.carry = static_cast<float*>(workspace);
+    p.flags = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + plan.carry);
+  }
+  if (g_withhold.armed) {
+    // one-shot diagnostic armed by ssm_selftest_withhold_carry on this host thread
+    if (plan.ctas > 0) {
+      p.test_withhold_cta = g_withhold.cta;
+      p.carry_wait_ns = static_cast<uint64_t>(g_withhold.limit_ns);
+    }
+    g_withhold.armed = false;
+  }
+  cudaError_t ce = ssm::ssd_fwd_launch(p, plan.ctas, stream);
   if (ce != cudaSuccess) return cuda_fail(ce, "ssd launch");
   return SSM_OK;
+}
+
+
+ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void* B, const void* C, const float* D,
+                       const float* dt_bias, int softplus_flag, const float* h0, void* y, float* final_state,
+                       int batch, int64_t seqlen, int nheads, int headdim, int dstate, int ngroups, ssm_dtype io_dtype,
+                       cudaStream_t stream) {
+  return ssm_ssd_fwd_ex(x, dt, A, B, C, D, dt_bias, softplus_flag, h0, y, final_state, batch, seqlen, nheads, headdim,
+                        dstate, ngroups, io_dtype, nullptr, 0, 0, stream);
+}
+
+size_t ssm_ssd_fwd_workspace_size(int batch, int64_t seqlen, int nheads, int ctas) {
+  if (batch < 1 || seqlen < 1 || nheads < 1 || ctas < 0) return 0;
+  return ssd_plan(batch, nheads, seqlen, ctas).workspace;
 }
 
 }  // extern "C"

@@ -90,6 +90,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ssm_ssd_state_update.argtypes = [vp] * 7 + [i32, vp, vp, i32, i32, i32, i32, i32, i32, vp]
     lib.ssm_ssd_fwd.restype = i32
     lib.ssm_ssd_fwd.argtypes = [vp] * 7 + [i32, vp, vp, vp, i32, i64, i32, i32, i32, i32, i32, vp]
+    lib.ssm_ssd_fwd_ex.restype = i32
+    lib.ssm_ssd_fwd_ex.argtypes = [vp] * 7 + [i32, vp, vp, vp, i32, i64, i32, i32, i32, i32, i32, vp, sz, i32, vp]
+    lib.ssm_ssd_fwd_workspace_size.restype = sz
+    lib.ssm_ssd_fwd_workspace_size.argtypes = [i32, i64, i32, i32]
     lib.ssm_scan_bwd_workspace_size.restype = sz
     lib.ssm_scan_bwd_workspace_size.argtypes = [i32, i32, i32, i64, i32]
     lib.ssm_scan_bwd.restype = i32
@@ -345,10 +349,13 @@ def selective_scan_bwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B:
 def ssd_fwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor, C: torch.Tensor,
             D: Optional[torch.Tensor] = None, dt_bias: Optional[torch.Tensor] = None, dt_softplus: bool = True,
             h0: Optional[torch.Tensor] = None, return_final_state: bool = True, *, out: Optional[torch.Tensor] = None,
-            final_state: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+            final_state: Optional[torch.Tensor] = None, balanced: bool = True, ctas: int = 0,
+            workspace: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """Mamba-2 SSD forward.  x (batch, L, nheads, headdim), dt (batch, L, nheads), B, C (batch, L,
     ngroups, dstate) in bf16; A, D, dt_bias (nheads,) f32; h0 (batch, nheads, headdim, dstate) f32.
-    Returns (y, final state)."""
+    balanced: the balanced schedule of ssm_ssd_fwd_ex where it applies (ctas: at most that many ranges,
+    0 = one per co-resident CTA; workspace: a uint8 device tensor reused if large enough, else one is
+    allocated); False: one CTA per sequence (ssm_ssd_fwd).  Returns (y, final state)."""
     lib = load_library()
     batch, L, nheads, headdim = x.shape
     ngroups, dstate = B.shape[2], B.shape[3]
@@ -369,11 +376,20 @@ def ssd_fwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
     if final_state is not None:
         _need(final_state, "final_state", (batch, nheads, headdim, dstate), torch.float32, dev)
     with torch.cuda.device(dev):
-        st = lib.ssm_ssd_fwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(dt_bias),
-                             int(bool(dt_softplus)), _ptr(h0), _ptr(y), _ptr(final_state), batch, L, nheads, headdim,
-                             dstate, ngroups, _io_code(io), _stream_handle(stream))
+        ws_bytes = int(lib.ssm_ssd_fwd_workspace_size(batch, L, nheads, int(ctas))) if balanced else 0
+        if ws_bytes and (workspace is None or workspace.numel() < ws_bytes):
+            workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        st = lib.ssm_ssd_fwd_ex(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(dt_bias),
+                                int(bool(dt_softplus)), _ptr(h0), _ptr(y), _ptr(final_state), batch, L, nheads,
+                                headdim, dstate, ngroups, _io_code(io), _ptr(workspace) if ws_bytes else None,
+                                ws_bytes, int(ctas), _stream_handle(stream))
     _check(lib, st)
     return y, final_state
+
+
+def ssd_workspace_size(batch: int, seqlen: int, nheads: int, ctas: int = 0) -> int:
+    """Bytes of workspace the balanced SSD schedule needs on the current device (0: one CTA per sequence)."""
+    return int(load_library().ssm_ssd_fwd_workspace_size(batch, seqlen, nheads, ctas))
 
 
 def ssd_state_update(x_t: torch.Tensor, dt_t: torch.Tensor, A: torch.Tensor, B_t: torch.Tensor, C_t: torch.Tensor,

@@ -119,6 +119,11 @@ def test_ssd_groups_h0_and_options(checked):
     ssd_t.test_ssd_groups_h0_and_options()
 
 
+@pytest.mark.parametrize("ctas", [1, 3, 7])
+def test_ssd_balanced_ranges(checked, ctas):
+    ssd_t.test_ssd_balanced_ranges_match_one_cta_per_sequence(ctas)
+
+
 @pytest.mark.parametrize("groups", [1, 2])
 def test_ssd_decode_steps(checked, groups):
     ssd_t.test_ssd_decode_steps_match_the_recurrence(groups)
@@ -143,8 +148,8 @@ def _close(a, b, tol):
 
 def test_full_size_workloads_stay_in_bounds():
     """The full-size workloads through the checked build: every global index of the prefill (balanced
-    and chunked schedules, exact ZOH), the backward, conv1d, the decode step, the SSD forward and its
-    decode step stays inside its buffer, and the results agree with the ordinary build's (the same
+    and chunked schedules, exact ZOH), the backward, conv1d, the decode step, the SSD forward (balanced
+    and one CTA per sequence) and its decode step stays inside its buffer, and the results agree with the ordinary build's (the same
     arithmetic: equal up to the order of the backward's cross-channel atomics)."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
@@ -171,7 +176,9 @@ def test_full_size_workloads_stay_in_bounds():
                "bwd": ssm.selective_scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], dy, **a),
                "conv": ssm.causal_conv1d_fwd(inp["u"], conv_w, conv_state=conv_s),
                "ssd": ssm.ssd_fwd(sin["x"], sin["dt"], sin["A"], sin["B"], sin["C"], D=sin["D"],
-                                  dt_bias=sin["dt_bias"])}
+                                  dt_bias=sin["dt_bias"]),
+               "ssd_grid": ssm.ssd_fwd(sin["x"], sin["dt"], sin["A"], sin["B"], sin["C"], D=sin["D"],
+                                       dt_bias=sin["dt_bias"], balanced=False)}
         state = torch.zeros((dw.batch, dw.dim, dw.dstate), device=dev)
         cst = torch.zeros((dw.batch, dw.dim, 3), device=dev)
         out["decode"] = [ssm.selective_state_update(din["x"][t], din["delta"][t], din["A"], din["B"][t], din["C"][t],
@@ -190,7 +197,9 @@ def test_full_size_workloads_stay_in_bounds():
         assert ssm.device_status() == ssm.SSM_OK
         got = run_all()
         assert ssm.device_status() == ssm.SSM_OK, "an index check failed at full size"
-    for k in ("scan", "chunked", "zoh", "conv", "ssd"):
+    for a, b in zip(ref["ssd"], ref["ssd_grid"]):   # the two SSD schedules: the same arithmetic
+        assert torch.equal(a, b)
+    for k in ("scan", "chunked", "zoh", "conv", "ssd", "ssd_grid"):
         for a, b in zip(got[k], ref[k]):
             if a is not None:
                 _close(a, b, 1e-5)

@@ -5,8 +5,8 @@ CTA-to-CTA carry): when a wait runs out, the kernel records a timeout in a statu
 ssm_selftest_bounded_wait runs each kind of wait against a condition that nothing satisfies; the
 timeout must reach the host through ssm_device_status, the word must be cleared by that read, and the
 context must remain usable (a scan afterwards still matches the oracle).  ssm_selftest_withhold_carry
-makes the real prefill kernel's CTA-to-CTA carry wait run out: one CTA of the balanced schedule
-writes its carry but never raises the flag that publishes it.
+makes the real prefill and SSD kernels' CTA-to-CTA carry waits run out: one CTA of a balanced
+schedule writes its carry but never raises the flag that publishes it.
 """
 import time
 
@@ -76,6 +76,32 @@ def test_withheld_carry_times_out_in_the_prefill_kernel():
     di = torch.tensor([c[1] for c in sorted(set(chans))])
     assert max_rel_err(to64(y[bi, di]), ry) <= 1e-2
     assert max_rel_err(to64(hL[bi, di]), rh) <= 1e-2
+
+
+def test_withheld_carry_times_out_in_the_ssd_kernel():
+    """The SSD forward's balanced schedule on 8 sequences of 5 chunks in 3 ranges: CTA 0 runs the head
+    of sequence 2 (chunks 0..3), CTA 1 its tail.  With CTA 0's publication withheld, CTA 1's wait gives
+    up after the armed 50 ms, the status read reports the timeout once, and the next call matches the
+    oracle."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    lib = ssm.load_library()
+    dev = torch.device("cuda:0")
+    w = W.SsdWorkload("adhoc", 2, 293, 4, 64, 128, 2, 2402)
+    inp = W.make_ssd_inputs(w, device=dev)
+    args = dict(D=inp["D"], dt_bias=inp["dt_bias"], ctas=3)
+    assert ssm.device_status() == ssm.SSM_OK
+    assert lib.ssm_selftest_withhold_carry(0, 50_000_000) == ssm.SSM_OK
+    t0 = time.monotonic()
+    ssm.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], **args)
+    assert ssm.device_status() == ssm.SSM_ERR_TIMEOUT
+    assert time.monotonic() - t0 < 10.0                            # the wait ended by itself
+    assert ssm.device_status() == ssm.SSM_OK                       # the read cleared the word
+    y, hT = ssm.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], **args)
+    assert ssm.device_status() == ssm.SSM_OK
+    ry, rh = oracle.ssd_scan(to64(inp["x"]), to64(inp["dt"]), to64(inp["A"]), to64(inp["B"]), to64(inp["C"]),
+                             D=to64(inp["D"]), dt_bias=to64(inp["dt_bias"]))
+    assert max_rel_err(to64(y), ry) <= 1e-2 and max_rel_err(to64(hT), rh) <= 1e-2
 
 
 def test_withhold_carry_rejects_a_negative_cta():

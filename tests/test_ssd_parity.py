@@ -3,7 +3,8 @@
 bf16 io with float32 accumulation and state: max relative error (floor 1e-3 of the largest
 reference value) of 1e-2, the bound used for every bf16-io path.  Small and ragged shapes compare
 every output; so do the full Mamba-2 layer and the full decode workload, in the configurations the
-benchmark times.
+benchmark times.  The balanced schedule (sequences split between CTAs, the state carried through the
+workspace) is compared with one CTA per sequence bit for bit and with the oracle.
 """
 import numpy as np
 import pytest
@@ -85,6 +86,63 @@ def test_ssd_mamba2_layer_full():
     y, hT = _run(inp)
     assert torch.isfinite(y).all()
     _check(y, hT, *_oracle(inp))
+
+
+def _run_sched(inp, balanced, ctas=0, h0=None):
+    y, hT = ssm.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], D=inp["D"], dt_bias=inp["dt_bias"],
+                        h0=h0, balanced=balanced, ctas=ctas)
+    torch.cuda.synchronize()
+    assert ssm.device_status() == ssm.SSM_OK
+    return y, hT
+
+
+@pytest.mark.parametrize("ctas", [1, 2, 3, 5, 7])
+def test_ssd_balanced_ranges_match_one_cta_per_sequence(ctas):
+    """The balanced schedule on 8 sequences (batch 2 x 4 heads, 2 groups) of 5 chunks, the last one
+    ragged (L 293), cut into at most `ctas` ranges: with 3, 5 or 7 ranges the cuts fall inside
+    sequences, so heads are published, tails continue from the carried state and whole sequences
+    run in between; one range runs every sequence in one CTA.  The per-chunk arithmetic is the same
+    and the carried state is exact float32, so y and the final state equal those of one CTA per
+    sequence bit for bit, and both match the oracle, with h0 given and without."""
+    dev = _dev()
+    w = W.SsdWorkload("adhoc", 2, 293, 4, 64, 128, 2, 2400)
+    inp = W.make_ssd_inputs(w, device=dev)
+    assert ssm.ssd_workspace_size(2, 293, 4, ctas) > 0
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    for h0 in (None, torch.randn((2, 4, 64, 128), generator=g, device=dev)):
+        yg, hg = _run_sched(inp, balanced=False, h0=h0)
+        yb, hb = _run_sched(inp, balanced=True, ctas=ctas, h0=h0)
+        assert torch.equal(yb, yg) and torch.equal(hb, hg)
+        _check(yb, hb, *_oracle(inp, h0=h0))
+
+
+def test_ssd_workspace_size_and_one_wave_shapes():
+    """No workspace when the sequences fit in one wave of resident CTAs (or in `ctas`), a carry per
+    range otherwise; the workload's 512 sequences take the balanced schedule on a B300."""
+    _dev()
+    assert ssm.ssd_workspace_size(2, 293, 4, 8) == 0           # 8 sequences on up to 8 ranges
+    assert ssm.ssd_workspace_size(2, 293, 4, 0) == 0           # fewer sequences than resident CTAs
+    ws = ssm.ssd_workspace_size(2, 293, 4, 3)
+    assert ws >= 3 * 64 * 128 * 4 + 4 * 4 and ws % 256 == 0   # carries, flags, range counter
+    w = W.WORKLOADS["mamba2-ssd-layer"]
+    assert ssm.ssd_workspace_size(w.batch, w.seqlen, w.nheads) > 0
+    lib = ssm.load_library()
+    assert lib.ssm_ssd_fwd_workspace_size(0, 293, 4, 0) == 0 and lib.ssm_ssd_fwd_workspace_size(2, 293, 4, -1) == 0
+
+
+def test_ssd_balanced_rejects_a_small_workspace():
+    dev = _dev()
+    w = W.SsdWorkload("adhoc", 2, 293, 4, 64, 128, 2, 2401)
+    inp = W.make_ssd_inputs(w, device=dev)
+    need = ssm.ssd_workspace_size(2, 293, 4, 3)
+    small = torch.empty(need - 256, dtype=torch.uint8, device=dev)
+    y = torch.empty_like(inp["x"])
+    lib = ssm.load_library()
+    st = lib.ssm_ssd_fwd_ex(inp["x"].data_ptr(), inp["dt"].data_ptr(), inp["A"].data_ptr(), inp["B"].data_ptr(),
+                            inp["C"].data_ptr(), None, None, 1, None, y.data_ptr(), None, 2, 293, 4, 64, 128, 2,
+                            ssm.SSM_BF16, small.data_ptr(), need - 256, 3, None)
+    assert st == ssm.SSM_ERR_INVALID_ARG
 
 
 def test_ssd_seqlen_zero_passes_the_state_through():
