@@ -363,8 +363,8 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
     return p.softplus ? softplus_fast(v) : v;
   };
   // tiles armed per barrier (loader thread) and units whose tiles every thread has waited for
-  int64_t armed[3] = {0, 0, 0};
-  int64_t started = 0;
+  int armed[3] = {0, 0, 0};   // (a CTA runs fewer than 2^31 units: the host keeps ranges below that)
+  int started = 0;
   if (tid == kLoader) {
     prefetch_tensormap(&tm.C);
     prefetch_tensormap(&tm.B);
@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
   const int jw = tid >> 2;                             // the w ∘ x row of this thread, chunks cw and cw + 1
   const uint32_t w_off0 = sw_chunk(jw, (tid & 3) * 2), w_off1 = sw_chunk(jw, (tid & 3) * 2 + 1);
   const int64_t y_step = static_cast<int64_t>(p.nheads) * kHd;   // elements per time step of x and y
-  int64_t k = 0;   // units (chunks) run so far: the parity of every barrier phase
+  int k = 0;   // units (chunks) run so far: the parity of every barrier phase
   for (int64_t si = 0; si < nseg && ok; ++si) {
     // the next segment, whose first chunk is requested during this segment's last one
     const bool more_seg = si + 1 < nseg;
@@ -626,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
   // loop left after a failed wait may have loads in flight)
   if (tid == kLoader) {
     for (int i = 0; i < 3; ++i)
-      for (int64_t k = started; k < armed[i]; ++k)
+      for (int k = started; k < armed[i]; ++k)
         (void)mbar_wait_bounded(&tbar[i], static_cast<uint32_t>(k & 1), &g_ssd_status, 100000000ull);
   }
   tc_fence_before();

@@ -100,6 +100,7 @@ SsdPlan ssd_plan(int batch, int nheads, int64_t seqlen, int ctas) {
   // G < nseq, so every range is longer than a sequence: a CTA's tail never waits for long
   const int64_t total = nseq * nchunks;
   pl.range = (total + G - 1) / G;
+  if (pl.range > (1LL << 30)) return SsdPlan();   // a CTA counts its units in 32 bits
   pl.ctas = static_cast<int>((total + pl.range - 1) / pl.range);
   pl.carry = round_up(static_cast<size_t>(pl.ctas) * ssm::ssd_head_dim() * ssm::ssd_state_dim() * sizeof(float), 256);
   pl.workspace = pl.carry + round_up(static_cast<size_t>(pl.ctas + 1) * sizeof(unsigned), 256);
