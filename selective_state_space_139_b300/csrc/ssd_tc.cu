@@ -420,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
         }
         const float a0 = d0 * cur.A2;
         float s2 = a0 + d1 * cur.A2;
-  #pragma unroll
+#pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const float u = __shfl_up_sync(0xffffffffu, s2, o);
           if (lane >= o) s2 += u;
@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
 
       // ---- P1: G = C B^T and Yo = C H^T on the tensor cores; meanwhile w ∘ x on the CUDA cores
       if (tid == 0) {
-  #pragma unroll
+#pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t ka = (ks >> 2) * (kQ * 128) + (ks & 3) * 32;
           tc_mma(tmem + 0, dadd(dK, TcSmem::kC + ka), dadd(dK, TcSmem::kB + ka), id_g, ks > 0);
@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
         // Yo = C H^T in every chunk, a segment's first one included (its H tiles are h0, the carried
         // state or zero): one fewer run-time branch in the issue and output phases (0.548 -> 0.540 ms,
         // outputs identical)
-  #pragma unroll
+#pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t ka = (ks >> 2) * (kQ * 128) + (ks & 3) * 32;
           tc_mma(tmem + 64, dadd(dK, TcSmem::kC + ka), dadd(dH, TcSmem::kHh + ks * 2048), id_yo, ks > 0);
@@ -459,12 +459,12 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
       const float cum_end = s_cum[kQ - 1];
       {
         const float wj = ex2_approx(cum_end - s_cum[jw]) * s_dl[jw];
-  #pragma unroll
+#pragma unroll
         for (int q = 0; q < 2; ++q) {
           const uint32_t o = q ? w_off1 : w_off0;
           float v[8];
           unpack_chunk(*reinterpret_cast<const uint4*>(sm + TcSmem::kX + o), v, __nv_bfloat16());
-  #pragma unroll
+#pragma unroll
           for (int e = 0; e < 8; ++e) v[e] *= wj;
           uint4 hi, lo;
           split8(v, hi, lo);
@@ -479,10 +479,10 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
 
       // ---- P2: S^T = B^T (w ∘ x) on the tensor cores; M = G ∘ e^{cum_i − cum_j} Δ_j on the CUDA cores
       if (tid == 0) {
-  #pragma unroll
+#pragma unroll
         for (int ks = 0; ks < 4; ++ks)
           tc_mma(tmem + 192, dadd(dN, TcSmem::kB + ks * 2048), dadd(dN, TcSmem::kWh + ks * 2048), id_s, ks > 0);
-  #pragma unroll
+#pragma unroll
         for (int ks = 0; ks < 4; ++ks)
           tc_mma(tmem + 192, dadd(dN, TcSmem::kB + ks * 2048), dadd(dN, TcSmem::kWl + ks * 2048), id_s, 1);
         tc_commit(&bars[1]);
@@ -502,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
         const float cr0 = s_cum[ri0], cr1 = s_cum[ri1];
         float gv[16];
         tc_ld_frag32(tmem + t_lane + pbase, gv);
-  #pragma unroll
+#pragma unroll
         for (int rr = 0; rr < 4; ++rr) {
           const int r = 4 * half + rr;                     // 16-byte column chunk of the row
           const int j = 8 * r + 2 * ft;
@@ -530,11 +530,11 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
 
       // ---- P3: Yd = M X on the tensor cores; the state update on the CUDA cores
       if (tid == 0) {
-  #pragma unroll
+#pragma unroll
         for (int ks = 0; ks < 4; ++ks)
           tc_mma(tmem + 0, dadd(dK, TcSmem::kMh + ks * 32), dadd(dN, TcSmem::kX + ks * 2048),
                  id_yd, ks > 0);
-  #pragma unroll
+#pragma unroll
         for (int ks = 0; ks < 4; ++ks)
           tc_mma(tmem + 0, dadd(dK, TcSmem::kMl + ks * 32), dadd(dN, TcSmem::kX + ks * 2048),
                  id_yd, 1);
@@ -551,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
         const float eE = ex2_approx(cum_end);
         float s[32];
         tc_ld32(tmem + t_lane + 192 + pbase, s);
-  #pragma unroll
+#pragma unroll
         for (int q = 0; q < 32; ++q) H[q] = fmaf(eE, H[q], s[q]);
       }
       store_state_tiles(state_off, s3);
@@ -561,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
       ok = ok && mbar_wait_bounded(&bars[2], par, &g_ssd_status);
       ok = __all_sync(0xffffffffu, ok);   // the tensor-memory loads below are warp-collective
       uint32_t xw[8];   // x at this lane's fragment positions, bf16 pairs: [r][row half]
-  #pragma unroll
+#pragma unroll
       for (int rr = 0; rr < 4; ++rr) {
         const uint32_t o0 = frag_off + ((rr ^ f3) << 4);
         xw[2 * rr] = *reinterpret_cast<const uint32_t*>(sm + TcSmem::kX + o0);
@@ -583,11 +583,11 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
           float yl[16];
           tc_ld_frag32(tmem + t_lane + 64 + pbase, yo);
           tc_ld_frag32(tmem + t_lane + 128 + pbase, yl);
-  #pragma unroll
+#pragma unroll
           for (int q = 0; q < 16; ++q) yo[q] += yl[q];
         }
         const int64_t y0 = y_base + t0 * y_step, y1 = y0 + 8 * y_step;
-  #pragma unroll
+#pragma unroll
         for (int r = 0; r < 4; ++r) {
           const int pc = pbase + 8 * r + 2 * ft;
           float v00 = yd[4 * r] + cur.Dh * bf16lo_to_f32(xw[2 * r]);
