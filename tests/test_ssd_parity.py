@@ -97,7 +97,7 @@ def _run_sched(inp, balanced, ctas=0, h0=None):
 
 
 @pytest.mark.parametrize("ctas", [1, 2, 3, 5, 7])
-def test_ssd_balanced_ranges_match_one_cta_per_sequence(ctas):
+def test_ssd_balanced_ranges_match_one_cta_per_sequence(ctas, L=293):
     """The balanced schedule on 8 sequences (batch 2 x 4 heads, 2 groups) of 5 chunks, the last one
     ragged (L 293), cut into at most `ctas` ranges: with 3, 5 or 7 ranges the cuts fall inside
     sequences, so heads are published, tails continue from the carried state and whole sequences
@@ -105,9 +105,9 @@ def test_ssd_balanced_ranges_match_one_cta_per_sequence(ctas):
     and the carried state is exact float32, so y and the final state equal those of one CTA per
     sequence bit for bit, and both match the oracle, with h0 given and without."""
     dev = _dev()
-    w = W.SsdWorkload("adhoc", 2, 293, 4, 64, 128, 2, 2400)
+    w = W.SsdWorkload("adhoc", 2, L, 4, 64, 128, 2, 2400 + L)
     inp = W.make_ssd_inputs(w, device=dev)
-    assert ssm.ssd_workspace_size(2, 293, 4, ctas) > 0
+    assert ssm.ssd_workspace_size(2, L, 4, ctas) > 0
     g = torch.Generator(device=dev)
     g.manual_seed(11)
     for h0 in (None, torch.randn((2, 4, 64, 128), generator=g, device=dev)):
@@ -115,6 +115,13 @@ def test_ssd_balanced_ranges_match_one_cta_per_sequence(ctas):
         yb, hb = _run_sched(inp, balanced=True, ctas=ctas, h0=h0)
         assert torch.equal(yb, yg) and torch.equal(hb, hg)
         _check(yb, hb, *_oracle(inp, h0=h0))
+
+
+@pytest.mark.parametrize("L,ctas", [(1, 3), (64, 3), (65, 7), (640, 3)])
+def test_ssd_balanced_lengths(L, ctas):
+    """The balanced schedule at one chunk (every range whole sequences), exactly one chunk, one step
+    into a second chunk, and ten chunks per sequence."""
+    test_ssd_balanced_ranges_match_one_cta_per_sequence(ctas, L)
 
 
 def test_ssd_workspace_size_and_one_wave_shapes():
