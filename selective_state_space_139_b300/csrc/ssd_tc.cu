@@ -175,8 +175,10 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
   __shared__ uint32_t tmem_slot;
   __shared__ int s_carry_ok;
   __shared__ int s_range;
-  __shared__ __align__(16) float s_dl[kQ];
-  __shared__ __align__(16) float s_cum[kQ];
+  // Δ and its prefix sum of a unit, in two buffers by unit parity: warp 0 fills the next unit's while
+  // the other warps still read this unit's (no barrier at the end of a unit)
+  __shared__ __align__(16) float s_dl[2][kQ];
+  __shared__ __align__(16) float s_cum[2][kQ];
   const int64_t L = p.L;
   const int nchunks = static_cast<int>((L + kQ - 1) / kQ);
   const int64_t nseq = static_cast<int64_t>(p.batch) * p.nheads;
@@ -402,8 +404,10 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
       seq_of(gs_n, nx);
     }
     const int64_t y_base = ((static_cast<int64_t>(cur.b) * L + ri0) * p.nheads + cur.h) * kHd;
-    for (int c = c0; c < c1 && ok; ++c, ++k) {
+    for (int c = c0; c < c1; ++c, ++k) {
       const int64_t t0 = static_cast<int64_t>(c) * kQ;
+      float* const dlb = s_dl[k & 1];
+      float* const cmb = s_cum[k & 1];
       const uint32_t par = static_cast<uint32_t>(k & 1);
       // the next unit: chunk c + 1 of this sequence, or the next segment's first chunk
       const bool last = c + 1 == c1;
@@ -427,17 +431,29 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
         }
         const float before = __shfl_up_sync(0xffffffffu, s2, 1);
         const float base = lane > 0 ? before : 0.0f;
-        *reinterpret_cast<float2*>(&s_dl[2 * lane]) = make_float2(d0, d1);
-        *reinterpret_cast<float2*>(&s_cum[2 * lane]) = make_float2(base + a0, s2);
+        *reinterpret_cast<float2*>(&dlb[2 * lane]) = make_float2(d0, d1);
+        *reinterpret_cast<float2*>(&cmb[2 * lane]) = make_float2(base + a0, s2);
       }
       ok = ok && mbar_wait_bounded(&tbar[0], par, &g_ssd_status);
       ok = ok && mbar_wait_bounded(&tbar[1], par, &g_ssd_status);
       ok = ok && mbar_wait_bounded(&tbar[2], par, &g_ssd_status);
       started = k + 1;
+      // the tiles, Δ and the H tiles of the previous unit's P3 are in place; every thread is done with
+      // the previous unit's tensor memory
       fence_async_smem();
       tc_fence_before();
-      __syncthreads();
+      ok = __syncthreads_and(ok) != 0;
       tc_fence_after();
+      if (!ok) break;
+      // x at this lane's fragment positions for P4's D x, bf16 pairs [r][row half], read now so that
+      // the next unit's x can be requested as soon as M X is done with the tile
+      uint32_t xw[8];
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const uint32_t o0 = frag_off + ((rr ^ f3) << 4);
+        xw[2 * rr] = *reinterpret_cast<const uint32_t*>(sm + TcSmem::kX + o0);
+        xw[2 * rr + 1] = *reinterpret_cast<const uint32_t*>(sm + TcSmem::kX + o0 + 1024);
+      }
 
       // ---- P1: G = C B^T and Yo = C H^T on the tensor cores; meanwhile w ∘ x on the CUDA cores
       if (tid == 0) {
@@ -456,9 +472,9 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
         }
         tc_commit(&bars[0]);
       }
-      const float cum_end = s_cum[kQ - 1];
+      const float cum_end = cmb[kQ - 1];
       {
-        const float wj = ex2_approx(cum_end - s_cum[jw]) * s_dl[jw];
+        const float wj = ex2_approx(cum_end - cmb[jw]) * dlb[jw];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           const uint32_t o = q ? w_off1 : w_off0;
@@ -499,15 +515,15 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
       // undefined once the status word reports a timeout), and the loop leaves at the next barrier.
       // Without the run-time branches around them: 0.540 -> 0.527 ms.
       {
-        const float cr0 = s_cum[ri0], cr1 = s_cum[ri1];
+        const float cr0 = cmb[ri0], cr1 = cmb[ri1];
         float gv[16];
         tc_ld_frag32(tmem + t_lane + pbase, gv);
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr) {
           const int r = 4 * half + rr;                     // 16-byte column chunk of the row
           const int j = 8 * r + 2 * ft;
-          const float2 cj = *reinterpret_cast<const float2*>(&s_cum[j]);
-          const float2 dj = *reinterpret_cast<const float2*>(&s_dl[j]);
+          const float2 cj = *reinterpret_cast<const float2*>(&cmb[j]);
+          const float2 dj = *reinterpret_cast<const float2*>(&dlb[j]);
           const float m00 = j <= ri0 ? gv[4 * rr] * ex2_approx(cr0 - cj.x) * dj.x : 0.0f;
           const float m01 = j + 1 <= ri0 ? gv[4 * rr + 1] * ex2_approx(cr0 - cj.y) * dj.y : 0.0f;
           const float m10 = j <= ri1 ? gv[4 * rr + 2] * ex2_approx(cr1 - cj.x) * dj.x : 0.0f;
@@ -555,28 +571,20 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
         for (int q = 0; q < 32; ++q) H[q] = fmaf(eE, H[q], s[q]);
       }
       store_state_tiles(state_off, s3);
-
-      // ---- P4: y = Yd + e^{cum_i} Yo + D x.  The x values this lane needs are taken into registers
-      // first so that the next unit's x can be requested before the output work.
-      ok = ok && mbar_wait_bounded(&bars[2], par, &g_ssd_status);
-      ok = __all_sync(0xffffffffu, ok);   // the tensor-memory loads below are warp-collective
-      uint32_t xw[8];   // x at this lane's fragment positions, bf16 pairs: [r][row half]
-#pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
-        const uint32_t o0 = frag_off + ((rr ^ f3) << 4);
-        xw[2 * rr] = *reinterpret_cast<const uint32_t*>(sm + TcSmem::kX + o0);
-        xw[2 * rr + 1] = *reinterpret_cast<const uint32_t*>(sm + TcSmem::kX + o0 + 1024);
-      }
-      tc_fence_before();
-      ok = __syncthreads_and(ok) != 0;   // Yd and every thread are done with x
-      tc_fence_after();
-      if (tid == kLoader && more) {   // Yd and every thread are done with x
+      // every thread read x before P2's barrier (w ∘ x, xw); once M X is done the tile is free (a
+      // failed wait leaves the next x unrequested: the next unit's tile wait then gives up)
+      if (tid == kLoader && more && mbar_wait_bounded(&bars[2], par, &g_ssd_status)) {
         fence_async_smem();
         issue_x(nh, nb, nt0);
         ++armed[2];
       }
+
+      // ---- P4: y = Yd + e^{cum_i} Yo + D x
+      ok = ok && mbar_wait_bounded(&bars[2], par, &g_ssd_status);
+      ok = __all_sync(0xffffffffu, ok);   // the tensor-memory loads below are warp-collective
+      tc_fence_after();
       {
-        const float e0 = ex2_approx(s_cum[ri0]), e1 = ex2_approx(s_cum[ri1]);
+        const float e0 = ex2_approx(cmb[ri0]), e1 = ex2_approx(cmb[ri1]);
         float yd[16], yo[16];
         tc_ld_frag32(tmem + t_lane + pbase, yd);
         {
@@ -602,11 +610,9 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
           if (t0 + ri1 < L) *reinterpret_cast<uint32_t*>(checked(yg, y1 + pc, nX, 2)) = pack_bf16x2(v10, v11);
         }
       }
-      fence_async_smem();   // the new H tiles, for the next unit's MMAs
-      tc_fence_before();
-      ok = __syncthreads_and(ok) != 0;
-      tc_fence_after();
     }
+    // CTA-uniform from here: the barriers of the segment switch below
+    ok = __syncthreads_and(ok) != 0;
     if (!ok) break;
     // The segment ends: its state leaves, the next segment's state replaces it in the H tiles (read
     // first by the next chunk's C·H^T, after that chunk's barrier and proxy fence).  Kept out of the
